@@ -1,0 +1,452 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle
+itself: published known answers, library routines the definition reduces to
+(numpy.searchsorted, torch.nn.functional.embedding_bag and its autograd,
+torch.optim.Adagrad), hand-worked examples, closed forms and invariants.
+CPU only."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from sparse_lookup_gb300 import synth
+from sparse_lookup_gb300.synth import ColumnSpec
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+MASK = (1 << 64) - 1
+
+
+def _golden(name):
+    out = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                out.append(line)
+    return out
+
+
+# ---------------------------------------------------------------- transform
+
+def test_splitmix64_published_seed0_sequence():
+    """Hash transform = one SplitMix64 output with state = ID; the outputs for
+    ID = i * gamma are the published seed-0 sequence."""
+    for line in _golden("splitmix64_seed0.txt"):
+        i, state, out = line.split()
+        assert int(state, 16) == (int(i) * 0x9E3779B97F4A7C15) & MASK
+        assert oracle.splitmix64(int(state, 16)) == int(out, 16)
+
+
+def test_hash_mod_is_unsigned_modulo_of_the_hash():
+    rng = np.random.default_rng(0)
+    ids = rng.integers(-2 ** 63, 2 ** 63 - 1, 500, dtype=np.int64, endpoint=True)
+    ids[:4] = [-2 ** 63, -1, 0, 2 ** 63 - 1]
+    for rows in (1, 2, 3, 1000, 999_983, 2 ** 31 - 1, 2 ** 40 + 7):
+        col = ColumnSpec("hash_mod", "sum", rows, 4, 0)
+        got = oracle.column_rows(col, ids)
+        want = [oracle.splitmix64(int(x) & MASK) % rows for x in ids]
+        assert got.tolist() == want
+        assert got.min() >= 0 and got.max() < rows
+
+
+def test_bucketize_matches_searchsorted_right():
+    """row = #{j : bnd[j] <= x}: numpy.searchsorted(side='right') for every
+    ordered x; a value equal to a boundary goes to the upper bucket."""
+    rng = np.random.default_rng(1)
+    for nb in (1, 2, 10, 100):
+        bnd = np.unique(rng.standard_normal(nb).astype(np.float32))
+        x = rng.standard_normal(2000).astype(np.float32)
+        x[:bnd.size] = bnd
+        x[-3:] = [np.inf, -np.inf, np.float32(bnd[-1]) + np.float32(1e-6)]
+        col = ColumnSpec("bucketize", "sum", bnd.size + 1, 4, 0, boundaries=bnd)
+        got = oracle.column_rows(col, x)
+        assert got.tolist() == np.searchsorted(bnd, x, side="right").tolist()
+        assert got[x == np.inf].tolist() == [bnd.size]
+        assert got[x == -np.inf].tolist() == [0]
+
+
+def test_bucketize_nan_goes_to_bucket_zero():
+    bnd = np.array([-1.0, 0.0, 2.0], np.float32)
+    col = ColumnSpec("bucketize", "sum", 4, 4, 0, boundaries=bnd)
+    assert oracle.column_rows(col, np.array([np.nan, -np.nan], np.float32)).tolist() == [0, 0]
+
+
+def test_identity_safety_drops_out_of_range():
+    col = ColumnSpec("identity", "sum", 10, 4, 0)
+    ids = np.array([0, 9, 10, -1, -2 ** 63, 2 ** 63 - 1, 5], np.int64)
+    assert oracle.column_rows(col, ids).tolist() == [0, 9, -1, -1, -1, -1, 5]
+    col = ColumnSpec("rows_given", "sum", 10, 4, 0)
+    assert oracle.column_rows(col, np.array([-1, 3, 11], np.int64)).tolist() == [-1, 3, -1]
+
+
+# ------------------------------------------------------------------ forward
+
+def _hand_table():
+    return np.array([[1, 2], [3, 4], [10, 20], [-5, 0.5]], np.float32)
+
+
+def test_forward_hand_worked_example():
+    """Three bags typed by hand: [0, 2], [], [1, 1, 7(out of range), -1]."""
+    E = _hand_table()
+    off = np.array([0, 2, 2, 6], np.int32)
+    ids = np.array([0, 2, 1, 1, 7, -1], np.int64)
+    dft = np.array([0.25, -0.75], np.float32)
+    cols = [ColumnSpec("identity", "sum", 4, 2, 0),
+            ColumnSpec("identity", "mean", 4, 2, 0, default=dft)]
+    out, _, rows = oracle.forward(cols, 3, [off, off], [ids, ids], [E], want_rows=True)
+    assert out.tolist() == [[11, 22, 5.5, 11],
+                            [0, 0, 0.25, -0.75],
+                            [6, 8, 3, 4]]
+    assert rows[0].tolist() == [0, 2, 1, 1, -1, -1]
+
+
+def test_forward_padded_hand_worked_example():
+    E = _hand_table()
+    off = np.array([0, 3, 3, 5], np.int32)
+    ids = np.array([3, 9, 1, 2, 0], np.int64)
+    cols = [ColumnSpec("identity", "padded", 4, 2, 0, pad_len=2)]
+    out, seq = oracle.forward(cols, 3, [off], [ids], [E])
+    assert out.shape == (3, 0)
+    assert seq[0].tolist() == [[[-5, 0.5], [0, 0]],
+                               [[0, 0], [0, 0]],
+                               [[10, 20], [1, 2]]]
+
+
+def _tables(w):
+    return [None if t is None else synth.make_table(t).numpy() for t in w.tables]
+
+
+def test_forward_matches_embedding_bag_in_fp64():
+    """On the valid IDs, SUM/MEAN pooling is torch.nn.functional.embedding_bag
+    (library routine) over the same CSR offsets; empty bags give the default."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    for seed in range(6):
+        w = synth.random_small(seed, allow_padded=False)
+        tabs = _tables(w)
+        out, _, rows = oracle.forward(w.columns, w.B, w.offsets, w.values, tabs, want_rows=True)
+        col0 = 0
+        for ci, c in enumerate(w.columns):
+            r = rows[ci]
+            off = w.offsets[ci].astype(np.int64)
+            keep = r >= 0
+            bag = np.repeat(np.arange(w.B), np.diff(off))[keep]
+            new_off = np.searchsorted(bag, np.arange(w.B + 1), side="left")
+            ref = F.embedding_bag(torch.from_numpy(r[keep]), torch.from_numpy(tabs[c.table]).double(),
+                                  torch.from_numpy(new_off[:-1]), mode=c.pooling).numpy()
+            nv = np.diff(new_off)
+            dft = np.zeros(c.dim) if c.default is None else c.default.astype(np.float64)
+            ref[nv == 0] = dft
+            got = out[:, col0:col0 + c.dim]
+            np.testing.assert_allclose(got, ref, rtol=1e-6, atol=1e-7)
+            col0 += c.dim
+
+
+def test_forward_invariants():
+    rng = np.random.default_rng(3)
+    E = rng.standard_normal((50, 8)).astype(np.float32)
+    F_ = rng.standard_normal((50, 8)).astype(np.float32)
+    B = 40
+    lens = rng.integers(0, 9, B)
+    off = synth.bag_offsets(lens)
+    ids = rng.integers(-3, 53, int(lens.sum())).astype(np.int64)
+    s = [ColumnSpec("identity", "sum", 50, 8, 0)]
+    m = [ColumnSpec("identity", "mean", 50, 8, 0)]
+    # single valid ID, mean pooling -> exactly its row
+    one = np.array([7], np.int64)
+    y, _ = oracle.forward(m, 1, [np.array([0, 1], np.int32)], [one], [E])
+    assert np.array_equal(y[0], E[7])
+    # all IDs dropped -> default vector (zeros when none)
+    bad = np.array([-1, 50, 99], np.int64)
+    y, _ = oracle.forward(s, 1, [np.array([0, 3], np.int32)], [bad], [E])
+    assert np.array_equal(y[0], np.zeros(8, np.float32))
+    # linearity: pool(aE + bF) = a pool(E) + b pool(F)
+    a, b = 0.75, -2.5
+    yE, _ = oracle.forward(s, B, [off], [ids], [E])
+    yF, _ = oracle.forward(s, B, [off], [ids], [F_])
+    yL, _ = oracle.forward(s, B, [off], [ids], [(a * E.astype(np.float64) + b * F_).astype(np.float32)])
+    np.testing.assert_allclose(yL, a * yE.astype(np.float64) + b * yF, rtol=1e-5, atol=1e-5)
+    # order of IDs inside a bag does not matter (up to rounding)
+    perm = ids.copy()
+    for i in range(B):
+        rng.shuffle(perm[off[i]:off[i + 1]])
+    yP, _ = oracle.forward(s, B, [off], [perm], [E])
+    np.testing.assert_allclose(yP, yE, rtol=1e-6, atol=1e-6)
+
+
+def test_forward_rejects_bad_offsets():
+    E = _hand_table()
+    col = [ColumnSpec("identity", "sum", 4, 2, 0)]
+    with pytest.raises(ValueError):
+        oracle.forward(col, 2, [np.array([1, 2, 3], np.int32)], [np.zeros(3, np.int64)], [E])
+    with pytest.raises(ValueError):
+        oracle.forward(col, 2, [np.array([0, 2, 1], np.int32)], [np.zeros(2, np.int64)], [E])
+
+
+# ----------------------------------------------------------------- backward
+
+def test_local_reduce_matches_recis_figure3():
+    """Unique rows + counts of a batch reproduce Figure 3's local reduce-ID:
+    same set of reduced IDs; counts rebuild the queries' multiplicity."""
+    for line in _golden("recis_fig3_local_reduce.txt"):
+        dev, q, red = [p.strip() for p in line.split("|")]
+        q = np.array([int(x) for x in q.split()], np.int64)
+        red = [int(x) for x in red.split()]
+        col = [ColumnSpec("identity", "sum", 10000, 2, 0)]
+        off = np.array([0, q.size], np.int32)
+        W = [np.zeros((10000, 2), np.float32)]
+        A = [np.zeros((10000, 2), np.float32)]
+        G = np.ones((1, 2), np.float32)
+        res = oracle.backward_adagrad(col, 1, [off], [q], G, None, W, A, 0.01, 1e-10)
+        assert set(res["row"].tolist()) == set(red)
+        assert res["row"].tolist() == sorted(red)
+        inv = {r: n for r, n in zip(res["row"].tolist(), res["count"].tolist())}
+        rebuilt = sorted(sum([[r] * n for r, n in inv.items()], []))
+        assert rebuilt == sorted(q.tolist())
+
+
+def test_backward_matches_embedding_bag_autograd():
+    """The aggregated gradient of each unique row is the dense gradient that
+    autograd of torch.nn.functional.embedding_bag (fp64) gives that row; rows
+    the batch does not touch receive nothing."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    for seed in range(5):
+        w = synth.random_small(seed + 10, allow_padded=False, shared_tables=False)
+        tabs = _tables(w)
+        width = sum(c.dim for c in w.columns)
+        G = synth.make_grad((w.B, width), seed).numpy()
+        W = [t.copy() for t in tabs]
+        A = [np.zeros_like(t) for t in tabs]
+        res = oracle.backward_adagrad(w.columns, w.B, w.offsets, w.values, G, None, W, A, 0.05, 1e-10)
+        col0 = 0
+        for ci, c in enumerate(w.columns):
+            r = oracle.column_rows(c, w.values[ci])
+            off = w.offsets[ci].astype(np.int64)
+            keep = r >= 0
+            bag = np.repeat(np.arange(w.B), np.diff(off))[keep]
+            new_off = np.searchsorted(bag, np.arange(w.B + 1), side="left")
+            E = torch.from_numpy(tabs[c.table]).double().requires_grad_(True)
+            y = F.embedding_bag(torch.from_numpy(r[keep]), E, torch.from_numpy(new_off[:-1]), mode=c.pooling)
+            y.backward(torch.from_numpy(G[:, col0:col0 + c.dim]).double())
+            dense = E.grad.numpy()
+            sel = res["table"] == c.table
+            touched = res["row"][sel]
+            got = np.array([g for g, s in zip(res["grad"], sel) if s]).reshape(-1, c.dim)
+            np.testing.assert_allclose(got, dense[touched], rtol=1e-6, atol=1e-6)
+            untouched = np.setdiff1d(np.arange(c.num_rows), touched)
+            assert np.all(dense[untouched] == 0)
+            assert np.array_equal(np.sort(touched), np.unique(r[keep]))
+            assert res["count"][sel].sum() == keep.sum()
+            col0 += c.dim
+
+
+def test_backward_gradient_sum_invariant():
+    """Sum over unique rows of the aggregated gradient = sum over valid
+    contributions of scale * G[bag] (per column and element, fp64)."""
+    w = synth.random_small(77, C=4, B=50, allow_padded=False, shared_tables=False)
+    tabs = _tables(w)
+    width = sum(c.dim for c in w.columns)
+    G = synth.make_grad((w.B, width), 5).numpy().astype(np.float64)
+    W = [t.copy() for t in tabs]
+    A = [np.zeros_like(t) for t in tabs]
+    res = oracle.backward_adagrad(w.columns, w.B, w.offsets, w.values, G.astype(np.float32), None,
+                                  W, A, 0.01, 1e-10)
+    col0 = 0
+    for ci, c in enumerate(w.columns):
+        r = oracle.column_rows(c, w.values[ci])
+        off = w.offsets[ci]
+        want = np.zeros(c.dim)
+        for b in range(w.B):
+            rr = r[off[b]:off[b + 1]]
+            nv = int((rr >= 0).sum())
+            if nv:
+                scale = 1.0 / nv if c.pooling == "mean" else 1.0
+                want += nv * scale * G[b, col0:col0 + c.dim].astype(np.float32).astype(np.float64)
+        sel = res["table"] == c.table
+        got = np.sum([g.astype(np.float64) for g, s in zip(res["grad"], sel) if s], axis=0) if sel.any() else 0
+        np.testing.assert_allclose(got, want, rtol=1e-5, atol=1e-4)
+        col0 += c.dim
+
+
+def test_adagrad_first_step_closed_form_and_torch():
+    """From acc = 0 one step gives acc = g^2 and W - lr*g/(|g| + eps); the
+    update is torch.optim.Adagrad's (library routine) with the aggregated
+    gradient as the dense gradient."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(11)
+    rows, dim, B = 30, 8, 25
+    lens = rng.integers(0, 6, B)
+    off = synth.bag_offsets(lens)
+    ids = rng.integers(0, rows, int(lens.sum())).astype(np.int64)
+    col = [ColumnSpec("identity", "sum", rows, dim, 0)]
+    W0 = rng.standard_normal((rows, dim)).astype(np.float32)
+    G = rng.standard_normal((B, dim)).astype(np.float32)
+    lr, eps = 0.01, 1e-10
+    W = [W0.copy()]
+    A = [np.zeros_like(W0)]
+    res = oracle.backward_adagrad(col, B, [off], [ids], G, None, W, A, lr, eps)
+    g = np.zeros_like(W0)
+    for r, gr in zip(res["row"], res["grad"]):
+        g[r] = gr
+    # closed form
+    np.testing.assert_array_equal(A[0], g * g)
+    touched = np.zeros(rows, bool)
+    touched[res["row"]] = True
+    cf = W0.astype(np.float64) - lr * g / (np.abs(g.astype(np.float64)) + eps)
+    np.testing.assert_allclose(W[0][touched], cf[touched], rtol=1e-6, atol=1e-7)
+    assert np.array_equal(W[0][~touched], W0[~touched])
+    # torch.optim.Adagrad, two steps
+    p = torch.nn.Parameter(torch.from_numpy(W0.copy()))
+    opt = torch.optim.Adagrad([p], lr=lr, eps=eps, initial_accumulator_value=0.0)
+    p.grad = torch.from_numpy(g.copy())
+    opt.step()
+    np.testing.assert_allclose(p.detach().numpy(), W[0], rtol=1e-6, atol=1e-7)
+    res2 = oracle.backward_adagrad(col, B, [off], [ids], G, None, W, A, lr, eps)
+    g2 = np.zeros_like(W0)
+    for r, gr in zip(res2["row"], res2["grad"]):
+        g2[r] = gr
+    p.grad = torch.from_numpy(g2.copy())
+    opt.step()
+    np.testing.assert_allclose(p.detach().numpy(), W[0], rtol=1e-6, atol=1e-7)
+    np.testing.assert_allclose(opt.state[p]["sum"].numpy(), A[0], rtol=1e-6, atol=1e-7)
+
+
+def test_backward_mean_and_padded_hand_example():
+    """Bag [1, 1, 3, 99] with MEAN (3 valid IDs): row 1 gets 2/3 G, row 3 gets
+    1/3 G.  PADDED column, pad 2, bag [2, 0, 1]: position 2 is cut, row 2 gets
+    Gseq[0,0], row 0 gets Gseq[0,1]."""
+    E = np.zeros((4, 2), np.float32)
+    off = np.array([0, 4], np.int32)
+    ids = np.array([1, 1, 3, 99], np.int64)
+    G = np.array([[3.0, -6.0]], np.float32)
+    res = oracle.backward_adagrad([ColumnSpec("identity", "mean", 4, 2, 0)], 1, [off], [ids], G, None,
+                                  [E.copy()], [E.copy()], 0.1, 1e-10)
+    assert res["row"].tolist() == [1, 3] and res["count"].tolist() == [2, 1]
+    np.testing.assert_allclose(res["grad"][0], [2.0, -4.0], rtol=1e-7)
+    np.testing.assert_allclose(res["grad"][1], [1.0, -2.0], rtol=1e-7)
+    off = np.array([0, 3], np.int32)
+    ids = np.array([2, 0, 1], np.int64)
+    Gs = np.array([[[1.0, 2.0], [3.0, 4.0]]], np.float32)
+    res = oracle.backward_adagrad([ColumnSpec("identity", "padded", 4, 2, 0, pad_len=2)], 1, [off], [ids],
+                                  None, [Gs], [E.copy()], [E.copy()], 0.1, 1e-10)
+    assert res["row"].tolist() == [0, 2] and res["count"].tolist() == [1, 1]
+    assert res["grad"][0].tolist() == [3.0, 4.0] and res["grad"][1].tolist() == [1.0, 2.0]
+
+
+def test_backward_shared_table_merges_columns():
+    """Two columns reading one physical table: a row touched by both is one
+    unique row whose gradient sums both columns' contributions."""
+    off = np.array([0, 1], np.int32)
+    cols = [ColumnSpec("identity", "sum", 5, 2, 0), ColumnSpec("identity", "sum", 5, 2, 0)]
+    G = np.array([[1.0, 2.0, 10.0, 20.0]], np.float32)
+    E = np.zeros((5, 2), np.float32)
+    res = oracle.backward_adagrad(cols, 1, [off, off], [np.array([4]), np.array([4])], G, None,
+                                  [E.copy()], [E.copy()], 0.1, 1e-10)
+    assert res["row"].tolist() == [4] and res["count"].tolist() == [2]
+    assert res["grad"][0].tolist() == [11.0, 22.0]
+
+
+# --------------------------------------------------------------- hash table
+
+def test_hash_hand_traced_scenario():
+    """Threshold 3, ttl 2, capacity 3 rows.  Traced by hand:
+    step 0: A A B B B C -> B reaches 3 (row 0, same call); A, C count.
+    step 1: A C D      -> A reaches 3 (row 1); C=2, D=1.
+    step 4: evict(now=4, ttl=2): B (seen 0), A, C, D (seen 1) idle > 2 -> all go;
+            rows 0, 1 return to the free list.
+    step 5: E E E F F F -> E, F admitted in key order, lowest free rows 0, 1.
+    step 6: G G G H H H -> G row 2 (bump), H finds no row: TABLE_FULL, -1.
+    step 7: H          -> still no row (count 4).
+    evict(now=8, ttl=2): E, F (seen 5) go, rows 1 and 0 are free again.
+    step 8: H          -> H (count 5, still above the threshold) takes row 0."""
+    h = oracle.Hash(3, 2, 3, 42, 0.5)
+    A, B_, C, D, E, F_, G_, H = 100, 50, 7, 8, 30, 20, 9, 10
+    rows, st = h.lookup_or_insert([0] * 6, [A, A, B_, B_, B_, C], 0)
+    assert st == 0 and rows.tolist() == [-1, -1, 0, 0, 0, -1]
+    rows, st = h.lookup_or_insert([0] * 3, [A, C, D], 1)
+    assert rows.tolist() == [1, -1, -1]
+    ex = h.export()
+    assert dict(zip(ex["key"].tolist(), ex["count"].tolist())) == {A: 3, B_: 3, C: 2, D: 1}
+    assert h.evict(3, 2) == 1            # only B (idle 3 > 2) at now = 3
+    assert h.evict(4, 2) == 3
+    assert h.size() == 0 and h.free_count() == 2
+    rows, st = h.lookup_or_insert([0] * 6, [E, E, E, F_, F_, F_], 5)
+    assert st == 0 and rows.tolist() == [1, 1, 1, 0, 0, 0]   # F < E: F takes row 0
+    rows, st = h.lookup_or_insert([0] * 6, [G_, G_, G_, H, H, H], 6)
+    assert st == oracle.ERR_FULL and rows.tolist() == [2, 2, 2, -1, -1, -1]
+    # H stays counting and is admitted as soon as a row is free again
+    rows, st = h.lookup_or_insert([0], [H], 7)
+    assert st == oracle.ERR_FULL and rows.tolist() == [-1]
+    assert h.evict(8, 2) == 2
+    rows, st = h.lookup_or_insert([0], [H], 8)
+    assert st == 0 and rows.tolist() == [0]
+
+
+def test_hash_init_values_are_exact_and_in_range():
+    vals = np.array([oracle.hash_init_value(5, 3, 123456789, d, 1.0) for d in range(64)])
+    assert np.all(vals >= -1.0) and np.all(vals < 1.0)
+    assert np.all(vals * 2 ** 23 == np.round(vals * 2 ** 23))   # 24-bit grid
+    v2 = np.array([oracle.hash_init_value(5, 3, 123456789, d, 0.01) for d in range(64)])
+    np.testing.assert_array_equal(v2, (vals.astype(np.float32) * np.float32(0.01)).astype(np.float32))
+    h = oracle.splitmix64(123456789 ^ (3 << 48) ^ 5 ^ 0)
+    assert vals[0] == ((h >> 40) - 2 ** 23) / 2 ** 23
+
+
+def _dict_model(stream, threshold, ttl, cap):
+    """Independent brute-force model of the table rules, with Python dicts
+    and a sorted list of free rows (used only on tiny streams)."""
+    ent, free, bump, outs = {}, [], 0, []
+    for step, tids, keys in stream:
+        for k in zip(tids, keys):
+            e = ent.setdefault(k, dict(count=0, row=-1, seen=step))
+            e["seen"] = step
+            if e["row"] < 0:
+                e["count"] += 1
+        new = sorted(k for k, e in ent.items() if e["row"] < 0 and e["count"] >= threshold)
+        free.sort()
+        for k in new:
+            if free:
+                ent[k]["row"] = free.pop(0)
+            elif bump < cap:
+                ent[k]["row"] = bump
+                bump += 1
+        outs.append([ent[k]["row"] for k in zip(tids, keys)])
+        for k in [k for k, e in ent.items() if step - e["seen"] > ttl]:
+            if ent[k]["row"] >= 0:
+                free.append(ent[k]["row"])
+            del ent[k]
+    return outs, ent
+
+
+def test_hash_matches_dict_model_and_invariants():
+    rng = np.random.default_rng(9)
+    thr, ttl, cap = 3, 4, 40
+    stream = []
+    for step in range(40):
+        n = int(rng.integers(0, 30))
+        keys = synth.zipf(rng, 60, 1.1, n)
+        tids = rng.integers(0, 3, n)
+        stream.append((step, tids.tolist(), keys.tolist()))
+    want, ent = _dict_model(stream, thr, ttl, cap)
+    h = oracle.Hash(cap, 4, thr, 1, 0.1)
+    for (step, tids, keys), w in zip(stream, want):
+        rows, _ = h.lookup_or_insert(tids, keys, step)
+        assert rows.tolist() == w
+        h.evict(step, ttl)
+        ex = h.export()
+        adm = ex["row"] >= 0
+        # injective key -> row, rows in range
+        assert len(set(ex["row"][adm].tolist())) == int(adm.sum())
+        assert np.all(ex["row"][adm] < cap)
+        # threshold rule: admitted entries reached it; counting ones did not
+        # (unless the pool is exhausted)
+        assert np.all(ex["count"][adm] >= thr)
+        if h.bump() < cap or h.free_count() > 0:
+            assert np.all(ex["count"][~adm] < thr)
+        # after the sweep no entry is idle longer than ttl
+        assert np.all(step - ex["last_seen"].astype(np.int64) <= ttl)
+        # free rows and used rows partition the rows handed out so far
+        assert int(adm.sum()) + h.free_count() == h.bump()
+    ex = h.export()
+    assert sorted(zip(ex["tid"].tolist(), ex["key"].tolist())) == sorted(ent.keys())
