@@ -1,0 +1,297 @@
+// plan.cu -- emb_plan_create / destroy / info / device status and the C-ABI
+// wrappers of the forward and backward launches.
+#include <algorithm>
+#include <cstring>
+#include <map>
+#include <new>
+
+#include "plan.cuh"
+
+using namespace emb;
+
+namespace {
+
+void free_plan(emb_plan_s* p) {
+  if (!p) return;
+  cudaFree(p->meta_d);
+  cudaFree(p->stream_cols_d);
+  cudaFree(p->tables_d);
+  cudaFree(p->table_base_d);
+  cudaFree(p->status_d);
+  Workspace& w = p->ws;
+  cudaFree(w.keys[0]);
+  cudaFree(w.keys[1]);
+  cudaFree(w.vals[0]);
+  cudaFree(w.vals[1]);
+  cudaFree(w.inv_n);
+  cudaFree(w.hist);
+  cudaFree(w.run_head);
+  cudaFree(w.n_runs);
+  cudaFree(w.scan_part);
+  cudaFree(w.partial);
+  delete p;
+}
+
+template <class T>
+cudaError_t dmalloc(T** ptr, size_t count, size_t* total) {
+  size_t bytes = sizeof(T) * (count > 0 ? count : 1);
+  *total += bytes;
+  return cudaMalloc((void**)ptr, bytes);
+}
+
+emb_status validate_column(const emb_column_desc& c, bool training) {
+  if (c.transform < EMB_T_IDENTITY || c.transform > EMB_T_ROWS_GIVEN) return EMB_ERR_INVALID_ARG;
+  if (c.pooling < EMB_POOL_SUM || c.pooling > EMB_POOL_NONE_PADDED) return EMB_ERR_INVALID_ARG;
+  if (c.num_rows < 1) return EMB_ERR_INVALID_ARG;
+  if (c.num_rows >= (int64_t(1) << 31)) return EMB_ERR_UNSUPPORTED;
+  if (c.dim < 4 || c.dim % 4 != 0) return EMB_ERR_INVALID_ARG;
+  if (c.dim > 256) return EMB_ERR_UNSUPPORTED;
+  if (c.reserved != 0) return EMB_ERR_INVALID_ARG;
+  if (!c.weight || !aligned16(c.weight)) return EMB_ERR_INVALID_ARG;
+  if (c.pooling == EMB_POOL_NONE_PADDED && c.pad_len < 1) return EMB_ERR_INVALID_ARG;
+  if (c.transform == EMB_T_BUCKETIZE) {
+    if (!c.boundaries || c.num_boundaries < 1) return EMB_ERR_INVALID_ARG;
+    if (c.num_boundaries > 4096) return EMB_ERR_UNSUPPORTED;
+    if (c.num_rows != (int64_t)c.num_boundaries + 1) return EMB_ERR_INVALID_ARG;
+  }
+  if (training && (!c.adagrad_acc || !aligned16(c.adagrad_acc))) return EMB_ERR_INVALID_ARG;
+  if (c.default_vec && !aligned16(c.default_vec)) return EMB_ERR_INVALID_ARG;
+  return EMB_OK;
+}
+
+}  // namespace
+
+extern "C" emb_status emb_plan_create(const emb_column_desc* cols, int32_t n_cols,
+                                      int32_t max_batch, int64_t max_ids, uint32_t flags,
+                                      emb_plan* out) {
+  if (!out) return EMB_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cols || n_cols < 1 || n_cols > 65535 || max_batch < 1) return EMB_ERR_INVALID_ARG;
+  if (flags & ~EMB_PLAN_TRAINING) return EMB_ERR_INVALID_ARG;
+  const bool training = (flags & EMB_PLAN_TRAINING) != 0;
+  if ((int64_t)n_cols * max_batch >= (int64_t(1) << 31)) return EMB_ERR_UNSUPPORTED;
+  if (training && (max_ids < 0 || max_ids >= (int64_t(1) << 30))) return EMB_ERR_UNSUPPORTED;
+  for (int32_t c = 0; c < n_cols; ++c) {
+    emb_status s = validate_column(cols[c], training);
+    if (s != EMB_OK) return s;
+  }
+
+  emb_plan_s* p = new (std::nothrow) emb_plan_s();
+  if (!p) return EMB_ERR_OOM;
+  p->n_cols = n_cols;
+  p->max_batch = max_batch;
+  p->max_ids = training ? max_ids : 0;
+  p->flags = flags;
+  p->training = training;
+  p->cols.assign(cols, cols + n_cols);
+
+  // Tables: columns with the same weight pointer share one table.
+  std::map<const float*, int32_t> table_of;
+  uint64_t base = 0;
+  for (int32_t c = 0; c < n_cols; ++c) {
+    const emb_column_desc& d = cols[c];
+    auto it = table_of.find(d.weight);
+    if (it == table_of.end()) {
+      int32_t t = (int32_t)p->tables_h.size();
+      table_of[d.weight] = t;
+      TableMeta tm{};
+      tm.weight = d.weight;
+      tm.acc = d.adagrad_acc;
+      tm.num_rows = d.num_rows;
+      tm.dim = d.dim;
+      tm.dim4 = d.dim / 4;
+      p->tables_h.push_back(tm);
+      p->table_base_h.push_back((uint32_t)base);
+      base += (uint64_t)d.num_rows;
+      p->col_table.push_back(t);
+    } else {
+      const TableMeta& tm = p->tables_h[it->second];
+      if (tm.num_rows != d.num_rows || tm.dim != d.dim || tm.acc != d.adagrad_acc) {
+        free_plan(p);
+        return EMB_ERR_INVALID_ARG;
+      }
+      p->col_table.push_back(it->second);
+    }
+  }
+  if (base >= 0xFFFFFFFFull) {
+    free_plan(p);
+    return EMB_ERR_UNSUPPORTED;
+  }
+  p->n_tables = (int32_t)p->tables_h.size();
+  p->table_base_h.push_back((uint32_t)base);
+  p->key_total = (uint32_t)base;
+  p->key_bits = 1;
+  while (p->key_bits < 32 && (uint64_t(1) << p->key_bits) <= base) ++p->key_bits;
+
+  // Column metadata, stream membership and output layout.
+  std::vector<int32_t> stream_cols[2];
+  int64_t out_col = 0, seq_unit = 0;
+  p->meta_h.resize(n_cols);
+  for (int32_t c = 0; c < n_cols; ++c) {
+    const emb_column_desc& d = cols[c];
+    ColMeta& m = p->meta_h[c];
+    m.weight = d.weight;
+    m.acc = d.adagrad_acc;
+    m.dflt = d.default_vec;
+    m.bnd = d.boundaries;
+    m.num_rows = d.num_rows;
+    m.mod = make_div_magic((uint64_t)d.num_rows);
+    m.dim = d.dim;
+    m.dim4 = d.dim / 4;
+    m.nb = d.transform == EMB_T_BUCKETIZE ? d.num_boundaries : 0;
+    m.transform = d.transform;
+    m.pooling = d.pooling;
+    m.pad_len = d.pooling == EMB_POOL_NONE_PADDED ? d.pad_len : 0;
+    m.table = p->col_table[c];
+    m.table_base = p->table_base_h[m.table];
+    m.col = c;
+    if (d.pooling == EMB_POOL_NONE_PADDED) {
+      m.out_col = -1;
+      m.seq_unit = seq_unit;
+      seq_unit += (int64_t)d.pad_len * d.dim;
+      p->n_padded++;
+    } else {
+      m.out_col = (int32_t)out_col;
+      m.seq_unit = 0;
+      out_col += d.dim;
+    }
+    p->max_dim = std::max(p->max_dim, d.dim);
+    stream_cols[d.transform == EMB_T_BUCKETIZE ? 1 : 0].push_back(c);
+  }
+  p->out_width = out_col;
+  p->seq_per_bag = seq_unit;
+  if (out_col >= (int64_t(1) << 31)) {
+    free_plan(p);
+    return EMB_ERR_UNSUPPORTED;
+  }
+  p->n_stream_cols[0] = (int32_t)stream_cols[0].size();
+  p->n_stream_cols[1] = (int32_t)stream_cols[1].size();
+  std::vector<int32_t> sc(stream_cols[0]);
+  sc.insert(sc.end(), stream_cols[1].begin(), stream_cols[1].end());
+
+  size_t total = 0;
+  cudaError_t e = cudaSuccess;
+  int dev = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = dmalloc(&p->meta_d, n_cols, &total);
+  if (e == cudaSuccess) e = dmalloc(&p->stream_cols_d, sc.size(), &total);
+  if (e == cudaSuccess) e = dmalloc(&p->tables_d, p->tables_h.size(), &total);
+  if (e == cudaSuccess) e = dmalloc(&p->table_base_d, p->table_base_h.size(), &total);
+  if (e == cudaSuccess) e = dmalloc(&p->status_d, 1, &total);
+  if (e == cudaSuccess) e = cudaMemcpy(p->meta_d, p->meta_h.data(), sizeof(ColMeta) * n_cols, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && !sc.empty())
+    e = cudaMemcpy(p->stream_cols_d, sc.data(), sizeof(int32_t) * sc.size(), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(p->tables_d, p->tables_h.data(), sizeof(TableMeta) * p->tables_h.size(), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(p->table_base_d, p->table_base_h.data(), sizeof(uint32_t) * p->table_base_h.size(),
+                   cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemset(p->status_d, 0, sizeof(uint32_t));
+
+  if (e == cudaSuccess && training) {
+    Workspace& w = p->ws;
+    const int64_t n = std::max<int64_t>(max_ids, 1);
+    w.max_tiles = (n + kSortTile - 1) / kSortTile;
+    w.n_units_max = (n + kUnit - 1) / kUnit;
+    const int passes = (p->key_bits + kRadixBits - 1) / kRadixBits;
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+      e = dmalloc(&w.keys[i], n, &total);
+      if (e == cudaSuccess) e = dmalloc(&w.vals[i], n, &total);
+    }
+    if (e == cudaSuccess) e = dmalloc(&w.inv_n, (size_t)n_cols * max_batch, &total);
+    // hist [4][kRadix], tile tickets [4], look-back words [passes][tiles][kRadix]
+    const size_t sort_words = 4 * kRadix + 4 + (size_t)passes * w.max_tiles * kRadix;
+    if (e == cudaSuccess) e = dmalloc(&w.hist, sort_words, &total);
+    if (e == cudaSuccess) {
+      w.tile_ctr = w.hist + 4 * kRadix;
+      w.lookback = w.tile_ctr + 4;
+    }
+    if (e == cudaSuccess) e = dmalloc(&w.run_head, n + 1, &total);
+    if (e == cudaSuccess) e = dmalloc(&w.n_runs, 4, &total);
+    if (e == cudaSuccess) e = dmalloc(&w.scan_part, (n + 1023) / 1024 + 64, &total);
+    if (e == cudaSuccess) e = dmalloc(&w.partial, (size_t)w.n_units_max * 2 * (p->max_dim / 4), &total);
+  }
+  p->ws.bytes = total;
+  if (e == cudaSuccess) p->fwd_ctas_per_sm = forward_ctas_per_sm();
+  if (e != cudaSuccess) {
+    free_plan(p);
+    cudaGetLastError();
+    return cuda_status(e);
+  }
+  *out = p;
+  return EMB_OK;
+}
+
+extern "C" emb_status emb_plan_destroy(emb_plan p) {
+  if (!p) return EMB_ERR_INVALID_ARG;
+  cudaDeviceSynchronize();
+  free_plan(p);
+  return EMB_OK;
+}
+
+extern "C" emb_status emb_plan_info(emb_plan p, int64_t* out_width, int64_t* seq_floats_per_bag,
+                                    int32_t* n_tables, int32_t* col_table, int64_t* workspace_bytes) {
+  if (!p) return EMB_ERR_INVALID_ARG;
+  if (out_width) *out_width = p->out_width;
+  if (seq_floats_per_bag) *seq_floats_per_bag = p->seq_per_bag;
+  if (n_tables) *n_tables = p->n_tables;
+  if (col_table) std::memcpy(col_table, p->col_table.data(), sizeof(int32_t) * p->n_cols);
+  if (workspace_bytes) *workspace_bytes = (int64_t)p->ws.bytes;
+  return EMB_OK;
+}
+
+extern "C" emb_status emb_forward(emb_plan p, int32_t batch, const int64_t* ids,
+                                  const int32_t* id_offsets, int64_t n_ids, const float* fvals,
+                                  const int32_t* f_offsets, int64_t n_fvals, float* out,
+                                  float* seq_out, int64_t* rows_dbg, void* stream) {
+  if (!p || batch < 0 || batch > p->max_batch || n_ids < 0 || n_fvals < 0) return EMB_ERR_INVALID_ARG;
+  if (n_ids >= (int64_t(1) << 31) || n_fvals >= (int64_t(1) << 31)) return EMB_ERR_UNSUPPORTED;
+  if (p->n_stream_cols[0] > 0 && (!id_offsets || (n_ids > 0 && !ids))) return EMB_ERR_INVALID_ARG;
+  if (p->n_stream_cols[1] > 0 && (!f_offsets || (n_fvals > 0 && !fvals))) return EMB_ERR_INVALID_ARG;
+  if (p->out_width > 0 && batch > 0 && (!out || !aligned16(out))) return EMB_ERR_INVALID_ARG;
+  if (p->n_padded > 0 && batch > 0 && (!seq_out || !aligned16(seq_out))) return EMB_ERR_INVALID_ARG;
+  if (p->training) {
+    if (n_ids + n_fvals > p->max_ids) return EMB_ERR_INVALID_ARG;
+    // padded gradient sources are addressed in float4 units below 2^31
+    if (p->seq_per_bag * (int64_t)batch / 4 >= (int64_t(1) << 31)) return EMB_ERR_UNSUPPORTED;
+  }
+  emb_status s = launch_forward(p, batch, ids, id_offsets, n_ids, fvals, f_offsets, n_fvals, out,
+                                seq_out, rows_dbg, (cudaStream_t)stream);
+  if (s == EMB_OK && p->training) {
+    p->have_forward = true;
+    p->last_batch = batch;
+    p->last_n = n_ids + n_fvals;
+    p->last_n_ids = n_ids;
+  }
+  return s;
+}
+
+extern "C" emb_status emb_backward_update(emb_plan p, const float* grad_out, const float* grad_seq,
+                                          float lr, float eps, void* stream,
+                                          const emb_backward_debug* dbg) {
+  if (!p || !p->training || !p->have_forward) return EMB_ERR_INVALID_ARG;
+  if (p->last_batch > 0 && p->out_width > 0 && !grad_out) return EMB_ERR_INVALID_ARG;
+  if (p->last_batch > 0 && p->n_padded > 0 && !grad_seq) return EMB_ERR_INVALID_ARG;
+  if (!(lr == lr) || !(eps == eps)) return EMB_ERR_INVALID_ARG;
+  return launch_backward(p, grad_out, grad_seq, lr, eps, (cudaStream_t)stream, dbg);
+}
+
+extern "C" emb_status emb_get_device_status(emb_plan p, void* stream) {
+  if (!p) return EMB_ERR_INVALID_ARG;
+  uint32_t st = 0;
+  EMB_CUDA_TRY(cudaStreamSynchronize((cudaStream_t)stream));
+  EMB_CUDA_TRY(cudaMemcpy(&st, p->status_d, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+  EMB_CUDA_TRY(cudaMemset(p->status_d, 0, sizeof(uint32_t)));
+  return (emb_status)st;
+}
+
+extern "C" emb_status emb_selftest_hash_mod(const int64_t* ids, int64_t n, int64_t num_rows,
+                                            int64_t* rows_out) {
+  if (n < 0 || num_rows < 1 || (n > 0 && (!ids || !rows_out))) return EMB_ERR_INVALID_ARG;
+  DivMagic g = make_div_magic((uint64_t)num_rows);
+  for (int64_t i = 0; i < n; ++i) rows_out[i] = (int64_t)mod_magic(splitmix64((uint64_t)ids[i]), g);
+  return EMB_OK;
+}
+
+extern "C" const char* emb_version(void) { return "sparse_lookup_gb300 0.1 (sm_103a)"; }

@@ -1,0 +1,110 @@
+// plan.cuh -- the plan handle: copied column descriptors, device metadata and
+// the workspace sized once at creation (library-internal).
+#pragma once
+
+#include <vector>
+
+#include "common.cuh"
+
+namespace emb {
+
+// Forward tiles cover this many stream elements at most (bags are owned by the
+// tile that holds their first element).
+constexpr int kFwdThreads = 256;
+constexpr int kFwdWarps = kFwdThreads / kWarp;
+constexpr int kLongBag = 128;         // longer bags are pooled by a whole CTA
+constexpr int kMaxTileElems = 8192;
+constexpr int kMaxLongPerTile = kMaxTileElems / kLongBag + 2;
+
+// Backward: contributions are processed in units of this many sorted entries
+// by one lane group; runs cut by a unit boundary are finished by a fixup pass.
+constexpr int kUnit = 128;
+constexpr uint32_t kPadBit = 0x80000000u;
+
+// Radix sort geometry (LSD, 8-bit digits, chained scan with decoupled
+// look-back).
+constexpr int kSortThreads = 512;
+constexpr int kSortItems = 15;
+constexpr int kSortTile = kSortThreads * kSortItems;
+constexpr int kRadixBits = 8;
+constexpr int kRadix = 1 << kRadixBits;
+
+struct Workspace {
+  // sort buffers: keys (global rows) and values (gradient sources)
+  uint32_t* keys[2] = {nullptr, nullptr};
+  uint32_t* vals[2] = {nullptr, nullptr};
+  float* inv_n = nullptr;          // [n_cols * max_batch] 1/n_valid of mean bags
+  uint32_t* hist = nullptr;        // [4][kRadix] digit counts of all passes
+  uint32_t* lookback = nullptr;    // [max_tiles][kRadix] chained-scan words
+  uint32_t* tile_ctr = nullptr;    // [4] tile tickets per pass
+  uint32_t* run_head = nullptr;    // [max_ids + 1] start of each run
+  uint32_t* n_runs = nullptr;      // [1]
+  uint32_t* scan_part = nullptr;   // per-block partial counts for run compaction
+  float4* partial = nullptr;       // [n_units][2][max_dim/4] cut-run partial sums
+  int64_t max_tiles = 0;
+  int64_t n_units_max = 0;
+  size_t bytes = 0;
+};
+
+}  // namespace emb
+
+struct emb_plan_s {
+  int32_t n_cols = 0;
+  int32_t max_batch = 0;
+  int64_t max_ids = 0;
+  uint32_t flags = 0;
+  bool training = false;
+  std::vector<emb_column_desc> cols;
+  std::vector<emb::ColMeta> meta_h;
+  std::vector<int32_t> col_table;
+  std::vector<emb::TableMeta> tables_h;
+  std::vector<uint32_t> table_base_h;  // [n_tables + 1]
+  emb::ColMeta* meta_d = nullptr;
+  int32_t* stream_cols_d = nullptr;    // id-stream columns, then f-stream columns
+  emb::TableMeta* tables_d = nullptr;
+  uint32_t* table_base_d = nullptr;
+  int32_t n_stream_cols[2] = {0, 0};
+  int32_t n_tables = 0;
+  int32_t n_padded = 0;
+  int32_t max_dim = 0;
+  int64_t out_width = 0;
+  int64_t seq_per_bag = 0;
+  uint32_t key_total = 0;              // sum of table rows == sentinel key
+  int key_bits = 0;
+  uint32_t* status_d = nullptr;
+  int sm_count = 0;
+  int fwd_ctas_per_sm = 0;
+  emb::Workspace ws;
+  // what the last forward recorded for the backward
+  bool have_forward = false;
+  int32_t last_batch = 0;
+  int64_t last_n = 0;
+  int64_t last_n_ids = 0;
+};
+
+namespace emb {
+
+inline emb_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return EMB_OK;
+  if (e == cudaErrorMemoryAllocation) return EMB_ERR_OOM;
+  return EMB_ERR_CUDA;
+}
+
+#define EMB_CUDA_TRY(x)                                  \
+  do {                                                   \
+    cudaError_t _e = (x);                                \
+    if (_e != cudaSuccess) return ::emb::cuda_status(_e); \
+  } while (0)
+
+// Launch-side entry points implemented in forward.cu / backward.cu.
+emb_status launch_forward(emb_plan_s* p, int32_t batch, const int64_t* ids,
+                          const int32_t* id_offsets, int64_t n_ids, const float* fvals,
+                          const int32_t* f_offsets, int64_t n_fvals, float* out,
+                          float* seq_out, int64_t* rows_dbg, cudaStream_t stream);
+int forward_ctas_per_sm();
+
+emb_status launch_backward(emb_plan_s* p, const float* grad_out, const float* grad_seq,
+                           float lr, float eps, cudaStream_t stream,
+                           const emb_backward_debug* dbg);
+
+}  // namespace emb
