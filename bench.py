@@ -111,8 +111,10 @@ def dist_env():
     return rank, world, local
 
 
-def make_workload(name):
+def make_workload(name, columns=None):
     if name == "inference":
+        if columns:
+            return synth.inference(n_cat=columns * 7 // 10, n_num=columns - columns * 7 // 10)
         return synth.inference()
     if name == "training":
         return synth.training()
@@ -193,7 +195,7 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     dev = "cuda"
-    w = make_workload(args.workload)
+    w = make_workload(args.workload, args.columns)
     tables = [None if t is None else synth.make_table(t, dev) for t in w.tables]
     ids_h, id_off_h, fv_h, f_off_h = synth.jagged(w)
     n_ids, n_f = ids_h.size, fv_h.size
@@ -325,6 +327,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="inference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--columns", type=int, default=None, help="inference: number of columns (profiling)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -5,22 +5,32 @@
 // skewed inputs"): each of the two jagged value streams is cut into tiles of
 // E consecutive elements; a CTA owns every (column, bag) segment whose FIRST
 // element lies in its tile, so each pooled output row has exactly one writer
-// (RecIS §3.2 Algorithm 1, forward: no atomics).  Inside a CTA, warps pull
-// short bags from a shared-memory cursor; bags longer than kLongBag elements
-// (or padded bags with pad_len > kLongBag) are pooled by all eight warps
-// together, each warp taking every eighth 32-element chunk, with a fixed-order
-// shared-memory reduction at the end.
+// (RecIS §3.2 Algorithm 1, forward: no atomics).
 //
-// Per 32-element chunk a warp loads the values coalesced (one per lane),
-// transforms them in parallel (SplitMix64 + invariant-divisor modulo, or a
-// binary search over the boundaries), applies the range guard, then gathers
-// rows with 16-byte loads: a row of dim floats is read by dim/4 lanes and
-// 32/(dim/4) rows are in flight per warp instruction, four instructions deep.
+// A CTA walks its segments in chunks that stay inside one column (one table,
+// one dim, one transform) and hold at most kChunkBags bags and kChunkElems
+// values of short bags:
+//   A. every thread transforms values of the chunk (coalesced 8-byte loads,
+//      SplitMix64 + invariant-divisor modulo, or a binary search over the
+//      boundaries), applies the range guard and writes the row to shared
+//      memory -- one memory round trip for the whole chunk;
+//   B. the chunk's values are split into equal ranges, one per lane group of
+//      dim/4 lanes (so every group runs the same trip count); a group gathers
+//      its rows with 16-byte loads four deep and sums them per bag; a bag that
+//      spans ranges leaves head/tail partials in shared memory which the
+//      group holding its first value adds up in range order (deterministic);
+//   C. bags longer than kLongBag (or padded bags with pad_len > kLongBag) are
+//      pooled / copied by all eight warps together.
+// Empty bags and bags whose values were all dropped get the default vector.
 #include <algorithm>
 
 #include "plan.cuh"
 
 namespace emb {
+
+constexpr int kChunkBags = 256;    // == kFwdThreads: one bag per thread in setup
+constexpr int kChunkElems = 4096;
+constexpr int kU = 4;              // row loads in flight per lane (halved when a lane holds two float4)
 
 struct FwdArgs {
   const ColMeta* meta;
@@ -45,6 +55,23 @@ struct FwdArgs {
   float* inv_n;            // training: 1/n_valid per mean bag
   uint32_t key_sentinel;
   uint32_t* status;
+};
+
+struct FwdSmem {
+  int32_t rows[kChunkElems];
+  uint8_t bag[kChunkElems];
+  int32_t pos[kChunkBags + 1];     // first slot of each bag's values in rows[]
+  int32_t lo[kChunkBags];          // first stream element of each bag
+  int32_t hi[kChunkBags];          // one past its last stream element; -1: long bag
+  int32_t len[kChunkBags];         // values of the bag held in rows[]
+  int32_t longs[kChunkBags];       // bags left for phase C
+  int32_t tailbag[kFwdThreads];    // per lane group: bag whose tail partial it holds
+  int32_t nvp[kFwdThreads][2];     // per lane group: valid counts of head/tail partials
+  float4 part[2][kFwdWarps * 64];  // per lane group: head / tail partial sums
+  int32_t warp_sum[kFwdWarps];
+  int32_t seg[2];
+  int32_t nlong;
+  ColMeta cm;                      // metadata of the chunk's column
 };
 
 __device__ __forceinline__ float4 f4zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
@@ -112,58 +139,6 @@ __device__ __forceinline__ void record(const FwdArgs& a, int st, int64_t t, int3
   }
 }
 
-// Sum of the rows of chunks chunk0, chunk0 + step, ... of [lo, hi) into the
-// caller's per-lane accumulators (lane group `grp`, float4 slot `sub`).
-template <int V>
-__device__ __forceinline__ void gather_pool(const FwdArgs& a, const ColMeta& m, int st, int64_t lo,
-                                            int64_t hi, int chunk0, int step, int glog,
-                                            uint32_t gsrc, float4 (&acc)[V], int& nv) {
-  const int lane = threadIdx.x & 31;
-  const int G = 32 >> glog;
-  const int grp = lane >> glog;
-  const int sub = lane & ((1 << glog) - 1);
-  const float* E = m.weight;
-  for (int64_t base = lo + (int64_t)chunk0 * 32; base < hi; base += (int64_t)step * 32) {
-    const int cnt = (int)(hi - base < 32 ? hi - base : 32);
-    int32_t row = -1;
-    if (lane < cnt) {
-      row = col_row(m, a.ids, a.fvals, base + lane);
-      record(a, st, base + lane, row, m, gsrc);
-    }
-    nv += __popc(__ballot_sync(kFull, row >= 0));
-    for (int k = 0; k < cnt; k += 4 * G) {
-      float4 v[4][V];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j = k + u * G + grp;
-        const int r = __shfl_sync(kFull, row, j & 31);
-        const bool ok = (j < cnt) && (r >= 0);
-#pragma unroll
-        for (int q = 0; q < V; ++q) {
-          const int f4 = sub + q * 32;
-          v[u][q] = (ok && f4 < m.dim4) ? ldg4(E + (int64_t)r * m.dim + f4 * 4) : f4zero();
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int q = 0; q < V; ++q) f4add(acc[q], v[u][q]);
-    }
-  }
-}
-
-template <int V>
-__device__ __forceinline__ void group_reduce(float4 (&acc)[V], int glog) {
-#pragma unroll
-  for (int q = 0; q < V; ++q)
-    for (int off = 1 << glog; off < 32; off <<= 1) {
-      acc[q].x += __shfl_xor_sync(kFull, acc[q].x, off);
-      acc[q].y += __shfl_xor_sync(kFull, acc[q].y, off);
-      acc[q].z += __shfl_xor_sync(kFull, acc[q].z, off);
-      acc[q].w += __shfl_xor_sync(kFull, acc[q].w, off);
-    }
-}
-
 // Final value of float4 slot f4 of a pooled bag: mean / sum / default.
 __device__ __forceinline__ float4 finish(const ColMeta& m, float4 s, int nv, int f4) {
   if (nv == 0) return m.dflt ? ldg4(m.dflt + f4 * 4) : f4zero();
@@ -177,31 +152,275 @@ __device__ __forceinline__ float4 finish(const ColMeta& m, float4 s, int nv, int
   return s;
 }
 
-// Padded (unpooled) copy of positions chunk0, chunk0 + step, ... of a bag.
-template <int V>
-__device__ __forceinline__ void padded_copy(const FwdArgs& a, const ColMeta& m, int st, int64_t lo,
-                                            int64_t hi, int32_t b, int chunk0, int step, int glog) {
-  const int lane = threadIdx.x & 31;
-  const int G = 32 >> glog;
-  const int grp = lane >> glog;
-  const int sub = lane & ((1 << glog) - 1);
-  const int P = m.pad_len;
-  const int64_t len = hi - lo;
-  const int64_t seq0 = m.seq_unit * a.batch + (int64_t)b * P * m.dim;
-  float* dst = a.seq_out + seq0;
-  const float* E = m.weight;
-  for (int64_t p0 = (int64_t)chunk0 * 32; p0 < P; p0 += (int64_t)step * 32) {
-    const int cnt = (int)(P - p0 < 32 ? P - p0 : 32);
-    int32_t row = -1;
-    const int64_t p = p0 + lane;
-    if (lane < cnt && p < len) {
-      row = col_row(m, a.ids, a.fvals, lo + p);
-      record(a, st, lo + p, row, m, kPadBit | (uint32_t)((seq0 + p * m.dim) >> 2));
-    }
-    for (int k = 0; k < cnt; k += 4 * G) {
-      float4 v[4][V];
+__device__ __forceinline__ int lanes_log2(int dim4) {
+  const int g = dim4 > 32 ? 32 : dim4;
+  int l = 0;
+  while ((1 << l) < g) ++l;
+  return l;
+}
+
+// Exclusive block scan of one int per thread (kFwdThreads threads).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sum, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sum[warp] = x;
+  __syncthreads();
+  int base = 0;
+  total = 0;
+#pragma unroll
+  for (int w = 0; w < kFwdWarps; ++w) {
+    const int s = warp_sum[w];
+    if (w < warp) base += s;
+    total += s;
+  }
+  __syncthreads();
+  return base + x - v;
+}
+
+// ---------------------------------------------------------------------------
+// phase B: pooled bags of a chunk, one equal range of values per lane group
+// ---------------------------------------------------------------------------
+template <int V>
+__device__ void pool_chunk(const FwdArgs& a, FwdSmem& sm, const ColMeta& m, int ns, int T, int b0,
+                           int glog) {
+  constexpr int U = kU / V;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int G = 32 >> glog;
+  const int grp = lane >> glog, sub = lane & ((1 << glog) - 1);
+  const int q = warp * G + grp;                 // lane group id
+  const int NG = kFwdWarps * G;
+  const int R = (T + NG - 1) / NG;
+  const int k0 = min(q * R, T), k1 = min(k0 + R, T);
+  const float* E = m.weight;
+
+  float4 acc[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) acc[v] = f4zero();
+  int nv = 0;
+  int curb = k0 < k1 ? (int)sm.bag[k0] : -1;
+  bool head = k0 > 0 && k0 < k1 && (int)sm.bag[k0 - 1] == curb;
+  if (sub == 0) sm.tailbag[q] = -1;
+
+  auto write_out = [&](int b, const float4 (&s)[V], int cnt) {
+    const int bag = b0 + b;
+    float* y = a.out + (int64_t)bag * a.ldo + m.out_col;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int f4 = sub + v * 32;
+      if (f4 < m.dim4) *reinterpret_cast<float4*>(y + f4 * 4) = finish(m, s[v], cnt, f4);
+    }
+    if (a.inv_n && sub == 0 && m.pooling == EMB_POOL_MEAN)
+      a.inv_n[(uint32_t)m.col * (uint32_t)a.batch + (uint32_t)bag] = cnt > 0 ? 1.0f / (float)cnt : 0.0f;
+  };
+  auto flush = [&](bool tail) {
+    if (!head && !tail) {
+      write_out(curb, acc, nv);
+    } else {
+      const int side = head ? 0 : 1;
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int f4 = sub + v * 32;
+        if (f4 < m.dim4) sm.part[side][q * m.dim4 + f4] = acc[v];
+      }
+      if (sub == 0) {
+        sm.nvp[q][side] = nv;
+        if (!head) sm.tailbag[q] = curb;
+      }
+    }
+  };
+
+  for (int j = 0; j < R; j += U) {
+    float4 vals[U][V];
+    int bg[U];
+    bool ok[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int k = k0 + j + u;
+      const bool in = k < k1;
+      const int r = in ? sm.rows[k] : -1;
+      bg[u] = in ? (int)sm.bag[k] : -1;
+      ok[u] = in && r >= 0;
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int f4 = sub + v * 32;
+        vals[u][v] = (ok[u] && f4 < m.dim4) ? ldg4(E + (int64_t)r * m.dim + f4 * 4) : f4zero();
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (bg[u] < 0) continue;
+      if (bg[u] != curb) {
+        flush(false);
+        curb = bg[u];
+        head = false;
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[v] = f4zero();
+        nv = 0;
+      }
+#pragma unroll
+      for (int v = 0; v < V; ++v) f4add(acc[v], vals[u][v]);
+      nv += ok[u];
+    }
+  }
+  if (k0 < k1) flush(k1 < T && (int)sm.bag[k1] == curb);
+  __syncthreads();
+
+  // the group holding a cut bag's first value adds the partials in order
+  const int tb = sm.tailbag[q];
+  if (tb >= 0) {
+    float4 s[V];
+    int cnt = sm.nvp[q][1];
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int f4 = sub + v * 32;
+      s[v] = f4 < m.dim4 ? sm.part[1][q * m.dim4 + f4] : f4zero();
+    }
+    const int last = (sm.pos[tb] + sm.len[tb] - 1) / R;
+    for (int q2 = q + 1; q2 <= last; ++q2) {
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int f4 = sub + v * 32;
+        if (f4 < m.dim4) f4add(s[v], sm.part[0][q2 * m.dim4 + f4]);
+      }
+      cnt += sm.nvp[q2][0];
+    }
+    write_out(tb, s, cnt);
+  }
+  // empty bags: default vector
+  for (int i = threadIdx.x; i < ns; i += kFwdThreads) {
+    if (sm.len[i] != 0 || sm.hi[i] < 0) continue;
+    float* y = a.out + (int64_t)(b0 + i) * a.ldo + m.out_col;
+    for (int f4 = 0; f4 < m.dim4; ++f4) *reinterpret_cast<float4*>(y + f4 * 4) = finish(m, f4zero(), 0, f4);
+    if (a.inv_n && m.pooling == EMB_POOL_MEAN)
+      a.inv_n[(uint32_t)m.col * (uint32_t)a.batch + (uint32_t)(b0 + i)] = 0.0f;
+  }
+}
+
+// phase B for padded columns: ns bags x pad_len output rows, flat over groups.
+template <int V>
+__device__ void pad_chunk(const FwdArgs& a, FwdSmem& sm, const ColMeta& m, int ns, int b0, int glog) {
+  constexpr int U = kU / V;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int G = 32 >> glog;
+  const int grp = lane >> glog, sub = lane & ((1 << glog) - 1);
+  const int q = warp * G + grp;
+  const int NG = kFwdWarps * G;
+  const int P = m.pad_len;
+  const int total = ns * P;
+  const float* E = m.weight;
+  for (int base = 0; base < total; base += NG * U) {
+    float4 vals[U][V];
+    int o[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      o[u] = base + u * NG + q;
+      int r = -1;
+      if (o[u] < total) {
+        const int i = o[u] / P, p = o[u] - i * P;
+        if (sm.hi[i] >= 0 && p < sm.len[i]) r = sm.rows[sm.pos[i] + p];
+      }
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int f4 = sub + v * 32;
+        vals[u][v] = (r >= 0 && f4 < m.dim4) ? ldg4(E + (int64_t)r * m.dim + f4 * 4) : f4zero();
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (o[u] >= total) continue;
+      const int i = o[u] / P, p = o[u] - i * P;
+      if (sm.hi[i] < 0) continue;   // long bag: phase C writes it
+      float* dst = a.seq_out + m.seq_unit * a.batch + ((int64_t)(b0 + i) * P + p) * m.dim;
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int f4 = sub + v * 32;
+        if (f4 < m.dim4) *reinterpret_cast<float4*>(dst + f4 * 4) = vals[u][v];
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// phase C: one long bag, all warps; values transformed on the fly
+// ---------------------------------------------------------------------------
+template <int V>
+__device__ void cta_bag(const FwdArgs& a, FwdSmem& sm, int st, const ColMeta& m, int32_t b, int64_t lo,
+                        int64_t hi, int glog) {
+  constexpr int U = kU / V;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int G = 32 >> glog;
+  const int grp = lane >> glog, sub = lane & ((1 << glog) - 1);
+  const float* E = m.weight;
+  if (m.pooling == EMB_POOL_NONE_PADDED) {
+    const int P = m.pad_len;
+    const int64_t len = hi - lo;
+    const int64_t seq0 = m.seq_unit * a.batch + (int64_t)b * P * m.dim;
+    float* dst = a.seq_out + seq0;
+    for (int64_t p0 = (int64_t)warp * 32; p0 < P; p0 += (int64_t)kFwdWarps * 32) {
+      const int cnt = (int)(P - p0 < 32 ? P - p0 : 32);
+      int32_t row = -1;
+      const int64_t p = p0 + lane;
+      if (lane < cnt && p < len) {
+        row = col_row(m, a.ids, a.fvals, lo + p);
+        record(a, st, lo + p, row, m, kPadBit | (uint32_t)((seq0 + p * m.dim) >> 2));
+      }
+      for (int k = 0; k < cnt; k += U * G) {
+        float4 v[U][V];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int j = k + u * G + grp;
+          const int r = __shfl_sync(kFull, row, j & 31);
+          const bool ok = (j < cnt) && (r >= 0);
+#pragma unroll
+          for (int q = 0; q < V; ++q) {
+            const int f4 = sub + q * 32;
+            v[u][q] = (ok && f4 < m.dim4) ? ldg4(E + (int64_t)r * m.dim + f4 * 4) : f4zero();
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int j = k + u * G + grp;
+#pragma unroll
+          for (int q = 0; q < V; ++q) {
+            const int f4 = sub + q * 32;
+            if (j < cnt && f4 < m.dim4) *reinterpret_cast<float4*>(dst + (p0 + j) * m.dim + f4 * 4) = v[u][q];
+          }
+        }
+      }
+    }
+    if (a.rows_dbg || a.keys)
+      for (int64_t t = lo + P + threadIdx.x; t < hi; t += kFwdThreads) {
+        const int64_t r = a.rec_base[st] + t;
+        if (a.rows_dbg) a.rows_dbg[r] = col_row(m, a.ids, a.fvals, t);
+        if (a.keys) {
+          a.keys[r] = a.key_sentinel;
+          a.vals[r] = 0u;
+        }
+      }
+    return;
+  }
+  const uint32_t gsrc = (uint32_t)m.col * (uint32_t)a.batch + (uint32_t)b;
+  float4 acc[V];
+#pragma unroll
+  for (int q = 0; q < V; ++q) acc[q] = f4zero();
+  int nv = 0;
+  for (int64_t base = lo + (int64_t)warp * 32; base < hi; base += (int64_t)kFwdWarps * 32) {
+    const int cnt = (int)(hi - base < 32 ? hi - base : 32);
+    int32_t row = -1;
+    if (lane < cnt) {
+      row = col_row(m, a.ids, a.fvals, base + lane);
+      record(a, st, base + lane, row, m, gsrc);
+    }
+    nv += __popc(__ballot_sync(kFull, row >= 0));
+    for (int k = 0; k < cnt; k += U * G) {
+      float4 v[U][V];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
         const int j = k + u * G + grp;
         const int r = __shfl_sync(kFull, row, j & 31);
         const bool ok = (j < cnt) && (r >= 0);
@@ -212,188 +431,164 @@ __device__ __forceinline__ void padded_copy(const FwdArgs& a, const ColMeta& m, 
         }
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int j = k + u * G + grp;
+      for (int u = 0; u < U; ++u)
 #pragma unroll
-        for (int q = 0; q < V; ++q) {
-          const int f4 = sub + q * 32;
-          if (j < cnt && f4 < m.dim4)
-            *reinterpret_cast<float4*>(dst + (p0 + j) * m.dim + f4 * 4) = v[u][q];
-        }
-      }
+        for (int q = 0; q < V; ++q) f4add(acc[q], v[u][q]);
     }
   }
-  // values past pad_len: no output, no gradient
-  if (a.rows_dbg || a.keys)
-    for (int64_t t = lo + P + (int64_t)chunk0 * 32 + lane; t < hi; t += (int64_t)step * 32) {
-      const int64_t r = a.rec_base[st] + t;
-      if (a.rows_dbg) a.rows_dbg[r] = col_row(m, a.ids, a.fvals, t);
-      if (a.keys) {
-        a.keys[r] = a.key_sentinel;
-        a.vals[r] = 0u;
-      }
-    }
-}
-
-struct SegInfo {
-  int32_t c;   // plan column
-  int32_t b;   // bag
-  int64_t lo, hi;
-};
-
-__device__ __forceinline__ SegInfo seg_info(const FwdArgs& a, int st, int s) {
-  SegInfo si;
-  const uint32_t cl = div_magic32((uint32_t)s, a.bdiv);
-  si.b = s - (int32_t)cl * a.batch;
-  si.c = __ldg(a.stream_cols + a.col_base[st] + cl);
-  bool bad = false;
-  const int32_t* offs = a.offs[st];
-  si.lo = clamp_off(__ldg(offs + s), a.n[st], bad);
-  si.hi = clamp_off(__ldg(offs + s + 1), a.n[st], bad);
-  if (si.hi < si.lo) { si.hi = si.lo; bad = true; }
-  if (bad && (threadIdx.x & 31) == 0) latch(a.status, EMB_ERR_BAD_INDEX);
-  return si;
-}
-
-// One warp pools (or copies) one whole bag.
-template <int V>
-__device__ void warp_bag(const FwdArgs& a, int st, const SegInfo& si, const ColMeta& m, int glog) {
-  const int lane = threadIdx.x & 31;
-  if (m.pooling == EMB_POOL_NONE_PADDED) {
-    padded_copy<V>(a, m, st, si.lo, si.hi, si.b, 0, 1, glog);
-    return;
-  }
-  const uint32_t gsrc = (uint32_t)si.c * (uint32_t)a.batch + (uint32_t)si.b;
-  float4 acc[V];
 #pragma unroll
-  for (int q = 0; q < V; ++q) acc[q] = f4zero();
-  int nv = 0;
-  gather_pool<V>(a, m, st, si.lo, si.hi, 0, 1, glog, gsrc, acc, nv);
-  group_reduce<V>(acc, glog);
-  if ((lane >> glog) == 0) {
-    float* y = a.out + (int64_t)si.b * a.ldo + m.out_col;
+  for (int q = 0; q < V; ++q)
+    for (int off = 1 << glog; off < 32; off <<= 1) {
+      acc[q].x += __shfl_xor_sync(kFull, acc[q].x, off);
+      acc[q].y += __shfl_xor_sync(kFull, acc[q].y, off);
+      acc[q].z += __shfl_xor_sync(kFull, acc[q].z, off);
+      acc[q].w += __shfl_xor_sync(kFull, acc[q].w, off);
+    }
+  float4* red = sm.part[0];   // [kFwdWarps][64]
+  if (grp == 0) {
 #pragma unroll
     for (int q = 0; q < V; ++q) {
-      const int f4 = (lane & ((1 << glog) - 1)) + q * 32;
-      if (f4 < m.dim4) *reinterpret_cast<float4*>(y + f4 * 4) = finish(m, acc[q], nv, f4);
+      const int f4 = sub + q * 32;
+      if (f4 < m.dim4) red[warp * 64 + f4] = acc[q];
     }
   }
-  if (a.inv_n && lane == 0 && m.pooling == EMB_POOL_MEAN) a.inv_n[gsrc] = nv > 0 ? 1.0f / (float)nv : 0.0f;
-}
-
-// All warps of the CTA pool (or copy) one long bag.
-template <int V>
-__device__ void cta_bag(const FwdArgs& a, int st, const SegInfo& si, const ColMeta& m, int glog,
-                        float4 (*s_red)[64], int* s_nv) {
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  if (m.pooling == EMB_POOL_NONE_PADDED) {
-    padded_copy<V>(a, m, st, si.lo, si.hi, si.b, warp, kFwdWarps, glog);
-    return;
-  }
-  const uint32_t gsrc = (uint32_t)si.c * (uint32_t)a.batch + (uint32_t)si.b;
-  float4 acc[V];
-#pragma unroll
-  for (int q = 0; q < V; ++q) acc[q] = f4zero();
-  int nv = 0;
-  gather_pool<V>(a, m, st, si.lo, si.hi, warp, kFwdWarps, glog, gsrc, acc, nv);
-  group_reduce<V>(acc, glog);
-  if ((lane >> glog) == 0) {
-#pragma unroll
-    for (int q = 0; q < V; ++q) {
-      const int f4 = (lane & ((1 << glog) - 1)) + q * 32;
-      if (f4 < m.dim4) s_red[warp][f4] = acc[q];
-    }
-  }
-  if (lane == 0) s_nv[warp] = nv;
+  if (lane == 0) sm.nvp[warp][0] = nv;
   __syncthreads();
   int tot = 0;
 #pragma unroll
-  for (int w = 0; w < kFwdWarps; ++w) tot += s_nv[w];
-  for (int f4 = threadIdx.x; f4 < m.dim4; f4 += blockDim.x) {
-    float4 s = s_red[0][f4];
+  for (int w = 0; w < kFwdWarps; ++w) tot += sm.nvp[w][0];
+  for (int f4 = threadIdx.x; f4 < m.dim4; f4 += kFwdThreads) {
+    float4 s = red[f4];
 #pragma unroll
-    for (int w = 1; w < kFwdWarps; ++w) f4add(s, s_red[w][f4]);
-    *reinterpret_cast<float4*>(a.out + (int64_t)si.b * a.ldo + m.out_col + f4 * 4) = finish(m, s, tot, f4);
+    for (int w = 1; w < kFwdWarps; ++w) f4add(s, red[w * 64 + f4]);
+    *reinterpret_cast<float4*>(a.out + (int64_t)b * a.ldo + m.out_col + f4 * 4) = finish(m, s, tot, f4);
   }
   if (a.inv_n && threadIdx.x == 0 && m.pooling == EMB_POOL_MEAN)
     a.inv_n[gsrc] = tot > 0 ? 1.0f / (float)tot : 0.0f;
   __syncthreads();
 }
 
-__device__ __forceinline__ int lanes_log2(int dim4) {
-  // lanes per row: next power of two >= min(dim4, 32)
-  int g = dim4 > 32 ? 32 : dim4;
-  int l = 0;
-  while ((1 << l) < g) ++l;
-  return l;
-}
-
-__global__ void __launch_bounds__(kFwdThreads) k_forward(const FwdArgs a) {
-  __shared__ int s_seg[2];
-  __shared__ int s_cursor;
-  __shared__ int s_nlong;
-  __shared__ int s_long[kMaxLongPerTile];
-  __shared__ float4 s_red[kFwdWarps][64];
-  __shared__ int s_nv[kFwdWarps];
-
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kFwdThreads, 4) k_forward(const FwdArgs a) {
+  __shared__ FwdSmem sm;
   int tile = blockIdx.x, st = 0;
   if (tile >= a.tiles[0]) {
     st = 1;
     tile -= a.tiles[0];
   }
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = a.ncols[st] * a.batch;
   const int64_t e0 = (int64_t)tile * a.tile_elems;
   const bool last = tile == a.tiles[st] - 1;
+  const int32_t* offs = a.offs[st];
+  const int64_t n = a.n[st];
   if (warp == 0) {
-    const int r = warp_lower_bound(a.offs[st], S, e0, a.n[st]);
-    if (lane == 0) s_seg[0] = r;
+    const int r = warp_lower_bound(offs, S, e0, n);
+    if (lane == 0) sm.seg[0] = r;
   } else if (warp == 1) {
-    const int r = last ? S : warp_lower_bound(a.offs[st], S, e0 + a.tile_elems, a.n[st]);
-    if (lane == 0) s_seg[1] = r;
-  }
-  if (threadIdx.x == 0) {
-    s_cursor = 0;
-    s_nlong = 0;
+    const int r = last ? S : warp_lower_bound(offs, S, e0 + a.tile_elems, n);
+    if (lane == 0) sm.seg[1] = r;
   }
   __syncthreads();
-  const int s_lo = s_seg[0], s_hi = s_seg[1];
+  const int s_hi = sm.seg[1];
+  int cur = sm.seg[0];
+  while (cur < s_hi) {
+    // ---- chunk setup: one bag per thread, all inside column cl0 ----
+    const int cl0 = (int)div_magic32((uint32_t)cur, a.bdiv);
+    const int b0 = cur - cl0 * a.batch;
+    const int navail = min(kChunkBags, min(s_hi, (cl0 + 1) * a.batch) - cur);
+    static_assert(sizeof(ColMeta) % 4 == 0 && sizeof(ColMeta) / 4 <= kFwdThreads, "metadata copy");
+    if (tid < (int)(sizeof(ColMeta) / 4))
+      reinterpret_cast<int32_t*>(&sm.cm)[tid] =
+          __ldg(reinterpret_cast<const int32_t*>(a.meta + __ldg(a.stream_cols + a.col_base[st] + cl0)) + tid);
+    __syncthreads();
+    const ColMeta& m = sm.cm;
+    const bool padded = m.pooling == EMB_POOL_NONE_PADDED;
+    int64_t lo = 0, hi = 0;
+    int used = 0;
+    bool is_long = false;
+    if (tid < navail) {
+      bool bad = false;
+      lo = clamp_off(__ldg(offs + cur + tid), n, bad);
+      hi = clamp_off(__ldg(offs + cur + tid + 1), n, bad);
+      if (hi < lo) { hi = lo; bad = true; }
+      if (bad) latch(a.status, EMB_ERR_BAD_INDEX);
+      const int64_t len = hi - lo;
+      is_long = (padded ? (int64_t)m.pad_len : len) > kLongBag;
+      used = is_long ? 0 : (int)(padded ? (len < m.pad_len ? len : (int64_t)m.pad_len) : len);
+    }
+    int total = 0;
+    const int pos = block_exclusive_scan(used, sm.warp_sum, total);
+    const bool fits = tid < navail && pos + used <= kChunkElems;
+    const int ns = __syncthreads_count(fits);
+    if (tid == 0) sm.nlong = 0;
+    __syncthreads();
+    if (tid < ns) {
+      sm.pos[tid] = pos;
+      sm.lo[tid] = (int32_t)lo;
+      sm.len[tid] = used;
+      sm.hi[tid] = is_long ? -1 : (int32_t)hi;
+      if (is_long) sm.longs[atomicAdd(&sm.nlong, 1)] = tid;
+      if (tid == ns - 1) sm.pos[ns] = pos + used;
+      for (int k = pos; k < pos + used; ++k) sm.bag[k] = (uint8_t)tid;
+    }
+    __syncthreads();
+    const int T = sm.pos[ns];
 
-  // Phase 1: short bags, one warp each, pulled from a shared cursor.
-  for (;;) {
-    int k = 0;
-    if (lane == 0) k = atomicAdd(&s_cursor, 1);
-    k = __shfl_sync(kFull, k, 0);
-    const int s = s_lo + k;
-    if (s >= s_hi) break;
-    const SegInfo si = seg_info(a, st, s);
-    const ColMeta m = a.meta[si.c];
-    const int work = m.pooling == EMB_POOL_NONE_PADDED ? m.pad_len : (int)(si.hi - si.lo);
-    if (work > kLongBag) {
-      int idx = 0;
-      if (lane == 0) idx = atomicAdd(&s_nlong, 1);
-      idx = __shfl_sync(kFull, idx, 0);
-      if (idx < kMaxLongPerTile) {
-        if (lane == 0) s_long[idx] = s;
-        continue;
+    // ---- phase A: transform every value of the chunk's short bags ----
+    for (int k = tid; k < T; k += kFwdThreads) {
+      const int i = sm.bag[k];
+      const int64_t t = (int64_t)sm.lo[i] + (k - sm.pos[i]);
+      const int32_t row = col_row(m, a.ids, a.fvals, t);
+      sm.rows[k] = row;
+      if (a.rows_dbg || a.keys) {
+        uint32_t gsrc;
+        if (padded)
+          gsrc = kPadBit | (uint32_t)((m.seq_unit * a.batch +
+                                       ((int64_t)(b0 + i) * m.pad_len + (k - sm.pos[i])) * m.dim) >> 2);
+        else
+          gsrc = (uint32_t)m.col * (uint32_t)a.batch + (uint32_t)(b0 + i);
+        record(a, st, t, row, m, gsrc);
       }
     }
-    const int glog = lanes_log2(m.dim4);
-    if (m.dim4 > 32) warp_bag<2>(a, st, si, m, glog);
-    else warp_bag<1>(a, st, si, m, glog);
-  }
-  __syncthreads();
+    // values past pad_len of short padded bags: no output, no gradient
+    if (padded && (a.rows_dbg || a.keys) && tid < ns && sm.hi[tid] >= 0)
+      for (int64_t t = (int64_t)sm.lo[tid] + m.pad_len; t < sm.hi[tid]; ++t) {
+        const int64_t r = a.rec_base[st] + t;
+        if (a.rows_dbg) a.rows_dbg[r] = col_row(m, a.ids, a.fvals, t);
+        if (a.keys) {
+          a.keys[r] = a.key_sentinel;
+          a.vals[r] = 0u;
+        }
+      }
+    __syncthreads();
 
-  // Phase 2: long bags, all warps together, one after the other.
-  const int nlong = min(s_nlong, kMaxLongPerTile);
-  for (int i = 0; i < nlong; ++i) {
-    const SegInfo si = seg_info(a, st, s_long[i]);
-    const ColMeta m = a.meta[si.c];
+    // ---- phase B: pool / copy ----
     const int glog = lanes_log2(m.dim4);
-    if (m.dim4 > 32) cta_bag<2>(a, st, si, m, glog, s_red, s_nv);
-    else cta_bag<1>(a, st, si, m, glog, s_red, s_nv);
+    if (padded) {
+      if (m.dim4 > 32) pad_chunk<2>(a, sm, m, ns, b0, glog);
+      else pad_chunk<1>(a, sm, m, ns, b0, glog);
+    } else {
+      if (m.dim4 > 32) pool_chunk<2>(a, sm, m, ns, T, b0, glog);
+      else pool_chunk<1>(a, sm, m, ns, T, b0, glog);
+    }
+    __syncthreads();
+
+    // ---- phase C: long bags of the chunk ----
+    const int nlong = sm.nlong;
+    for (int j = 0; j < nlong; ++j) {
+      const int i = sm.longs[j];
+      bool bad = false;
+      const int64_t blo = clamp_off(__ldg(offs + cur + i), n, bad);
+      int64_t bhi = clamp_off(__ldg(offs + cur + i + 1), n, bad);
+      if (bhi < blo) bhi = blo;
+      if (m.dim4 > 32) cta_bag<2>(a, sm, st, m, b0 + i, blo, bhi, glog);
+      else cta_bag<1>(a, sm, st, m, b0 + i, blo, bhi, glog);
+    }
+    __syncthreads();
+    cur += ns;
   }
 }
 
@@ -440,8 +635,8 @@ emb_status launch_forward(emb_plan_s* p, int32_t batch, const int64_t* ids, cons
   a.status = p->status_d;
   const int64_t total = n_ids + n_fvals;
   const int64_t resident = (int64_t)p->sm_count * p->fwd_ctas_per_sm;
-  int64_t want = total / std::max<int64_t>(1, 4 * resident);
-  int64_t E = 256;
+  const int64_t want = total / std::max<int64_t>(1, 8 * resident);
+  int64_t E = 512;
   while (E < want && E < kMaxTileElems) E <<= 1;
   a.tile_elems = (int32_t)E;
   a.tiles[0] = a.ncols[0] > 0 ? (int32_t)(n_ids / E + 1) : 0;
