@@ -1,13 +1,675 @@
-// backward.cu -- K-B: radix sort of (global row, gradient source) pairs,
-// per-unique-row gradient reduction and the fused sparse Adagrad update.
+// backward.cu -- K-B: backward of the fused forward plus one sparse Adagrad
+// step (RecIS §3.2 Algorithm 1, backward semantics: each valid contribution
+// r carries w_r * G[s(r), :]; Figure 3: local reduce-ID of the touched rows).
+//
+// Instead of the pages' wave-level merge with global atomics, the
+// contributions the forward recorded as (global row, gradient source) pairs
+// are radix-sorted by row, so every unique row becomes one contiguous run
+// with exactly one writer:
+//   1. k_digit_hist  -- digit histograms of all passes in one read of the keys;
+//   2. k_onesweep    -- per 8-bit digit pass, a stable LSD scatter: a CTA
+//                       ranks its tile in shared memory, publishes per-digit
+//                       counts and resolves its global offsets by decoupled
+//                       look-back over the earlier tiles (Adinets & Merrill,
+//                       "Onesweep", 2022); every wait is bounded;
+//   3. k_segreduce   -- lane groups of dim/4 lanes take equal ranges of sorted
+//                       contributions, gather scale * G rows with 16-byte
+//                       loads and sum each run; a run owned by one group is
+//                       finished at once (fp32 Adagrad on its row); runs cut
+//                       by group boundaries are combined in shared memory in
+//                       group order, runs cut by CTA boundaries leave partials;
+//   4. k_seg_fixup   -- sums the CTA partials of each cut run in CTA order and
+//                       finishes it.
+// The sum order is fixed by the sort (stable) and the range layout, so a run
+// of the same inputs gives bit-identical results.
+#include <algorithm>
+
 #include "plan.cuh"
 
 namespace emb {
 
-emb_status launch_backward(emb_plan_s* p, const float* grad_out, const float* grad_seq, float lr,
-                           float eps, cudaStream_t stream, const emb_backward_debug* dbg) {
-  (void)p; (void)grad_out; (void)grad_seq; (void)lr; (void)eps; (void)stream; (void)dbg;
-  return EMB_ERR_UNSUPPORTED;
+constexpr uint32_t kFlagAgg = 1u << 30;
+constexpr uint32_t kFlagInc = 2u << 30;
+constexpr uint32_t kCountMask = (1u << 30) - 1;
+constexpr int kSpinLimit = 1 << 22;
+constexpr int kSortWarps = kSortThreads / 32;
+constexpr int kSegThreads = 256;
+constexpr int kSegWarps = kSegThreads / 32;
+constexpr int kSegU = 4;
+
+// ---------------------------------------------------------------------------
+// radix sort
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(512) k_digit_hist(const uint32_t* __restrict__ keys, int64_t n, int passes,
+                                                    uint32_t* __restrict__ hist) {
+  __shared__ uint32_t h[4 * kRadix];
+  for (int i = threadIdx.x; i < 4 * kRadix; i += blockDim.x) h[i] = 0;
+  __syncthreads();
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const uint32_t k = __ldg(keys + i);
+    for (int p = 0; p < passes; ++p) atomicAdd(&h[p * kRadix + ((k >> (p * kRadixBits)) & (kRadix - 1))], 1u);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < passes * kRadix; i += blockDim.x)
+    if (h[i]) atomicAdd(&hist[i], h[i]);
+}
+
+struct SortSmem {
+  uint32_t keys[kSortTile];
+  uint32_t vals[kSortTile];
+  uint32_t whist[kSortWarps][kRadix];  // per-warp digit counts, then warp offsets
+  uint32_t dstart[kRadix];             // first slot of each digit inside the tile
+  uint32_t goff[kRadix];               // global position of the tile's first item of each digit
+  uint32_t hscan[kRadix];              // exclusive scan of the pass histogram
+  uint32_t wsum[kSortWarps];
+  uint32_t tile;
+};
+
+// Exclusive scan over the first 256 threads' values (all threads call).
+__device__ __forceinline__ uint32_t scan256(uint32_t v, uint32_t* wsum) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31 && warp < kRadix / 32) wsum[warp] = x;
+  __syncthreads();
+  uint32_t base = 0;
+  if (warp < kRadix / 32)
+    for (int w = 0; w < warp; ++w) base += wsum[w];
+  __syncthreads();
+  return base + x - v;
+}
+
+__global__ void __launch_bounds__(kSortThreads, 2)
+    k_onesweep(const uint32_t* __restrict__ kin, const uint32_t* __restrict__ vin, uint32_t* __restrict__ kout,
+               uint32_t* __restrict__ vout, int64_t n, int shift, const uint32_t* __restrict__ hist,
+               uint32_t* lookback, uint32_t* tile_ctr, uint32_t* status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  SortSmem& sm = *reinterpret_cast<SortSmem*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) sm.tile = atomicAdd(tile_ctr, 1u);
+  for (int i = tid; i < kSortWarps * kRadix; i += kSortThreads) (&sm.whist[0][0])[i] = 0;
+  const uint32_t hs = scan256(tid < kRadix ? __ldg(hist + tid) : 0u, sm.wsum);
+  if (tid < kRadix) sm.hscan[tid] = hs;
+  __syncthreads();
+  const uint32_t t = sm.tile;
+  const int64_t base = (int64_t)t * kSortTile;
+  const int64_t wbase = base + (int64_t)warp * 32 * kSortItems;
+
+  uint32_t k[kSortItems], v[kSortItems], r[kSortItems];
+#pragma unroll
+  for (int i = 0; i < kSortItems; ++i) {
+    const int64_t idx = wbase + i * 32 + lane;
+    const bool ok = idx < n;
+    k[i] = ok ? kin[idx] : 0u;
+    v[i] = ok ? vin[idx] : 0u;
+  }
+  const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < kSortItems; ++i) {
+    const int64_t idx = wbase + i * 32 + lane;
+    const uint32_t d = idx < n ? (k[i] >> shift) & (kRadix - 1) : (uint32_t)kRadix;
+    const unsigned peers = __match_any_sync(kFull, d);
+    const int leader = __ffs(peers) - 1;
+    uint32_t old = 0;
+    if (lane == leader && d < (uint32_t)kRadix) {
+      old = sm.whist[warp][d];
+      sm.whist[warp][d] = old + __popc(peers);
+    }
+    old = __shfl_sync(kFull, old, leader);
+    r[i] = old + __popc(peers & lt);
+  }
+  __syncthreads();
+
+  uint32_t cnt = 0;
+  if (tid < kRadix) {
+    for (int w = 0; w < kSortWarps; ++w) {
+      const uint32_t c = sm.whist[w][tid];
+      sm.whist[w][tid] = cnt;
+      cnt += c;
+    }
+    volatile uint32_t* mine = lookback + (int64_t)t * kRadix + tid;
+    *mine = (t == 0 ? kFlagInc : kFlagAgg) | cnt;
+  }
+  const uint32_t ds = scan256(cnt, sm.wsum);
+  if (tid < kRadix) {
+    sm.dstart[tid] = ds;
+    uint32_t excl = 0;
+    if (t > 0) {
+      int64_t j = (int64_t)t - 1;
+      int spins = 0;
+      while (j >= 0) {
+        const uint32_t w = *(volatile const uint32_t*)(lookback + j * kRadix + tid);
+        const uint32_t flag = w & ~kCountMask;
+        if (flag == 0u) {
+          if (++spins > kSpinLimit) {
+            latch(status, EMB_ERR_TIMEOUT);
+            break;
+          }
+          __nanosleep(32);
+          continue;
+        }
+        excl += w & kCountMask;
+        if (flag == kFlagInc) break;
+        --j;
+      }
+      *(volatile uint32_t*)(lookback + (int64_t)t * kRadix + tid) = kFlagInc | ((excl + cnt) & kCountMask);
+    }
+    sm.goff[tid] = sm.hscan[tid] + excl;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kSortItems; ++i) {
+    const int64_t idx = wbase + i * 32 + lane;
+    if (idx < n) {
+      const uint32_t d = (k[i] >> shift) & (kRadix - 1);
+      const uint32_t pos = sm.dstart[d] + sm.whist[warp][d] + r[i];
+      sm.keys[pos] = k[i];
+      sm.vals[pos] = v[i];
+    }
+  }
+  __syncthreads();
+  const int tile_n = (int)(n - base < kSortTile ? n - base : kSortTile);
+  for (int j = tid; j < tile_n; j += kSortThreads) {
+    const uint32_t key = sm.keys[j];
+    const uint32_t d = (key >> shift) & (kRadix - 1);
+    const uint32_t o = sm.goff[d] + (j - sm.dstart[d]);
+    if (o < (uint64_t)n) {   // always true unless a look-back wait gave up
+      kout[o] = key;
+      vout[o] = sm.vals[j];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// run ranks (debug outputs only): rank[i] = number of run heads before i
+// ---------------------------------------------------------------------------
+constexpr int kScanBlock = 1024;
+
+__device__ __forceinline__ bool is_head(const uint32_t* keys, int64_t i, uint32_t sentinel) {
+  const uint32_t k = keys[i];
+  return k != sentinel && (i == 0 || keys[i - 1] != k);
+}
+
+__global__ void __launch_bounds__(kScanBlock) k_rank_reduce(const uint32_t* keys, int64_t n, uint32_t sentinel,
+                                                            uint32_t* part) {
+  const int64_t i = blockIdx.x * (int64_t)kScanBlock + threadIdx.x;
+  const int c = __syncthreads_count(i < n && is_head(keys, i, sentinel));
+  if (threadIdx.x == 0) part[blockIdx.x] = (uint32_t)c;
+}
+
+__global__ void __launch_bounds__(kScanBlock) k_rank_top(uint32_t* part, int nb, int64_t* n_unique) {
+  __shared__ uint32_t wsum[32];
+  __shared__ uint32_t carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int b0 = 0; b0 < nb; b0 += kScanBlock) {
+    const int i = b0 + threadIdx.x;
+    const uint32_t v = i < nb ? part[i] : 0u;
+    uint32_t x = v;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    uint32_t base = carry;
+    for (int w = 0; w < warp; ++w) base += wsum[w];
+    uint32_t tot = 0;
+    for (int w = 0; w < 32; ++w) tot += wsum[w];
+    if (i < nb) part[i] = base + x - v;
+    __syncthreads();
+    if (threadIdx.x == 0) carry += tot;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0 && n_unique) *n_unique = carry;
+}
+
+__global__ void __launch_bounds__(kScanBlock) k_rank_down(const uint32_t* keys, int64_t n, uint32_t sentinel,
+                                                          const uint32_t* part, uint32_t* rank) {
+  __shared__ uint32_t wsum[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t i = blockIdx.x * (int64_t)kScanBlock + threadIdx.x;
+  const uint32_t v = (i < n && is_head(keys, i, sentinel)) ? 1u : 0u;
+  uint32_t x = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  uint32_t base = part[blockIdx.x];
+  for (int w = 0; w < warp; ++w) base += wsum[w];
+  if (i < n) rank[i] = base + x - v;
+}
+
+// ---------------------------------------------------------------------------
+// segmented reduce + Adagrad
+// ---------------------------------------------------------------------------
+struct SegArgs {
+  const uint32_t* keys;
+  const uint32_t* vals;
+  int64_t n;
+  uint32_t sentinel;
+  const int4* colg;       // per column: out_col, 1 if MEAN, dim/4
+  const float* inv_n;
+  const float* grad_out;
+  int64_t ldg;
+  const float* grad_seq;
+  DivMagic32 bdiv;
+  int32_t batch;
+  const TableMeta* tables;
+  const uint32_t* table_base;
+  int32_t n_tables;
+  float lr, eps;
+  float4* partial;      // [n_blocks][2][maxdim4]: head / tail partial of each CTA
+  int32_t* part_pos;    // [n_blocks][2]: end of the head run / start of the tail run
+  uint8_t* part_thru;   // [n_blocks]: the CTA lies inside one run that continues past it
+  int32_t maxdim4;
+  int32_t glog;
+  // debug outputs
+  const uint32_t* rank;
+  int32_t* dbg_table;
+  int64_t* dbg_row;
+  int32_t* dbg_count;
+  float* dbg_grad;
+  int32_t dbg_ld;
+};
+
+struct SegSmem {
+  float4 part[2][kSegWarps * 64];
+  int32_t tail_start[kSegThreads];   // per group: start of its tail run, -1 if none
+  int32_t head_end[kSegThreads];     // per group: end of its head run, -1 if no head run
+  uint8_t head_thru[kSegThreads];    // per group: head run covers the whole range and goes on
+};
+
+__device__ __forceinline__ float4 seg_f4zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+
+__device__ __forceinline__ void seg_f4add(float4& a, const float4& b) {
+  a.x += b.x;
+  a.y += b.y;
+  a.z += b.z;
+  a.w += b.w;
+}
+
+__device__ __forceinline__ float adagrad1(float& w, float& acc, float g, float lr, float eps) {
+  const float a = __fadd_rn(acc, __fmul_rn(g, g));
+  const float den = __fadd_rn(__fsqrt_rn(a), eps);
+  acc = a;
+  w = __fsub_rn(w, __fdiv_rn(__fmul_rn(lr, g), den));
+  return w;
+}
+
+__device__ __forceinline__ int table_of_key(const uint32_t* base, int nt, uint32_t key) {
+  int lo = 0, hi = nt;  // largest t with base[t] <= key
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(base + mid) <= key) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// The unique writer of a row: Adagrad step with the summed gradient g.
+template <int V>
+__device__ void finish_row(const SegArgs& a, uint32_t key, int64_t start, int64_t end, const float4 (&g)[V],
+                           int sub) {
+  const int t = table_of_key(a.table_base, a.n_tables, key);
+  const int64_t row = key - __ldg(a.table_base + t);
+  const TableMeta tm = a.tables[t];
+  float* W = tm.weight + row * tm.dim;
+  float* A = tm.acc + row * tm.dim;
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    const int f4 = sub + v * 32;
+    if (f4 < tm.dim4) {
+      float4 w = *reinterpret_cast<float4*>(W + f4 * 4);
+      float4 ac = *reinterpret_cast<float4*>(A + f4 * 4);
+      adagrad1(w.x, ac.x, g[v].x, a.lr, a.eps);
+      adagrad1(w.y, ac.y, g[v].y, a.lr, a.eps);
+      adagrad1(w.z, ac.z, g[v].z, a.lr, a.eps);
+      adagrad1(w.w, ac.w, g[v].w, a.lr, a.eps);
+      *reinterpret_cast<float4*>(W + f4 * 4) = w;
+      *reinterpret_cast<float4*>(A + f4 * 4) = ac;
+    }
+  }
+  if (a.rank) {
+    const uint32_t u = a.rank[start];
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int f4 = sub + v * 32;
+      if (f4 < tm.dim4 && a.dbg_grad)
+        *reinterpret_cast<float4*>(a.dbg_grad + (int64_t)u * a.dbg_ld + f4 * 4) = g[v];
+    }
+    if (sub == 0) {
+      if (a.dbg_table) a.dbg_table[u] = t;
+      if (a.dbg_row) a.dbg_row[u] = row;
+      if (a.dbg_count) a.dbg_count[u] = (int32_t)(end - start);
+    }
+  }
+}
+
+// Gradient source of a contribution: pointer to its G row, its scale and the
+// float4 count of the row (padded sources take the dim of the key's table).
+__device__ __forceinline__ const float* grad_src(const SegArgs& a, uint32_t val, uint32_t key, float& scale,
+                                                 int& d4, uint32_t& lkey, int& ld4) {
+  if (val & kPadBit) {
+    scale = 1.0f;
+    if (key != lkey) {
+      lkey = key;
+      ld4 = a.tables[table_of_key(a.table_base, a.n_tables, key)].dim4;
+    }
+    d4 = ld4;
+    return a.grad_seq + (int64_t)(val & ~kPadBit) * 4;
+  }
+  const uint32_t c = div_magic32(val, a.bdiv);
+  const uint32_t b = val - c * (uint32_t)a.batch;
+  const int4 cg = __ldg(a.colg + c);
+  scale = cg.y ? __ldg(a.inv_n + val) : 1.0f;
+  d4 = cg.z;
+  return a.grad_out + (int64_t)b * a.ldg + cg.x;
+}
+
+template <int V>
+__global__ void __launch_bounds__(kSegThreads) k_segreduce(const SegArgs a) {
+  constexpr int U = kSegU / V;
+  __shared__ SegSmem sm;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int glog = a.glog;
+  const int G = 32 >> glog;
+  const int grp = lane >> glog, sub = lane & ((1 << glog) - 1);
+  const int q = warp * G + grp;
+  const int NG = kSegWarps * G;
+  const int64_t B0 = (int64_t)blockIdx.x * NG * kUnit;
+  const int64_t B1 = min(B0 + (int64_t)NG * kUnit, a.n);
+  const int64_t k0 = min(B0 + (int64_t)q * kUnit, B1), k1 = min(k0 + kUnit, B1);
+  const int D4 = a.maxdim4;
+
+  float4 acc[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) acc[v] = seg_f4zero();
+  uint32_t cur = k0 < k1 ? __ldg(a.keys + k0) : a.sentinel;
+  bool head = k0 < k1 && k0 > 0 && __ldg(a.keys + k0 - 1) == cur;
+  int64_t run_start = k0;
+  if (sub == 0) {
+    sm.tail_start[q] = -1;
+    sm.head_end[q] = -1;
+    sm.head_thru[q] = 0;
+  }
+  __syncwarp();
+
+  auto flush = [&](int64_t end, bool tail) {
+    if (cur == a.sentinel) return;
+    if (!head && !tail) {
+      finish_row<V>(a, cur, run_start, end, acc, sub);
+      return;
+    }
+    const int side = head ? 0 : 1;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int f4 = sub + v * 32;
+      if (f4 < D4) sm.part[side][q * D4 + f4] = acc[v];
+    }
+    if (sub == 0) {
+      if (head) {
+        sm.head_end[q] = (int32_t)(end - B0);
+        sm.head_thru[q] = tail ? 1 : 0;
+      } else {
+        sm.tail_start[q] = (int32_t)(run_start - B0);
+      }
+    }
+  };
+
+  uint32_t lkey = a.sentinel;
+  int ld4 = 0;
+  for (int64_t j = k0; j < k1; j += U) {
+    float4 gv[U][V];
+    uint32_t kk[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t k = j + u;
+      const bool in = k < k1;
+      kk[u] = in ? __ldg(a.keys + k) : a.sentinel;
+      float scale = 1.0f;
+      int d4 = 0;
+      const float* src = nullptr;
+      if (in && kk[u] != a.sentinel) src = grad_src(a, __ldg(a.vals + k), kk[u], scale, d4, lkey, ld4);
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int f4 = sub + v * 32;
+        float4 x = seg_f4zero();
+        if (src && f4 < d4) {
+          x = __ldg(reinterpret_cast<const float4*>(src + f4 * 4));
+          if (scale != 1.0f) {
+            x.x *= scale;
+            x.y *= scale;
+            x.z *= scale;
+            x.w *= scale;
+          }
+        }
+        gv[u][v] = x;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t k = j + u;
+      if (k >= k1) break;
+      if (kk[u] != cur) {
+        flush(k, false);
+        cur = kk[u];
+        head = false;
+        run_start = k;
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[v] = seg_f4zero();
+      }
+#pragma unroll
+      for (int v = 0; v < V; ++v) seg_f4add(acc[v], gv[u][v]);
+    }
+  }
+  if (k0 < k1) flush(k1, k1 < a.n && __ldg(a.keys + k1) == cur);
+  __syncthreads();
+
+  // runs cut inside the CTA: the group holding the run's start adds the head
+  // partials of the following groups in order
+  const int ts = sm.tail_start[q];
+  int32_t* P = a.part_pos + (int64_t)blockIdx.x * 2;
+  float4* GP = a.partial + (int64_t)blockIdx.x * 2 * D4;
+  if (ts >= 0) {
+    float4 s[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int f4 = sub + v * 32;
+      s[v] = f4 < D4 ? sm.part[1][q * D4 + f4] : seg_f4zero();
+    }
+    int q2 = q + 1;
+    bool thru = true;
+    int64_t end = B1;
+    while (q2 < NG && thru) {
+      if (sm.head_end[q2] < 0) break;   // empty group (past the end of the data)
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int f4 = sub + v * 32;
+        if (f4 < D4) seg_f4add(s[v], sm.part[0][q2 * D4 + f4]);
+      }
+      thru = sm.head_thru[q2];
+      end = B0 + sm.head_end[q2];
+      ++q2;
+    }
+    const uint32_t key = __ldg(a.keys + B0 + ts);
+    if (q2 == NG && thru) {
+      // the run continues into the next CTA: leave a tail partial
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int f4 = sub + v * 32;
+        if (f4 < D4) GP[D4 + f4] = s[v];
+      }
+      if (sub == 0) P[1] = (int32_t)ts;
+    } else {
+      finish_row<V>(a, key, B0 + ts, end, s, sub);
+    }
+  }
+  // the run cut at the CTA start: group 0 sums the head partials it spans
+  if (q == 0) {
+    bool thru = false;
+    int64_t end = B0;
+    float4 s[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) s[v] = seg_f4zero();
+    if (sm.head_end[0] >= 0) {
+      int q2 = 0;
+      thru = true;
+      while (q2 < NG && thru) {
+        if (sm.head_end[q2] < 0) { thru = false; break; }
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+          const int f4 = sub + v * 32;
+          if (f4 < D4) seg_f4add(s[v], sm.part[0][q2 * D4 + f4]);
+        }
+        thru = sm.head_thru[q2];
+        end = B0 + sm.head_end[q2];
+        ++q2;
+      }
+      if (q2 < NG) thru = false;
+    }
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int f4 = sub + v * 32;
+      if (f4 < D4) GP[f4] = s[v];
+    }
+    if (sub == 0) {
+      P[0] = (int32_t)(end - B0);
+      a.part_thru[blockIdx.x] = thru ? 1 : 0;
+    }
+  }
+}
+
+// Runs cut by CTA boundaries: one lane group per boundary b (between CTA b-1
+// and CTA b) that is the first boundary inside its run.
+template <int V>
+__global__ void __launch_bounds__(kSegThreads) k_seg_fixup(const SegArgs a, int n_blocks, int64_t span) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int glog = a.glog;
+  const int G = 32 >> glog;
+  const int grp = lane >> glog, sub = lane & ((1 << glog) - 1);
+  const int64_t b = 1 + (int64_t)blockIdx.x * kSegWarps * G + warp * G + grp;
+  if (b >= n_blocks) return;
+  const int64_t pos = b * span;
+  if (pos >= a.n) return;
+  const uint32_t key = __ldg(a.keys + pos);
+  if (key == a.sentinel || __ldg(a.keys + pos - 1) != key) return;
+  if (b > 1 && __ldg(a.keys + (b - 1) * span - 1) == key) return;  // an earlier boundary owns it
+  const int D4 = a.maxdim4;
+  float4 s[V];
+  const float4* T = a.partial + (b - 1) * 2 * D4 + D4;
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    const int f4 = sub + v * 32;
+    s[v] = f4 < D4 ? T[f4] : seg_f4zero();
+  }
+  const int64_t start = (b - 1) * span + a.part_pos[(b - 1) * 2 + 1];
+  int64_t c = b, end = pos;
+  for (;;) {
+    const float4* H = a.partial + c * 2 * D4;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const int f4 = sub + v * 32;
+      if (f4 < D4) seg_f4add(s[v], H[f4]);
+    }
+    end = c * span + a.part_pos[c * 2];
+    if (!a.part_thru[c] || c + 1 >= n_blocks) break;
+    ++c;
+  }
+  finish_row<V>(a, key, start, end, s, sub);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+emb_status launch_backward(emb_plan_s* p, const float* grad_out, const float* grad_seq, float lr, float eps,
+                           cudaStream_t stream, const emb_backward_debug* dbg) {
+  Workspace& w = p->ws;
+  const int64_t n = p->last_n;
+  const bool want_dbg = dbg && (dbg->uniq_table || dbg->uniq_row || dbg->counts || dbg->agg_grad || dbg->n_unique);
+  if (n == 0) {
+    if (want_dbg && dbg->n_unique) EMB_CUDA_TRY(cudaMemsetAsync(dbg->n_unique, 0, sizeof(int64_t), stream));
+    return EMB_OK;
+  }
+  const int passes = (p->key_bits + kRadixBits - 1) / kRadixBits;
+  const int64_t tiles = (n + kSortTile - 1) / kSortTile;
+  const size_t sort_words = 4 * kRadix + 4 + (size_t)passes * tiles * kRadix;
+  EMB_CUDA_TRY(cudaMemsetAsync(w.hist, 0, sort_words * sizeof(uint32_t), stream));
+  {
+    const int grid = (int)std::min<int64_t>((n + 511) / 512, (int64_t)p->sm_count * 4);
+    k_digit_hist<<<grid, 512, 0, stream>>>(w.keys[0], n, passes, w.hist);
+  }
+  static bool attr_set = false;
+  if (!attr_set) {
+    EMB_CUDA_TRY(cudaFuncSetAttribute(k_onesweep, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)sizeof(SortSmem)));
+    attr_set = true;
+  }
+  for (int ps = 0; ps < passes; ++ps) {
+    const int in = ps & 1, out = in ^ 1;
+    k_onesweep<<<(unsigned)tiles, kSortThreads, sizeof(SortSmem), stream>>>(
+        w.keys[in], w.vals[in], w.keys[out], w.vals[out], n, ps * kRadixBits, w.hist + ps * kRadix,
+        w.lookback + (size_t)ps * tiles * kRadix, w.tile_ctr + ps, p->status_d);
+  }
+  EMB_CUDA_TRY(cudaGetLastError());
+  const uint32_t* skeys = w.keys[passes & 1];
+  const uint32_t* svals = w.vals[passes & 1];
+
+  SegArgs a{};
+  a.keys = skeys;
+  a.vals = svals;
+  a.n = n;
+  a.sentinel = p->key_total;
+  a.colg = p->colg_d;
+  a.inv_n = w.inv_n;
+  a.grad_out = grad_out;
+  a.ldg = p->out_width;
+  a.grad_seq = grad_seq;
+  a.batch = p->last_batch > 0 ? p->last_batch : 1;
+  a.bdiv = make_div_magic32((uint32_t)a.batch);
+  a.tables = p->tables_d;
+  a.table_base = p->table_base_d;
+  a.n_tables = p->n_tables;
+  a.lr = lr;
+  a.eps = eps;
+  a.maxdim4 = p->max_dim / 4;
+  int g = a.maxdim4 > 32 ? 32 : a.maxdim4, glog = 0;
+  while ((1 << glog) < g) ++glog;
+  a.glog = glog;
+  const int NG = kSegWarps * (32 >> glog);
+  const int64_t span = (int64_t)NG * kUnit;
+  const int64_t n_blocks = (n + span - 1) / span;
+  if (n_blocks > w.n_units_max) return EMB_ERR_UNSUPPORTED;
+  a.partial = w.partial;
+  a.part_pos = w.part_pos;
+  a.part_thru = w.part_thru;
+  if (want_dbg) {
+    const int nb = (int)((n + kScanBlock - 1) / kScanBlock);
+    k_rank_reduce<<<nb, kScanBlock, 0, stream>>>(skeys, n, p->key_total, w.scan_part);
+    k_rank_top<<<1, kScanBlock, 0, stream>>>(w.scan_part, nb, dbg->n_unique);
+    k_rank_down<<<nb, kScanBlock, 0, stream>>>(skeys, n, p->key_total, w.scan_part, w.run_head);
+    a.rank = w.run_head;
+    a.dbg_table = dbg->uniq_table;
+    a.dbg_row = dbg->uniq_row;
+    a.dbg_count = dbg->counts;
+    a.dbg_grad = dbg->agg_grad;
+    a.dbg_ld = p->max_dim;
+  }
+  const unsigned fix_grid = (unsigned)std::max<int64_t>(1, (n_blocks - 1 + NG - 1) / NG);
+  if (a.maxdim4 > 32) {
+    k_segreduce<2><<<(unsigned)n_blocks, kSegThreads, 0, stream>>>(a);
+    if (n_blocks > 1) k_seg_fixup<2><<<fix_grid, kSegThreads, 0, stream>>>(a, (int)n_blocks, span);
+  } else {
+    k_segreduce<1><<<(unsigned)n_blocks, kSegThreads, 0, stream>>>(a);
+    if (n_blocks > 1) k_seg_fixup<1><<<fix_grid, kSegThreads, 0, stream>>>(a, (int)n_blocks, span);
+  }
+  return cuda_status(cudaGetLastError());
 }
 
 }  // namespace emb

@@ -15,6 +15,7 @@ void free_plan(emb_plan_s* p) {
   if (!p) return;
   cudaFree(p->meta_d);
   cudaFree(p->stream_cols_d);
+  cudaFree(p->colg_d);
   cudaFree(p->tables_d);
   cudaFree(p->table_base_d);
   cudaFree(p->status_d);
@@ -29,6 +30,8 @@ void free_plan(emb_plan_s* p) {
   cudaFree(w.n_runs);
   cudaFree(w.scan_part);
   cudaFree(w.partial);
+  cudaFree(w.part_pos);
+  cudaFree(w.part_thru);
   delete p;
 }
 
@@ -176,6 +179,7 @@ extern "C" emb_status emb_plan_create(const emb_column_desc* cols, int32_t n_col
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess) e = dmalloc(&p->meta_d, n_cols, &total);
   if (e == cudaSuccess) e = dmalloc(&p->stream_cols_d, sc.size(), &total);
+  if (e == cudaSuccess) e = dmalloc(&p->colg_d, n_cols, &total);
   if (e == cudaSuccess) e = dmalloc(&p->tables_d, p->tables_h.size(), &total);
   if (e == cudaSuccess) e = dmalloc(&p->table_base_d, p->table_base_h.size(), &total);
   if (e == cudaSuccess) e = dmalloc(&p->status_d, 1, &total);
@@ -188,6 +192,12 @@ extern "C" emb_status emb_plan_create(const emb_column_desc* cols, int32_t n_col
     e = cudaMemcpy(p->table_base_d, p->table_base_h.data(), sizeof(uint32_t) * p->table_base_h.size(),
                    cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(p->status_d, 0, sizeof(uint32_t));
+  if (e == cudaSuccess) {
+    std::vector<int4> cg(n_cols);
+    for (int32_t c = 0; c < n_cols; ++c)
+      cg[c] = make_int4(p->meta_h[c].out_col, cols[c].pooling == EMB_POOL_MEAN ? 1 : 0, cols[c].dim / 4, 0);
+    e = cudaMemcpy(p->colg_d, cg.data(), sizeof(int4) * n_cols, cudaMemcpyHostToDevice);
+  }
 
   if (e == cudaSuccess && training) {
     Workspace& w = p->ws;
@@ -211,6 +221,8 @@ extern "C" emb_status emb_plan_create(const emb_column_desc* cols, int32_t n_col
     if (e == cudaSuccess) e = dmalloc(&w.n_runs, 4, &total);
     if (e == cudaSuccess) e = dmalloc(&w.scan_part, (n + 1023) / 1024 + 64, &total);
     if (e == cudaSuccess) e = dmalloc(&w.partial, (size_t)w.n_units_max * 2 * (p->max_dim / 4), &total);
+    if (e == cudaSuccess) e = dmalloc(&w.part_pos, (size_t)w.n_units_max * 2, &total);
+    if (e == cudaSuccess) e = dmalloc(&w.part_thru, (size_t)w.n_units_max, &total);
   }
   p->ws.bytes = total;
   if (e == cudaSuccess) p->fwd_ctas_per_sm = forward_ctas_per_sm();

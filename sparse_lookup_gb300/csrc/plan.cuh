@@ -41,6 +41,8 @@ struct Workspace {
   uint32_t* n_runs = nullptr;      // [1]
   uint32_t* scan_part = nullptr;   // per-block partial counts for run compaction
   float4* partial = nullptr;       // [n_units][2][max_dim/4] cut-run partial sums
+  int32_t* part_pos = nullptr;     // [n_units][2] run boundaries of those partials
+  uint8_t* part_thru = nullptr;    // [n_units] CTA lies inside one continuing run
   int64_t max_tiles = 0;
   int64_t n_units_max = 0;
   size_t bytes = 0;
@@ -61,6 +63,7 @@ struct emb_plan_s {
   std::vector<uint32_t> table_base_h;  // [n_tables + 1]
   emb::ColMeta* meta_d = nullptr;
   int32_t* stream_cols_d = nullptr;    // id-stream columns, then f-stream columns
+  int4* colg_d = nullptr;              // per column: (out_col, 1 if MEAN, dim/4) for the backward
   emb::TableMeta* tables_d = nullptr;
   uint32_t* table_base_d = nullptr;
   int32_t n_stream_cols[2] = {0, 0};

@@ -109,3 +109,142 @@ def oracle_sampled_forward(w, tables_dev, bags):
         out, seq = oracle.forward([spec], 1, [np.array([0, ids.size], np.int32)], [ids], [sub])
         res[(c, b)] = seq[0][0] if col.pooling == "padded" else out[0]
     return res
+
+
+U32 = 2.0 ** -24
+
+
+def gamma(k):
+    """Higham's gamma_k = k u / (1 - k u) for fp32 (u = 2^-24): any order of
+    summing k terms errs by at most gamma_{k-1} * sum|terms|."""
+    ku = np.asarray(k, np.float64) * U32
+    return ku / (1.0 - ku)
+
+
+class TrainStep:
+    """One forward + backward/Adagrad step of a workload on the device through
+    the C ABI, and the oracle's result for the same inputs."""
+
+    def __init__(self, w, acc_init=0.0, grad_seed=77, device="cuda"):
+        import torch
+        import sparse_lookup_gb300 as sl
+        self.w = w
+        m = Materialized(w, device, with_acc=True, acc_init=acc_init)
+        self.m = m
+        self.W0 = m.host_tables()
+        self.A0 = [None if a is None else a.cpu().numpy() for a in m.accs]
+        n = m.n_ids + m.n_f
+        self.plan = sl.Plan(w.columns, m.tables, m.accs, max_batch=max(w.B, 1), max_ids=max(n, 1), training=True)
+        self.out, self.seq = self.plan.forward(w.B, m.ids, m.id_off, m.fv, m.f_off)
+        width = self.plan.out_width
+        self.G = synth.make_grad((w.B, max(width, 1)), grad_seed, device)[:, :width].contiguous()
+        self.Gseq = None
+        if self.plan.seq_per_bag:
+            self.Gseq = synth.make_grad((w.B * self.plan.seq_per_bag,), grad_seed + 1, device)
+        self.dbg = self.plan.backward_update(self.G if width else None, self.Gseq, w.lr, w.eps, debug=True)
+        torch.cuda.synchronize()
+        self.status = self.plan.device_status()
+        self.info = self.plan.info
+
+    def oracle(self):
+        w = self.w
+        G = self.G.cpu().numpy()
+        gseq = None
+        if self.Gseq is not None:
+            s = self.Gseq.cpu().numpy()
+            sl_, _ = seq_slices(w.columns, w.B)
+            gseq = [None if sp is None else s[sp[0]:sp[0] + int(np.prod(sp[1]))].reshape(sp[1]) for sp in sl_]
+        Wr = [None if t is None else t.copy() for t in self.W0]
+        Ar = [None if t is None else t.copy() for t in self.A0]
+        nt = len(Wr)
+        dummy = np.zeros((1, 1), np.float32)
+        Wl = [Wr[i] if Wr[i] is not None else dummy for i in range(nt)]
+        Al = [Ar[i] if Ar[i] is not None else dummy for i in range(nt)]
+        ref = oracle.backward_adagrad(w.columns, w.B, w.offsets, w.values, G, gseq, Wl, Al, w.lr, w.eps)
+        # magnitudes for the summation-error bound: the same aggregation of |G|
+        Wd = [np.zeros_like(x) for x in Wl]
+        Ad = [np.zeros_like(x) for x in Al]
+        absg = oracle.backward_adagrad(w.columns, w.B, w.offsets, w.values, np.abs(G),
+                                       None if gseq is None else [None if g is None else np.abs(g) for g in gseq],
+                                       Wd, Ad, w.lr, w.eps)
+        return ref, absg, Wl, Al
+
+    def gpu_table_to_spec(self):
+        """GPU table index (first appearance of a weight pointer) -> spec table id."""
+        out = {}
+        for c, t in zip(self.w.columns, self.info["col_table"]):
+            out.setdefault(t, c.table)
+        return out
+
+
+def check_train_step(ts, max_ambiguous_frac=1e-5):
+    """Bit-exact unique rows and counts; aggregated gradient within the fp32
+    summation bound; weights within 1e-5 rel / 1e-6 abs except elements that
+    fp32 summation leaves ill-conditioned (the first Adagrad step from acc = 0
+    has dW/dg = lr eps / g^2, and a sign fp32 does not determine flips the
+    step); accumulators within the bound the gradient error implies.  Returns
+    the number of elements outside the tolerance (all ill-conditioned), which
+    must stay below max(16, 1e-5 of the updated elements): one cancelling
+    pair of bags repeats its element in every row the two bags share."""
+    assert ts.status == 0, "device status %d" % ts.status
+    ref, absg, Wr, Ar = ts.oracle()
+    n = len(ref["row"])
+    d = ts.dbg
+    assert int(d["row"].numel()) == n, (int(d["row"].numel()), n)
+    t2s = ts.gpu_table_to_spec()
+    gt = np.array([t2s[int(t)] for t in d["table"].cpu().numpy()], np.int64)
+    assert np.array_equal(gt, ref["table"]), "unique tables"
+    assert np.array_equal(d["row"].cpu().numpy(), ref["row"]), "unique rows"
+    assert np.array_equal(d["count"].cpu().numpy().astype(np.int64), ref["count"]), "counts"
+    g = d["grad"].cpu().numpy()
+    excluded, total = 0, 0
+    dims = {c.table: c.dim for c in ts.w.columns}
+    bound_of = {}
+    for i in range(n):
+        dim = dims[int(ref["table"][i])]
+        gr = ref["grad"][i].astype(np.float64)
+        k = int(ref["count"][i]) + 1
+        bnd = gamma(k) * absg["grad"][i].astype(np.float64) + 1e-30
+        # probabilistic bound (Higham & Mary, 2019): lambda sqrt(k) u sum|x|,
+        # used only to decide which weights fp32 leaves ill-conditioned
+        pbnd = np.minimum(bnd, 8.0 * np.sqrt(k) * U32 * absg["grad"][i].astype(np.float64)) + 1e-30
+        bound_of[(int(ref["table"][i]), int(ref["row"][i]))] = (gr, pbnd)
+        err = np.abs(g[i, :dim].astype(np.float64) - gr)
+        ok = (err <= ATOL + RTOL * np.abs(gr)) | (err <= bnd)
+        assert ok.all(), "aggregated gradient of row %s: err %s bound %s" % (
+            (int(ref["table"][i]), int(ref["row"][i])), err[~ok][:4], bnd[~ok][:4])
+    # weights and accumulators
+    for t_gpu, t_spec in t2s.items():
+        Wg = ts.m.tables[t_spec].cpu().numpy()
+        Ag = ts.m.accs[t_spec].cpu().numpy()
+        W0 = ts.W0[t_spec]
+        touched = np.zeros(W0.shape[0], bool)
+        sel = ref["table"] == t_spec
+        touched[ref["row"][sel]] = True
+        assert np.array_equal(Wg[~touched], W0[~touched]), "untouched rows changed"
+        assert np.array_equal(Ag[~touched], ts.A0[t_spec][~touched]), "untouched accumulators changed"
+        lr, eps = ts.w.lr, ts.w.eps
+        for r in ref["row"][sel]:
+            gr, bnd = bound_of[(t_spec, int(r))]
+            # ill-conditioned: the weight range that gradients within the
+            # summation bound produce is wider than the tolerance (includes a
+            # sign that fp32 does not determine)
+            a0 = ts.A0[t_spec][r].astype(np.float64)
+            w0 = W0[r].astype(np.float64)
+            step = lambda gg: w0 - lr * gg / (np.sqrt(a0 + gg * gg) + eps)
+            spread = np.abs(step(gr + bnd) - step(gr - bnd))
+            amb = spread > ATOL + RTOL * np.abs(step(gr))
+            total += gr.size
+            wr = Wr[t_spec][r].astype(np.float64)
+            err = np.abs(Wg[r].astype(np.float64) - wr)
+            within = err <= ATOL + RTOL * np.abs(wr)
+            excluded += int((amb & ~within).sum())
+            okw = within | amb
+            assert okw.all(), "weights of row %d: %s vs %s" % (r, Wg[r][~okw][:4], wr[~okw][:4])
+            ar = Ar[t_spec][r].astype(np.float64)
+            abound = 2 * np.abs(gr) * bnd + bnd * bnd + 4 * U32 * np.abs(ar)
+            erra = np.abs(Ag[r].astype(np.float64) - ar)
+            oka = (erra <= ATOL + RTOL * np.abs(ar)) | (erra <= abound) | amb
+            assert oka.all(), "accumulator of row %d: %s vs %s" % (r, Ag[r][~oka][:4], ar[~oka][:4])
+    assert excluded <= max(16, max_ambiguous_frac * total), (excluded, total)
+    return excluded

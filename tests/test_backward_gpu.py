@@ -1,0 +1,102 @@
+"""GPU parity of the backward (radix sort, unique rows and counts, segmented
+gradient reduction) and the fused sparse Adagrad update, through the C ABI."""
+import numpy as np
+import pytest
+
+import sparse_lookup_gb300 as sl
+from sparse_lookup_gb300 import build as slbuild
+from sparse_lookup_gb300 import synth
+from sparse_lookup_gb300.synth import ColumnSpec, TableSpec, Workload
+
+from helpers import TrainStep, check_train_step
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    slbuild.build()
+    sl.lib()
+
+
+def test_tiny_training_step():
+    check_train_step(TrainStep(synth.tiny()))
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_random_small_plans(seed):
+    check_train_step(TrainStep(synth.random_small(100 + seed)))
+
+
+def test_well_conditioned_accumulator_start():
+    """acc0 = 0.1: no first-step sign sensitivity, nothing excluded."""
+    assert check_train_step(TrainStep(synth.random_small(7), acc_init=0.1)) == 0
+
+
+def test_hot_row_spans_many_ctas():
+    """One row receives 300k contributions (runs cut by many CTA boundaries),
+    next to a uniform spread."""
+    rng = np.random.default_rng(4)
+    B = 3000
+    lens = rng.integers(50, 150, B)
+    n = int(lens.sum())
+    ids = rng.integers(0, 5000, n).astype(np.int64)
+    ids[rng.random(n) < 0.9] = 1234
+    for dim in (8, 64, 200):
+        cols = [ColumnSpec("identity", "sum", 5000, dim, 0), ColumnSpec("identity", "mean", 5000, dim, 1)]
+        w = Workload("hot", B, cols, [TableSpec(5000, dim, 3), TableSpec(5000, dim, 4)],
+                     [synth.bag_offsets(lens)] * 2, [ids, ids], lr=0.01)
+        check_train_step(TrainStep(w))
+
+
+def test_padded_and_mean_sequences_small():
+    w = synth.sequences(seed=5, mode="padded", C=3, B=40, rows=3000, dim=128, len_lo=50, len_hi=300,
+                        pad_len=200)
+    check_train_step(TrainStep(w))
+    w = synth.sequences(seed=6, mode="mean", C=3, B=40, rows=3000, dim=128, len_lo=50, len_hi=300)
+    check_train_step(TrainStep(w))
+
+
+def test_shared_table_columns_merge():
+    rng = np.random.default_rng(9)
+    B = 500
+    cols = [ColumnSpec("rows_given", "sum", 2000, 32, 0) for _ in range(6)]
+    offs, vals = [], []
+    for c in range(6):
+        lens = rng.integers(0, 6, B)
+        offs.append(synth.bag_offsets(lens))
+        v = rng.integers(-1, 2000, int(lens.sum())).astype(np.int64)
+        vals.append(v)
+    w = Workload("shared", B, cols, [TableSpec(2000, 32, 1)], offs, vals, lr=0.01)
+    check_train_step(TrainStep(w))
+
+
+def test_deterministic_updates():
+    a = TrainStep(synth.random_small(21))
+    b = TrainStep(synth.random_small(21))
+    for t in range(len(a.m.tables)):
+        if a.m.tables[t] is None:
+            continue
+        assert np.array_equal(a.m.tables[t].cpu().numpy(), b.m.tables[t].cpu().numpy())
+        assert np.array_equal(a.m.accs[t].cpu().numpy(), b.m.accs[t].cpu().numpy())
+
+
+def test_backward_without_forward_is_rejected():
+    import torch
+    w = synth.tiny()
+    from helpers import Materialized
+    m = Materialized(w, "cuda", with_acc=True)
+    plan = sl.Plan(w.columns, m.tables, m.accs, max_batch=w.B, max_ids=m.n_ids, training=True)
+    g = torch.zeros((w.B, plan.out_width), device="cuda")
+    with pytest.raises(sl.EmbError) as e:
+        plan.backward_update(g, None, 0.01, 1e-10)
+    assert e.value.status == 1
+
+
+def test_empty_batch_backward():
+    import torch
+    w = Workload("empty", 5, [ColumnSpec("identity", "sum", 10, 8, 0)], [TableSpec(10, 8, 1)],
+                 [np.zeros(6, np.int32)], [np.zeros(0, np.int64)])
+    ts = TrainStep(w)
+    assert ts.status == 0
+    assert int(ts.dbg["row"].numel()) == 0
