@@ -271,6 +271,37 @@ emb_status hash_get_device_status(emb_hash h, void* stream);
 /* Frees the table and its row pool (synchronizes the device first). */
 emb_status hash_destroy(emb_hash h);
 
+/* emb_sparse_adagrad_noalloc -- one sparse Adagrad step on one table, with
+ * duplicate rows merged, that allocates no memory.  The pages have no
+ * counterpart to this call: it exists for callers that cannot call
+ * cudaMalloc -- a host framework that owns all device memory through its own
+ * pool (a raw allocation would bypass its accounting or fail against its
+ * reservation), a serving process that forbids allocation after start-up to
+ * keep latency bounded, or a plugin that is only ever handed pointers.  Such
+ * callers cannot create a plan, whose workspace is allocated at creation.
+ *
+ * rows[i] (int64, [n]) names the row that gradient grads[i, :] (fp32 [n, dim],
+ * row-major, 16-byte aligned) belongs to; rows outside [0, num_rows) are
+ * ignored.  The gradients of equal rows are summed (same sort, run reduction
+ * and fp32 Adagrad as emb_backward_update), then every touched row of weight
+ * and acc ([num_rows, dim] fp32, 16-byte aligned) takes one step
+ *   acc += g*g;  w -= lr * g / (sqrt(acc) + eps).
+ *
+ * Scratch: a fixed area of about 4.7 MB compiled into the library as a
+ * file-scope device array; every GPU that loads the library holds it until
+ * the process exits.  Limits: n <= 262144 (2^18), dim <= 256, num_rows <
+ * 2^31; larger sizes return EMB_ERR_UNSUPPORTED before any work is queued.
+ * The first call on a device looks up the area's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls on a device share the one area, which keeps the last
+ * call's contents (each call clears what must start at zero): calls whose
+ * work overlaps on the GPU -- on different streams, or from different host
+ * threads -- race and corrupt each other's results; serialize them.
+ * Calls no cudaMalloc, cudaFree or allocating library routine. */
+emb_status emb_sparse_adagrad_noalloc(const int64_t* rows, int64_t n, const float* grads, float* weight,
+                                      float* acc, int64_t num_rows, int32_t dim, float lr, float eps,
+                                      void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Host-side self tests of arithmetic shared by host and device code         */
 /* ------------------------------------------------------------------------ */

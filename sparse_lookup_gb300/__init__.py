@@ -83,6 +83,8 @@ _SIGS = {
                               POINTER(c_int64), c_void_p]),
     "hash_get_device_status": (c_int32, [c_void_p, c_void_p]),
     "hash_destroy": (c_int32, [c_void_p]),
+    "emb_sparse_adagrad_noalloc": (c_int32, [c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_int64, c_int32,
+                                             c_float, c_float, c_void_p]),
     "emb_selftest_hash_mod": (c_int32, [c_void_p, c_int64, c_int64, c_void_p]),
     "emb_version": (c_char_p, []),
 }
@@ -208,6 +210,13 @@ def hash_get_device_status(h, stream=None):
 
 def hash_destroy(h):
     _check(lib().hash_destroy(h), "hash_destroy")
+
+
+def emb_sparse_adagrad_noalloc(rows, n, grads, weight, acc, num_rows, dim, lr, eps, stream=None):
+    """One sparse Adagrad step on one table with no allocation (fixed scratch
+    inside the library; n <= 2^18, dim <= 256)."""
+    _check(lib().emb_sparse_adagrad_noalloc(ptr(rows), n, ptr(grads), ptr(weight), ptr(acc), num_rows, dim, lr,
+                                            eps, _stream(stream)), "emb_sparse_adagrad_noalloc")
 
 
 def emb_selftest_hash_mod(ids, num_rows):

@@ -673,3 +673,160 @@ emb_status launch_backward(emb_plan_s* p, const float* grad_out, const float* gr
 }
 
 }  // namespace emb
+
+// ===========================================================================
+// emb_sparse_adagrad_noalloc: the sort + run reduction + Adagrad update above,
+// for one table, on a fixed scratch area compiled into the library instead of
+// memory from cudaMalloc.
+// ===========================================================================
+namespace emb {
+namespace {
+
+constexpr int64_t kNoAllocMaxN = int64_t(1) << 18;   // contributions per call
+constexpr int kNoAllocMaxDim = 256;
+constexpr int64_t kNoAllocTiles = (kNoAllocMaxN + kSortTile - 1) / kSortTile;
+constexpr int64_t kNoAllocBlocks = (kNoAllocMaxN + kSegWarps * kUnit - 1) / (kSegWarps * kUnit);
+constexpr size_t kNoAllocSortWords = 4 * kRadix + 4 + 4 * kNoAllocTiles * kRadix;
+
+struct NoAllocScratch {
+  uint32_t keys[2][kNoAllocMaxN];
+  uint32_t vals[2][kNoAllocMaxN];
+  uint32_t sortw[kNoAllocSortWords];   // histograms, tile tickets, look-back words
+  float4 partial[kNoAllocBlocks * 2 * (kNoAllocMaxDim / 4)];
+  int32_t part_pos[kNoAllocBlocks * 2];
+  uint8_t part_thru[kNoAllocBlocks];
+  TableMeta table;
+  uint32_t table_base[2];
+  int4 colg;
+};
+
+}  // namespace
+
+// The scratch area: every GPU that loads the library holds one copy until the
+// process exits; all calls on a device share it.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[sizeof(NoAllocScratch)];
+
+__global__ void k_noalloc_setup(NoAllocScratch* s, float* weight, float* acc, int64_t num_rows, int32_t dim) {
+  if (threadIdx.x == 0) {
+    s->table.weight = weight;
+    s->table.acc = acc;
+    s->table.num_rows = num_rows;
+    s->table.dim = dim;
+    s->table.dim4 = dim / 4;
+    s->table_base[0] = 0u;
+    s->table_base[1] = (uint32_t)num_rows;
+    s->colg = make_int4(0, 0, dim / 4, 0);
+  }
+}
+
+// (row, contribution index) pairs; a row outside [0, num_rows) is dropped by
+// giving it the sentinel key num_rows, which sorts after every valid row.
+__global__ void k_noalloc_pairs(const int64_t* __restrict__ rows, int64_t n, int64_t num_rows,
+                                uint32_t* __restrict__ keys, uint32_t* __restrict__ vals) {
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i < n) {
+    const int64_t r = rows[i];
+    keys[i] = (r >= 0 && r < num_rows) ? (uint32_t)r : (uint32_t)num_rows;
+    vals[i] = (uint32_t)i;
+  }
+}
+
+namespace {
+constexpr int kNoAllocMaxDevices = 64;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch area on the current device, looked up once
+// per device (the first call on a device does this set-up).
+emb_status noalloc_scratch(NoAllocScratch** out) {
+  int dev = 0;
+  EMB_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return EMB_ERR_UNSUPPORTED;
+  if (!g_noalloc_addr[dev]) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr) {
+      cudaGetLastError();
+      return EMB_ERR_CUDA;
+    }
+    g_noalloc_addr[dev] = ptr;
+  }
+  *out = static_cast<NoAllocScratch*>(g_noalloc_addr[dev]);
+  return EMB_OK;
+}
+}  // namespace
+
+}  // namespace emb
+
+extern "C" emb_status emb_sparse_adagrad_noalloc(const int64_t* rows, int64_t n, const float* grads,
+                                                 float* weight, float* acc, int64_t num_rows, int32_t dim,
+                                                 float lr, float eps, void* stream_) {
+  using namespace emb;
+  if (n < 0 || num_rows < 1 || dim < 4 || dim % 4 != 0) return EMB_ERR_INVALID_ARG;
+  if (n > kNoAllocMaxN || dim > kNoAllocMaxDim || num_rows >= (int64_t(1) << 31)) return EMB_ERR_UNSUPPORTED;
+  if (!weight || !acc || !aligned16(weight) || !aligned16(acc)) return EMB_ERR_INVALID_ARG;
+  if (n > 0 && (!rows || !grads || !aligned16(grads))) return EMB_ERR_INVALID_ARG;
+  if (!(lr == lr) || !(eps == eps)) return EMB_ERR_INVALID_ARG;
+  NoAllocScratch* s = nullptr;
+  emb_status st = noalloc_scratch(&s);
+  if (st != EMB_OK) return st;
+  if (n == 0) return EMB_OK;
+  cudaStream_t stream = (cudaStream_t)stream_;
+
+  int key_bits = 1;
+  while (key_bits < 32 && (uint64_t(1) << key_bits) <= (uint64_t)num_rows) ++key_bits;
+  const int passes = (key_bits + kRadixBits - 1) / kRadixBits;
+  const int64_t tiles = (n + kSortTile - 1) / kSortTile;
+  uint32_t* hist = s->sortw;
+  uint32_t* tile_ctr = hist + 4 * kRadix;
+  uint32_t* lookback = tile_ctr + 4;
+  // the area keeps the previous call's contents: clear what must start at zero
+  EMB_CUDA_TRY(cudaMemsetAsync(hist, 0, (4 * kRadix + 4 + (size_t)passes * tiles * kRadix) * sizeof(uint32_t),
+                               stream));
+  k_noalloc_setup<<<1, 32, 0, stream>>>(s, weight, acc, num_rows, dim);
+  k_noalloc_pairs<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(rows, n, num_rows, s->keys[0], s->vals[0]);
+  k_digit_hist<<<(unsigned)std::min<int64_t>((n + 511) / 512, 256), 512, 0, stream>>>(s->keys[0], n, passes, hist);
+  EMB_CUDA_TRY(cudaFuncSetAttribute(k_onesweep, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)sizeof(SortSmem)));
+  for (int ps = 0; ps < passes; ++ps) {
+    const int in = ps & 1, out = in ^ 1;
+    k_onesweep<<<(unsigned)tiles, kSortThreads, sizeof(SortSmem), stream>>>(
+        s->keys[in], s->vals[in], s->keys[out], s->vals[out], n, ps * kRadixBits, hist + ps * kRadix,
+        lookback + (size_t)ps * tiles * kRadix, tile_ctr + ps, nullptr);
+  }
+  SegArgs a{};
+  a.keys = s->keys[passes & 1];
+  a.vals = s->vals[passes & 1];
+  a.n = n;
+  a.sentinel = (uint32_t)num_rows;
+  a.colg = &s->colg;
+  a.inv_n = nullptr;
+  a.grad_out = grads;
+  a.ldg = dim;
+  a.grad_seq = nullptr;
+  a.batch = (int32_t)n;
+  a.bdiv = make_div_magic32((uint32_t)n);
+  a.tables = &s->table;
+  a.table_base = s->table_base;
+  a.n_tables = 1;
+  a.lr = lr;
+  a.eps = eps;
+  a.maxdim4 = dim / 4;
+  int g = a.maxdim4 > 32 ? 32 : a.maxdim4, glog = 0;
+  while ((1 << glog) < g) ++glog;
+  a.glog = glog;
+  const int NG = kSegWarps * (32 >> glog);
+  const int64_t span = (int64_t)NG * kUnit;
+  const int64_t n_blocks = (n + span - 1) / span;
+  a.partial = s->partial;
+  a.part_pos = s->part_pos;
+  a.part_thru = s->part_thru;
+  const unsigned fix_grid = (unsigned)std::max<int64_t>(1, (n_blocks - 1 + NG - 1) / NG);
+  if (a.maxdim4 > 32) {
+    k_segreduce<2><<<(unsigned)n_blocks, kSegThreads, 0, stream>>>(a);
+    if (n_blocks > 1) k_seg_fixup<2><<<fix_grid, kSegThreads, 0, stream>>>(a, (int)n_blocks, span);
+  } else {
+    k_segreduce<1><<<(unsigned)n_blocks, kSegThreads, 0, stream>>>(a);
+    if (n_blocks > 1) k_seg_fixup<1><<<fix_grid, kSegThreads, 0, stream>>>(a, (int)n_blocks, span);
+  }
+  return cuda_status(cudaGetLastError());
+}
