@@ -46,15 +46,19 @@ def common_flags(extra=()):
                    "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr"] + list(extra)
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    if not force and not is_stale():
+def build(force: bool = False, verbose: bool = False, extra=(), out: str = None) -> str:
+    """Compile and link; `extra` adds nvcc flags, `out` writes the library
+    elsewhere (objects then go to a build folder of their own)."""
+    lib_path = out or LIB
+    build_dir = BUILD if out is None else lib_path + ".objs"
+    if out is None and not force and not is_stale():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         cmd = [cc] + common_flags(extra) + ["-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
@@ -68,13 +72,13 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
             objs.append(obj)
             if verbose and log:
                 print(log)
-    tmp = LIB + ".tmp.%d" % os.getpid()
+    tmp = lib_path + ".tmp.%d" % os.getpid()
     cmd = [cc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("nvcc link failed:\n%s\n%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

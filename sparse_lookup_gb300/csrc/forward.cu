@@ -3,24 +3,28 @@
 //
 // Work decomposition (element-count tiling, RecIS §3.1 "Thread mapping for
 // skewed inputs"): each of the two jagged value streams is cut into tiles of
-// E consecutive elements; a CTA owns every (column, bag) segment whose FIRST
-// element lies in its tile, so each pooled output row has exactly one writer
-// (RecIS §3.2 Algorithm 1, forward: no atomics).
+// E consecutive elements and every WARP owns one tile: the (column, bag)
+// segments whose FIRST element lies in the tile.  Each pooled output row
+// therefore has exactly one writer (RecIS §3.2 Algorithm 1, forward: no
+// atomics), and warps never wait on each other -- there is no CTA barrier,
+// so a warp stalled on memory never holds up another.
 //
-// A CTA walks its segments in chunks that stay inside one column (one table,
-// one dim, one transform) and hold at most kChunkBags bags and kChunkElems
-// values of short bags:
-//   A. every thread transforms values of the chunk (coalesced 8-byte loads,
-//      SplitMix64 + invariant-divisor modulo, or a binary search over the
-//      boundaries), applies the range guard and writes the row to shared
-//      memory -- one memory round trip for the whole chunk;
-//   B. the chunk's values are split into equal ranges, one per lane group of
-//      dim/4 lanes (so every group runs the same trip count); a group gathers
-//      its rows with 16-byte loads four deep and sums them per bag; a bag that
-//      spans ranges leaves head/tail partials in shared memory which the
-//      group holding its first value adds up in range order (deterministic);
-//   C. bags longer than kLongBag (or padded bags with pad_len > kLongBag) are
-//      pooled / copied by all eight warps together.
+// A warp walks its segments in chunks that stay inside one column (one table,
+// one dim, one transform) and hold at most 32 bags and kWarpElems values of
+// short bags:
+//   setup  one lane per bag loads the bag's CSR range; a warp scan places the
+//          bags' values back to back in shared memory;
+//   A.     lanes transform the chunk's values (coalesced 8-byte loads,
+//          SplitMix64 + invariant-divisor modulo, or a binary search over the
+//          boundaries), apply the range guard and park the rows in shared
+//          memory;
+//   B.     lane groups of dim/4 lanes take equal ranges of those values (the
+//          same trip count for every group), gather rows with 16-byte loads
+//          four deep and sum them per bag; a bag that spans ranges leaves
+//          head/tail partials which the group holding its first value adds up
+//          in range order (deterministic);
+//   C.     bags longer than kLongBag (padded: pad_len > kLongBag) are pooled /
+//          copied by the whole warp, 32 values per step.
 // Empty bags and bags whose values were all dropped get the default vector.
 #include <algorithm>
 
@@ -28,9 +32,9 @@
 
 namespace emb {
 
-constexpr int kChunkBags = 256;    // == kFwdThreads: one bag per thread in setup
-constexpr int kChunkElems = 4096;
-constexpr int kU = 4;              // row loads in flight per lane (halved when a lane holds two float4)
+constexpr int kWarpElems = 512;    // values of short bags one warp chunk holds
+constexpr int kU = 4;              // row loads in flight per lane (halved for two float4 per lane)
+constexpr int kFwdWarpsPerCta = kFwdThreads / kWarp;
 
 struct FwdArgs {
   const ColMeta* meta;
@@ -41,7 +45,7 @@ struct FwdArgs {
   int64_t n[2];
   int32_t ncols[2];
   int32_t col_base[2];
-  int32_t tiles[2];
+  int64_t tiles[2];
   int32_t tile_elems;
   int32_t batch;
   DivMagic32 bdiv;
@@ -57,21 +61,16 @@ struct FwdArgs {
   uint32_t* status;
 };
 
-struct FwdSmem {
-  int32_t rows[kChunkElems];
-  uint8_t bag[kChunkElems];
-  int32_t pos[kChunkBags + 1];     // first slot of each bag's values in rows[]
-  int32_t lo[kChunkBags];          // first stream element of each bag
-  int32_t hi[kChunkBags];          // one past its last stream element; -1: long bag
-  int32_t len[kChunkBags];         // values of the bag held in rows[]
-  int32_t longs[kChunkBags];       // bags left for phase C
-  int32_t tailbag[kFwdThreads];    // per lane group: bag whose tail partial it holds
-  int32_t nvp[kFwdThreads][2];     // per lane group: valid counts of head/tail partials
-  float4 part[2][kFwdWarps * 64];  // per lane group: head / tail partial sums
-  int32_t warp_sum[kFwdWarps];
-  int32_t seg[2];
-  int32_t nlong;
-  ColMeta cm;                      // metadata of the chunk's column
+struct __align__(16) WarpSmem {
+  float4 part[2][64];      // head / tail partial sums, [group * dim/4 + slot]
+  int32_t rows[kWarpElems];
+  uint8_t bag[kWarpElems];
+  int32_t pos[33];         // first slot of each bag's values in rows[]
+  int32_t lo[32];          // first stream element of each bag
+  int32_t len[32];         // values of the bag held in rows[]
+  int32_t tailbag[32];     // per lane group: bag whose tail partial it holds
+  int32_t nvp[32][2];      // per lane group: valid counts of head / tail partials
+  ColMeta cm;              // metadata of the chunk's column
 };
 
 __device__ __forceinline__ float4 f4zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
@@ -112,11 +111,16 @@ __device__ int warp_lower_bound(const int32_t* offs, int S, int64_t e, int64_t n
   return lo + __popc(__ballot_sync(kFull, less));
 }
 
-// Transformed, guarded row of element t of a column; -1 when dropped.
-__device__ __forceinline__ int32_t col_row(const ColMeta& m, const int64_t* ids, const float* fvals,
-                                           int64_t t) {
+// Raw value of element t (int64 id, or the fp32 bits of a bucketize value).
+__device__ __forceinline__ int64_t col_load(const ColMeta& m, const int64_t* ids, const float* fvals, int64_t t) {
+  if (m.transform == EMB_T_BUCKETIZE) return (int64_t)__float_as_int(__ldcs(fvals + t));
+  return __ldcs(ids + t);
+}
+
+// Transformed, guarded row of a raw value; -1 when dropped.
+__device__ __forceinline__ int32_t col_transform(const ColMeta& m, int64_t v) {
   if (m.transform == EMB_T_BUCKETIZE) {
-    const float x = __ldcs(fvals + t);
+    const float x = __int_as_float((int32_t)v);
     int lo = 0, hi = m.nb;
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
@@ -124,9 +128,13 @@ __device__ __forceinline__ int32_t col_row(const ColMeta& m, const int64_t* ids,
     }
     return lo;
   }
-  const int64_t v = __ldcs(ids + t);
   if (m.transform == EMB_T_HASH_MOD) return (int32_t)mod_magic(splitmix64((uint64_t)v), m.mod);
   return (v >= 0 && v < m.num_rows) ? (int32_t)v : -1;
+}
+
+__device__ __forceinline__ int32_t col_row(const ColMeta& m, const int64_t* ids, const float* fvals,
+                                           int64_t t) {
+  return col_transform(m, col_load(m, ids, fvals, t));
 }
 
 __device__ __forceinline__ void record(const FwdArgs& a, int st, int64_t t, int32_t row,
@@ -137,6 +145,31 @@ __device__ __forceinline__ void record(const FwdArgs& a, int st, int64_t t, int3
     a.keys[r] = row >= 0 ? m.table_base + (uint32_t)row : a.key_sentinel;
     a.vals[r] = gsrc;
   }
+}
+
+__device__ __forceinline__ void record_cut(const FwdArgs& a, int st, int64_t t, const ColMeta& m) {
+  // a value past pad_len: no output, no gradient
+  const int64_t r = a.rec_base[st] + t;
+  if (a.rows_dbg) a.rows_dbg[r] = col_row(m, a.ids, a.fvals, t);
+  if (a.keys) {
+    a.keys[r] = a.key_sentinel;
+    a.vals[r] = 0u;
+  }
+}
+
+// Compensated (Neumaier) accumulation: the error of a long fp32 sum stays
+// near one rounding of the result instead of growing with the chain length.
+__device__ __forceinline__ void kadd(float& s, float& c, float x) {
+  const float t = s + x;
+  c += (fabsf(s) >= fabsf(x)) ? ((s - t) + x) : ((x - t) + s);
+  s = t;
+}
+
+__device__ __forceinline__ void kadd4(float4& s, float4& c, const float4& x) {
+  kadd(s.x, c.x, x.x);
+  kadd(s.y, c.y, x.y);
+  kadd(s.z, c.z, x.z);
+  kadd(s.w, c.w, x.w);
 }
 
 // Final value of float4 slot f4 of a pooled bag: mean / sum / default.
@@ -159,42 +192,25 @@ __device__ __forceinline__ int lanes_log2(int dim4) {
   return l;
 }
 
-// Exclusive block scan of one int per thread (kFwdThreads threads).
-__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sum, int& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(kFull, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) warp_sum[warp] = x;
-  __syncthreads();
-  int base = 0;
-  total = 0;
-#pragma unroll
-  for (int w = 0; w < kFwdWarps; ++w) {
-    const int s = warp_sum[w];
-    if (w < warp) base += s;
-    total += s;
-  }
-  __syncthreads();
-  return base + x - v;
+__device__ __forceinline__ uint32_t pooled_gsrc(const FwdArgs& a, const ColMeta& m, int32_t bag) {
+  return (uint32_t)m.col * (uint32_t)a.batch + (uint32_t)bag;
+}
+
+__device__ __forceinline__ uint32_t padded_gsrc(const FwdArgs& a, const ColMeta& m, int32_t bag, int64_t p) {
+  return kPadBit | (uint32_t)((m.seq_unit * a.batch + ((int64_t)bag * m.pad_len + p) * m.dim) >> 2);
 }
 
 // ---------------------------------------------------------------------------
-// phase B: pooled bags of a chunk, one equal range of values per lane group
+// phase B, pooled: equal value ranges per lane group
 // ---------------------------------------------------------------------------
 template <int V>
-__device__ void pool_chunk(const FwdArgs& a, FwdSmem& sm, const ColMeta& m, int ns, int T, int b0,
-                           int glog) {
+__device__ void warp_pool_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m, int ns, int T, int b0,
+                                int glog, unsigned longmask) {
   constexpr int U = kU / V;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   const int G = 32 >> glog;
-  const int grp = lane >> glog, sub = lane & ((1 << glog) - 1);
-  const int q = warp * G + grp;                 // lane group id
-  const int NG = kFwdWarps * G;
-  const int R = (T + NG - 1) / NG;
+  const int q = lane >> glog, sub = lane & ((1 << glog) - 1);
+  const int R = (T + G - 1) / G;
   const int k0 = min(q * R, T), k1 = min(k0 + R, T);
   const float* E = m.weight;
 
@@ -202,9 +218,9 @@ __device__ void pool_chunk(const FwdArgs& a, FwdSmem& sm, const ColMeta& m, int 
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = f4zero();
   int nv = 0;
-  int curb = k0 < k1 ? (int)sm.bag[k0] : -1;
-  bool head = k0 > 0 && k0 < k1 && (int)sm.bag[k0 - 1] == curb;
-  if (sub == 0) sm.tailbag[q] = -1;
+  int curb = k0 < k1 ? (int)ws.bag[k0] : -1;
+  bool head = k0 > 0 && k0 < k1 && (int)ws.bag[k0 - 1] == curb;
+  if (sub == 0) ws.tailbag[q] = -1;
 
   auto write_out = [&](int b, const float4 (&s)[V], int cnt) {
     const int bag = b0 + b;
@@ -215,22 +231,22 @@ __device__ void pool_chunk(const FwdArgs& a, FwdSmem& sm, const ColMeta& m, int 
       if (f4 < m.dim4) *reinterpret_cast<float4*>(y + f4 * 4) = finish(m, s[v], cnt, f4);
     }
     if (a.inv_n && sub == 0 && m.pooling == EMB_POOL_MEAN)
-      a.inv_n[(uint32_t)m.col * (uint32_t)a.batch + (uint32_t)bag] = cnt > 0 ? 1.0f / (float)cnt : 0.0f;
+      a.inv_n[pooled_gsrc(a, m, bag)] = cnt > 0 ? 1.0f / (float)cnt : 0.0f;
   };
   auto flush = [&](bool tail) {
     if (!head && !tail) {
       write_out(curb, acc, nv);
-    } else {
-      const int side = head ? 0 : 1;
+      return;
+    }
+    const int side = head ? 0 : 1;
 #pragma unroll
-      for (int v = 0; v < V; ++v) {
-        const int f4 = sub + v * 32;
-        if (f4 < m.dim4) sm.part[side][q * m.dim4 + f4] = acc[v];
-      }
-      if (sub == 0) {
-        sm.nvp[q][side] = nv;
-        if (!head) sm.tailbag[q] = curb;
-      }
+    for (int v = 0; v < V; ++v) {
+      const int f4 = sub + v * 32;
+      if (f4 < m.dim4) ws.part[side][q * m.dim4 + f4] = acc[v];
+    }
+    if (sub == 0) {
+      ws.nvp[q][side] = nv;
+      if (!head) ws.tailbag[q] = curb;
     }
   };
 
@@ -242,8 +258,8 @@ __device__ void pool_chunk(const FwdArgs& a, FwdSmem& sm, const ColMeta& m, int 
     for (int u = 0; u < U; ++u) {
       const int k = k0 + j + u;
       const bool in = k < k1;
-      const int r = in ? sm.rows[k] : -1;
-      bg[u] = in ? (int)sm.bag[k] : -1;
+      const int r = in ? ws.rows[k] : -1;
+      bg[u] = in ? (int)ws.bag[k] : -1;
       ok[u] = in && r >= 0;
 #pragma unroll
       for (int v = 0; v < V; ++v) {
@@ -267,62 +283,59 @@ __device__ void pool_chunk(const FwdArgs& a, FwdSmem& sm, const ColMeta& m, int 
       nv += ok[u];
     }
   }
-  if (k0 < k1) flush(k1 < T && (int)sm.bag[k1] == curb);
-  __syncthreads();
+  if (k0 < k1) flush(k1 < T && (int)ws.bag[k1] == curb);
+  __syncwarp();
 
   // the group holding a cut bag's first value adds the partials in order
-  const int tb = sm.tailbag[q];
+  const int tb = ws.tailbag[q];
   if (tb >= 0) {
     float4 s[V];
-    int cnt = sm.nvp[q][1];
+    int cnt = ws.nvp[q][1];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
       const int f4 = sub + v * 32;
-      s[v] = f4 < m.dim4 ? sm.part[1][q * m.dim4 + f4] : f4zero();
+      s[v] = f4 < m.dim4 ? ws.part[1][q * m.dim4 + f4] : f4zero();
     }
-    const int last = (sm.pos[tb] + sm.len[tb] - 1) / R;
+    const int last = (ws.pos[tb] + ws.len[tb] - 1) / R;
     for (int q2 = q + 1; q2 <= last; ++q2) {
 #pragma unroll
       for (int v = 0; v < V; ++v) {
         const int f4 = sub + v * 32;
-        if (f4 < m.dim4) f4add(s[v], sm.part[0][q2 * m.dim4 + f4]);
+        if (f4 < m.dim4) f4add(s[v], ws.part[0][q2 * m.dim4 + f4]);
       }
-      cnt += sm.nvp[q2][0];
+      cnt += ws.nvp[q2][0];
     }
     write_out(tb, s, cnt);
   }
   // empty bags: default vector
-  for (int i = threadIdx.x; i < ns; i += kFwdThreads) {
-    if (sm.len[i] != 0 || sm.hi[i] < 0) continue;
-    float* y = a.out + (int64_t)(b0 + i) * a.ldo + m.out_col;
+  if (lane < ns && ws.len[lane] == 0 && !((longmask >> lane) & 1u)) {
+    float* y = a.out + (int64_t)(b0 + lane) * a.ldo + m.out_col;
     for (int f4 = 0; f4 < m.dim4; ++f4) *reinterpret_cast<float4*>(y + f4 * 4) = finish(m, f4zero(), 0, f4);
-    if (a.inv_n && m.pooling == EMB_POOL_MEAN)
-      a.inv_n[(uint32_t)m.col * (uint32_t)a.batch + (uint32_t)(b0 + i)] = 0.0f;
+    if (a.inv_n && m.pooling == EMB_POOL_MEAN) a.inv_n[pooled_gsrc(a, m, b0 + lane)] = 0.0f;
   }
 }
 
-// phase B for padded columns: ns bags x pad_len output rows, flat over groups.
+// phase B, padded (short pad_len): ns bags x pad_len output rows, flat over groups
 template <int V>
-__device__ void pad_chunk(const FwdArgs& a, FwdSmem& sm, const ColMeta& m, int ns, int b0, int glog) {
+__device__ void warp_pad_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m, int ns, int b0, int glog,
+                               unsigned longmask) {
   constexpr int U = kU / V;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   const int G = 32 >> glog;
-  const int grp = lane >> glog, sub = lane & ((1 << glog) - 1);
-  const int q = warp * G + grp;
-  const int NG = kFwdWarps * G;
+  const int q = lane >> glog, sub = lane & ((1 << glog) - 1);
   const int P = m.pad_len;
   const int total = ns * P;
   const float* E = m.weight;
-  for (int base = 0; base < total; base += NG * U) {
+  for (int base = 0; base < total; base += G * U) {
     float4 vals[U][V];
     int o[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      o[u] = base + u * NG + q;
+      o[u] = base + u * G + q;
       int r = -1;
       if (o[u] < total) {
         const int i = o[u] / P, p = o[u] - i * P;
-        if (sm.hi[i] >= 0 && p < sm.len[i]) r = sm.rows[sm.pos[i] + p];
+        if (p < ws.len[i]) r = ws.rows[ws.pos[i] + p];
       }
 #pragma unroll
       for (int v = 0; v < V; ++v) {
@@ -334,7 +347,7 @@ __device__ void pad_chunk(const FwdArgs& a, FwdSmem& sm, const ColMeta& m, int n
     for (int u = 0; u < U; ++u) {
       if (o[u] >= total) continue;
       const int i = o[u] / P, p = o[u] - i * P;
-      if (sm.hi[i] < 0) continue;   // long bag: phase C writes it
+      if ((longmask >> i) & 1u) continue;
       float* dst = a.seq_out + m.seq_unit * a.batch + ((int64_t)(b0 + i) * P + p) * m.dim;
 #pragma unroll
       for (int v = 0; v < V; ++v) {
@@ -346,28 +359,27 @@ __device__ void pad_chunk(const FwdArgs& a, FwdSmem& sm, const ColMeta& m, int n
 }
 
 // ---------------------------------------------------------------------------
-// phase C: one long bag, all warps; values transformed on the fly
+// phase C: one long bag, the whole warp, values transformed on the fly
 // ---------------------------------------------------------------------------
 template <int V>
-__device__ void cta_bag(const FwdArgs& a, FwdSmem& sm, int st, const ColMeta& m, int32_t b, int64_t lo,
-                        int64_t hi, int glog) {
+__device__ void warp_long_bag(const FwdArgs& a, int st, const ColMeta& m, int32_t b, int64_t lo, int64_t hi,
+                              int glog) {
   constexpr int U = kU / V;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   const int G = 32 >> glog;
   const int grp = lane >> glog, sub = lane & ((1 << glog) - 1);
   const float* E = m.weight;
   if (m.pooling == EMB_POOL_NONE_PADDED) {
     const int P = m.pad_len;
     const int64_t len = hi - lo;
-    const int64_t seq0 = m.seq_unit * a.batch + (int64_t)b * P * m.dim;
-    float* dst = a.seq_out + seq0;
-    for (int64_t p0 = (int64_t)warp * 32; p0 < P; p0 += (int64_t)kFwdWarps * 32) {
+    float* dst = a.seq_out + m.seq_unit * a.batch + (int64_t)b * P * m.dim;
+    for (int64_t p0 = 0; p0 < P; p0 += 32) {
       const int cnt = (int)(P - p0 < 32 ? P - p0 : 32);
       int32_t row = -1;
       const int64_t p = p0 + lane;
       if (lane < cnt && p < len) {
         row = col_row(m, a.ids, a.fvals, lo + p);
-        record(a, st, lo + p, row, m, kPadBit | (uint32_t)((seq0 + p * m.dim) >> 2));
+        record(a, st, lo + p, row, m, padded_gsrc(a, m, b, p));
       }
       for (int k = 0; k < cnt; k += U * G) {
         float4 v[U][V];
@@ -394,22 +406,18 @@ __device__ void cta_bag(const FwdArgs& a, FwdSmem& sm, int st, const ColMeta& m,
       }
     }
     if (a.rows_dbg || a.keys)
-      for (int64_t t = lo + P + threadIdx.x; t < hi; t += kFwdThreads) {
-        const int64_t r = a.rec_base[st] + t;
-        if (a.rows_dbg) a.rows_dbg[r] = col_row(m, a.ids, a.fvals, t);
-        if (a.keys) {
-          a.keys[r] = a.key_sentinel;
-          a.vals[r] = 0u;
-        }
-      }
+      for (int64_t t = lo + P + lane; t < hi; t += 32) record_cut(a, st, t, m);
     return;
   }
-  const uint32_t gsrc = (uint32_t)m.col * (uint32_t)a.batch + (uint32_t)b;
-  float4 acc[V];
+  const uint32_t gsrc = pooled_gsrc(a, m, b);
+  float4 acc[V], cmp[V];
 #pragma unroll
-  for (int q = 0; q < V; ++q) acc[q] = f4zero();
+  for (int q = 0; q < V; ++q) {
+    acc[q] = f4zero();
+    cmp[q] = f4zero();
+  }
   int nv = 0;
-  for (int64_t base = lo + (int64_t)warp * 32; base < hi; base += (int64_t)kFwdWarps * 32) {
+  for (int64_t base = lo; base < hi; base += 32) {
     const int cnt = (int)(hi - base < 32 ? hi - base : 32);
     int32_t row = -1;
     if (lane < cnt) {
@@ -433,8 +441,15 @@ __device__ void cta_bag(const FwdArgs& a, FwdSmem& sm, int st, const ColMeta& m,
 #pragma unroll
       for (int u = 0; u < U; ++u)
 #pragma unroll
-        for (int q = 0; q < V; ++q) f4add(acc[q], v[u][q]);
+        for (int q = 0; q < V; ++q) kadd4(acc[q], cmp[q], v[u][q]);
     }
+  }
+#pragma unroll
+  for (int q = 0; q < V; ++q) {
+    acc[q].x += cmp[q].x;
+    acc[q].y += cmp[q].y;
+    acc[q].z += cmp[q].z;
+    acc[q].w += cmp[q].w;
   }
 #pragma unroll
   for (int q = 0; q < V; ++q)
@@ -444,150 +459,117 @@ __device__ void cta_bag(const FwdArgs& a, FwdSmem& sm, int st, const ColMeta& m,
       acc[q].z += __shfl_xor_sync(kFull, acc[q].z, off);
       acc[q].w += __shfl_xor_sync(kFull, acc[q].w, off);
     }
-  float4* red = sm.part[0];   // [kFwdWarps][64]
   if (grp == 0) {
+    float* y = a.out + (int64_t)b * a.ldo + m.out_col;
 #pragma unroll
     for (int q = 0; q < V; ++q) {
       const int f4 = sub + q * 32;
-      if (f4 < m.dim4) red[warp * 64 + f4] = acc[q];
+      if (f4 < m.dim4) *reinterpret_cast<float4*>(y + f4 * 4) = finish(m, acc[q], nv, f4);
     }
   }
-  if (lane == 0) sm.nvp[warp][0] = nv;
-  __syncthreads();
-  int tot = 0;
-#pragma unroll
-  for (int w = 0; w < kFwdWarps; ++w) tot += sm.nvp[w][0];
-  for (int f4 = threadIdx.x; f4 < m.dim4; f4 += kFwdThreads) {
-    float4 s = red[f4];
-#pragma unroll
-    for (int w = 1; w < kFwdWarps; ++w) f4add(s, red[w * 64 + f4]);
-    *reinterpret_cast<float4*>(a.out + (int64_t)b * a.ldo + m.out_col + f4 * 4) = finish(m, s, tot, f4);
-  }
-  if (a.inv_n && threadIdx.x == 0 && m.pooling == EMB_POOL_MEAN)
-    a.inv_n[gsrc] = tot > 0 ? 1.0f / (float)tot : 0.0f;
-  __syncthreads();
+  if (a.inv_n && lane == 0 && m.pooling == EMB_POOL_MEAN) a.inv_n[gsrc] = nv > 0 ? 1.0f / (float)nv : 0.0f;
 }
 
 // ---------------------------------------------------------------------------
-// the kernel
+// the kernel: one warp per element tile
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kFwdThreads, 4) k_forward(const FwdArgs a) {
-  __shared__ FwdSmem sm;
-  int tile = blockIdx.x, st = 0;
+  __shared__ WarpSmem smem[kFwdWarpsPerCta];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  WarpSmem& ws = smem[warp];
+  int64_t tile = (int64_t)blockIdx.x * kFwdWarpsPerCta + warp;
+  if (tile >= a.tiles[0] + a.tiles[1]) return;   // no CTA-wide barrier below
+  int st = 0;
   if (tile >= a.tiles[0]) {
     st = 1;
     tile -= a.tiles[0];
   }
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = a.ncols[st] * a.batch;
-  const int64_t e0 = (int64_t)tile * a.tile_elems;
-  const bool last = tile == a.tiles[st] - 1;
   const int32_t* offs = a.offs[st];
   const int64_t n = a.n[st];
-  if (warp == 0) {
-    const int r = warp_lower_bound(offs, S, e0, n);
-    if (lane == 0) sm.seg[0] = r;
-  } else if (warp == 1) {
-    const int r = last ? S : warp_lower_bound(offs, S, e0 + a.tile_elems, n);
-    if (lane == 0) sm.seg[1] = r;
-  }
-  __syncthreads();
-  const int s_hi = sm.seg[1];
-  int cur = sm.seg[0];
+  const int64_t e0 = tile * a.tile_elems;
+  const bool last = tile == a.tiles[st] - 1;
+  int cur = warp_lower_bound(offs, S, e0, n);
+  const int s_hi = last ? S : warp_lower_bound(offs, S, e0 + a.tile_elems, n);
+
   while (cur < s_hi) {
-    // ---- chunk setup: one bag per thread, all inside column cl0 ----
+    // ---- setup: one lane per bag, all inside column cl0 ----
     const int cl0 = (int)div_magic32((uint32_t)cur, a.bdiv);
     const int b0 = cur - cl0 * a.batch;
-    const int navail = min(kChunkBags, min(s_hi, (cl0 + 1) * a.batch) - cur);
-    static_assert(sizeof(ColMeta) % 4 == 0 && sizeof(ColMeta) / 4 <= kFwdThreads, "metadata copy");
-    if (tid < (int)(sizeof(ColMeta) / 4))
-      reinterpret_cast<int32_t*>(&sm.cm)[tid] =
-          __ldg(reinterpret_cast<const int32_t*>(a.meta + __ldg(a.stream_cols + a.col_base[st] + cl0)) + tid);
-    __syncthreads();
-    const ColMeta& m = sm.cm;
+    const int navail = min(32, min(s_hi, (cl0 + 1) * a.batch) - cur);
+    static_assert(sizeof(ColMeta) % 4 == 0 && sizeof(ColMeta) / 4 <= 32, "metadata copy");
+    if (lane < (int)(sizeof(ColMeta) / 4))
+      reinterpret_cast<int32_t*>(&ws.cm)[lane] =
+          __ldg(reinterpret_cast<const int32_t*>(a.meta + __ldg(a.stream_cols + a.col_base[st] + cl0)) + lane);
+    __syncwarp();
+    const ColMeta& m = ws.cm;
     const bool padded = m.pooling == EMB_POOL_NONE_PADDED;
     int64_t lo = 0, hi = 0;
     int used = 0;
     bool is_long = false;
-    if (tid < navail) {
+    if (lane < navail) {
       bool bad = false;
-      lo = clamp_off(__ldg(offs + cur + tid), n, bad);
-      hi = clamp_off(__ldg(offs + cur + tid + 1), n, bad);
+      lo = clamp_off(__ldg(offs + cur + lane), n, bad);
+      hi = clamp_off(__ldg(offs + cur + lane + 1), n, bad);
       if (hi < lo) { hi = lo; bad = true; }
       if (bad) latch(a.status, EMB_ERR_BAD_INDEX);
       const int64_t len = hi - lo;
       is_long = (padded ? (int64_t)m.pad_len : len) > kLongBag;
       used = is_long ? 0 : (int)(padded ? (len < m.pad_len ? len : (int64_t)m.pad_len) : len);
     }
-    int total = 0;
-    const int pos = block_exclusive_scan(used, sm.warp_sum, total);
-    const bool fits = tid < navail && pos + used <= kChunkElems;
-    const int ns = __syncthreads_count(fits);
-    if (tid == 0) sm.nlong = 0;
-    __syncthreads();
-    if (tid < ns) {
-      sm.pos[tid] = pos;
-      sm.lo[tid] = (int32_t)lo;
-      sm.len[tid] = used;
-      sm.hi[tid] = is_long ? -1 : (int32_t)hi;
-      if (is_long) sm.longs[atomicAdd(&sm.nlong, 1)] = tid;
-      if (tid == ns - 1) sm.pos[ns] = pos + used;
-      for (int k = pos; k < pos + used; ++k) sm.bag[k] = (uint8_t)tid;
+    int incl = used;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
     }
-    __syncthreads();
-    const int T = sm.pos[ns];
+    const int pos = incl - used;
+    const int ns = __popc(__ballot_sync(kFull, lane < navail && incl <= kWarpElems));
+    const unsigned longmask = __ballot_sync(kFull, lane < ns && is_long);
+    if (lane < ns) {
+      ws.pos[lane] = pos;
+      ws.lo[lane] = (int32_t)lo;
+      ws.len[lane] = used;
+    }
+    if (lane == ns - 1) ws.pos[ns] = incl;
+    __syncwarp();
+    const int T = ws.pos[ns];
 
-    // ---- phase A: transform every value of the chunk's short bags ----
-    for (int k = tid; k < T; k += kFwdThreads) {
-      const int i = sm.bag[k];
-      const int64_t t = (int64_t)sm.lo[i] + (k - sm.pos[i]);
+    // ---- phase A: transform the chunk's values into shared memory ----
+    for (int k = lane; k < T; k += 32) {
+      int i = 0;                             // last bag whose first slot is <= k
+      for (int step = 16; step > 0; step >>= 1)
+        if (i + step < ns && ws.pos[i + step] <= k) i += step;
+      const int64_t t = (int64_t)ws.lo[i] + (k - ws.pos[i]);
       const int32_t row = col_row(m, a.ids, a.fvals, t);
-      sm.rows[k] = row;
-      if (a.rows_dbg || a.keys) {
-        uint32_t gsrc;
-        if (padded)
-          gsrc = kPadBit | (uint32_t)((m.seq_unit * a.batch +
-                                       ((int64_t)(b0 + i) * m.pad_len + (k - sm.pos[i])) * m.dim) >> 2);
-        else
-          gsrc = (uint32_t)m.col * (uint32_t)a.batch + (uint32_t)(b0 + i);
-        record(a, st, t, row, m, gsrc);
-      }
+      ws.rows[k] = row;
+      ws.bag[k] = (uint8_t)i;
+      if (a.rows_dbg || a.keys)
+        record(a, st, t, row, m, padded ? padded_gsrc(a, m, b0 + i, k - ws.pos[i]) : pooled_gsrc(a, m, b0 + i));
     }
-    // values past pad_len of short padded bags: no output, no gradient
-    if (padded && (a.rows_dbg || a.keys) && tid < ns && sm.hi[tid] >= 0)
-      for (int64_t t = (int64_t)sm.lo[tid] + m.pad_len; t < sm.hi[tid]; ++t) {
-        const int64_t r = a.rec_base[st] + t;
-        if (a.rows_dbg) a.rows_dbg[r] = col_row(m, a.ids, a.fvals, t);
-        if (a.keys) {
-          a.keys[r] = a.key_sentinel;
-          a.vals[r] = 0u;
-        }
-      }
-    __syncthreads();
+    if (padded && (a.rows_dbg || a.keys) && lane < ns && !is_long)
+      for (int64_t t = lo + m.pad_len; t < hi; ++t) record_cut(a, st, t, m);
+    __syncwarp();
 
     // ---- phase B: pool / copy ----
     const int glog = lanes_log2(m.dim4);
     if (padded) {
-      if (m.dim4 > 32) pad_chunk<2>(a, sm, m, ns, b0, glog);
-      else pad_chunk<1>(a, sm, m, ns, b0, glog);
+      if (m.dim4 > 32) warp_pad_chunk<2>(a, ws, m, ns, b0, glog, longmask);
+      else warp_pad_chunk<1>(a, ws, m, ns, b0, glog, longmask);
     } else {
-      if (m.dim4 > 32) pool_chunk<2>(a, sm, m, ns, T, b0, glog);
-      else pool_chunk<1>(a, sm, m, ns, T, b0, glog);
+      if (m.dim4 > 32) warp_pool_chunk<2>(a, ws, m, ns, T, b0, glog, longmask);
+      else warp_pool_chunk<1>(a, ws, m, ns, T, b0, glog, longmask);
     }
-    __syncthreads();
 
     // ---- phase C: long bags of the chunk ----
-    const int nlong = sm.nlong;
-    for (int j = 0; j < nlong; ++j) {
-      const int i = sm.longs[j];
-      bool bad = false;
-      const int64_t blo = clamp_off(__ldg(offs + cur + i), n, bad);
-      int64_t bhi = clamp_off(__ldg(offs + cur + i + 1), n, bad);
-      if (bhi < blo) bhi = blo;
-      if (m.dim4 > 32) cta_bag<2>(a, sm, st, m, b0 + i, blo, bhi, glog);
-      else cta_bag<1>(a, sm, st, m, b0 + i, blo, bhi, glog);
+    for (unsigned lm = longmask; lm; lm &= lm - 1) {
+      const int i = __ffs(lm) - 1;
+      const int64_t blo = __shfl_sync(kFull, lo, i);
+      const int64_t bhi = __shfl_sync(kFull, hi, i);
+      if (m.dim4 > 32) warp_long_bag<2>(a, st, m, b0 + i, blo, bhi, glog);
+      else warp_long_bag<1>(a, st, m, b0 + i, blo, bhi, glog);
     }
-    __syncthreads();
+    __syncwarp();
     cur += ns;
   }
 }
@@ -633,17 +615,19 @@ emb_status launch_forward(emb_plan_s* p, int32_t batch, const int64_t* ids, cons
   }
   a.key_sentinel = p->key_total;
   a.status = p->status_d;
+  // tiles: about 8 per resident warp, between 256 and kMaxTileElems values
   const int64_t total = n_ids + n_fvals;
-  const int64_t resident = (int64_t)p->sm_count * p->fwd_ctas_per_sm;
-  const int64_t want = total / std::max<int64_t>(1, 8 * resident);
-  int64_t E = 512;
+  const int64_t warps = (int64_t)p->sm_count * p->fwd_ctas_per_sm * kFwdWarpsPerCta;
+  const int64_t want = total / std::max<int64_t>(1, 8 * warps);
+  int64_t E = 256;
   while (E < want && E < kMaxTileElems) E <<= 1;
   a.tile_elems = (int32_t)E;
-  a.tiles[0] = a.ncols[0] > 0 ? (int32_t)(n_ids / E + 1) : 0;
-  a.tiles[1] = a.ncols[1] > 0 ? (int32_t)(n_fvals / E + 1) : 0;
-  const int grid = a.tiles[0] + a.tiles[1];
-  if (grid == 0) return EMB_OK;
-  k_forward<<<grid, kFwdThreads, 0, stream>>>(a);
+  a.tiles[0] = a.ncols[0] > 0 ? n_ids / E + 1 : 0;
+  a.tiles[1] = a.ncols[1] > 0 ? n_fvals / E + 1 : 0;
+  const int64_t tiles = a.tiles[0] + a.tiles[1];
+  if (tiles == 0) return EMB_OK;
+  const int64_t grid = (tiles + kFwdWarpsPerCta - 1) / kFwdWarpsPerCta;
+  k_forward<<<(unsigned)grid, kFwdThreads, 0, stream>>>(a);
   return cuda_status(cudaGetLastError());
 }
 

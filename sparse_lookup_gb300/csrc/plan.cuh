@@ -10,7 +10,10 @@ namespace emb {
 
 // Forward tiles cover this many stream elements at most (bags are owned by the
 // tile that holds their first element).
-constexpr int kFwdThreads = 256;
+#ifndef EMB_FWD_THREADS
+#define EMB_FWD_THREADS 256
+#endif
+constexpr int kFwdThreads = EMB_FWD_THREADS;
 constexpr int kFwdWarps = kFwdThreads / kWarp;
 constexpr int kLongBag = 128;         // longer bags are pooled by a whole CTA
 constexpr int kMaxTileElems = 8192;
