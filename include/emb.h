@@ -216,7 +216,9 @@ emb_status emb_get_device_status(emb_plan plan, void* stream);
 typedef struct emb_hash_s* emb_hash;
 
 /* hash_create -- a GPU key -> row table over a private row pool.
- *  num_slots      power of two, 2^10 .. 2^31: open-addressing slots of 16 B
+ *  num_slots      power of two, 2^10 .. 2^31: open-addressing slots of 16 B.
+ *                 Expired entries leave tombstones that are never reused, so
+ *                 keep (keys ever inserted) well below num_slots.
  *  row_capacity   rows in the pool, 1 .. 2^31-1
  *  dim            floats per row (4..256, multiple of 4)
  *  admit_threshold occurrences a key needs before it gets a row (>= 1)
@@ -224,12 +226,15 @@ typedef struct emb_hash_s* emb_hash;
  *  init_seed, init_scale: a new row's element d is
  *                 init_scale * ((splitmix64(key ^ (tid << 48) ^ seed ^ d)
  *                 >> 40) - 2^23) * 2^-23, its accumulator 0.
+ *  max_keys_per_call  largest n a hash_lookup_or_insert will pass (< 2^30);
+ *                 sizes the admission workspace so lookups never allocate.
  *  out            (host) receives the handle.
  * Keys are (table id, key) pairs with 0 <= tid < 2^15 and 0 <= key < 2^48;
- * distinct pairs never share an entry or a row. */
+ * distinct pairs never share an entry or a row.  Allocates the slots, the
+ * row pool and the workspace once and synchronizes the device. */
 emb_status hash_create(int64_t num_slots, int64_t row_capacity, int32_t dim,
                        int32_t admit_threshold, int32_t max_probes, uint64_t init_seed,
-                       float init_scale, emb_hash* out);
+                       float init_scale, int64_t max_keys_per_call, emb_hash* out);
 
 /* Borrowed views of the row pool: weight and accumulator [row_capacity, dim]
  * fp32, owned by the handle (valid until hash_destroy).  Either may be NULL. */
@@ -244,10 +249,12 @@ emb_status hash_rows(emb_hash h, float** weight, float** acc);
  * hash_create.  rows_out[i] is the row of occurrence i, or -1 while its key
  * is not admitted (also for a key outside the key range, which latches
  * EMB_ERR_INVALID_ARG).  A full pool latches EMB_ERR_TABLE_FULL (the keys left
- * without a row keep counting and are admitted once rows are free); probing
- * max_probes slots without a place latches EMB_ERR_PROBE_LIMIT.
+ * without a row keep counting and are admitted by their first occurrence in a
+ * later call, once rows are free; calls are told apart by `step`, so steps of
+ * consecutive calls should differ); probing max_probes slots without a place
+ * latches EMB_ERR_PROBE_LIMIT and returns -1 for that occurrence.
  *  table_ids [n] int32; keys [n] int64; rows_out [n] int64 (feeds emb_forward
- *  columns of transform EMB_T_ROWS_GIVEN directly).  n < 2^31. */
+ *  columns of transform EMB_T_ROWS_GIVEN directly).  n <= max_keys_per_call. */
 emb_status hash_lookup_or_insert(emb_hash h, const int32_t* table_ids, const int64_t* keys,
                                  int64_t n, uint32_t step, int64_t* rows_out, void* stream);
 
@@ -257,11 +264,11 @@ emb_status hash_lookup_or_insert(emb_hash h, const int32_t* table_ids, const int
 emb_status hash_evict_expired(emb_hash h, uint32_t now, uint32_t ttl, void* stream,
                               int64_t* n_evicted_dev);
 
-/* hash_export -- every live entry, in slot order: tids, keys, rows (-1 while
- * counting), counts (occurrences counted so far), last_seen; each output is an
- * optional device array of `cap` entries.  *n_out (host) receives the number
- * of live entries (which may exceed cap: only cap are written).
- * Synchronizes `stream`. */
+/* hash_export -- every live entry, in no particular order: tids, keys, rows
+ * (-1 while counting), counts (occurrences counted so far while counting; -1
+ * once admitted), last_seen; each output is an optional device array of `cap`
+ * entries.  *n_out (host) receives the number of live entries (which may
+ * exceed cap: only cap are written).  Synchronizes `stream`. */
 emb_status hash_export(emb_hash h, int32_t* tids, int64_t* keys, int64_t* rows, int32_t* counts,
                        uint32_t* last_seen, int64_t cap, int64_t* n_out, void* stream);
 

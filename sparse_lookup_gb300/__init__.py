@@ -75,7 +75,8 @@ _SIGS = {
     "emb_backward_update": (c_int32, [c_void_p, c_void_p, c_void_p, c_float, c_float, c_void_p,
                                       POINTER(EmbBackwardDebug)]),
     "emb_get_device_status": (c_int32, [c_void_p, c_void_p]),
-    "hash_create": (c_int32, [c_int64, c_int64, c_int32, c_int32, c_int32, c_uint64, c_float, POINTER(c_void_p)]),
+    "hash_create": (c_int32, [c_int64, c_int64, c_int32, c_int32, c_int32, c_uint64, c_float, c_int64,
+                              POINTER(c_void_p)]),
     "hash_rows": (c_int32, [c_void_p, POINTER(c_void_p), POINTER(c_void_p)]),
     "hash_lookup_or_insert": (c_int32, [c_void_p, c_void_p, c_void_p, c_int64, c_uint32, c_void_p, c_void_p]),
     "hash_evict_expired": (c_int32, [c_void_p, c_uint32, c_uint32, c_void_p, c_void_p]),
@@ -175,10 +176,12 @@ def emb_get_device_status(plan, stream=None):
     return int(lib().emb_get_device_status(plan, _stream(stream)))
 
 
-def hash_create(num_slots, row_capacity, dim, admit_threshold, max_probes, init_seed, init_scale):
+def hash_create(num_slots, row_capacity, dim, admit_threshold, max_probes, init_seed, init_scale,
+                max_keys_per_call):
     h = c_void_p()
     _check(lib().hash_create(num_slots, row_capacity, dim, admit_threshold, max_probes,
-                             init_seed & 0xFFFFFFFFFFFFFFFF, init_scale, ctypes.byref(h)), "hash_create")
+                             init_seed & 0xFFFFFFFFFFFFFFFF, init_scale, max_keys_per_call, ctypes.byref(h)),
+           "hash_create")
     return h.value
 
 
@@ -321,3 +324,77 @@ class Plan:
 
     def device_status(self, stream=None):
         return emb_get_device_status(self.handle, stream)
+
+
+class HashTable:
+    """Collision-free dynamic table on the device (hash_* entry points).
+    ``weight`` / ``acc`` are torch views of the row pool owned by the table."""
+
+    def __init__(self, num_slots, row_capacity, dim, admit_threshold, max_probes, init_seed, init_scale,
+                 max_keys_per_call):
+        import torch
+        self.dim = dim
+        self.row_capacity = row_capacity
+        self.handle = hash_create(num_slots, row_capacity, dim, admit_threshold, max_probes, init_seed,
+                                  init_scale, max_keys_per_call)
+        w, a = hash_rows(self.handle)
+        self.weight_ptr, self.acc_ptr = w, a
+        self.weight = _device_view(w, (row_capacity, dim))
+        self.acc = _device_view(a, (row_capacity, dim))
+
+    def lookup_or_insert(self, table_ids, keys, step, rows_out=None, stream=None):
+        import torch
+        n = keys.numel()
+        if rows_out is None:
+            rows_out = torch.empty(n, dtype=torch.int64, device=keys.device)
+        hash_lookup_or_insert(self.handle, table_ids, keys, n, step, rows_out, stream)
+        return rows_out
+
+    def evict_expired(self, now, ttl, stream=None, n_evicted=None):
+        hash_evict_expired(self.handle, now, ttl, stream, n_evicted)
+
+    def export(self, cap=None, stream=None):
+        """All live entries as host numpy arrays sorted by (tid, key)."""
+        import numpy as np
+        import torch
+        n = hash_export(self.handle, None, None, None, None, None, 0, stream)
+        cap = n if cap is None else cap
+        dev = "cuda"
+        t = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+        k = torch.empty(max(cap, 1), dtype=torch.int64, device=dev)
+        r = torch.empty(max(cap, 1), dtype=torch.int64, device=dev)
+        c = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+        s = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+        n = hash_export(self.handle, t, k, r, c, s, cap, stream)
+        m = min(n, cap)
+        t, k, r, c = [x[:m].cpu().numpy() for x in (t, k, r, c)]
+        s = s[:m].cpu().numpy().view(np.uint32)
+        order = np.lexsort((k, t))
+        return dict(tid=t[order], key=k[order], row=r[order], count=c[order], last_seen=s[order])
+
+    def device_status(self, stream=None):
+        return hash_get_device_status(self.handle, stream)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            hash_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _device_view(ptr_value, shape):
+    """A torch float32 tensor viewing library-owned device memory (no copy)."""
+    import torch
+
+    class _Holder:
+        pass
+
+    h = _Holder()
+    h.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": "<f4", "data": (ptr_value, False),
+                                  "version": 2, "strides": None}
+    return torch.as_tensor(h, device="cuda")

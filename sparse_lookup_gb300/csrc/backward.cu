@@ -6,12 +6,9 @@
 // contributions the forward recorded as (global row, gradient source) pairs
 // are radix-sorted by row, so every unique row becomes one contiguous run
 // with exactly one writer:
-//   1. k_digit_hist  -- digit histograms of all passes in one read of the keys;
-//   2. k_onesweep    -- per 8-bit digit pass, a stable LSD scatter: a CTA
-//                       ranks its tile in shared memory, publishes per-digit
-//                       counts and resolves its global offsets by decoupled
-//                       look-back over the earlier tiles (Adinets & Merrill,
-//                       "Onesweep", 2022); every wait is bounded;
+//   1-2. radix_sort_pairs (radix.cuh) -- one read of the keys for the digit
+//                       histograms, then one stable chained-scan scatter per
+//                       8-bit digit with bounded decoupled look-back;
 //   3. k_segreduce   -- lane groups of dim/4 lanes take equal ranges of sorted
 //                       contributions, gather scale * G rows with 16-byte
 //                       loads and sum each run; a run owned by one group is
@@ -25,164 +22,13 @@
 #include <algorithm>
 
 #include "plan.cuh"
+#include "radix.cuh"
 
 namespace emb {
 
-constexpr uint32_t kFlagAgg = 1u << 30;
-constexpr uint32_t kFlagInc = 2u << 30;
-constexpr uint32_t kCountMask = (1u << 30) - 1;
-constexpr int kSpinLimit = 1 << 22;
-constexpr int kSortWarps = kSortThreads / 32;
 constexpr int kSegThreads = 256;
 constexpr int kSegWarps = kSegThreads / 32;
 constexpr int kSegU = 4;
-
-// ---------------------------------------------------------------------------
-// radix sort
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(512) k_digit_hist(const uint32_t* __restrict__ keys, int64_t n, int passes,
-                                                    uint32_t* __restrict__ hist) {
-  __shared__ uint32_t h[4 * kRadix];
-  for (int i = threadIdx.x; i < 4 * kRadix; i += blockDim.x) h[i] = 0;
-  __syncthreads();
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-    const uint32_t k = __ldg(keys + i);
-    for (int p = 0; p < passes; ++p) atomicAdd(&h[p * kRadix + ((k >> (p * kRadixBits)) & (kRadix - 1))], 1u);
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < passes * kRadix; i += blockDim.x)
-    if (h[i]) atomicAdd(&hist[i], h[i]);
-}
-
-struct SortSmem {
-  uint32_t keys[kSortTile];
-  uint32_t vals[kSortTile];
-  uint32_t whist[kSortWarps][kRadix];  // per-warp digit counts, then warp offsets
-  uint32_t dstart[kRadix];             // first slot of each digit inside the tile
-  uint32_t goff[kRadix];               // global position of the tile's first item of each digit
-  uint32_t hscan[kRadix];              // exclusive scan of the pass histogram
-  uint32_t wsum[kSortWarps];
-  uint32_t tile;
-};
-
-// Exclusive scan over the first 256 threads' values (all threads call).
-__device__ __forceinline__ uint32_t scan256(uint32_t v, uint32_t* wsum) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(kFull, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31 && warp < kRadix / 32) wsum[warp] = x;
-  __syncthreads();
-  uint32_t base = 0;
-  if (warp < kRadix / 32)
-    for (int w = 0; w < warp; ++w) base += wsum[w];
-  __syncthreads();
-  return base + x - v;
-}
-
-__global__ void __launch_bounds__(kSortThreads, 2)
-    k_onesweep(const uint32_t* __restrict__ kin, const uint32_t* __restrict__ vin, uint32_t* __restrict__ kout,
-               uint32_t* __restrict__ vout, int64_t n, int shift, const uint32_t* __restrict__ hist,
-               uint32_t* lookback, uint32_t* tile_ctr, uint32_t* status) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  SortSmem& sm = *reinterpret_cast<SortSmem*>(smem_raw);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) sm.tile = atomicAdd(tile_ctr, 1u);
-  for (int i = tid; i < kSortWarps * kRadix; i += kSortThreads) (&sm.whist[0][0])[i] = 0;
-  const uint32_t hs = scan256(tid < kRadix ? __ldg(hist + tid) : 0u, sm.wsum);
-  if (tid < kRadix) sm.hscan[tid] = hs;
-  __syncthreads();
-  const uint32_t t = sm.tile;
-  const int64_t base = (int64_t)t * kSortTile;
-  const int64_t wbase = base + (int64_t)warp * 32 * kSortItems;
-
-  uint32_t k[kSortItems], v[kSortItems], r[kSortItems];
-#pragma unroll
-  for (int i = 0; i < kSortItems; ++i) {
-    const int64_t idx = wbase + i * 32 + lane;
-    const bool ok = idx < n;
-    k[i] = ok ? kin[idx] : 0u;
-    v[i] = ok ? vin[idx] : 0u;
-  }
-  const unsigned lt = (1u << lane) - 1u;
-#pragma unroll
-  for (int i = 0; i < kSortItems; ++i) {
-    const int64_t idx = wbase + i * 32 + lane;
-    const uint32_t d = idx < n ? (k[i] >> shift) & (kRadix - 1) : (uint32_t)kRadix;
-    const unsigned peers = __match_any_sync(kFull, d);
-    const int leader = __ffs(peers) - 1;
-    uint32_t old = 0;
-    if (lane == leader && d < (uint32_t)kRadix) {
-      old = sm.whist[warp][d];
-      sm.whist[warp][d] = old + __popc(peers);
-    }
-    old = __shfl_sync(kFull, old, leader);
-    r[i] = old + __popc(peers & lt);
-  }
-  __syncthreads();
-
-  uint32_t cnt = 0;
-  if (tid < kRadix) {
-    for (int w = 0; w < kSortWarps; ++w) {
-      const uint32_t c = sm.whist[w][tid];
-      sm.whist[w][tid] = cnt;
-      cnt += c;
-    }
-    volatile uint32_t* mine = lookback + (int64_t)t * kRadix + tid;
-    *mine = (t == 0 ? kFlagInc : kFlagAgg) | cnt;
-  }
-  const uint32_t ds = scan256(cnt, sm.wsum);
-  if (tid < kRadix) {
-    sm.dstart[tid] = ds;
-    uint32_t excl = 0;
-    if (t > 0) {
-      int64_t j = (int64_t)t - 1;
-      int spins = 0;
-      while (j >= 0) {
-        const uint32_t w = *(volatile const uint32_t*)(lookback + j * kRadix + tid);
-        const uint32_t flag = w & ~kCountMask;
-        if (flag == 0u) {
-          if (++spins > kSpinLimit) {
-            latch(status, EMB_ERR_TIMEOUT);
-            break;
-          }
-          __nanosleep(32);
-          continue;
-        }
-        excl += w & kCountMask;
-        if (flag == kFlagInc) break;
-        --j;
-      }
-      *(volatile uint32_t*)(lookback + (int64_t)t * kRadix + tid) = kFlagInc | ((excl + cnt) & kCountMask);
-    }
-    sm.goff[tid] = sm.hscan[tid] + excl;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int i = 0; i < kSortItems; ++i) {
-    const int64_t idx = wbase + i * 32 + lane;
-    if (idx < n) {
-      const uint32_t d = (k[i] >> shift) & (kRadix - 1);
-      const uint32_t pos = sm.dstart[d] + sm.whist[warp][d] + r[i];
-      sm.keys[pos] = k[i];
-      sm.vals[pos] = v[i];
-    }
-  }
-  __syncthreads();
-  const int tile_n = (int)(n - base < kSortTile ? n - base : kSortTile);
-  for (int j = tid; j < tile_n; j += kSortThreads) {
-    const uint32_t key = sm.keys[j];
-    const uint32_t d = (key >> shift) & (kRadix - 1);
-    const uint32_t o = sm.goff[d] + (j - sm.dstart[d]);
-    if (o < (uint64_t)n) {   // always true unless a look-back wait gave up
-      kout[o] = key;
-      vout[o] = sm.vals[j];
-    }
-  }
-}
 
 // ---------------------------------------------------------------------------
 // run ranks (debug outputs only): rank[i] = number of run heads before i
@@ -598,28 +444,12 @@ emb_status launch_backward(emb_plan_s* p, const float* grad_out, const float* gr
     return EMB_OK;
   }
   const int passes = (p->key_bits + kRadixBits - 1) / kRadixBits;
-  const int64_t tiles = (n + kSortTile - 1) / kSortTile;
-  const size_t sort_words = 4 * kRadix + 4 + (size_t)passes * tiles * kRadix;
-  EMB_CUDA_TRY(cudaMemsetAsync(w.hist, 0, sort_words * sizeof(uint32_t), stream));
-  {
-    const int grid = (int)std::min<int64_t>((n + 511) / 512, (int64_t)p->sm_count * 4);
-    k_digit_hist<<<grid, 512, 0, stream>>>(w.keys[0], n, passes, w.hist);
-  }
-  static bool attr_set = false;
-  if (!attr_set) {
-    EMB_CUDA_TRY(cudaFuncSetAttribute(k_onesweep, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)sizeof(SortSmem)));
-    attr_set = true;
-  }
-  for (int ps = 0; ps < passes; ++ps) {
-    const int in = ps & 1, out = in ^ 1;
-    k_onesweep<<<(unsigned)tiles, kSortThreads, sizeof(SortSmem), stream>>>(
-        w.keys[in], w.vals[in], w.keys[out], w.vals[out], n, ps * kRadixBits, w.hist + ps * kRadix,
-        w.lookback + (size_t)ps * tiles * kRadix, w.tile_ctr + ps, p->status_d);
-  }
-  EMB_CUDA_TRY(cudaGetLastError());
-  const uint32_t* skeys = w.keys[passes & 1];
-  const uint32_t* svals = w.vals[passes & 1];
+  int res = 0;
+  emb_status st = radix_sort_pairs<uint32_t>(w.keys, w.vals, n, nullptr, n, passes, w.hist, p->sm_count,
+                                             p->status_d, stream, &res);
+  if (st != EMB_OK) return st;
+  const uint32_t* skeys = w.keys[res];
+  const uint32_t* svals = w.vals[res];
 
   SegArgs a{};
   a.keys = skeys;
@@ -686,7 +516,7 @@ constexpr int64_t kNoAllocMaxN = int64_t(1) << 18;   // contributions per call
 constexpr int kNoAllocMaxDim = 256;
 constexpr int64_t kNoAllocTiles = (kNoAllocMaxN + kSortTile - 1) / kSortTile;
 constexpr int64_t kNoAllocBlocks = (kNoAllocMaxN + kSegWarps * kUnit - 1) / (kSegWarps * kUnit);
-constexpr size_t kNoAllocSortWords = 4 * kRadix + 4 + 4 * kNoAllocTiles * kRadix;
+constexpr size_t kNoAllocSortWords = 4 * kRadix + 4 + 4 * kNoAllocTiles * kRadix;  // sort_scratch_words(4, max n)
 
 struct NoAllocScratch {
   uint32_t keys[2][kNoAllocMaxN];
@@ -734,10 +564,12 @@ __global__ void k_noalloc_pairs(const int64_t* __restrict__ rows, int64_t n, int
 namespace {
 constexpr int kNoAllocMaxDevices = 64;
 void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+int g_noalloc_sms[kNoAllocMaxDevices] = {};
 
-// Device address of the scratch area on the current device, looked up once
-// per device (the first call on a device does this set-up).
-emb_status noalloc_scratch(NoAllocScratch** out) {
+// Device address of the scratch area on the current device (and its SM
+// count), looked up once per device: the first call on a device does this
+// set-up.
+emb_status noalloc_scratch(NoAllocScratch** out, int* sms) {
   int dev = 0;
   EMB_CUDA_TRY(cudaGetDevice(&dev));
   if (dev < 0 || dev >= kNoAllocMaxDevices) return EMB_ERR_UNSUPPORTED;
@@ -748,9 +580,13 @@ emb_status noalloc_scratch(NoAllocScratch** out) {
       cudaGetLastError();
       return EMB_ERR_CUDA;
     }
+    int count = 0;
+    EMB_CUDA_TRY(cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev));
+    g_noalloc_sms[dev] = count > 0 ? count : 1;
     g_noalloc_addr[dev] = ptr;
   }
   *out = static_cast<NoAllocScratch*>(g_noalloc_addr[dev]);
+  *sms = g_noalloc_sms[dev];
   return EMB_OK;
 }
 }  // namespace
@@ -767,7 +603,8 @@ extern "C" emb_status emb_sparse_adagrad_noalloc(const int64_t* rows, int64_t n,
   if (n > 0 && (!rows || !grads || !aligned16(grads))) return EMB_ERR_INVALID_ARG;
   if (!(lr == lr) || !(eps == eps)) return EMB_ERR_INVALID_ARG;
   NoAllocScratch* s = nullptr;
-  emb_status st = noalloc_scratch(&s);
+  int sms = 1;
+  emb_status st = noalloc_scratch(&s, &sms);
   if (st != EMB_OK) return st;
   if (n == 0) return EMB_OK;
   cudaStream_t stream = (cudaStream_t)stream_;
@@ -775,27 +612,17 @@ extern "C" emb_status emb_sparse_adagrad_noalloc(const int64_t* rows, int64_t n,
   int key_bits = 1;
   while (key_bits < 32 && (uint64_t(1) << key_bits) <= (uint64_t)num_rows) ++key_bits;
   const int passes = (key_bits + kRadixBits - 1) / kRadixBits;
-  const int64_t tiles = (n + kSortTile - 1) / kSortTile;
-  uint32_t* hist = s->sortw;
-  uint32_t* tile_ctr = hist + 4 * kRadix;
-  uint32_t* lookback = tile_ctr + 4;
-  // the area keeps the previous call's contents: clear what must start at zero
-  EMB_CUDA_TRY(cudaMemsetAsync(hist, 0, (4 * kRadix + 4 + (size_t)passes * tiles * kRadix) * sizeof(uint32_t),
-                               stream));
   k_noalloc_setup<<<1, 32, 0, stream>>>(s, weight, acc, num_rows, dim);
   k_noalloc_pairs<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(rows, n, num_rows, s->keys[0], s->vals[0]);
-  k_digit_hist<<<(unsigned)std::min<int64_t>((n + 511) / 512, 256), 512, 0, stream>>>(s->keys[0], n, passes, hist);
-  EMB_CUDA_TRY(cudaFuncSetAttribute(k_onesweep, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)sizeof(SortSmem)));
-  for (int ps = 0; ps < passes; ++ps) {
-    const int in = ps & 1, out = in ^ 1;
-    k_onesweep<<<(unsigned)tiles, kSortThreads, sizeof(SortSmem), stream>>>(
-        s->keys[in], s->vals[in], s->keys[out], s->vals[out], n, ps * kRadixBits, hist + ps * kRadix,
-        lookback + (size_t)ps * tiles * kRadix, tile_ctr + ps, nullptr);
-  }
+  uint32_t* const nk[2] = {s->keys[0], s->keys[1]};
+  uint32_t* const nv[2] = {s->vals[0], s->vals[1]};
+  int res = 0;
+  // the sort clears its part of the area (histograms, tickets, look-back words) itself
+  st = radix_sort_pairs<uint32_t>(nk, nv, n, nullptr, n, passes, s->sortw, sms, nullptr, stream, &res);
+  if (st != EMB_OK) return st;
   SegArgs a{};
-  a.keys = s->keys[passes & 1];
-  a.vals = s->vals[passes & 1];
+  a.keys = s->keys[res];
+  a.vals = s->vals[res];
   a.n = n;
   a.sentinel = (uint32_t)num_rows;
   a.colg = &s->colg;

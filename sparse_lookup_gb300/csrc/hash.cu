@@ -1,15 +1,560 @@
-// hash.cu -- K-H: the collision-free dynamic table (Monolith §2.1 "Tabel Hash").
-#include "common.cuh"
+// hash.cu -- K-H: the collision-free dynamic table (Monolith §2.1 "Tabel
+// Hash": distinct IDs never share an embedding; an ID enters the table only
+// once it has been seen often enough; IDs idle for longer than a set period
+// expire).
+//
+// The page's table is a cuckoo map on a CPU parameter server.  On one GPU the
+// same contract -- distinct (table id, key) pairs never share an entry or a
+// row -- is kept by an open-addressing table with linear probing in HBM:
+//   slot (16 B) = key (tid << 48 | key), state, last_seen
+//   state >= 0: the admitted key's row; state < 0: still counting, with
+//   count = -1 - state.
+// An insert claims a slot with a compare-and-swap only after its probe has
+// reached an EMPTY slot (so the key is known to be absent), taking the first
+// tombstone or EMPTY slot on its path; threads inserting the same key meet at
+// the same slot.  Expired entries become tombstones that probes step over and
+// inserts reuse; the expiry sweep also turns tombstone runs that end at an
+// EMPTY slot back into EMPTY slots.
+//
+//   K-H1 k_hash_probe  one thread per occurrence: find or insert the key
+//                      (bounded probing), touch last_seen, count; the one
+//                      occurrence whose count reaches the threshold lists the
+//                      key for admission.
+//   K-H2 admission     the listed keys are radix-sorted by (tid, key); the
+//                      i-th key takes the i-th free row of the pool (a bitmap
+//                      of used rows, scanned per word), which is the same as
+//                      "rows released by expiry in ascending order, then rows
+//                      never used"; its weights are initialised from its key.
+//        k_hash_fix    occurrences of keys admitted in this call get the row.
+//   K-H3 k_hash_evict  one sweep over the slots removes entries idle > ttl
+//                      and releases their rows.
+#include <algorithm>
+#include <new>
 
-extern "C" emb_status hash_create(int64_t, int64_t, int32_t, int32_t, int32_t, uint64_t, float, emb_hash* out) {
-  if (out) *out = nullptr;
-  return EMB_ERR_UNSUPPORTED;
+#include "plan.cuh"
+#include "radix.cuh"
+
+namespace emb {
+
+constexpr unsigned long long kEmptyKey = ~0ull;
+constexpr unsigned long long kTombKey = ~0ull - 1ull;
+constexpr int kTidBits = 15;
+constexpr int kKeyBits = 48;
+constexpr int kHashPasses = 8;   // 63-bit packed keys, 8-bit digits
+
+struct __align__(16) Slot {
+  unsigned long long key;
+  int32_t state;        // low half of the second 8-byte word
+  uint32_t last_seen;   // high half: (state, last_seen) change together by CAS
+};
+static_assert(sizeof(Slot) == 16, "slot layout");
+
+}  // namespace emb
+
+struct emb_hash_s {
+  int64_t num_slots = 0;
+  int64_t cap = 0;
+  int64_t max_keys = 0;
+  int32_t dim = 0;
+  int32_t thr = 0;
+  int32_t max_probes = 0;
+  uint64_t seed = 0;
+  float init_scale = 0.f;
+  emb::Slot* slots = nullptr;
+  float* W = nullptr;
+  float* acc = nullptr;
+  uint32_t* used = nullptr;        // bitmap of rows in use, bits past cap set
+  int64_t n_words = 0;
+  uint32_t* free_scan = nullptr;   // [n_words + 1] exclusive prefix of free rows per word
+  uint32_t* scan_part = nullptr;   // per 1024-word block partials
+  uint64_t* nkeys[2] = {nullptr, nullptr};
+  uint32_t* nvals[2] = {nullptr, nullptr};
+  uint32_t* counters = nullptr;    // [0] listed keys, [1] exported entries
+  uint32_t* sort_scratch = nullptr;
+  uint32_t* status = nullptr;
+  int sm_count = 0;
+};
+
+namespace emb {
+
+struct HashArgs {
+  Slot* slots;
+  uint64_t mask;
+  int32_t max_probes;
+  int32_t thr;
+  uint32_t* n_new;
+  uint64_t* nkeys;
+  uint32_t* nvals;
+  int64_t max_keys;
+  uint32_t* status;
+};
+
+__device__ __forceinline__ uint64_t home_slot(uint64_t fkey, uint64_t mask) {
+  return splitmix64(fkey ^ 0x5851F42D4C957F2Dull) & mask;
 }
-extern "C" emb_status hash_rows(emb_hash, float**, float**) { return EMB_ERR_UNSUPPORTED; }
-extern "C" emb_status hash_lookup_or_insert(emb_hash, const int32_t*, const int64_t*, int64_t, uint32_t,
-                                            int64_t*, void*) { return EMB_ERR_UNSUPPORTED; }
-extern "C" emb_status hash_evict_expired(emb_hash, uint32_t, uint32_t, void*, int64_t*) { return EMB_ERR_UNSUPPORTED; }
-extern "C" emb_status hash_export(emb_hash, int32_t*, int64_t*, int64_t*, int32_t*, uint32_t*, int64_t, int64_t*,
-                                  void*) { return EMB_ERR_UNSUPPORTED; }
-extern "C" emb_status hash_get_device_status(emb_hash, void*) { return EMB_ERR_UNSUPPORTED; }
-extern "C" emb_status hash_destroy(emb_hash) { return EMB_ERR_UNSUPPORTED; }
+
+// K-H1
+__global__ void __launch_bounds__(256) k_hash_probe(const HashArgs h, const int32_t* __restrict__ tids,
+                                                    const int64_t* __restrict__ keys, int64_t n, uint32_t step,
+                                                    int64_t* __restrict__ rows_out) {
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int32_t tid = tids[i];
+  const int64_t key = keys[i];
+  if (tid < 0 || tid >= (1 << kTidBits) || key < 0 || key >= (int64_t(1) << kKeyBits)) {
+    latch(h.status, EMB_ERR_INVALID_ARG);
+    rows_out[i] = -1;
+    return;
+  }
+  const unsigned long long fkey = ((unsigned long long)tid << kKeyBits) | (unsigned long long)key;
+  // Probe from the home slot until the key or an EMPTY slot turns up (the
+  // EMPTY slot proves the key is absent), remembering the first slot that
+  // could take it (a tombstone or that EMPTY slot); claim that slot by CAS on
+  // the value seen there.  If another key took it first, keep probing after
+  // it.  Within one call slots only change from EMPTY/tombstone to a key, and
+  // every thread inserting the same key walks the same path, so they all end
+  // at the one slot the first of them claimed.
+  uint64_t start = home_slot(fkey, h.mask);
+  int64_t found = -1;
+  int budget = h.max_probes;
+  while (budget > 0 && found < 0) {
+    uint64_t pos = start;
+    int64_t avail = -1;
+    unsigned long long avail_val = 0;
+    bool seen_empty = false;
+    while (budget > 0) {
+      const unsigned long long k = *(volatile unsigned long long*)&h.slots[pos].key;
+      --budget;
+      if (k == fkey) {
+        found = (int64_t)pos;
+        break;
+      }
+      if (k == kEmptyKey) {
+        if (avail < 0) {
+          avail = (int64_t)pos;
+          avail_val = kEmptyKey;
+        }
+        seen_empty = true;
+        break;
+      }
+      if (k == kTombKey && avail < 0) {
+        avail = (int64_t)pos;
+        avail_val = kTombKey;
+      }
+      pos = (pos + 1) & h.mask;
+    }
+    if (found >= 0 || !seen_empty) break;
+    const unsigned long long old = atomicCAS(&h.slots[avail].key, avail_val, fkey);
+    if (old == avail_val || old == fkey) {
+      found = avail;
+      break;
+    }
+    start = ((uint64_t)avail + 1) & h.mask;
+  }
+  if (found < 0) {
+    latch(h.status, EMB_ERR_PROBE_LIMIT);
+    rows_out[i] = -1;
+    return;
+  }
+  Slot* s = &h.slots[found];
+  const int32_t state = *(volatile int32_t*)&s->state;
+  if (state >= 0) {
+    if (*(volatile uint32_t*)&s->last_seen != step) s->last_seen = step;
+    rows_out[i] = state;
+    return;
+  }
+  // count and touch in ONE atomic update of (state, last_seen), so that "first
+  // occurrence of this call" and "count reached the threshold" are decided on
+  // the same order of updates
+  unsigned long long* sw = reinterpret_cast<unsigned long long*>(&s->state);
+  unsigned long long cur = *(volatile unsigned long long*)sw, prev;
+  int32_t old;
+  do {
+    prev = cur;
+    old = (int32_t)(uint32_t)(prev & 0xffffffffull);
+    if (old >= 0) break;   // admitted meanwhile (not within one call; kept for safety)
+    const unsigned long long nxt = ((unsigned long long)step << 32) | (uint32_t)(old - 1);
+    cur = atomicCAS(sw, prev, nxt);
+  } while (cur != prev);
+  if (old >= 0) {
+    rows_out[i] = old;
+    return;
+  }
+  const uint32_t old_seen = (uint32_t)(prev >> 32);
+  const int32_t count_old = -1 - old, count_new = count_old + 1;
+  // the occurrence that reaches the threshold lists the key; a key left
+  // without a row by a full pool is listed again by its first occurrence
+  if (count_new >= h.thr && (count_old < h.thr || old_seen != step)) {
+    const uint32_t idx = atomicAdd(h.n_new, 1u);
+    if ((int64_t)idx < h.max_keys) {
+      h.nkeys[idx] = fkey;
+      h.nvals[idx] = (uint32_t)found;
+    }
+  }
+  rows_out[i] = -2 - found;
+}
+
+// free rows per word of the used-row bitmap, exclusive prefix over words
+constexpr int kScanBlk = 1024;
+
+__global__ void __launch_bounds__(kScanBlk) k_free_reduce(const uint32_t* used, int64_t nw, uint32_t* part) {
+  const int64_t w = blockIdx.x * (int64_t)kScanBlk + threadIdx.x;
+  const uint32_t f = w < nw ? (uint32_t)__popc(~used[w]) : 0u;
+  uint32_t s = f;
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+  __shared__ uint32_t ws[32];
+  if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t t = 0;
+    for (int j = 0; j < kScanBlk / 32; ++j) t += ws[j];
+    part[blockIdx.x] = t;
+  }
+}
+
+__global__ void __launch_bounds__(kScanBlk) k_scan_parts(uint32_t* part, int nb) {
+  __shared__ uint32_t wsum[32];
+  __shared__ uint32_t carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int b0 = 0; b0 < nb; b0 += kScanBlk) {
+    const int i = b0 + threadIdx.x;
+    const uint32_t v = i < nb ? part[i] : 0u;
+    uint32_t x = v;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(kFull, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    uint32_t base = carry, tot = 0;
+    for (int w = 0; w < 32; ++w) {
+      if (w < warp) base += wsum[w];
+      tot += wsum[w];
+    }
+    if (i < nb) part[i] = base + x - v;
+    __syncthreads();
+    if (threadIdx.x == 0) carry += tot;
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(kScanBlk) k_free_down(const uint32_t* used, int64_t nw, const uint32_t* part,
+                                                        uint32_t* free_scan) {
+  __shared__ uint32_t wsum[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t w = blockIdx.x * (int64_t)kScanBlk + threadIdx.x;
+  const uint32_t f = w < nw ? (uint32_t)__popc(~used[w]) : 0u;
+  uint32_t x = f;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  uint32_t base = part[blockIdx.x];
+  for (int j = 0; j < warp; ++j) base += wsum[j];
+  if (w < nw) free_scan[w] = base + x - f;
+  if (w == nw - 1) free_scan[nw] = base + x;
+}
+
+__device__ __forceinline__ float init_value(uint64_t fkey, uint64_t seed, int d, float scale) {
+  const uint64_t hsh = splitmix64(fkey ^ seed ^ (uint64_t)(uint32_t)d);
+  const int32_t v = (int32_t)(hsh >> 40) - 8388608;
+  const float f = __fmul_rn((float)v, 1.0f / 8388608.0f);
+  return __fmul_rn(f, scale);
+}
+
+// K-H2: the i-th listed key (ascending) takes the i-th free row.  The bitmap
+// is only read here (every warp sees the same snapshot); k_hash_mark sets the
+// bits of the rows handed out afterwards.
+__global__ void __launch_bounds__(256) k_hash_admit(Slot* slots, const uint64_t* __restrict__ skeys,
+                                                    const uint32_t* __restrict__ svals, const uint32_t* n_new,
+                                                    int64_t max_keys, uint32_t* used, const uint32_t* free_scan,
+                                                    int64_t nw, float* W, float* A, int dim, uint64_t seed,
+                                                    float scale, uint32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t nn = ((int64_t)*n_new < max_keys) ? (int64_t)*n_new : max_keys;
+  const uint32_t total_free = free_scan[nw];
+  for (int64_t i = warp; i < nn; i += nwarps) {
+    if (i >= (int64_t)total_free) {
+      if (lane == 0) latch(status, EMB_ERR_TABLE_FULL);
+      continue;
+    }
+    // word holding the i-th free row: last w with free_scan[w] <= i
+    int64_t lo = 0, hi = nw;   // free_scan[lo] <= i < free_scan[hi]
+    while (hi - lo > 1) {
+      const int64_t mid = (lo + hi) >> 1;
+      if (free_scan[mid] <= (uint32_t)i) lo = mid; else hi = mid;
+    }
+    uint32_t freebits = ~used[lo];
+    for (uint32_t r = (uint32_t)i - free_scan[lo]; r > 0; --r) freebits &= freebits - 1u;
+    const int bit = __ffs(freebits) - 1;
+    const int64_t row = lo * 32 + bit;
+    const uint64_t fkey = skeys[i];
+    if (lane == 0) slots[svals[i]].state = (int32_t)row;
+    for (int d = lane; d < dim; d += 32) {
+      W[row * dim + d] = init_value(fkey, seed, d, scale);
+      A[row * dim + d] = 0.0f;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) k_hash_mark(const Slot* slots, const uint32_t* __restrict__ svals,
+                                                   const uint32_t* n_new, int64_t max_keys, uint32_t* used) {
+  const int64_t nn = ((int64_t)*n_new < max_keys) ? (int64_t)*n_new : max_keys;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nn; i += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t st = slots[svals[i]].state;
+    if (st >= 0) atomicOr(&used[st >> 5], 1u << (st & 31));
+  }
+}
+
+__global__ void __launch_bounds__(256) k_hash_fix(const Slot* slots, int64_t n, int64_t* rows_out) {
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int64_t v = rows_out[i];
+  if (v <= -2) {
+    const int32_t st = slots[-2 - v].state;
+    rows_out[i] = st >= 0 ? st : -1;
+  }
+}
+
+// K-H3.  Tombstones are cleared where that is safe: a run of tombstones
+// directly before an EMPTY slot lies on no live key's probe path (such a path
+// would have to cross the EMPTY slot), so the run may become EMPTY again.
+// Slots emptied by other threads during the sweep only leave tombstones
+// behind, never a broken path.
+constexpr int kTombWalk = 4096;
+
+__global__ void __launch_bounds__(256) k_hash_evict(Slot* slots, int64_t ns, uint32_t now, uint32_t ttl,
+                                                    uint32_t* used, unsigned long long* n_evicted) {
+  unsigned long long cnt = 0;
+  const uint64_t mask = (uint64_t)ns - 1;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < ns; i += (int64_t)gridDim.x * blockDim.x) {
+    const unsigned long long k = *(volatile unsigned long long*)&slots[i].key;
+    if (k == kEmptyKey) {
+      uint64_t j = ((uint64_t)i - 1) & mask;
+      for (int w = 0; w < kTombWalk; ++w, j = (j - 1) & mask) {
+        if (*(volatile unsigned long long*)&slots[j].key != kTombKey) break;
+        slots[j].key = kEmptyKey;
+      }
+      continue;
+    }
+    if (k == kTombKey) continue;
+    const uint32_t ls = slots[i].last_seen;
+    if ((int64_t)now - (int64_t)ls > (int64_t)ttl) {
+      const int32_t st = slots[i].state;
+      if (st >= 0) atomicAnd(&used[st >> 5], ~(1u << (st & 31)));
+      slots[i].state = -1;
+      *(volatile unsigned long long*)&slots[i].key = kTombKey;
+      ++cnt;
+    }
+  }
+  if (n_evicted) {
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(kFull, cnt, o);
+    if ((threadIdx.x & 31) == 0 && cnt) atomicAdd(n_evicted, cnt);
+  }
+}
+
+__global__ void k_hash_init(Slot* slots, int64_t ns, uint32_t* used, int64_t nw, int64_t cap) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < ns; i += (int64_t)gridDim.x * blockDim.x) {
+    slots[i].key = kEmptyKey;
+    slots[i].state = -1;
+    slots[i].last_seen = 0;
+  }
+  for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < nw; w += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t first = w * 32;
+    uint32_t bits = 0;
+    for (int b = 0; b < 32; ++b)
+      if (first + b >= cap) bits |= 1u << b;   // rows past the pool are never free
+    used[w] = bits;
+  }
+}
+
+__global__ void k_hash_export(const Slot* slots, int64_t ns, int32_t* tids, int64_t* keys, int64_t* rows,
+                              int32_t* counts, uint32_t* last_seen, int64_t cap, uint32_t* ctr) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < ns; i += (int64_t)gridDim.x * blockDim.x) {
+    const unsigned long long k = slots[i].key;
+    if (k == kEmptyKey || k == kTombKey) continue;
+    const uint32_t idx = atomicAdd(ctr, 1u);
+    if ((int64_t)idx >= cap) continue;
+    const int32_t st = slots[i].state;
+    if (tids) tids[idx] = (int32_t)(k >> kKeyBits);
+    if (keys) keys[idx] = (int64_t)(k & ((1ull << kKeyBits) - 1));
+    if (rows) rows[idx] = st >= 0 ? st : -1;
+    if (counts) counts[idx] = st >= 0 ? -1 : -1 - st;
+    if (last_seen) last_seen[idx] = slots[i].last_seen;
+  }
+}
+
+}  // namespace emb
+
+using namespace emb;
+
+namespace {
+
+void free_hash(emb_hash_s* h) {
+  if (!h) return;
+  cudaFree(h->slots);
+  cudaFree(h->W);
+  cudaFree(h->acc);
+  cudaFree(h->used);
+  cudaFree(h->free_scan);
+  cudaFree(h->scan_part);
+  cudaFree(h->nkeys[0]);
+  cudaFree(h->nkeys[1]);
+  cudaFree(h->nvals[0]);
+  cudaFree(h->nvals[1]);
+  cudaFree(h->counters);
+  cudaFree(h->sort_scratch);
+  cudaFree(h->status);
+  delete h;
+}
+
+}  // namespace
+
+extern "C" emb_status hash_create(int64_t num_slots, int64_t row_capacity, int32_t dim, int32_t admit_threshold,
+                                  int32_t max_probes, uint64_t init_seed, float init_scale,
+                                  int64_t max_keys_per_call, emb_hash* out) {
+  if (!out) return EMB_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (num_slots < 1024 || (num_slots & (num_slots - 1)) != 0) return EMB_ERR_INVALID_ARG;
+  if (num_slots > (int64_t(1) << 31)) return EMB_ERR_UNSUPPORTED;
+  if (row_capacity < 1 || row_capacity >= (int64_t(1) << 31)) return EMB_ERR_INVALID_ARG;
+  if (dim < 4 || dim % 4 != 0 || dim > 256) return EMB_ERR_INVALID_ARG;
+  if (admit_threshold < 1 || max_probes < 1) return EMB_ERR_INVALID_ARG;
+  if (max_keys_per_call < 1 || max_keys_per_call >= (int64_t(1) << 30)) return EMB_ERR_INVALID_ARG;
+  if (!(init_scale == init_scale)) return EMB_ERR_INVALID_ARG;
+  emb_hash_s* h = new (std::nothrow) emb_hash_s();
+  if (!h) return EMB_ERR_OOM;
+  h->num_slots = num_slots;
+  h->cap = row_capacity;
+  h->max_keys = max_keys_per_call;
+  h->dim = dim;
+  h->thr = admit_threshold;
+  h->max_probes = max_probes;
+  h->seed = init_seed;
+  h->init_scale = init_scale;
+  h->n_words = (row_capacity + 31) / 32;
+  cudaError_t e = cudaSuccess;
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, dev);
+  auto alloc = [&](auto** p, size_t bytes) {
+    if (e == cudaSuccess) e = cudaMalloc((void**)p, bytes > 0 ? bytes : 1);
+  };
+  alloc(&h->slots, sizeof(Slot) * (size_t)num_slots);
+  alloc(&h->W, sizeof(float) * (size_t)row_capacity * dim);
+  alloc(&h->acc, sizeof(float) * (size_t)row_capacity * dim);
+  alloc(&h->used, sizeof(uint32_t) * (size_t)h->n_words);
+  alloc(&h->free_scan, sizeof(uint32_t) * (size_t)(h->n_words + 1));
+  alloc(&h->scan_part, sizeof(uint32_t) * (size_t)((h->n_words + kScanBlk - 1) / kScanBlk + 1));
+  for (int i = 0; i < 2; ++i) {
+    alloc(&h->nkeys[i], sizeof(uint64_t) * (size_t)max_keys_per_call);
+    alloc(&h->nvals[i], sizeof(uint32_t) * (size_t)max_keys_per_call);
+  }
+  alloc(&h->counters, sizeof(uint32_t) * 4);
+  alloc(&h->sort_scratch, sizeof(uint32_t) * sort_scratch_words<uint64_t>(kHashPasses, max_keys_per_call));
+  alloc(&h->status, sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMemset(h->W, 0, sizeof(float) * (size_t)row_capacity * dim);
+  if (e == cudaSuccess) e = cudaMemset(h->acc, 0, sizeof(float) * (size_t)row_capacity * dim);
+  if (e == cudaSuccess) e = cudaMemset(h->status, 0, sizeof(uint32_t));
+  if (e == cudaSuccess) {
+    k_hash_init<<<h->sm_count * 8, 256>>>(h->slots, num_slots, h->used, h->n_words, row_capacity);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    free_hash(h);
+    cudaGetLastError();
+    return cuda_status(e);
+  }
+  *out = h;
+  return EMB_OK;
+}
+
+extern "C" emb_status hash_rows(emb_hash h, float** weight, float** acc) {
+  if (!h) return EMB_ERR_INVALID_ARG;
+  if (weight) *weight = h->W;
+  if (acc) *acc = h->acc;
+  return EMB_OK;
+}
+
+extern "C" emb_status hash_lookup_or_insert(emb_hash h, const int32_t* table_ids, const int64_t* keys, int64_t n,
+                                            uint32_t step, int64_t* rows_out, void* stream_) {
+  if (!h || n < 0) return EMB_ERR_INVALID_ARG;
+  if (n > h->max_keys) return EMB_ERR_UNSUPPORTED;
+  if (n == 0) return EMB_OK;
+  if (!table_ids || !keys || !rows_out) return EMB_ERR_INVALID_ARG;
+  cudaStream_t stream = (cudaStream_t)stream_;
+  HashArgs a{};
+  a.slots = h->slots;
+  a.mask = (uint64_t)h->num_slots - 1;
+  a.max_probes = h->max_probes;
+  a.thr = h->thr;
+  a.n_new = h->counters;
+  a.nkeys = h->nkeys[0];
+  a.nvals = h->nvals[0];
+  a.max_keys = h->max_keys;
+  a.status = h->status;
+  EMB_CUDA_TRY(cudaMemsetAsync(h->counters, 0, sizeof(uint32_t), stream));
+  k_hash_probe<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(a, table_ids, keys, n, step, rows_out);
+  int res = 0;
+  emb_status st = radix_sort_pairs<uint64_t>(h->nkeys, h->nvals, 0, h->counters, n, kHashPasses, h->sort_scratch,
+                                             h->sm_count, h->status, stream, &res);
+  if (st != EMB_OK) return st;
+  const int nb = (int)((h->n_words + kScanBlk - 1) / kScanBlk);
+  k_free_reduce<<<nb, kScanBlk, 0, stream>>>(h->used, h->n_words, h->scan_part);
+  k_scan_parts<<<1, kScanBlk, 0, stream>>>(h->scan_part, nb);
+  k_free_down<<<nb, kScanBlk, 0, stream>>>(h->used, h->n_words, h->scan_part, h->free_scan);
+  k_hash_admit<<<h->sm_count * 4, 256, 0, stream>>>(h->slots, h->nkeys[res], h->nvals[res], h->counters,
+                                                     h->max_keys, h->used, h->free_scan, h->n_words, h->W, h->acc,
+                                                     h->dim, h->seed, h->init_scale, h->status);
+  k_hash_mark<<<h->sm_count * 2, 256, 0, stream>>>(h->slots, h->nvals[res], h->counters, h->max_keys, h->used);
+  k_hash_fix<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(h->slots, n, rows_out);
+  return cuda_status(cudaGetLastError());
+}
+
+extern "C" emb_status hash_evict_expired(emb_hash h, uint32_t now, uint32_t ttl, void* stream_,
+                                         int64_t* n_evicted_dev) {
+  if (!h) return EMB_ERR_INVALID_ARG;
+  cudaStream_t stream = (cudaStream_t)stream_;
+  if (n_evicted_dev) EMB_CUDA_TRY(cudaMemsetAsync(n_evicted_dev, 0, sizeof(int64_t), stream));
+  k_hash_evict<<<h->sm_count * 8, 256, 0, stream>>>(h->slots, h->num_slots, now, ttl, h->used,
+                                                     reinterpret_cast<unsigned long long*>(n_evicted_dev));
+  return cuda_status(cudaGetLastError());
+}
+
+extern "C" emb_status hash_export(emb_hash h, int32_t* tids, int64_t* keys, int64_t* rows, int32_t* counts,
+                                  uint32_t* last_seen, int64_t cap, int64_t* n_out, void* stream_) {
+  if (!h || !n_out || cap < 0) return EMB_ERR_INVALID_ARG;
+  cudaStream_t stream = (cudaStream_t)stream_;
+  EMB_CUDA_TRY(cudaMemsetAsync(h->counters + 1, 0, sizeof(uint32_t), stream));
+  k_hash_export<<<h->sm_count * 8, 256, 0, stream>>>(h->slots, h->num_slots, tids, keys, rows, counts, last_seen,
+                                                      cap, h->counters + 1);
+  EMB_CUDA_TRY(cudaGetLastError());
+  uint32_t cnt = 0;
+  EMB_CUDA_TRY(cudaMemcpyAsync(&cnt, h->counters + 1, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream));
+  EMB_CUDA_TRY(cudaStreamSynchronize(stream));
+  *n_out = cnt;
+  return EMB_OK;
+}
+
+extern "C" emb_status hash_get_device_status(emb_hash h, void* stream) {
+  if (!h) return EMB_ERR_INVALID_ARG;
+  uint32_t st = 0;
+  EMB_CUDA_TRY(cudaStreamSynchronize((cudaStream_t)stream));
+  EMB_CUDA_TRY(cudaMemcpy(&st, h->status, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+  EMB_CUDA_TRY(cudaMemset(h->status, 0, sizeof(uint32_t)));
+  return (emb_status)st;
+}
+
+extern "C" emb_status hash_destroy(emb_hash h) {
+  if (!h) return EMB_ERR_INVALID_ARG;
+  cudaDeviceSynchronize();
+  free_hash(h);
+  return EMB_OK;
+}

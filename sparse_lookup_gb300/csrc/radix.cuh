@@ -1,0 +1,232 @@
+// radix.cuh -- stable LSD radix sort of (key, u32 value) pairs, one 8-bit
+// digit per pass: a single read of the keys builds the digit histograms of all
+// passes, then each pass is one chained-scan scatter kernel in which a CTA
+// ranks its tile in shared memory, publishes its per-digit counts and finds
+// its global offsets by decoupled look-back over the earlier tiles (Adinets &
+// Merrill, "Onesweep: a faster least significant digit radix sort for GPUs",
+// 2022).  Tiles are taken in launch order from a ticket counter, so a CTA
+// only ever waits on CTAs that are already running; every wait is bounded and
+// latches EMB_ERR_TIMEOUT instead of hanging.
+//
+// The element count may live in device memory (n_dev != nullptr): grids are
+// then sized for the capacity and tiles past the count do nothing.
+#pragma once
+
+#include "plan.cuh"
+
+namespace emb {
+
+constexpr uint32_t kFlagAgg = 1u << 30;
+constexpr uint32_t kFlagInc = 2u << 30;
+constexpr uint32_t kCountMask = (1u << 30) - 1;
+constexpr int kSpinLimit = 1 << 22;
+constexpr int kSortWarps = kSortThreads / 32;
+
+template <class K>
+struct SortItems;
+template <>
+struct SortItems<uint32_t> {
+  static constexpr int value = kSortItems;
+};
+template <>
+struct SortItems<uint64_t> {
+  static constexpr int value = 8;
+};
+
+template <class K>
+struct SortSmemT {
+  static constexpr int kTile = kSortThreads * SortItems<K>::value;
+  K keys[kTile];
+  uint32_t vals[kTile];
+  uint32_t whist[kSortWarps][kRadix];  // per-warp digit counts, then warp offsets
+  uint32_t dstart[kRadix];             // first slot of each digit inside the tile
+  uint32_t goff[kRadix];               // global position of the tile's first item of each digit
+  uint32_t hscan[kRadix];              // exclusive scan of the pass histogram
+  uint32_t wsum[kSortWarps];
+  uint32_t tile;
+};
+
+__device__ __forceinline__ int64_t sort_count(int64_t n, const uint32_t* n_dev) {
+  return n_dev ? (int64_t)*((volatile const uint32_t*)n_dev) : n;
+}
+
+template <class K>
+__global__ void __launch_bounds__(512) k_digit_hist_t(const K* __restrict__ keys, int64_t n0,
+                                                      const uint32_t* n_dev, int passes,
+                                                      uint32_t* __restrict__ hist) {
+  __shared__ uint32_t h[8 * kRadix];
+  const int64_t n = sort_count(n0, n_dev);
+  for (int i = threadIdx.x; i < passes * kRadix; i += blockDim.x) h[i] = 0;
+  __syncthreads();
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const K k = keys[i];
+    for (int p = 0; p < passes; ++p) atomicAdd(&h[p * kRadix + (uint32_t)((k >> (p * kRadixBits)) & (kRadix - 1))], 1u);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < passes * kRadix; i += blockDim.x)
+    if (h[i]) atomicAdd(&hist[i], h[i]);
+}
+
+// Exclusive scan over the first 256 threads' values (all threads call).
+__device__ __forceinline__ uint32_t sort_scan256(uint32_t v, uint32_t* wsum) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31 && warp < kRadix / 32) wsum[warp] = x;
+  __syncthreads();
+  uint32_t base = 0;
+  if (warp < kRadix / 32)
+    for (int w = 0; w < warp; ++w) base += wsum[w];
+  __syncthreads();
+  return base + x - v;
+}
+
+template <class K>
+__global__ void __launch_bounds__(kSortThreads, 2)
+    k_onesweep_t(const K* __restrict__ kin, const uint32_t* __restrict__ vin, K* __restrict__ kout,
+                 uint32_t* __restrict__ vout, int64_t n0, const uint32_t* n_dev, int shift,
+                 const uint32_t* __restrict__ hist, uint32_t* lookback, uint32_t* tile_ctr, uint32_t* status) {
+  constexpr int ITEMS = SortItems<K>::value;
+  constexpr int TILE = SortSmemT<K>::kTile;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  SortSmemT<K>& sm = *reinterpret_cast<SortSmemT<K>*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t n = sort_count(n0, n_dev);
+  const int64_t tiles = (n + TILE - 1) / TILE;
+  if (tid == 0) sm.tile = atomicAdd(tile_ctr, 1u);
+  for (int i = tid; i < kSortWarps * kRadix; i += kSortThreads) (&sm.whist[0][0])[i] = 0;
+  const uint32_t hs = sort_scan256(tid < kRadix ? __ldg(hist + tid) : 0u, sm.wsum);
+  if (tid < kRadix) sm.hscan[tid] = hs;
+  __syncthreads();
+  const uint32_t t = sm.tile;
+  if ((int64_t)t >= tiles) return;   // past the data: nobody waits on this ticket
+  const int64_t base = (int64_t)t * TILE;
+  const int64_t wbase = base + (int64_t)warp * 32 * ITEMS;
+
+  K k[ITEMS];
+  uint32_t v[ITEMS], r[ITEMS];
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    const int64_t idx = wbase + i * 32 + lane;
+    const bool ok = idx < n;
+    k[i] = ok ? kin[idx] : (K)0;
+    v[i] = ok ? vin[idx] : 0u;
+  }
+  const unsigned lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    const int64_t idx = wbase + i * 32 + lane;
+    const uint32_t d = idx < n ? (uint32_t)((k[i] >> shift) & (kRadix - 1)) : (uint32_t)kRadix;
+    const unsigned peers = __match_any_sync(kFull, d);
+    const int leader = __ffs(peers) - 1;
+    uint32_t old = 0;
+    if (lane == leader && d < (uint32_t)kRadix) {
+      old = sm.whist[warp][d];
+      sm.whist[warp][d] = old + __popc(peers);
+    }
+    old = __shfl_sync(kFull, old, leader);
+    r[i] = old + __popc(peers & lt);
+  }
+  __syncthreads();
+
+  uint32_t cnt = 0;
+  if (tid < kRadix) {
+    for (int w = 0; w < kSortWarps; ++w) {
+      const uint32_t c = sm.whist[w][tid];
+      sm.whist[w][tid] = cnt;
+      cnt += c;
+    }
+    volatile uint32_t* mine = lookback + (int64_t)t * kRadix + tid;
+    *mine = (t == 0 ? kFlagInc : kFlagAgg) | cnt;
+  }
+  const uint32_t ds = sort_scan256(cnt, sm.wsum);
+  if (tid < kRadix) {
+    sm.dstart[tid] = ds;
+    uint32_t excl = 0;
+    if (t > 0) {
+      int64_t j = (int64_t)t - 1;
+      int spins = 0;
+      while (j >= 0) {
+        const uint32_t w = *(volatile const uint32_t*)(lookback + j * kRadix + tid);
+        const uint32_t flag = w & ~kCountMask;
+        if (flag == 0u) {
+          if (++spins > kSpinLimit) {
+            latch(status, EMB_ERR_TIMEOUT);
+            break;
+          }
+          __nanosleep(32);
+          continue;
+        }
+        excl += w & kCountMask;
+        if (flag == kFlagInc) break;
+        --j;
+      }
+      *(volatile uint32_t*)(lookback + (int64_t)t * kRadix + tid) = kFlagInc | ((excl + cnt) & kCountMask);
+    }
+    sm.goff[tid] = sm.hscan[tid] + excl;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    const int64_t idx = wbase + i * 32 + lane;
+    if (idx < n) {
+      const uint32_t d = (uint32_t)((k[i] >> shift) & (kRadix - 1));
+      const uint32_t pos = sm.dstart[d] + sm.whist[warp][d] + r[i];
+      sm.keys[pos] = k[i];
+      sm.vals[pos] = v[i];
+    }
+  }
+  __syncthreads();
+  const int tile_n = (int)(n - base < TILE ? n - base : TILE);
+  for (int j = tid; j < tile_n; j += kSortThreads) {
+    const K key = sm.keys[j];
+    const uint32_t d = (uint32_t)((key >> shift) & (kRadix - 1));
+    const uint64_t o = (uint64_t)sm.goff[d] + (uint64_t)(j - sm.dstart[d]);
+    if (o < (uint64_t)n) {   // always true unless a look-back wait gave up
+      kout[o] = key;
+      vout[o] = sm.vals[j];
+    }
+  }
+}
+
+// Words of scratch the sort needs: hist [passes][256], tickets [passes],
+// look-back words [passes][tiles][256].
+template <class K>
+inline size_t sort_scratch_words(int passes, int64_t cap) {
+  const int64_t tiles = (cap + SortSmemT<K>::kTile - 1) / SortSmemT<K>::kTile;
+  return (size_t)passes * kRadix + passes + (size_t)passes * tiles * kRadix;
+}
+
+// Sorts keys[0]/vals[0] (n pairs, or *n_dev of at most cap) into keys[p&1],
+// vals[p&1] with p = passes.  `scratch` holds sort_scratch_words() words and
+// is cleared here.  Returns the index of the buffer holding the result.
+template <class K>
+inline emb_status radix_sort_pairs(K* const keys[2], uint32_t* const vals[2], int64_t n, const uint32_t* n_dev,
+                                   int64_t cap, int passes, uint32_t* scratch, int sm_count, uint32_t* status,
+                                   cudaStream_t stream, int* result) {
+  *result = 0;
+  if (cap <= 0 || passes <= 0) return EMB_OK;
+  const int64_t tiles = (cap + SortSmemT<K>::kTile - 1) / SortSmemT<K>::kTile;
+  uint32_t* hist = scratch;
+  uint32_t* tickets = hist + (size_t)passes * kRadix;
+  uint32_t* lookback = tickets + passes;
+  EMB_CUDA_TRY(cudaMemsetAsync(scratch, 0, sort_scratch_words<K>(passes, cap) * sizeof(uint32_t), stream));
+  const int hgrid = (int)std::min<int64_t>((cap + 511) / 512, (int64_t)sm_count * 4);
+  k_digit_hist_t<K><<<hgrid, 512, 0, stream>>>(keys[0], n, n_dev, passes, hist);
+  EMB_CUDA_TRY(cudaFuncSetAttribute(k_onesweep_t<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)sizeof(SortSmemT<K>)));
+  for (int ps = 0; ps < passes; ++ps) {
+    const int in = ps & 1, out = in ^ 1;
+    k_onesweep_t<K><<<(unsigned)tiles, kSortThreads, sizeof(SortSmemT<K>), stream>>>(
+        keys[in], vals[in], keys[out], vals[out], n, n_dev, ps * kRadixBits, hist + ps * kRadix,
+        lookback + (size_t)ps * tiles * kRadix, tickets + ps, status);
+  }
+  *result = passes & 1;
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace emb

@@ -248,3 +248,72 @@ def check_train_step(ts, max_ambiguous_frac=1e-5):
             assert oka.all(), "accumulator of row %d: %s vs %s" % (r, Ag[r][~oka][:4], ar[~oka][:4])
     assert excluded <= max(16, max_ambiguous_frac * total), (excluded, total)
     return excluded
+
+
+def compare_hash_maps(gpu, ref, what=""):
+    """Exported maps must be identical as (tid, key) -> row maps, with equal
+    counts while counting and equal last_seen."""
+    assert np.array_equal(gpu["tid"], ref["tid"].astype(np.int32)), what + " tids"
+    assert np.array_equal(gpu["key"], ref["key"]), what + " keys"
+    assert np.array_equal(gpu["row"], ref["row"]), what + " rows"
+    counting = ref["row"] < 0
+    assert np.array_equal(gpu["count"][counting], ref["count"][counting].astype(np.int32)), what + " counts"
+    assert np.array_equal(gpu["last_seen"], ref["last_seen"]), what + " last_seen"
+
+
+class DynamicRun:
+    """The dynamic-table training loop through the C ABI -- per step:
+    hash_lookup_or_insert -> emb_forward (rows_given columns over the table's
+    row pool) -> emb_backward_update -> hash_evict_expired -- next to the
+    oracle doing the same on the host."""
+
+    def __init__(self, C, B, steps, num_slots, cap, dim=32, thr=3, ttl=10, seed=1005, alpha=1.2, key_bits=34,
+                 max_len=5, lr=0.01, max_probes=128, check_every=1):
+        import torch
+        import sparse_lookup_gb300 as sl
+        self.C, self.B, self.steps, self.ttl, self.lr = C, B, steps, ttl, lr
+        self.seed, self.alpha, self.key_bits, self.max_len = seed, alpha, key_bits, max_len
+        self.check_every = check_every
+        max_keys = C * B * max_len
+        self.ht = sl.HashTable(num_slots, cap, dim, thr, max_probes, seed, 0.01, max_keys)
+        self.oh = oracle.Hash(cap, dim, thr, seed, 0.01)
+        self.cols = [synth.ColumnSpec("rows_given", "sum", cap, dim, 0) for _ in range(C)]
+        self.plan = sl.Plan(self.cols, [self.ht.weight], [self.ht.acc], max_batch=B, max_ids=max_keys,
+                            training=True)
+
+    def step(self, t, check):
+        import torch
+        offs, keys = synth.dynamic_keys(self.seed, t, self.C, self.B, self.alpha, self.key_bits, self.max_len)
+        tids = np.concatenate([np.full(k.size, c, np.int32) for c, k in enumerate(keys)])
+        allk = np.concatenate(keys)
+        rows = self.ht.lookup_or_insert(torch.from_numpy(tids).cuda(), torch.from_numpy(allk).cuda(), t)
+        ids_off = np.concatenate([[0], np.cumsum(np.concatenate([np.diff(o) for o in offs]))]).astype(np.int32)
+        out, _ = self.plan.forward(self.B, rows, torch.from_numpy(ids_off).cuda(), None, None)
+        G = synth.make_grad((self.B, self.plan.out_width), 500 + t, "cuda")
+        self.plan.backward_update(G, None, self.lr, 1e-10)
+        self.ht.evict_expired(t, self.ttl)
+        torch.cuda.synchronize()
+        st_h, st_p = self.ht.device_status(), self.plan.device_status()
+        # oracle
+        rows_o, st_o = self.oh.lookup_or_insert(tids, allk, t)
+        res = dict(status=(st_h, st_p, st_o))
+        if check:
+            res["rows"] = (rows.cpu().numpy(), rows_o)
+            vals = []
+            pos = 0
+            for o in offs:
+                n = int(o[-1])
+                vals.append(rows_o[pos:pos + n])
+                pos += n
+            res["out"] = (out.cpu().numpy(), oracle.forward(self.cols, self.B, offs, vals, [self.oh.W])[0])
+        else:
+            vals = []
+            pos = 0
+            for o in offs:
+                n = int(o[-1])
+                vals.append(rows_o[pos:pos + n])
+                pos += n
+        oracle.backward_adagrad(self.cols, self.B, offs, vals, G.cpu().numpy(), None, [self.oh.W], [self.oh.acc],
+                                self.lr, 1e-10)
+        self.oh.evict(t, self.ttl)
+        return res
