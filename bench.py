@@ -3,19 +3,26 @@
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                 [--workload inference|training|sequences-mean|sequences-padded|dynamic|tiny]
 
-One JSON line on rank 0.  Default workload: the 1000-column inference
-forward (700 hash-mod + 300 bucketize columns, batch 512).  A step is one
-fused forward over one batch (training workloads: forward + backward +
-Adagrad).  Inputs are resident in HBM before timing; L2 is flushed (a write of
-twice its size) between timed steps, outside the per-step CUDA events.
+One JSON line on rank 0.  Default workload: the 1000-column inference forward
+(700 hash-mod + 300 bucketize columns, batch 512, dims 8..64, bags 1..20).
+A step is one pass of the workload's hot path over one batch:
+  inference            the fused forward;
+  training, sequences  forward + backward (sort, run reduction) + Adagrad;
+  dynamic              hash lookup-or-insert + forward + backward/Adagrad +
+                       expiry sweep (one step of the 50-step stream).
+Inputs are resident in HBM before timing; L2 is flushed (a write of twice its
+size) between timed steps, outside the per-step CUDA events.
 
-value    pooled rows gathered per second (valid IDs whose row was read)
-roofline algorithmic bytes of the dominant kernel per launch / its mean event
-         time, against the measured HBM copy bandwidth
-e2e      the same metric through the C ABI with pinned HOST inputs: H2D of the
-         step's IDs and offsets, the forward, D2H of the pooled output
-cpu_baseline the CPU oracle on a bounded sample of the same workload
---impl reference  times the CPU oracle (the reference arm of this build).
+value         pooled rows gathered per second (valid IDs whose row was read)
+roofline      the forward kernel: its algorithmic bytes per launch / its mean
+              event time, against the measured HBM copy bandwidth;
+              roofline_backward: the same for the whole backward call
+gather_ceiling the rate random row gathers of the workload's row sizes reach
+              on this GPU (measured beside the run), for reference
+e2e           the same metric through the C ABI with pinned HOST buffers: H2D of
+              the step's inputs, the step, D2H of the pooled output
+cpu_baseline  the CPU oracle (one thread) on a bounded sample of the workload
+--impl reference  times that oracle alone (the reference arm of this build).
 """
 import argparse
 import json
@@ -35,6 +42,7 @@ from sparse_lookup_gb300 import synth  # noqa: E402
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM = 6800.0
+TRAIN_WORKLOADS = ("training", "sequences-mean", "sequences-padded", "tiny")
 
 
 def peaks():
@@ -84,6 +92,7 @@ class ClockSampler:
         res = {"sm_mhz": None, "sm_max_mhz": None, "reasons": []}
         if not self.samples:
             return res
+
         def num(x):
             try:
                 return float(x)
@@ -117,22 +126,27 @@ def make_workload(name, columns=None):
             return synth.inference(n_cat=columns * 7 // 10, n_num=columns - columns * 7 // 10)
         return synth.inference()
     if name == "training":
-        return synth.training()
+        return synth.training(C=columns) if columns else synth.training()
     if name == "sequences-mean":
-        return synth.sequences(mode="mean")
+        return synth.sequences(mode="mean", C=columns or 20)
     if name == "sequences-padded":
-        return synth.sequences(mode="padded")
+        return synth.sequences(mode="padded", C=columns or 20)
     if name == "tiny":
         return synth.tiny()
+    if name == "dynamic":
+        return synth.dynamic(C=columns) if columns else synth.dynamic()
     raise SystemExit("unknown workload %s" % name)
 
 
-def forward_bytes(w, rows_valid_per_col):
-    """Algorithmic bytes of one forward: per column the offsets, the values,
-    the boundaries, one row read per valid value and one output row write per
-    bag (padded columns: pad_len rows per bag)."""
+# ---------------------------------------------------------------------------
+# algorithmic bytes
+# ---------------------------------------------------------------------------
+
+def forward_bytes(w, valid_per_col):
+    """Per column: the offsets, the values, the boundaries, one row read per
+    valid value and one output row per bag (padded columns: pad_len rows)."""
     total = 0
-    for c, o, nv in zip(w.columns, w.offsets, rows_valid_per_col):
+    for c, o, nv in zip(w.columns, w.offsets, valid_per_col):
         n = int(o[-1])
         e = 4 if c.transform == "bucketize" else 8
         nb = 0 if c.boundaries is None else c.boundaries.size
@@ -141,9 +155,75 @@ def forward_bytes(w, rows_valid_per_col):
     return total
 
 
-def cpu_oracle_rate(w, tables_dev, budget_s=12.0):
-    """The oracle (single thread) on a bounded sample: whole columns, in
-    order, until about budget_s of CPU work.  Returns (rows/s, sample text)."""
+def backward_bytes(w, n_contrib, valid_per_col, n_unique, dim):
+    """The recorded (row, source) pairs read once (8 B), one sort round trip
+    (16 B), one gradient row gathered per valid contribution, and the read +
+    write of weight and accumulator rows of every unique row."""
+    grad = sum(nv * 4 * c.dim for c, nv in zip(w.columns, valid_per_col))
+    return n_contrib * 8 + n_contrib * 16 + grad + n_unique * 16 * dim
+
+
+# ---------------------------------------------------------------------------
+# timing harness
+# ---------------------------------------------------------------------------
+
+def timed_steps(torch, steps, stream, flush, body):
+    """Run `steps` steps; body(i, marks) records events around its parts in
+    the dict `marks` (name -> (start, end)).  L2 is flushed before each step
+    outside the events.  Returns per-part lists of milliseconds and the wall
+    time of the loop."""
+    recs = []
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        flush.fill_(float(i))
+        marks = {}
+        body(i, marks)
+        recs.append(marks)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    out = {}
+    for marks in recs:
+        for k, (a, b) in marks.items():
+            out.setdefault(k, []).append(a.elapsed_time(b))
+    return out, wall
+
+
+def event_pair(torch):
+    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+
+def row_sizes_mix(w, valid_per_col):
+    mix = {}
+    for c, nv in zip(w.columns, valid_per_col):
+        mix[c.dim * 4] = mix.get(c.dim * 4, 0) + nv
+    return mix
+
+
+def gather_ceiling(torch, sl, mix, dev, budget_bytes=8 << 30):
+    """Random-row gather rate of this GPU for the workload's row sizes: one
+    gather-only pass per row size over a table larger than L2 (the library's
+    calibration kernel), combined by the workload's row counts."""
+    out = {}
+    total_rows = sum(mix.values())
+    if not total_rows or not hasattr(sl, "emb_calibrate_gather"):
+        return None
+    t_sum = 0.0
+    for nbytes, rows in sorted(mix.items()):
+        gbs = sl.calibrate_gather_rate(nbytes // 4, table_bytes=min(budget_bytes, 8 << 30))
+        out[str(nbytes)] = round(gbs, 1)
+        t_sum += rows * nbytes / (gbs * 1e9)
+    bytes_total = sum(r * b for b, r in mix.items())
+    return {"per_row_bytes_gbs": out, "mix_gbs": bytes_total / t_sum / 1e9}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle samples
+# ---------------------------------------------------------------------------
+
+def cpu_forward_sample(w, tables_dev, budget_s=12.0):
+    """The oracle forward (one thread) on whole columns in order until about
+    budget_s of CPU work."""
     import oracle
     t_used, rows_done, cols_done = 0.0, 0, 0
     for ci, c in enumerate(w.columns):
@@ -159,31 +239,125 @@ def cpu_oracle_rate(w, tables_dev, budget_s=12.0):
             break
     sample = "%d of %d columns, all %d bags each (%d rows gathered), oracle forward, 1 thread" % (
         cols_done, len(w.columns), w.B, rows_done)
-    return rows_done / t_used, sample, cols_done
+    return rows_done / t_used, sample
 
+
+def cpu_train_sample(w, tables_dev, G_dev, budget_s=12.0):
+    """The oracle forward + backward/Adagrad (one thread) on whole columns in
+    order until about budget_s of CPU work (host copies of their tables)."""
+    import oracle
+    t_used, rows_done, cols_done = 0.0, 0, 0
+    col0 = 0
+    G = None
+    for ci, c in enumerate(w.columns):
+        if c.pooling == "padded":
+            gs = synth.make_grad((w.B, c.pad_len, c.dim), 900 + ci, "cpu").numpy()
+            g = None
+        else:
+            if G is None:
+                G = G_dev.cpu().numpy() if G_dev is not None else None
+            g = G[:, col0:col0 + c.dim] if G is not None else None
+            gs = None
+        W = tables_dev[c.table].cpu().numpy()
+        A = np.zeros_like(W)
+        spec = synth.ColumnSpec(c.transform, c.pooling, c.num_rows, c.dim, 0, boundaries=c.boundaries,
+                                default=c.default, pad_len=c.pad_len)
+        t0 = time.perf_counter()
+        _, _, rows = oracle.forward([spec], w.B, [w.offsets[ci]], [w.values[ci]], [W], want_rows=True)
+        oracle.backward_adagrad([spec], w.B, [w.offsets[ci]], [w.values[ci]],
+                                np.ascontiguousarray(g) if g is not None else None, [gs] if gs is not None else None,
+                                [W], [A], w.lr, w.eps)
+        t_used += time.perf_counter() - t0
+        rows_done += int((rows[0] >= 0).sum())
+        cols_done += 1
+        if c.pooling != "padded":
+            col0 += c.dim
+        if t_used > budget_s:
+            break
+    sample = "%d of %d columns, all %d bags each (%d rows gathered), oracle forward + backward + Adagrad, " \
+             "1 thread" % (cols_done, len(w.columns), w.B, rows_done)
+    return rows_done / t_used, sample
+
+
+def cpu_dynamic_sample(w, budget_s=12.0):
+    """The oracle hash step + forward + backward/Adagrad (one thread) on the
+    first steps of the dynamic stream, scaled down to 10 columns."""
+    import oracle
+    ex = w.extra
+    C = min(10, len(w.columns))
+    cap = ex["row_capacity"]
+    dim = w.columns[0].dim
+    oh = oracle.Hash(cap, dim, ex["threshold"], ex["init_seed"], ex["init_scale"])
+    cols = [synth.ColumnSpec("rows_given", "sum", cap, dim, 0) for _ in range(C)]
+    t_used, rows_done, steps = 0.0, 0, 0
+    for t in range(ex["steps"]):
+        offs, keys = synth.dynamic_keys(w.seed, t, C, w.B, ex["alpha"], ex["key_bits"])
+        tids = np.concatenate([np.full(k.size, c, np.int32) for c, k in enumerate(keys)])
+        allk = np.concatenate(keys)
+        G = synth.make_grad((w.B, C * dim), 500 + t, "cpu").numpy()
+        t0 = time.perf_counter()
+        rows, _ = oh.lookup_or_insert(tids, allk, t)
+        vals, pos = [], 0
+        for o in offs:
+            vals.append(rows[pos:pos + int(o[-1])])
+            pos += int(o[-1])
+        oracle.forward(cols, w.B, offs, vals, [oh.W])
+        oracle.backward_adagrad(cols, w.B, offs, vals, G, None, [oh.W], [oh.acc], w.lr, w.eps)
+        oh.evict(t, ex["ttl"])
+        t_used += time.perf_counter() - t0
+        rows_done += int((rows >= 0).sum())
+        steps += 1
+        if t_used > budget_s:
+            break
+    return rows_done / max(t_used, 1e-9), "%d steps of the stream with %d of %d columns (%d rows gathered), " \
+        "oracle hash + forward + backward + Adagrad + expiry, 1 thread" % (steps, C, len(w.columns), rows_done)
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle alone
+# ---------------------------------------------------------------------------
 
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    import torch
-    w = make_workload(args.workload)
-    dev = "cpu"
-    tables = [None if t is None else synth.make_table(t, dev) for t in w.tables]
-    times, rows = [], 0
+    w = make_workload(args.workload, args.columns)
+    per = max(2.0, 20.0 / max(1, args.steps + args.warmup))
+    vals = []
     for i in range(args.warmup + args.steps):
-        rate, sample, _ = cpu_oracle_rate(w, tables, budget_s=max(2.0, 20.0 / max(1, args.steps + args.warmup)))
+        if args.workload == "dynamic":
+            rate, sample = cpu_dynamic_sample(w, budget_s=per)
+        else:
+            tables = [None if t is None else synth.make_table(t, "cpu") for t in w.tables]
+            if args.workload in TRAIN_WORKLOADS:
+                width = sum(c.dim for c in w.columns if c.pooling != "padded")
+                G = synth.make_grad((w.B, max(width, 1)), 77, "cpu")[:, :width] if width else None
+                rate, sample = cpu_train_sample(w, tables, G, budget_s=per)
+            else:
+                rate, sample = cpu_forward_sample(w, tables, budget_s=per)
         if i >= args.warmup:
-            times.append(rate)
-    v = statistics.mean(times)
-    line = {"impl": "reference", "metric": "pooled rows gathered/sec (forward)", "value": v, "unit": "rows/s",
+            vals.append(rate)
+    v = statistics.mean(vals)
+    line = {"impl": "reference", "metric": metric_name(args.workload), "value": v, "unit": "rows/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
-            "dtype": "f32", "data": "synthetic", "config": {"workload": w.name, "batch": w.B,
-                                                            "columns": len(w.columns)},
+            "dtype": "f64 accumulate / f32 storage", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.B, "columns": len(w.columns)},
             "cpu_baseline": {"value": v, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
+
+def metric_name(workload):
+    if workload in TRAIN_WORKLOADS:
+        return "pooled rows gathered/sec (fwd+bwd+update)"
+    if workload == "dynamic":
+        return "pooled rows gathered/sec (hash+fwd+bwd+update+expiry)"
+    return "pooled rows gathered/sec (forward)"
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
 
 def run_ours(args):
     import torch
@@ -195,128 +369,296 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     dev = "cuda"
-    w = make_workload(args.workload, args.columns)
-    tables = [None if t is None else synth.make_table(t, dev) for t in w.tables]
-    ids_h, id_off_h, fv_h, f_off_h = synth.jagged(w)
-    n_ids, n_f = ids_h.size, fv_h.size
-    ids = torch.from_numpy(ids_h).to(dev) if n_ids or id_off_h.size > 1 else None
-    id_off = torch.from_numpy(id_off_h).to(dev) if id_off_h.size > 1 else None
-    fv = torch.from_numpy(fv_h).to(dev) if f_off_h.size > 1 else None
-    f_off = torch.from_numpy(f_off_h).to(dev) if f_off_h.size > 1 else None
-    plan = sl.Plan(w.columns, tables, None, max_batch=w.B)
     stream = torch.cuda.current_stream()
-
-    # one untimed call to count the valid rows (from the library's own rows)
-    rows_dbg = torch.empty(n_ids + n_f, dtype=torch.int64, device=dev)
-    out, seq = plan.forward(w.B, ids, id_off, fv, f_off, rows_dbg=rows_dbg)
-    torch.cuda.synchronize()
-    st = plan.device_status()
-    if st != 0:
-        raise SystemExit("device status %d" % st)
-    r = rows_dbg.cpu().numpy()
-    valid_per_col, pos = [], {0: 0, 1: n_ids}
-    for c, o in zip(w.columns, w.offsets):
-        s = 1 if c.transform == "bucketize" else 0
-        n = int(o[-1])
-        valid_per_col.append(int((r[pos[s]:pos[s] + n] >= 0).sum()))
-        pos[s] += n
-    del rows_dbg
-    rows_per_step = sum(valid_per_col)
-    fbytes = forward_bytes(w, valid_per_col)
-
+    w = make_workload(args.workload, args.columns)
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     flush = torch.empty(int(2 * l2 // 4), dtype=torch.float32, device=dev)
+    if args.workload == "dynamic":
+        res = bench_dynamic(torch, sl, w, args, dev, stream, flush)
+    else:
+        res = bench_plan(torch, sl, w, args, dev, stream, flush, train=args.workload in TRAIN_WORKLOADS)
 
-    def step():
-        plan.forward(w.B, ids, id_off, fv, f_off, out=out, seq_out=seq)
-
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    clk = ClockSampler(local)
-    clk.start()
-    time.sleep(0.3)
-    torch.cuda.synchronize()
-    t_wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.fill_(float(i))
-        evs[i][0].record(stream)
-        step()
-        evs[i][1].record(stream)
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall0
-    if world > 1:
-        torch.distributed.barrier()
-    clocks = clk.stop()
-    ms = [a.elapsed_time(b) for a, b in evs]
-    ms_step = statistics.mean(ms)
+    clocks = res.pop("clocks")
+    ms_step = res["ms_step"]
     if world > 1:
         t = torch.tensor([ms_step], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms_step = float(t.item())
-    value = rows_per_step * world / (ms_step / 1e3)
-    achieved = fbytes / (ms_step / 1e3) / 1e9
     peak, peak_kind = peaks()
-
-    # end to end through the C ABI with pinned host buffers
-    ids_p = torch.from_numpy(ids_h).pin_memory() if ids is not None else None
-    id_off_p = torch.from_numpy(id_off_h).pin_memory() if id_off is not None else None
-    fv_p = torch.from_numpy(fv_h).pin_memory() if fv is not None else None
-    f_off_p = torch.from_numpy(f_off_h).pin_memory() if f_off is not None else None
-    out_p = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in (ids_p, id_off_p, fv_p, f_off_p) if x is not None)
-    d2h = out_p.numel() * out_p.element_size()
-
-    def e2e_step():
-        for src, dst in ((ids_p, ids), (id_off_p, id_off), (fv_p, fv), (f_off_p, f_off)):
-            if src is not None:
-                dst.copy_(src, non_blocking=True)
-        step()
-        out_p.copy_(out, non_blocking=True)
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e_ms = []
-    for i in range(args.steps):
-        flush.fill_(float(i))
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        e2e_step()
-        b.record(stream)
-        b.synchronize()
-        e_ms.append(a.elapsed_time(b))
-    e2e_value = rows_per_step * world / (statistics.mean(e_ms) / 1e3)
-
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        rate, sample, _ = cpu_oracle_rate(w, tables, budget_s=12.0)
-        cpu = {"value": rate, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": sample}
-
+    value = res["rows_per_step"] * world / (ms_step / 1e3)
+    fw_ms = statistics.mean(res["times"]["fwd"])
+    achieved = res["fbytes"] / (fw_ms / 1e3) / 1e9
     line = {
-        "metric": "pooled rows gathered/sec (forward)",
+        "metric": metric_name(args.workload),
         "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak" if world > 1 else "none",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.B, "columns": len(w.columns), "ids_per_step": n_ids + n_f,
-                   "rows_gathered_per_step": rows_per_step, "l2": "flushed between steps (2x L2 write, outside events)",
-                   "parallelism": "replicas" if world > 1 else "1 GPU"},
+        "config": dict(res["config"], workload=w.name, batch=w.B, columns=len(w.columns),
+                       l2="flushed between steps (2x L2 write, outside events)",
+                       parallelism="replicas" if world > 1 else "1 GPU"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None, "kernel": "k_forward",
-                     "bytes_per_launch": fbytes, "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)"},
-        "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps,
+                     "bytes_per_launch": res["fbytes"], "launch_ms": fw_ms,
+                     "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy burst)"},
+        "step_ms": {k: statistics.mean(v) for k, v in res["times"].items()},
+        "e2e": res["e2e"],
+        "gpu_launches": res["launches"],
         "clocks": clocks,
-        "cpu_baseline": cpu,
-        "wall_s_timed": t_wall,
+        "cpu_baseline": res.get("cpu"),
+        "wall_s_timed": res["wall"],
     }
+    if "bbytes" in res:
+        b_ms = statistics.mean(res["times"]["bwd"])
+        ab = res["bbytes"] / (b_ms / 1e3) / 1e9
+        line["roofline_backward"] = {"bound": "hbm", "achieved": ab, "peak": peak, "unit": "GB/s", "frac": ab / peak,
+                                     "bytes_per_call": res["bbytes"], "call_ms": b_ms,
+                                     "kernels": "digit histogram, radix passes, run reduction + Adagrad, fixup"}
+    if res.get("ceiling"):
+        line["gather_ceiling"] = res["ceiling"]
+        line["gather_ceiling"]["frac_forward"] = achieved / res["ceiling"]["mix_gbs"]
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def valid_counts(w, rows_dbg, n_ids):
+    r = rows_dbg.cpu().numpy()
+    out, pos = [], {0: 0, 1: n_ids}
+    for c, o in zip(w.columns, w.offsets):
+        s = 1 if c.transform == "bucketize" else 0
+        n = int(o[-1])
+        rr = r[pos[s]:pos[s] + n]
+        if c.pooling == "padded":
+            # values past pad_len are not read
+            lens = np.diff(o)
+            keep = np.concatenate([np.arange(l) < c.pad_len for l in lens]) if n else np.zeros(0, bool)
+            out.append(int(((rr >= 0) & keep).sum()))
+        else:
+            out.append(int((rr >= 0).sum()))
+        pos[s] += n
+    return out
+
+
+def bench_plan(torch, sl, w, args, dev, stream, flush, train):
+    tables = [None if t is None else synth.make_table(t, dev) for t in w.tables]
+    accs = [None if t is None else torch.zeros_like(t) for t in tables] if train else None
+    ids_h, id_off_h, fv_h, f_off_h = synth.jagged(w)
+    n_ids, n_f = ids_h.size, fv_h.size
+    has_id, has_f = id_off_h.size > 1, f_off_h.size > 1
+    ids = torch.from_numpy(ids_h).to(dev) if has_id else None
+    id_off = torch.from_numpy(id_off_h).to(dev) if has_id else None
+    fv = torch.from_numpy(fv_h).to(dev) if has_f else None
+    f_off = torch.from_numpy(f_off_h).to(dev) if has_f else None
+    n_all = n_ids + n_f
+    plan = sl.Plan(w.columns, tables, accs, max_batch=w.B, max_ids=max(n_all, 1) if train else 0, training=train)
+
+    rows_dbg = torch.empty(max(n_all, 1), dtype=torch.int64, device=dev)
+    out, seq = plan.forward(w.B, ids, id_off, fv, f_off, rows_dbg=rows_dbg)
+    torch.cuda.synchronize()
+    if plan.device_status() != 0:
+        raise SystemExit("device status after the forward")
+    valid = valid_counts(w, rows_dbg, n_ids)
+    del rows_dbg
+    rows_per_step = sum(valid)
+    fbytes = forward_bytes(w, valid)
+    res = {"rows_per_step": rows_per_step, "fbytes": fbytes,
+           "config": {"ids_per_step": n_all, "rows_gathered_per_step": rows_per_step}}
+    G = Gseq = None
+    if train:
+        width = plan.out_width
+        G = synth.make_grad((w.B, max(width, 1)), 77, dev)[:, :width].contiguous() if width else None
+        Gseq = synth.make_grad((w.B * plan.seq_per_bag,), 78, dev) if plan.seq_per_bag else None
+        dbg = plan.backward_update(G, Gseq, w.lr, w.eps, debug=True)
+        torch.cuda.synchronize()
+        n_unique = int(dbg["row"].numel())
+        del dbg
+        res["bbytes"] = backward_bytes(w, n_all, valid, n_unique, max(c.dim for c in w.columns))
+        res["config"]["unique_rows_per_step"] = n_unique
+
+    def body(i, marks):
+        a, b = event_pair(torch)
+        a.record(stream)
+        plan.forward(w.B, ids, id_off, fv, f_off, out=out, seq_out=seq)
+        b.record(stream)
+        marks["fwd"] = (a, b)
+        if train:
+            c, d = event_pair(torch)
+            c.record(stream)
+            plan.backward_update(G, Gseq, w.lr, w.eps)
+            d.record(stream)
+            marks["bwd"] = (c, d)
+        marks["step"] = (a, d if train else b)
+
+    for _ in range(max(3, args.warmup)):
+        body(0, {})
+    torch.cuda.synchronize()
+    clk = ClockSampler(torch.cuda.current_device())
+    clk.start()
+    time.sleep(0.3)
+    times, wall = timed_steps(torch, args.steps, stream, flush, body)
+    res["clocks"] = clk.stop()
+    res["times"] = {k: v for k, v in times.items() if k != "step"}
+    res["ms_step"] = statistics.mean(times["step"])
+    res["wall"] = wall
+    passes = 0
+    if train:
+        passes = plan_sort_passes(plan)
+    res["launches"] = args.steps * (1 + (0 if not train else 3 + passes))
+    if plan.device_status() != 0:
+        raise SystemExit("device status after the timed steps")
+
+    # end to end through the C ABI with pinned host buffers
+    host = [(torch.from_numpy(x).pin_memory(), d) for x, d in ((ids_h, ids), (id_off_h, id_off), (fv_h, fv),
+                                                              (f_off_h, f_off)) if d is not None]
+    g_host = G.cpu().pin_memory() if G is not None else None
+    out_p = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x, _ in host) + (g_host.numel() * 4 if g_host is not None else 0)
+    d2h = out_p.numel() * out_p.element_size()
+
+    def e2e_body(i, marks):
+        a, b = event_pair(torch)
+        a.record(stream)
+        for src, dst in host:
+            dst.copy_(src, non_blocking=True)
+        if g_host is not None:
+            G.copy_(g_host, non_blocking=True)
+        plan.forward(w.B, ids, id_off, fv, f_off, out=out, seq_out=seq)
+        out_p.copy_(out, non_blocking=True)
+        if train:
+            plan.backward_update(G, Gseq, w.lr, w.eps)
+        b.record(stream)
+        marks["e2e"] = (a, b)
+
+    for _ in range(3):
+        e2e_body(0, {})
+    et, _ = timed_steps(torch, args.steps, stream, flush, e2e_body)
+    res["e2e"] = {"value": rows_per_step / (statistics.mean(et["e2e"]) / 1e3), "unit": "rows/s",
+                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    res["ceiling"] = gather_ceiling(torch, sl, row_sizes_mix(w, valid), dev) if not args.no_ceiling else None
+    if not args.no_cpu_baseline and dist_env()[0] == 0:
+        if train:
+            rate, sample = cpu_train_sample(w, tables, G, budget_s=12.0)
+        else:
+            rate, sample = cpu_forward_sample(w, tables, budget_s=12.0)
+        res["cpu"] = {"value": rate, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": sample}
+    return res
+
+
+def plan_sort_passes(plan):
+    """Radix passes of the backward: 8 bits of the global row key per pass."""
+    tables = {}
+    for c in plan.columns:
+        tables[c.table] = int(c.num_rows)
+    bits = max(1, int(sum(tables.values())).bit_length())
+    return (bits + 7) // 8
+
+
+def bench_dynamic(torch, sl, w, args, dev, stream, flush):
+    ex = w.extra
+    C, B = len(w.columns), w.B
+    dim = w.columns[0].dim
+    nsteps = max(3, args.warmup) + args.steps
+    # every step's keys resident on the device before timing
+    batches = []
+    max_n = 0
+    for t in range(nsteps):
+        offs, keys = synth.dynamic_keys(w.seed, t, C, B, ex["alpha"], ex["key_bits"])
+        tids = np.concatenate([np.full(k.size, c, np.int32) for c, k in enumerate(keys)])
+        allk = np.concatenate(keys)
+        lens = np.concatenate([np.diff(o) for o in offs])
+        off = np.zeros(lens.size + 1, np.int32)
+        np.cumsum(lens, out=off[1:])
+        batches.append((torch.from_numpy(tids).to(dev), torch.from_numpy(allk).to(dev), torch.from_numpy(off).to(dev),
+                        tids, allk, off))
+        max_n = max(max_n, allk.size)
+    ht = sl.HashTable(ex["num_slots"], ex["row_capacity"], dim, ex["threshold"], ex["max_probes"],
+                      ex["init_seed"], ex["init_scale"], max_n)
+    plan = sl.Plan(w.columns, [ht.weight], [ht.acc], max_batch=B, max_ids=max_n, training=True)
+    out = torch.empty((B, plan.out_width), device=dev)
+    G = synth.make_grad((B, plan.out_width), 77, dev)
+    rows = torch.empty(max_n, dtype=torch.int64, device=dev)
+    state = {"t": 0, "rows": 0}
+
+    def body(i, marks):
+        t = state["t"]
+        tids, keys, off = batches[t][:3]
+        n = keys.numel()
+        a, b = event_pair(torch)
+        c, d = event_pair(torch)
+        e, f = event_pair(torch)
+        a.record(stream)
+        ht.lookup_or_insert(tids, keys, t, rows_out=rows[:n])
+        b.record(stream)
+        plan.forward(B, rows[:n], off, None, None, out=out)
+        c.record(stream)
+        plan.backward_update(G, None, w.lr, w.eps)
+        d.record(stream)
+        ht.evict_expired(t, ex["ttl"])
+        e.record(stream)
+        marks["hash"] = (a, b)
+        marks["fwd"] = (b, c)
+        marks["bwd"] = (c, d)
+        marks["evict"] = (d, e)
+        marks["step"] = (a, e)
+        state["t"] = t + 1
+
+    for _ in range(max(3, args.warmup)):
+        body(0, {})
+    torch.cuda.synchronize()
+    clk = ClockSampler(torch.cuda.current_device())
+    clk.start()
+    time.sleep(0.3)
+    t_first = state["t"]
+    times, wall = timed_steps(torch, args.steps, stream, flush, body)
+    clocks = clk.stop()
+    # valid rows and bytes, from the library's own rows of the last timed step
+    n_last = batches[state["t"] - 1][1].numel()
+    r = rows[:n_last].cpu().numpy()
+    valid = int((r >= 0).sum())
+    width = plan.out_width
+    fbytes = (C * (B + 1) * 4 + n_last * 8 + valid * 4 * dim + B * 4 * width)
+    res = {"rows_per_step": valid, "fbytes": fbytes, "clocks": clocks,
+           "times": {k: v for k, v in times.items() if k != "step"},
+           "ms_step": statistics.mean(times["step"]), "wall": wall,
+           "config": {"ids_per_step": n_last, "rows_gathered_per_step": valid, "num_slots": ex["num_slots"],
+                      "row_capacity": ex["row_capacity"], "threshold": ex["threshold"], "ttl": ex["ttl"],
+                      "stream_steps_timed": [t_first, state["t"] - 1]},
+           "launches": args.steps * (16 + 1 + (3 + plan_sort_passes(plan)) + 1)}
+    if ht.device_status() not in (0, 5) or plan.device_status() != 0:
+        raise SystemExit("device status after the timed steps")
+
+    # end to end: keys, table ids and offsets from pinned host memory
+    hb = [(torch.from_numpy(x).pin_memory(), d) for x, d in ((batches[0][3], batches[0][0]),
+                                                            (batches[0][4], batches[0][1]),
+                                                            (batches[0][5], batches[0][2]))]
+    out_p = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x, _ in hb)
+
+    def e2e_body(i, marks):
+        a, b = event_pair(torch)
+        a.record(stream)
+        for src, dst in hb:
+            dst.copy_(src, non_blocking=True)
+        t = state["t"]
+        n = batches[0][1].numel()
+        ht.lookup_or_insert(batches[0][0], batches[0][1], t, rows_out=rows[:n])
+        plan.forward(B, rows[:n], batches[0][2], None, None, out=out)
+        out_p.copy_(out, non_blocking=True)
+        plan.backward_update(G, None, w.lr, w.eps)
+        ht.evict_expired(t, ex["ttl"])
+        b.record(stream)
+        marks["e2e"] = (a, b)
+        state["t"] = t + 1
+
+    et, _ = timed_steps(torch, min(args.steps, 5), stream, flush, e2e_body)
+    res["e2e"] = {"value": valid / (statistics.mean(et["e2e"]) / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                  "d2h_bytes_per_step": out_p.numel() * 4}
+    res["ceiling"] = gather_ceiling(torch, sl, {dim * 4: valid}, dev) if not args.no_ceiling else None
+    if not args.no_cpu_baseline and dist_env()[0] == 0:
+        rate, sample = cpu_dynamic_sample(w, budget_s=12.0)
+        res["cpu"] = {"value": rate, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": sample}
+    return res
 
 
 def main():
@@ -327,7 +669,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="inference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--columns", type=int, default=None, help="inference: number of columns (profiling)")
+    ap.add_argument("--no-ceiling", action="store_true")
+    ap.add_argument("--columns", type=int, default=None, help="number of columns (smaller profiling cases)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -318,6 +318,15 @@ emb_status emb_sparse_adagrad_noalloc(const int64_t* rows, int64_t n, const floa
  * division-by-invariant-integer of the modulo).  All pointers are host. */
 emb_status emb_selftest_hash_mod(const int64_t* ids, int64_t n, int64_t num_rows, int64_t* rows_out);
 
+/* emb_calibrate_gather -- measurement support, no counterpart on the pages:
+ * reads rows row_idx[0..n) of table [num_rows, dim] (fp32, 16-byte aligned)
+ * with the forward's access shape and nothing else, so that a benchmark can
+ * time the random-row gather rate of this GPU for a row size.  row_idx are
+ * uint32 rows < num_rows (not checked: the caller draws them in range); sink
+ * is a device float that is practically never written. */
+emb_status emb_calibrate_gather(const float* table, int64_t num_rows, int32_t dim, const uint32_t* row_idx,
+                                int64_t n, float* sink, void* stream);
+
 /* Library version string (host, static storage). */
 const char* emb_version(void);
 

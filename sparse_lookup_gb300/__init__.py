@@ -86,6 +86,7 @@ _SIGS = {
     "hash_destroy": (c_int32, [c_void_p]),
     "emb_sparse_adagrad_noalloc": (c_int32, [c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_int64, c_int32,
                                              c_float, c_float, c_void_p]),
+    "emb_calibrate_gather": (c_int32, [c_void_p, c_int64, c_int32, c_void_p, c_int64, c_void_p, c_void_p]),
     "emb_selftest_hash_mod": (c_int32, [c_void_p, c_int64, c_int64, c_void_p]),
     "emb_version": (c_char_p, []),
 }
@@ -220,6 +221,33 @@ def emb_sparse_adagrad_noalloc(rows, n, grads, weight, acc, num_rows, dim, lr, e
     inside the library; n <= 2^18, dim <= 256)."""
     _check(lib().emb_sparse_adagrad_noalloc(ptr(rows), n, ptr(grads), ptr(weight), ptr(acc), num_rows, dim, lr,
                                             eps, _stream(stream)), "emb_sparse_adagrad_noalloc")
+
+
+def emb_calibrate_gather(table, num_rows, dim, row_idx, n, sink, stream=None):
+    _check(lib().emb_calibrate_gather(ptr(table), num_rows, dim, ptr(row_idx), n, ptr(sink), _stream(stream)),
+           "emb_calibrate_gather")
+
+
+def calibrate_gather_rate(dim, table_bytes=8 << 30, n=1 << 25, reps=5, seed=0):
+    """GB/s of random row gathers of `dim` floats over a table of table_bytes
+    (larger than L2), timed with CUDA events on the current stream."""
+    import torch
+    rows = max(1, table_bytes // (dim * 4))
+    table = torch.zeros((rows, dim), dtype=torch.float32, device="cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    idx = torch.randint(0, rows, (n,), generator=g, device="cuda", dtype=torch.int64).to(torch.int32)
+    sink = torch.zeros(1, device="cuda")
+    emb_calibrate_gather(table, rows, dim, idx, n, sink)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        emb_calibrate_gather(table, rows, dim, idx, n, sink)
+    b.record()
+    b.synchronize()
+    ms = a.elapsed_time(b) / reps
+    del table, idx
+    return n * dim * 4 / (ms / 1e3) / 1e9
 
 
 def emb_selftest_hash_mod(ids, num_rows):
