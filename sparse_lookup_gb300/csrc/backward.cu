@@ -28,7 +28,6 @@ namespace emb {
 
 constexpr int kSegThreads = 256;
 constexpr int kSegWarps = kSegThreads / 32;
-constexpr int kSegU = 4;
 
 // ---------------------------------------------------------------------------
 // run ranks (debug outputs only): rank[i] = number of run heads before i
@@ -76,7 +75,8 @@ __global__ void __launch_bounds__(kScanBlock) k_rank_top(uint32_t* part, int nb,
 }
 
 __global__ void __launch_bounds__(kScanBlock) k_rank_down(const uint32_t* keys, int64_t n, uint32_t sentinel,
-                                                          const uint32_t* part, uint32_t* rank) {
+                                                          const uint32_t* part, uint32_t* rank_incl,
+                                                          uint32_t* head_pos) {
   __shared__ uint32_t wsum[32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t i = blockIdx.x * (int64_t)kScanBlock + threadIdx.x;
@@ -90,7 +90,45 @@ __global__ void __launch_bounds__(kScanBlock) k_rank_down(const uint32_t* keys, 
   __syncthreads();
   uint32_t base = part[blockIdx.x];
   for (int w = 0; w < warp; ++w) base += wsum[w];
-  if (i < n) rank[i] = base + x - v;
+  if (i < n) {
+    rank_incl[i] = base + x;               // heads at or before i
+    if (v) head_pos[base + x - 1] = (uint32_t)i;
+  }
+}
+
+__device__ __forceinline__ int table_of_key(const uint32_t* base, int nt, uint32_t key) {
+  int lo = 0, hi = nt;  // largest t with base[t] <= key
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(base + mid) <= key) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Debug outputs of each unique row: table, row and number of contributions.
+__global__ void k_dbg_runs(const uint32_t* keys, int64_t n, uint32_t sentinel, const uint32_t* head_pos,
+                           const int64_t* n_unique, const uint32_t* table_base, int n_tables, int32_t* dbg_table,
+                           int64_t* dbg_row, int32_t* dbg_count) {
+  const int64_t nu = *n_unique;
+  for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < nu; u += (int64_t)gridDim.x * blockDim.x) {
+    const uint32_t p = head_pos[u];
+    int64_t pn;
+    if (u + 1 < nu) {
+      pn = head_pos[u + 1];
+    } else {  // first sentinel key: lower bound of the sentinel in the sorted keys
+      int64_t lo = p, hi = n;
+      while (lo < hi) {
+        const int64_t mid = (lo + hi) >> 1;
+        if (keys[mid] < sentinel) lo = mid + 1; else hi = mid;
+      }
+      pn = lo;
+    }
+    const uint32_t key = keys[p];
+    const int t = table_of_key(table_base, n_tables, key);
+    if (dbg_table) dbg_table[u] = t;
+    if (dbg_row) dbg_row[u] = (int64_t)(key - table_base[t]);
+    if (dbg_count) dbg_count[u] = (int32_t)(pn - p);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -126,12 +164,6 @@ struct SegArgs {
   int32_t dbg_ld;
 };
 
-struct SegSmem {
-  float4 part[2][kSegWarps * 64];
-  int32_t tail_start[kSegThreads];   // per group: start of its tail run, -1 if none
-  int32_t head_end[kSegThreads];     // per group: end of its head run, -1 if no head run
-  uint8_t head_thru[kSegThreads];    // per group: head run covers the whole range and goes on
-};
 
 __device__ __forceinline__ float4 seg_f4zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 
@@ -142,27 +174,27 @@ __device__ __forceinline__ void seg_f4add(float4& a, const float4& b) {
   a.w += b.w;
 }
 
-__device__ __forceinline__ float adagrad1(float& w, float& acc, float g, float lr, float eps) {
+
+// One Adagrad step on one element (torch.optim.Adagrad with lr_decay =
+// weight_decay = 0, eps outside the root): acc += g*g; w -= lr*g/(sqrt(acc)+eps).
+// The square root and the reciprocal use the hardware's approximate forms
+// (within a couple of ulp): the accumulator is exact, the weight step
+// lr*g/(sqrt(acc)+eps) carries a relative error of about 1e-7.
+__device__ __forceinline__ void adagrad1_fast(float& w, float& acc, float g, float lr, float eps) {
   const float a = __fadd_rn(acc, __fmul_rn(g, g));
-  const float den = __fadd_rn(__fsqrt_rn(a), eps);
+  float r, inv;
+  asm("sqrt.approx.f32 %0, %1;" : "=f"(r) : "f"(a));
+  const float den = __fadd_rn(r, eps);
+  asm("rcp.approx.f32 %0, %1;" : "=f"(inv) : "f"(den));
   acc = a;
-  w = __fsub_rn(w, __fdiv_rn(__fmul_rn(lr, g), den));
-  return w;
+  w = __fsub_rn(w, __fmul_rn(__fmul_rn(lr, g), inv));
 }
 
-__device__ __forceinline__ int table_of_key(const uint32_t* base, int nt, uint32_t key) {
-  int lo = 0, hi = nt;  // largest t with base[t] <= key
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (__ldg(base + mid) <= key) lo = mid; else hi = mid;
-  }
-  return lo;
-}
 
-// The unique writer of a row: Adagrad step with the summed gradient g.
+// The unique writer of a row: Adagrad step with the summed gradient g.  `end`
+// is one past the run's last sorted position (debug: its rank).
 template <int V>
-__device__ void finish_row(const SegArgs& a, uint32_t key, int64_t start, int64_t end, const float4 (&g)[V],
-                           int sub) {
+__device__ void finish_row(const SegArgs& a, uint32_t key, int64_t end, const float4 (&g)[V], int sub) {
   const int t = table_of_key(a.table_base, a.n_tables, key);
   const int64_t row = key - __ldg(a.table_base + t);
   const TableMeta tm = a.tables[t];
@@ -174,26 +206,20 @@ __device__ void finish_row(const SegArgs& a, uint32_t key, int64_t start, int64_
     if (f4 < tm.dim4) {
       float4 w = *reinterpret_cast<float4*>(W + f4 * 4);
       float4 ac = *reinterpret_cast<float4*>(A + f4 * 4);
-      adagrad1(w.x, ac.x, g[v].x, a.lr, a.eps);
-      adagrad1(w.y, ac.y, g[v].y, a.lr, a.eps);
-      adagrad1(w.z, ac.z, g[v].z, a.lr, a.eps);
-      adagrad1(w.w, ac.w, g[v].w, a.lr, a.eps);
+      adagrad1_fast(w.x, ac.x, g[v].x, a.lr, a.eps);
+      adagrad1_fast(w.y, ac.y, g[v].y, a.lr, a.eps);
+      adagrad1_fast(w.z, ac.z, g[v].z, a.lr, a.eps);
+      adagrad1_fast(w.w, ac.w, g[v].w, a.lr, a.eps);
       *reinterpret_cast<float4*>(W + f4 * 4) = w;
       *reinterpret_cast<float4*>(A + f4 * 4) = ac;
     }
   }
-  if (a.rank) {
-    const uint32_t u = a.rank[start];
+  if (a.rank && a.dbg_grad) {
+    const uint32_t u = a.rank[end - 1] - 1;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
       const int f4 = sub + v * 32;
-      if (f4 < tm.dim4 && a.dbg_grad)
-        *reinterpret_cast<float4*>(a.dbg_grad + (int64_t)u * a.dbg_ld + f4 * 4) = g[v];
-    }
-    if (sub == 0) {
-      if (a.dbg_table) a.dbg_table[u] = t;
-      if (a.dbg_row) a.dbg_row[u] = row;
-      if (a.dbg_count) a.dbg_count[u] = (int32_t)(end - start);
+      if (f4 < tm.dim4) *reinterpret_cast<float4*>(a.dbg_grad + (int64_t)u * a.dbg_ld + f4 * 4) = g[v];
     }
   }
 }
@@ -219,166 +245,350 @@ __device__ __forceinline__ const float* grad_src(const SegArgs& a, uint32_t val,
   return a.grad_out + (int64_t)b * a.ldg + cg.x;
 }
 
-template <int V>
-__global__ void __launch_bounds__(kSegThreads) k_segreduce(const SegArgs a) {
-  constexpr int U = kSegU / V;
-  __shared__ SegSmem sm;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int glog = a.glog;
-  const int G = 32 >> glog;
-  const int grp = lane >> glog, sub = lane & ((1 << glog) - 1);
-  const int q = warp * G + grp;
-  const int NG = kSegWarps * G;
-  const int64_t B0 = (int64_t)blockIdx.x * NG * kUnit;
-  const int64_t B1 = min(B0 + (int64_t)NG * kUnit, a.n);
-  const int64_t k0 = min(B0 + (int64_t)q * kUnit, B1), k1 = min(k0 + kUnit, B1);
-  const int D4 = a.maxdim4;
-
-  float4 acc[V];
-#pragma unroll
-  for (int v = 0; v < V; ++v) acc[v] = seg_f4zero();
-  uint32_t cur = k0 < k1 ? __ldg(a.keys + k0) : a.sentinel;
-  bool head = k0 < k1 && k0 > 0 && __ldg(a.keys + k0 - 1) == cur;
-  int64_t run_start = k0;
-  if (sub == 0) {
-    sm.tail_start[q] = -1;
-    sm.head_end[q] = -1;
-    sm.head_thru[q] = 0;
-  }
-  __syncwarp();
-
-  auto flush = [&](int64_t end, bool tail) {
-    if (cur == a.sentinel) return;
-    if (!head && !tail) {
-      finish_row<V>(a, cur, run_start, end, acc, sub);
-      return;
+// Rows of the table a key belongs to, tracked while keys ascend.
+struct TableCursor {
+  int t = -1;
+  uint32_t base = 0, next = 0;
+  __device__ __forceinline__ void seek(const SegArgs& a, uint32_t key) {
+    if (t < 0 || key < base || key >= next) {
+      t = table_of_key(a.table_base, a.n_tables, key);
+      base = __ldg(a.table_base + t);
+      next = __ldg(a.table_base + t + 1);
     }
-    const int side = head ? 0 : 1;
+  }
+};
+
+// Ask the memory system to stage `bytes` (a multiple of 16, 16-byte aligned)
+// starting at p into L2, without waiting and without using registers.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// A finished run whose weight and accumulator loads are in flight; its
+// Adagrad step is applied when the lane group finishes its next run (or at
+// the end), so the loads overlap the gathers in between.
+template <int V>
+struct PendingRow {
+  bool on = false;
+  int64_t end = 0;
+  int dim4 = 0;
+  float* W = nullptr;
+  float* A = nullptr;
+  float4 g[V], w[V], acc[V];
+
+  __device__ __forceinline__ void issue(const SegArgs& a, const TableCursor& tc, uint32_t k, int64_t e,
+                                        const float4 (&grad)[V], int sub) {
+    on = true;
+    end = e;
+    const TableMeta& tm = a.tables[tc.t];
+    const int64_t row = k - tc.base;
+    dim4 = tm.dim4;
+    W = tm.weight + row * tm.dim;
+    A = tm.acc + row * tm.dim;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      g[v] = grad[v];
+      const int f4 = sub + v * 32;
+      if (f4 < dim4) {
+        w[v] = *reinterpret_cast<const float4*>(W + f4 * 4);
+        acc[v] = *reinterpret_cast<const float4*>(A + f4 * 4);
+      }
+    }
+  }
+
+  __device__ __forceinline__ void retire(const SegArgs& a, int sub) {
+    if (!on) return;
+    on = false;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
       const int f4 = sub + v * 32;
-      if (f4 < D4) sm.part[side][q * D4 + f4] = acc[v];
-    }
-    if (sub == 0) {
-      if (head) {
-        sm.head_end[q] = (int32_t)(end - B0);
-        sm.head_thru[q] = tail ? 1 : 0;
-      } else {
-        sm.tail_start[q] = (int32_t)(run_start - B0);
+      if (f4 < dim4) {
+        adagrad1_fast(w[v].x, acc[v].x, g[v].x, a.lr, a.eps);
+        adagrad1_fast(w[v].y, acc[v].y, g[v].y, a.lr, a.eps);
+        adagrad1_fast(w[v].z, acc[v].z, g[v].z, a.lr, a.eps);
+        adagrad1_fast(w[v].w, acc[v].w, g[v].w, a.lr, a.eps);
+        *reinterpret_cast<float4*>(W + f4 * 4) = w[v];
+        *reinterpret_cast<float4*>(A + f4 * 4) = acc[v];
       }
     }
-  };
-
-  uint32_t lkey = a.sentinel;
-  int ld4 = 0;
-  for (int64_t j = k0; j < k1; j += U) {
-    float4 gv[U][V];
-    uint32_t kk[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t k = j + u;
-      const bool in = k < k1;
-      kk[u] = in ? __ldg(a.keys + k) : a.sentinel;
-      float scale = 1.0f;
-      int d4 = 0;
-      const float* src = nullptr;
-      if (in && kk[u] != a.sentinel) src = grad_src(a, __ldg(a.vals + k), kk[u], scale, d4, lkey, ld4);
+    if (a.rank && a.dbg_grad) {
+      const uint32_t u = a.rank[end - 1] - 1;
 #pragma unroll
       for (int v = 0; v < V; ++v) {
         const int f4 = sub + v * 32;
-        float4 x = seg_f4zero();
-        if (src && f4 < d4) {
-          x = __ldg(reinterpret_cast<const float4*>(src + f4 * 4));
-          if (scale != 1.0f) {
-            x.x *= scale;
-            x.y *= scale;
-            x.z *= scale;
-            x.w *= scale;
-          }
-        }
-        gv[u][v] = x;
+        if (f4 < dim4) *reinterpret_cast<float4*>(a.dbg_grad + (int64_t)u * a.dbg_ld + f4 * 4) = g[v];
       }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t k = j + u;
-      if (k >= k1) break;
-      if (kk[u] != cur) {
-        flush(k, false);
-        cur = kk[u];
-        head = false;
-        run_start = k;
-#pragma unroll
-        for (int v = 0; v < V; ++v) acc[v] = seg_f4zero();
-      }
-#pragma unroll
-      for (int v = 0; v < V; ++v) seg_f4add(acc[v], gv[u][v]);
     }
   }
-  if (k0 < k1) flush(k1, k1 < a.n && __ldg(a.keys + k1) == cur);
+};
+
+constexpr int kSegSpan = 2048;                    // sorted entries per CTA
+constexpr int kSegPerThread = kSegSpan / kSegThreads;
+constexpr int kSegWarpSpan = kSegSpan / kSegWarps;
+constexpr uint32_t kOffPad = 0x80000000u;         // offset refers to grad_seq
+constexpr uint32_t kNoKey = 0xFFFFFFFFu;          // above every key and the sentinel
+
+struct SegSmem3 {
+  float4 part[2][kSegWarps * 64];   // head / tail partial of each warp
+  uint32_t key[kSegSpan];
+  uint32_t off[kSegSpan];           // float4 offset of the gradient row (+ kOffPad)
+  float scale[kSegSpan];
+  uint8_t d4[kSegSpan];             // float4 slots of the row
+  uint32_t tail_key[kSegWarps];     // per warp: key of the run left open at its end
+  int32_t tail_valid[kSegWarps];
+  int32_t head_end[kSegWarps];      // per warp: end of the run cut at its start, -1 if none
+  int32_t head_thru[kSegWarps];     // per warp: that run covers the whole range and goes on
+};
+
+__device__ __forceinline__ float4 shfl_up4(const float4& x, int d) {
+  return make_float4(__shfl_up_sync(kFull, x.x, d), __shfl_up_sync(kFull, x.y, d), __shfl_up_sync(kFull, x.z, d),
+                     __shfl_up_sync(kFull, x.w, d));
+}
+
+__device__ __forceinline__ float4 shfl4(const float4& x, int src) {
+  return make_float4(__shfl_sync(kFull, x.x, src), __shfl_sync(kFull, x.y, src), __shfl_sync(kFull, x.z, src),
+                     __shfl_sync(kFull, x.w, src));
+}
+
+// Runs of sorted contributions are reduced by WARPS: a warp walks its range
+// G entries at a time (one per lane group of dim/4 lanes), a segmented scan by
+// key over the groups (lane shuffles) sums equal keys, and every group whose
+// entry ends a run applies the Adagrad step in the same predicated instruction
+// stream -- groups never diverge into separate update paths.
+template <int V>
+__global__ void __launch_bounds__(kSegThreads, 3) k_segreduce(const SegArgs a) {
+  __shared__ SegSmem3 sm;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int glog = a.glog;
+  const int G = 32 >> glog;
+  const int q = lane >> glog, sub = lane & ((1 << glog) - 1);
+  const int64_t B0 = (int64_t)blockIdx.x * kSegSpan;
+  const int64_t B1 = min(B0 + (int64_t)kSegSpan, a.n);
+  const int span = (int)(B1 - B0);
+  const int D4 = a.maxdim4;
+
+  // ---- decode the CTA's entries, coalesced, into shared memory; the
+  //      weight and accumulator rows of every run that starts here are
+  //      prefetched into L2 so that the updates below find them there ----
+  uint32_t lkey = a.sentinel;
+  int ld4 = 0;
+  TableCursor ptc;
+#pragma unroll
+  for (int k = 0; k < kSegPerThread; ++k) {
+    const int e = k * kSegThreads + tid;
+    uint32_t key = a.sentinel, off = 0;
+    float sc = 0.0f;
+    int d4 = 0;
+    if (e < span) {
+      key = __ldg(a.keys + B0 + e);
+      if (key != a.sentinel && (B0 + e == 0 || __ldg(a.keys + B0 + e - 1) != key)) {
+        ptc.seek(a, key);
+        const TableMeta& tm = a.tables[ptc.t];
+        const int64_t row = key - ptc.base;
+        prefetch_l2(tm.weight + row * tm.dim, (uint32_t)tm.dim * 4u);
+        prefetch_l2(tm.acc + row * tm.dim, (uint32_t)tm.dim * 4u);
+      }
+      if (key != a.sentinel) {
+        const uint32_t val = __ldg(a.vals + B0 + e);
+        if (val & kPadBit) {
+          if (key != lkey) {
+            lkey = key;
+            ld4 = a.tables[table_of_key(a.table_base, a.n_tables, key)].dim4;
+          }
+          d4 = ld4;
+          sc = 1.0f;
+          off = kOffPad | (val & ~kPadBit);
+        } else {
+          const uint32_t c = div_magic32(val, a.bdiv);
+          const uint32_t b = val - c * (uint32_t)a.batch;
+          const int4 cg = __ldg(a.colg + c);
+          sc = cg.y ? __ldg(a.inv_n + val) : 1.0f;
+          d4 = cg.z;
+          off = (uint32_t)(((int64_t)b * a.ldg + cg.x) >> 2);
+        }
+      }
+    }
+    sm.key[e] = key;
+    sm.off[e] = off;
+    sm.scale[e] = sc;
+    sm.d4[e] = (uint8_t)d4;
+  }
+  if (lane == 0) {
+    sm.tail_valid[warp] = 0;
+    sm.head_end[warp] = -1;
+    sm.head_thru[warp] = 0;
+  }
   __syncthreads();
 
-  // runs cut inside the CTA: the group holding the run's start adds the head
-  // partials of the following groups in order
-  const int ts = sm.tail_start[q];
+  // ---- per warp: segmented reduction over its range ----
+  const int ws0 = min(warp * kSegWarpSpan, span), ws1 = min(ws0 + kSegWarpSpan, span);
+  const uint32_t key_after = ws1 < span ? sm.key[ws1] : (B1 < a.n ? __ldg(a.keys + B1) : kNoKey);
+  uint32_t ckey = kNoKey;   // run open at the chunk start, summed in `carry`
+  bool chead = false;       // that run started before this warp's range
+  float4 carry[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) carry[v] = seg_f4zero();
+  if (ws0 < ws1) {
+    ckey = sm.key[ws0];
+    const uint32_t prev = ws0 > 0 ? sm.key[ws0 - 1] : (B0 > 0 ? __ldg(a.keys + B0 - 1) : kNoKey);
+    chead = prev == ckey && ckey != a.sentinel;
+  }
+  TableCursor tc;
+  PendingRow<V> pend;
+  for (int c0 = ws0; c0 < ws1; c0 += G) {
+    const int e = c0 + q;
+    const bool valid = e < ws1;
+    const uint32_t key = valid ? sm.key[e] : kNoKey;
+    float4 x[V];
+    {
+      const uint32_t off = valid ? sm.off[e] : 0u;
+      const int d4 = valid ? (int)sm.d4[e] : 0;
+      const float sc = valid ? sm.scale[e] : 0.0f;
+      const float* src = (off & kOffPad) ? a.grad_seq + (int64_t)(off & ~kOffPad) * 4
+                                         : a.grad_out + (int64_t)off * 4;
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int f4 = sub + v * 32;
+        x[v] = seg_f4zero();
+        if (f4 < d4) {
+          x[v] = __ldg(reinterpret_cast<const float4*>(src + f4 * 4));
+          if (sc != 1.0f) {
+            x[v].x *= sc;
+            x[v].y *= sc;
+            x[v].z *= sc;
+            x[v].w *= sc;
+          }
+        }
+      }
+    }
+    // segmented inclusive scan over the lane groups, by key
+    for (int d = 1; d < G; d <<= 1) {
+      const uint32_t ky = __shfl_up_sync(kFull, key, d << glog);
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const float4 y = shfl_up4(x[v], d << glog);
+        if (q >= d && ky == key) seg_f4add(x[v], y);
+      }
+    }
+    const bool in_carry = key == ckey;
+    if (in_carry) {
+#pragma unroll
+      for (int v = 0; v < V; ++v) seg_f4add(x[v], carry[v]);
+    }
+    // does this entry end its run?
+    uint32_t nk = __shfl_down_sync(kFull, key, (1 << glog) & 31);
+    if (q == G - 1 || e + 1 >= ws1) nk = (e + 1 < ws1) ? sm.key[e + 1] : key_after;
+    const bool ends = valid && key != a.sentinel && nk != key;
+    if (ends) {
+      if (in_carry && chead) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+          const int f4 = sub + v * 32;
+          if (f4 < D4) sm.part[0][warp * D4 + f4] = x[v];
+        }
+        if (sub == 0) sm.head_end[warp] = e + 1;
+      } else {
+        pend.retire(a, sub);
+        tc.seek(a, key);
+        pend.issue(a, tc, key, B0 + e + 1, x, sub);
+      }
+    }
+    // the run reaching the chunk end is carried into the next chunk
+    const int ql = min(G - 1, ws1 - 1 - c0);
+    const int src_lane = (ql << glog) + sub;
+    const uint32_t lk = __shfl_sync(kFull, key, ql << glog);
+    const bool lends = __shfl_sync(kFull, (int)ends, ql << glog) != 0;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      const float4 lx = shfl4(x[v], src_lane);
+      carry[v] = lends ? seg_f4zero() : lx;
+    }
+    chead = chead && !lends && lk == ckey;
+    ckey = lends ? kNoKey : lk;
+  }
+  // run left open at the warp end
+  if (ckey != kNoKey && ckey != a.sentinel && ws0 < ws1) {
+    const int side = chead ? 0 : 1;
+    if (q == 0) {
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int f4 = sub + v * 32;
+        if (f4 < D4) sm.part[side][warp * D4 + f4] = carry[v];
+      }
+    }
+    if (lane == 0) {
+      if (chead) {
+        sm.head_end[warp] = ws1;
+        sm.head_thru[warp] = 1;
+      } else {
+        sm.tail_valid[warp] = 1;
+        sm.tail_key[warp] = ckey;
+      }
+    }
+  }
+  pend.retire(a, sub);
+  __syncthreads();
+
+  // ---- runs cut between warps: the warp holding a run's start (group 0)
+  //      adds the head partials of the following warps in order ----
   int32_t* P = a.part_pos + (int64_t)blockIdx.x * 2;
   float4* GP = a.partial + (int64_t)blockIdx.x * 2 * D4;
-  if (ts >= 0) {
+  if (q == 0 && sm.tail_valid[warp]) {
     float4 s[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
       const int f4 = sub + v * 32;
-      s[v] = f4 < D4 ? sm.part[1][q * D4 + f4] : seg_f4zero();
+      s[v] = f4 < D4 ? sm.part[1][warp * D4 + f4] : seg_f4zero();
     }
-    int q2 = q + 1;
+    int w2 = warp + 1;
     bool thru = true;
-    int64_t end = B1;
-    while (q2 < NG && thru) {
-      if (sm.head_end[q2] < 0) break;   // empty group (past the end of the data)
+    int end = span;
+    while (w2 < kSegWarps && thru) {
+      if (sm.head_end[w2] < 0) break;
 #pragma unroll
       for (int v = 0; v < V; ++v) {
         const int f4 = sub + v * 32;
-        if (f4 < D4) seg_f4add(s[v], sm.part[0][q2 * D4 + f4]);
+        if (f4 < D4) seg_f4add(s[v], sm.part[0][w2 * D4 + f4]);
       }
-      thru = sm.head_thru[q2];
-      end = B0 + sm.head_end[q2];
-      ++q2;
+      thru = sm.head_thru[w2] != 0;
+      end = sm.head_end[w2];
+      ++w2;
     }
-    const uint32_t key = __ldg(a.keys + B0 + ts);
-    if (q2 == NG && thru) {
-      // the run continues into the next CTA: leave a tail partial
+    if (w2 == kSegWarps && thru) {
 #pragma unroll
       for (int v = 0; v < V; ++v) {
         const int f4 = sub + v * 32;
         if (f4 < D4) GP[D4 + f4] = s[v];
       }
-      if (sub == 0) P[1] = (int32_t)ts;
     } else {
-      finish_row<V>(a, key, B0 + ts, end, s, sub);
+      finish_row<V>(a, sm.tail_key[warp], B0 + end, s, sub);
     }
   }
-  // the run cut at the CTA start: group 0 sums the head partials it spans
-  if (q == 0) {
+  // ---- the run cut at the CTA start: warp 0 sums the head partials ----
+  if (warp == 0 && q == 0) {
     bool thru = false;
-    int64_t end = B0;
+    int end = 0;
     float4 s[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) s[v] = seg_f4zero();
     if (sm.head_end[0] >= 0) {
-      int q2 = 0;
+      int w2 = 0;
       thru = true;
-      while (q2 < NG && thru) {
-        if (sm.head_end[q2] < 0) { thru = false; break; }
+      while (w2 < kSegWarps && thru) {
+        if (sm.head_end[w2] < 0) {
+          thru = false;
+          break;
+        }
 #pragma unroll
         for (int v = 0; v < V; ++v) {
           const int f4 = sub + v * 32;
-          if (f4 < D4) seg_f4add(s[v], sm.part[0][q2 * D4 + f4]);
+          if (f4 < D4) seg_f4add(s[v], sm.part[0][w2 * D4 + f4]);
         }
-        thru = sm.head_thru[q2];
-        end = B0 + sm.head_end[q2];
-        ++q2;
+        thru = sm.head_thru[w2] != 0;
+        end = sm.head_end[w2];
+        ++w2;
       }
-      if (q2 < NG) thru = false;
+      if (w2 < kSegWarps) thru = false;
     }
 #pragma unroll
     for (int v = 0; v < V; ++v) {
@@ -386,7 +596,7 @@ __global__ void __launch_bounds__(kSegThreads) k_segreduce(const SegArgs a) {
       if (f4 < D4) GP[f4] = s[v];
     }
     if (sub == 0) {
-      P[0] = (int32_t)(end - B0);
+      P[0] = end;
       a.part_thru[blockIdx.x] = thru ? 1 : 0;
     }
   }
@@ -415,7 +625,6 @@ __global__ void __launch_bounds__(kSegThreads) k_seg_fixup(const SegArgs a, int 
     const int f4 = sub + v * 32;
     s[v] = f4 < D4 ? T[f4] : seg_f4zero();
   }
-  const int64_t start = (b - 1) * span + a.part_pos[(b - 1) * 2 + 1];
   int64_t c = b, end = pos;
   for (;;) {
     const float4* H = a.partial + c * 2 * D4;
@@ -428,7 +637,7 @@ __global__ void __launch_bounds__(kSegThreads) k_seg_fixup(const SegArgs a, int 
     if (!a.part_thru[c] || c + 1 >= n_blocks) break;
     ++c;
   }
-  finish_row<V>(a, key, start, end, s, sub);
+  finish_row<V>(a, key, end, s, sub);
 }
 
 // ---------------------------------------------------------------------------
@@ -473,7 +682,7 @@ emb_status launch_backward(emb_plan_s* p, const float* grad_out, const float* gr
   while ((1 << glog) < g) ++glog;
   a.glog = glog;
   const int NG = kSegWarps * (32 >> glog);
-  const int64_t span = (int64_t)NG * kUnit;
+  const int64_t span = kSegSpan;
   const int64_t n_blocks = (n + span - 1) / span;
   if (n_blocks > w.n_units_max) return EMB_ERR_UNSUPPORTED;
   a.partial = w.partial;
@@ -482,8 +691,9 @@ emb_status launch_backward(emb_plan_s* p, const float* grad_out, const float* gr
   if (want_dbg) {
     const int nb = (int)((n + kScanBlock - 1) / kScanBlock);
     k_rank_reduce<<<nb, kScanBlock, 0, stream>>>(skeys, n, p->key_total, w.scan_part);
-    k_rank_top<<<1, kScanBlock, 0, stream>>>(w.scan_part, nb, dbg->n_unique);
-    k_rank_down<<<nb, kScanBlock, 0, stream>>>(skeys, n, p->key_total, w.scan_part, w.run_head);
+    k_rank_top<<<1, kScanBlock, 0, stream>>>(w.scan_part, nb,
+                                             dbg->n_unique ? dbg->n_unique : reinterpret_cast<int64_t*>(w.n_runs));
+    k_rank_down<<<nb, kScanBlock, 0, stream>>>(skeys, n, p->key_total, w.scan_part, w.run_head, w.head_pos);
     a.rank = w.run_head;
     a.dbg_table = dbg->uniq_table;
     a.dbg_row = dbg->uniq_row;
@@ -498,6 +708,11 @@ emb_status launch_backward(emb_plan_s* p, const float* grad_out, const float* gr
   } else {
     k_segreduce<1><<<(unsigned)n_blocks, kSegThreads, 0, stream>>>(a);
     if (n_blocks > 1) k_seg_fixup<1><<<fix_grid, kSegThreads, 0, stream>>>(a, (int)n_blocks, span);
+  }
+  if (want_dbg && (dbg->uniq_table || dbg->uniq_row || dbg->counts)) {
+    const int64_t* nu = dbg->n_unique ? dbg->n_unique : reinterpret_cast<const int64_t*>(w.n_runs);
+    k_dbg_runs<<<p->sm_count * 4, 256, 0, stream>>>(skeys, n, p->key_total, w.head_pos, nu, p->table_base_d,
+                                                    p->n_tables, dbg->uniq_table, dbg->uniq_row, dbg->counts);
   }
   return cuda_status(cudaGetLastError());
 }
@@ -642,7 +857,7 @@ extern "C" emb_status emb_sparse_adagrad_noalloc(const int64_t* rows, int64_t n,
   while ((1 << glog) < g) ++glog;
   a.glog = glog;
   const int NG = kSegWarps * (32 >> glog);
-  const int64_t span = (int64_t)NG * kUnit;
+  const int64_t span = kSegSpan;
   const int64_t n_blocks = (n + span - 1) / span;
   a.partial = s->partial;
   a.part_pos = s->part_pos;

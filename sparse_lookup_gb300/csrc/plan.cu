@@ -27,6 +27,7 @@ void free_plan(emb_plan_s* p) {
   cudaFree(w.inv_n);
   cudaFree(w.hist);
   cudaFree(w.run_head);
+  cudaFree(w.head_pos);
   cudaFree(w.n_runs);
   cudaFree(w.scan_part);
   cudaFree(w.partial);
@@ -218,6 +219,7 @@ extern "C" emb_status emb_plan_create(const emb_column_desc* cols, int32_t n_col
       w.lookback = w.tile_ctr + 4;
     }
     if (e == cudaSuccess) e = dmalloc(&w.run_head, n + 1, &total);
+    if (e == cudaSuccess) e = dmalloc(&w.head_pos, n, &total);
     if (e == cudaSuccess) e = dmalloc(&w.n_runs, 4, &total);
     if (e == cudaSuccess) e = dmalloc(&w.scan_part, (n + 1023) / 1024 + 64, &total);
     if (e == cudaSuccess) e = dmalloc(&w.partial, (size_t)w.n_units_max * 2 * (p->max_dim / 4), &total);

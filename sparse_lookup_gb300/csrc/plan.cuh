@@ -40,7 +40,8 @@ struct Workspace {
   uint32_t* hist = nullptr;        // [4][kRadix] digit counts of all passes
   uint32_t* lookback = nullptr;    // [max_tiles][kRadix] chained-scan words
   uint32_t* tile_ctr = nullptr;    // [4] tile tickets per pass
-  uint32_t* run_head = nullptr;    // [max_ids + 1] start of each run
+  uint32_t* run_head = nullptr;    // [max_ids + 1] debug: runs started at or before each position
+  uint32_t* head_pos = nullptr;    // [max_ids] debug: position of each run's first entry
   uint32_t* n_runs = nullptr;      // [1]
   uint32_t* scan_part = nullptr;   // per-block partial counts for run compaction
   float4* partial = nullptr;       // [n_units][2][max_dim/4] cut-run partial sums
