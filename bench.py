@@ -135,6 +135,9 @@ def make_workload(name, columns=None):
         return synth.tiny()
     if name == "dynamic":
         return synth.dynamic(C=columns) if columns else synth.dynamic()
+    if name == "dynamic-small":
+        # profiling size: 10 columns over a 2^24-slot table with 2^22 rows
+        return synth.dynamic(C=columns or 10, num_slots=1 << 24, row_capacity=1 << 22)
     raise SystemExit("unknown workload %s" % name)
 
 
@@ -325,7 +328,7 @@ def run_reference(args):
     per = max(2.0, 20.0 / max(1, args.steps + args.warmup))
     vals = []
     for i in range(args.warmup + args.steps):
-        if args.workload == "dynamic":
+        if args.workload.startswith("dynamic"):
             rate, sample = cpu_dynamic_sample(w, budget_s=per)
         else:
             tables = [None if t is None else synth.make_table(t, "cpu") for t in w.tables]
@@ -350,7 +353,7 @@ def run_reference(args):
 def metric_name(workload):
     if workload in TRAIN_WORKLOADS:
         return "pooled rows gathered/sec (fwd+bwd+update)"
-    if workload == "dynamic":
+    if workload.startswith("dynamic"):
         return "pooled rows gathered/sec (hash+fwd+bwd+update+expiry)"
     return "pooled rows gathered/sec (forward)"
 
@@ -373,7 +376,7 @@ def run_ours(args):
     w = make_workload(args.workload, args.columns)
     l2 = torch.cuda.get_device_properties(local).L2_cache_size
     flush = torch.empty(int(2 * l2 // 4), dtype=torch.float32, device=dev)
-    if args.workload == "dynamic":
+    if args.workload.startswith("dynamic"):
         res = bench_dynamic(torch, sl, w, args, dev, stream, flush)
     else:
         res = bench_plan(torch, sl, w, args, dev, stream, flush, train=args.workload in TRAIN_WORKLOADS)
@@ -603,9 +606,15 @@ def bench_dynamic(torch, sl, w, args, dev, stream, flush):
         marks["step"] = (a, e)
         state["t"] = t + 1
 
+    # the first call meets a cold table (every key new); reported beside the
+    # steady-state steps, not inside them
+    warm = []
     for _ in range(max(3, args.warmup)):
-        body(0, {})
+        m = {}
+        body(0, m)
+        warm.append(m)
     torch.cuda.synchronize()
+    first_step = {k: warm[0][k][0].elapsed_time(warm[0][k][1]) for k in ("hash", "fwd", "bwd", "evict", "step")}
     clk = ClockSampler(torch.cuda.current_device())
     clk.start()
     time.sleep(0.3)
@@ -623,7 +632,8 @@ def bench_dynamic(torch, sl, w, args, dev, stream, flush):
            "ms_step": statistics.mean(times["step"]), "wall": wall,
            "config": {"ids_per_step": n_last, "rows_gathered_per_step": valid, "num_slots": ex["num_slots"],
                       "row_capacity": ex["row_capacity"], "threshold": ex["threshold"], "ttl": ex["ttl"],
-                      "stream_steps_timed": [t_first, state["t"] - 1]},
+                      "stream_steps_timed": [t_first, state["t"] - 1],
+                      "cold_first_step_ms": first_step},
            "launches": args.steps * (16 + 1 + (3 + plan_sort_passes(plan)) + 1)}
     if ht.device_status() not in (0, 5) or plan.device_status() != 0:
         raise SystemExit("device status after the timed steps")

@@ -163,22 +163,36 @@ __global__ void __launch_bounds__(256) k_hash_probe(const HashArgs h, const int3
     rows_out[i] = state;
     return;
   }
-  // count and touch in ONE atomic update of (state, last_seen), so that "first
-  // occurrence of this call" and "count reached the threshold" are decided on
-  // the same order of updates
+  // Count and touch with atomic updates of the whole (state, last_seen) word,
+  // so that "first occurrence of this call" and "count reached the threshold"
+  // are decided on one order of updates.  Only the occurrences that find
+  // last_seen behind the current step race by CAS to set it; once it equals
+  // the step it stays there for the rest of the call, and every later
+  // occurrence counts with one atomic add (no retry loop, which on hot keys
+  // of a cold table would serialise thousands of CAS attempts).  Adding
+  // 2^64 - 1 takes one off the low half without a borrow into last_seen,
+  // since a not-yet-admitted state is negative (count below 2^31 - 1).
   unsigned long long* sw = reinterpret_cast<unsigned long long*>(&s->state);
-  unsigned long long cur = *(volatile unsigned long long*)sw, prev;
-  int32_t old;
-  do {
+  unsigned long long prev = *(volatile unsigned long long*)sw;
+  int32_t old = (int32_t)(uint32_t)(prev & 0xffffffffull);
+  bool counted = false;
+  while (old < 0 && (uint32_t)(prev >> 32) != step) {
+    const unsigned long long nxt = ((unsigned long long)step << 32) | ((uint32_t)old - 1u);
+    const unsigned long long cur = atomicCAS(sw, prev, nxt);
+    if (cur == prev) {
+      counted = true;
+      break;
+    }
     prev = cur;
     old = (int32_t)(uint32_t)(prev & 0xffffffffull);
-    if (old >= 0) break;   // admitted meanwhile (not within one call; kept for safety)
-    const unsigned long long nxt = ((unsigned long long)step << 32) | (uint32_t)(old - 1);
-    cur = atomicCAS(sw, prev, nxt);
-  } while (cur != prev);
-  if (old >= 0) {
+  }
+  if (old >= 0) {   // admitted meanwhile (not within one call; kept for safety)
     rows_out[i] = old;
     return;
+  }
+  if (!counted) {
+    prev = atomicAdd(sw, ~0ull);
+    old = (int32_t)(uint32_t)(prev & 0xffffffffull);
   }
   const uint32_t old_seen = (uint32_t)(prev >> 32);
   const int32_t count_old = -1 - old, count_new = count_old + 1;
