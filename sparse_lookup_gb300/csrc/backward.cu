@@ -9,12 +9,14 @@
 //   1-2. radix_sort_pairs (radix.cuh) -- one read of the keys for the digit
 //                       histograms, then one stable chained-scan scatter per
 //                       8-bit digit with bounded decoupled look-back;
-//   3. k_segreduce   -- lane groups of dim/4 lanes take equal ranges of sorted
-//                       contributions, gather scale * G rows with 16-byte
-//                       loads and sum each run; a run owned by one group is
-//                       finished at once (fp32 Adagrad on its row); runs cut
-//                       by group boundaries are combined in shared memory in
-//                       group order, runs cut by CTA boundaries leave partials;
+//   3. k_segreduce   -- lane groups of dim/4 lanes each walk an equal
+//                       contiguous range of sorted contributions in order,
+//                       gathering scale * G rows with 16-byte loads (several
+//                       in flight) and summing each run; a run that begins
+//                       and ends in one range is finished at once (fp32
+//                       Adagrad on its row); runs cut by range boundaries are
+//                       combined in shared memory in range order, runs cut by
+//                       CTA boundaries leave partials;
 //   4. k_seg_fixup   -- sums the CTA partials of each cut run in CTA order and
 //                       finishes it.
 // The sum order is fixed by the sort (stable) and the range layout, so a run
@@ -324,44 +326,58 @@ struct PendingRow {
 
 constexpr int kSegSpan = 2048;                    // sorted entries per CTA
 constexpr int kSegPerThread = kSegSpan / kSegThreads;
-constexpr int kSegWarpSpan = kSegSpan / kSegWarps;
+// Gradient rows in flight per lane group (4 rows of V float4 per lane) and
+// resident CTAs per SM: measured on the training and sequence workloads,
+// three CTAs of 4-deep groups beat two CTAs of 4-, 6- or 8-deep groups (more
+// warps hide the gather latency better than deeper groups); rows wider than
+// 128 floats keep two CTAs to stay within the registers.
+template <int V>
+struct SegDepth {
+  static constexpr int value = 4;
+  static constexpr int ctas = V == 1 ? 3 : 2;
+};
+constexpr int kSegMaxGroups = kSegWarps * 32;     // dim 4: 32 one-lane groups per warp
 constexpr uint32_t kOffPad = 0x80000000u;         // offset refers to grad_seq
 constexpr uint32_t kNoKey = 0xFFFFFFFFu;          // above every key and the sentinel
 
-struct SegSmem3 {
-  float4 part[2][kSegWarps * 64];   // head / tail partial of each warp
-  uint32_t key[kSegSpan];
-  uint32_t off[kSegSpan];           // float4 offset of the gradient row (+ kOffPad)
-  float scale[kSegSpan];
-  uint8_t d4[kSegSpan];             // float4 slots of the row
-  uint32_t tail_key[kSegWarps];     // per warp: key of the run left open at its end
-  int32_t tail_valid[kSegWarps];
-  int32_t head_end[kSegWarps];      // per warp: end of the run cut at its start, -1 if none
-  int32_t head_thru[kSegWarps];     // per warp: that run covers the whole range and goes on
+// One decoded contribution: its row key, the float4 offset of its gradient
+// row (kOffPad: in grad_seq), the scale (1/n of a mean bag, else 1) and the
+// float4 count of the row.
+struct __align__(16) SegRec {
+  uint32_t key;
+  uint32_t off;
+  float scale;
+  uint32_t d4;
 };
 
-__device__ __forceinline__ float4 shfl_up4(const float4& x, int d) {
-  return make_float4(__shfl_up_sync(kFull, x.x, d), __shfl_up_sync(kFull, x.y, d), __shfl_up_sync(kFull, x.z, d),
-                     __shfl_up_sync(kFull, x.w, d));
-}
+struct SegSmem {
+  SegRec rec[kSegSpan];
+  float4 part[2][kSegWarps * 64];       // head / tail partial of each lane group
+  int32_t head_end[kSegMaxGroups];      // end of the run cut at the group's start, -1 if none
+  uint32_t tail_key[kSegMaxGroups];     // key of the run left open at the group's end
+  uint8_t head_thru[kSegMaxGroups];     // that head run covers the whole range and goes on
+  uint8_t tail_valid[kSegMaxGroups];
+};
 
-__device__ __forceinline__ float4 shfl4(const float4& x, int src) {
-  return make_float4(__shfl_sync(kFull, x.x, src), __shfl_sync(kFull, x.y, src), __shfl_sync(kFull, x.z, src),
-                     __shfl_sync(kFull, x.w, src));
-}
-
-// Runs of sorted contributions are reduced by WARPS: a warp walks its range
-// G entries at a time (one per lane group of dim/4 lanes), a segmented scan by
-// key over the groups (lane shuffles) sums equal keys, and every group whose
-// entry ends a run applies the Adagrad step in the same predicated instruction
-// stream -- groups never diverge into separate update paths.
+// Runs of sorted contributions are reduced by LANE GROUPS of dim/4 lanes
+// (one float4 column slice per lane): the CTA's span is cut into equal
+// contiguous ranges, one per group, and a group walks its range in order,
+// SegDepth<V> gradient rows in flight, adding each row into the open run's sum and
+// closing the run where the key changes.  A run closed inside the range that
+// also began there is finished at once (Adagrad on its row, deferred by one
+// run so the weight/accumulator loads overlap the next gathers); a run cut at
+// the range start leaves a head partial and one open at the range end a tail
+// partial, combined in group order after a barrier (and across CTAs by
+// k_seg_fixup).
 template <int V>
-__global__ void __launch_bounds__(kSegThreads, 3) k_segreduce(const SegArgs a) {
-  __shared__ SegSmem3 sm;
+__global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(const SegArgs a) {
+  __shared__ SegSmem sm;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int glog = a.glog;
   const int G = 32 >> glog;
   const int q = lane >> glog, sub = lane & ((1 << glog) - 1);
+  const int NG = kSegWarps * G;
+  const int grp = warp * G + q;
   const int64_t B0 = (int64_t)blockIdx.x * kSegSpan;
   const int64_t B1 = min(B0 + (int64_t)kSegSpan, a.n);
   const int span = (int)(B1 - B0);
@@ -376,11 +392,14 @@ __global__ void __launch_bounds__(kSegThreads, 3) k_segreduce(const SegArgs a) {
 #pragma unroll
   for (int k = 0; k < kSegPerThread; ++k) {
     const int e = k * kSegThreads + tid;
-    uint32_t key = a.sentinel, off = 0;
-    float sc = 0.0f;
-    int d4 = 0;
+    SegRec r;
+    r.key = a.sentinel;
+    r.off = 0u;
+    r.scale = 0.0f;
+    r.d4 = 0u;
     if (e < span) {
-      key = __ldg(a.keys + B0 + e);
+      const uint32_t key = __ldg(a.keys + B0 + e);
+      r.key = key;
       if (key != a.sentinel && (B0 + e == 0 || __ldg(a.keys + B0 + e - 1) != key)) {
         ptc.seek(a, key);
         const TableMeta& tm = a.tables[ptc.t];
@@ -395,200 +414,190 @@ __global__ void __launch_bounds__(kSegThreads, 3) k_segreduce(const SegArgs a) {
             lkey = key;
             ld4 = a.tables[table_of_key(a.table_base, a.n_tables, key)].dim4;
           }
-          d4 = ld4;
-          sc = 1.0f;
-          off = kOffPad | (val & ~kPadBit);
+          r.d4 = (uint32_t)ld4;
+          r.scale = 1.0f;
+          r.off = kOffPad | (val & ~kPadBit);
         } else {
           const uint32_t c = div_magic32(val, a.bdiv);
           const uint32_t b = val - c * (uint32_t)a.batch;
           const int4 cg = __ldg(a.colg + c);
-          sc = cg.y ? __ldg(a.inv_n + val) : 1.0f;
-          d4 = cg.z;
-          off = (uint32_t)(((int64_t)b * a.ldg + cg.x) >> 2);
+          r.scale = cg.y ? __ldg(a.inv_n + val) : 1.0f;
+          r.d4 = (uint32_t)cg.z;
+          r.off = (uint32_t)(((int64_t)b * a.ldg + cg.x) >> 2);
         }
       }
     }
-    sm.key[e] = key;
-    sm.off[e] = off;
-    sm.scale[e] = sc;
-    sm.d4[e] = (uint8_t)d4;
+    sm.rec[e] = r;
   }
-  if (lane == 0) {
-    sm.tail_valid[warp] = 0;
-    sm.head_end[warp] = -1;
-    sm.head_thru[warp] = 0;
+  for (int g = tid; g < NG; g += kSegThreads) {
+    sm.head_end[g] = -1;
+    sm.head_thru[g] = 0;
+    sm.tail_valid[g] = 0;
   }
   __syncthreads();
 
-  // ---- per warp: segmented reduction over its range ----
-  const int ws0 = min(warp * kSegWarpSpan, span), ws1 = min(ws0 + kSegWarpSpan, span);
-  const uint32_t key_after = ws1 < span ? sm.key[ws1] : (B1 < a.n ? __ldg(a.keys + B1) : kNoKey);
-  uint32_t ckey = kNoKey;   // run open at the chunk start, summed in `carry`
-  bool chead = false;       // that run started before this warp's range
-  float4 carry[V];
-#pragma unroll
-  for (int v = 0; v < V; ++v) carry[v] = seg_f4zero();
-  if (ws0 < ws1) {
-    ckey = sm.key[ws0];
-    const uint32_t prev = ws0 > 0 ? sm.key[ws0 - 1] : (B0 > 0 ? __ldg(a.keys + B0 - 1) : kNoKey);
+  // ---- per lane group: its contiguous range, in order ----
+  const int R = kSegSpan / NG;
+  const int r0 = min(grp * R, span), r1 = min(r0 + R, span);
+  uint32_t ckey = kNoKey;   // key of the open run
+  bool chead = false;       // the open run began before this range
+  if (r0 < r1) {
+    ckey = sm.rec[r0].key;
+    const uint32_t prev = r0 > 0 ? sm.rec[r0 - 1].key : (B0 > 0 ? __ldg(a.keys + B0 - 1) : kNoKey);
     chead = prev == ckey && ckey != a.sentinel;
   }
+  float4 acc[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) acc[v] = seg_f4zero();
   TableCursor tc;
   PendingRow<V> pend;
-  for (int c0 = ws0; c0 < ws1; c0 += G) {
-    const int e = c0 + q;
-    const bool valid = e < ws1;
-    const uint32_t key = valid ? sm.key[e] : kNoKey;
-    float4 x[V];
-    {
-      const uint32_t off = valid ? sm.off[e] : 0u;
-      const int d4 = valid ? (int)sm.d4[e] : 0;
-      const float sc = valid ? sm.scale[e] : 0.0f;
-      const float* src = (off & kOffPad) ? a.grad_seq + (int64_t)(off & ~kOffPad) * 4
-                                         : a.grad_out + (int64_t)off * 4;
+  constexpr int kSegU = SegDepth<V>::value;
+  for (int i0 = r0; i0 < r1; i0 += kSegU) {
+    uint32_t key[kSegU];
+    float sc[kSegU];
+    float4 x[kSegU][V];
+#pragma unroll
+    for (int u = 0; u < kSegU; ++u) {
+      const int e = i0 + u;
+      const SegRec r = e < r1 ? sm.rec[e] : SegRec{kNoKey, 0u, 0.0f, 0u};
+      key[u] = r.key;
+      sc[u] = r.scale;
+      const float* src = (r.off & kOffPad) ? a.grad_seq + (int64_t)(r.off & ~kOffPad) * 4
+                                           : a.grad_out + (int64_t)r.off * 4;
 #pragma unroll
       for (int v = 0; v < V; ++v) {
         const int f4 = sub + v * 32;
-        x[v] = seg_f4zero();
-        if (f4 < d4) {
-          x[v] = __ldg(reinterpret_cast<const float4*>(src + f4 * 4));
-          if (sc != 1.0f) {
-            x[v].x *= sc;
-            x[v].y *= sc;
-            x[v].z *= sc;
-            x[v].w *= sc;
+        x[u][v] = f4 < (int)r.d4 ? __ldg(reinterpret_cast<const float4*>(src + f4 * 4)) : seg_f4zero();
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kSegU; ++u) {
+      if (i0 + u < r1 && key[u] != ckey) {   // the open run ends before this entry
+        if (ckey != a.sentinel) {
+          if (chead) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) {
+              const int f4 = sub + v * 32;
+              if (f4 < D4) sm.part[0][grp * D4 + f4] = acc[v];
+            }
+            if (sub == 0) sm.head_end[grp] = i0 + u;
+          } else {
+            pend.retire(a, sub);
+            tc.seek(a, ckey);
+            pend.issue(a, tc, ckey, B0 + i0 + u, acc, sub);
           }
         }
+        ckey = key[u];
+        chead = false;
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[v] = seg_f4zero();
       }
-    }
-    // segmented inclusive scan over the lane groups, by key
-    for (int d = 1; d < G; d <<= 1) {
-      const uint32_t ky = __shfl_up_sync(kFull, key, d << glog);
 #pragma unroll
       for (int v = 0; v < V; ++v) {
-        const float4 y = shfl_up4(x[v], d << glog);
-        if (q >= d && ky == key) seg_f4add(x[v], y);
+        acc[v].x = fmaf(x[u][v].x, sc[u], acc[v].x);
+        acc[v].y = fmaf(x[u][v].y, sc[u], acc[v].y);
+        acc[v].z = fmaf(x[u][v].z, sc[u], acc[v].z);
+        acc[v].w = fmaf(x[u][v].w, sc[u], acc[v].w);
       }
     }
-    const bool in_carry = key == ckey;
-    if (in_carry) {
-#pragma unroll
-      for (int v = 0; v < V; ++v) seg_f4add(x[v], carry[v]);
-    }
-    // does this entry end its run?
-    uint32_t nk = __shfl_down_sync(kFull, key, (1 << glog) & 31);
-    if (q == G - 1 || e + 1 >= ws1) nk = (e + 1 < ws1) ? sm.key[e + 1] : key_after;
-    const bool ends = valid && key != a.sentinel && nk != key;
-    if (ends) {
-      if (in_carry && chead) {
+  }
+  // the run open at the range end: finished here, or left as a partial
+  if (r0 < r1 && ckey != a.sentinel) {
+    const uint32_t key_after = r1 < span ? sm.rec[r1].key : (B1 < a.n ? __ldg(a.keys + B1) : kNoKey);
+    if (key_after != ckey) {
+      if (chead) {
 #pragma unroll
         for (int v = 0; v < V; ++v) {
           const int f4 = sub + v * 32;
-          if (f4 < D4) sm.part[0][warp * D4 + f4] = x[v];
+          if (f4 < D4) sm.part[0][grp * D4 + f4] = acc[v];
         }
-        if (sub == 0) sm.head_end[warp] = e + 1;
+        if (sub == 0) sm.head_end[grp] = r1;
       } else {
         pend.retire(a, sub);
-        tc.seek(a, key);
-        pend.issue(a, tc, key, B0 + e + 1, x, sub);
+        tc.seek(a, ckey);
+        pend.issue(a, tc, ckey, B0 + r1, acc, sub);
       }
-    }
-    // the run reaching the chunk end is carried into the next chunk
-    const int ql = min(G - 1, ws1 - 1 - c0);
-    const int src_lane = (ql << glog) + sub;
-    const uint32_t lk = __shfl_sync(kFull, key, ql << glog);
-    const bool lends = __shfl_sync(kFull, (int)ends, ql << glog) != 0;
-#pragma unroll
-    for (int v = 0; v < V; ++v) {
-      const float4 lx = shfl4(x[v], src_lane);
-      carry[v] = lends ? seg_f4zero() : lx;
-    }
-    chead = chead && !lends && lk == ckey;
-    ckey = lends ? kNoKey : lk;
-  }
-  // run left open at the warp end
-  if (ckey != kNoKey && ckey != a.sentinel && ws0 < ws1) {
-    const int side = chead ? 0 : 1;
-    if (q == 0) {
+    } else {
+      const int side = chead ? 0 : 1;
 #pragma unroll
       for (int v = 0; v < V; ++v) {
         const int f4 = sub + v * 32;
-        if (f4 < D4) sm.part[side][warp * D4 + f4] = carry[v];
+        if (f4 < D4) sm.part[side][grp * D4 + f4] = acc[v];
       }
-    }
-    if (lane == 0) {
-      if (chead) {
-        sm.head_end[warp] = ws1;
-        sm.head_thru[warp] = 1;
-      } else {
-        sm.tail_valid[warp] = 1;
-        sm.tail_key[warp] = ckey;
+      if (sub == 0) {
+        if (chead) {
+          sm.head_end[grp] = r1;
+          sm.head_thru[grp] = 1;
+        } else {
+          sm.tail_valid[grp] = 1;
+          sm.tail_key[grp] = ckey;
+        }
       }
     }
   }
   pend.retire(a, sub);
   __syncthreads();
 
-  // ---- runs cut between warps: the warp holding a run's start (group 0)
-  //      adds the head partials of the following warps in order ----
+  // ---- runs cut between groups: the group holding a run's start adds the
+  //      head partials of the following groups in order ----
   int32_t* P = a.part_pos + (int64_t)blockIdx.x * 2;
   float4* GP = a.partial + (int64_t)blockIdx.x * 2 * D4;
-  if (q == 0 && sm.tail_valid[warp]) {
+  if (sm.tail_valid[grp]) {
     float4 s[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
       const int f4 = sub + v * 32;
-      s[v] = f4 < D4 ? sm.part[1][warp * D4 + f4] : seg_f4zero();
+      s[v] = f4 < D4 ? sm.part[1][grp * D4 + f4] : seg_f4zero();
     }
-    int w2 = warp + 1;
+    int g2 = grp + 1;
     bool thru = true;
     int end = span;
-    while (w2 < kSegWarps && thru) {
-      if (sm.head_end[w2] < 0) break;
+    while (g2 < NG && thru) {
+      if (sm.head_end[g2] < 0) break;
 #pragma unroll
       for (int v = 0; v < V; ++v) {
         const int f4 = sub + v * 32;
-        if (f4 < D4) seg_f4add(s[v], sm.part[0][w2 * D4 + f4]);
+        if (f4 < D4) seg_f4add(s[v], sm.part[0][g2 * D4 + f4]);
       }
-      thru = sm.head_thru[w2] != 0;
-      end = sm.head_end[w2];
-      ++w2;
+      thru = sm.head_thru[g2] != 0;
+      end = sm.head_end[g2];
+      ++g2;
     }
-    if (w2 == kSegWarps && thru) {
+    if (g2 == NG && thru) {
 #pragma unroll
       for (int v = 0; v < V; ++v) {
         const int f4 = sub + v * 32;
         if (f4 < D4) GP[D4 + f4] = s[v];
       }
     } else {
-      finish_row<V>(a, sm.tail_key[warp], B0 + end, s, sub);
+      finish_row<V>(a, sm.tail_key[grp], B0 + end, s, sub);
     }
   }
-  // ---- the run cut at the CTA start: warp 0 sums the head partials ----
-  if (warp == 0 && q == 0) {
+  // ---- the run cut at the CTA start: group 0 sums the head partials ----
+  if (grp == 0) {
     bool thru = false;
     int end = 0;
     float4 s[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) s[v] = seg_f4zero();
     if (sm.head_end[0] >= 0) {
-      int w2 = 0;
+      int g2 = 0;
       thru = true;
-      while (w2 < kSegWarps && thru) {
-        if (sm.head_end[w2] < 0) {
+      while (g2 < NG && thru) {
+        if (sm.head_end[g2] < 0) {
           thru = false;
           break;
         }
 #pragma unroll
         for (int v = 0; v < V; ++v) {
           const int f4 = sub + v * 32;
-          if (f4 < D4) seg_f4add(s[v], sm.part[0][w2 * D4 + f4]);
+          if (f4 < D4) seg_f4add(s[v], sm.part[0][g2 * D4 + f4]);
         }
-        thru = sm.head_thru[w2] != 0;
-        end = sm.head_end[w2];
-        ++w2;
+        thru = sm.head_thru[g2] != 0;
+        end = sm.head_end[g2];
+        ++g2;
       }
-      if (w2 < kSegWarps) thru = false;
+      if (g2 < NG) thru = false;
     }
 #pragma unroll
     for (int v = 0; v < V; ++v) {
