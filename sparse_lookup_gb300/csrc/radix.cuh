@@ -9,7 +9,8 @@
 // latches EMB_ERR_TIMEOUT instead of hanging.
 //
 // The element count may live in device memory (n_dev != nullptr): grids are
-// then sized for the capacity and tiles past the count do nothing.
+// then sized for the capacity, the count is clamped to it and tiles past the
+// count do nothing.
 #pragma once
 
 #include "plan.cuh"
@@ -20,6 +21,7 @@ constexpr uint32_t kFlagAgg = 1u << 30;
 constexpr uint32_t kFlagInc = 2u << 30;
 constexpr uint32_t kCountMask = (1u << 30) - 1;
 constexpr int kSpinLimit = 1 << 22;
+constexpr int kLookWin = 8;   // look-back words loaded per round trip
 constexpr int kSortWarps = kSortThreads / 32;
 
 template <class K>
@@ -46,8 +48,11 @@ struct SortSmemT {
   uint32_t tile;
 };
 
+// Element count: n, or the count in device memory clamped to the capacity n.
 __device__ __forceinline__ int64_t sort_count(int64_t n, const uint32_t* n_dev) {
-  return n_dev ? (int64_t)*((volatile const uint32_t*)n_dev) : n;
+  if (!n_dev) return n;
+  const int64_t c = (int64_t)*((volatile const uint32_t*)n_dev);
+  return c < n ? c : n;
 }
 
 template <class K>
@@ -65,6 +70,21 @@ __global__ void __launch_bounds__(512) k_digit_hist_t(const K* __restrict__ keys
   __syncthreads();
   for (int i = threadIdx.x; i < passes * kRadix; i += blockDim.x)
     if (h[i]) atomicAdd(&hist[i], h[i]);
+}
+
+// Lanes of the warp holding the same digit d, found with one ballot per digit
+// bit: the mask starts full and each ballot keeps the lanes that agree with
+// this lane on that bit.  BITS = kRadixBits + 1 when some lanes hold the "no
+// item" marker kRadix.  All lanes must call.
+template <int BITS>
+__device__ __forceinline__ unsigned warp_match_digit(uint32_t d) {
+  unsigned peers = kFull;
+#pragma unroll
+  for (int b = 0; b < BITS; ++b) {
+    const unsigned m = __ballot_sync(kFull, (d >> b) & 1u);
+    peers &= ((d >> b) & 1u) ? m : ~m;
+  }
+  return peers;
 }
 
 // Exclusive scan over the first 256 threads' values (all threads call).
@@ -86,50 +106,55 @@ __device__ __forceinline__ uint32_t sort_scan256(uint32_t v, uint32_t* wsum) {
 }
 
 template <class K>
-__global__ void __launch_bounds__(kSortThreads, 2)
-    k_onesweep_t(const K* __restrict__ kin, const uint32_t* __restrict__ vin, K* __restrict__ kout,
-                 uint32_t* __restrict__ vout, int64_t n0, const uint32_t* n_dev, int shift,
-                 const uint32_t* __restrict__ hist, uint32_t* lookback, uint32_t* tile_ctr, uint32_t* status) {
+__device__ __forceinline__ uint32_t sort_digit(K k, int shift) {
+  return (uint32_t)(k >> shift) & (uint32_t)(kRadix - 1);
+}
+
+// One tile of a pass: rank the items by digit within the tile (stable: warp
+// order, then item order, then lane order), publish the tile's digit counts,
+// place the items in shared memory in digit order, find the tile's global
+// digit offsets by look-back, write out.  FULL: the tile holds TILE items
+// (no per-item bounds, one ballot less).
+template <class K>
+__device__ __forceinline__ void onesweep_tile(SortSmemT<K>& sm, const K* __restrict__ kin,
+                                              const uint32_t* __restrict__ vin, K* __restrict__ kout,
+                                              uint32_t* __restrict__ vout, uint32_t n, uint32_t t, int tile_n,
+                                              int shift, uint32_t* lookback, uint32_t* status) {
+  const bool FULL = tile_n == SortSmemT<K>::kTile;
   constexpr int ITEMS = SortItems<K>::value;
   constexpr int TILE = SortSmemT<K>::kTile;
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  SortSmemT<K>& sm = *reinterpret_cast<SortSmemT<K>*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t n = sort_count(n0, n_dev);
-  const int64_t tiles = (n + TILE - 1) / TILE;
-  if (tid == 0) sm.tile = atomicAdd(tile_ctr, 1u);
-  for (int i = tid; i < kSortWarps * kRadix; i += kSortThreads) (&sm.whist[0][0])[i] = 0;
-  const uint32_t hs = sort_scan256(tid < kRadix ? __ldg(hist + tid) : 0u, sm.wsum);
-  if (tid < kRadix) sm.hscan[tid] = hs;
-  __syncthreads();
-  const uint32_t t = sm.tile;
-  if ((int64_t)t >= tiles) return;   // past the data: nobody waits on this ticket
-  const int64_t base = (int64_t)t * TILE;
-  const int64_t wbase = base + (int64_t)warp * 32 * ITEMS;
+  const int w0 = warp * 32 * ITEMS;            // the warp's first item in the tile
+  const K* wk = kin + (size_t)t * TILE + w0;
+  const uint32_t* wv = vin + (size_t)t * TILE + w0;
 
   K k[ITEMS];
-  uint32_t v[ITEMS], r[ITEMS];
+  uint32_t v[ITEMS];
+  uint32_t r2[(ITEMS + 1) / 2];   // in-warp ranks (< 2^16), two per register
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) {
-    const int64_t idx = wbase + i * 32 + lane;
-    const bool ok = idx < n;
-    k[i] = ok ? kin[idx] : (K)0;
-    v[i] = ok ? vin[idx] : 0u;
+    const int o = i * 32 + lane;
+    const bool ok = FULL || w0 + o < tile_n;
+    k[i] = ok ? wk[o] : (K)0;
+    v[i] = ok ? wv[o] : 0u;
   }
   const unsigned lt = (1u << lane) - 1u;
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) {
-    const int64_t idx = wbase + i * 32 + lane;
-    const uint32_t d = idx < n ? (uint32_t)((k[i] >> shift) & (kRadix - 1)) : (uint32_t)kRadix;
-    const unsigned peers = __match_any_sync(kFull, d);
-    const int leader = __ffs(peers) - 1;
+    const bool ok = FULL || w0 + i * 32 + lane < tile_n;
+    const uint32_t d = ok ? sort_digit(k[i], shift) : (uint32_t)kRadix;
+    const unsigned peers = FULL ? warp_match_digit<kRadixBits>(d) : warp_match_digit<kRadixBits + 1>(d);
+    const int leader = 31 - __clz(peers);
     uint32_t old = 0;
-    if (lane == leader && d < (uint32_t)kRadix) {
+    if (lane == leader && ok) {
       old = sm.whist[warp][d];
       sm.whist[warp][d] = old + __popc(peers);
     }
     old = __shfl_sync(kFull, old, leader);
-    r[i] = old + __popc(peers & lt);
+    __syncwarp();   // the counter update is seen by the next item's leader
+    const uint32_t rank = old + __popc(peers & lt);
+    if (i & 1) r2[i >> 1] |= rank << 16;
+    else r2[i >> 1] = rank;
   }
   __syncthreads();
 
@@ -140,57 +165,100 @@ __global__ void __launch_bounds__(kSortThreads, 2)
       sm.whist[w][tid] = cnt;
       cnt += c;
     }
-    volatile uint32_t* mine = lookback + (int64_t)t * kRadix + tid;
-    *mine = (t == 0 ? kFlagInc : kFlagAgg) | cnt;
+    *(volatile uint32_t*)(lookback + (size_t)t * kRadix + tid) = (t == 0 ? kFlagInc : kFlagAgg) | cnt;
   }
   const uint32_t ds = sort_scan256(cnt, sm.wsum);
   if (tid < kRadix) {
     sm.dstart[tid] = ds;
+    for (int w = 0; w < kSortWarps; ++w) sm.whist[w][tid] += ds;   // slot of each warp's first item of the digit
+  }
+  __syncthreads();
+  // the tile's items into shared memory in digit order; this frees their
+  // registers before the look-back below
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    if (FULL || w0 + i * 32 + lane < tile_n) {
+      const uint32_t rank = (i & 1) ? r2[i >> 1] >> 16 : r2[i >> 1] & 0xffffu;
+      const uint32_t pos = sm.whist[warp][sort_digit(k[i], shift)] + rank;
+      sm.keys[pos] = k[i];
+      sm.vals[pos] = v[i];
+    }
+  }
+  if (tid < kRadix) {
     uint32_t excl = 0;
     if (t > 0) {
+      // Walk back kLookWin predecessors per round trip: their words are
+      // loaded together, then taken newest first, summing aggregates up to
+      // the first inclusive prefix.  A word not yet published stops the
+      // round; the next round starts at it.  Tile 0 always publishes an
+      // inclusive prefix, so the walk never passes it.
       int64_t j = (int64_t)t - 1;
       int spins = 0;
-      while (j >= 0) {
-        const uint32_t w = *(volatile const uint32_t*)(lookback + j * kRadix + tid);
-        const uint32_t flag = w & ~kCountMask;
-        if (flag == 0u) {
+      bool done = false;
+      while (!done) {
+        uint32_t w[kLookWin];
+#pragma unroll
+        for (int q = 0; q < kLookWin; ++q)
+          w[q] = j - q >= 0 ? *(volatile const uint32_t*)(lookback + (j - q) * kRadix + tid) : kFlagInc;
+        int q = 0;
+#pragma unroll
+        for (int qq = 0; qq < kLookWin; ++qq) {
+          if (q == qq) {
+            const uint32_t flag = w[qq] & ~kCountMask;
+            if (flag != 0u) {
+              excl += w[qq] & kCountMask;
+              if (flag == kFlagInc) done = true;
+              else ++q;
+            }
+          }
+        }
+        if (done) break;
+        j -= q;
+        if (q < kLookWin) {   // word j is not published yet
           if (++spins > kSpinLimit) {
             latch(status, EMB_ERR_TIMEOUT);
             break;
           }
           __nanosleep(32);
-          continue;
         }
-        excl += w & kCountMask;
-        if (flag == kFlagInc) break;
-        --j;
       }
-      *(volatile uint32_t*)(lookback + (int64_t)t * kRadix + tid) = kFlagInc | ((excl + cnt) & kCountMask);
+      *(volatile uint32_t*)(lookback + (size_t)t * kRadix + tid) = kFlagInc | ((excl + cnt) & kCountMask);
     }
-    sm.goff[tid] = sm.hscan[tid] + excl;
+    // output position of shared slot j of this digit: goff + (j - dstart)
+    sm.goff[tid] = sm.hscan[tid] + excl - ds;
   }
   __syncthreads();
-#pragma unroll
-  for (int i = 0; i < ITEMS; ++i) {
-    const int64_t idx = wbase + i * 32 + lane;
-    if (idx < n) {
-      const uint32_t d = (uint32_t)((k[i] >> shift) & (kRadix - 1));
-      const uint32_t pos = sm.dstart[d] + sm.whist[warp][d] + r[i];
-      sm.keys[pos] = k[i];
-      sm.vals[pos] = v[i];
-    }
-  }
-  __syncthreads();
-  const int tile_n = (int)(n - base < TILE ? n - base : TILE);
-  for (int j = tid; j < tile_n; j += kSortThreads) {
+  for (int j = tid; j < (FULL ? TILE : tile_n); j += kSortThreads) {
     const K key = sm.keys[j];
-    const uint32_t d = (uint32_t)((key >> shift) & (kRadix - 1));
-    const uint64_t o = (uint64_t)sm.goff[d] + (uint64_t)(j - sm.dstart[d]);
-    if (o < (uint64_t)n) {   // always true unless a look-back wait gave up
+    const uint32_t o = sm.goff[sort_digit(key, shift)] + (uint32_t)j;
+    if (o < n) {   // always true unless a look-back wait gave up
       kout[o] = key;
       vout[o] = sm.vals[j];
     }
   }
+}
+
+template <class K>
+__global__ void __launch_bounds__(kSortThreads, 2)
+    k_onesweep_t(const K* __restrict__ kin, const uint32_t* __restrict__ vin, K* __restrict__ kout,
+                 uint32_t* __restrict__ vout, int64_t n0, const uint32_t* n_dev, int shift,
+                 const uint32_t* __restrict__ hist, uint32_t* lookback, uint32_t* tile_ctr, uint32_t* status) {
+  constexpr int TILE = SortSmemT<K>::kTile;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  SortSmemT<K>& sm = *reinterpret_cast<SortSmemT<K>*>(smem_raw);
+  const int tid = threadIdx.x;
+  const int64_t n = sort_count(n0, n_dev);
+  const int64_t tiles = (n + TILE - 1) / TILE;
+  if (tid == 0) sm.tile = atomicAdd(tile_ctr, 1u);
+  for (int i = tid; i < kSortWarps * kRadix; i += kSortThreads) (&sm.whist[0][0])[i] = 0;
+  const uint32_t hs = sort_scan256(tid < kRadix ? __ldg(hist + tid) : 0u, sm.wsum);
+  if (tid < kRadix) sm.hscan[tid] = hs;
+  __syncthreads();
+  const uint32_t t = sm.tile;
+  if ((int64_t)t >= tiles) return;   // past the data: nobody waits on this ticket
+  const int64_t left = n - (int64_t)t * TILE;
+  onesweep_tile<K>(sm, kin, vin, kout, vout, (uint32_t)n, t, left >= TILE ? TILE : (int)left, shift, lookback,
+                   status);
 }
 
 // Words of scratch the sort needs: hist [passes][256], tickets [passes],
@@ -210,6 +278,8 @@ inline emb_status radix_sort_pairs(K* const keys[2], uint32_t* const vals[2], in
                                    cudaStream_t stream, int* result) {
   *result = 0;
   if (cap <= 0 || passes <= 0) return EMB_OK;
+  if (cap > (int64_t)kCountMask) return EMB_ERR_UNSUPPORTED;   // look-back words count in 30 bits
+  if (n_dev) n = cap;
   const int64_t tiles = (cap + SortSmemT<K>::kTile - 1) / SortSmemT<K>::kTile;
   uint32_t* hist = scratch;
   uint32_t* tickets = hist + (size_t)passes * kRadix;
