@@ -34,6 +34,7 @@ namespace emb {
 
 constexpr int kWarpElems = 512;    // values of short bags one warp chunk holds
 constexpr int kU = 4;              // row loads in flight per lane (halved for two float4 per lane)
+constexpr int kUA = 4;             // raw values in flight per lane in phase A
 constexpr int kFwdWarpsPerCta = kFwdThreads / kWarp;
 
 struct FwdArgs {
@@ -535,17 +536,37 @@ __global__ void __launch_bounds__(kFwdThreads, 4) k_forward(const FwdArgs a) {
     __syncwarp();
     const int T = ws.pos[ns];
 
-    // ---- phase A: transform the chunk's values into shared memory ----
-    for (int k = lane; k < T; k += 32) {
-      int i = 0;                             // last bag whose first slot is <= k
-      for (int step = 16; step > 0; step >>= 1)
-        if (i + step < ns && ws.pos[i + step] <= k) i += step;
-      const int64_t t = (int64_t)ws.lo[i] + (k - ws.pos[i]);
-      const int32_t row = col_row(m, a.ids, a.fvals, t);
-      ws.rows[k] = row;
-      ws.bag[k] = (uint8_t)i;
-      if (a.rows_dbg || a.keys)
-        record(a, st, t, row, m, padded ? padded_gsrc(a, m, b0 + i, k - ws.pos[i]) : pooled_gsrc(a, m, b0 + i));
+    // ---- phase A: transform the chunk's values into shared memory, the raw
+    //      values of kUA slots per lane loaded before any is transformed ----
+    for (int k0 = 0; k0 < T; k0 += 32 * kUA) {
+      int64_t raw[kUA];
+      int bi[kUA];
+#pragma unroll
+      for (int u = 0; u < kUA; ++u) {
+        const int k = k0 + u * 32 + lane;
+        int i = 0;                           // last bag whose first slot is <= k
+        raw[u] = 0;
+        if (k < T) {
+          for (int step = 16; step > 0; step >>= 1)
+            if (i + step < ns && ws.pos[i + step] <= k) i += step;
+          raw[u] = col_load(m, a.ids, a.fvals, (int64_t)ws.lo[i] + (k - ws.pos[i]));
+        }
+        bi[u] = i;
+      }
+#pragma unroll
+      for (int u = 0; u < kUA; ++u) {
+        const int k = k0 + u * 32 + lane;
+        if (k < T) {
+          const int i = bi[u];
+          const int32_t row = col_transform(m, raw[u]);
+          ws.rows[k] = row;
+          ws.bag[k] = (uint8_t)i;
+          if (a.rows_dbg || a.keys) {
+            const int64_t t = (int64_t)ws.lo[i] + (k - ws.pos[i]);
+            record(a, st, t, row, m, padded ? padded_gsrc(a, m, b0 + i, k - ws.pos[i]) : pooled_gsrc(a, m, b0 + i));
+          }
+        }
+      }
     }
     if (padded && (a.rows_dbg || a.keys) && lane < ns && !is_long)
       for (int64_t t = lo + m.pad_len; t < hi; ++t) record_cut(a, st, t, m);
