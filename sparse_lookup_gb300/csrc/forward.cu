@@ -60,6 +60,9 @@ struct FwdArgs {
   float* inv_n;            // training: 1/n_valid per mean bag
   uint32_t key_sentinel;
   uint32_t* status;
+  unsigned long long* ticket;   // [0] next tile, [1] warps done; both 0 between launches
+  int64_t n_warps;              // warps launched
+  int32_t dynamic;              // schedule: 0 static, 1 persistent warps with tickets
 };
 
 struct __align__(16) WarpSmem {
@@ -474,12 +477,42 @@ __device__ void warp_long_bag(const FwdArgs& a, int st, const ColMeta& m, int32_
 // ---------------------------------------------------------------------------
 // the kernel: one warp per element tile
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int64_t tile);
+
+// Two schedules.  Static: one tile per warp, the grid covers all tiles (warps
+// of one CTA hold neighbouring tiles, whose offset searches share L1).
+// Dynamic, for long bags: persistent warps start on the tile of their own
+// index, then take tiles in ticket order from a counter until none is left,
+// so a warp that drew short bags takes the next tile at once instead of
+// idling beside a sibling that drew long ones; the last warp to finish
+// resets the counter for the next launch (CUDA-graph safe: no host state
+// changes between launches).
 __global__ void __launch_bounds__(kFwdThreads, 4) k_forward(const FwdArgs a) {
   __shared__ WarpSmem smem[kFwdWarpsPerCta];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   WarpSmem& ws = smem[warp];
-  int64_t tile = (int64_t)blockIdx.x * kFwdWarpsPerCta + warp;
-  if (tile >= a.tiles[0] + a.tiles[1]) return;   // no CTA-wide barrier below
+  const int64_t n_tiles = a.tiles[0] + a.tiles[1];
+  // the first tile of every warp is its warp index; tickets count from there
+  int64_t tile = (int64_t)blockIdx.x * kFwdWarpsPerCta + (threadIdx.x >> 5);
+  while (tile < n_tiles) {
+    forward_tile(a, ws, tile);
+    if (!a.dynamic) break;   // static: one tile per warp
+    unsigned long long tk = 0;
+    if (lane == 0) tk = atomicAdd(&a.ticket[0], 1ull);
+    tile = a.n_warps + (int64_t)__shfl_sync(kFull, tk, 0);
+  }
+  if (a.dynamic && lane == 0) {
+    __threadfence();   // this warp's last ticket is taken before it counts itself done
+    if (atomicAdd(&a.ticket[1], 1ull) == (unsigned long long)(a.n_warps - 1)) {
+      __threadfence();
+      atomicExch(&a.ticket[0], 0ull);
+      atomicExch(&a.ticket[1], 0ull);
+    }
+  }
+}
+
+__device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int64_t tile) {
+  const int lane = threadIdx.x & 31;
   int st = 0;
   if (tile >= a.tiles[0]) {
     st = 1;
@@ -636,18 +669,27 @@ emb_status launch_forward(emb_plan_s* p, int32_t batch, const int64_t* ids, cons
   }
   a.key_sentinel = p->key_total;
   a.status = p->status_d;
-  // tiles: about 8 per resident warp, between 256 and kMaxTileElems values
+  // Schedule and tile size by the mean bag length (measured on the pooled,
+  // training and sequence workloads): bags of a few values -> static, about
+  // 16 tiles per resident warp, at least 256 values; long bags (a warp pools
+  // one whole) -> dynamic, about 32 tiles per resident warp, at least 128.
   const int64_t total = n_ids + n_fvals;
   const int64_t warps = (int64_t)p->sm_count * p->fwd_ctas_per_sm * kFwdWarpsPerCta;
-  const int64_t want = total / std::max<int64_t>(1, 8 * warps);
-  int64_t E = 256;
+  const int64_t segs = (int64_t)batch * (p->n_stream_cols[0] + p->n_stream_cols[1]);
+  a.dynamic = total > (int64_t)(kLongBag / 2) * std::max<int64_t>(segs, 1) ? 1 : 0;
+  const int64_t want = total / std::max<int64_t>(1, (a.dynamic ? 32 : 16) * warps);
+  int64_t E = a.dynamic ? 128 : 256;
   while (E < want && E < kMaxTileElems) E <<= 1;
   a.tile_elems = (int32_t)E;
   a.tiles[0] = a.ncols[0] > 0 ? n_ids / E + 1 : 0;
   a.tiles[1] = a.ncols[1] > 0 ? n_fvals / E + 1 : 0;
   const int64_t tiles = a.tiles[0] + a.tiles[1];
   if (tiles == 0) return EMB_OK;
-  const int64_t grid = (tiles + kFwdWarpsPerCta - 1) / kFwdWarpsPerCta;
+  const int64_t resident = (int64_t)p->sm_count * p->fwd_ctas_per_sm;
+  int64_t grid = (tiles + kFwdWarpsPerCta - 1) / kFwdWarpsPerCta;
+  if (a.dynamic) grid = std::min<int64_t>(grid, resident);
+  a.ticket = p->fwd_ticket;
+  a.n_warps = grid * kFwdWarpsPerCta;
   k_forward<<<(unsigned)grid, kFwdThreads, 0, stream>>>(a);
   return cuda_status(cudaGetLastError());
 }

@@ -19,6 +19,7 @@ void free_plan(emb_plan_s* p) {
   cudaFree(p->tables_d);
   cudaFree(p->table_base_d);
   cudaFree(p->status_d);
+  cudaFree(p->fwd_ticket);
   Workspace& w = p->ws;
   cudaFree(w.keys[0]);
   cudaFree(w.keys[1]);
@@ -184,6 +185,8 @@ extern "C" emb_status emb_plan_create(const emb_column_desc* cols, int32_t n_col
   if (e == cudaSuccess) e = dmalloc(&p->tables_d, p->tables_h.size(), &total);
   if (e == cudaSuccess) e = dmalloc(&p->table_base_d, p->table_base_h.size(), &total);
   if (e == cudaSuccess) e = dmalloc(&p->status_d, 1, &total);
+  if (e == cudaSuccess) e = dmalloc(&p->fwd_ticket, 2, &total);
+  if (e == cudaSuccess) e = cudaMemset(p->fwd_ticket, 0, 2 * sizeof(unsigned long long));
   if (e == cudaSuccess) e = cudaMemcpy(p->meta_d, p->meta_h.data(), sizeof(ColMeta) * n_cols, cudaMemcpyHostToDevice);
   if (e == cudaSuccess && !sc.empty())
     e = cudaMemcpy(p->stream_cols_d, sc.data(), sizeof(int32_t) * sc.size(), cudaMemcpyHostToDevice);

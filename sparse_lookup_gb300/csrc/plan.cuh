@@ -79,6 +79,7 @@ struct emb_plan_s {
   uint32_t key_total = 0;              // sum of table rows == sentinel key
   int key_bits = 0;
   uint32_t* status_d = nullptr;
+  unsigned long long* fwd_ticket = nullptr;   // forward tile tickets (next tile, warps done)
   int sm_count = 0;
   int fwd_ctas_per_sm = 0;
   emb::Workspace ws;
