@@ -116,7 +116,8 @@ typedef struct emb_plan_s* emb_plan;
  *  n_cols    1 .. 65535
  *  max_batch 1 .. 2^31-1; n_cols * max_batch < 2^31
  *  max_ids   training plans: the largest n_ids + n_fvals a forward will see
- *            (< 2^31); ignored otherwise
+ *            (< 2^30: the backward's radix sort counts in 30 bits); ignored
+ *            otherwise
  *  flags     EMB_PLAN_TRAINING or 0
  *  out       (host) receives the plan
  * Limits: the distinct tables' row counts must sum below 2^32 - 1 (the
@@ -169,7 +170,9 @@ emb_status emb_plan_info(emb_plan plan, int64_t* out_width, int64_t* seq_floats_
  * A training plan also records, in its workspace, each contribution's row and
  * bag for emb_backward_update; batch <= max_batch and n_ids + n_fvals <=
  * max_ids are then required.  The input buffers must stay unchanged until the
- * backward of this forward has been queued. */
+ * backward of this forward has been queued.
+ * Calls on one plan must be ordered (one stream, or streams joined by events):
+ * the forward's tile counter and the training workspace belong to the plan. */
 emb_status emb_forward(emb_plan plan, int32_t batch,
                        const int64_t* ids, const int32_t* id_offsets, int64_t n_ids,
                        const float* fvals, const int32_t* f_offsets, int64_t n_fvals,
