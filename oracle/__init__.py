@@ -62,6 +62,11 @@ def lib():
                                            c_void_p, c_void_p, c_int64, c_void_p, c_void_p,
                                            c_void_p, c_float, c_float, c_int64, POINTER(c_int64),
                                            c_void_p, c_void_p, c_void_p, c_void_p, c_int64]
+        L.orc_backward_rows.restype = c_int32
+        L.orc_backward_rows.argtypes = [POINTER(_Col), c_int32, c_int32, c_void_p, c_void_p, c_void_p,
+                                        c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_void_p,
+                                        c_void_p, c_void_p, c_int32, c_float, c_float, c_void_p,
+                                        c_void_p, c_void_p]
         L.orc_hash_init_value.restype = c_float
         L.orc_hash_init_value.argtypes = [c_uint64, c_int32, c_int64, c_int32, c_float]
         L.orc_hash_create.restype = c_void_p
@@ -210,6 +215,58 @@ def backward_adagrad(cols, B, offsets, values, G, Gseq, W, acc, lr, eps):
         grads.append(u_grad[pos:pos + d].copy())
         pos += d
     return dict(table=u_table[:n].copy(), row=u_row[:n].copy(), count=u_count[:n].copy(), grad=grads)
+
+
+def backward_rows(cols, B, offsets, values, G, Gseq, targets, W_rows, acc_rows, lr, eps):
+    """The backward + Adagrad of backward_adagrad restricted to chosen rows,
+    for tables too large to copy to the host.  targets: (table, row) pairs;
+    W_rows / acc_rows: float32 [n_targets, dim] host copies of those rows
+    before the step, updated in place.  Each target's gradient is summed in
+    the same order as backward_adagrad sums it.  Returns dict(table, row,
+    count, grad [n, dim] fp32, absgrad [n, dim] fp64: sum of |scale * G|),
+    ascending by (table, row) (W_rows / acc_rows must follow that order)."""
+    arr, keep, width = _cols(cols)
+    C = len(cols)
+    offs = [np.ascontiguousarray(o, np.int32) for o in offsets]
+    ids, fv = _values(cols, values)
+    G = np.ascontiguousarray(G, np.float32) if G is not None else np.zeros((B, 1), np.float32)
+    gs = [None if g is None else np.ascontiguousarray(g, np.float32) for g in (Gseq or [None] * C)]
+    t_table = np.ascontiguousarray([t for t, _ in targets], np.int32)
+    t_row = np.ascontiguousarray([r for _, r in targets], np.int64)
+    order = np.lexsort((t_row, t_table))
+    assert np.array_equal(order, np.arange(len(targets))), "targets must ascend by (table, row)"
+    assert W_rows.dtype == np.float32 and W_rows.flags.c_contiguous and W_rows.shape == acc_rows.shape
+    assert acc_rows.dtype == np.float32 and acc_rows.flags.c_contiguous
+    n, ld = W_rows.shape
+    count = np.zeros(max(n, 1), np.int64)
+    grad = np.zeros((max(n, 1), ld), np.float32)
+    absg = np.zeros((max(n, 1), ld), np.float64)
+    st = lib().orc_backward_rows(arr, C, B, _ptr_array(offs), _ptr_array(ids), _ptr_array(fv), _ptr(G),
+                                 G.shape[1], _ptr_array(gs), n, _ptr(t_table), _ptr(t_row), _ptr(W_rows),
+                                 _ptr(acc_rows), ld, c_float(lr), c_float(eps), _ptr(count), _ptr(grad),
+                                 _ptr(absg))
+    if st != OK:
+        raise ValueError("oracle backward_rows failed: %d" % st)
+    return dict(table=t_table, row=t_row, count=count[:n], grad=grad[:n], absgrad=absg[:n])
+
+
+def unique_counts(cols, B, offsets, values):
+    """Distinct (table, row) pairs that receive a gradient, ascending, with
+    the number of contributions each (RecIS §3.2 Figure 3, local reduce-ID
+    with counts): the valid rows of every column (padded columns: the first
+    pad_len values of a bag), counted by numpy.unique."""
+    keys = []
+    for c, o, v in zip(cols, offsets, values):
+        rows = column_rows(c, v)
+        o = np.asarray(o, np.int64)
+        valid = rows >= 0
+        if c.pooling == "padded":
+            bag = np.repeat(np.arange(B), np.diff(o))
+            valid &= (np.arange(rows.size) - o[bag]) < c.pad_len
+        keys.append(np.int64(c.table) * (np.int64(1) << 40) + rows[valid])
+    allk = np.concatenate(keys) if keys else np.zeros(0, np.int64)
+    u, cnt = np.unique(allk, return_counts=True)
+    return dict(table=(u >> 40).astype(np.int64), row=u & ((np.int64(1) << 40) - 1), count=cnt.astype(np.int64))
 
 
 def hash_init_value(seed, tid, key, d, init_scale):

@@ -338,6 +338,91 @@ int orc_backward_adagrad(const orc_col* cols, int32_t C, int32_t B,
     return ORC_OK;
 }
 
+/* The same backward for a chosen set of rows only, for workloads whose
+ * tables are too large to copy to the host: targets (t_table[i], t_row[i]),
+ * strictly ascending by (table, row).  Every valid contribution is visited in
+ * the order orc_backward_adagrad lists them; one whose row is a target adds
+ * scale_r * G to that target's fp64 sum (and |scale_r * G| to t_abs), so each
+ * target's sum is formed in the same order as in orc_backward_adagrad.  Then
+ * each target row takes its Adagrad step on the compact host rows
+ * W_rows / acc_rows ([n_targets, ld], the target's dim floats used).
+ * Outputs: t_count [n_targets]; t_grad [n_targets, ld] fp32-rounded sums;
+ * t_abs [n_targets, ld] fp64 sums of magnitudes (NULL to skip). */
+static int64_t find_target(int64_t n, const int32_t* tt, const int64_t* tr, int32_t table, int64_t row)
+{
+    int64_t lo = 0, hi = n;
+    while (lo < hi) {
+        int64_t mid = lo + (hi - lo) / 2;
+        if (tt[mid] < table || (tt[mid] == table && tr[mid] < row)) lo = mid + 1; else hi = mid;
+    }
+    return (lo < n && tt[lo] == table && tr[lo] == row) ? lo : -1;
+}
+
+int orc_backward_rows(const orc_col* cols, int32_t C, int32_t B,
+                      const int32_t* const* offsets, const int64_t* const* ids,
+                      const float* const* fvals, const float* G, int64_t ldG,
+                      const float* const* Gseq, int64_t n_targets, const int32_t* t_table,
+                      const int64_t* t_row, float* W_rows, float* acc_rows, int32_t ld,
+                      float lr, float eps, int64_t* t_count, float* t_grad, double* t_abs)
+{
+    if (!cols || C < 0 || B < 0 || n_targets < 0 || ld < 1) return ORC_ERR_ARG;
+    for (int64_t i = 1; i < n_targets; ++i)
+        if (t_table[i] < t_table[i - 1] || (t_table[i] == t_table[i - 1] && t_row[i] <= t_row[i - 1]))
+            return ORC_ERR_ARG;
+    for (int32_t ci = 0; ci < C; ++ci)
+        if (check_offsets(offsets[ci], B)) return ORC_ERR_ARG;
+    size_t cells = (size_t)(n_targets > 0 ? n_targets : 1) * (size_t)ld;
+    double* S = (double*)calloc(cells, sizeof(double));
+    double* A = (double*)calloc(cells, sizeof(double));
+    int32_t* tdim = (int32_t*)calloc((size_t)(n_targets > 0 ? n_targets : 1), sizeof(int32_t));
+    if (!S || !A || !tdim) { free(S); free(A); free(tdim); return ORC_ERR_OOM; }
+    for (int64_t i = 0; i < n_targets; ++i) t_count[i] = 0;
+    for (int32_t ci = 0; ci < C; ++ci) {
+        const orc_col* c = &cols[ci];
+        if (c->dim > ld) { free(S); free(A); free(tdim); return ORC_ERR_ARG; }
+        const int32_t* off = offsets[ci];
+        int64_t nvals = off[B];
+        int64_t* rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)(nvals > 0 ? nvals : 1));
+        if (!rows) { free(S); free(A); free(tdim); return ORC_ERR_OOM; }
+        orc_column_rows(c, nvals, ids ? ids[ci] : NULL, fvals ? fvals[ci] : NULL, rows);
+        for (int32_t b = 0; b < B; ++b) {
+            int64_t lo = off[b], hi = off[b + 1];
+            if (c->pooling == ORC_PADDED && hi - lo > c->pad_len) hi = lo + c->pad_len;
+            int64_t nv = 0;
+            for (int64_t t = lo; t < hi; ++t) nv += rows[t] >= 0;
+            for (int64_t t = lo; t < hi; ++t) {
+                if (rows[t] < 0) continue;
+                int64_t k = find_target(n_targets, t_table, t_row, c->table, rows[t]);
+                if (k < 0) continue;
+                double scale = (c->pooling == ORC_MEAN) ? 1.0 / (double)nv : 1.0;
+                const float* src;
+                if (c->pooling == ORC_PADDED)
+                    src = Gseq[ci] + ((int64_t)b * c->pad_len + (t - lo)) * c->dim;
+                else
+                    src = G + (int64_t)b * ldG + c->out_col;
+                for (int32_t d = 0; d < c->dim; ++d) {
+                    S[k * ld + d] += scale * (double)src[d];
+                    A[k * ld + d] += fabs(scale * (double)src[d]);
+                }
+                tdim[k] = c->dim;
+                t_count[k] += 1;
+            }
+        }
+        free(rows);
+    }
+    for (int64_t k = 0; k < n_targets; ++k) {
+        for (int32_t d = 0; d < tdim[k]; ++d) {
+            adagrad_elem(&W_rows[k * ld + d], &acc_rows[k * ld + d], S[k * ld + d], lr, eps);
+            if (t_grad) t_grad[k * ld + d] = (float)S[k * ld + d];
+            if (t_abs) t_abs[k * ld + d] = A[k * ld + d];
+        }
+    }
+    free(S);
+    free(A);
+    free(tdim);
+    return ORC_OK;
+}
+
 /* ------------------------------------------------------------------------ */
 /* a8 + a9: collision-free hash table with frequency filter and expiry       */
 /* [Monolith §2.1 "Tabel Hash"]                                              */

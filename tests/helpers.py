@@ -177,15 +177,48 @@ class TrainStep:
         return out
 
 
+def check_row_update(key, gr, absg, count, g_gpu, w0, a0, w_gpu, a_gpu, w_ref, a_ref, lr, eps):
+    """One touched row: the aggregated gradient within the fp32 summation
+    bound of the oracle's fp64 sum; the updated weights within 1e-5 rel /
+    1e-6 abs except elements that fp32 summation leaves ill-conditioned (the
+    first Adagrad step from acc = 0 has dW/dg = lr eps / g^2, and a sign fp32
+    does not determine flips the step); the accumulator within the bound the
+    gradient error implies.  Returns (elements outside the tolerance, all of
+    them ill-conditioned; elements checked)."""
+    gr = np.asarray(gr, np.float64)
+    absg = np.asarray(absg, np.float64)
+    k = int(count) + 1
+    bnd = gamma(k) * absg + 1e-30
+    err = np.abs(np.asarray(g_gpu, np.float64) - gr)
+    ok = (err <= ATOL + RTOL * np.abs(gr)) | (err <= bnd)
+    assert ok.all(), "aggregated gradient of row %s: err %s bound %s" % (key, err[~ok][:4], bnd[~ok][:4])
+    # probabilistic bound (Higham & Mary, 2019): lambda sqrt(k) u sum|x|,
+    # used only to decide which weights fp32 leaves ill-conditioned
+    pbnd = np.minimum(bnd, 8.0 * np.sqrt(k) * U32 * absg) + 1e-30
+    a0 = np.asarray(a0, np.float64)
+    w0 = np.asarray(w0, np.float64)
+    step = lambda gg: w0 - lr * gg / (np.sqrt(a0 + gg * gg) + eps)
+    spread = np.abs(step(gr + pbnd) - step(gr - pbnd))
+    amb = spread > ATOL + RTOL * np.abs(step(gr))
+    wr = np.asarray(w_ref, np.float64)
+    errw = np.abs(np.asarray(w_gpu, np.float64) - wr)
+    within = errw <= ATOL + RTOL * np.abs(wr)
+    okw = within | amb
+    assert okw.all(), "weights of row %s: %s vs %s" % (key, np.asarray(w_gpu)[~okw][:4], wr[~okw][:4])
+    ar = np.asarray(a_ref, np.float64)
+    abound = 2 * np.abs(gr) * pbnd + pbnd * pbnd + 4 * U32 * np.abs(ar)
+    erra = np.abs(np.asarray(a_gpu, np.float64) - ar)
+    oka = (erra <= ATOL + RTOL * np.abs(ar)) | (erra <= abound) | amb
+    assert oka.all(), "accumulator of row %s: %s vs %s" % (key, np.asarray(a_gpu)[~oka][:4], ar[~oka][:4])
+    return int((amb & ~within).sum()), gr.size
+
+
 def check_train_step(ts, max_ambiguous_frac=1e-5):
-    """Bit-exact unique rows and counts; aggregated gradient within the fp32
-    summation bound; weights within 1e-5 rel / 1e-6 abs except elements that
-    fp32 summation leaves ill-conditioned (the first Adagrad step from acc = 0
-    has dW/dg = lr eps / g^2, and a sign fp32 does not determine flips the
-    step); accumulators within the bound the gradient error implies.  Returns
-    the number of elements outside the tolerance (all ill-conditioned), which
-    must stay below max(16, 1e-5 of the updated elements): one cancelling
-    pair of bags repeats its element in every row the two bags share."""
+    """Bit-exact unique rows and counts; every touched row checked by
+    check_row_update; untouched rows unchanged.  Returns the number of
+    elements outside the tolerance (all ill-conditioned), which must stay
+    below max(16, 1e-5 of the updated elements): one cancelling pair of bags
+    repeats its element in every row the two bags share."""
     assert ts.status == 0, "device status %d" % ts.status
     ref, absg, Wr, Ar = ts.oracle()
     n = len(ref["row"])
@@ -199,21 +232,7 @@ def check_train_step(ts, max_ambiguous_frac=1e-5):
     g = d["grad"].cpu().numpy()
     excluded, total = 0, 0
     dims = {c.table: c.dim for c in ts.w.columns}
-    bound_of = {}
-    for i in range(n):
-        dim = dims[int(ref["table"][i])]
-        gr = ref["grad"][i].astype(np.float64)
-        k = int(ref["count"][i]) + 1
-        bnd = gamma(k) * absg["grad"][i].astype(np.float64) + 1e-30
-        # probabilistic bound (Higham & Mary, 2019): lambda sqrt(k) u sum|x|,
-        # used only to decide which weights fp32 leaves ill-conditioned
-        pbnd = np.minimum(bnd, 8.0 * np.sqrt(k) * U32 * absg["grad"][i].astype(np.float64)) + 1e-30
-        bound_of[(int(ref["table"][i]), int(ref["row"][i]))] = (gr, pbnd)
-        err = np.abs(g[i, :dim].astype(np.float64) - gr)
-        ok = (err <= ATOL + RTOL * np.abs(gr)) | (err <= bnd)
-        assert ok.all(), "aggregated gradient of row %s: err %s bound %s" % (
-            (int(ref["table"][i]), int(ref["row"][i])), err[~ok][:4], bnd[~ok][:4])
-    # weights and accumulators
+    index = {(int(ref["table"][i]), int(ref["row"][i])): i for i in range(n)}
     for t_gpu, t_spec in t2s.items():
         Wg = ts.m.tables[t_spec].cpu().numpy()
         Ag = ts.m.accs[t_spec].cpu().numpy()
@@ -223,29 +242,14 @@ def check_train_step(ts, max_ambiguous_frac=1e-5):
         touched[ref["row"][sel]] = True
         assert np.array_equal(Wg[~touched], W0[~touched]), "untouched rows changed"
         assert np.array_equal(Ag[~touched], ts.A0[t_spec][~touched]), "untouched accumulators changed"
-        lr, eps = ts.w.lr, ts.w.eps
+        dim = dims[t_spec]
         for r in ref["row"][sel]:
-            gr, bnd = bound_of[(t_spec, int(r))]
-            # ill-conditioned: the weight range that gradients within the
-            # summation bound produce is wider than the tolerance (includes a
-            # sign that fp32 does not determine)
-            a0 = ts.A0[t_spec][r].astype(np.float64)
-            w0 = W0[r].astype(np.float64)
-            step = lambda gg: w0 - lr * gg / (np.sqrt(a0 + gg * gg) + eps)
-            spread = np.abs(step(gr + bnd) - step(gr - bnd))
-            amb = spread > ATOL + RTOL * np.abs(step(gr))
-            total += gr.size
-            wr = Wr[t_spec][r].astype(np.float64)
-            err = np.abs(Wg[r].astype(np.float64) - wr)
-            within = err <= ATOL + RTOL * np.abs(wr)
-            excluded += int((amb & ~within).sum())
-            okw = within | amb
-            assert okw.all(), "weights of row %d: %s vs %s" % (r, Wg[r][~okw][:4], wr[~okw][:4])
-            ar = Ar[t_spec][r].astype(np.float64)
-            abound = 2 * np.abs(gr) * bnd + bnd * bnd + 4 * U32 * np.abs(ar)
-            erra = np.abs(Ag[r].astype(np.float64) - ar)
-            oka = (erra <= ATOL + RTOL * np.abs(ar)) | (erra <= abound) | amb
-            assert oka.all(), "accumulator of row %d: %s vs %s" % (r, Ag[r][~oka][:4], ar[~oka][:4])
+            i = index[(t_spec, int(r))]
+            e, m = check_row_update((t_spec, int(r)), ref["grad"][i], absg["grad"][i], ref["count"][i],
+                                    g[i, :dim], W0[r], ts.A0[t_spec][r], Wg[r], Ag[r], Wr[t_spec][r],
+                                    Ar[t_spec][r], ts.w.lr, ts.w.eps)
+            excluded += e
+            total += m
     assert excluded <= max(16, max_ambiguous_frac * total), (excluded, total)
     return excluded
 
@@ -281,7 +285,10 @@ class DynamicRun:
         self.plan = sl.Plan(self.cols, [self.ht.weight], [self.ht.acc], max_batch=B, max_ids=max_keys,
                             training=True)
 
-    def step(self, t, check):
+    def step(self, t, check, check_out=None):
+        """One step; check: return the rows of both sides; check_out (default:
+        check): also the pooled outputs of both sides."""
+        check_out = check if check_out is None else check_out
         import torch
         offs, keys = synth.dynamic_keys(self.seed, t, self.C, self.B, self.alpha, self.key_bits, self.max_len)
         tids = np.concatenate([np.full(k.size, c, np.int32) for c, k in enumerate(keys)])
@@ -297,22 +304,16 @@ class DynamicRun:
         # oracle
         rows_o, st_o = self.oh.lookup_or_insert(tids, allk, t)
         res = dict(status=(st_h, st_p, st_o))
+        vals = []
+        pos = 0
+        for o in offs:
+            n = int(o[-1])
+            vals.append(rows_o[pos:pos + n])
+            pos += n
         if check:
             res["rows"] = (rows.cpu().numpy(), rows_o)
-            vals = []
-            pos = 0
-            for o in offs:
-                n = int(o[-1])
-                vals.append(rows_o[pos:pos + n])
-                pos += n
+        if check_out:
             res["out"] = (out.cpu().numpy(), oracle.forward(self.cols, self.B, offs, vals, [self.oh.W])[0])
-        else:
-            vals = []
-            pos = 0
-            for o in offs:
-                n = int(o[-1])
-                vals.append(rows_o[pos:pos + n])
-                pos += n
         oracle.backward_adagrad(self.cols, self.B, offs, vals, G.cpu().numpy(), None, [self.oh.W], [self.oh.acc],
                                 self.lr, 1e-10)
         self.oh.evict(t, self.ttl)

@@ -450,3 +450,82 @@ def test_hash_matches_dict_model_and_invariants():
         assert int(adm.sum()) + h.free_count() == h.bump()
     ex = h.export()
     assert sorted(zip(ex["tid"].tolist(), ex["key"].tolist())) == sorted(ent.keys())
+
+
+def _seq_grads(w, seed):
+    """Upstream gradients of the padded columns ([B, pad_len, dim] each)."""
+    r = np.random.default_rng(seed)
+    return [r.standard_normal((w.B, c.pad_len, c.dim)).astype(np.float32) if c.pooling == "padded" else None
+            for c in w.columns]
+
+
+def test_backward_rows_equals_the_full_backward_on_its_rows():
+    """backward_rows over every touched row (and over a subset) gives the
+    counts, fp32 aggregated gradients and updated W/acc of backward_adagrad
+    bit for bit: the same contributions summed in the same order."""
+    for seed in range(8):
+        w = synth.random_small(seed)
+        tabs = _tables(w)
+        width = sum(c.dim for c in w.columns if c.pooling != "padded")
+        G = synth.make_grad((w.B, max(width, 1)), 9 + seed).numpy()[:, :width]
+        Gs = _seq_grads(w, seed)
+        W = [None if t is None else t.copy() for t in tabs]
+        A = [None if t is None else np.full_like(t, 0.25) for t in tabs]
+        Wl = [x if x is not None else np.zeros((1, 1), np.float32) for x in W]
+        Al = [x if x is not None else np.zeros((1, 1), np.float32) for x in A]
+        W0 = [x.copy() for x in Wl]
+        A0 = [x.copy() for x in Al]
+        ref = oracle.backward_adagrad(w.columns, w.B, w.offsets, w.values, G, Gs, Wl, Al, w.lr, w.eps)
+        n = len(ref["row"])
+        if n == 0:
+            continue
+        dims = {c.table: c.dim for c in w.columns}
+        ld = max(dims.values())
+        for pick in (np.arange(n), np.arange(n)[::3]):
+            targets = [(int(ref["table"][i]), int(ref["row"][i])) for i in pick]
+            Wr = np.zeros((len(targets), ld), np.float32)
+            Ar = np.zeros((len(targets), ld), np.float32)
+            for k, (t, r) in enumerate(targets):
+                Wr[k, :dims[t]] = W0[t][r]
+                Ar[k, :dims[t]] = A0[t][r]
+            got = oracle.backward_rows(w.columns, w.B, w.offsets, w.values, G, Gs, targets, Wr, Ar, w.lr, w.eps)
+            assert np.array_equal(got["count"], ref["count"][pick]), seed
+            for k, (i, (t, r)) in enumerate(zip(pick, targets)):
+                d = dims[t]
+                assert np.array_equal(got["grad"][k, :d], ref["grad"][i]), (seed, t, r)
+                assert np.array_equal(Wr[k, :d], Wl[t][r]), (seed, t, r)
+                assert np.array_equal(Ar[k, :d], Al[t][r]), (seed, t, r)
+                assert np.all(got["absgrad"][k, :d] >= np.abs(got["grad"][k, :d]) * (1 - 1e-6)), (seed, t, r)
+
+
+def test_backward_rows_magnitudes_are_the_sum_of_abs_terms():
+    """absgrad of a row = the aggregated gradient of |G| (checked on a hand
+    example: MEAN bag [1, 1, 3], G = [3, -6] -> row 1 gets 2/3 |G|)."""
+    off = np.array([0, 3], np.int32)
+    ids = np.array([1, 1, 3], np.int64)
+    G = np.array([[3.0, -6.0]], np.float32)
+    Wr = np.zeros((2, 2), np.float32)
+    Ar = np.zeros((2, 2), np.float32)
+    got = oracle.backward_rows([ColumnSpec("identity", "mean", 4, 2, 0)], 1, [off], [ids], G, None,
+                               [(0, 1), (0, 3)], Wr, Ar, 0.1, 1e-10)
+    assert got["count"].tolist() == [2, 1]
+    np.testing.assert_allclose(got["grad"], [[2.0, -4.0], [1.0, -2.0]], rtol=1e-7)
+    np.testing.assert_allclose(got["absgrad"], [[2.0, 4.0], [1.0, 2.0]], rtol=1e-12)
+
+
+def test_unique_counts_equals_the_backward_listing():
+    """numpy.unique over the valid rows (library routine) lists the same
+    (table, row, count) as the C oracle's sorted run listing."""
+    for seed in range(10):
+        w = synth.random_small(100 + seed)
+        tabs = _tables(w)
+        width = sum(c.dim for c in w.columns if c.pooling != "padded")
+        G = np.zeros((w.B, max(width, 1)), np.float32)
+        Gs = _seq_grads(w, seed)
+        Wl = [x.copy() if x is not None else np.zeros((1, 1), np.float32) for x in tabs]
+        Al = [np.zeros_like(x) for x in Wl]
+        ref = oracle.backward_adagrad(w.columns, w.B, w.offsets, w.values, G, Gs, Wl, Al, w.lr, w.eps)
+        got = oracle.unique_counts(w.columns, w.B, w.offsets, w.values)
+        assert np.array_equal(got["table"], ref["table"].astype(np.int64)), seed
+        assert np.array_equal(got["row"], ref["row"]), seed
+        assert np.array_equal(got["count"], ref["count"]), seed
