@@ -297,7 +297,7 @@ emb_status hash_destroy(emb_hash h);
  * and acc ([num_rows, dim] fp32, 16-byte aligned) takes one step
  *   acc += g*g;  w -= lr * g / (sqrt(acc) + eps).
  *
- * Scratch: a fixed area of about 4.7 MB compiled into the library as a
+ * Scratch: a fixed area of about 6.4 MB compiled into the library as a
  * file-scope device array; every GPU that loads the library holds it until
  * the process exits.  Limits: n <= 262144 (2^18), dim <= 256, num_rows <
  * 2^31; larger sizes return EMB_ERR_UNSUPPORTED before any work is queued.

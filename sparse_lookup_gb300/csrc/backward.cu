@@ -28,7 +28,7 @@
 
 namespace emb {
 
-constexpr int kSegThreads = 256;
+constexpr int kSegThreads = 128;
 constexpr int kSegWarps = kSegThreads / 32;
 
 // ---------------------------------------------------------------------------
@@ -157,6 +157,7 @@ struct SegArgs {
   uint8_t* part_thru;   // [n_blocks]: the CTA lies inside one run that continues past it
   int32_t maxdim4;
   int32_t glog;
+  int32_t span;           // sorted entries per CTA (a multiple of the lane groups per CTA)
   // debug outputs
   const uint32_t* rank;
   int32_t* dbg_table;
@@ -247,15 +248,24 @@ __device__ __forceinline__ const float* grad_src(const SegArgs& a, uint32_t val,
   return a.grad_out + (int64_t)b * a.ldg + cg.x;
 }
 
-// Rows of the table a key belongs to, tracked while keys ascend.
+// The table a key belongs to and its metadata, tracked while keys ascend
+// (reloaded only when the key leaves the current table's range).
 struct TableCursor {
   int t = -1;
   uint32_t base = 0, next = 0;
+  float* weight = nullptr;
+  float* acc = nullptr;
+  int dim = 0, dim4 = 0;
   __device__ __forceinline__ void seek(const SegArgs& a, uint32_t key) {
     if (t < 0 || key < base || key >= next) {
       t = table_of_key(a.table_base, a.n_tables, key);
       base = __ldg(a.table_base + t);
       next = __ldg(a.table_base + t + 1);
+      const TableMeta& tm = a.tables[t];
+      weight = tm.weight;
+      acc = tm.acc;
+      dim = tm.dim;
+      dim4 = tm.dim4;
     }
   }
 };
@@ -282,11 +292,10 @@ struct PendingRow {
                                         const float4 (&grad)[V], int sub) {
     on = true;
     end = e;
-    const TableMeta& tm = a.tables[tc.t];
     const int64_t row = k - tc.base;
-    dim4 = tm.dim4;
-    W = tm.weight + row * tm.dim;
-    A = tm.acc + row * tm.dim;
+    dim4 = tc.dim4;
+    W = tc.weight + row * tc.dim;
+    A = tc.acc + row * tc.dim;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
       g[v] = grad[v];
@@ -324,17 +333,28 @@ struct PendingRow {
   }
 };
 
-constexpr int kSegSpan = 2048;                    // sorted entries per CTA
-constexpr int kSegPerThread = kSegSpan / kSegThreads;
+// Sorted entries per CTA: about 64 per lane group (measured best on the
+// training and sequence workloads), between 256 and kSegSpanMax.
+constexpr int kSegSpanMax = 1024;
+constexpr int kSegPerThread = kSegSpanMax / kSegThreads;
+constexpr int kSegPerGroup = 64;
+
+inline int seg_span(int glog) {
+  const int ng = kSegThreads / 32 * (32 >> glog);
+  const int s = kSegPerGroup * ng;
+  return s < 256 ? 256 : (s > kSegSpanMax ? kSegSpanMax : s);
+}
 // Gradient rows in flight per lane group (4 rows of V float4 per lane) and
-// resident CTAs per SM: measured on the training and sequence workloads,
-// three CTAs of 4-deep groups beat two CTAs of 4-, 6- or 8-deep groups (more
-// warps hide the gather latency better than deeper groups); rows wider than
-// 128 floats keep two CTAs to stay within the registers.
+// resident CTAs per SM.  Measured on the training and sequence workloads:
+// 4-deep groups in more warps beat 6- or 8-deep groups in fewer (more warps
+// hide the gather latency better), and six 4-warp CTAs over 1024
+// contributions beat three 8-warp CTAs over 2048 (a CTA's warps wait at its
+// barrier for its slowest lane group; smaller CTAs wait less).  Rows wider
+// than 128 floats take fewer CTAs to stay within the registers.
 template <int V>
 struct SegDepth {
   static constexpr int value = 4;
-  static constexpr int ctas = V == 1 ? 3 : 2;
+  static constexpr int ctas = V == 1 ? 6 : 4;
 };
 constexpr int kSegMaxGroups = kSegWarps * 32;     // dim 4: 32 one-lane groups per warp
 constexpr uint32_t kOffPad = 0x80000000u;         // offset refers to grad_seq
@@ -351,7 +371,7 @@ struct __align__(16) SegRec {
 };
 
 struct SegSmem {
-  SegRec rec[kSegSpan];
+  SegRec rec[kSegSpanMax];
   float4 part[2][kSegWarps * 64];       // head / tail partial of each lane group
   int32_t head_end[kSegMaxGroups];      // end of the run cut at the group's start, -1 if none
   uint32_t tail_key[kSegMaxGroups];     // key of the run left open at the group's end
@@ -378,8 +398,8 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
   const int q = lane >> glog, sub = lane & ((1 << glog) - 1);
   const int NG = kSegWarps * G;
   const int grp = warp * G + q;
-  const int64_t B0 = (int64_t)blockIdx.x * kSegSpan;
-  const int64_t B1 = min(B0 + (int64_t)kSegSpan, a.n);
+  const int64_t B0 = (int64_t)blockIdx.x * a.span;
+  const int64_t B1 = min(B0 + (int64_t)a.span, a.n);
   const int span = (int)(B1 - B0);
   const int D4 = a.maxdim4;
 
@@ -391,6 +411,7 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
   TableCursor ptc;
 #pragma unroll
   for (int k = 0; k < kSegPerThread; ++k) {
+    if (k * kSegThreads >= span) break;
     const int e = k * kSegThreads + tid;
     SegRec r;
     r.key = a.sentinel;
@@ -402,10 +423,9 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
       r.key = key;
       if (key != a.sentinel && (B0 + e == 0 || __ldg(a.keys + B0 + e - 1) != key)) {
         ptc.seek(a, key);
-        const TableMeta& tm = a.tables[ptc.t];
         const int64_t row = key - ptc.base;
-        prefetch_l2(tm.weight + row * tm.dim, (uint32_t)tm.dim * 4u);
-        prefetch_l2(tm.acc + row * tm.dim, (uint32_t)tm.dim * 4u);
+        prefetch_l2(ptc.weight + row * ptc.dim, (uint32_t)ptc.dim * 4u);
+        prefetch_l2(ptc.acc + row * ptc.dim, (uint32_t)ptc.dim * 4u);
       }
       if (key != a.sentinel) {
         const uint32_t val = __ldg(a.vals + B0 + e);
@@ -437,7 +457,7 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
   __syncthreads();
 
   // ---- per lane group: its contiguous range, in order ----
-  const int R = kSegSpan / NG;
+  const int R = a.span / NG;
   const int r0 = min(grp * R, span), r1 = min(r0 + R, span);
   uint32_t ckey = kNoKey;   // key of the open run
   bool chead = false;       // the open run began before this range
@@ -691,7 +711,8 @@ emb_status launch_backward(emb_plan_s* p, const float* grad_out, const float* gr
   while ((1 << glog) < g) ++glog;
   a.glog = glog;
   const int NG = kSegWarps * (32 >> glog);
-  const int64_t span = kSegSpan;
+  a.span = seg_span(glog);
+  const int64_t span = a.span;
   const int64_t n_blocks = (n + span - 1) / span;
   if (n_blocks > w.n_units_max) return EMB_ERR_UNSUPPORTED;
   a.partial = w.partial;
@@ -739,7 +760,7 @@ namespace {
 constexpr int64_t kNoAllocMaxN = int64_t(1) << 18;   // contributions per call
 constexpr int kNoAllocMaxDim = 256;
 constexpr int64_t kNoAllocTiles = (kNoAllocMaxN + kSortTile - 1) / kSortTile;
-constexpr int64_t kNoAllocBlocks = (kNoAllocMaxN + kSegWarps * kUnit - 1) / (kSegWarps * kUnit);
+constexpr int64_t kNoAllocBlocks = (kNoAllocMaxN + 255) / 256;   // the smallest span seg_span() returns
 constexpr size_t kNoAllocSortWords = 4 * kRadix + 4 + 4 * kNoAllocTiles * kRadix;  // sort_scratch_words(4, max n)
 
 struct NoAllocScratch {
@@ -866,7 +887,8 @@ extern "C" emb_status emb_sparse_adagrad_noalloc(const int64_t* rows, int64_t n,
   while ((1 << glog) < g) ++glog;
   a.glog = glog;
   const int NG = kSegWarps * (32 >> glog);
-  const int64_t span = kSegSpan;
+  a.span = seg_span(glog);
+  const int64_t span = a.span;
   const int64_t n_blocks = (n + span - 1) / span;
   a.partial = s->partial;
   a.part_pos = s->part_pos;
