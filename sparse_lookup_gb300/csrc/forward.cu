@@ -35,6 +35,7 @@ namespace emb {
 constexpr int kWarpElems = 512;    // values of short bags one warp chunk holds
 constexpr int kU = 4;              // row loads in flight per lane (halved for two float4 per lane)
 constexpr int kUA = 4;             // raw values in flight per lane in phase A
+constexpr int kUPool = 4;          // row loads in flight per lane when pooling short bags (8 spills)
 constexpr int kFwdWarpsPerCta = kFwdThreads / kWarp;
 
 struct FwdArgs {
@@ -210,7 +211,8 @@ __device__ __forceinline__ uint32_t padded_gsrc(const FwdArgs& a, const ColMeta&
 template <int V>
 __device__ void warp_pool_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m, int ns, int T, int b0,
                                 int glog, unsigned longmask) {
-  constexpr int U = kU / V;
+  constexpr int U = kUPool / V;
+  const int dim = m.dim, dim4 = m.dim4;
   const int lane = threadIdx.x & 31;
   const int G = 32 >> glog;
   const int q = lane >> glog, sub = lane & ((1 << glog) - 1);
@@ -256,27 +258,26 @@ __device__ void warp_pool_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m
 
   for (int j = 0; j < R; j += U) {
     float4 vals[U][V];
-    int bg[U];
-    bool ok[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int k = k0 + j + u;
-      const bool in = k < k1;
-      const int r = in ? ws.rows[k] : -1;
-      bg[u] = in ? (int)ws.bag[k] : -1;
-      ok[u] = in && r >= 0;
+      const int r = k < k1 ? ws.rows[k] : -1;
 #pragma unroll
       for (int v = 0; v < V; ++v) {
         const int f4 = sub + v * 32;
-        vals[u][v] = (ok[u] && f4 < m.dim4) ? ldg4(E + (int64_t)r * m.dim + f4 * 4) : f4zero();
+        vals[u][v] = (r >= 0 && f4 < dim4) ? ldg4(E + (int64_t)r * dim + f4 * 4) : f4zero();
       }
     }
+    // bag and validity are read again from shared memory rather than held
+    // in registers across the loads, which leaves room for more loads in flight
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      if (bg[u] < 0) continue;
-      if (bg[u] != curb) {
+      const int k = k0 + j + u;
+      if (k >= k1) break;
+      const int bg = (int)ws.bag[k];
+      if (bg != curb) {
         flush(false);
-        curb = bg[u];
+        curb = bg;
         head = false;
 #pragma unroll
         for (int v = 0; v < V; ++v) acc[v] = f4zero();
@@ -284,7 +285,7 @@ __device__ void warp_pool_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m
       }
 #pragma unroll
       for (int v = 0; v < V; ++v) f4add(acc[v], vals[u][v]);
-      nv += ok[u];
+      nv += ws.rows[k] >= 0;
     }
   }
   if (k0 < k1) flush(k1 < T && (int)ws.bag[k1] == curb);
