@@ -116,6 +116,36 @@ __device__ int warp_lower_bound(const int32_t* offs, int S, int64_t e, int64_t n
   return lo + __popc(__ballot_sync(kFull, less));
 }
 
+// Both ends of a tile at once: the first s with clamp(offs[s]) >= e_lo and
+// the first with clamp(offs[s]) >= e_hi, each searched by half the warp with
+// 16-ary rounds (lanes 0-15: e_lo, lanes 16-31: e_hi), so the two searches
+// share their round trips.
+__device__ int2 warp_lower_bound2(const int32_t* offs, int S, int64_t e_lo, int64_t e_hi, int64_t n) {
+  const int lane = threadIdx.x & 31;
+  const int h = lane >> 4, sl = lane & 15;
+  const unsigned half = h ? 0xffff0000u : 0x0000ffffu;
+  const int64_t e = h ? e_hi : e_lo;
+  bool bad = false;
+  int lo = 0, hi = S;
+  for (;;) {
+    const bool more = hi - lo > 16;
+    if (!__any_sync(kFull, more)) break;
+    const int step = (hi - lo + 15) >> 4;
+    const int p = lo + (sl + 1) * step - 1;
+    const bool less = more && (p < hi) && (clamp_off(__ldg(offs + p), n, bad) < e);
+    const int k = __popc(__ballot_sync(kFull, less) & half);
+    if (more) {
+      const int nlo = min(lo + k * step, hi);
+      hi = min(hi, nlo + step - 1);
+      lo = nlo;
+    }
+  }
+  const int p = lo + sl;
+  const bool less = (p < hi) && (clamp_off(__ldg(offs + p), n, bad) < e);
+  const int r = lo + __popc(__ballot_sync(kFull, less) & half);
+  return make_int2(__shfl_sync(kFull, r, 0), __shfl_sync(kFull, r, 16));
+}
+
 // Raw value of element t (int64 id, or the fp32 bits of a bucketize value).
 __device__ __forceinline__ int64_t col_load(const ColMeta& m, const int64_t* ids, const float* fvals, int64_t t) {
   if (m.transform == EMB_T_BUCKETIZE) return (int64_t)__float_as_int(__ldcs(fvals + t));
@@ -524,8 +554,9 @@ __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int
   const int64_t n = a.n[st];
   const int64_t e0 = tile * a.tile_elems;
   const bool last = tile == a.tiles[st] - 1;
-  int cur = warp_lower_bound(offs, S, e0, n);
-  const int s_hi = last ? S : warp_lower_bound(offs, S, e0 + a.tile_elems, n);
+  const int2 ends = warp_lower_bound2(offs, S, e0, last ? INT64_MAX : e0 + a.tile_elems, n);
+  int cur = ends.x;
+  const int s_hi = ends.y;
 
   while (cur < s_hi) {
     // ---- setup: one lane per bag, all inside column cl0 ----
@@ -587,12 +618,44 @@ __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int
         }
         bi[u] = i;
       }
+      int32_t rowv[kUA];
+      if (m.transform == EMB_T_BUCKETIZE) {
+        // the kUA binary searches advance together, so their boundary loads
+        // are in flight at the same time: row = #{j : bnd[j] <= x}
+        int blo[kUA], blen[kUA];
+        float x[kUA];
+#pragma unroll
+        for (int u = 0; u < kUA; ++u) {
+          blo[u] = 0;
+          blen[u] = m.nb;
+          x[u] = __int_as_float((int32_t)raw[u]);
+        }
+        bool more = m.nb > 0;
+        while (more) {
+          more = false;
+#pragma unroll
+          for (int u = 0; u < kUA; ++u) {
+            if (blen[u] > 0) {
+              const int half = blen[u] >> 1;
+              const bool go = __ldg(m.bnd + blo[u] + half) <= x[u];
+              blo[u] = go ? blo[u] + half + 1 : blo[u];
+              blen[u] = go ? blen[u] - half - 1 : half;
+              more |= blen[u] > 0;
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kUA; ++u) rowv[u] = blo[u];
+      } else {
+#pragma unroll
+        for (int u = 0; u < kUA; ++u) rowv[u] = col_transform(m, raw[u]);
+      }
 #pragma unroll
       for (int u = 0; u < kUA; ++u) {
         const int k = k0 + u * 32 + lane;
         if (k < T) {
           const int i = bi[u];
-          const int32_t row = col_transform(m, raw[u]);
+          const int32_t row = rowv[u];
           ws.rows[k] = row;
           ws.bag[k] = (uint8_t)i;
           if (a.rows_dbg || a.keys) {
