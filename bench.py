@@ -320,6 +320,21 @@ def cpu_dynamic_sample(w, budget_s=12.0):
 # reference arm: the oracle alone
 # ---------------------------------------------------------------------------
 
+class HostTables:
+    """Host copies of a workload's tables, drawn on first use (the same seeded
+    values the device tables hold), so that a sample touching a few columns
+    does not draw all of them."""
+
+    def __init__(self, w):
+        self.w = w
+        self.cache = {}
+
+    def __getitem__(self, t):
+        if t not in self.cache:
+            self.cache[t] = synth.make_table(self.w.tables[t], "cpu")
+        return self.cache[t]
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -327,27 +342,49 @@ def run_reference(args):
     w = make_workload(args.workload, args.columns)
     per = max(2.0, 20.0 / max(1, args.steps + args.warmup))
     vals = []
+    tables = HostTables(w)
+    G = None
+    if args.workload in TRAIN_WORKLOADS:
+        width = sum(c.dim for c in w.columns if c.pooling != "padded")
+        G = synth.make_grad((w.B, max(width, 1)), 77, "cpu")[:, :width] if width else None
     for i in range(args.warmup + args.steps):
         if args.workload.startswith("dynamic"):
             rate, sample = cpu_dynamic_sample(w, budget_s=per)
         else:
-            tables = [None if t is None else synth.make_table(t, "cpu") for t in w.tables]
             if args.workload in TRAIN_WORKLOADS:
-                width = sum(c.dim for c in w.columns if c.pooling != "padded")
-                G = synth.make_grad((w.B, max(width, 1)), 77, "cpu")[:, :width] if width else None
                 rate, sample = cpu_train_sample(w, tables, G, budget_s=per)
             else:
                 rate, sample = cpu_forward_sample(w, tables, budget_s=per)
         if i >= args.warmup:
             vals.append(rate)
     v = statistics.mean(vals)
+    # one whole step of the workload at the sampled rate
+    if args.workload.startswith("dynamic"):
+        per_step = w.B * len(w.columns) * 2.5   # mean bag length of U{0..5}
+    else:
+        per_step = sum(int(o[-1]) for o in w.offsets)
     line = {"impl": "reference", "metric": metric_name(args.workload), "value": v, "unit": "rows/s",
-            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
-            "dtype": "f64 accumulate / f32 storage", "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.B, "columns": len(w.columns)},
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": per_step / v * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64 accumulate / f32 storage", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.B, "columns": len(w.columns),
+                       "l2": "host run (no GPU)", "parallelism": "1 host core"},
             "cpu_baseline": {"value": v, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+# DRAM bytes per algorithmic byte of k_forward from the committed ncu capture
+# (profiles/k_forward_inference.md: 97.4 MB of DRAM traffic for 136.84 MB of
+# algorithmic bytes on the 200-column case).  A full launch is too large to
+# capture; its traffic is the same ratio times its algorithmic bytes.  Set to
+# None whenever k_forward changes until it is captured again.
+FORWARD_TRAFFIC_RATIO = {"inference": 97.4 / 136.84}
+
+
+def traffic_estimate(workload, fbytes):
+    r = FORWARD_TRAFFIC_RATIO.get(workload)
+    return None if r is None else r * fbytes
 
 
 def metric_name(workload):
@@ -394,14 +431,14 @@ def run_ours(args):
     line = {
         "metric": metric_name(args.workload),
         "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak" if world > 1 else "none",
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": dict(res["config"], workload=w.name, batch=w.B, columns=len(w.columns),
                        l2="flushed between steps (2x L2 write, outside events)",
                        parallelism="replicas" if world > 1 else "1 GPU"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "kernel": "k_forward",
-                     "bytes_per_launch": res["fbytes"], "launch_ms": fw_ms,
+                     "frac": achieved / peak, "traffic": traffic_estimate(w.name, res["fbytes"]),
+                     "kernel": "k_forward", "bytes_per_launch": res["fbytes"], "launch_ms": fw_ms,
                      "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy burst)"},
         "step_ms": {k: statistics.mean(v) for k, v in res["times"].items()},
         "e2e": res["e2e"],
@@ -514,10 +551,15 @@ def bench_plan(torch, sl, w, args, dev, stream, flush, train):
     # end to end through the C ABI with pinned host buffers
     host = [(torch.from_numpy(x).pin_memory(), d) for x, d in ((ids_h, ids), (id_off_h, id_off), (fv_h, fv),
                                                               (f_off_h, f_off)) if d is not None]
+    # upstream gradients come from the caller too; the step's result read back
+    # is the forward output (pooled and, for padded columns, unpooled)
     g_host = G.cpu().pin_memory() if G is not None else None
+    gs_host = Gseq.cpu().pin_memory() if Gseq is not None else None
     out_p = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x, _ in host) + (g_host.numel() * 4 if g_host is not None else 0)
-    d2h = out_p.numel() * out_p.element_size()
+    seq_p = torch.empty(seq.shape, dtype=seq.dtype).pin_memory() if seq is not None else None
+    h2d = sum(x.numel() * x.element_size() for x, _ in host) + sum(
+        x.numel() * 4 for x in (g_host, gs_host) if x is not None)
+    d2h = sum(x.numel() * x.element_size() for x in (out_p, seq_p) if x is not None)
 
     def e2e_body(i, marks):
         a, b = event_pair(torch)
@@ -526,8 +568,12 @@ def bench_plan(torch, sl, w, args, dev, stream, flush, train):
             dst.copy_(src, non_blocking=True)
         if g_host is not None:
             G.copy_(g_host, non_blocking=True)
+        if gs_host is not None:
+            Gseq.copy_(gs_host, non_blocking=True)
         plan.forward(w.B, ids, id_off, fv, f_off, out=out, seq_out=seq)
         out_p.copy_(out, non_blocking=True)
+        if seq_p is not None:
+            seq_p.copy_(seq, non_blocking=True)
         if train:
             plan.backward_update(G, Gseq, w.lr, w.eps)
         b.record(stream)
