@@ -633,6 +633,7 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
 
 // Runs cut by CTA boundaries: one lane group per boundary b (between CTA b-1
 // and CTA b) that is the first boundary inside its run.
+constexpr int kFixLook = 8;
 template <int V>
 __global__ void __launch_bounds__(kSegThreads) k_seg_fixup(const SegArgs a, int n_blocks, int64_t span) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -654,17 +655,38 @@ __global__ void __launch_bounds__(kSegThreads) k_seg_fixup(const SegArgs a, int 
     const int f4 = sub + v * 32;
     s[v] = f4 < D4 ? T[f4] : seg_f4zero();
   }
+  // CTAs c, c+1, ... contribute their head partials while the one before
+  // lies wholly inside the run; their flags and partials are loaded
+  // kFixLook at a time (independent loads), then added in CTA order
   int64_t c = b, end = pos;
-  for (;;) {
-    const float4* H = a.partial + c * 2 * D4;
+  bool go = true;
+  while (go) {
+    bool thru[kFixLook];
+    int32_t hp[kFixLook];
+    float4 h[kFixLook][V];
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
-      const int f4 = sub + v * 32;
-      if (f4 < D4) seg_f4add(s[v], H[f4]);
+    for (int j = 0; j < kFixLook; ++j) {
+      const int64_t cj = c + j;
+      const bool in = cj < n_blocks;
+      thru[j] = in && a.part_thru[cj];
+      hp[j] = in ? a.part_pos[cj * 2] : 0;
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int f4 = sub + v * 32;
+        h[j][v] = (in && f4 < D4) ? a.partial[cj * 2 * D4 + f4] : seg_f4zero();
+      }
     }
-    end = c * span + a.part_pos[c * 2];
-    if (!a.part_thru[c] || c + 1 >= n_blocks) break;
-    ++c;
+#pragma unroll
+    for (int j = 0; j < kFixLook; ++j) {
+      if (go) {
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+          if (sub + v * 32 < D4) seg_f4add(s[v], h[j][v]);
+        end = (c + j) * span + hp[j];
+        go = thru[j] && c + j + 1 < n_blocks;
+      }
+    }
+    c += kFixLook;
   }
   finish_row<V>(a, key, end, s, sub);
 }
