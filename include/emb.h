@@ -220,8 +220,10 @@ typedef struct emb_hash_s* emb_hash;
 
 /* hash_create -- a GPU key -> row table over a private row pool.
  *  num_slots      power of two, 2^10 .. 2^31: open-addressing slots of 16 B.
- *                 Expired entries leave tombstones that are never reused, so
- *                 keep (keys ever inserted) well below num_slots.
+ *                 Expired entries leave tombstones; inserts reuse them and
+ *                 expiry turns a tombstone run that ends at an empty slot
+ *                 back into empty slots.  Keep the live keys well below
+ *                 num_slots (probe lengths grow with the load).
  *  row_capacity   rows in the pool, 1 .. 2^31-1
  *  dim            floats per row (4..256, multiple of 4)
  *  admit_threshold occurrences a key needs before it gets a row (>= 1)
@@ -230,7 +232,8 @@ typedef struct emb_hash_s* emb_hash;
  *                 init_scale * ((splitmix64(key ^ (tid << 48) ^ seed ^ d)
  *                 >> 40) - 2^23) * 2^-23, its accumulator 0.
  *  max_keys_per_call  largest n a hash_lookup_or_insert will pass (< 2^30);
- *                 sizes the admission workspace so lookups never allocate.
+ *                 sizes the admission workspace and 16 lists of touched slots
+ *                 (about 90 B per key in all) so lookups never allocate.
  *  out            (host) receives the handle.
  * Keys are (table id, key) pairs with 0 <= tid < 2^15 and 0 <= key < 2^48;
  * distinct pairs never share an entry or a row.  Allocates the slots, the
@@ -257,12 +260,18 @@ emb_status hash_rows(emb_hash h, float** weight, float** acc);
  * consecutive calls should differ); probing max_probes slots without a place
  * latches EMB_ERR_PROBE_LIMIT and returns -1 for that occurrence.
  *  table_ids [n] int32; keys [n] int64; rows_out [n] int64 (feeds emb_forward
- *  columns of transform EMB_T_ROWS_GIVEN directly).  n <= max_keys_per_call. */
+ *  columns of transform EMB_T_ROWS_GIVEN directly).  n <= max_keys_per_call.
+ *  step      any value but 2^32 - 1 (which marks slots never touched). */
 emb_status hash_lookup_or_insert(emb_hash h, const int32_t* table_ids, const int64_t* keys,
                                  int64_t n, uint32_t step, int64_t* rows_out, void* stream);
 
 /* hash_evict_expired -- remove every entry, admitted or still counting, with
- * now - last_seen > ttl; admitted rows return to the free pool.
+ * now - last_seen > ttl; admitted rows return to the free pool.  Each lookup
+ * lists the slots it touched first; an expiry checks only the lists of steps
+ * more than ttl behind `now`.  With one lookup per step and ttl <= 14 that is
+ * the whole work; a second lookup at one step, or more than 16 steps with
+ * live lists, makes expiries sweep every slot until those lookups are more
+ * than ttl steps old.  The result is the same either way.
  * n_evicted_dev: optional device int64 receiving the number removed. */
 emb_status hash_evict_expired(emb_hash h, uint32_t now, uint32_t ttl, void* stream,
                               int64_t* n_evicted_dev);

@@ -26,8 +26,12 @@
 //                      "rows released by expiry in ascending order, then rows
 //                      never used"; its weights are initialised from its key.
 //        k_hash_fix    occurrences of keys admitted in this call get the row.
-//   K-H3 k_hash_evict  one sweep over the slots removes entries idle > ttl
-//                      and releases their rows.
+//   K-H3 expiry       removes entries idle > ttl and releases their rows:
+//                      k_hash_evict_lists checks only the slots that the
+//                      lookups of the due steps touched first (each lookup
+//                      lists those slots); k_hash_evict sweeps every slot
+//                      when a touch may have gone unlisted (a second lookup
+//                      at one step, more live steps than lists).
 #include <algorithm>
 #include <new>
 
@@ -38,9 +42,18 @@ namespace emb {
 
 constexpr unsigned long long kEmptyKey = ~0ull;
 constexpr unsigned long long kTombKey = ~0ull - 1ull;
+// last_seen of a slot that holds no entry: a value no lookup step may take,
+// so the first touch of a new entry always moves last_seen (and is listed)
+constexpr uint32_t kNeverSeen = 0xFFFFFFFFu;
+// the (state, last_seen) word of a slot that holds no entry
+constexpr unsigned long long kFreeWord = ((unsigned long long)kNeverSeen << 32) | 0xFFFFFFFFull;
 constexpr int kTidBits = 15;
 constexpr int kKeyBits = 48;
 constexpr int kHashPasses = 8;   // 63-bit packed keys, 8-bit digits
+// Lists of the slots each lookup call touched first, kept for incremental
+// expiry: with one lookup per step and expiry every step, ttl + 2 lists are
+// live at a time, so ttl <= kTouchLists - 2 never needs a full sweep.
+constexpr int kTouchLists = 16;
 
 struct __align__(16) Slot {
   unsigned long long key;
@@ -73,6 +86,15 @@ struct emb_hash_s {
   uint32_t* sort_scratch = nullptr;
   uint32_t* status = nullptr;
   int sm_count = 0;
+  // incremental expiry: the slots whose last_seen a lookup call moved to its
+  // step, one list per step
+  uint32_t* touch = nullptr;            // [kTouchLists][max_keys]
+  uint32_t* touch_n = nullptr;          // [kTouchLists] entries per list
+  uint32_t list_step[emb::kTouchLists] = {};
+  bool list_live[emb::kTouchLists] = {};
+  int cur_list = -1;                    // list of the latest lookup's step
+  bool lists_valid = true;              // every touch not yet expired is in a live list
+  int64_t unrecorded_step = -1;         // latest step whose touches were not all listed
 };
 
 namespace emb {
@@ -87,7 +109,15 @@ struct HashArgs {
   uint32_t* nvals;
   int64_t max_keys;
   uint32_t* status;
+  uint32_t* touch;     // list for this call's first touches, or nullptr
+  uint32_t* touch_n;
 };
+
+// One 16-byte read of a whole slot: the key word and the (state, last_seen)
+// word together, in one memory transaction.
+__device__ __forceinline__ void load_slot(const Slot* p, unsigned long long& key, unsigned long long& sw) {
+  asm volatile("ld.volatile.global.v2.u64 {%0, %1}, [%2];" : "=l"(key), "=l"(sw) : "l"(p) : "memory");
+}
 
 __device__ __forceinline__ uint64_t home_slot(uint64_t fkey, uint64_t mask) {
   return splitmix64(fkey ^ 0x5851F42D4C957F2Dull) & mask;
@@ -117,16 +147,21 @@ __global__ void __launch_bounds__(256) k_hash_probe(const HashArgs h, const int3
   uint64_t start = home_slot(fkey, h.mask);
   int64_t found = -1;
   int budget = h.max_probes;
+  unsigned long long sw_seen = 0;   // (state, last_seen) word read with the key
+  bool have_sw = false;
   while (budget > 0 && found < 0) {
     uint64_t pos = start;
     int64_t avail = -1;
     unsigned long long avail_val = 0;
     bool seen_empty = false;
     while (budget > 0) {
-      const unsigned long long k = *(volatile unsigned long long*)&h.slots[pos].key;
+      unsigned long long k, w;
+      load_slot(&h.slots[pos], k, w);
       --budget;
       if (k == fkey) {
         found = (int64_t)pos;
+        sw_seen = w;
+        have_sw = true;
         break;
       }
       if (k == kEmptyKey) {
@@ -157,55 +192,79 @@ __global__ void __launch_bounds__(256) k_hash_probe(const HashArgs h, const int3
     return;
   }
   Slot* s = &h.slots[found];
-  const int32_t state = *(volatile int32_t*)&s->state;
-  if (state >= 0) {
-    if (*(volatile uint32_t*)&s->last_seen != step) s->last_seen = step;
-    rows_out[i] = state;
-    return;
-  }
-  // Count and touch with atomic updates of the whole (state, last_seen) word,
-  // so that "first occurrence of this call" and "count reached the threshold"
-  // are decided on one order of updates.  Only the occurrences that find
-  // last_seen behind the current step race by CAS to set it; once it equals
-  // the step it stays there for the rest of the call, and every later
-  // occurrence counts with one atomic add (no retry loop, which on hot keys
-  // of a cold table would serialise thousands of CAS attempts).  Adding
-  // 2^64 - 1 takes one off the low half without a borrow into last_seen,
-  // since a not-yet-admitted state is negative (count below 2^31 - 1).
   unsigned long long* sw = reinterpret_cast<unsigned long long*>(&s->state);
-  unsigned long long prev = *(volatile unsigned long long*)sw;
-  int32_t old = (int32_t)(uint32_t)(prev & 0xffffffffull);
-  bool counted = false;
-  while (old < 0 && (uint32_t)(prev >> 32) != step) {
-    const unsigned long long nxt = ((unsigned long long)step << 32) | ((uint32_t)old - 1u);
-    const unsigned long long cur = atomicCAS(sw, prev, nxt);
-    if (cur == prev) {
-      counted = true;
-      break;
+  if (!have_sw) sw_seen = *(volatile unsigned long long*)sw;   // the slot was just claimed
+  // An admitted state does not change within a call (admission runs after
+  // the probes), so the word read with the key decides; a counting state
+  // read there may be stale, which the atomics below correct.
+  int32_t old = (int32_t)(uint32_t)(sw_seen & 0xffffffffull);
+  int64_t out;
+  bool first = false;   // this occurrence moved last_seen to this step
+  if (old >= 0) {
+    out = old;
+    if ((uint32_t)(sw_seen >> 32) != step) first = atomicExch(&s->last_seen, step) != step;
+  } else {
+    // Count and touch with atomic updates of the whole (state, last_seen)
+    // word, so that "first occurrence of this call" and "count reached the
+    // threshold" are decided on one order of updates.  Only the occurrences
+    // that find last_seen behind the current step race by CAS to set it;
+    // once it equals the step it stays there for the rest of the call, and
+    // every later occurrence counts with one atomic add (no retry loop, which
+    // on hot keys of a cold table would serialise thousands of CAS attempts).
+    // Adding 2^64 - 1 takes one off the low half without a borrow into
+    // last_seen, since a not-yet-admitted state is negative (count below
+    // 2^31 - 1).
+    unsigned long long prev = sw_seen;
+    bool counted = false;
+    while (old < 0 && (uint32_t)(prev >> 32) != step) {
+      const unsigned long long nxt = ((unsigned long long)step << 32) | ((uint32_t)old - 1u);
+      const unsigned long long cur = atomicCAS(sw, prev, nxt);
+      if (cur == prev) {
+        counted = true;
+        first = true;
+        break;
+      }
+      prev = cur;
+      old = (int32_t)(uint32_t)(prev & 0xffffffffull);
     }
-    prev = cur;
-    old = (int32_t)(uint32_t)(prev & 0xffffffffull);
-  }
-  if (old >= 0) {   // admitted meanwhile (not within one call; kept for safety)
-    rows_out[i] = old;
-    return;
-  }
-  if (!counted) {
-    prev = atomicAdd(sw, ~0ull);
-    old = (int32_t)(uint32_t)(prev & 0xffffffffull);
-  }
-  const uint32_t old_seen = (uint32_t)(prev >> 32);
-  const int32_t count_old = -1 - old, count_new = count_old + 1;
-  // the occurrence that reaches the threshold lists the key; a key left
-  // without a row by a full pool is listed again by its first occurrence
-  if (count_new >= h.thr && (count_old < h.thr || old_seen != step)) {
-    const uint32_t idx = atomicAdd(h.n_new, 1u);
-    if ((int64_t)idx < h.max_keys) {
-      h.nkeys[idx] = fkey;
-      h.nvals[idx] = (uint32_t)found;
+    if (old >= 0) {   // admitted meanwhile (not within one call; kept for safety)
+      out = old;
+    } else {
+      if (!counted) {
+        prev = atomicAdd(sw, ~0ull);
+        old = (int32_t)(uint32_t)(prev & 0xffffffffull);
+      }
+      const uint32_t old_seen = (uint32_t)(prev >> 32);
+      const int32_t count_old = -1 - old, count_new = count_old + 1;
+      // the occurrence that reaches the threshold lists the key; a key left
+      // without a row by a full pool is listed again by its first occurrence
+      if (count_new >= h.thr && (count_old < h.thr || old_seen != step)) {
+        const uint32_t idx = atomicAdd(h.n_new, 1u);
+        if ((int64_t)idx < h.max_keys) {
+          h.nkeys[idx] = fkey;
+          h.nvals[idx] = (uint32_t)found;
+        }
+      }
+      out = -2 - found;
     }
   }
-  rows_out[i] = -2 - found;
+  rows_out[i] = out;
+  // a slot's first touch of the call goes on the call's list (one per
+  // distinct slot, so at most n entries), one atomic per warp
+  if (h.touch) {
+    const unsigned act = __activemask();
+    const unsigned fm = __ballot_sync(act, first);
+    if (fm) {
+      const int lane = threadIdx.x & 31, leader = __ffs(act) - 1;
+      uint32_t base = 0;
+      if (lane == leader) base = atomicAdd(h.touch_n, (uint32_t)__popc(fm));
+      base = __shfl_sync(act, base, leader);
+      if (first) {
+        const uint32_t idx = base + (uint32_t)__popc(fm & ((1u << lane) - 1u));
+        if ((int64_t)idx < h.max_keys) h.touch[idx] = (uint32_t)found;
+      }
+    }
+  }
 }
 
 // free rows per word of the used-row bitmap, exclusive prefix over words
@@ -362,9 +421,53 @@ __global__ void __launch_bounds__(256) k_hash_evict(Slot* slots, int64_t ns, uin
     if ((int64_t)now - (int64_t)ls > (int64_t)ttl) {
       const int32_t st = slots[i].state;
       if (st >= 0) atomicAnd(&used[st >> 5], ~(1u << (st & 31)));
-      slots[i].state = -1;
+      *reinterpret_cast<unsigned long long*>(&slots[i].state) = kFreeWord;
       *(volatile unsigned long long*)&slots[i].key = kTombKey;
       ++cnt;
+    }
+  }
+  if (n_evicted) {
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(kFull, cnt, o);
+    if ((threadIdx.x & 31) == 0 && cnt) atomicAdd(n_evicted, cnt);
+  }
+}
+
+// Incremental expiry: the slots on the lists of steps now - ttl - 1 and
+// before, instead of all slots.  An entry is on the list of every step whose
+// lookup touched it first, so each entry idle longer than ttl is on one of
+// these lists; it is removed when its last_seen still says so (a later touch
+// keeps it).  A slot on two lists is removed once (CAS on the key).  After a
+// removal the tombstone run ending at this slot becomes EMPTY when the next
+// slot is EMPTY (no probe passes an EMPTY slot, so none needs the run).
+struct EvictLists {
+  const uint32_t* list[kTouchLists];
+  const uint32_t* count[kTouchLists];
+  int n;
+};
+
+__global__ void __launch_bounds__(256) k_hash_evict_lists(Slot* slots, uint64_t mask, const EvictLists L,
+                                                          int64_t cap, uint32_t now, uint32_t ttl, uint32_t* used,
+                                                          unsigned long long* n_evicted) {
+  unsigned long long cnt = 0;
+  const int64_t g0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x, gs = (int64_t)gridDim.x * blockDim.x;
+  for (int l = 0; l < L.n; ++l) {
+    const int64_t nl = min((int64_t)*L.count[l], cap);
+    for (int64_t j = g0; j < nl; j += gs) {
+      const uint64_t p = L.list[l][j];
+      unsigned long long k, w;
+      load_slot(&slots[p], k, w);
+      if (k == kEmptyKey || k == kTombKey) continue;
+      if ((int64_t)now - (int64_t)(uint32_t)(w >> 32) <= (int64_t)ttl) continue;
+      if (atomicCAS(&slots[p].key, k, kTombKey) != k) continue;
+      const int32_t st = (int32_t)(uint32_t)(w & 0xffffffffull);
+      if (st >= 0) atomicAnd(&used[st >> 5], ~(1u << (st & 31)));
+      *reinterpret_cast<unsigned long long*>(&slots[p].state) = kFreeWord;
+      ++cnt;
+      if (*(volatile unsigned long long*)&slots[(p + 1) & mask].key == kEmptyKey) {
+        uint64_t q = p;
+        for (int t = 0; t < kTombWalk; ++t, q = (q - 1) & mask)
+          if (atomicCAS(&slots[q].key, kTombKey, kEmptyKey) != kTombKey) break;
+      }
     }
   }
   if (n_evicted) {
@@ -377,7 +480,7 @@ __global__ void k_hash_init(Slot* slots, int64_t ns, uint32_t* used, int64_t nw,
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < ns; i += (int64_t)gridDim.x * blockDim.x) {
     slots[i].key = kEmptyKey;
     slots[i].state = -1;
-    slots[i].last_seen = 0;
+    slots[i].last_seen = kNeverSeen;
   }
   for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < nw; w += (int64_t)gridDim.x * blockDim.x) {
     const int64_t first = w * 32;
@@ -425,6 +528,8 @@ void free_hash(emb_hash_s* h) {
   cudaFree(h->counters);
   cudaFree(h->sort_scratch);
   cudaFree(h->status);
+  cudaFree(h->touch);
+  cudaFree(h->touch_n);
   delete h;
 }
 
@@ -473,6 +578,8 @@ extern "C" emb_status hash_create(int64_t num_slots, int64_t row_capacity, int32
   alloc(&h->counters, sizeof(uint32_t) * 4);
   alloc(&h->sort_scratch, sizeof(uint32_t) * sort_scratch_words<uint64_t>(kHashPasses, max_keys_per_call));
   alloc(&h->status, sizeof(uint32_t));
+  alloc(&h->touch, sizeof(uint32_t) * (size_t)kTouchLists * (size_t)max_keys_per_call);
+  alloc(&h->touch_n, sizeof(uint32_t) * kTouchLists);
   if (e == cudaSuccess) e = cudaMemset(h->W, 0, sizeof(float) * (size_t)row_capacity * dim);
   if (e == cudaSuccess) e = cudaMemset(h->acc, 0, sizeof(float) * (size_t)row_capacity * dim);
   if (e == cudaSuccess) e = cudaMemset(h->status, 0, sizeof(uint32_t));
@@ -499,7 +606,7 @@ extern "C" emb_status hash_rows(emb_hash h, float** weight, float** acc) {
 
 extern "C" emb_status hash_lookup_or_insert(emb_hash h, const int32_t* table_ids, const int64_t* keys, int64_t n,
                                             uint32_t step, int64_t* rows_out, void* stream_) {
-  if (!h || n < 0) return EMB_ERR_INVALID_ARG;
+  if (!h || n < 0 || step == kNeverSeen) return EMB_ERR_INVALID_ARG;
   if (n > h->max_keys) return EMB_ERR_UNSUPPORTED;
   if (n == 0) return EMB_OK;
   if (!table_ids || !keys || !rows_out) return EMB_ERR_INVALID_ARG;
@@ -514,6 +621,29 @@ extern "C" emb_status hash_lookup_or_insert(emb_hash h, const int32_t* table_ids
   a.nvals = h->nvals[0];
   a.max_keys = h->max_keys;
   a.status = h->status;
+  // the list for this call's first touches: a fresh one per step; a second
+  // call at the same step, or no free list, leaves touches unlisted, and
+  // expiry then sweeps all slots until those touches have aged out
+  a.touch = nullptr;
+  a.touch_n = nullptr;
+  int fresh = -1;
+  if (!(h->cur_list >= 0 && h->list_step[h->cur_list] == step))
+    for (int l = 0; l < kTouchLists; ++l)
+      if (!h->list_live[l]) {
+        fresh = l;
+        break;
+      }
+  if (fresh >= 0) {
+    EMB_CUDA_TRY(cudaMemsetAsync(h->touch_n + fresh, 0, sizeof(uint32_t), stream));
+    h->list_live[fresh] = true;
+    h->list_step[fresh] = step;
+    h->cur_list = fresh;
+    a.touch = h->touch + (size_t)fresh * (size_t)h->max_keys;
+    a.touch_n = h->touch_n + fresh;
+  } else {
+    h->lists_valid = false;
+    if ((int64_t)step > h->unrecorded_step) h->unrecorded_step = step;
+  }
   EMB_CUDA_TRY(cudaMemsetAsync(h->counters, 0, sizeof(uint32_t), stream));
   k_hash_probe<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(a, table_ids, keys, n, step, rows_out);
   int res = 0;
@@ -537,8 +667,30 @@ extern "C" emb_status hash_evict_expired(emb_hash h, uint32_t now, uint32_t ttl,
   if (!h) return EMB_ERR_INVALID_ARG;
   cudaStream_t stream = (cudaStream_t)stream_;
   if (n_evicted_dev) EMB_CUDA_TRY(cudaMemsetAsync(n_evicted_dev, 0, sizeof(int64_t), stream));
-  k_hash_evict<<<h->sm_count * 8, 256, 0, stream>>>(h->slots, h->num_slots, now, ttl, h->used,
-                                                     reinterpret_cast<unsigned long long*>(n_evicted_dev));
+  // lists whose step is more than ttl behind `now`: every entry idle longer
+  // than ttl is on one of them (while the lists are complete)
+  EvictLists L{};
+  for (int l = 0; l < kTouchLists; ++l)
+    if (h->list_live[l] && (int64_t)now - (int64_t)h->list_step[l] > (int64_t)ttl) {
+      L.list[L.n] = h->touch + (size_t)l * (size_t)h->max_keys;
+      L.count[L.n] = h->touch_n + l;
+      ++L.n;
+      h->list_live[l] = false;
+      if (h->cur_list == l) h->cur_list = -1;
+    }
+  if (!h->lists_valid) {
+    k_hash_evict<<<h->sm_count * 8, 256, 0, stream>>>(h->slots, h->num_slots, now, ttl, h->used,
+                                                       reinterpret_cast<unsigned long long*>(n_evicted_dev));
+    // the unlisted touches are all expired once now is past them by more than ttl
+    if ((int64_t)now - h->unrecorded_step > (int64_t)ttl) {
+      h->lists_valid = true;
+      h->unrecorded_step = -1;
+    }
+  } else if (L.n > 0) {
+    k_hash_evict_lists<<<h->sm_count * 4, 256, 0, stream>>>(h->slots, (uint64_t)h->num_slots - 1, L, h->max_keys,
+                                                             now, ttl, h->used,
+                                                             reinterpret_cast<unsigned long long*>(n_evicted_dev));
+  }
   return cuda_status(cudaGetLastError());
 }
 

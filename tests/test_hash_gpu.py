@@ -73,6 +73,35 @@ def test_random_streams_match_oracle(seed, thr, ttl, cap):
         assert np.array_equal(w[ex["row"][adm]], oh.W[ex["row"][adm]]), "initial rows"
 
 
+@pytest.mark.parametrize("seed", [11, 12])
+def test_irregular_calls_match_oracle(seed):
+    """Expiry stays exact when lookups repeat a step, skip steps, or are not
+    followed by an expiry, and when ttl changes from call to call or exceeds
+    the window of touch lists (those cases fall back to full sweeps).  The
+    row pool never fills here: a repeated step does not re-list keys a full
+    pool left without a row (calls are told apart by their step)."""
+    rng = np.random.default_rng(seed)
+    cap = 4000
+    ht = sl.HashTable(1 << 12, cap, 8, 2, 256, seed, 0.1, 2000)
+    oh = oracle.Hash(cap, 8, 2, seed, 0.1)
+    step = 0
+    for it in range(60):
+        step += int(rng.choice([0, 1, 1, 1, 2, 5]))
+        for _ in range(int(rng.choice([1, 1, 2]))):
+            n = int(rng.integers(1, 2000))
+            keys = synth.zipf(rng, 300, 1.1, n)
+            tids = rng.integers(0, 3, n).astype(np.int32)
+            got, st = lookup(ht, tids, keys, step)
+            want, st_o = oh.lookup_or_insert(tids, keys, step)
+            assert st == 0 and st_o == 0, (st, st_o)
+            assert got == want.tolist(), "iteration %d" % it
+        if rng.random() < 0.8:
+            ttl = int(rng.choice([0, 1, 3, 10, 14, 20, 40]))
+            ht.evict_expired(step, ttl)
+            oh.evict(step, ttl)
+            compare_hash_maps(ht.export(), oh.export(), "iteration %d" % it)
+
+
 def test_probe_limit_is_reported_not_hung():
     ht = sl.HashTable(1024, 4096, 4, 1, 2, 1, 0.1, 5000)
     keys = np.arange(5000, dtype=np.int64) * 7919
