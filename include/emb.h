@@ -233,7 +233,7 @@ typedef struct emb_hash_s* emb_hash;
  *                 >> 40) - 2^23) * 2^-23, its accumulator 0.
  *  max_keys_per_call  largest n a hash_lookup_or_insert will pass (< 2^30);
  *                 sizes the admission workspace and 16 lists of touched slots
- *                 (about 90 B per key in all) so lookups never allocate.
+ *                 (about 95 B per key in all) so lookups never allocate.
  *  out            (host) receives the handle.
  * Keys are (table id, key) pairs with 0 <= tid < 2^15 and 0 <= key < 2^48;
  * distinct pairs never share an entry or a row.  Allocates the slots, the

@@ -80,6 +80,7 @@ struct emb_hash_s {
   int64_t n_words = 0;
   uint32_t* free_scan = nullptr;   // [n_words + 1] exclusive prefix of free rows per word
   uint32_t* scan_part = nullptr;   // per 1024-word block partials
+  uint32_t* free_rows = nullptr;   // [max_keys] the lowest free rows, ascending
   uint64_t* nkeys[2] = {nullptr, nullptr};
   uint32_t* nvals[2] = {nullptr, nullptr};
   uint32_t* counters = nullptr;    // [0] listed keys, [1] exported entries
@@ -313,12 +314,16 @@ __global__ void __launch_bounds__(kScanBlk) k_scan_parts(uint32_t* part, int nb)
   }
 }
 
+// ... and the free rows themselves, in ascending order, as far as the keys
+// listed for admission need them: free_rows[i] = the i-th free row.
 __global__ void __launch_bounds__(kScanBlk) k_free_down(const uint32_t* used, int64_t nw, const uint32_t* part,
-                                                        uint32_t* free_scan) {
+                                                        uint32_t* free_scan, const uint32_t* n_new, int64_t max_keys,
+                                                        uint32_t* free_rows) {
   __shared__ uint32_t wsum[32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t w = blockIdx.x * (int64_t)kScanBlk + threadIdx.x;
-  const uint32_t f = w < nw ? (uint32_t)__popc(~used[w]) : 0u;
+  const uint32_t bits = w < nw ? ~used[w] : 0u;
+  const uint32_t f = (uint32_t)__popc(bits);
   uint32_t x = f;
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t y = __shfl_up_sync(kFull, x, o);
@@ -330,6 +335,9 @@ __global__ void __launch_bounds__(kScanBlk) k_free_down(const uint32_t* used, in
   for (int j = 0; j < warp; ++j) base += wsum[j];
   if (w < nw) free_scan[w] = base + x - f;
   if (w == nw - 1) free_scan[nw] = base + x;
+  const int64_t need = ((int64_t)*n_new < max_keys) ? (int64_t)*n_new : max_keys;
+  int64_t pos = (int64_t)(base + x - f);
+  for (uint32_t b = bits; b && pos < need; b &= b - 1u, ++pos) free_rows[pos] = (uint32_t)(w * 32 + __ffs(b) - 1);
 }
 
 __device__ __forceinline__ float init_value(uint64_t fkey, uint64_t seed, int d, float scale) {
@@ -339,14 +347,13 @@ __device__ __forceinline__ float init_value(uint64_t fkey, uint64_t seed, int d,
   return __fmul_rn(f, scale);
 }
 
-// K-H2: the i-th listed key (ascending) takes the i-th free row.  The bitmap
-// is only read here (every warp sees the same snapshot); k_hash_mark sets the
-// bits of the rows handed out afterwards.
+// K-H2: the i-th listed key (ascending) takes the i-th free row, listed by
+// k_free_down; k_hash_mark sets the bits of the rows handed out afterwards.
 __global__ void __launch_bounds__(256) k_hash_admit(Slot* slots, const uint64_t* __restrict__ skeys,
                                                     const uint32_t* __restrict__ svals, const uint32_t* n_new,
-                                                    int64_t max_keys, uint32_t* used, const uint32_t* free_scan,
-                                                    int64_t nw, float* W, float* A, int dim, uint64_t seed,
-                                                    float scale, uint32_t* status) {
+                                                    int64_t max_keys, const uint32_t* free_scan,
+                                                    const uint32_t* __restrict__ free_rows, int64_t nw, float* W,
+                                                    float* A, int dim, uint64_t seed, float scale, uint32_t* status) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -357,16 +364,7 @@ __global__ void __launch_bounds__(256) k_hash_admit(Slot* slots, const uint64_t*
       if (lane == 0) latch(status, EMB_ERR_TABLE_FULL);
       continue;
     }
-    // word holding the i-th free row: last w with free_scan[w] <= i
-    int64_t lo = 0, hi = nw;   // free_scan[lo] <= i < free_scan[hi]
-    while (hi - lo > 1) {
-      const int64_t mid = (lo + hi) >> 1;
-      if (free_scan[mid] <= (uint32_t)i) lo = mid; else hi = mid;
-    }
-    uint32_t freebits = ~used[lo];
-    for (uint32_t r = (uint32_t)i - free_scan[lo]; r > 0; --r) freebits &= freebits - 1u;
-    const int bit = __ffs(freebits) - 1;
-    const int64_t row = lo * 32 + bit;
+    const int64_t row = free_rows[i];
     const uint64_t fkey = skeys[i];
     if (lane == 0) slots[svals[i]].state = (int32_t)row;
     for (int d = lane; d < dim; d += 32) {
@@ -521,6 +519,7 @@ void free_hash(emb_hash_s* h) {
   cudaFree(h->used);
   cudaFree(h->free_scan);
   cudaFree(h->scan_part);
+  cudaFree(h->free_rows);
   cudaFree(h->nkeys[0]);
   cudaFree(h->nkeys[1]);
   cudaFree(h->nvals[0]);
@@ -571,6 +570,7 @@ extern "C" emb_status hash_create(int64_t num_slots, int64_t row_capacity, int32
   alloc(&h->used, sizeof(uint32_t) * (size_t)h->n_words);
   alloc(&h->free_scan, sizeof(uint32_t) * (size_t)(h->n_words + 1));
   alloc(&h->scan_part, sizeof(uint32_t) * (size_t)((h->n_words + kScanBlk - 1) / kScanBlk + 1));
+  alloc(&h->free_rows, sizeof(uint32_t) * (size_t)max_keys_per_call);
   for (int i = 0; i < 2; ++i) {
     alloc(&h->nkeys[i], sizeof(uint64_t) * (size_t)max_keys_per_call);
     alloc(&h->nvals[i], sizeof(uint32_t) * (size_t)max_keys_per_call);
@@ -653,10 +653,11 @@ extern "C" emb_status hash_lookup_or_insert(emb_hash h, const int32_t* table_ids
   const int nb = (int)((h->n_words + kScanBlk - 1) / kScanBlk);
   k_free_reduce<<<nb, kScanBlk, 0, stream>>>(h->used, h->n_words, h->scan_part);
   k_scan_parts<<<1, kScanBlk, 0, stream>>>(h->scan_part, nb);
-  k_free_down<<<nb, kScanBlk, 0, stream>>>(h->used, h->n_words, h->scan_part, h->free_scan);
+  k_free_down<<<nb, kScanBlk, 0, stream>>>(h->used, h->n_words, h->scan_part, h->free_scan, h->counters,
+                                           h->max_keys, h->free_rows);
   k_hash_admit<<<h->sm_count * 4, 256, 0, stream>>>(h->slots, h->nkeys[res], h->nvals[res], h->counters,
-                                                     h->max_keys, h->used, h->free_scan, h->n_words, h->W, h->acc,
-                                                     h->dim, h->seed, h->init_scale, h->status);
+                                                     h->max_keys, h->free_scan, h->free_rows, h->n_words, h->W,
+                                                     h->acc, h->dim, h->seed, h->init_scale, h->status);
   k_hash_mark<<<h->sm_count * 2, 256, 0, stream>>>(h->slots, h->nvals[res], h->counters, h->max_keys, h->used);
   k_hash_fix<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(h->slots, n, rows_out);
   return cuda_status(cudaGetLastError());

@@ -238,7 +238,13 @@ __device__ __forceinline__ void onesweep_tile(SortSmemT<K>& sm, const K* __restr
   }
 }
 
-template <class K>
+// One tile per CTA (PERSIST = false; the grid covers the tiles), or
+// persistent CTAs that take tiles in ticket order until none is left
+// (PERSIST = true, for counts that live on the device: the grid is sized for
+// the capacity, and CTAs past the count cost one ticket each).  Either way a
+// tile only ever waits on tiles whose tickets were drawn earlier, by CTAs
+// already running.
+template <class K, bool PERSIST>
 __global__ void __launch_bounds__(kSortThreads, 2)
     k_onesweep_t(const K* __restrict__ kin, const uint32_t* __restrict__ vin, K* __restrict__ kout,
                  uint32_t* __restrict__ vout, int64_t n0, const uint32_t* n_dev, int shift,
@@ -249,16 +255,19 @@ __global__ void __launch_bounds__(kSortThreads, 2)
   const int tid = threadIdx.x;
   const int64_t n = sort_count(n0, n_dev);
   const int64_t tiles = (n + TILE - 1) / TILE;
-  if (tid == 0) sm.tile = atomicAdd(tile_ctr, 1u);
-  for (int i = tid; i < kSortWarps * kRadix; i += kSortThreads) (&sm.whist[0][0])[i] = 0;
   const uint32_t hs = sort_scan256(tid < kRadix ? __ldg(hist + tid) : 0u, sm.wsum);
   if (tid < kRadix) sm.hscan[tid] = hs;
-  __syncthreads();
-  const uint32_t t = sm.tile;
-  if ((int64_t)t >= tiles) return;   // past the data: nobody waits on this ticket
-  const int64_t left = n - (int64_t)t * TILE;
-  onesweep_tile<K>(sm, kin, vin, kout, vout, (uint32_t)n, t, left >= TILE ? TILE : (int)left, shift, lookback,
-                   status);
+  do {
+    if (tid == 0) sm.tile = atomicAdd(tile_ctr, 1u);
+    for (int i = tid; i < kSortWarps * kRadix; i += kSortThreads) (&sm.whist[0][0])[i] = 0;
+    __syncthreads();
+    const uint32_t t = sm.tile;
+    if ((int64_t)t >= tiles) return;   // past the data: nobody waits on this ticket
+    const int64_t left = n - (int64_t)t * TILE;
+    onesweep_tile<K>(sm, kin, vin, kout, vout, (uint32_t)n, t, left >= TILE ? TILE : (int)left, shift, lookback,
+                     status);
+    if (PERSIST) __syncthreads();   // the tile's shared memory is free again
+  } while (PERSIST);
 }
 
 // Words of scratch the sort needs: hist [passes][256], tickets [passes],
@@ -287,13 +296,22 @@ inline emb_status radix_sort_pairs(K* const keys[2], uint32_t* const vals[2], in
   EMB_CUDA_TRY(cudaMemsetAsync(scratch, 0, sort_scratch_words<K>(passes, cap) * sizeof(uint32_t), stream));
   const int hgrid = (int)std::min<int64_t>((cap + 511) / 512, (int64_t)sm_count * 4);
   k_digit_hist_t<K><<<hgrid, 512, 0, stream>>>(keys[0], n, n_dev, passes, hist);
-  EMB_CUDA_TRY(cudaFuncSetAttribute(k_onesweep_t<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const bool persist = n_dev != nullptr;
+  const int64_t grid = persist ? std::min<int64_t>(tiles, (int64_t)sm_count * 2) : tiles;   // two CTAs fit an SM
+  EMB_CUDA_TRY(cudaFuncSetAttribute(k_onesweep_t<K, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)sizeof(SortSmemT<K>)));
+  EMB_CUDA_TRY(cudaFuncSetAttribute(k_onesweep_t<K, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)sizeof(SortSmemT<K>)));
   for (int ps = 0; ps < passes; ++ps) {
     const int in = ps & 1, out = in ^ 1;
-    k_onesweep_t<K><<<(unsigned)tiles, kSortThreads, sizeof(SortSmemT<K>), stream>>>(
-        keys[in], vals[in], keys[out], vals[out], n, n_dev, ps * kRadixBits, hist + ps * kRadix,
-        lookback + (size_t)ps * tiles * kRadix, tickets + ps, status);
+    if (persist)
+      k_onesweep_t<K, true><<<(unsigned)grid, kSortThreads, sizeof(SortSmemT<K>), stream>>>(
+          keys[in], vals[in], keys[out], vals[out], n, n_dev, ps * kRadixBits, hist + ps * kRadix,
+          lookback + (size_t)ps * tiles * kRadix, tickets + ps, status);
+    else
+      k_onesweep_t<K, false><<<(unsigned)grid, kSortThreads, sizeof(SortSmemT<K>), stream>>>(
+          keys[in], vals[in], keys[out], vals[out], n, n_dev, ps * kRadixBits, hist + ps * kRadix,
+          lookback + (size_t)ps * tiles * kRadix, tickets + ps, status);
   }
   *result = passes & 1;
   return cuda_status(cudaGetLastError());
