@@ -703,9 +703,8 @@ emb_status launch_backward(emb_plan_s* p, const float* grad_out, const float* gr
     if (want_dbg && dbg->n_unique) EMB_CUDA_TRY(cudaMemsetAsync(dbg->n_unique, 0, sizeof(int64_t), stream));
     return EMB_OK;
   }
-  const int passes = (p->key_bits + kRadixBits - 1) / kRadixBits;
   int res = 0;
-  emb_status st = radix_sort_pairs<uint32_t>(w.keys, w.vals, n, nullptr, n, passes, w.hist, p->sm_count,
+  emb_status st = radix_sort_pairs<uint32_t>(w.keys, w.vals, n, nullptr, n, p->key_bits, w.hist, p->sm_count,
                                              p->status_d, stream, &res);
   if (st != EMB_OK) return st;
   const uint32_t* skeys = w.keys[res];
@@ -783,7 +782,8 @@ constexpr int64_t kNoAllocMaxN = int64_t(1) << 18;   // contributions per call
 constexpr int kNoAllocMaxDim = 256;
 constexpr int64_t kNoAllocTiles = (kNoAllocMaxN + kSortTile - 1) / kSortTile;
 constexpr int64_t kNoAllocBlocks = (kNoAllocMaxN + 255) / 256;   // the smallest span seg_span() returns
-constexpr size_t kNoAllocSortWords = 4 * kRadix + 4 + 4 * kNoAllocTiles * kRadix;  // sort_scratch_words(4, max n)
+// sort_scratch_words for up to 32-bit keys: four passes of 8-bit digits
+constexpr size_t kNoAllocSortWords = 4 * 256 + 4 + 4 * kNoAllocTiles * 256;
 
 struct NoAllocScratch {
   uint32_t keys[2][kNoAllocMaxN];
@@ -878,14 +878,13 @@ extern "C" emb_status emb_sparse_adagrad_noalloc(const int64_t* rows, int64_t n,
 
   int key_bits = 1;
   while (key_bits < 32 && (uint64_t(1) << key_bits) <= (uint64_t)num_rows) ++key_bits;
-  const int passes = (key_bits + kRadixBits - 1) / kRadixBits;
   k_noalloc_setup<<<1, 32, 0, stream>>>(s, weight, acc, num_rows, dim);
   k_noalloc_pairs<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(rows, n, num_rows, s->keys[0], s->vals[0]);
   uint32_t* const nk[2] = {s->keys[0], s->keys[1]};
   uint32_t* const nv[2] = {s->vals[0], s->vals[1]};
   int res = 0;
   // the sort clears its part of the area (histograms, tickets, look-back words) itself
-  st = radix_sort_pairs<uint32_t>(nk, nv, n, nullptr, n, passes, s->sortw, sms, nullptr, stream, &res);
+  st = radix_sort_pairs<uint32_t>(nk, nv, n, nullptr, n, key_bits, s->sortw, sms, nullptr, stream, &res);
   if (st != EMB_OK) return st;
   SegArgs a{};
   a.keys = s->keys[res];

@@ -49,7 +49,7 @@ constexpr uint32_t kNeverSeen = 0xFFFFFFFFu;
 constexpr unsigned long long kFreeWord = ((unsigned long long)kNeverSeen << 32) | 0xFFFFFFFFull;
 constexpr int kTidBits = 15;
 constexpr int kKeyBits = 48;
-constexpr int kHashPasses = 8;   // 63-bit packed keys, 8-bit digits
+constexpr int kHashKeyBits = 63;   // packed (tid << 48 | key) sort keys
 // Lists of the slots each lookup call touched first, kept for incremental
 // expiry: with one lookup per step and expiry every step, ttl + 2 lists are
 // live at a time, so ttl <= kTouchLists - 2 never needs a full sweep.
@@ -576,7 +576,7 @@ extern "C" emb_status hash_create(int64_t num_slots, int64_t row_capacity, int32
     alloc(&h->nvals[i], sizeof(uint32_t) * (size_t)max_keys_per_call);
   }
   alloc(&h->counters, sizeof(uint32_t) * 4);
-  alloc(&h->sort_scratch, sizeof(uint32_t) * sort_scratch_words<uint64_t>(kHashPasses, max_keys_per_call));
+  alloc(&h->sort_scratch, sizeof(uint32_t) * sort_scratch_words<uint64_t>(kHashKeyBits, max_keys_per_call));
   alloc(&h->status, sizeof(uint32_t));
   alloc(&h->touch, sizeof(uint32_t) * (size_t)kTouchLists * (size_t)max_keys_per_call);
   alloc(&h->touch_n, sizeof(uint32_t) * kTouchLists);
@@ -647,7 +647,7 @@ extern "C" emb_status hash_lookup_or_insert(emb_hash h, const int32_t* table_ids
   EMB_CUDA_TRY(cudaMemsetAsync(h->counters, 0, sizeof(uint32_t), stream));
   k_hash_probe<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(a, table_ids, keys, n, step, rows_out);
   int res = 0;
-  emb_status st = radix_sort_pairs<uint64_t>(h->nkeys, h->nvals, 0, h->counters, n, kHashPasses, h->sort_scratch,
+  emb_status st = radix_sort_pairs<uint64_t>(h->nkeys, h->nvals, 0, h->counters, n, kHashKeyBits, h->sort_scratch,
                                              h->sm_count, h->status, stream, &res);
   if (st != EMB_OK) return st;
   const int nb = (int)((h->n_words + kScanBlk - 1) / kScanBlk);

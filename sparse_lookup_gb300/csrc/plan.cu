@@ -6,6 +6,7 @@
 #include <new>
 
 #include "plan.cuh"
+#include "radix.cuh"
 
 using namespace emb;
 
@@ -208,19 +209,12 @@ extern "C" emb_status emb_plan_create(const emb_column_desc* cols, int32_t n_col
     const int64_t n = std::max<int64_t>(max_ids, 1);
     w.max_tiles = (n + kSortTile - 1) / kSortTile;
     w.n_units_max = (n + kUnit - 1) / kUnit;
-    const int passes = (p->key_bits + kRadixBits - 1) / kRadixBits;
     for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
       e = dmalloc(&w.keys[i], n, &total);
       if (e == cudaSuccess) e = dmalloc(&w.vals[i], n, &total);
     }
     if (e == cudaSuccess) e = dmalloc(&w.inv_n, (size_t)n_cols * max_batch, &total);
-    // hist [4][kRadix], tile tickets [4], look-back words [passes][tiles][kRadix]
-    const size_t sort_words = 4 * kRadix + 4 + (size_t)passes * w.max_tiles * kRadix;
-    if (e == cudaSuccess) e = dmalloc(&w.hist, sort_words, &total);
-    if (e == cudaSuccess) {
-      w.tile_ctr = w.hist + 4 * kRadix;
-      w.lookback = w.tile_ctr + 4;
-    }
+    if (e == cudaSuccess) e = dmalloc(&w.hist, sort_scratch_words<uint32_t>(p->key_bits, n), &total);
     if (e == cudaSuccess) e = dmalloc(&w.run_head, n + 1, &total);
     if (e == cudaSuccess) e = dmalloc(&w.head_pos, n, &total);
     if (e == cudaSuccess) e = dmalloc(&w.n_runs, 4, &total);

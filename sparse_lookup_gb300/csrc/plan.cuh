@@ -24,22 +24,18 @@ constexpr int kMaxLongPerTile = kMaxTileElems / kLongBag + 2;
 constexpr int kUnit = 128;
 constexpr uint32_t kPadBit = 0x80000000u;
 
-// Radix sort geometry (LSD, 8-bit digits, chained scan with decoupled
-// look-back).
+// Radix sort geometry (LSD, 8- or 10-bit digits, chained scan with decoupled
+// look-back): threads per CTA and 32-bit pairs per thread of a tile.
 constexpr int kSortThreads = 512;
 constexpr int kSortItems = 15;
 constexpr int kSortTile = kSortThreads * kSortItems;
-constexpr int kRadixBits = 8;
-constexpr int kRadix = 1 << kRadixBits;
 
 struct Workspace {
   // sort buffers: keys (global rows) and values (gradient sources)
   uint32_t* keys[2] = {nullptr, nullptr};
   uint32_t* vals[2] = {nullptr, nullptr};
   float* inv_n = nullptr;          // [n_cols * max_batch] 1/n_valid of mean bags
-  uint32_t* hist = nullptr;        // [4][kRadix] digit counts of all passes
-  uint32_t* lookback = nullptr;    // [max_tiles][kRadix] chained-scan words
-  uint32_t* tile_ctr = nullptr;    // [4] tile tickets per pass
+  uint32_t* hist = nullptr;        // the sort's scratch: histograms, tile tickets, look-back words
   uint32_t* run_head = nullptr;    // [max_ids + 1] debug: runs started at or before each position
   uint32_t* head_pos = nullptr;    // [max_ids] debug: position of each run's first entry
   uint32_t* n_runs = nullptr;      // [1]

@@ -1,5 +1,6 @@
-// radix.cuh -- stable LSD radix sort of (key, u32 value) pairs, one 8-bit
-// digit per pass: a single read of the keys builds the digit histograms of all
+// radix.cuh -- stable LSD radix sort of (key, u32 value) pairs, 8-bit digits
+// (the kernels take the digit width as a parameter; sort_plan picks it): a
+// single read of the keys builds the digit histograms of all
 // passes, then each pass is one chained-scan scatter kernel in which a CTA
 // ranks its tile in shared memory, publishes its per-digit counts and finds
 // its global offsets by decoupled look-back over the earlier tiles (Adinets &
@@ -13,6 +14,8 @@
 // count do nothing.
 #pragma once
 
+#include <type_traits>
+
 #include "plan.cuh"
 
 namespace emb {
@@ -23,6 +26,7 @@ constexpr uint32_t kCountMask = (1u << 30) - 1;
 constexpr int kSpinLimit = 1 << 22;
 constexpr int kLookWin = 8;   // look-back words loaded per round trip
 constexpr int kSortWarps = kSortThreads / 32;
+constexpr int kMaxSortPasses = 8;
 
 template <class K>
 struct SortItems;
@@ -36,17 +40,36 @@ struct SortItems<uint64_t> {
 };
 
 template <class K>
+constexpr int sort_tile() {
+  return kSortThreads * SortItems<K>::value;
+}
+
+template <class K, int BITS>
 struct SortSmemT {
-  static constexpr int kTile = kSortThreads * SortItems<K>::value;
+  static constexpr int kR = 1 << BITS;
+  static constexpr int kTile = sort_tile<K>();
+  // per-warp digit counts, then slots: at most kTile, so 16 bits hold them
+  using Count = typename std::conditional<(BITS > 8), uint16_t, uint32_t>::type;
   K keys[kTile];
   uint32_t vals[kTile];
-  uint32_t whist[kSortWarps][kRadix];  // per-warp digit counts, then warp offsets
-  uint32_t dstart[kRadix];             // first slot of each digit inside the tile
-  uint32_t goff[kRadix];               // global position of the tile's first item of each digit
-  uint32_t hscan[kRadix];              // exclusive scan of the pass histogram
+  Count whist[kSortWarps][kR];         // per-warp digit counts, then each warp's first slot
+  uint32_t dstart[kR];                 // first slot of each digit inside the tile
+  uint32_t goff[kR];                   // output position of shared slot j of a digit, minus j
+  uint32_t hscan[kR];                  // exclusive scan of the pass histogram
   uint32_t wsum[kSortWarps];
   uint32_t tile;
 };
+
+// Digit width and number of passes for keys of key_bits bits.  8-bit digits:
+// measured on 41.75 M training pairs of 30-bit keys, three passes of 10-bit
+// digits (1024 bins, 7.5 pairs per bin and tile) took 1.44 ms against 1.21 ms
+// for four passes of 8-bit digits -- the per-tile digit work and the shorter
+// output runs cost more than the pass saved.
+inline void sort_plan(int key_bits, int* bits, int* passes) {
+  const int kb = key_bits < 1 ? 1 : key_bits;
+  *bits = 8;
+  *passes = (kb + 7) / 8;
+}
 
 // Element count: n, or the count in device memory clamped to the capacity n.
 __device__ __forceinline__ int64_t sort_count(int64_t n, const uint32_t* n_dev) {
@@ -55,59 +78,74 @@ __device__ __forceinline__ int64_t sort_count(int64_t n, const uint32_t* n_dev) 
   return c < n ? c : n;
 }
 
-template <class K>
+template <class K, int BITS>
+__device__ __forceinline__ uint32_t sort_digit(K k, int shift) {
+  return (uint32_t)(k >> shift) & (uint32_t)((1 << BITS) - 1);
+}
+
+// Digit histograms of all passes in one read of the keys.
+template <class K, int BITS>
 __global__ void __launch_bounds__(512) k_digit_hist_t(const K* __restrict__ keys, int64_t n0,
                                                       const uint32_t* n_dev, int passes,
                                                       uint32_t* __restrict__ hist) {
-  __shared__ uint32_t h[8 * kRadix];
+  constexpr int R = 1 << BITS;
+  __shared__ uint32_t h[kMaxSortPasses * R];
   const int64_t n = sort_count(n0, n_dev);
-  for (int i = threadIdx.x; i < passes * kRadix; i += blockDim.x) h[i] = 0;
+  for (int i = threadIdx.x; i < passes * R; i += blockDim.x) h[i] = 0;
   __syncthreads();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const K k = keys[i];
-    for (int p = 0; p < passes; ++p) atomicAdd(&h[p * kRadix + (uint32_t)((k >> (p * kRadixBits)) & (kRadix - 1))], 1u);
+    for (int p = 0; p < passes; ++p) atomicAdd(&h[p * R + sort_digit<K, BITS>(k, p * BITS)], 1u);
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < passes * kRadix; i += blockDim.x)
+  for (int i = threadIdx.x; i < passes * R; i += blockDim.x)
     if (h[i]) atomicAdd(&hist[i], h[i]);
 }
 
 // Lanes of the warp holding the same digit d, found with one ballot per digit
 // bit: the mask starts full and each ballot keeps the lanes that agree with
-// this lane on that bit.  BITS = kRadixBits + 1 when some lanes hold the "no
-// item" marker kRadix.  All lanes must call.
-template <int BITS>
+// this lane on that bit.  NB = digit bits + 1 when some lanes hold the "no
+// item" marker 1 << digit bits.  All lanes must call.
+template <int NB>
 __device__ __forceinline__ unsigned warp_match_digit(uint32_t d) {
   unsigned peers = kFull;
 #pragma unroll
-  for (int b = 0; b < BITS; ++b) {
+  for (int b = 0; b < NB; ++b) {
     const unsigned m = __ballot_sync(kFull, (d >> b) & 1u);
     peers &= ((d >> b) & 1u) ? m : ~m;
   }
   return peers;
 }
 
-// Exclusive scan over the first 256 threads' values (all threads call).
-__device__ __forceinline__ uint32_t sort_scan256(uint32_t v, uint32_t* wsum) {
+// Exclusive scan of R per-digit values over the CTA: thread t holds the
+// values of digits t*PER .. t*PER+PER-1 in v[] (PER = R / kSortThreads, at
+// least 1; threads past the last digit hold zeros).  All threads call.
+template <int R>
+__device__ __forceinline__ void sort_scan_digits(uint32_t (&v)[(R + kSortThreads - 1) / kSortThreads],
+                                                 uint32_t* wsum) {
+  constexpr int PER = (R + kSortThreads - 1) / kSortThreads;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t x = v;
+  uint32_t tot = 0;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const uint32_t c = v[q];
+    v[q] = tot;   // exclusive within the thread
+    tot += c;
+  }
+  uint32_t x = tot;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const uint32_t y = __shfl_up_sync(kFull, x, o);
     if (lane >= o) x += y;
   }
-  if (lane == 31 && warp < kRadix / 32) wsum[warp] = x;
+  if (lane == 31) wsum[warp] = x;
   __syncthreads();
   uint32_t base = 0;
-  if (warp < kRadix / 32)
-    for (int w = 0; w < warp; ++w) base += wsum[w];
+  for (int w = 0; w < warp; ++w) base += wsum[w];
   __syncthreads();
-  return base + x - v;
-}
-
-template <class K>
-__device__ __forceinline__ uint32_t sort_digit(K k, int shift) {
-  return (uint32_t)(k >> shift) & (uint32_t)(kRadix - 1);
+  base += x - tot;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) v[q] += base;
 }
 
 // One tile of a pass: rank the items by digit within the tile (stable: warp
@@ -115,14 +153,17 @@ __device__ __forceinline__ uint32_t sort_digit(K k, int shift) {
 // place the items in shared memory in digit order, find the tile's global
 // digit offsets by look-back, write out.  FULL: the tile holds TILE items
 // (no per-item bounds, one ballot less).
-template <class K>
-__device__ __forceinline__ void onesweep_tile(SortSmemT<K>& sm, const K* __restrict__ kin,
+template <class K, int BITS>
+__device__ __forceinline__ void onesweep_tile(SortSmemT<K, BITS>& sm, const K* __restrict__ kin,
                                               const uint32_t* __restrict__ vin, K* __restrict__ kout,
                                               uint32_t* __restrict__ vout, uint32_t n, uint32_t t, int tile_n,
                                               int shift, uint32_t* lookback, uint32_t* status) {
-  const bool FULL = tile_n == SortSmemT<K>::kTile;
+  using Count = typename SortSmemT<K, BITS>::Count;
+  constexpr int R = 1 << BITS;
+  constexpr int PER = (R + kSortThreads - 1) / kSortThreads;   // digits per thread
   constexpr int ITEMS = SortItems<K>::value;
-  constexpr int TILE = SortSmemT<K>::kTile;
+  constexpr int TILE = sort_tile<K>();
+  const bool FULL = tile_n == TILE;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int w0 = warp * 32 * ITEMS;            // the warp's first item in the tile
   const K* wk = kin + (size_t)t * TILE + w0;
@@ -142,13 +183,13 @@ __device__ __forceinline__ void onesweep_tile(SortSmemT<K>& sm, const K* __restr
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) {
     const bool ok = FULL || w0 + i * 32 + lane < tile_n;
-    const uint32_t d = ok ? sort_digit(k[i], shift) : (uint32_t)kRadix;
-    const unsigned peers = FULL ? warp_match_digit<kRadixBits>(d) : warp_match_digit<kRadixBits + 1>(d);
+    const uint32_t d = ok ? sort_digit<K, BITS>(k[i], shift) : (uint32_t)R;
+    const unsigned peers = FULL ? warp_match_digit<BITS>(d) : warp_match_digit<BITS + 1>(d);
     const int leader = 31 - __clz(peers);
     uint32_t old = 0;
     if (lane == leader && ok) {
       old = sm.whist[warp][d];
-      sm.whist[warp][d] = old + __popc(peers);
+      sm.whist[warp][d] = (Count)(old + __popc(peers));
     }
     old = __shfl_sync(kFull, old, leader);
     __syncwarp();   // the counter update is seen by the next item's leader
@@ -158,19 +199,34 @@ __device__ __forceinline__ void onesweep_tile(SortSmemT<K>& sm, const K* __restr
   }
   __syncthreads();
 
-  uint32_t cnt = 0;
-  if (tid < kRadix) {
-    for (int w = 0; w < kSortWarps; ++w) {
-      const uint32_t c = sm.whist[w][tid];
-      sm.whist[w][tid] = cnt;
-      cnt += c;
+  // per digit: warp offsets, the tile's count (published at once), the
+  // digit's first slot in the tile
+  const int d0 = tid * PER;
+  uint32_t cnt[PER], ds[PER];
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int d = d0 + q;
+    uint32_t c = 0;
+    if (d < R) {
+      for (int w = 0; w < kSortWarps; ++w) {
+        const uint32_t x = sm.whist[w][d];
+        sm.whist[w][d] = (Count)c;
+        c += x;
+      }
+      *(volatile uint32_t*)(lookback + (size_t)t * R + d) = (t == 0 ? kFlagInc : kFlagAgg) | c;
     }
-    *(volatile uint32_t*)(lookback + (size_t)t * kRadix + tid) = (t == 0 ? kFlagInc : kFlagAgg) | cnt;
+    cnt[q] = c;
+    ds[q] = c;
   }
-  const uint32_t ds = sort_scan256(cnt, sm.wsum);
-  if (tid < kRadix) {
-    sm.dstart[tid] = ds;
-    for (int w = 0; w < kSortWarps; ++w) sm.whist[w][tid] += ds;   // slot of each warp's first item of the digit
+  sort_scan_digits<R>(ds, sm.wsum);
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int d = d0 + q;
+    if (d < R) {
+      sm.dstart[d] = ds[q];
+      for (int w = 0; w < kSortWarps; ++w)   // slot of each warp's first item of the digit
+        sm.whist[w][d] = (Count)(sm.whist[w][d] + ds[q]);
+    }
   }
   __syncthreads();
   // the tile's items into shared memory in digit order; this frees their
@@ -179,12 +235,15 @@ __device__ __forceinline__ void onesweep_tile(SortSmemT<K>& sm, const K* __restr
   for (int i = 0; i < ITEMS; ++i) {
     if (FULL || w0 + i * 32 + lane < tile_n) {
       const uint32_t rank = (i & 1) ? r2[i >> 1] >> 16 : r2[i >> 1] & 0xffffu;
-      const uint32_t pos = sm.whist[warp][sort_digit(k[i], shift)] + rank;
+      const uint32_t pos = sm.whist[warp][sort_digit<K, BITS>(k[i], shift)] + rank;
       sm.keys[pos] = k[i];
       sm.vals[pos] = v[i];
     }
   }
-  if (tid < kRadix) {
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const int d = d0 + q;
+    if (d >= R) continue;
     uint32_t excl = 0;
     if (t > 0) {
       // Walk back kLookWin predecessors per round trip: their words are
@@ -198,23 +257,23 @@ __device__ __forceinline__ void onesweep_tile(SortSmemT<K>& sm, const K* __restr
       while (!done) {
         uint32_t w[kLookWin];
 #pragma unroll
-        for (int q = 0; q < kLookWin; ++q)
-          w[q] = j - q >= 0 ? *(volatile const uint32_t*)(lookback + (j - q) * kRadix + tid) : kFlagInc;
-        int q = 0;
+        for (int z = 0; z < kLookWin; ++z)
+          w[z] = j - z >= 0 ? *(volatile const uint32_t*)(lookback + (j - z) * R + d) : kFlagInc;
+        int z = 0;
 #pragma unroll
-        for (int qq = 0; qq < kLookWin; ++qq) {
-          if (q == qq) {
-            const uint32_t flag = w[qq] & ~kCountMask;
+        for (int zz = 0; zz < kLookWin; ++zz) {
+          if (z == zz) {
+            const uint32_t flag = w[zz] & ~kCountMask;
             if (flag != 0u) {
-              excl += w[qq] & kCountMask;
+              excl += w[zz] & kCountMask;
               if (flag == kFlagInc) done = true;
-              else ++q;
+              else ++z;
             }
           }
         }
         if (done) break;
-        j -= q;
-        if (q < kLookWin) {   // word j is not published yet
+        j -= z;
+        if (z < kLookWin) {   // word j is not published yet
           if (++spins > kSpinLimit) {
             latch(status, EMB_ERR_TIMEOUT);
             break;
@@ -222,15 +281,15 @@ __device__ __forceinline__ void onesweep_tile(SortSmemT<K>& sm, const K* __restr
           __nanosleep(32);
         }
       }
-      *(volatile uint32_t*)(lookback + (size_t)t * kRadix + tid) = kFlagInc | ((excl + cnt) & kCountMask);
+      *(volatile uint32_t*)(lookback + (size_t)t * R + d) = kFlagInc | ((excl + cnt[q]) & kCountMask);
     }
     // output position of shared slot j of this digit: goff + (j - dstart)
-    sm.goff[tid] = sm.hscan[tid] + excl - ds;
+    sm.goff[d] = sm.hscan[d] + excl - ds[q];
   }
   __syncthreads();
   for (int j = tid; j < (FULL ? TILE : tile_n); j += kSortThreads) {
     const K key = sm.keys[j];
-    const uint32_t o = sm.goff[sort_digit(key, shift)] + (uint32_t)j;
+    const uint32_t o = sm.goff[sort_digit<K, BITS>(key, shift)] + (uint32_t)j;
     if (o < n) {   // always true unless a look-back wait gave up
       kout[o] = key;
       vout[o] = sm.vals[j];
@@ -244,75 +303,103 @@ __device__ __forceinline__ void onesweep_tile(SortSmemT<K>& sm, const K* __restr
 // the capacity, and CTAs past the count cost one ticket each).  Either way a
 // tile only ever waits on tiles whose tickets were drawn earlier, by CTAs
 // already running.
-template <class K, bool PERSIST>
+template <class K, int BITS, bool PERSIST>
 __global__ void __launch_bounds__(kSortThreads, 2)
     k_onesweep_t(const K* __restrict__ kin, const uint32_t* __restrict__ vin, K* __restrict__ kout,
                  uint32_t* __restrict__ vout, int64_t n0, const uint32_t* n_dev, int shift,
                  const uint32_t* __restrict__ hist, uint32_t* lookback, uint32_t* tile_ctr, uint32_t* status) {
-  constexpr int TILE = SortSmemT<K>::kTile;
+  constexpr int R = 1 << BITS;
+  constexpr int PER = (R + kSortThreads - 1) / kSortThreads;
+  constexpr int TILE = sort_tile<K>();
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  SortSmemT<K>& sm = *reinterpret_cast<SortSmemT<K>*>(smem_raw);
+  SortSmemT<K, BITS>& sm = *reinterpret_cast<SortSmemT<K, BITS>*>(smem_raw);
   const int tid = threadIdx.x;
   const int64_t n = sort_count(n0, n_dev);
   const int64_t tiles = (n + TILE - 1) / TILE;
-  const uint32_t hs = sort_scan256(tid < kRadix ? __ldg(hist + tid) : 0u, sm.wsum);
-  if (tid < kRadix) sm.hscan[tid] = hs;
+  {
+    uint32_t hv[PER];
+#pragma unroll
+    for (int q = 0; q < PER; ++q) hv[q] = tid * PER + q < R ? __ldg(hist + tid * PER + q) : 0u;
+    sort_scan_digits<R>(hv, sm.wsum);
+#pragma unroll
+    for (int q = 0; q < PER; ++q)
+      if (tid * PER + q < R) sm.hscan[tid * PER + q] = hv[q];
+  }
   do {
     if (tid == 0) sm.tile = atomicAdd(tile_ctr, 1u);
-    for (int i = tid; i < kSortWarps * kRadix; i += kSortThreads) (&sm.whist[0][0])[i] = 0;
+    for (int i = tid; i < kSortWarps * R; i += kSortThreads) (&sm.whist[0][0])[i] = 0;
     __syncthreads();
     const uint32_t t = sm.tile;
     if ((int64_t)t >= tiles) return;   // past the data: nobody waits on this ticket
     const int64_t left = n - (int64_t)t * TILE;
-    onesweep_tile<K>(sm, kin, vin, kout, vout, (uint32_t)n, t, left >= TILE ? TILE : (int)left, shift, lookback,
-                     status);
+    onesweep_tile<K, BITS>(sm, kin, vin, kout, vout, (uint32_t)n, t, left >= TILE ? TILE : (int)left, shift,
+                           lookback, status);
     if (PERSIST) __syncthreads();   // the tile's shared memory is free again
   } while (PERSIST);
 }
 
-// Words of scratch the sort needs: hist [passes][256], tickets [passes],
-// look-back words [passes][tiles][256].
+// Words of scratch the sort of keys with key_bits bits needs for cap pairs:
+// hist [passes][R], tickets [passes], look-back words [passes][tiles][R].
 template <class K>
-inline size_t sort_scratch_words(int passes, int64_t cap) {
-  const int64_t tiles = (cap + SortSmemT<K>::kTile - 1) / SortSmemT<K>::kTile;
-  return (size_t)passes * kRadix + passes + (size_t)passes * tiles * kRadix;
+inline size_t sort_scratch_words(int key_bits, int64_t cap) {
+  int bits = 8, passes = 1;
+  sort_plan(key_bits, &bits, &passes);
+  const size_t R = (size_t)1 << bits;
+  const int64_t tiles = (cap + sort_tile<K>() - 1) / sort_tile<K>();
+  return (size_t)passes * R + passes + (size_t)passes * tiles * R;
 }
 
-// Sorts keys[0]/vals[0] (n pairs, or *n_dev of at most cap) into keys[p&1],
-// vals[p&1] with p = passes.  `scratch` holds sort_scratch_words() words and
-// is cleared here.  Returns the index of the buffer holding the result.
-template <class K>
-inline emb_status radix_sort_pairs(K* const keys[2], uint32_t* const vals[2], int64_t n, const uint32_t* n_dev,
-                                   int64_t cap, int passes, uint32_t* scratch, int sm_count, uint32_t* status,
-                                   cudaStream_t stream, int* result) {
-  *result = 0;
-  if (cap <= 0 || passes <= 0) return EMB_OK;
-  if (cap > (int64_t)kCountMask) return EMB_ERR_UNSUPPORTED;   // look-back words count in 30 bits
-  if (n_dev) n = cap;
-  const int64_t tiles = (cap + SortSmemT<K>::kTile - 1) / SortSmemT<K>::kTile;
+template <class K, int BITS>
+inline emb_status radix_sort_passes(K* const keys[2], uint32_t* const vals[2], int64_t n, const uint32_t* n_dev,
+                                    int64_t cap, int passes, uint32_t* scratch, int sm_count, uint32_t* status,
+                                    cudaStream_t stream) {
+  constexpr int R = 1 << BITS;
+  const int64_t tiles = (cap + sort_tile<K>() - 1) / sort_tile<K>();
   uint32_t* hist = scratch;
-  uint32_t* tickets = hist + (size_t)passes * kRadix;
+  uint32_t* tickets = hist + (size_t)passes * R;
   uint32_t* lookback = tickets + passes;
-  EMB_CUDA_TRY(cudaMemsetAsync(scratch, 0, sort_scratch_words<K>(passes, cap) * sizeof(uint32_t), stream));
   const int hgrid = (int)std::min<int64_t>((cap + 511) / 512, (int64_t)sm_count * 4);
-  k_digit_hist_t<K><<<hgrid, 512, 0, stream>>>(keys[0], n, n_dev, passes, hist);
+  k_digit_hist_t<K, BITS><<<hgrid, 512, 0, stream>>>(keys[0], n, n_dev, passes, hist);
   const bool persist = n_dev != nullptr;
   const int64_t grid = persist ? std::min<int64_t>(tiles, (int64_t)sm_count * 2) : tiles;   // two CTAs fit an SM
-  EMB_CUDA_TRY(cudaFuncSetAttribute(k_onesweep_t<K, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)sizeof(SortSmemT<K>)));
-  EMB_CUDA_TRY(cudaFuncSetAttribute(k_onesweep_t<K, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)sizeof(SortSmemT<K>)));
+  const int smem = (int)sizeof(SortSmemT<K, BITS>);
+  EMB_CUDA_TRY(cudaFuncSetAttribute(k_onesweep_t<K, BITS, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    smem));
+  EMB_CUDA_TRY(cudaFuncSetAttribute(k_onesweep_t<K, BITS, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    smem));
   for (int ps = 0; ps < passes; ++ps) {
     const int in = ps & 1, out = in ^ 1;
     if (persist)
-      k_onesweep_t<K, true><<<(unsigned)grid, kSortThreads, sizeof(SortSmemT<K>), stream>>>(
-          keys[in], vals[in], keys[out], vals[out], n, n_dev, ps * kRadixBits, hist + ps * kRadix,
-          lookback + (size_t)ps * tiles * kRadix, tickets + ps, status);
+      k_onesweep_t<K, BITS, true><<<(unsigned)grid, kSortThreads, smem, stream>>>(
+          keys[in], vals[in], keys[out], vals[out], n, n_dev, ps * BITS, hist + ps * R,
+          lookback + (size_t)ps * tiles * R, tickets + ps, status);
     else
-      k_onesweep_t<K, false><<<(unsigned)grid, kSortThreads, sizeof(SortSmemT<K>), stream>>>(
-          keys[in], vals[in], keys[out], vals[out], n, n_dev, ps * kRadixBits, hist + ps * kRadix,
-          lookback + (size_t)ps * tiles * kRadix, tickets + ps, status);
+      k_onesweep_t<K, BITS, false><<<(unsigned)grid, kSortThreads, smem, stream>>>(
+          keys[in], vals[in], keys[out], vals[out], n, n_dev, ps * BITS, hist + ps * R,
+          lookback + (size_t)ps * tiles * R, tickets + ps, status);
   }
+  return EMB_OK;
+}
+
+// Sorts keys[0]/vals[0] (n pairs, or *n_dev of at most cap) by their low
+// key_bits bits into keys[p&1], vals[p&1] with p = the number of passes.
+// `scratch` holds sort_scratch_words<K>(key_bits, cap) words and is cleared
+// here.  Returns the index of the buffer holding the result.
+template <class K>
+inline emb_status radix_sort_pairs(K* const keys[2], uint32_t* const vals[2], int64_t n, const uint32_t* n_dev,
+                                   int64_t cap, int key_bits, uint32_t* scratch, int sm_count, uint32_t* status,
+                                   cudaStream_t stream, int* result) {
+  *result = 0;
+  if (cap <= 0 || key_bits <= 0) return EMB_OK;
+  if (cap > (int64_t)kCountMask) return EMB_ERR_UNSUPPORTED;   // look-back words count in 30 bits
+  if (n_dev) n = cap;
+  int bits = 8, passes = 1;
+  sort_plan(key_bits, &bits, &passes);
+  if (passes > kMaxSortPasses) return EMB_ERR_UNSUPPORTED;
+  EMB_CUDA_TRY(cudaMemsetAsync(scratch, 0, sort_scratch_words<K>(key_bits, cap) * sizeof(uint32_t), stream));
+  const emb_status st =
+      radix_sort_passes<K, 8>(keys, vals, n, n_dev, cap, passes, scratch, sm_count, status, stream);
+  if (st != EMB_OK) return st;
   *result = passes & 1;
   return cuda_status(cudaGetLastError());
 }
