@@ -584,6 +584,28 @@ def bench_plan(torch, sl, w, args, dev, stream, flush, train):
     et, _ = timed_steps(torch, args.steps, stream, flush, e2e_body)
     res["e2e"] = {"value": rows_per_step / (statistics.mean(et["e2e"]) / 1e3), "unit": "rows/s",
                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    if args.graph:
+        # one whole step captured in a CUDA graph and replayed back to back:
+        # the step without per-launch host cost (L2 not flushed between replays)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            plan.forward(w.B, ids, id_off, fv, f_off, out=out, seq_out=seq)
+            if train:
+                plan.backward_update(G, Gseq, w.lr, w.eps)
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = event_pair(torch)
+        a.record(stream)
+        for _ in range(args.graph):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / args.graph
+        res["config"]["graph"] = {"replays": args.graph, "us_per_step": us,
+                                  "rows_per_s": rows_per_step / (us * 1e-6),
+                                  "l2": "not flushed between replays"}
+        if plan.device_status() != 0:
+            raise SystemExit("device status after the graph replays")
     res["ceiling"] = gather_ceiling(torch, sl, row_sizes_mix(w, valid), dev) if not args.no_ceiling else None
     if not args.no_cpu_baseline and dist_env()[0] == 0:
         if train:
@@ -727,6 +749,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ceiling", action="store_true")
     ap.add_argument("--columns", type=int, default=None, help="number of columns (smaller profiling cases)")
+    ap.add_argument("--graph", type=int, default=0,
+                    help="also time this many back-to-back replays of one step captured in a CUDA graph")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
