@@ -120,6 +120,24 @@ def dist_env():
     return rank, world, local
 
 
+def sync_ranks(torch):
+    """Barrier across the replicas (nothing to do for one process)."""
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def aggregate_ranks(torch, ms_step, rows_per_step, device):
+    """Whole-job throughput of N replicas: every rank's rows over the slowest
+    rank's step time.  Returns (max ms per step, rows per second)."""
+    world = 1
+    t = torch.tensor([float(ms_step)], dtype=torch.float64, device=device)
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        world = torch.distributed.get_world_size()
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms = float(t.item())
+    return ms, rows_per_step * world / (ms / 1e3)
+
+
 def make_workload(name, columns=None):
     if name == "inference":
         if columns:
@@ -176,6 +194,7 @@ def timed_steps(torch, steps, stream, flush, body):
     outside the events.  Returns per-part lists of milliseconds and the wall
     time of the loop."""
     recs = []
+    sync_ranks(torch)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(steps):
@@ -184,6 +203,7 @@ def timed_steps(torch, steps, stream, flush, body):
         body(i, marks)
         recs.append(marks)
     torch.cuda.synchronize()
+    sync_ranks(torch)
     wall = time.perf_counter() - t0
     out = {}
     for marks in recs:
@@ -419,13 +439,9 @@ def run_ours(args):
         res = bench_plan(torch, sl, w, args, dev, stream, flush, train=args.workload in TRAIN_WORKLOADS)
 
     clocks = res.pop("clocks")
-    ms_step = res["ms_step"]
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step, value = aggregate_ranks(torch, res["ms_step"], res["rows_per_step"], dev)
+    _, res["e2e"]["value"] = aggregate_ranks(torch, res["e2e_ms"], res["rows_per_step"], dev)
     peak, peak_kind = peaks()
-    value = res["rows_per_step"] * world / (ms_step / 1e3)
     fw_ms = statistics.mean(res["times"]["fwd"])
     achieved = res["fbytes"] / (fw_ms / 1e3) / 1e9
     line = {
@@ -582,7 +598,8 @@ def bench_plan(torch, sl, w, args, dev, stream, flush, train):
     for _ in range(3):
         e2e_body(0, {})
     et, _ = timed_steps(torch, args.steps, stream, flush, e2e_body)
-    res["e2e"] = {"value": rows_per_step / (statistics.mean(et["e2e"]) / 1e3), "unit": "rows/s",
+    res["e2e_ms"] = statistics.mean(et["e2e"])
+    res["e2e"] = {"value": rows_per_step / (res["e2e_ms"] / 1e3), "unit": "rows/s",
                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     if args.graph:
         # one whole step captured in a CUDA graph and replayed back to back:
@@ -730,7 +747,8 @@ def bench_dynamic(torch, sl, w, args, dev, stream, flush):
         state["t"] = t + 1
 
     et, _ = timed_steps(torch, min(args.steps, 5), stream, flush, e2e_body)
-    res["e2e"] = {"value": valid / (statistics.mean(et["e2e"]) / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+    res["e2e_ms"] = statistics.mean(et["e2e"])
+    res["e2e"] = {"value": valid / (res["e2e_ms"] / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
                   "d2h_bytes_per_step": out_p.numel() * 4}
     res["ceiling"] = gather_ceiling(torch, sl, {dim * 4: valid}, dev) if not args.no_ceiling else None
     if not args.no_cpu_baseline and dist_env()[0] == 0:
