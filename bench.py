@@ -223,6 +223,28 @@ def row_sizes_mix(w, valid_per_col):
     return mix
 
 
+def calibrate_gather_rate(sl, dim, table_bytes=8 << 30, n=1 << 25, reps=5, seed=0):
+    """GB/s of random row gathers of `dim` floats over a table of table_bytes
+    (larger than L2), timed with CUDA events on the current stream."""
+    import torch
+    rows = max(1, table_bytes // (dim * 4))
+    table = torch.zeros((rows, dim), dtype=torch.float32, device="cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    idx = torch.randint(0, rows, (n,), generator=g, device="cuda", dtype=torch.int64).to(torch.int32)
+    sink = torch.zeros(1, device="cuda")
+    sl.emb_calibrate_gather(table, rows, dim, idx, n, sink)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        sl.emb_calibrate_gather(table, rows, dim, idx, n, sink)
+    b.record()
+    b.synchronize()
+    ms = a.elapsed_time(b) / reps
+    del table, idx
+    return n * dim * 4 / (ms / 1e3) / 1e9
+
+
 def gather_ceiling(torch, sl, mix, dev, budget_bytes=8 << 30):
     """Random-row gather rate of this GPU for the workload's row sizes: one
     gather-only pass per row size over a table larger than L2 (the library's
@@ -233,7 +255,7 @@ def gather_ceiling(torch, sl, mix, dev, budget_bytes=8 << 30):
         return None
     t_sum = 0.0
     for nbytes, rows in sorted(mix.items()):
-        gbs = sl.calibrate_gather_rate(nbytes // 4, table_bytes=min(budget_bytes, 8 << 30))
+        gbs = calibrate_gather_rate(sl, nbytes // 4, table_bytes=min(budget_bytes, 8 << 30))
         out[str(nbytes)] = round(gbs, 1)
         t_sum += rows * nbytes / (gbs * 1e9)
     bytes_total = sum(r * b for b, r in mix.items())

@@ -228,28 +228,6 @@ def emb_calibrate_gather(table, num_rows, dim, row_idx, n, sink, stream=None):
            "emb_calibrate_gather")
 
 
-def calibrate_gather_rate(dim, table_bytes=8 << 30, n=1 << 25, reps=5, seed=0):
-    """GB/s of random row gathers of `dim` floats over a table of table_bytes
-    (larger than L2), timed with CUDA events on the current stream."""
-    import torch
-    rows = max(1, table_bytes // (dim * 4))
-    table = torch.zeros((rows, dim), dtype=torch.float32, device="cuda")
-    g = torch.Generator(device="cuda")
-    g.manual_seed(seed)
-    idx = torch.randint(0, rows, (n,), generator=g, device="cuda", dtype=torch.int64).to(torch.int32)
-    sink = torch.zeros(1, device="cuda")
-    emb_calibrate_gather(table, rows, dim, idx, n, sink)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(reps):
-        emb_calibrate_gather(table, rows, dim, idx, n, sink)
-    b.record()
-    b.synchronize()
-    ms = a.elapsed_time(b) / reps
-    del table, idx
-    return n * dim * 4 / (ms / 1e3) / 1e9
-
-
 def emb_selftest_hash_mod(ids, num_rows):
     import numpy as np
     ids = np.ascontiguousarray(ids, np.int64)

@@ -8,24 +8,21 @@
 
 namespace emb {
 
-// Forward tiles cover this many stream elements at most (bags are owned by the
-// tile that holds their first element).
-#ifndef EMB_FWD_THREADS
-#define EMB_FWD_THREADS 256
-#endif
-constexpr int kFwdThreads = EMB_FWD_THREADS;
-constexpr int kFwdWarps = kFwdThreads / kWarp;
-constexpr int kLongBag = 128;         // longer bags are pooled by a whole CTA
+// Forward: threads per CTA (each warp works alone on its tiles); bags longer
+// than kLongBag values are pooled by the whole warp; a tile covers at most
+// kMaxTileElems stream elements (bags are owned by the tile that holds their
+// first element).
+constexpr int kFwdThreads = 256;
+constexpr int kLongBag = 128;
 constexpr int kMaxTileElems = 8192;
-constexpr int kMaxLongPerTile = kMaxTileElems / kLongBag + 2;
 
-// Backward: contributions are processed in units of this many sorted entries
-// by one lane group; runs cut by a unit boundary are finished by a fixup pass.
+// Backward: the run-reduction CTAs take at least this many sorted entries
+// each; the per-CTA partial buffers are sized for n / kUnit CTAs.
 constexpr int kUnit = 128;
 constexpr uint32_t kPadBit = 0x80000000u;
 
-// Radix sort geometry (LSD, 8- or 10-bit digits, chained scan with decoupled
-// look-back): threads per CTA and 32-bit pairs per thread of a tile.
+// Radix sort geometry (LSD, chained scan with decoupled look-back): threads
+// per CTA and 32-bit pairs per thread of a tile.
 constexpr int kSortThreads = 512;
 constexpr int kSortItems = 15;
 constexpr int kSortTile = kSortThreads * kSortItems;
