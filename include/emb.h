@@ -89,7 +89,11 @@ typedef struct {
     const float* boundaries;  /* EMB_T_BUCKETIZE: [num_boundaries] fp32, strictly
                                  increasing, 1 <= num_boundaries <= 4096         */
     int32_t num_boundaries;
-    int32_t reserved;         /* must be 0                                       */
+    int32_t max_len;          /* EMB_POOL_SUM / MEAN: pool only the first max_len
+                                 values of each bag, the rest read nothing and get
+                                 no gradient (sequence truncation, RecIS §2.1);
+                                 0 = all.  Must be 0 for EMB_POOL_NONE_PADDED
+                                 (pad_len cuts there).                          */
     float* weight;            /* [num_rows, dim] fp32 row-major, 16-byte aligned.
                                  Columns given the SAME pointer share one table
                                  (same num_rows and dim required); the backward

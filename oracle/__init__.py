@@ -38,6 +38,8 @@ class _Col(ctypes.Structure):
         ("pad_len", c_int32),
         ("default_vec", c_void_p),
         ("out_col", c_int64),
+        ("max_len", c_int32),
+        ("reserved", c_int32),
     ]
 
 
@@ -118,6 +120,7 @@ def _cols(cols):
         arr[i].pad_len = int(getattr(c, "pad_len", 0) or 0)
         arr[i].default_vec = None if dft is None else dft.ctypes.data
         arr[i].out_col = off if c.pooling != "padded" else 0
+        arr[i].max_len = int(getattr(c, "max_len", 0) or 0)
         if c.pooling != "padded":
             off += int(c.dim)
     return arr, keep, off
@@ -260,9 +263,10 @@ def unique_counts(cols, B, offsets, values):
         rows = column_rows(c, v)
         o = np.asarray(o, np.int64)
         valid = rows >= 0
-        if c.pooling == "padded":
+        cut = c.pad_len if c.pooling == "padded" else int(getattr(c, "max_len", 0) or 0)
+        if cut > 0:
             bag = np.repeat(np.arange(B), np.diff(o))
-            valid &= (np.arange(rows.size) - o[bag]) < c.pad_len
+            valid &= (np.arange(rows.size) - o[bag]) < cut
         keys.append(np.int64(c.table) * (np.int64(1) << 40) + rows[valid])
     allk = np.concatenate(keys) if keys else np.zeros(0, np.int64)
     u, cnt = np.unique(allk, return_counts=True)

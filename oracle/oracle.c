@@ -45,7 +45,9 @@
  *    keys are ordered by (table id, key) ascending and take the lowest free
  *    rows: the free list in ascending order first, then a bump pointer;
  *  - expiry: an entry (admitted or still counting) is removed when
- *    now - last_seen > ttl; its row returns to the free list.
+ *    now - last_seen > ttl; its row returns to the free list;
+ *  - sequence truncation: a SUM / MEAN column with max_len > 0 uses only the
+ *    first max_len values of each bag (dropped IDs among them stay dropped).
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -71,7 +73,20 @@ typedef struct {
     const float* default_vec; /* [dim] or NULL => zeros                       */
     int64_t out_col;          /* pooled: float offset of the column in a row of
                                  the concatenated output                      */
+    int32_t max_len;          /* SUM / MEAN: a bag is its first max_len values
+                                 (sequence truncation; 0 = all)               */
+    int32_t reserved;
 } orc_col;
+
+/* End of the values of bag [lo, hi) that the column uses: PADDED keeps the
+ * first pad_len, a truncated pooled column the first max_len [RecIS §2.1,
+ * SeqTrunc: a long sequence feature keeps its first elements]. */
+static int64_t bag_end(const orc_col* c, int64_t lo, int64_t hi)
+{
+    if (c->pooling == ORC_PADDED && hi - lo > c->pad_len) return lo + c->pad_len;
+    if (c->pooling != ORC_PADDED && c->max_len > 0 && hi - lo > c->max_len) return lo + c->max_len;
+    return hi;
+}
 
 /* ------------------------------------------------------------------------ */
 /* a1: feature transform                                                     */
@@ -179,6 +194,7 @@ int orc_forward(const orc_col* cols, int32_t C, int32_t B,
                 }
                 continue;
             }
+            hi = bag_end(c, lo, hi);
             int64_t nv = 0;
             for (int32_t d = 0; d < c->dim; ++d) S[d] = 0.0;
             for (int64_t t = lo; t < hi; ++t) {
@@ -277,7 +293,7 @@ int orc_backward_adagrad(const orc_col* cols, int32_t C, int32_t B,
         orc_column_rows(c, nvals, ids ? ids[ci] : NULL, fvals ? fvals[ci] : NULL, rows);
         for (int32_t b = 0; b < B; ++b) {
             int64_t lo = off[b], hi = off[b + 1];
-            if (c->pooling == ORC_PADDED && hi - lo > c->pad_len) hi = lo + c->pad_len;
+            hi = bag_end(c, lo, hi);
             int64_t nv = 0;
             for (int64_t t = lo; t < hi; ++t) nv += rows[t] >= 0;
             for (int64_t t = lo; t < hi; ++t) {
@@ -387,7 +403,7 @@ int orc_backward_rows(const orc_col* cols, int32_t C, int32_t B,
         orc_column_rows(c, nvals, ids ? ids[ci] : NULL, fvals ? fvals[ci] : NULL, rows);
         for (int32_t b = 0; b < B; ++b) {
             int64_t lo = off[b], hi = off[b + 1];
-            if (c->pooling == ORC_PADDED && hi - lo > c->pad_len) hi = lo + c->pad_len;
+            hi = bag_end(c, lo, hi);
             int64_t nv = 0;
             for (int64_t t = lo; t < hi; ++t) nv += rows[t] >= 0;
             for (int64_t t = lo; t < hi; ++t) {

@@ -45,7 +45,7 @@ class EmbColumnDesc(ctypes.Structure):
         ("pad_len", c_int32),
         ("boundaries", c_void_p),
         ("num_boundaries", c_int32),
-        ("reserved", c_int32),
+        ("max_len", c_int32),
         ("weight", c_void_p),
         ("adagrad_acc", c_void_p),
         ("default_vec", c_void_p),
@@ -264,6 +264,7 @@ class Plan:
             d.num_rows = int(c.num_rows)
             d.dim = int(c.dim)
             d.pad_len = int(getattr(c, "pad_len", 0) or 0)
+            d.max_len = int(getattr(c, "max_len", 0) or 0) if c.pooling != "padded" else 0
             if getattr(c, "boundaries", None) is not None:
                 b = torch.as_tensor(c.boundaries, dtype=torch.float32).to(device).contiguous()
                 self._keep.append(b)

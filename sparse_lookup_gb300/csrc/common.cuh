@@ -120,6 +120,7 @@ struct ColMeta {
   int32_t transform;
   int32_t pooling;
   int32_t pad_len;
+  int32_t trunc;           // pooled: only the first trunc values of a bag (0 = all)
   int32_t table;
   uint32_t table_base;     // first global row of the column's table
   int32_t out_col;         // pooled: float offset inside an output row

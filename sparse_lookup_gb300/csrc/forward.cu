@@ -579,6 +579,7 @@ __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int
       hi = clamp_off(__ldg(offs + cur + lane + 1), n, bad);
       if (hi < lo) { hi = lo; bad = true; }
       if (bad) latch(a.status, EMB_ERR_BAD_INDEX);
+      if (m.trunc > 0 && hi - lo > m.trunc) hi = lo + m.trunc;   // sequence truncation (pooled only)
       const int64_t len = hi - lo;
       is_long = (padded ? (int64_t)m.pad_len : len) > kLongBag;
       used = is_long ? 0 : (int)(padded ? (len < m.pad_len ? len : (int64_t)m.pad_len) : len);
@@ -667,6 +668,22 @@ __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int
     }
     if (padded && (a.rows_dbg || a.keys) && lane < ns && !is_long)
       for (int64_t t = lo + m.pad_len; t < hi; ++t) record_cut(a, st, t, m);
+    if (m.trunc > 0 && (a.rows_dbg || a.keys)) {
+      // values past a truncated bag's first trunc: no output, no gradient; the
+      // whole warp writes their records, one cut bag at a time
+      bool cutb = false;
+      if (lane < ns) {
+        bool bad = false;
+        cutb = clamp_off(__ldg(offs + cur + lane + 1), n, bad) > hi;
+      }
+      for (unsigned cm = __ballot_sync(kFull, cutb); cm; cm &= cm - 1) {
+        const int i = __ffs(cm) - 1;
+        const int64_t t0 = __shfl_sync(kFull, hi, i);
+        bool bad = false;
+        const int64_t t1 = clamp_off(__ldg(offs + cur + i + 1), n, bad);
+        for (int64_t t = t0 + lane; t < t1; t += 32) record_cut(a, st, t, m);
+      }
+    }
     __syncwarp();
 
     // ---- phase B: pool / copy ----

@@ -52,7 +52,7 @@ emb_status validate_column(const emb_column_desc& c, bool training) {
   if (c.num_rows >= (int64_t(1) << 31)) return EMB_ERR_UNSUPPORTED;
   if (c.dim < 4 || c.dim % 4 != 0) return EMB_ERR_INVALID_ARG;
   if (c.dim > 256) return EMB_ERR_UNSUPPORTED;
-  if (c.reserved != 0) return EMB_ERR_INVALID_ARG;
+  if (c.max_len < 0 || (c.pooling == EMB_POOL_NONE_PADDED && c.max_len != 0)) return EMB_ERR_INVALID_ARG;
   if (!c.weight || !aligned16(c.weight)) return EMB_ERR_INVALID_ARG;
   if (c.pooling == EMB_POOL_NONE_PADDED && c.pad_len < 1) return EMB_ERR_INVALID_ARG;
   if (c.transform == EMB_T_BUCKETIZE) {
@@ -148,6 +148,7 @@ extern "C" emb_status emb_plan_create(const emb_column_desc* cols, int32_t n_col
     m.transform = d.transform;
     m.pooling = d.pooling;
     m.pad_len = d.pooling == EMB_POOL_NONE_PADDED ? d.pad_len : 0;
+    m.trunc = d.pooling == EMB_POOL_NONE_PADDED ? 0 : d.max_len;
     m.table = p->col_table[c];
     m.table_base = p->table_base_h[m.table];
     m.col = c;

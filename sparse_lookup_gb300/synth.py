@@ -42,6 +42,7 @@ class ColumnSpec:
     boundaries: np.ndarray | None = None
     default: np.ndarray | None = None
     pad_len: int = 0
+    max_len: int = 0               # sum / mean: pool only a bag's first max_len values (0 = all)
 
 
 @dataclass
@@ -271,11 +272,13 @@ def dynamic(seed: int = 1005, C: int = 100, B: int = 16384, dim: int = 32, steps
 
 def random_small(seed: int, C: int | None = None, B: int | None = None, train: bool = True,
                  dims=(4, 8, 12, 16, 32, 64, 128), allow_padded: bool = True,
-                 shared_tables: bool = True) -> Workload:
+                 shared_tables: bool = True, allow_trunc: bool = True) -> Workload:
     """Small mixed plans for parity tests: every transform and pooling, dims
     that are not powers of two, empty bags, long bags, out-of-range and
-    extreme int64 IDs, NaN/inf feature values, defaults, shared tables."""
+    extreme int64 IDs, NaN/inf feature values, defaults, shared tables,
+    truncated bags."""
     r = np.random.default_rng([seed, 7])
+    rt = np.random.default_rng([seed, 8])   # sequence truncation, drawn apart from the rest
     C = int(r.integers(1, 12)) if C is None else C
     B = int(r.integers(1, 70)) if B is None else B
     cols, tabs, offs, vals = [], [], [], []
@@ -318,8 +321,9 @@ def random_small(seed: int, C: int | None = None, B: int | None = None, train: b
                     v = r.integers(-5, rows + 5, n, dtype=np.int64)
         default = r.standard_normal(dim).astype(np.float32) if r.random() < 0.3 else None
         pad = int(r.integers(1, 50)) if pooling == "padded" else 0
+        trunc = int(rt.integers(1, 25)) if allow_trunc and pooling != "padded" and rt.random() < 0.3 else 0
         cols.append(ColumnSpec(str(kind), pooling, rows, dim, table, boundaries=bnd,
-                               default=default, pad_len=pad))
+                               default=default, pad_len=pad, max_len=trunc))
         if table == c:
             tabs.append(TableSpec(rows, dim, seed * 1000 + c))
         else:

@@ -8,7 +8,8 @@ from sparse_lookup_gb300 import build as slbuild
 from sparse_lookup_gb300 import synth
 from sparse_lookup_gb300.synth import ColumnSpec, TableSpec, Workload
 
-from helpers import TrainStep, check_train_step
+import oracle
+from helpers import TrainStep, assert_close, check_train_step
 
 pytestmark = pytest.mark.gpu
 
@@ -55,6 +56,21 @@ def test_padded_and_mean_sequences_small():
     check_train_step(TrainStep(w))
     w = synth.sequences(seed=6, mode="mean", C=3, B=40, rows=3000, dim=128, len_lo=50, len_hi=300)
     check_train_step(TrainStep(w))
+
+
+def test_truncated_sequences():
+    """Sequence truncation: long bags cut to their first 150 values (still
+    pooled by the whole warp) and to their first 40 (short-bag path), sum and
+    mean, forward + backward against the oracle; the cut values get no
+    gradient."""
+    from dataclasses import replace
+    for mode, cut in (("mean", 150), ("mean", 40)):
+        w = synth.sequences(seed=7, mode=mode, C=3, B=40, rows=3000, dim=128, len_lo=50, len_hi=400)
+        w.columns = [replace(c, max_len=cut, pooling=p) for c, p in zip(w.columns, ("mean", "sum", "mean"))]
+        ts = TrainStep(w)
+        check_train_step(ts)
+        ref, _, rows = oracle.forward(w.columns, w.B, w.offsets, w.values, ts.W0, want_rows=True)
+        assert_close(ts.out.cpu().numpy(), ref, "pooled, max_len %d" % cut)
 
 
 def test_shared_table_columns_merge():

@@ -122,7 +122,7 @@ def test_forward_matches_embedding_bag_in_fp64():
     torch = pytest.importorskip("torch")
     F = torch.nn.functional
     for seed in range(6):
-        w = synth.random_small(seed, allow_padded=False)
+        w = synth.random_small(seed, allow_padded=False, allow_trunc=False)
         tabs = _tables(w)
         out, _, rows = oracle.forward(w.columns, w.B, w.offsets, w.values, tabs, want_rows=True)
         col0 = 0
@@ -212,7 +212,7 @@ def test_backward_matches_embedding_bag_autograd():
     torch = pytest.importorskip("torch")
     F = torch.nn.functional
     for seed in range(5):
-        w = synth.random_small(seed + 10, allow_padded=False, shared_tables=False)
+        w = synth.random_small(seed + 10, allow_padded=False, shared_tables=False, allow_trunc=False)
         tabs = _tables(w)
         width = sum(c.dim for c in w.columns)
         G = synth.make_grad((w.B, width), seed).numpy()
@@ -244,7 +244,7 @@ def test_backward_matches_embedding_bag_autograd():
 def test_backward_gradient_sum_invariant():
     """Sum over unique rows of the aggregated gradient = sum over valid
     contributions of scale * G[bag] (per column and element, fp64)."""
-    w = synth.random_small(77, C=4, B=50, allow_padded=False, shared_tables=False)
+    w = synth.random_small(77, C=4, B=50, allow_padded=False, shared_tables=False, allow_trunc=False)
     tabs = _tables(w)
     width = sum(c.dim for c in w.columns)
     G = synth.make_grad((w.B, width), 5).numpy().astype(np.float64)
@@ -529,3 +529,65 @@ def test_unique_counts_equals_the_backward_listing():
         assert np.array_equal(got["table"], ref["table"].astype(np.int64)), seed
         assert np.array_equal(got["row"], ref["row"]), seed
         assert np.array_equal(got["count"], ref["count"]), seed
+
+
+def test_truncation_hand_example():
+    """SUM with max_len 2 on bag [1, 2, 3, 99] pools rows 1 and 2; MEAN with
+    max_len 3 on [1, 99, 3, 2] averages rows 1 and 3 (99 is dropped inside the
+    kept prefix, 2 lies past it); only the kept values receive gradient."""
+    E = np.arange(40, dtype=np.float32).reshape(10, 4)
+    off = np.array([0, 4], np.int32)
+    cs = ColumnSpec("identity", "sum", 10, 4, 0, max_len=2)
+    out, _ = oracle.forward([cs], 1, [off], [np.array([1, 2, 3, 99], np.int64)], [E])
+    assert np.array_equal(out[0], E[1] + E[2])
+    cm = ColumnSpec("identity", "mean", 10, 4, 0, max_len=3)
+    out, _ = oracle.forward([cm], 1, [off], [np.array([1, 99, 3, 2], np.int64)], [E])
+    assert np.array_equal(out[0], (E[1] + E[3]) / 2)
+    G = np.ones((1, 4), np.float32)
+    res = oracle.backward_adagrad([cm], 1, [off], [np.array([1, 99, 3, 2], np.int64)], G, None,
+                                  [E.copy()], [np.zeros_like(E)], 0.1, 1e-10)
+    assert res["row"].tolist() == [1, 3] and res["count"].tolist() == [1, 1]
+    np.testing.assert_allclose(res["grad"][0], [0.5] * 4)
+
+
+def test_truncation_equals_cut_inputs():
+    """A truncated column gives the forward, backward and unique counts of the
+    same column fed only each bag's first max_len values (the plain
+    definition, by numpy slicing)."""
+    from dataclasses import replace
+    for seed in range(12):
+        w = synth.random_small(300 + seed, allow_padded=False)
+        if not any(c.max_len for c in w.columns):
+            continue
+        cut_cols, cut_offs, cut_vals = [], [], []
+        for c, o, v in zip(w.columns, w.offsets, w.values):
+            if c.max_len:
+                lens = np.minimum(np.diff(o), c.max_len)
+                keep = np.concatenate([np.arange(o[b], o[b] + lens[b]) for b in range(w.B)] or
+                                      [np.zeros(0, np.int64)]).astype(np.int64)
+                cut_offs.append(synth.bag_offsets(lens))
+                cut_vals.append(v[keep])
+                cut_cols.append(replace(c, max_len=0))
+            else:
+                cut_offs.append(o)
+                cut_vals.append(v)
+                cut_cols.append(c)
+        tabs = _tables(w)
+        a, _ = oracle.forward(w.columns, w.B, w.offsets, w.values, tabs)
+        b, _ = oracle.forward(cut_cols, w.B, cut_offs, cut_vals, tabs)
+        assert np.array_equal(a, b), seed
+        ua = oracle.unique_counts(w.columns, w.B, w.offsets, w.values)
+        ub = oracle.unique_counts(cut_cols, w.B, cut_offs, cut_vals)
+        for k in ("table", "row", "count"):
+            assert np.array_equal(ua[k], ub[k]), (seed, k)
+        width = sum(c.dim for c in w.columns)
+        G = synth.make_grad((w.B, max(width, 1)), seed).numpy()[:, :width]
+        dummy = np.zeros((1, 1), np.float32)   # placeholders keep the list indexed by table
+        Wa = [x.copy() if x is not None else dummy.copy() for x in tabs]
+        Wb = [x.copy() if x is not None else dummy.copy() for x in tabs]
+        Aa = [np.zeros_like(x) for x in Wa]
+        Ab = [np.zeros_like(x) for x in Wb]
+        oracle.backward_adagrad(w.columns, w.B, w.offsets, w.values, G, None, Wa, Aa, w.lr, w.eps)
+        oracle.backward_adagrad(cut_cols, w.B, cut_offs, cut_vals, G, None, Wb, Ab, w.lr, w.eps)
+        for x, y in zip(Wa + Aa, Wb + Ab):
+            assert np.array_equal(x, y), seed
