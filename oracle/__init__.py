@@ -40,6 +40,7 @@ class _Col(ctypes.Structure):
         ("out_col", c_int64),
         ("max_len", c_int32),
         ("reserved", c_int32),
+        ("weights", c_void_p),
     ]
 
 
@@ -100,13 +101,17 @@ def _ptr_array(arrs):
     return arr
 
 
-def _cols(cols):
-    """ctypes column array; pooled columns get consecutive out_col offsets.
+def _cols(cols, weights=None):
+    """ctypes column array; pooled columns get consecutive out_col offsets;
+    weights: optional per-column fp32 value weights (None entries: none).
     Returns (array, keep-alive list, pooled width)."""
     arr = (_Col * max(1, len(cols)))()
     keep = []
     off = 0
     for i, c in enumerate(cols):
+        wts = None if weights is None or weights[i] is None else np.ascontiguousarray(weights[i], np.float32)
+        keep.append(wts)
+        arr[i].weights = None if wts is None else wts.ctypes.data
         bnd = None if getattr(c, "boundaries", None) is None else np.ascontiguousarray(c.boundaries, np.float32)
         dft = None if getattr(c, "default", None) is None else np.ascontiguousarray(c.default, np.float32)
         keep += [bnd, dft]
@@ -156,11 +161,12 @@ def column_rows(col, values) -> np.ndarray:
     return out[:n]
 
 
-def forward(cols, B, offsets, values, tables, want_rows=False):
+def forward(cols, B, offsets, values, tables, want_rows=False, weights=None):
     """Pooled output [B, sum(dim of pooled cols)] (fp32), padded outputs
     (list, None for pooled columns) and optionally the rows per column.
+    weights: optional per-column value weights, used by SUM columns.
     RecIS §3.2 Algorithm 1 (forward); RECom guards and default fill."""
-    arr, keep, width = _cols(cols)
+    arr, keep, width = _cols(cols, weights)
     C = len(cols)
     offs = [np.ascontiguousarray(o, np.int32) for o in offsets]
     ids, fv = _values(cols, values)
@@ -180,13 +186,14 @@ def forward(cols, B, offsets, values, tables, want_rows=False):
     return out, seq
 
 
-def backward_adagrad(cols, B, offsets, values, G, Gseq, W, acc, lr, eps):
+def backward_adagrad(cols, B, offsets, values, G, Gseq, W, acc, lr, eps, weights=None):
     """Backward + sparse Adagrad (RecIS §3.2 Algorithm 1 backward semantics,
     Figure 3 local reduce-ID; Adagrad as in torch.optim.Adagrad).
     W, acc: lists of float32 host tables per physical table, updated in place.
     Returns dict(table, row, count, grad) over unique rows, ascending by
-    (table, row); grad is a list of float32 [dim] arrays."""
-    arr, keep, width = _cols(cols)
+    (table, row); grad is a list of float32 [dim] arrays.  weights: optional
+    per-column value weights (SUM columns pass w_r G to their rows)."""
+    arr, keep, width = _cols(cols, weights)
     C = len(cols)
     offs = [np.ascontiguousarray(o, np.int32) for o in offsets]
     ids, fv = _values(cols, values)
@@ -220,7 +227,7 @@ def backward_adagrad(cols, B, offsets, values, G, Gseq, W, acc, lr, eps):
     return dict(table=u_table[:n].copy(), row=u_row[:n].copy(), count=u_count[:n].copy(), grad=grads)
 
 
-def backward_rows(cols, B, offsets, values, G, Gseq, targets, W_rows, acc_rows, lr, eps):
+def backward_rows(cols, B, offsets, values, G, Gseq, targets, W_rows, acc_rows, lr, eps, weights=None):
     """The backward + Adagrad of backward_adagrad restricted to chosen rows,
     for tables too large to copy to the host.  targets: (table, row) pairs;
     W_rows / acc_rows: float32 [n_targets, dim] host copies of those rows
@@ -228,7 +235,7 @@ def backward_rows(cols, B, offsets, values, G, Gseq, targets, W_rows, acc_rows, 
     the same order as backward_adagrad sums it.  Returns dict(table, row,
     count, grad [n, dim] fp32, absgrad [n, dim] fp64: sum of |scale * G|),
     ascending by (table, row) (W_rows / acc_rows must follow that order)."""
-    arr, keep, width = _cols(cols)
+    arr, keep, width = _cols(cols, weights)
     C = len(cols)
     offs = [np.ascontiguousarray(o, np.int32) for o in offsets]
     ids, fv = _values(cols, values)

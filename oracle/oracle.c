@@ -76,7 +76,16 @@ typedef struct {
     int32_t max_len;          /* SUM / MEAN: a bag is its first max_len values
                                  (sequence truncation; 0 = all)               */
     int32_t reserved;
+    const float* weights;     /* SUM: per-value weights w_r (NULL = all 1)     */
 } orc_col;
+
+/* Weight of value t of a column: w_t for a weighted SUM column [RecIS §3.2,
+ * Algorithm 1: y_s = sum_r w_r E[idx_r], and the backward passes w_r G[s]
+ * to row idx_r], else 1. */
+static double value_weight(const orc_col* c, int64_t t)
+{
+    return (c->pooling == ORC_SUM && c->weights) ? (double)c->weights[t] : 1.0;
+}
 
 /* End of the values of bag [lo, hi) that the column uses: PADDED keeps the
  * first pad_len, a truncated pooled column the first max_len [RecIS §2.1,
@@ -201,7 +210,8 @@ int orc_forward(const orc_col* cols, int32_t C, int32_t B,
                 int64_t r = rows[t];
                 if (r < 0) continue;
                 ++nv;
-                for (int32_t d = 0; d < c->dim; ++d) S[d] += (double)E[r * c->dim + d];
+                const double wt = value_weight(c, t);
+                for (int32_t d = 0; d < c->dim; ++d) S[d] += wt * (double)E[r * c->dim + d];
             }
             float* y = out + (int64_t)b * ldo + c->out_col;
             for (int32_t d = 0; d < c->dim; ++d) {
@@ -229,7 +239,7 @@ typedef struct {
     int64_t row;
     int64_t seq;    /* position in the order the contributions were listed  */
     int32_t b, t;   /* bag and position inside it                           */
-    double scale;   /* 1 for SUM / PADDED, 1/n_valid for MEAN               */
+    double scale;   /* w_r (1 unweighted) for SUM, 1 for PADDED, 1/n_valid for MEAN */
 } contrib;
 
 static int cmp_contrib(const void* pa, const void* pb)
@@ -305,7 +315,7 @@ int orc_backward_adagrad(const orc_col* cols, int32_t C, int32_t B,
                 e->seq = n;
                 e->b = b;
                 e->t = (int32_t)(t - lo);
-                e->scale = (c->pooling == ORC_MEAN) ? 1.0 / (double)nv : 1.0;
+                e->scale = (c->pooling == ORC_MEAN) ? 1.0 / (double)nv : value_weight(c, t);
                 ++n;
             }
         }
@@ -410,7 +420,7 @@ int orc_backward_rows(const orc_col* cols, int32_t C, int32_t B,
                 if (rows[t] < 0) continue;
                 int64_t k = find_target(n_targets, t_table, t_row, c->table, rows[t]);
                 if (k < 0) continue;
-                double scale = (c->pooling == ORC_MEAN) ? 1.0 / (double)nv : 1.0;
+                double scale = (c->pooling == ORC_MEAN) ? 1.0 / (double)nv : value_weight(c, t);
                 const float* src;
                 if (c->pooling == ORC_PADDED)
                     src = Gseq[ci] + ((int64_t)b * c->pad_len + (t - lo)) * c->dim;

@@ -66,6 +66,7 @@ class Workload:
     train: bool = False
     seed: int = 0
     extra: dict = field(default_factory=dict)
+    weights: list | None = None    # per column fp32 value weights (weighted SUM bags), or None
 
     @property
     def n_values(self) -> int:
@@ -272,11 +273,12 @@ def dynamic(seed: int = 1005, C: int = 100, B: int = 16384, dim: int = 32, steps
 
 def random_small(seed: int, C: int | None = None, B: int | None = None, train: bool = True,
                  dims=(4, 8, 12, 16, 32, 64, 128), allow_padded: bool = True,
-                 shared_tables: bool = True, allow_trunc: bool = True) -> Workload:
+                 shared_tables: bool = True, allow_trunc: bool = True,
+                 allow_weights: bool = True) -> Workload:
     """Small mixed plans for parity tests: every transform and pooling, dims
     that are not powers of two, empty bags, long bags, out-of-range and
     extreme int64 IDs, NaN/inf feature values, defaults, shared tables,
-    truncated bags."""
+    truncated bags, value weights (used by SUM columns)."""
     r = np.random.default_rng([seed, 7])
     rt = np.random.default_rng([seed, 8])   # sequence truncation, drawn apart from the rest
     C = int(r.integers(1, 12)) if C is None else C
@@ -330,7 +332,10 @@ def random_small(seed: int, C: int | None = None, B: int | None = None, train: b
             tabs.append(None)
         offs.append(bag_offsets(lens))
         vals.append(v)
-    return Workload("random%d" % seed, B, cols, tabs, offs, vals, lr=0.05, train=train, seed=seed)
+    wts = None
+    if allow_weights and rt.random() < 0.3:
+        wts = [rt.uniform(-1.0, 2.0, int(o[-1])).astype(np.float32) for o in offs]
+    return Workload("random%d" % seed, B, cols, tabs, offs, vals, lr=0.05, train=train, seed=seed, weights=wts)
 
 
 # --------------------------------------------------------------------------
@@ -381,3 +386,16 @@ def jagged(w: Workload):
     ids, id_off = stream(id_cols, np.int64)
     fv, f_off = stream(f_cols, np.float32)
     return ids, id_off, fv, f_off
+
+
+def jagged_weights(w: Workload):
+    """The value weights laid out like jagged()'s two streams, or (None, None)
+    for an unweighted workload."""
+    if w.weights is None:
+        return None, None
+    out = []
+    for want in (False, True):
+        parts = [np.asarray(w.weights[i], np.float32) for i, c in enumerate(w.columns)
+                 if (c.transform == "bucketize") == want]
+        out.append(np.concatenate(parts) if parts else np.zeros(0, np.float32))
+    return out[0], out[1]

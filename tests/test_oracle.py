@@ -122,7 +122,7 @@ def test_forward_matches_embedding_bag_in_fp64():
     torch = pytest.importorskip("torch")
     F = torch.nn.functional
     for seed in range(6):
-        w = synth.random_small(seed, allow_padded=False, allow_trunc=False)
+        w = synth.random_small(seed, allow_padded=False, allow_trunc=False, allow_weights=False)
         tabs = _tables(w)
         out, _, rows = oracle.forward(w.columns, w.B, w.offsets, w.values, tabs, want_rows=True)
         col0 = 0
@@ -212,7 +212,8 @@ def test_backward_matches_embedding_bag_autograd():
     torch = pytest.importorskip("torch")
     F = torch.nn.functional
     for seed in range(5):
-        w = synth.random_small(seed + 10, allow_padded=False, shared_tables=False, allow_trunc=False)
+        w = synth.random_small(seed + 10, allow_padded=False, shared_tables=False, allow_trunc=False,
+                               allow_weights=False)
         tabs = _tables(w)
         width = sum(c.dim for c in w.columns)
         G = synth.make_grad((w.B, width), seed).numpy()
@@ -244,7 +245,8 @@ def test_backward_matches_embedding_bag_autograd():
 def test_backward_gradient_sum_invariant():
     """Sum over unique rows of the aggregated gradient = sum over valid
     contributions of scale * G[bag] (per column and element, fp64)."""
-    w = synth.random_small(77, C=4, B=50, allow_padded=False, shared_tables=False, allow_trunc=False)
+    w = synth.random_small(77, C=4, B=50, allow_padded=False, shared_tables=False, allow_trunc=False,
+                           allow_weights=False)
     tabs = _tables(w)
     width = sum(c.dim for c in w.columns)
     G = synth.make_grad((w.B, width), 5).numpy().astype(np.float64)
@@ -475,7 +477,8 @@ def test_backward_rows_equals_the_full_backward_on_its_rows():
         Al = [x if x is not None else np.zeros((1, 1), np.float32) for x in A]
         W0 = [x.copy() for x in Wl]
         A0 = [x.copy() for x in Al]
-        ref = oracle.backward_adagrad(w.columns, w.B, w.offsets, w.values, G, Gs, Wl, Al, w.lr, w.eps)
+        ref = oracle.backward_adagrad(w.columns, w.B, w.offsets, w.values, G, Gs, Wl, Al, w.lr, w.eps,
+                                      weights=w.weights)
         n = len(ref["row"])
         if n == 0:
             continue
@@ -488,7 +491,8 @@ def test_backward_rows_equals_the_full_backward_on_its_rows():
             for k, (t, r) in enumerate(targets):
                 Wr[k, :dims[t]] = W0[t][r]
                 Ar[k, :dims[t]] = A0[t][r]
-            got = oracle.backward_rows(w.columns, w.B, w.offsets, w.values, G, Gs, targets, Wr, Ar, w.lr, w.eps)
+            got = oracle.backward_rows(w.columns, w.B, w.offsets, w.values, G, Gs, targets, Wr, Ar, w.lr, w.eps,
+                                       weights=w.weights)
             assert np.array_equal(got["count"], ref["count"][pick]), seed
             for k, (i, (t, r)) in enumerate(zip(pick, targets)):
                 d = dims[t]
@@ -559,22 +563,26 @@ def test_truncation_equals_cut_inputs():
         w = synth.random_small(300 + seed, allow_padded=False)
         if not any(c.max_len for c in w.columns):
             continue
-        cut_cols, cut_offs, cut_vals = [], [], []
-        for c, o, v in zip(w.columns, w.offsets, w.values):
+        cut_cols, cut_offs, cut_vals, cut_wts = [], [], [], []
+        wts = w.weights or [None] * len(w.columns)
+        for c, o, v, wt in zip(w.columns, w.offsets, w.values, wts):
             if c.max_len:
                 lens = np.minimum(np.diff(o), c.max_len)
                 keep = np.concatenate([np.arange(o[b], o[b] + lens[b]) for b in range(w.B)] or
                                       [np.zeros(0, np.int64)]).astype(np.int64)
                 cut_offs.append(synth.bag_offsets(lens))
                 cut_vals.append(v[keep])
+                cut_wts.append(None if wt is None else wt[keep])
                 cut_cols.append(replace(c, max_len=0))
             else:
                 cut_offs.append(o)
                 cut_vals.append(v)
+                cut_wts.append(wt)
                 cut_cols.append(c)
+        cw = None if w.weights is None else cut_wts
         tabs = _tables(w)
-        a, _ = oracle.forward(w.columns, w.B, w.offsets, w.values, tabs)
-        b, _ = oracle.forward(cut_cols, w.B, cut_offs, cut_vals, tabs)
+        a, _ = oracle.forward(w.columns, w.B, w.offsets, w.values, tabs, weights=w.weights)
+        b, _ = oracle.forward(cut_cols, w.B, cut_offs, cut_vals, tabs, weights=cw)
         assert np.array_equal(a, b), seed
         ua = oracle.unique_counts(w.columns, w.B, w.offsets, w.values)
         ub = oracle.unique_counts(cut_cols, w.B, cut_offs, cut_vals)
@@ -587,7 +595,66 @@ def test_truncation_equals_cut_inputs():
         Wb = [x.copy() if x is not None else dummy.copy() for x in tabs]
         Aa = [np.zeros_like(x) for x in Wa]
         Ab = [np.zeros_like(x) for x in Wb]
-        oracle.backward_adagrad(w.columns, w.B, w.offsets, w.values, G, None, Wa, Aa, w.lr, w.eps)
-        oracle.backward_adagrad(cut_cols, w.B, cut_offs, cut_vals, G, None, Wb, Ab, w.lr, w.eps)
+        oracle.backward_adagrad(w.columns, w.B, w.offsets, w.values, G, None, Wa, Aa, w.lr, w.eps,
+                                weights=w.weights)
+        oracle.backward_adagrad(cut_cols, w.B, cut_offs, cut_vals, G, None, Wb, Ab, w.lr, w.eps, weights=cw)
         for x, y in zip(Wa + Aa, Wb + Ab):
             assert np.array_equal(x, y), seed
+
+
+def test_weighted_bag_hand_example():
+    """SUM bag [1, 2, 1] with weights [0.5, 2, -1] pools -0.5 E1 + 2 E2; the
+    backward passes -0.5 G to row 1 and 2 G to row 2; MEAN and PADDED columns
+    ignore weights."""
+    E = np.arange(40, dtype=np.float32).reshape(10, 4)
+    off = np.array([0, 3], np.int32)
+    ids = np.array([1, 2, 1], np.int64)
+    wts = [np.array([0.5, 2.0, -1.0], np.float32)]
+    cs = ColumnSpec("identity", "sum", 10, 4, 0)
+    out, _ = oracle.forward([cs], 1, [off], [ids], [E], weights=wts)
+    np.testing.assert_allclose(out[0], -0.5 * E[1] + 2 * E[2], rtol=1e-7)
+    G = np.array([[1.0, -2.0, 3.0, 4.0]], np.float32)
+    res = oracle.backward_adagrad([cs], 1, [off], [ids], G, None, [E.copy()], [np.zeros_like(E)], 0.1, 1e-10,
+                                  weights=wts)
+    assert res["row"].tolist() == [1, 2] and res["count"].tolist() == [2, 1]
+    np.testing.assert_allclose(res["grad"][0], -0.5 * G[0], rtol=1e-7)
+    np.testing.assert_allclose(res["grad"][1], 2.0 * G[0], rtol=1e-7)
+    cm = ColumnSpec("identity", "mean", 10, 4, 0)
+    out_w, _ = oracle.forward([cm], 1, [off], [ids], [E], weights=wts)
+    out_u, _ = oracle.forward([cm], 1, [off], [ids], [E])
+    assert np.array_equal(out_w, out_u)
+
+
+def test_weighted_bags_match_embedding_bag_per_sample_weights():
+    """Weighted SUM pooling and its backward are torch embedding_bag with
+    per_sample_weights (library routine) in fp64, forward and autograd."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    rng = np.random.default_rng(3)
+    for trial in range(4):
+        rows, dim, B = int(rng.integers(5, 300)), int(rng.choice([4, 8, 16])), int(rng.integers(1, 40))
+        lens = rng.integers(0, 12, B)
+        off = synth.bag_offsets(lens)
+        n = int(lens.sum())
+        ids = rng.integers(-2, rows + 2, n).astype(np.int64)   # some dropped
+        wts = rng.uniform(-1, 2, n).astype(np.float32)
+        E = rng.standard_normal((rows, dim)).astype(np.float32)
+        G = rng.standard_normal((B, dim)).astype(np.float32)
+        cs = ColumnSpec("identity", "sum", rows, dim, 0)
+        out, _ = oracle.forward([cs], B, [off], [ids], [E], weights=[wts])
+        keep = (ids >= 0) & (ids < rows)
+        bag = np.repeat(np.arange(B), lens)[keep]
+        new_off = np.searchsorted(bag, np.arange(B), side="left")
+        Et = torch.from_numpy(E).double().requires_grad_(True)
+        ref = F.embedding_bag(torch.from_numpy(ids[keep]), Et, torch.from_numpy(new_off), mode="sum",
+                              per_sample_weights=torch.from_numpy(wts[keep]).double())
+        np.testing.assert_allclose(out, ref.detach().numpy(), rtol=1e-6, atol=1e-6)
+        ref.backward(torch.from_numpy(G).double())
+        res = oracle.backward_adagrad([cs], B, [off], [ids], G, None, [E.copy()], [np.zeros_like(E)], 0.1, 1e-10,
+                                      weights=[wts])
+        g = Et.grad.numpy()
+        for r, gr in zip(res["row"], res["grad"]):
+            np.testing.assert_allclose(gr, g[r], rtol=1e-5, atol=1e-6)
+        touched = np.zeros(rows, bool)
+        touched[res["row"]] = True
+        assert np.all(g[~touched] == 0)
