@@ -159,6 +159,11 @@ emb_status emb_plan_info(emb_plan plan, int64_t* out_width, int64_t* seq_floats_
  *                   id_offsets has n_id_cols*batch + 1 int32 entries,
  *                   id_offsets[0] == 0, non-decreasing, last == n_ids.
  *  fvals, f_offsets the same for the BUCKETIZE columns (fp32 values).
+ *  id_weights, f_weights  optional fp32 weights, one per value of each
+ *                   stream (NULL: none).  A SUM column of a weighted stream
+ *                   pools sum_r w_r * E[row_r] and its backward passes
+ *                   w_r * G to row_r [RecIS §3.2 Algorithm 1, w_r]; MEAN and
+ *                   padded columns ignore the weights.
  *  n_ids, n_fvals   element counts of the two value arrays.  Offsets outside
  *                   [0, n] are clamped on the device (never read out of
  *                   bounds) and latch EMB_ERR_BAD_INDEX.
@@ -173,13 +178,14 @@ emb_status emb_plan_info(emb_plan plan, int64_t* out_width, int64_t* seq_floats_
  *           (id stream first), -1 where dropped.  NULL in production.
  * A training plan also records, in its workspace, each contribution's row and
  * bag for emb_backward_update; batch <= max_batch and n_ids + n_fvals <=
- * max_ids are then required.  The input buffers must stay unchanged until the
- * backward of this forward has been queued.
+ * max_ids are then required (the weights are copied there too, 8 B per
+ * value).  The input buffers must stay unchanged until the backward of this
+ * forward has been queued.
  * Calls on one plan must be ordered (one stream, or streams joined by events):
  * the forward's tile counter and the training workspace belong to the plan. */
 emb_status emb_forward(emb_plan plan, int32_t batch,
-                       const int64_t* ids, const int32_t* id_offsets, int64_t n_ids,
-                       const float* fvals, const int32_t* f_offsets, int64_t n_fvals,
+                       const int64_t* ids, const int32_t* id_offsets, const float* id_weights, int64_t n_ids,
+                       const float* fvals, const int32_t* f_offsets, const float* f_weights, int64_t n_fvals,
                        float* out, float* seq_out, int64_t* rows_dbg, void* stream);
 
 /* Optional device outputs of emb_backward_update, for parity checks. */
@@ -198,8 +204,8 @@ typedef struct {
  * local reduce-ID; §4.3 sparse learning rate].
  *
  * Every valid contribution r of bag b of column c carries scale_r *
- * grad_out[b, col_off_c : col_off_c + dim_c] (scale 1 for SUM, 1/n_valid for
- * MEAN), or grad_seq[b, t, :] of its padded column.  The contributions are
+ * grad_out[b, col_off_c : col_off_c + dim_c] (scale w_r for SUM -- 1 without
+ * weights --, 1/n_valid for MEAN), or grad_seq[b, t, :] of its padded column.  The contributions are
  * radix-sorted by global row, the runs give the unique rows and counts, each
  * unique row's gradient g is summed by exactly one writer, then
  *   acc += g*g;  w -= lr * g / (sqrt(acc) + eps)

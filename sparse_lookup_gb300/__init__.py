@@ -70,8 +70,8 @@ _SIGS = {
     "emb_plan_destroy": (c_int32, [c_void_p]),
     "emb_plan_info": (c_int32, [c_void_p, POINTER(c_int64), POINTER(c_int64), POINTER(c_int32), c_void_p,
                                 POINTER(c_int64)]),
-    "emb_forward": (c_int32, [c_void_p, c_int32, c_void_p, c_void_p, c_int64, c_void_p, c_void_p, c_int64,
-                              c_void_p, c_void_p, c_void_p, c_void_p]),
+    "emb_forward": (c_int32, [c_void_p, c_int32, c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_void_p,
+                              c_void_p, c_int64, c_void_p, c_void_p, c_void_p, c_void_p]),
     "emb_backward_update": (c_int32, [c_void_p, c_void_p, c_void_p, c_float, c_float, c_void_p,
                                       POINTER(EmbBackwardDebug)]),
     "emb_get_device_status": (c_int32, [c_void_p, c_void_p]),
@@ -162,10 +162,11 @@ def emb_plan_info(plan, n_cols):
                 col_table=list(ct)[:n_cols], workspace_bytes=ws.value)
 
 
-def emb_forward(plan, batch, ids, id_offsets, n_ids, fvals, f_offsets, n_fvals, out, seq_out,
-                rows_dbg=None, stream=None):
-    _check(lib().emb_forward(plan, batch, ptr(ids), ptr(id_offsets), n_ids, ptr(fvals), ptr(f_offsets), n_fvals,
-                             ptr(out), ptr(seq_out), ptr(rows_dbg), _stream(stream)), "emb_forward")
+def emb_forward(plan, batch, ids, id_offsets, id_weights, n_ids, fvals, f_offsets, f_weights, n_fvals, out,
+                seq_out, rows_dbg=None, stream=None):
+    _check(lib().emb_forward(plan, batch, ptr(ids), ptr(id_offsets), ptr(id_weights), n_ids, ptr(fvals),
+                             ptr(f_offsets), ptr(f_weights), n_fvals, ptr(out), ptr(seq_out), ptr(rows_dbg),
+                             _stream(stream)), "emb_forward")
 
 
 def emb_backward_update(plan, grad_out, grad_seq, lr, eps, stream=None, dbg=None):
@@ -297,7 +298,7 @@ class Plan:
             pass
 
     def forward(self, batch, ids, id_offsets, fvals, f_offsets, out=None, seq_out=None, rows_dbg=None,
-                stream=None):
+                stream=None, id_weights=None, f_weights=None):
         import torch
         dev = id_offsets.device if id_offsets is not None else f_offsets.device
         if out is None:
@@ -306,8 +307,11 @@ class Plan:
             seq_out = torch.empty((batch * self.seq_per_bag,), dtype=torch.float32, device=dev)
         n_ids = 0 if ids is None else ids.numel()
         n_f = 0 if fvals is None else fvals.numel()
-        emb_forward(self.handle, batch, ids, id_offsets, n_ids, fvals, f_offsets, n_f, out, seq_out,
-                    rows_dbg, stream)
+        for wt, vals in ((id_weights, ids), (f_weights, fvals)):
+            if wt is not None and (vals is None or wt.numel() != vals.numel() or wt.dtype != torch.float32):
+                raise ValueError("value weights: one float32 per value of their stream")
+        emb_forward(self.handle, batch, ids, id_offsets, id_weights, n_ids, fvals, f_offsets, f_weights, n_f,
+                    out, seq_out, rows_dbg, stream)
         return out, seq_out
 
     def backward_update(self, grad_out, grad_seq, lr, eps, stream=None, debug=False):

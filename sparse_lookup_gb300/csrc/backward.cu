@@ -143,6 +143,7 @@ struct SegArgs {
   uint32_t sentinel;
   const int4* colg;       // per column: out_col, 1 if MEAN, dim/4
   const float* inv_n;
+  const uint2* rec_src;   // weighted forwards: (gradient source, weight bits) per record; vals hold records
   const float* grad_out;
   int64_t ldg;
   const float* grad_seq;
@@ -225,27 +226,6 @@ __device__ void finish_row(const SegArgs& a, uint32_t key, int64_t end, const fl
       if (f4 < tm.dim4) *reinterpret_cast<float4*>(a.dbg_grad + (int64_t)u * a.dbg_ld + f4 * 4) = g[v];
     }
   }
-}
-
-// Gradient source of a contribution: pointer to its G row, its scale and the
-// float4 count of the row (padded sources take the dim of the key's table).
-__device__ __forceinline__ const float* grad_src(const SegArgs& a, uint32_t val, uint32_t key, float& scale,
-                                                 int& d4, uint32_t& lkey, int& ld4) {
-  if (val & kPadBit) {
-    scale = 1.0f;
-    if (key != lkey) {
-      lkey = key;
-      ld4 = a.tables[table_of_key(a.table_base, a.n_tables, key)].dim4;
-    }
-    d4 = ld4;
-    return a.grad_seq + (int64_t)(val & ~kPadBit) * 4;
-  }
-  const uint32_t c = div_magic32(val, a.bdiv);
-  const uint32_t b = val - c * (uint32_t)a.batch;
-  const int4 cg = __ldg(a.colg + c);
-  scale = cg.y ? __ldg(a.inv_n + val) : 1.0f;
-  d4 = cg.z;
-  return a.grad_out + (int64_t)b * a.ldg + cg.x;
 }
 
 // The table a key belongs to and its metadata, tracked while keys ascend
@@ -428,7 +408,13 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
         prefetch_l2(ptc.acc + row * ptc.dim, (uint32_t)ptc.dim * 4u);
       }
       if (key != a.sentinel) {
-        const uint32_t val = __ldg(a.vals + B0 + e);
+        uint32_t val = __ldg(a.vals + B0 + e);
+        float wr = 1.0f;   // value weight of a SUM contribution
+        if (a.rec_src) {
+          const uint2 rs = __ldg(a.rec_src + val);
+          val = rs.x;
+          wr = __uint_as_float(rs.y);
+        }
         if (val & kPadBit) {
           if (key != lkey) {
             lkey = key;
@@ -441,7 +427,7 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
           const uint32_t c = div_magic32(val, a.bdiv);
           const uint32_t b = val - c * (uint32_t)a.batch;
           const int4 cg = __ldg(a.colg + c);
-          r.scale = cg.y ? __ldg(a.inv_n + val) : 1.0f;
+          r.scale = cg.y ? __ldg(a.inv_n + val) : wr;
           r.d4 = (uint32_t)cg.z;
           r.off = (uint32_t)(((int64_t)b * a.ldg + cg.x) >> 2);
         }
@@ -717,6 +703,7 @@ emb_status launch_backward(emb_plan_s* p, const float* grad_out, const float* gr
   a.sentinel = p->key_total;
   a.colg = p->colg_d;
   a.inv_n = w.inv_n;
+  a.rec_src = p->last_weighted ? w.rec_src : nullptr;
   a.grad_out = grad_out;
   a.ldg = p->out_width;
   a.grad_seq = grad_seq;

@@ -43,6 +43,7 @@ struct FwdArgs {
   const int32_t* stream_cols;
   const int64_t* ids;
   const float* fvals;
+  const float* wts[2];     // per-value weights of each stream (SUM columns), or null
   const int32_t* offs[2];
   int64_t n[2];
   int32_t ncols[2];
@@ -57,7 +58,8 @@ struct FwdArgs {
   int64_t* rows_dbg;
   int64_t rec_base[2];     // record index of element 0 of each stream
   uint32_t* keys;          // training: global row per contribution (sentinel if none)
-  uint32_t* vals;          // training: gradient source per contribution
+  uint32_t* vals;          // training: gradient source per contribution (its record, when weighted)
+  uint2* rec_src;          // weighted training: (gradient source, weight bits) per record
   float* inv_n;            // training: 1/n_valid per mean bag
   uint32_t key_sentinel;
   uint32_t* status;
@@ -85,6 +87,17 @@ __device__ __forceinline__ void f4add(float4& a, const float4& b) {
   a.y += b.y;
   a.z += b.z;
   a.w += b.w;
+}
+
+__device__ __forceinline__ void f4fma(float4& a, float w, const float4& b) {
+  a.x = fmaf(w, b.x, a.x);
+  a.y = fmaf(w, b.y, a.y);
+  a.z = fmaf(w, b.z, a.z);
+  a.w = fmaf(w, b.w, a.w);
+}
+
+__device__ __forceinline__ float4 f4scale(float w, const float4& b) {
+  return make_float4(w * b.x, w * b.y, w * b.z, w * b.w);
 }
 
 __device__ __forceinline__ float4 ldg4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
@@ -172,13 +185,22 @@ __device__ __forceinline__ int32_t col_row(const ColMeta& m, const int64_t* ids,
   return col_transform(m, col_load(m, ids, fvals, t));
 }
 
+// WT: the launch carries value weights (training then records them)
+template <bool WT>
 __device__ __forceinline__ void record(const FwdArgs& a, int st, int64_t t, int32_t row,
                                        const ColMeta& m, uint32_t gsrc) {
   const int64_t r = a.rec_base[st] + t;
   if (a.rows_dbg) a.rows_dbg[r] = row;
   if (a.keys) {
     a.keys[r] = row >= 0 ? m.table_base + (uint32_t)row : a.key_sentinel;
-    a.vals[r] = gsrc;
+    if (WT && a.rec_src) {
+      // the sort carries the record; the backward reads source and weight here
+      const float w = (m.pooling == EMB_POOL_SUM && a.wts[st]) ? __ldg(a.wts[st] + t) : 1.0f;
+      a.rec_src[r] = make_uint2(gsrc, __float_as_uint(w));
+      a.vals[r] = (uint32_t)r;
+    } else {
+      a.vals[r] = gsrc;
+    }
   }
 }
 
@@ -236,11 +258,12 @@ __device__ __forceinline__ uint32_t padded_gsrc(const FwdArgs& a, const ColMeta&
 }
 
 // ---------------------------------------------------------------------------
-// phase B, pooled: equal value ranges per lane group
+// phase B, pooled: equal value ranges per lane group; WT: a SUM column of a
+// weighted stream, each row scaled by its value's weight W[t]
 // ---------------------------------------------------------------------------
-template <int V>
-__device__ void warp_pool_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m, int ns, int T, int b0,
-                                int glog, unsigned longmask) {
+template <int V, bool WT>
+__device__ void warp_pool_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m, const float* W, int ns, int T,
+                                int b0, int glog, unsigned longmask) {
   constexpr int U = kUPool / V;
   const int dim = m.dim, dim4 = m.dim4;
   const int lane = threadIdx.x & 31;
@@ -288,6 +311,7 @@ __device__ void warp_pool_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m
 
   for (int j = 0; j < R; j += U) {
     float4 vals[U][V];
+    float wu[WT ? U : 1];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int k = k0 + j + u;
@@ -296,6 +320,13 @@ __device__ void warp_pool_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m
       for (int v = 0; v < V; ++v) {
         const int f4 = sub + v * 32;
         vals[u][v] = (r >= 0 && f4 < dim4) ? ldg4(E + (int64_t)r * dim + f4 * 4) : f4zero();
+      }
+      if constexpr (WT) {
+        wu[u] = 0.0f;
+        if (r >= 0) {
+          const int bg = (int)ws.bag[k];
+          wu[u] = __ldg(W + (int64_t)ws.lo[bg] + (k - ws.pos[bg]));
+        }
       }
     }
     // bag and validity are read again from shared memory rather than held
@@ -314,7 +345,10 @@ __device__ void warp_pool_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m
         nv = 0;
       }
 #pragma unroll
-      for (int v = 0; v < V; ++v) f4add(acc[v], vals[u][v]);
+      for (int v = 0; v < V; ++v) {
+        if constexpr (WT) f4fma(acc[v], wu[u], vals[u][v]);
+        else f4add(acc[v], vals[u][v]);
+      }
       nv += ws.rows[k] >= 0;
     }
   }
@@ -396,9 +430,9 @@ __device__ void warp_pad_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m,
 // ---------------------------------------------------------------------------
 // phase C: one long bag, the whole warp, values transformed on the fly
 // ---------------------------------------------------------------------------
-template <int V>
-__device__ void warp_long_bag(const FwdArgs& a, int st, const ColMeta& m, int32_t b, int64_t lo, int64_t hi,
-                              int glog) {
+template <int V, bool WT>
+__device__ void warp_long_bag(const FwdArgs& a, int st, const ColMeta& m, const float* W, int32_t b, int64_t lo,
+                              int64_t hi, int glog) {
   constexpr int U = kU / V;
   const int lane = threadIdx.x & 31;
   const int G = 32 >> glog;
@@ -414,7 +448,7 @@ __device__ void warp_long_bag(const FwdArgs& a, int st, const ColMeta& m, int32_
       const int64_t p = p0 + lane;
       if (lane < cnt && p < len) {
         row = col_row(m, a.ids, a.fvals, lo + p);
-        record(a, st, lo + p, row, m, padded_gsrc(a, m, b, p));
+        record<WT>(a, st, lo + p, row, m, padded_gsrc(a, m, b, p));
       }
       for (int k = 0; k < cnt; k += U * G) {
         float4 v[U][V];
@@ -455,9 +489,11 @@ __device__ void warp_long_bag(const FwdArgs& a, int st, const ColMeta& m, int32_
   for (int64_t base = lo; base < hi; base += 32) {
     const int cnt = (int)(hi - base < 32 ? hi - base : 32);
     int32_t row = -1;
+    float wl = 1.0f;
     if (lane < cnt) {
       row = col_row(m, a.ids, a.fvals, base + lane);
-      record(a, st, base + lane, row, m, gsrc);
+      record<WT>(a, st, base + lane, row, m, gsrc);
+      if (WT && W && row >= 0) wl = __ldg(W + base + lane);
     }
     nv += __popc(__ballot_sync(kFull, row >= 0));
     for (int k = 0; k < cnt; k += U * G) {
@@ -471,6 +507,14 @@ __device__ void warp_long_bag(const FwdArgs& a, int st, const ColMeta& m, int32_
         for (int q = 0; q < V; ++q) {
           const int f4 = sub + q * 32;
           v[u][q] = (ok && f4 < m.dim4) ? ldg4(E + (int64_t)r * m.dim + f4 * 4) : f4zero();
+        }
+      }
+      if (WT && W) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const float wj = __shfl_sync(kFull, wl, (k + u * G + grp) & 31);
+#pragma unroll
+          for (int q = 0; q < V; ++q) v[u][q] = f4scale(wj, v[u][q]);
         }
       }
 #pragma unroll
@@ -508,6 +552,7 @@ __device__ void warp_long_bag(const FwdArgs& a, int st, const ColMeta& m, int32_
 // ---------------------------------------------------------------------------
 // the kernel: one warp per element tile
 // ---------------------------------------------------------------------------
+template <bool WT>
 __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int64_t tile);
 
 // Two schedules.  Static: one tile per warp, the grid covers all tiles (warps
@@ -518,6 +563,9 @@ __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int
 // idling beside a sibling that drew long ones; the last warp to finish
 // resets the counter for the next launch (CUDA-graph safe: no host state
 // changes between launches).
+// WT: a launch with value weights gets its own instance, so the unweighted
+// one keeps its registers for loads in flight.
+template <bool WT>
 __global__ void __launch_bounds__(kFwdThreads, 4) k_forward(const FwdArgs a) {
   __shared__ WarpSmem smem[kFwdWarpsPerCta];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -526,7 +574,7 @@ __global__ void __launch_bounds__(kFwdThreads, 4) k_forward(const FwdArgs a) {
   // the first tile of every warp is its warp index; tickets count from there
   int64_t tile = (int64_t)blockIdx.x * kFwdWarpsPerCta + (threadIdx.x >> 5);
   while (tile < n_tiles) {
-    forward_tile(a, ws, tile);
+    forward_tile<WT>(a, ws, tile);
     if (!a.dynamic) break;   // static: one tile per warp
     unsigned long long tk = 0;
     if (lane == 0) tk = atomicAdd(&a.ticket[0], 1ull);
@@ -542,6 +590,7 @@ __global__ void __launch_bounds__(kFwdThreads, 4) k_forward(const FwdArgs a) {
   }
 }
 
+template <bool WT>
 __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int64_t tile) {
   const int lane = threadIdx.x & 31;
   int st = 0;
@@ -661,7 +710,7 @@ __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int
           ws.bag[k] = (uint8_t)i;
           if (a.rows_dbg || a.keys) {
             const int64_t t = (int64_t)ws.lo[i] + (k - ws.pos[i]);
-            record(a, st, t, row, m, padded ? padded_gsrc(a, m, b0 + i, k - ws.pos[i]) : pooled_gsrc(a, m, b0 + i));
+            record<WT>(a, st, t, row, m, padded ? padded_gsrc(a, m, b0 + i, k - ws.pos[i]) : pooled_gsrc(a, m, b0 + i));
           }
         }
       }
@@ -688,12 +737,16 @@ __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int
 
     // ---- phase B: pool / copy ----
     const int glog = lanes_log2(m.dim4);
+    const float* W = WT && m.pooling == EMB_POOL_SUM ? a.wts[st] : nullptr;   // value weights
     if (padded) {
       if (m.dim4 > 32) warp_pad_chunk<2>(a, ws, m, ns, b0, glog, longmask);
       else warp_pad_chunk<1>(a, ws, m, ns, b0, glog, longmask);
+    } else if (WT && W) {
+      if (m.dim4 > 32) warp_pool_chunk<2, true>(a, ws, m, W, ns, T, b0, glog, longmask);
+      else warp_pool_chunk<1, true>(a, ws, m, W, ns, T, b0, glog, longmask);
     } else {
-      if (m.dim4 > 32) warp_pool_chunk<2>(a, ws, m, ns, T, b0, glog, longmask);
-      else warp_pool_chunk<1>(a, ws, m, ns, T, b0, glog, longmask);
+      if (m.dim4 > 32) warp_pool_chunk<2, false>(a, ws, m, W, ns, T, b0, glog, longmask);
+      else warp_pool_chunk<1, false>(a, ws, m, W, ns, T, b0, glog, longmask);
     }
 
     // ---- phase C: long bags of the chunk ----
@@ -701,8 +754,8 @@ __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int
       const int i = __ffs(lm) - 1;
       const int64_t blo = __shfl_sync(kFull, lo, i);
       const int64_t bhi = __shfl_sync(kFull, hi, i);
-      if (m.dim4 > 32) warp_long_bag<2>(a, st, m, b0 + i, blo, bhi, glog);
-      else warp_long_bag<1>(a, st, m, b0 + i, blo, bhi, glog);
+      if (m.dim4 > 32) warp_long_bag<2, WT>(a, st, m, W, b0 + i, blo, bhi, glog);
+      else warp_long_bag<1, WT>(a, st, m, W, b0 + i, blo, bhi, glog);
     }
     __syncwarp();
     cur += ns;
@@ -711,7 +764,7 @@ __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int
 
 int forward_ctas_per_sm() {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_forward, kFwdThreads, 0) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_forward<false>, kFwdThreads, 0) != cudaSuccess) {
     cudaGetLastError();
     n = 4;
   }
@@ -719,14 +772,17 @@ int forward_ctas_per_sm() {
 }
 
 emb_status launch_forward(emb_plan_s* p, int32_t batch, const int64_t* ids, const int32_t* id_offsets,
-                          int64_t n_ids, const float* fvals, const int32_t* f_offsets, int64_t n_fvals,
-                          float* out, float* seq_out, int64_t* rows_dbg, cudaStream_t stream) {
+                          const float* id_weights, int64_t n_ids, const float* fvals, const int32_t* f_offsets,
+                          const float* f_weights, int64_t n_fvals, float* out, float* seq_out, int64_t* rows_dbg,
+                          cudaStream_t stream) {
   if (batch == 0) return EMB_OK;
   FwdArgs a{};
   a.meta = p->meta_d;
   a.stream_cols = p->stream_cols_d;
   a.ids = ids;
   a.fvals = fvals;
+  a.wts[0] = id_weights;
+  a.wts[1] = f_weights;
   a.offs[0] = id_offsets;
   a.offs[1] = f_offsets;
   a.n[0] = n_ids;
@@ -747,6 +803,7 @@ emb_status launch_forward(emb_plan_s* p, int32_t batch, const int64_t* ids, cons
     a.keys = p->ws.keys[0];
     a.vals = p->ws.vals[0];
     a.inv_n = p->ws.inv_n;
+    if (id_weights || f_weights) a.rec_src = p->ws.rec_src;
   }
   a.key_sentinel = p->key_total;
   a.status = p->status_d;
@@ -771,7 +828,8 @@ emb_status launch_forward(emb_plan_s* p, int32_t batch, const int64_t* ids, cons
   if (a.dynamic) grid = std::min<int64_t>(grid, resident);
   a.ticket = p->fwd_ticket;
   a.n_warps = grid * kFwdWarpsPerCta;
-  k_forward<<<(unsigned)grid, kFwdThreads, 0, stream>>>(a);
+  if (a.wts[0] || a.wts[1]) k_forward<true><<<(unsigned)grid, kFwdThreads, 0, stream>>>(a);
+  else k_forward<false><<<(unsigned)grid, kFwdThreads, 0, stream>>>(a);
   return cuda_status(cudaGetLastError());
 }
 

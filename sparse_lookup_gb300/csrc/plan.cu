@@ -27,6 +27,7 @@ void free_plan(emb_plan_s* p) {
   cudaFree(w.vals[0]);
   cudaFree(w.vals[1]);
   cudaFree(w.inv_n);
+  cudaFree(w.rec_src);
   cudaFree(w.hist);
   cudaFree(w.run_head);
   cudaFree(w.head_pos);
@@ -215,6 +216,7 @@ extern "C" emb_status emb_plan_create(const emb_column_desc* cols, int32_t n_col
       if (e == cudaSuccess) e = dmalloc(&w.vals[i], n, &total);
     }
     if (e == cudaSuccess) e = dmalloc(&w.inv_n, (size_t)n_cols * max_batch, &total);
+    if (e == cudaSuccess) e = dmalloc(&w.rec_src, n, &total);
     if (e == cudaSuccess) e = dmalloc(&w.hist, sort_scratch_words<uint32_t>(p->key_bits, n), &total);
     if (e == cudaSuccess) e = dmalloc(&w.run_head, n + 1, &total);
     if (e == cudaSuccess) e = dmalloc(&w.head_pos, n, &total);
@@ -254,9 +256,10 @@ extern "C" emb_status emb_plan_info(emb_plan p, int64_t* out_width, int64_t* seq
 }
 
 extern "C" emb_status emb_forward(emb_plan p, int32_t batch, const int64_t* ids,
-                                  const int32_t* id_offsets, int64_t n_ids, const float* fvals,
-                                  const int32_t* f_offsets, int64_t n_fvals, float* out,
-                                  float* seq_out, int64_t* rows_dbg, void* stream) {
+                                  const int32_t* id_offsets, const float* id_weights, int64_t n_ids,
+                                  const float* fvals, const int32_t* f_offsets, const float* f_weights,
+                                  int64_t n_fvals, float* out, float* seq_out, int64_t* rows_dbg,
+                                  void* stream) {
   if (!p || batch < 0 || batch > p->max_batch || n_ids < 0 || n_fvals < 0) return EMB_ERR_INVALID_ARG;
   if (n_ids >= (int64_t(1) << 31) || n_fvals >= (int64_t(1) << 31)) return EMB_ERR_UNSUPPORTED;
   if (p->n_stream_cols[0] > 0 && (!id_offsets || (n_ids > 0 && !ids))) return EMB_ERR_INVALID_ARG;
@@ -268,13 +271,16 @@ extern "C" emb_status emb_forward(emb_plan p, int32_t batch, const int64_t* ids,
     // padded gradient sources are addressed in float4 units below 2^31
     if (p->seq_per_bag * (int64_t)batch / 4 >= (int64_t(1) << 31)) return EMB_ERR_UNSUPPORTED;
   }
-  emb_status s = launch_forward(p, batch, ids, id_offsets, n_ids, fvals, f_offsets, n_fvals, out,
-                                seq_out, rows_dbg, (cudaStream_t)stream);
+  if (n_ids == 0) id_weights = nullptr;
+  if (n_fvals == 0) f_weights = nullptr;
+  emb_status s = launch_forward(p, batch, ids, id_offsets, id_weights, n_ids, fvals, f_offsets, f_weights,
+                                n_fvals, out, seq_out, rows_dbg, (cudaStream_t)stream);
   if (s == EMB_OK && p->training) {
     p->have_forward = true;
     p->last_batch = batch;
     p->last_n = n_ids + n_fvals;
     p->last_n_ids = n_ids;
+    p->last_weighted = id_weights || f_weights;
   }
   return s;
 }

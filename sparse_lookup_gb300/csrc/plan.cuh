@@ -32,6 +32,7 @@ struct Workspace {
   uint32_t* keys[2] = {nullptr, nullptr};
   uint32_t* vals[2] = {nullptr, nullptr};
   float* inv_n = nullptr;          // [n_cols * max_batch] 1/n_valid of mean bags
+  uint2* rec_src = nullptr;        // [max_ids] weighted forwards: (gradient source, weight bits) per record
   uint32_t* hist = nullptr;        // the sort's scratch: histograms, tile tickets, look-back words
   uint32_t* run_head = nullptr;    // [max_ids + 1] debug: runs started at or before each position
   uint32_t* head_pos = nullptr;    // [max_ids] debug: position of each run's first entry
@@ -81,6 +82,7 @@ struct emb_plan_s {
   int32_t last_batch = 0;
   int64_t last_n = 0;
   int64_t last_n_ids = 0;
+  bool last_weighted = false;   // the last forward carried value weights (records hold rec_src)
 };
 
 namespace emb {
@@ -98,10 +100,10 @@ inline emb_status cuda_status(cudaError_t e) {
   } while (0)
 
 // Launch-side entry points implemented in forward.cu / backward.cu.
-emb_status launch_forward(emb_plan_s* p, int32_t batch, const int64_t* ids,
-                          const int32_t* id_offsets, int64_t n_ids, const float* fvals,
-                          const int32_t* f_offsets, int64_t n_fvals, float* out,
-                          float* seq_out, int64_t* rows_dbg, cudaStream_t stream);
+emb_status launch_forward(emb_plan_s* p, int32_t batch, const int64_t* ids, const int32_t* id_offsets,
+                          const float* id_weights, int64_t n_ids, const float* fvals, const int32_t* f_offsets,
+                          const float* f_weights, int64_t n_fvals, float* out, float* seq_out, int64_t* rows_dbg,
+                          cudaStream_t stream);
 int forward_ctas_per_sm();
 
 emb_status launch_backward(emb_plan_s* p, const float* grad_out, const float* grad_seq,

@@ -45,6 +45,9 @@ class Materialized:
         self.f_off = torch.from_numpy(f_off).to(device) if n_f_cols else None
         self.n_ids = ids.size
         self.n_f = fv.size
+        idw, fw = synth.jagged_weights(w)
+        self.idw = torch.from_numpy(idw).to(device) if idw is not None and n_id_cols else None
+        self.fw = torch.from_numpy(fw).to(device) if fw is not None and n_f_cols else None
 
     def host_tables(self):
         return [None if t is None else t.cpu().numpy() for t in self.tables]
@@ -135,7 +138,8 @@ class TrainStep:
         self.A0 = [None if a is None else a.cpu().numpy() for a in m.accs]
         n = m.n_ids + m.n_f
         self.plan = sl.Plan(w.columns, m.tables, m.accs, max_batch=max(w.B, 1), max_ids=max(n, 1), training=True)
-        self.out, self.seq = self.plan.forward(w.B, m.ids, m.id_off, m.fv, m.f_off)
+        self.out, self.seq = self.plan.forward(w.B, m.ids, m.id_off, m.fv, m.f_off, id_weights=m.idw,
+                                               f_weights=m.fw)
         width = self.plan.out_width
         self.G = synth.make_grad((w.B, max(width, 1)), grad_seed, device)[:, :width].contiguous()
         self.Gseq = None
@@ -160,13 +164,15 @@ class TrainStep:
         dummy = np.zeros((1, 1), np.float32)
         Wl = [Wr[i] if Wr[i] is not None else dummy for i in range(nt)]
         Al = [Ar[i] if Ar[i] is not None else dummy for i in range(nt)]
-        ref = oracle.backward_adagrad(w.columns, w.B, w.offsets, w.values, G, gseq, Wl, Al, w.lr, w.eps)
+        ref = oracle.backward_adagrad(w.columns, w.B, w.offsets, w.values, G, gseq, Wl, Al, w.lr, w.eps,
+                                      weights=w.weights)
         # magnitudes for the summation-error bound: the same aggregation of |G|
         Wd = [np.zeros_like(x) for x in Wl]
         Ad = [np.zeros_like(x) for x in Al]
         absg = oracle.backward_adagrad(w.columns, w.B, w.offsets, w.values, np.abs(G),
                                        None if gseq is None else [None if g is None else np.abs(g) for g in gseq],
-                                       Wd, Ad, w.lr, w.eps)
+                                       Wd, Ad, w.lr, w.eps,
+                                       weights=None if w.weights is None else [np.abs(x) for x in w.weights])
         return ref, absg, Wl, Al
 
     def gpu_table_to_spec(self):

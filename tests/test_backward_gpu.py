@@ -73,6 +73,40 @@ def test_truncated_sequences():
         assert_close(ts.out.cpu().numpy(), ref, "pooled, max_len %d" % cut)
 
 
+def _weigh(w, seed):
+    rng = np.random.default_rng(seed)
+    w.weights = [rng.uniform(-1.0, 2.0, int(o[-1])).astype(np.float32) for o in w.offsets]
+    return w
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_weighted_random_small_plans(seed):
+    """Value weights on every column of a random plan (both streams; SUM
+    columns use them, MEAN and padded ones ignore them): pooled output and
+    training step against the oracle."""
+    w = _weigh(synth.random_small(300 + seed), seed)
+    ts = TrainStep(w)
+    check_train_step(ts)
+    ref, _ = oracle.forward(w.columns, w.B, w.offsets, w.values, ts.W0, weights=w.weights)
+    if ref.shape[1]:
+        assert_close(ts.out.cpu().numpy(), ref, "weighted pooled output")
+
+
+@pytest.mark.parametrize("dim", [8, 128, 200])
+def test_weighted_long_and_short_bags(dim):
+    """Weighted SUM bags of 50-400 values (short bags pooled by lane groups,
+    long ones by the whole warp) beside an unweighted MEAN column of the
+    same stream."""
+    from dataclasses import replace
+    w = synth.sequences(seed=8, mode="mean", C=3, B=40, rows=3000, dim=dim, len_lo=50, len_hi=400)
+    w.columns = [replace(c, pooling=p) for c, p in zip(w.columns, ("sum", "mean", "sum"))]
+    _weigh(w, dim)
+    ts = TrainStep(w)
+    check_train_step(ts)
+    ref, _ = oracle.forward(w.columns, w.B, w.offsets, w.values, ts.W0, weights=w.weights)
+    assert_close(ts.out.cpu().numpy(), ref, "weighted pooled output")
+
+
 def test_shared_table_columns_merge():
     rng = np.random.default_rng(9)
     B = 500

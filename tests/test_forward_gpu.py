@@ -26,7 +26,8 @@ def run_forward(w, training=False):
     plan = sl.Plan(w.columns, m.tables, m.accs, max_batch=max(w.B, 1),
                    max_ids=max(m.n_ids + m.n_f, 1), training=training)
     rows_dbg = torch.full((max(m.n_ids + m.n_f, 1),), -7, dtype=torch.int64, device="cuda")
-    out, seq = plan.forward(w.B, m.ids, m.id_off, m.fv, m.f_off, rows_dbg=rows_dbg)
+    out, seq = plan.forward(w.B, m.ids, m.id_off, m.fv, m.f_off, rows_dbg=rows_dbg, id_weights=m.idw,
+                            f_weights=m.fw)
     torch.cuda.synchronize()
     assert plan.device_status() == 0
     return m, plan, out, seq, rows_dbg
@@ -34,7 +35,8 @@ def run_forward(w, training=False):
 
 def check_full(w, m, out, seq, rows_dbg):
     tabs = m.host_tables()
-    ref_out, ref_seq, ref_rows = oracle.forward(w.columns, w.B, w.offsets, w.values, tabs, want_rows=True)
+    ref_out, ref_seq, ref_rows = oracle.forward(w.columns, w.B, w.offsets, w.values, tabs, want_rows=True,
+                                                weights=w.weights)
     for c, (got, ref) in enumerate(zip(m.rows_dbg_split(rows_dbg), ref_rows)):
         assert np.array_equal(got, ref), "rows of column %d" % c
     if ref_out.shape[1]:
@@ -116,8 +118,8 @@ def test_zero_batch_is_a_no_op():
     m = Materialized(w, "cuda")
     plan = sl.Plan(w.columns, m.tables, None, max_batch=w.B)
     out = torch.empty((0, plan.out_width), device="cuda")
-    sl.emb_forward(plan.handle, 0, m.ids, torch.zeros(1, dtype=torch.int32, device="cuda"), 0, None, None, 0,
-                   out, None)
+    sl.emb_forward(plan.handle, 0, m.ids, torch.zeros(1, dtype=torch.int32, device="cuda"), None, 0, None, None,
+                   None, 0, out, None)
     torch.cuda.synchronize()
     assert plan.device_status() == 0
 
