@@ -1,12 +1,14 @@
 """Benchmark of the GB300 multi-column embedding front end.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                [--workload inference|training|sequences-mean|sequences-padded|dynamic|tiny]
+                [--workload inference|inference-onehot|training|sequences-mean|
+                            sequences-padded|dynamic|dynamic-small|tiny]
 
 One JSON line on rank 0.  Default workload: the 1000-column inference forward
 (700 hash-mod + 300 bucketize columns, batch 512, dims 8..64, bags 1..20).
 A step is one pass of the workload's hot path over one batch:
-  inference            the fused forward;
+  inference            the fused forward (inference-onehot: the same
+                       columns with one value per bag, batch 4096);
   training, sequences  forward + backward (sort, run reduction) + Adagrad;
   dynamic              hash lookup-or-insert + forward + backward/Adagrad +
                        expiry sweep (one step of the 50-step stream).
@@ -143,6 +145,12 @@ def make_workload(name, columns=None):
         if columns:
             return synth.inference(n_cat=columns * 7 // 10, n_num=columns - columns * 7 // 10)
         return synth.inference()
+    if name == "inference-onehot":
+        # the inference columns with one value per bag, at batch 4096
+        if columns:
+            return synth.inference(n_cat=columns * 7 // 10, n_num=columns - columns * 7 // 10, B=4096,
+                                   one_hot=True)
+        return synth.inference(B=4096, one_hot=True)
     if name == "training":
         return synth.training(C=columns) if columns else synth.training()
     if name == "sequences-mean":
@@ -416,12 +424,13 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-# DRAM bytes per algorithmic byte of k_forward from the committed ncu capture
-# (profiles/k_forward_inference.md: 97.4 MB of DRAM traffic for 136.84 MB of
-# algorithmic bytes on the 200-column case).  A full launch is too large to
-# capture; its traffic is the same ratio times its algorithmic bytes.  Set to
-# None whenever k_forward changes until it is captured again.
-FORWARD_TRAFFIC_RATIO = {"inference": 97.4 / 136.84}
+# DRAM bytes per algorithmic byte of k_forward from the committed ncu captures
+# of the 200-column cases (97.41 MB of DRAM
+# traffic for 136.84 MB of algorithmic bytes with bags of 1..20 values,
+# 126.39 MB for 197.08 MB with one value per bag).  A full launch is too large
+# to capture; its traffic is the same ratio times its algorithmic bytes.  Set
+# to {} whenever k_forward changes until it is captured again.
+FORWARD_TRAFFIC_RATIO = {"inference": 97.41 / 136.84, "inference-onehot": 126.39 / 197.08}
 
 
 def traffic_estimate(workload, fbytes):

@@ -36,6 +36,7 @@ constexpr int kWarpElems = 512;    // values of short bags one warp chunk holds
 constexpr int kU = 4;              // row loads in flight per lane (halved for two float4 per lane)
 constexpr int kUA = 4;             // raw values in flight per lane in phase A
 constexpr int kUPool = 4;          // row loads in flight per lane when pooling short bags (8 spills)
+constexpr int kOneHotBags = 256;   // bags of one value each that one warp chunk copies
 constexpr int kFwdWarpsPerCta = kFwdThreads / kWarp;
 
 struct FwdArgs {
@@ -178,6 +179,41 @@ __device__ __forceinline__ int32_t col_transform(const ColMeta& m, int64_t v) {
   }
   if (m.transform == EMB_T_HASH_MOD) return (int32_t)mod_magic(splitmix64((uint64_t)v), m.mod);
   return (v >= 0 && v < m.num_rows) ? (int32_t)v : -1;
+}
+
+// Rows of kUA raw values of one column.  Bucketize: the kUA binary searches
+// advance together, so their boundary loads are in flight at the same time
+// (row = #{j : bnd[j] <= x}).
+__device__ __forceinline__ void transform_batch(const ColMeta& m, const int64_t (&raw)[kUA], int32_t (&rowv)[kUA]) {
+  if (m.transform == EMB_T_BUCKETIZE) {
+    int blo[kUA], blen[kUA];
+    float x[kUA];
+#pragma unroll
+    for (int u = 0; u < kUA; ++u) {
+      blo[u] = 0;
+      blen[u] = m.nb;
+      x[u] = __int_as_float((int32_t)raw[u]);
+    }
+    bool more = m.nb > 0;
+    while (more) {
+      more = false;
+#pragma unroll
+      for (int u = 0; u < kUA; ++u) {
+        if (blen[u] > 0) {
+          const int half = blen[u] >> 1;
+          const bool go = __ldg(m.bnd + blo[u] + half) <= x[u];
+          blo[u] = go ? blo[u] + half + 1 : blo[u];
+          blen[u] = go ? blen[u] - half - 1 : half;
+          more |= blen[u] > 0;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kUA; ++u) rowv[u] = blo[u];
+  } else {
+#pragma unroll
+    for (int u = 0; u < kUA; ++u) rowv[u] = col_transform(m, raw[u]);
+  }
 }
 
 __device__ __forceinline__ int32_t col_row(const ColMeta& m, const int64_t* ids, const float* fvals,
@@ -550,6 +586,76 @@ __device__ void warp_long_bag(const FwdArgs& a, int st, const ColMeta& m, const 
 }
 
 // ---------------------------------------------------------------------------
+// one-hot chunk: nb pooled bags of exactly one value each, the values
+// t0 .. t0 + nb - 1 of the stream.  A bag's result is its one row (times its
+// weight, or the default vector when the value is dropped), so the chunk is
+// a transform and a row copy: no offsets per bag, no reduction, and up to
+// kOneHotBags bags share each round trip.  WT: the launch carries weights
+// (records hold them); W: this column's value weights, or null.
+// ---------------------------------------------------------------------------
+template <int V, bool WT>
+__device__ void warp_onehot_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m, const float* W, int st,
+                                  int64_t t0, int nb, int b0, int glog) {
+  constexpr int U = kUPool / V;
+  const int lane = threadIdx.x & 31;
+  for (int k0 = 0; k0 < nb; k0 += 32 * kUA) {
+    int64_t raw[kUA];
+#pragma unroll
+    for (int u = 0; u < kUA; ++u) {
+      const int k = k0 + u * 32 + lane;
+      raw[u] = k < nb ? col_load(m, a.ids, a.fvals, t0 + k) : 0;
+    }
+    int32_t rowv[kUA];
+    transform_batch(m, raw, rowv);
+#pragma unroll
+    for (int u = 0; u < kUA; ++u) {
+      const int k = k0 + u * 32 + lane;
+      if (k < nb) {
+        ws.rows[k] = rowv[u];
+        if (a.rows_dbg || a.keys) record<WT>(a, st, t0 + k, rowv[u], m, pooled_gsrc(a, m, b0 + k));
+      }
+    }
+  }
+  __syncwarp();
+  const int G = 32 >> glog;
+  const int q = lane >> glog, sub = lane & ((1 << glog) - 1);
+  const float* E = m.weight;
+  for (int j = q; j < nb; j += G * U) {
+    float4 vals[U][V];
+    int r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int k = j + u * G;
+      r[u] = k < nb ? ws.rows[k] : -1;
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int f4 = sub + v * 32;
+        vals[u][v] = (r[u] >= 0 && f4 < m.dim4) ? ldg4(E + (int64_t)r[u] * m.dim + f4 * 4) : f4zero();
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int k = j + u * G;
+      if (k >= nb) break;
+      const int cnt = r[u] >= 0 ? 1 : 0;
+      const bool wt = WT && W != nullptr;
+      const float wk = (wt && cnt) ? __ldg(W + t0 + k) : 1.0f;
+      float* y = a.out + (int64_t)(b0 + k) * a.ldo + m.out_col;
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int f4 = sub + v * 32;
+        if (f4 < m.dim4) {
+          const float4 e = wt ? f4scale(wk, vals[u][v]) : vals[u][v];
+          *reinterpret_cast<float4*>(y + f4 * 4) = finish(m, e, cnt, f4);
+        }
+      }
+      if (a.inv_n && sub == 0 && m.pooling == EMB_POOL_MEAN) a.inv_n[pooled_gsrc(a, m, b0 + k)] = (float)cnt;
+    }
+  }
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
 // the kernel: one warp per element tile
 // ---------------------------------------------------------------------------
 template <bool WT>
@@ -621,17 +727,37 @@ __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int
     const bool padded = m.pooling == EMB_POOL_NONE_PADDED;
     int64_t lo = 0, hi = 0;
     int used = 0;
-    bool is_long = false;
+    bool is_long = false, one = false;
     if (lane < navail) {
       bool bad = false;
       lo = clamp_off(__ldg(offs + cur + lane), n, bad);
       hi = clamp_off(__ldg(offs + cur + lane + 1), n, bad);
       if (hi < lo) { hi = lo; bad = true; }
       if (bad) latch(a.status, EMB_ERR_BAD_INDEX);
+      one = !bad && hi - lo == 1;
       if (m.trunc > 0 && hi - lo > m.trunc) hi = lo + m.trunc;   // sequence truncation (pooled only)
       const int64_t len = hi - lo;
       is_long = (padded ? (int64_t)m.pad_len : len) > kLongBag;
       used = is_long ? 0 : (int)(padded ? (len < m.pad_len ? len : (int64_t)m.pad_len) : len);
+    }
+    if (!padded && __ballot_sync(kFull, one) == kFull) {
+      // ---- 32 bags of one value each: extend the run of one-value bags
+      //      (offsets that step by exactly 1) up to kOneHotBags bags ----
+      const int64_t lo0 = __shfl_sync(kFull, lo, 0);
+      const int lim = min(kOneHotBags, min(s_hi, (cl0 + 1) * a.batch) - cur);
+      int stop = lim;   // bags [0, stop) hold one value each
+#pragma unroll
+      for (int i = 0; i < kOneHotBags / 32 - 1; ++i) {
+        const int k = 33 + i * 32 + lane;   // offsets index after the chunk's first 32 bags
+        if (k <= lim && ((int64_t)__ldg(offs + cur + k) != lo0 + k || lo0 + k > n)) stop = min(stop, k - 1);
+      }
+      stop = __reduce_min_sync(kFull, stop);
+      const float* W = WT && m.pooling == EMB_POOL_SUM ? a.wts[st] : nullptr;
+      const int glog = lanes_log2(m.dim4);
+      if (m.dim4 > 32) warp_onehot_chunk<2, WT>(a, ws, m, W, st, lo0, stop, b0, glog);
+      else warp_onehot_chunk<1, WT>(a, ws, m, W, st, lo0, stop, b0, glog);
+      cur += stop;
+      continue;
     }
     int incl = used;
 #pragma unroll
@@ -669,37 +795,7 @@ __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int
         bi[u] = i;
       }
       int32_t rowv[kUA];
-      if (m.transform == EMB_T_BUCKETIZE) {
-        // the kUA binary searches advance together, so their boundary loads
-        // are in flight at the same time: row = #{j : bnd[j] <= x}
-        int blo[kUA], blen[kUA];
-        float x[kUA];
-#pragma unroll
-        for (int u = 0; u < kUA; ++u) {
-          blo[u] = 0;
-          blen[u] = m.nb;
-          x[u] = __int_as_float((int32_t)raw[u]);
-        }
-        bool more = m.nb > 0;
-        while (more) {
-          more = false;
-#pragma unroll
-          for (int u = 0; u < kUA; ++u) {
-            if (blen[u] > 0) {
-              const int half = blen[u] >> 1;
-              const bool go = __ldg(m.bnd + blo[u] + half) <= x[u];
-              blo[u] = go ? blo[u] + half + 1 : blo[u];
-              blen[u] = go ? blen[u] - half - 1 : half;
-              more |= blen[u] > 0;
-            }
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < kUA; ++u) rowv[u] = blo[u];
-      } else {
-#pragma unroll
-        for (int u = 0; u < kUA; ++u) rowv[u] = col_transform(m, raw[u]);
-      }
+      transform_batch(m, raw, rowv);
 #pragma unroll
       for (int u = 0; u < kUA; ++u) {
         const int k = k0 + u * 32 + lane;

@@ -173,7 +173,9 @@ def tiny(seed: int = 1001) -> Workload:
     return Workload("tiny", B, cols, tabs, offs, vals, lr=0.01, train=True, seed=seed)
 
 
-def inference(seed: int = 1002, n_cat: int = 700, n_num: int = 300, B: int = 512) -> Workload:
+def inference(seed: int = 1002, n_cat: int = 700, n_num: int = 300, B: int = 512,
+              one_hot: bool = False) -> Workload:
+    """one_hot: every bag holds exactly one value (the same columns)."""
     cols, tabs, offs, vals = [], [], [], []
     coin = np.random.default_rng([seed, 99])
     for c in range(n_cat + n_num):
@@ -182,6 +184,8 @@ def inference(seed: int = 1002, n_cat: int = 700, n_num: int = 300, B: int = 512
         pooling = "sum" if coin.random() < 0.5 else "mean"
         lens = r.integers(1, 21, B)
         lens[r.random(B) < 0.05] = 0
+        if one_hot:
+            lens = np.ones(B, np.int64)
         n = int(lens.sum())
         if c < n_cat:
             rows = int(log_uniform_int(r, 1e3, 1e6, 1)[0])
@@ -195,7 +199,8 @@ def inference(seed: int = 1002, n_cat: int = 700, n_num: int = 300, B: int = 512
             vals.append(r.standard_normal(n).astype(np.float32))
         tabs.append(TableSpec(rows, dim, seed * 10000 + c))
         offs.append(bag_offsets(lens))
-    return Workload("inference", B, cols, tabs, offs, vals, train=False, seed=seed)
+    return Workload("inference-onehot" if one_hot else "inference", B, cols, tabs, offs, vals, train=False,
+                    seed=seed)
 
 
 def training(seed: int = 1003, C: int = 200, B: int = 8192, rows_lo: float = 1e5,
@@ -269,6 +274,45 @@ def dynamic(seed: int = 1005, C: int = 100, B: int = 16384, dim: int = 32, steps
                    steps=steps, key_bits=key_bits, alpha=alpha, max_probes=128,
                    init_seed=seed, init_scale=0.01)
     return w
+
+
+def onehot_small(seed: int, C: int = 6, B: int | None = None, weighted: bool = False) -> Workload:
+    """Columns whose bags hold one value each, with runs broken here and
+    there by an empty bag or a bag of 2-3 values (sometimes cut back to one
+    by max_len), over every transform and pooling and dims up to 256."""
+    r = np.random.default_rng([seed, 17])
+    B = int(r.integers(200, 1500)) if B is None else B
+    cols, tabs, offs, vals = [], [], [], []
+    for c in range(C):
+        kind = str(r.choice(["identity", "hash_mod", "bucketize"]))
+        dim = int(r.choice([4, 8, 16, 32, 64, 128, 200, 256]))
+        pooling = str(r.choice(["sum", "mean", "sum", "mean", "padded"]))
+        lens = np.ones(B, np.int64)
+        breaks = r.random(B) < float(r.choice([0.0, 0.002, 0.02]))
+        lens[breaks] = r.choice(np.array([0, 2, 3]), int(breaks.sum()))
+        n = int(lens.sum())
+        bnd = None
+        if kind == "bucketize":
+            bnd = np.unique(np.sort(r.standard_normal(int(r.integers(1, 60))).astype(np.float32)))
+            rows = int(bnd.size) + 1
+            v = r.standard_normal(n).astype(np.float32)
+            v[r.random(n) < 0.02] = np.nan
+        else:
+            rows = int(r.integers(1, 5000))
+            if kind == "identity":
+                v = r.integers(-3, rows + 3, n, dtype=np.int64)
+            else:
+                v = r.integers(-2 ** 63, 2 ** 63 - 1, n, dtype=np.int64, endpoint=True)
+        default = r.standard_normal(dim).astype(np.float32) if r.random() < 0.4 else None
+        pad = int(r.integers(1, 4)) if pooling == "padded" else 0
+        trunc = 1 if pooling != "padded" and r.random() < 0.3 else 0
+        cols.append(ColumnSpec(kind, pooling, rows, dim, c, boundaries=bnd, default=default, pad_len=pad,
+                               max_len=trunc))
+        tabs.append(TableSpec(rows, dim, seed * 1000 + 500 + c))
+        offs.append(bag_offsets(lens))
+        vals.append(v)
+    wts = [r.uniform(-1.0, 2.0, int(o[-1])).astype(np.float32) for o in offs] if weighted else None
+    return Workload("onehot%d" % seed, B, cols, tabs, offs, vals, lr=0.05, seed=seed, weights=wts)
 
 
 def random_small(seed: int, C: int | None = None, B: int | None = None, train: bool = True,

@@ -107,6 +107,13 @@ def test_weighted_long_and_short_bags(dim):
     assert_close(ts.out.cpu().numpy(), ref, "weighted pooled output")
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_one_value_bags(seed):
+    """Training step over runs of one-value bags (records written by the
+    copy path), half the plans weighted."""
+    check_train_step(TrainStep(synth.onehot_small(50 + seed, weighted=seed % 2 == 0)))
+
+
 def test_shared_table_columns_merge():
     rng = np.random.default_rng(9)
     B = 500

@@ -64,6 +64,16 @@ def test_random_small_plans(seed):
     check_full(w, m, out, seq, rows)
 
 
+@pytest.mark.parametrize("seed", range(12))
+def test_one_value_bags(seed):
+    """Runs of one-value bags (copied without pooling, up to 256 bags per
+    warp chunk) broken by empty and longer bags at random places; half the
+    plans weighted."""
+    w = synth.onehot_small(seed, weighted=seed % 2 == 1)
+    m, plan, out, seq, rows = run_forward(w)
+    check_full(w, m, out, seq, rows)
+
+
 @pytest.mark.parametrize("dim", [4, 12, 20, 36, 60, 124, 128, 132, 200, 256])
 def test_every_dim_class(dim):
     """Lane-group widths 1..32 and the two-float4-per-lane path (dim > 128)."""
