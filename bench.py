@@ -538,7 +538,8 @@ def bench_plan(torch, sl, w, args, dev, stream, flush, train):
     fv = torch.from_numpy(fv_h).to(dev) if has_f else None
     f_off = torch.from_numpy(f_off_h).to(dev) if has_f else None
     n_all = n_ids + n_f
-    plan = sl.Plan(w.columns, tables, accs, max_batch=w.B, max_ids=max(n_all, 1) if train else 0, training=train)
+    plan = sl.Plan(w.columns, tables, accs, max_batch=w.B, max_ids=max(n_all, 1) if train else 0, training=train,
+                   backward=args.backward if train else "sort")
 
     rows_dbg = torch.empty(max(n_all, 1), dtype=torch.int64, device=dev)
     out, seq = plan.forward(w.B, ids, id_off, fv, f_off, rows_dbg=rows_dbg)
@@ -562,6 +563,7 @@ def bench_plan(torch, sl, w, args, dev, stream, flush, train):
         del dbg
         res["bbytes"] = backward_bytes(w, n_all, valid, n_unique, max(c.dim for c in w.columns))
         res["config"]["unique_rows_per_step"] = n_unique
+        res["config"]["backward"] = args.backward
 
     def body(i, marks):
         a, b = event_pair(torch)
@@ -588,10 +590,12 @@ def bench_plan(torch, sl, w, args, dev, stream, flush, train):
     res["times"] = {k: v for k, v in times.items() if k != "step"}
     res["ms_step"] = statistics.mean(times["step"])
     res["wall"] = wall
-    passes = 0
+    bwd_launches = 0
     if train:
-        passes = plan_sort_passes(plan)
-    res["launches"] = args.steps * (1 + (0 if not train else 3 + passes))
+        # sort: histogram, passes, run reduction, fixup; atomic: mark, count,
+        # scan, emit, scatter, update
+        bwd_launches = 6 if args.backward == "atomic" else 3 + plan_sort_passes(plan)
+    res["launches"] = args.steps * (1 + bwd_launches)
     if plan.device_status() != 0:
         raise SystemExit("device status after the timed steps")
 
@@ -693,7 +697,8 @@ def bench_dynamic(torch, sl, w, args, dev, stream, flush):
         max_n = max(max_n, allk.size)
     ht = sl.HashTable(ex["num_slots"], ex["row_capacity"], dim, ex["threshold"], ex["max_probes"],
                       ex["init_seed"], ex["init_scale"], max_n)
-    plan = sl.Plan(w.columns, [ht.weight], [ht.acc], max_batch=B, max_ids=max_n, training=True)
+    plan = sl.Plan(w.columns, [ht.weight], [ht.acc], max_batch=B, max_ids=max_n, training=True,
+                   backward=args.backward)
     out = torch.empty((B, plan.out_width), device=dev)
     G = synth.make_grad((B, plan.out_width), 77, dev)
     rows = torch.empty(max_n, dtype=torch.int64, device=dev)
@@ -749,8 +754,9 @@ def bench_dynamic(torch, sl, w, args, dev, stream, flush):
            "config": {"ids_per_step": n_last, "rows_gathered_per_step": valid, "num_slots": ex["num_slots"],
                       "row_capacity": ex["row_capacity"], "threshold": ex["threshold"], "ttl": ex["ttl"],
                       "stream_steps_timed": [t_first, state["t"] - 1],
-                      "cold_first_step_ms": first_step},
-           "launches": args.steps * (16 + 1 + (3 + plan_sort_passes(plan)) + 1)}
+                      "cold_first_step_ms": first_step, "backward": args.backward},
+           "launches": args.steps * (16 + 1 + (6 if args.backward == "atomic" else 3 + plan_sort_passes(plan))
+                                     + 1)}
     if ht.device_status() not in (0, 5) or plan.device_status() != 0:
         raise SystemExit("device status after the timed steps")
 
@@ -798,6 +804,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ceiling", action="store_true")
     ap.add_argument("--columns", type=int, default=None, help="number of columns (smaller profiling cases)")
+    ap.add_argument("--backward", default="sort", choices=["sort", "atomic"],
+                    help="training workloads: the sort-based backward or the atomic one")
     ap.add_argument("--graph", type=int, default=0,
                     help="also time this many back-to-back replays of one step captured in a CUDA graph")
     args = ap.parse_args()

@@ -106,6 +106,18 @@ typedef struct {
 /* Plan flags. */
 #define EMB_PLAN_TRAINING 1u  /* allocate the backward workspace; emb_forward
                                  then also records what the backward needs   */
+#define EMB_PLAN_ATOMIC_BACKWARD 2u
+                              /* with EMB_PLAN_TRAINING: emb_backward_update
+                                 merges equal rows inside each warp and adds
+                                 the sums to a compact gradient with global
+                                 atomics instead of sorting [RecIS §3.2
+                                 Algorithm 1, backward]; extra device memory:
+                                 4 B per table row (row -> slot map) plus
+                                 max_ids * max_dim * 4 B (compact gradient).
+                                 Same update; the summation order then depends
+                                 on scheduling (results within the fp32
+                                 summation bound, not bit-identical run to
+                                 run).                                        */
 
 typedef struct emb_plan_s* emb_plan;
 
@@ -207,7 +219,9 @@ typedef struct {
  * grad_out[b, col_off_c : col_off_c + dim_c] (scale w_r for SUM -- 1 without
  * weights --, 1/n_valid for MEAN), or grad_seq[b, t, :] of its padded column.  The contributions are
  * radix-sorted by global row, the runs give the unique rows and counts, each
- * unique row's gradient g is summed by exactly one writer, then
+ * unique row's gradient g is summed by exactly one writer (atomic plans: a
+ * bitmap of touched rows gives them in ascending order and g is accumulated
+ * with atomics), then
  *   acc += g*g;  w -= lr * g / (sqrt(acc) + eps)
  * element-wise in fp32 (torch.optim.Adagrad with lr_decay = weight_decay = 0).
  * Rows not touched by the batch are not read or written.

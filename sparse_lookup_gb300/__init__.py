@@ -28,6 +28,7 @@ STATUS = {
 TRANSFORM = {"identity": 0, "hash_mod": 1, "bucketize": 2, "rows_given": 3}
 POOLING = {"sum": 0, "mean": 1, "padded": 2}
 PLAN_TRAINING = 1
+PLAN_ATOMIC_BACKWARD = 2
 
 
 class EmbError(RuntimeError):
@@ -250,9 +251,12 @@ class Plan:
     transform, pooling, num_rows, dim, table, boundaries, default, pad_len
     (e.g. synth.ColumnSpec).  ``weights[t]`` / ``accs[t]`` are the device
     tables of physical table t.  The device copies of boundaries and default
-    vectors are owned here and live as long as the plan."""
+    vectors are owned here and live as long as the plan.  backward: "sort"
+    (radix sort + run reduction, deterministic) or "atomic" (warp merge +
+    atomics into a compact gradient)."""
 
-    def __init__(self, columns, weights, accs=None, max_batch=1, max_ids=0, training=False, device="cuda"):
+    def __init__(self, columns, weights, accs=None, max_batch=1, max_ids=0, training=False, device="cuda",
+                 backward="sort"):
         import torch
         self.columns = list(columns)
         self.training = training
@@ -279,7 +283,11 @@ class Plan:
             if accs is not None:
                 d.adagrad_acc = accs[c.table].data_ptr()
             descs.append(d)
-        self.handle = emb_plan_create(descs, max_batch, max_ids, PLAN_TRAINING if training else 0)
+        if backward not in ("sort", "atomic"):
+            raise ValueError("backward: 'sort' or 'atomic'")
+        flags = (PLAN_TRAINING if training else 0) | (PLAN_ATOMIC_BACKWARD if backward == "atomic" else 0)
+        self.backward = backward
+        self.handle = emb_plan_create(descs, max_batch, max_ids, flags)
         self.info = emb_plan_info(self.handle, len(descs))
         self.out_width = self.info["out_width"]
         self.seq_per_bag = self.info["seq_floats_per_bag"]
@@ -325,7 +333,7 @@ class Plan:
                  uniq_table=torch.empty(cap, dtype=torch.int32, device=dev),
                  uniq_row=torch.empty(cap, dtype=torch.int64, device=dev),
                  counts=torch.empty(cap, dtype=torch.int32, device=dev),
-                 agg_grad=torch.empty((cap, self.max_dim), dtype=torch.float32, device=dev))
+                 agg_grad=torch.zeros((cap, self.max_dim), dtype=torch.float32, device=dev))
         dbg = EmbBackwardDebug(*[t[k].data_ptr() for k in ("n_unique", "uniq_table", "uniq_row", "counts",
                                                            "agg_grad")])
         emb_backward_update(self.handle, grad_out, grad_seq, lr, eps, stream, dbg)

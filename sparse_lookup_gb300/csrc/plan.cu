@@ -28,6 +28,13 @@ void free_plan(emb_plan_s* p) {
   cudaFree(w.vals[1]);
   cudaFree(w.inv_n);
   cudaFree(w.rec_src);
+  cudaFree(w.touched);
+  cudaFree(w.bit_part);
+  cudaFree(w.n_uniq);
+  cudaFree(w.uniq);
+  cudaFree(w.slot_of);
+  cudaFree(w.cgrad);
+  cudaFree(w.ucount);
   cudaFree(w.hist);
   cudaFree(w.run_head);
   cudaFree(w.head_pos);
@@ -74,8 +81,9 @@ extern "C" emb_status emb_plan_create(const emb_column_desc* cols, int32_t n_col
   if (!out) return EMB_ERR_INVALID_ARG;
   *out = nullptr;
   if (!cols || n_cols < 1 || n_cols > 65535 || max_batch < 1) return EMB_ERR_INVALID_ARG;
-  if (flags & ~EMB_PLAN_TRAINING) return EMB_ERR_INVALID_ARG;
+  if (flags & ~(EMB_PLAN_TRAINING | EMB_PLAN_ATOMIC_BACKWARD)) return EMB_ERR_INVALID_ARG;
   const bool training = (flags & EMB_PLAN_TRAINING) != 0;
+  if ((flags & EMB_PLAN_ATOMIC_BACKWARD) && !training) return EMB_ERR_INVALID_ARG;
   if ((int64_t)n_cols * max_batch >= (int64_t(1) << 31)) return EMB_ERR_UNSUPPORTED;
   if (training && (max_ids < 0 || max_ids >= (int64_t(1) << 30))) return EMB_ERR_UNSUPPORTED;
   for (int32_t c = 0; c < n_cols; ++c) {
@@ -225,6 +233,21 @@ extern "C" emb_status emb_plan_create(const emb_column_desc* cols, int32_t n_col
     if (e == cudaSuccess) e = dmalloc(&w.partial, (size_t)w.n_units_max * 2 * (p->max_dim / 4), &total);
     if (e == cudaSuccess) e = dmalloc(&w.part_pos, (size_t)w.n_units_max * 2, &total);
     if (e == cudaSuccess) e = dmalloc(&w.part_thru, (size_t)w.n_units_max, &total);
+    if (e == cudaSuccess && (flags & EMB_PLAN_ATOMIC_BACKWARD)) {
+      p->atomic_bwd = true;
+      const size_t words = ((size_t)p->key_total + 31) / 32;
+      const size_t cg = (size_t)n * p->max_dim;
+      e = dmalloc(&w.touched, words, &total);
+      if (e == cudaSuccess) e = cudaMemset(w.touched, 0, sizeof(uint32_t) * std::max<size_t>(words, 1));
+      if (e == cudaSuccess) e = dmalloc(&w.bit_part, (words + 1023) / 1024, &total);
+      if (e == cudaSuccess) e = dmalloc(&w.n_uniq, 1, &total);
+      if (e == cudaSuccess) e = dmalloc(&w.uniq, n, &total);
+      if (e == cudaSuccess) e = dmalloc(&w.slot_of, (size_t)p->key_total, &total);
+      if (e == cudaSuccess) e = dmalloc(&w.cgrad, cg, &total);
+      if (e == cudaSuccess) e = cudaMemset(w.cgrad, 0, sizeof(float) * std::max<size_t>(cg, 1));
+      if (e == cudaSuccess) e = dmalloc(&w.ucount, n, &total);
+      if (e == cudaSuccess) e = cudaMemset(w.ucount, 0, sizeof(uint32_t) * n);
+    }
   }
   p->ws.bytes = total;
   if (e == cudaSuccess) p->fwd_ctas_per_sm = forward_ctas_per_sm();
@@ -292,6 +315,7 @@ extern "C" emb_status emb_backward_update(emb_plan p, const float* grad_out, con
   if (p->last_batch > 0 && p->out_width > 0 && !grad_out) return EMB_ERR_INVALID_ARG;
   if (p->last_batch > 0 && p->n_padded > 0 && !grad_seq) return EMB_ERR_INVALID_ARG;
   if (!(lr == lr) || !(eps == eps)) return EMB_ERR_INVALID_ARG;
+  if (p->atomic_bwd) return launch_backward_atomic(p, grad_out, grad_seq, lr, eps, (cudaStream_t)stream, dbg);
   return launch_backward(p, grad_out, grad_seq, lr, eps, (cudaStream_t)stream, dbg);
 }
 

@@ -41,6 +41,14 @@ struct Workspace {
   float4* partial = nullptr;       // [n_units][2][max_dim/4] cut-run partial sums
   int32_t* part_pos = nullptr;     // [n_units][2] run boundaries of those partials
   uint8_t* part_thru = nullptr;    // [n_units] CTA lies inside one continuing run
+  // atomic backward (EMB_PLAN_ATOMIC_BACKWARD)
+  uint32_t* touched = nullptr;     // [ceil(rows / 32)] bitmap of the rows a step touches (kept clear)
+  uint32_t* bit_part = nullptr;    // per 1024-word block: set bits, then their exclusive prefix
+  int64_t* n_uniq = nullptr;       // [1] touched rows of the step
+  uint32_t* uniq = nullptr;        // [max_ids] touched global rows, ascending (slot -> row)
+  uint32_t* slot_of = nullptr;     // [rows] global row -> slot, valid for the step's touched rows
+  float* cgrad = nullptr;          // [max_ids, max_dim] compact gradient (kept zero between steps)
+  uint32_t* ucount = nullptr;      // [max_ids] debug: contributions per slot (kept zero)
   int64_t max_tiles = 0;
   int64_t n_units_max = 0;
   size_t bytes = 0;
@@ -54,6 +62,7 @@ struct emb_plan_s {
   int64_t max_ids = 0;
   uint32_t flags = 0;
   bool training = false;
+  bool atomic_bwd = false;             // backward by atomics into a compact gradient
   std::vector<emb_column_desc> cols;
   std::vector<emb::ColMeta> meta_h;
   std::vector<int32_t> col_table;
@@ -99,7 +108,7 @@ inline emb_status cuda_status(cudaError_t e) {
     if (_e != cudaSuccess) return ::emb::cuda_status(_e); \
   } while (0)
 
-// Launch-side entry points implemented in forward.cu / backward.cu.
+// Launch-side entry points implemented in forward.cu / backward.cu / atomic.cu.
 emb_status launch_forward(emb_plan_s* p, int32_t batch, const int64_t* ids, const int32_t* id_offsets,
                           const float* id_weights, int64_t n_ids, const float* fvals, const int32_t* f_offsets,
                           const float* f_weights, int64_t n_fvals, float* out, float* seq_out, int64_t* rows_dbg,
@@ -109,5 +118,7 @@ int forward_ctas_per_sm();
 emb_status launch_backward(emb_plan_s* p, const float* grad_out, const float* grad_seq,
                            float lr, float eps, cudaStream_t stream,
                            const emb_backward_debug* dbg);
+emb_status launch_backward_atomic(emb_plan_s* p, const float* grad_out, const float* grad_seq, float lr, float eps,
+                                  cudaStream_t stream, const emb_backward_debug* dbg);
 
 }  // namespace emb

@@ -128,7 +128,7 @@ class TrainStep:
     """One forward + backward/Adagrad step of a workload on the device through
     the C ABI, and the oracle's result for the same inputs."""
 
-    def __init__(self, w, acc_init=0.0, grad_seed=77, device="cuda"):
+    def __init__(self, w, acc_init=0.0, grad_seed=77, device="cuda", backward="sort"):
         import torch
         import sparse_lookup_gb300 as sl
         self.w = w
@@ -137,7 +137,8 @@ class TrainStep:
         self.W0 = m.host_tables()
         self.A0 = [None if a is None else a.cpu().numpy() for a in m.accs]
         n = m.n_ids + m.n_f
-        self.plan = sl.Plan(w.columns, m.tables, m.accs, max_batch=max(w.B, 1), max_ids=max(n, 1), training=True)
+        self.plan = sl.Plan(w.columns, m.tables, m.accs, max_batch=max(w.B, 1), max_ids=max(n, 1), training=True,
+                            backward=backward)
         self.out, self.seq = self.plan.forward(w.B, m.ids, m.id_off, m.fv, m.f_off, id_weights=m.idw,
                                                f_weights=m.fw)
         width = self.plan.out_width
@@ -149,6 +150,24 @@ class TrainStep:
         torch.cuda.synchronize()
         self.status = self.plan.device_status()
         self.info = self.plan.info
+
+    def again(self, grad_seed):
+        """Another step on the same plan and inputs with a new upstream
+        gradient, from the tables as the previous step left them."""
+        import torch
+        w, m = self.w, self.m
+        self.W0 = m.host_tables()
+        self.A0 = [None if a is None else a.cpu().numpy() for a in m.accs]
+        self.out, self.seq = self.plan.forward(w.B, m.ids, m.id_off, m.fv, m.f_off, id_weights=m.idw,
+                                               f_weights=m.fw)
+        width = self.plan.out_width
+        self.G = synth.make_grad((w.B, max(width, 1)), grad_seed, "cuda")[:, :width].contiguous()
+        if self.plan.seq_per_bag:
+            self.Gseq = synth.make_grad((w.B * self.plan.seq_per_bag,), grad_seed + 1, "cuda")
+        self.dbg = self.plan.backward_update(self.G if width else None, self.Gseq, w.lr, w.eps, debug=True)
+        torch.cuda.synchronize()
+        self.status = self.plan.device_status()
+        return self
 
     def oracle(self):
         w = self.w

@@ -86,5 +86,11 @@ def test_plan_create_rejects_bad_arguments_on_host(L):
     with pytest.raises(sl.EmbError) as e:                          # training without accumulator
         sl.emb_plan_create([d], 4, 100, sl.PLAN_TRAINING)
     assert e.value.status == 1
+    with pytest.raises(sl.EmbError) as e:                          # atomic backward without training
+        sl.emb_plan_create([d], 4, 100, sl.PLAN_ATOMIC_BACKWARD)
+    assert e.value.status == 1
+    with pytest.raises(sl.EmbError) as e:                          # unknown flag bit
+        sl.emb_plan_create([d], 4, 100, 4)
+    assert e.value.status == 1
     with pytest.raises(sl.EmbError):
         sl.emb_plan_create([d], 0, 0, 0)                           # batch 0
