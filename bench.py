@@ -499,7 +499,9 @@ def run_ours(args):
         ab = res["bbytes"] / (b_ms / 1e3) / 1e9
         line["roofline_backward"] = {"bound": "hbm", "achieved": ab, "peak": peak, "unit": "GB/s", "frac": ab / peak,
                                      "bytes_per_call": res["bbytes"], "call_ms": b_ms,
-                                     "kernels": "digit histogram, radix passes, run reduction + Adagrad, fixup"}
+                                     "kernels": ("row bitmap, slot compaction, warp-merged atomics, Adagrad pass"
+                                                 if args.backward == "atomic" else
+                                                 "digit histogram, radix passes, run reduction + Adagrad, fixup")}
     if res.get("ceiling"):
         line["gather_ceiling"] = res["ceiling"]
         line["gather_ceiling"]["frac_forward"] = achieved / res["ceiling"]["mix_gbs"]

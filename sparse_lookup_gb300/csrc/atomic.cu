@@ -39,7 +39,8 @@ namespace {
 
 constexpr int kBitsBlock = 1024;     // bitmap words per counting / emitting block
 constexpr int kAtomThreads = 256;
-constexpr int kAtomU = 4;            // gradient rows in flight per lane (halved for two float4 per lane)
+constexpr int kAtomU = 8;            // gradient rows in flight per lane (halved for two float4 per lane)
+constexpr uint32_t kNoSlot = 0xffffffffu;
 constexpr uint32_t kOffPadA = 0x80000000u;   // compact source offset: into the padded gradient
 
 struct AtomArgs {
@@ -130,7 +131,7 @@ __global__ void __launch_bounds__(kBitsBlock) k_bits_emit(uint32_t* touched, int
 }
 
 struct __align__(16) AtomRec {
-  uint32_t key;
+  uint32_t slot;    // compact gradient row (kNoSlot: dropped contribution)
   uint32_t off;     // float4 offset of the gradient row (kOffPadA: in the padded gradient)
   float scale;
   uint32_t d4;
@@ -165,9 +166,8 @@ __device__ __forceinline__ void atom_decode(const AtomArgs& a, uint32_t key, uin
 }
 
 template <int V>
-__device__ __forceinline__ void atom_flush(const AtomArgs& a, uint32_t key, uint32_t d4, const float4 (&acc)[V],
+__device__ __forceinline__ void atom_flush(const AtomArgs& a, uint32_t slot, uint32_t d4, const float4 (&acc)[V],
                                            int cnt, int sub) {
-  const uint32_t slot = __ldg(a.slot_of + key);
   float* dst = a.cgrad + (int64_t)slot * a.cld;
 #pragma unroll
   for (int v = 0; v < V; ++v) {
@@ -193,17 +193,22 @@ __global__ void __launch_bounds__(kAtomThreads) k_atomic_scatter(const AtomArgs 
   for (int64_t base = (int64_t)blockIdx.x * kAtomThreads + (threadIdx.x & ~31); base < a.n; base += stride) {
     const int64_t i = base + lane;
     AtomRec r;
-    r.key = a.sentinel;
+    r.slot = kNoSlot;
     r.off = 0u;
     r.scale = 0.0f;
     r.d4 = 0u;
+    uint32_t key = a.sentinel;
     if (i < a.n) {
-      r.key = __ldg(a.keys + i);
-      if (r.key != a.sentinel) atom_decode(a, r.key, __ldg(a.vals + i), r, lkey, ld4);
+      key = __ldg(a.keys + i);
+      const uint32_t val = __ldg(a.vals + i);
+      if (key != a.sentinel) {
+        r.slot = __ldg(a.slot_of + key);   // in flight with the decoding loads
+        atom_decode(a, key, val, r, lkey, ld4);
+      }
     }
     // equal rows of the 32 contributions: groups ordered by their first lane,
     // members by lane
-    const unsigned peers = __match_any_sync(kFull, r.key);
+    const unsigned peers = __match_any_sync(kFull, key);
     const int leader = __ffs(peers) - 1;
     const int gsize = leader == lane ? __popc(peers) : 0;
     int incl = gsize;
@@ -221,14 +226,14 @@ __global__ void __launch_bounds__(kAtomThreads) k_atomic_scatter(const AtomArgs 
     float4 acc[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-    uint32_t ckey = a.sentinel, cd4 = 0;
+    uint32_t cslot = kNoSlot, cd4 = 0;
     int cnt = 0;
     for (int j = 0; j < R; j += U) {
       float4 g[U][V];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const AtomRec e = j + u < R ? wr[q * R + j + u] : AtomRec{a.sentinel, 0u, 0.0f, 0u};
-        const bool ok = e.key != a.sentinel;
+        const AtomRec e = j + u < R ? wr[q * R + j + u] : AtomRec{kNoSlot, 0u, 0.0f, 0u};
+        const bool ok = e.slot != kNoSlot;
         const float* src = (e.off & kOffPadA) ? a.grad_seq + (int64_t)(e.off & ~kOffPadA) * 4
                                               : a.grad_out + (int64_t)e.off * 4;
 #pragma unroll
@@ -243,9 +248,9 @@ __global__ void __launch_bounds__(kAtomThreads) k_atomic_scatter(const AtomArgs 
       for (int u = 0; u < U; ++u) {
         if (j + u >= R) break;
         const AtomRec& e = wr[q * R + j + u];
-        if (e.key != ckey) {
-          if (ckey != a.sentinel) atom_flush<V>(a, ckey, cd4, acc, cnt, sub);
-          ckey = e.key;
+        if (e.slot != cslot) {
+          if (cslot != kNoSlot) atom_flush<V>(a, cslot, cd4, acc, cnt, sub);
+          cslot = e.slot;
           cd4 = e.d4;
           cnt = 0;
 #pragma unroll
@@ -261,7 +266,7 @@ __global__ void __launch_bounds__(kAtomThreads) k_atomic_scatter(const AtomArgs 
         }
       }
     }
-    if (ckey != a.sentinel) atom_flush<V>(a, ckey, cd4, acc, cnt, sub);
+    if (cslot != kNoSlot) atom_flush<V>(a, cslot, cd4, acc, cnt, sub);
     __syncwarp();
   }
 }
