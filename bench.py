@@ -481,7 +481,9 @@ def run_ours(args):
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": dict(res["config"], workload=w.name, batch=w.B, columns=len(w.columns),
-                       l2="flushed between steps (2x L2 write, outside events)",
+                       l2=("not flushed: steps pipelined; the table's slots and rows exceed L2"
+                           if getattr(args, "pipeline", False) else
+                           "flushed between steps (2x L2 write, outside events)"),
                        parallelism="replicas" if world > 1 else "1 GPU"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic_estimate(w.name, res["fbytes"]),
@@ -683,7 +685,7 @@ def bench_dynamic(torch, sl, w, args, dev, stream, flush):
     ex = w.extra
     C, B = len(w.columns), w.B
     dim = w.columns[0].dim
-    nsteps = max(3, args.warmup) + args.steps
+    nsteps = max(3, args.warmup) + args.steps * (2 if args.pipeline else 1)
     # every step's keys resident on the device before timing
     batches = []
     max_n = 0
@@ -742,21 +744,26 @@ def bench_dynamic(torch, sl, w, args, dev, stream, flush):
     clk.start()
     time.sleep(0.3)
     t_first = state["t"]
-    times, wall = timed_steps(torch, args.steps, stream, flush, body)
+    if args.pipeline:
+        times, wall = pipelined_steps(torch, ht, plan, batches, state, w, args, stream, G, out)
+    else:
+        times, wall = timed_steps(torch, args.steps, stream, flush, body)
     clocks = clk.stop()
     # valid rows and bytes, from the library's own rows of the last timed step
     n_last = batches[state["t"] - 1][1].numel()
-    r = rows[:n_last].cpu().numpy()
+    r = (state["rows_last"] if "rows_last" in state else rows[:n_last]).cpu().numpy()
     valid = int((r >= 0).sum())
     width = plan.out_width
     fbytes = (C * (B + 1) * 4 + n_last * 8 + valid * 4 * dim + B * 4 * width)
     res = {"rows_per_step": valid, "fbytes": fbytes, "clocks": clocks,
            "times": {k: v for k, v in times.items() if k != "step"},
-           "ms_step": statistics.mean(times["step"]), "wall": wall,
+           "ms_step": statistics.mean(times["step"] if "step" in times else times["pipelined_step"]), "wall": wall,
            "config": {"ids_per_step": n_last, "rows_gathered_per_step": valid, "num_slots": ex["num_slots"],
                       "row_capacity": ex["row_capacity"], "threshold": ex["threshold"], "ttl": ex["ttl"],
                       "stream_steps_timed": [t_first, state["t"] - 1],
-                      "cold_first_step_ms": first_step, "backward": args.backward},
+                      "cold_first_step_ms": first_step, "backward": args.backward,
+                      "pipeline": bool(args.pipeline),
+                      "sequential_unflushed_ms": state.get("sequential_unflushed_ms")},
            "launches": args.steps * (16 + 1 + (6 if args.backward == "atomic" else 3 + plan_sort_passes(plan))
                                      + 1)}
     if ht.device_status() not in (0, 5) or plan.device_status() != 0:
@@ -796,6 +803,60 @@ def bench_dynamic(torch, sl, w, args, dev, stream, flush):
     return res
 
 
+def pipelined_steps(torch, ht, plan, batches, state, w, args, stream, G, out):
+    """K dynamic-table steps through DynamicPipeline: the lookup of step t+1
+    and the expiry of step t on a low-priority stream beside step t's
+    backward.  Steps overlap, so L2 is not flushed between them (the table's
+    slots and rows are larger than L2); the time is the whole window / K,
+    pipeline fill and drain included."""
+    from sparse_lookup_gb300.pipeline import DynamicPipeline
+    B = w.B
+    max_n = max(b[1].numel() for b in batches)
+    ttl = w.extra["ttl"]
+    k = args.steps
+    # the same steps in order on one stream, unflushed, for comparison
+    rows = torch.empty(max_n, dtype=torch.int64, device=out.device)
+    t0 = state["t"]
+    torch.cuda.synchronize()
+    a, b = event_pair(torch)
+    a.record(stream)
+    for t in range(t0, t0 + k):
+        tids, keys, off = batches[t][:3]
+        n = keys.numel()
+        ht.lookup_or_insert(tids, keys, t, rows_out=rows[:n])
+        plan.forward(B, rows[:n], off, None, None, out=out)
+        plan.backward_update(G, None, w.lr, w.eps)
+        ht.evict_expired(t, ttl)
+    b.record(stream)
+    torch.cuda.synchronize()
+    state["sequential_unflushed_ms"] = a.elapsed_time(b) / k
+    pipe = DynamicPipeline(ht, plan, ttl, B, max_n)
+    t0 = t0 + k
+    sync_ranks(torch)
+    torch.cuda.synchronize()
+    a, b = event_pair(torch)
+    wall0 = time.perf_counter()
+    a.record(stream)
+    pipe.prefetch(t0, batches[t0][0], batches[t0][1])
+    fwd = []
+    for t in range(t0, t0 + k):
+        fwd.append(event_pair(torch))
+        pipe.forward(t, batches[t][2], out, events=fwd[-1])
+        if t + 1 < t0 + k:
+            pipe.prefetch(t + 1, batches[t + 1][0], batches[t + 1][1])
+        pipe.backward(G, w.lr, w.eps)
+    pipe.finish()
+    b.record(stream)
+    torch.cuda.synchronize()
+    sync_ranks(torch)
+    wall = time.perf_counter() - wall0
+    state["t"] = t0 + k
+    # the library's rows of the last step, for the valid-row count
+    n_last = batches[t0 + k - 1][1].numel()
+    state["rows_last"] = pipe.rows[(t0 + k - 1) % 2][:n_last]
+    return {"pipelined_step": [a.elapsed_time(b) / k] * k, "fwd": [x.elapsed_time(y) for x, y in fwd]}, wall
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -806,6 +867,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ceiling", action="store_true")
     ap.add_argument("--columns", type=int, default=None, help="number of columns (smaller profiling cases)")
+    ap.add_argument("--pipeline", action="store_true",
+                    help="dynamic workload: pipelined steps (next lookup beside this backward)")
     ap.add_argument("--backward", default="sort", choices=["sort", "atomic"],
                     help="training workloads: the sort-based backward or the atomic one")
     ap.add_argument("--graph", type=int, default=0,
