@@ -41,7 +41,14 @@ class _Col(ctypes.Structure):
         ("max_len", c_int32),
         ("reserved", c_int32),
         ("weights", c_void_p),
+        ("table_dtype", c_int32),
+        ("reserved2", c_int32),
+        ("row_scale", c_void_p),
     ]
+
+
+TABLE_DTYPE = {"f32": 0, "bf16": 1, "f16": 2, "i8": 3}
+_TABLE_NP = {"f32": np.float32, "bf16": np.uint16, "f16": np.uint16, "i8": np.int8}
 
 
 _lib = None
@@ -101,9 +108,11 @@ def _ptr_array(arrs):
     return arr
 
 
-def _cols(cols, weights=None):
+def _cols(cols, weights=None, table_dtypes=None, row_scales=None):
     """ctypes column array; pooled columns get consecutive out_col offsets;
-    weights: optional per-column fp32 value weights (None entries: none).
+    weights: optional per-column fp32 value weights (None entries: none);
+    table_dtypes / row_scales: optional per physical table storage type
+    ("f32", "bf16", "f16", "i8") and int8 row scales.
     Returns (array, keep-alive list, pooled width)."""
     arr = (_Col * max(1, len(cols)))()
     keep = []
@@ -126,6 +135,12 @@ def _cols(cols, weights=None):
         arr[i].default_vec = None if dft is None else dft.ctypes.data
         arr[i].out_col = off if c.pooling != "padded" else 0
         arr[i].max_len = int(getattr(c, "max_len", 0) or 0)
+        dt = "f32" if table_dtypes is None else table_dtypes[c.table]
+        arr[i].table_dtype = TABLE_DTYPE[dt]
+        if dt == "i8":
+            sc = np.ascontiguousarray(row_scales[c.table], np.float32)
+            keep.append(sc)
+            arr[i].row_scale = sc.ctypes.data
         if c.pooling != "padded":
             off += int(c.dim)
     return arr, keep, off
@@ -161,16 +176,20 @@ def column_rows(col, values) -> np.ndarray:
     return out[:n]
 
 
-def forward(cols, B, offsets, values, tables, want_rows=False, weights=None):
+def forward(cols, B, offsets, values, tables, want_rows=False, weights=None, table_dtypes=None,
+            row_scales=None):
     """Pooled output [B, sum(dim of pooled cols)] (fp32), padded outputs
     (list, None for pooled columns) and optionally the rows per column.
     weights: optional per-column value weights, used by SUM columns.
+    table_dtypes: optional storage type per physical table ("f32", "bf16" or
+    "f16" as uint16 bit patterns, "i8" with row_scales[t] per row).
     RecIS §3.2 Algorithm 1 (forward); RECom guards and default fill."""
-    arr, keep, width = _cols(cols, weights)
+    arr, keep, width = _cols(cols, weights, table_dtypes, row_scales)
     C = len(cols)
     offs = [np.ascontiguousarray(o, np.int32) for o in offsets]
     ids, fv = _values(cols, values)
-    tabs = [np.ascontiguousarray(t, np.float32) for t in tables]
+    tabs = [np.ascontiguousarray(t, _TABLE_NP["f32" if table_dtypes is None else table_dtypes[i]])
+            for i, t in enumerate(tables)]
     out = np.zeros((B, max(width, 1)), np.float32)
     seq = [np.zeros((B, c.pad_len, c.dim), np.float32) if c.pooling == "padded" else None for c in cols]
     rows = [np.empty(max(int(o[B]), 1), np.int64) for o in offs] if want_rows else None

@@ -77,7 +77,50 @@ typedef struct {
                                  (sequence truncation; 0 = all)               */
     int32_t reserved;
     const float* weights;     /* SUM: per-value weights w_r (NULL = all 1)     */
+    int32_t table_dtype;      /* ORC_DT_*: how the table's elements are stored */
+    int32_t reserved2;
+    const float* row_scale;   /* ORC_DT_I8: [num_rows] scale of each row        */
 } orc_col;
+
+/* Element storage of a table [the RecIS evaluation lists an int8 table beside
+ * fp32 ones, Table 3; the reading here: bf16, IEEE binary16, or int8 with
+ * one fp32 scale per row]. */
+enum { ORC_DT_F32 = 0, ORC_DT_BF16 = 1, ORC_DT_F16 = 2, ORC_DT_I8 = 3 };
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction
+ * bits; exponent 0 holds zero and the subnormals (fraction x 2^-24),
+ * exponent 31 infinity (fraction 0) and NaN. */
+static double half_value(uint16_t h)
+{
+    const int sign = h >> 15, ex = (h >> 10) & 31, fr = h & 1023;
+    double v;
+    if (ex == 0) v = ldexp((double)fr, -24);
+    else if (ex == 31) v = fr ? NAN : INFINITY;
+    else v = ldexp((double)(fr | 1024), ex - 25);
+    return sign ? -v : v;
+}
+
+/* bfloat16: the upper 16 bits of an IEEE binary32 (same sign and exponent,
+ * 7 fraction bits). */
+static double bf16_value(uint16_t h)
+{
+    const uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Element d of row r of the column's table, exactly (int8: scale * q). */
+static double table_value(const orc_col* c, const void* E, int64_t r, int32_t d)
+{
+    const int64_t e = r * c->dim + d;
+    switch (c->table_dtype) {
+    case ORC_DT_BF16: return bf16_value(((const uint16_t*)E)[e]);
+    case ORC_DT_F16: return half_value(((const uint16_t*)E)[e]);
+    case ORC_DT_I8: return (double)c->row_scale[r] * (double)((const int8_t*)E)[e];
+    default: return (double)((const float*)E)[e];
+    }
+}
 
 /* Weight of value t of a column: w_t for a weighted SUM column [RecIS §3.2,
  * Algorithm 1: y_s = sum_r w_r E[idx_r], and the backward passes w_r G[s]
@@ -164,7 +207,8 @@ static int check_offsets(const int32_t* off, int32_t B)
 /* Forward of all columns.
  * offsets[c]: int32 [B+1] CSR of column c (relative to its own values);
  * ids[c] (int64) or fvals[c] (fp32, BUCKETIZE) hold its values;
- * tables[t]: row-major fp32 [num_rows, dim] of physical table t;
+ * tables[t]: row-major [num_rows, dim] of physical table t, elements stored
+ *   as the columns' table_dtype says (fp32 unless stated);
  * out: [B, ldo] fp32, column c pooled into out[b*ldo + out_col + d];
  * seq_out[c]: PADDED columns, [B, pad_len, dim]; rows_out[c]: optional rows.
  *
@@ -176,7 +220,7 @@ static int check_offsets(const int32_t* off, int32_t B)
  * given a default; RecIS §3.2: an empty segment pools to zero]. */
 int orc_forward(const orc_col* cols, int32_t C, int32_t B,
                 const int32_t* const* offsets, const int64_t* const* ids,
-                const float* const* fvals, const float* const* tables,
+                const float* const* fvals, const void* const* tables,
                 float* out, int64_t ldo, float* const* seq_out,
                 int64_t* const* rows_out)
 {
@@ -191,7 +235,7 @@ int orc_forward(const orc_col* cols, int32_t C, int32_t B,
         if (!rows || !S) { free(rows); free(S); return ORC_ERR_OOM; }
         orc_column_rows(c, n, ids ? ids[ci] : NULL, fvals ? fvals[ci] : NULL, rows);
         if (rows_out && rows_out[ci]) memcpy(rows_out[ci], rows, sizeof(int64_t) * (size_t)n);
-        const float* E = tables[c->table];
+        const void* E = tables[c->table];
         for (int32_t b = 0; b < B; ++b) {
             int64_t lo = off[b], hi = off[b + 1];
             if (c->pooling == ORC_PADDED) {
@@ -199,7 +243,7 @@ int orc_forward(const orc_col* cols, int32_t C, int32_t B,
                 for (int32_t t = 0; t < c->pad_len; ++t) {
                     int64_t r = (lo + t < hi) ? rows[lo + t] : -1;
                     for (int32_t d = 0; d < c->dim; ++d)
-                        y[(int64_t)t * c->dim + d] = (r >= 0) ? E[r * c->dim + d] : 0.0f;
+                        y[(int64_t)t * c->dim + d] = (r >= 0) ? (float)table_value(c, E, r, d) : 0.0f;
                 }
                 continue;
             }
@@ -211,7 +255,7 @@ int orc_forward(const orc_col* cols, int32_t C, int32_t B,
                 if (r < 0) continue;
                 ++nv;
                 const double wt = value_weight(c, t);
-                for (int32_t d = 0; d < c->dim; ++d) S[d] += wt * (double)E[r * c->dim + d];
+                for (int32_t d = 0; d < c->dim; ++d) S[d] += wt * table_value(c, E, r, d);
             }
             float* y = out + (int64_t)b * ldo + c->out_col;
             for (int32_t d = 0; d < c->dim; ++d) {

@@ -658,3 +658,101 @@ def test_weighted_bags_match_embedding_bag_per_sample_weights():
         touched = np.zeros(rows, bool)
         touched[res["row"]] = True
         assert np.all(g[~touched] == 0)
+
+
+def _copy_column(dim, rows):
+    """A padded column of pad_len 1 with one value per bag: the forward copies
+    each bag's row (no pooling arithmetic)."""
+    return [ColumnSpec("identity", "padded", rows, dim, 0, pad_len=1)], synth.bag_offsets(np.ones(rows, np.int64))
+
+
+def test_bf16_rows_hand_values():
+    """bfloat16 is the upper half of a binary32: 0x3F80 = 1, 0xC000 = -2,
+    0x4049 = 3.140625, 0x0001 = 2^-133, 0x7F80 = inf, 0x8000 = -0."""
+    cols, off = _copy_column(4, 2)
+    E = np.array([[0x3F80, 0xC000, 0x4049, 0x0001], [0x7F80, 0x8000, 0x3F00, 0xBF80]], np.uint16)
+    _, seq = oracle.forward(cols, 2, [off], [np.arange(2)], [E], table_dtypes=["bf16"])
+    want = np.array([[1.0, -2.0, 3.140625, 2.0 ** -133], [np.inf, -0.0, 0.5, -1.0]], np.float32)
+    assert np.array_equal(seq[0][:, 0, :], want)
+    assert np.signbit(seq[0][1, 0, 1])
+
+
+def test_bf16_rows_match_torch_conversion():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(11)
+    bits = rng.integers(0, 1 << 16, (500, 8)).astype(np.uint16)
+    cols, off = _copy_column(8, 500)
+    _, seq = oracle.forward(cols, 500, [off], [np.arange(500)], [bits], table_dtypes=["bf16"])
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+    got = seq[0][:, 0, :]
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_f16_rows_every_bit_pattern():
+    """All 65536 binary16 patterns against numpy's float16 -> float32."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16).reshape(-1, 4)
+    rows = bits.shape[0]
+    cols, off = _copy_column(4, rows)
+    _, seq = oracle.forward(cols, rows, [off], [np.arange(rows)], [bits], table_dtypes=["f16"])
+    ref = bits.view(np.float16).astype(np.float32)
+    got = seq[0][:, 0, :]
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
+
+
+def test_int8_rows_are_scale_times_q():
+    """Every q in [-128, 127] with a power-of-two scale (exact), and a hand
+    example pooled: rows (2, -3) x 0.5 and (100, 1) x 0.25 sum to (26, -1.25)."""
+    q = np.arange(-128, 128, dtype=np.int16).astype(np.int8).reshape(-1, 4)
+    rows = q.shape[0]
+    cols, off = _copy_column(4, rows)
+    scale = np.full(rows, 0.25, np.float32)
+    _, seq = oracle.forward(cols, rows, [off], [np.arange(rows)], [q], table_dtypes=["i8"], row_scales=[scale])
+    assert np.array_equal(seq[0][:, 0, :], q.astype(np.float32) / 4)
+    E = np.array([[2, -3, 0, 0], [100, 1, 0, 0]], np.int8)
+    cs = [ColumnSpec("identity", "sum", 2, 4, 0)]
+    out, _ = oracle.forward(cs, 1, [np.array([0, 2], np.int32)], [np.array([0, 1])], [E], table_dtypes=["i8"],
+                            row_scales=[np.array([0.5, 0.25], np.float32)])
+    assert np.array_equal(out[0], np.array([26.0, -1.25, 0, 0], np.float32))
+
+
+def test_low_precision_tables_pool_like_their_fp32_values():
+    """A low-precision table pools exactly like an fp32 table holding its
+    element values (where those are fp32-representable): every pooling, the
+    padded copy, weights, shared tables."""
+    torch = pytest.importorskip("torch")
+    for seed in range(6):
+        w = synth.random_small(400 + seed, train=False)
+        dts, scales, tabs_lp, tabs_32 = [], [], [], []
+        rng = np.random.default_rng(seed)
+        for t, spec in enumerate(w.tables):
+            if spec is None:
+                dts.append("f32"), scales.append(None), tabs_lp.append(np.zeros((1, 4), np.float32))
+                tabs_32.append(np.zeros((1, 4), np.float32))
+                continue
+            E = rng.standard_normal((spec.num_rows, spec.dim)).astype(np.float32)
+            dt = ["bf16", "f16", "i8", "f32"][(seed + t) % 4]
+            if dt == "bf16":
+                b = torch.from_numpy(E).to(torch.bfloat16)
+                lp, e32 = b.view(torch.int16).numpy().view(np.uint16), b.float().numpy()
+                sc = None
+            elif dt == "f16":
+                h = E.astype(np.float16)
+                lp, e32, sc = h.view(np.uint16), h.astype(np.float32), None
+            elif dt == "i8":
+                lp = rng.integers(-128, 128, E.shape).astype(np.int8)
+                sc = (2.0 ** rng.integers(-8, 0, spec.num_rows)).astype(np.float32)   # exact products
+                e32 = lp.astype(np.float32) * sc[:, None]
+            else:
+                lp, e32, sc = E, E, None
+            dts.append(dt), scales.append(sc), tabs_lp.append(lp), tabs_32.append(e32)
+        a = oracle.forward(w.columns, w.B, w.offsets, w.values, tabs_lp, weights=w.weights, table_dtypes=dts,
+                           row_scales=scales)
+        b = oracle.forward(w.columns, w.B, w.offsets, w.values, tabs_32, weights=w.weights)
+        assert np.array_equal(a[0], b[0])
+        for x, y in zip(a[1], b[1]):
+            assert (x is None and y is None) or np.array_equal(x, y)
