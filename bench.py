@@ -171,7 +171,15 @@ def make_workload(name, columns=None):
 # algorithmic bytes
 # ---------------------------------------------------------------------------
 
-def forward_bytes(w, valid_per_col):
+ELEM_BYTES = {"f32": 4, "bf16": 2, "f16": 2, "i8": 1}
+
+
+def row_bytes(c, table_dtype="f32"):
+    """Bytes one gathered row reads: its elements, plus the row's scale for int8."""
+    return ELEM_BYTES[table_dtype] * c.dim + (4 if table_dtype == "i8" else 0)
+
+
+def forward_bytes(w, valid_per_col, table_dtype="f32"):
     """Per column: the offsets, the values, the boundaries, one row read per
     valid value and one output row per bag (padded columns: pad_len rows)."""
     total = 0
@@ -179,7 +187,7 @@ def forward_bytes(w, valid_per_col):
         n = int(o[-1])
         e = 4 if c.transform == "bucketize" else 8
         nb = 0 if c.boundaries is None else c.boundaries.size
-        total += (w.B + 1) * 4 + n * e + 4 * nb + nv * 4 * c.dim
+        total += (w.B + 1) * 4 + n * e + 4 * nb + nv * row_bytes(c, table_dtype)
         total += w.B * 4 * c.dim * (c.pad_len if c.pooling == "padded" else 1)
     return total
 
@@ -224,10 +232,13 @@ def event_pair(torch):
     return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
 
-def row_sizes_mix(w, valid_per_col):
+def row_sizes_mix(w, valid_per_col, table_dtype="f32"):
+    """Rows gathered per row size (rounded up to the 16 B the calibration
+    kernel moves per lane)."""
     mix = {}
     for c, nv in zip(w.columns, valid_per_col):
-        mix[c.dim * 4] = mix.get(c.dim * 4, 0) + nv
+        b = (row_bytes(c, table_dtype) + 15) // 16 * 16
+        mix[b] = mix.get(b, 0) + nv
     return mix
 
 
@@ -274,17 +285,19 @@ def gather_ceiling(torch, sl, mix, dev, budget_bytes=8 << 30):
 # CPU oracle samples
 # ---------------------------------------------------------------------------
 
-def cpu_forward_sample(w, tables_dev, budget_s=12.0):
+def cpu_forward_sample(w, tables_dev, budget_s=12.0, table_dtype="f32", scales_dev=None):
     """The oracle forward (one thread) on whole columns in order until about
     budget_s of CPU work."""
     import oracle
     t_used, rows_done, cols_done = 0.0, 0, 0
     for ci, c in enumerate(w.columns):
-        tab = tables_dev[c.table].cpu().numpy()
+        tab = synth.table_host(tables_dev[c.table])
+        sc = None if scales_dev is None or scales_dev[c.table] is None else scales_dev[c.table].cpu().numpy()
         spec = synth.ColumnSpec(c.transform, c.pooling, c.num_rows, c.dim, 0, boundaries=c.boundaries,
                                 default=c.default, pad_len=c.pad_len)
         t0 = time.perf_counter()
-        _, _, rows = oracle.forward([spec], w.B, [w.offsets[ci]], [w.values[ci]], [tab], want_rows=True)
+        _, _, rows = oracle.forward([spec], w.B, [w.offsets[ci]], [w.values[ci]], [tab], want_rows=True,
+                                    table_dtypes=[table_dtype], row_scales=[sc])
         t_used += time.perf_counter() - t0
         rows_done += int((rows[0] >= 0).sum())
         cols_done += 1
@@ -375,36 +388,54 @@ class HostTables:
     values the device tables hold), so that a sample touching a few columns
     does not draw all of them."""
 
-    def __init__(self, w):
+    def __init__(self, w, table_dtype="f32"):
         self.w = w
+        self.dtype = table_dtype
         self.cache = {}
+        self.scales = _HostScales(self)
+
+    def _get(self, t):
+        if t not in self.cache:
+            self.cache[t] = synth.lowp_table(synth.make_table(self.w.tables[t], "cpu"), self.dtype)
+        return self.cache[t]
 
     def __getitem__(self, t):
-        if t not in self.cache:
-            self.cache[t] = synth.make_table(self.w.tables[t], "cpu")
-        return self.cache[t]
+        return self._get(t)[0]
+
+
+class _HostScales:
+    """Per-row scales of HostTables' int8 tables, by table index."""
+
+    def __init__(self, host):
+        self.host = host
+
+    def __getitem__(self, t):
+        return self.host._get(t)[1]
 
 
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
+    if args.table_dtype != "f32" and (is_training(args) or args.workload.startswith("dynamic")):
+        raise SystemExit("low-precision tables are read-only: forward workloads only")
     w = make_workload(args.workload, args.columns)
     per = max(2.0, 20.0 / max(1, args.steps + args.warmup))
     vals = []
-    tables = HostTables(w)
+    tables = HostTables(w, args.table_dtype)
     G = None
-    if args.workload in TRAIN_WORKLOADS:
+    if is_training(args):
         width = sum(c.dim for c in w.columns if c.pooling != "padded")
         G = synth.make_grad((w.B, max(width, 1)), 77, "cpu")[:, :width] if width else None
     for i in range(args.warmup + args.steps):
         if args.workload.startswith("dynamic"):
             rate, sample = cpu_dynamic_sample(w, budget_s=per)
         else:
-            if args.workload in TRAIN_WORKLOADS:
+            if is_training(args):
                 rate, sample = cpu_train_sample(w, tables, G, budget_s=per)
             else:
-                rate, sample = cpu_forward_sample(w, tables, budget_s=per)
+                rate, sample = cpu_forward_sample(w, tables, budget_s=per, table_dtype=args.table_dtype,
+                                                  scales_dev=tables.scales)
         if i >= args.warmup:
             vals.append(rate)
     v = statistics.mean(vals)
@@ -413,11 +444,12 @@ def run_reference(args):
         per_step = w.B * len(w.columns) * 2.5   # mean bag length of U{0..5}
     else:
         per_step = sum(int(o[-1]) for o in w.offsets)
-    line = {"impl": "reference", "metric": metric_name(args.workload), "value": v, "unit": "rows/s",
+    line = {"impl": "reference", "metric": metric_name(args.workload, args.forward_only), "value": v,
+            "unit": "rows/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": per_step / v * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64 accumulate / f32 storage", "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.B, "columns": len(w.columns),
+            "config": {"workload": w.name, "batch": w.B, "columns": len(w.columns), "table_dtype": args.table_dtype,
                        "l2": "host run (no GPU)", "parallelism": "1 host core"},
             "cpu_baseline": {"value": v, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -438,8 +470,12 @@ def traffic_estimate(workload, fbytes):
     return None if r is None else r * fbytes
 
 
-def metric_name(workload):
-    if workload in TRAIN_WORKLOADS:
+def is_training(args):
+    return args.workload in TRAIN_WORKLOADS and not getattr(args, "forward_only", False)
+
+
+def metric_name(workload, forward_only=False):
+    if workload in TRAIN_WORKLOADS and not forward_only:
         return "pooled rows gathered/sec (fwd+bwd+update)"
     if workload.startswith("dynamic"):
         return "pooled rows gathered/sec (hash+fwd+bwd+update+expiry)"
@@ -467,7 +503,7 @@ def run_ours(args):
     if args.workload.startswith("dynamic"):
         res = bench_dynamic(torch, sl, w, args, dev, stream, flush)
     else:
-        res = bench_plan(torch, sl, w, args, dev, stream, flush, train=args.workload in TRAIN_WORKLOADS)
+        res = bench_plan(torch, sl, w, args, dev, stream, flush, train=is_training(args))
 
     clocks = res.pop("clocks")
     ms_step, value = aggregate_ranks(torch, res["ms_step"], res["rows_per_step"], dev)
@@ -476,7 +512,7 @@ def run_ours(args):
     fw_ms = statistics.mean(res["times"]["fwd"])
     achieved = res["fbytes"] / (fw_ms / 1e3) / 1e9
     line = {
-        "metric": metric_name(args.workload),
+        "metric": metric_name(args.workload, args.forward_only),
         "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -486,7 +522,9 @@ def run_ours(args):
                            "flushed between steps (2x L2 write, outside events)"),
                        parallelism="replicas" if world > 1 else "1 GPU"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic_estimate(w.name, res["fbytes"]),
+                     "frac": achieved / peak,
+                     "traffic": traffic_estimate(w.name if args.table_dtype == "f32" else
+                                                 "%s-%s" % (w.name, args.table_dtype), res["fbytes"]),
                      "kernel": "k_forward", "bytes_per_launch": res["fbytes"], "launch_ms": fw_ms,
                      "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy burst)"},
         "step_ms": {k: statistics.mean(v) for k, v in res["times"].items()},
@@ -542,8 +580,17 @@ def bench_plan(torch, sl, w, args, dev, stream, flush, train):
     fv = torch.from_numpy(fv_h).to(dev) if has_f else None
     f_off = torch.from_numpy(f_off_h).to(dev) if has_f else None
     n_all = n_ids + n_f
+    dt = args.table_dtype
+    scales = None
+    if dt != "f32":
+        if train:
+            raise SystemExit("low-precision tables are read-only: forward workloads only")
+        conv = [None if t is None else synth.lowp_table(t, dt) for t in tables]
+        tables = [None if x is None else x[0] for x in conv]
+        scales = [None if x is None else x[1] for x in conv]
+        del conv
     plan = sl.Plan(w.columns, tables, accs, max_batch=w.B, max_ids=max(n_all, 1) if train else 0, training=train,
-                   backward=args.backward if train else "sort")
+                   backward=args.backward if train else "sort", row_scales=scales)
 
     rows_dbg = torch.empty(max(n_all, 1), dtype=torch.int64, device=dev)
     out, seq = plan.forward(w.B, ids, id_off, fv, f_off, rows_dbg=rows_dbg)
@@ -553,9 +600,9 @@ def bench_plan(torch, sl, w, args, dev, stream, flush, train):
     valid = valid_counts(w, rows_dbg, n_ids)
     del rows_dbg
     rows_per_step = sum(valid)
-    fbytes = forward_bytes(w, valid)
+    fbytes = forward_bytes(w, valid, dt)
     res = {"rows_per_step": rows_per_step, "fbytes": fbytes,
-           "config": {"ids_per_step": n_all, "rows_gathered_per_step": rows_per_step}}
+           "config": {"ids_per_step": n_all, "rows_gathered_per_step": rows_per_step, "table_dtype": dt}}
     G = Gseq = None
     if train:
         width = plan.out_width
@@ -662,12 +709,12 @@ def bench_plan(torch, sl, w, args, dev, stream, flush, train):
                                   "l2": "not flushed between replays"}
         if plan.device_status() != 0:
             raise SystemExit("device status after the graph replays")
-    res["ceiling"] = gather_ceiling(torch, sl, row_sizes_mix(w, valid), dev) if not args.no_ceiling else None
+    res["ceiling"] = gather_ceiling(torch, sl, row_sizes_mix(w, valid, dt), dev) if not args.no_ceiling else None
     if not args.no_cpu_baseline and dist_env()[0] == 0:
         if train:
             rate, sample = cpu_train_sample(w, tables, G, budget_s=12.0)
         else:
-            rate, sample = cpu_forward_sample(w, tables, budget_s=12.0)
+            rate, sample = cpu_forward_sample(w, tables, budget_s=12.0, table_dtype=dt, scales_dev=scales)
         res["cpu"] = {"value": rate, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": sample}
     return res
 
@@ -867,6 +914,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-ceiling", action="store_true")
     ap.add_argument("--columns", type=int, default=None, help="number of columns (smaller profiling cases)")
+    ap.add_argument("--forward-only", action="store_true",
+                    help="training workloads: time the forward alone (inference over the same inputs)")
+    ap.add_argument("--table-dtype", default="f32", choices=["f32", "bf16", "f16", "i8"],
+                    help="forward workloads: store the tables as bf16, fp16 or int8 with per-row scales")
     ap.add_argument("--pipeline", action="store_true",
                     help="dynamic workload: pipelined steps (next lookup beside this backward)")
     ap.add_argument("--backward", default="sort", choices=["sort", "atomic"],

@@ -76,6 +76,18 @@ typedef enum {
                                  IDs; the bag is cut after pad_len values     */
 } emb_pooling;
 
+/* Storage type of a table's rows (the RecIS evaluation lists an int8 table
+ * beside fp32 ones, Table 3).  Lookups convert each element to fp32 and pool
+ * in fp32: bf16 and fp16 convert exactly; int8 element q of row r reads as
+ * row_scale[r] * q (one fp32 rounding).  Low-precision tables are read-only:
+ * only inference plans take them. */
+typedef enum {
+    EMB_DT_F32 = 0,
+    EMB_DT_BF16 = 1,
+    EMB_DT_F16 = 2,
+    EMB_DT_I8 = 3
+} emb_table_dtype;
+
 /* Safety handling [RECom "Why this problem is worth solving"]: a value whose
  * row falls outside [0, num_rows) is dropped (it reads nothing, counts for
  * nothing, receives no gradient).  A pooled bag with no valid value yields
@@ -94,13 +106,18 @@ typedef struct {
                                  no gradient (sequence truncation, RecIS §2.1);
                                  0 = all.  Must be 0 for EMB_POOL_NONE_PADDED
                                  (pad_len cuts there).                          */
-    float* weight;            /* [num_rows, dim] fp32 row-major, 16-byte aligned.
-                                 Columns given the SAME pointer share one table
-                                 (same num_rows and dim required); the backward
-                                 then merges their gradients per row.           */
+    float* weight;            /* [num_rows, dim] row-major in table_dtype (fp32
+                                 unless stated), 16-byte aligned.  Columns given
+                                 the SAME pointer share one table (same
+                                 num_rows, dim and table_dtype required); the
+                                 backward then merges their gradients per row. */
     float* adagrad_acc;       /* [num_rows, dim] fp32 Adagrad accumulator, same
                                  sharing; required by training plans             */
     const float* default_vec; /* [dim] fp32 or NULL (zeros)                      */
+    int32_t table_dtype;      /* emb_table_dtype; 0 = fp32                       */
+    int32_t reserved;         /* 0                                               */
+    const float* row_scale;   /* EMB_DT_I8: [num_rows] fp32 scale per row,
+                                 4-byte aligned; otherwise ignored               */
 } emb_column_desc;
 
 /* Plan flags. */

@@ -26,6 +26,7 @@ STATUS = {
     7: "EMB_ERR_BAD_INDEX", 8: "EMB_ERR_TIMEOUT",
 }
 TRANSFORM = {"identity": 0, "hash_mod": 1, "bucketize": 2, "rows_given": 3}
+TABLE_DTYPE = {"float32": 0, "bfloat16": 1, "float16": 2, "int8": 3}   # torch dtype name -> emb_table_dtype
 POOLING = {"sum": 0, "mean": 1, "padded": 2}
 PLAN_TRAINING = 1
 PLAN_ATOMIC_BACKWARD = 2
@@ -50,6 +51,9 @@ class EmbColumnDesc(ctypes.Structure):
         ("weight", c_void_p),
         ("adagrad_acc", c_void_p),
         ("default_vec", c_void_p),
+        ("table_dtype", c_int32),
+        ("reserved", c_int32),
+        ("row_scale", c_void_p),
     ]
 
 
@@ -253,10 +257,13 @@ class Plan:
     tables of physical table t.  The device copies of boundaries and default
     vectors are owned here and live as long as the plan.  backward: "sort"
     (radix sort + run reduction, deterministic) or "atomic" (warp merge +
-    atomics into a compact gradient)."""
+    atomics into a compact gradient).  A table's storage type follows its
+    tensor's dtype (float32, bfloat16, float16, or int8 with
+    ``row_scales[t]``, fp32 per row); low-precision tables are for inference
+    plans."""
 
     def __init__(self, columns, weights, accs=None, max_batch=1, max_ids=0, training=False, device="cuda",
-                 backward="sort"):
+                 backward="sort", row_scales=None):
         import torch
         self.columns = list(columns)
         self.training = training
@@ -279,7 +286,11 @@ class Plan:
                 v = torch.as_tensor(c.default, dtype=torch.float32).to(device).contiguous()
                 self._keep.append(v)
                 d.default_vec = v.data_ptr()
-            d.weight = weights[c.table].data_ptr()
+            tw = weights[c.table]
+            d.weight = tw.data_ptr()
+            d.table_dtype = TABLE_DTYPE[str(tw.dtype).replace("torch.", "")]
+            if d.table_dtype == TABLE_DTYPE["int8"]:
+                d.row_scale = row_scales[c.table].data_ptr()
             if accs is not None:
                 d.adagrad_acc = accs[c.table].data_ptr()
             descs.append(d)

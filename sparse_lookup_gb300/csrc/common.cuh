@@ -107,8 +107,9 @@ __device__ __forceinline__ void latch(uint32_t* st, uint32_t code) {
 // Metadata the kernels read.
 // ---------------------------------------------------------------------------
 struct ColMeta {
-  const float* weight;     // table [num_rows, dim]
+  const float* weight;     // table [num_rows, dim] in dtype
   float* acc;              // Adagrad accumulator (training)
+  const float* qscale;     // EMB_DT_I8: per-row scale
   const float* dflt;       // default vector or nullptr
   const float* bnd;        // bucketize boundaries
   int64_t num_rows;
@@ -125,6 +126,7 @@ struct ColMeta {
   uint32_t table_base;     // first global row of the column's table
   int32_t out_col;         // pooled: float offset inside an output row
   int32_t col;             // plan column index
+  int32_t dtype;           // emb_table_dtype of the rows
 };
 
 struct TableMeta {

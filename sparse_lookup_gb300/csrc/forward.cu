@@ -28,6 +28,10 @@
 // Empty bags and bags whose values were all dropped get the default vector.
 #include <algorithm>
 
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
 #include "plan.cuh"
 
 namespace emb {
@@ -102,6 +106,99 @@ __device__ __forceinline__ float4 f4scale(float w, const float4& b) {
 }
 
 __device__ __forceinline__ float4 ldg4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+
+// One lane's share of a row -- elements 4 f4 .. 4 f4 + 3 -- as loaded, for
+// rows stored as DT (emb_table_dtype).  A batch of these stays in flight in
+// its stored width (two registers for bf16 / fp16) and becomes fp32 only
+// where it is used: bf16 and fp16 convert exactly (bf16 is the upper half of
+// an fp32), int8 element q reads as scale * q.
+template <int DT>
+struct RowRaw {
+  float4 x;
+};
+template <>
+struct RowRaw<EMB_DT_BF16> {
+  uint2 x;
+};
+template <>
+struct RowRaw<EMB_DT_F16> {
+  uint2 x;
+};
+template <>
+struct RowRaw<EMB_DT_I8> {
+  uint32_t q;
+  float s;
+};
+
+// Rows in flight per lane in the whole-warp and padded paths scale with the
+// registers a raw share takes: two for the low-precision types against four
+// for fp32 (measured: 5 % faster on long bf16 bags; in the lane-group paths
+// of short bags the deeper batches measured slower and are not used).
+template <int DT>
+constexpr int kRawScale = DT == EMB_DT_F32 ? 1 : 2;
+
+template <int DT>
+__device__ __forceinline__ RowRaw<DT> raw_zero() {
+  RowRaw<DT> z;
+  if constexpr (DT == EMB_DT_F32) {
+    z.x = f4zero();
+  } else if constexpr (DT == EMB_DT_I8) {
+    z.q = 0u;
+    z.s = 0.0f;
+  } else {
+    z.x = make_uint2(0u, 0u);
+  }
+  return z;
+}
+
+template <int DT>
+__device__ __forceinline__ RowRaw<DT> row_raw(const float* E, int dim, const float* qs, int32_t r, int f4) {
+  const int64_t e = (int64_t)r * dim + f4 * 4;
+  RowRaw<DT> v;
+  if constexpr (DT == EMB_DT_F32) {
+    v.x = ldg4(E + e);
+  } else if constexpr (DT == EMB_DT_I8) {
+    v.q = __ldg(reinterpret_cast<const uint32_t*>(reinterpret_cast<const int8_t*>(E) + e));
+    v.s = __ldg(qs + r);
+  } else {
+    v.x = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(E) + e));
+  }
+  return v;
+}
+
+template <int DT>
+__device__ __forceinline__ float4 raw_f4(const RowRaw<DT>& v) {
+  if constexpr (DT == EMB_DT_F32) {
+    return v.x;
+  } else if constexpr (DT == EMB_DT_I8) {
+    const int32_t q = (int32_t)v.q;
+    return make_float4(v.s * (float)((q << 24) >> 24), v.s * (float)((q << 16) >> 24),
+                       v.s * (float)((q << 8) >> 24), v.s * (float)(q >> 24));
+  } else if constexpr (DT == EMB_DT_BF16) {
+    return make_float4(__uint_as_float(v.x.x << 16), __uint_as_float(v.x.x & 0xffff0000u),
+                       __uint_as_float(v.x.y << 16), __uint_as_float(v.x.y & 0xffff0000u));
+  } else {
+    const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&v.x.x));
+    const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&v.x.y));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+  }
+}
+
+// Calls f with the column's storage type as a compile-time constant: only
+// fp32 unless the launch has low-precision tables (LP).
+template <bool LP, class F>
+__device__ __forceinline__ void with_dtype(int dtype, F&& f) {
+  if constexpr (!LP) {
+    f(std::integral_constant<int, EMB_DT_F32>{});
+  } else {
+    switch (dtype) {
+      case EMB_DT_BF16: f(std::integral_constant<int, EMB_DT_BF16>{}); break;
+      case EMB_DT_F16: f(std::integral_constant<int, EMB_DT_F16>{}); break;
+      case EMB_DT_I8: f(std::integral_constant<int, EMB_DT_I8>{}); break;
+      default: f(std::integral_constant<int, EMB_DT_F32>{}); break;
+    }
+  }
+}
 
 __device__ __forceinline__ int64_t clamp_off(int32_t o, int64_t n, bool& bad) {
   int64_t v = o;
@@ -297,7 +394,7 @@ __device__ __forceinline__ uint32_t padded_gsrc(const FwdArgs& a, const ColMeta&
 // phase B, pooled: equal value ranges per lane group; WT: a SUM column of a
 // weighted stream, each row scaled by its value's weight W[t]
 // ---------------------------------------------------------------------------
-template <int V, bool WT>
+template <int V, bool WT, int DT>
 __device__ void warp_pool_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m, const float* W, int ns, int T,
                                 int b0, int glog, unsigned longmask) {
   constexpr int U = kUPool / V;
@@ -308,6 +405,7 @@ __device__ void warp_pool_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m
   const int R = (T + G - 1) / G;
   const int k0 = min(q * R, T), k1 = min(k0 + R, T);
   const float* E = m.weight;
+  const float* qs = m.qscale;
 
   float4 acc[V];
 #pragma unroll
@@ -346,7 +444,7 @@ __device__ void warp_pool_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m
   };
 
   for (int j = 0; j < R; j += U) {
-    float4 vals[U][V];
+    RowRaw<DT> vals[U][V];
     float wu[WT ? U : 1];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -355,7 +453,7 @@ __device__ void warp_pool_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m
 #pragma unroll
       for (int v = 0; v < V; ++v) {
         const int f4 = sub + v * 32;
-        vals[u][v] = (r >= 0 && f4 < dim4) ? ldg4(E + (int64_t)r * dim + f4 * 4) : f4zero();
+        vals[u][v] = (r >= 0 && f4 < dim4) ? row_raw<DT>(E, dim, qs, r, f4) : raw_zero<DT>();
       }
       if constexpr (WT) {
         wu[u] = 0.0f;
@@ -382,8 +480,8 @@ __device__ void warp_pool_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m
       }
 #pragma unroll
       for (int v = 0; v < V; ++v) {
-        if constexpr (WT) f4fma(acc[v], wu[u], vals[u][v]);
-        else f4add(acc[v], vals[u][v]);
+        if constexpr (WT) f4fma(acc[v], wu[u], raw_f4<DT>(vals[u][v]));
+        else f4add(acc[v], raw_f4<DT>(vals[u][v]));
       }
       nv += ws.rows[k] >= 0;
     }
@@ -421,10 +519,10 @@ __device__ void warp_pool_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m
 }
 
 // phase B, padded (short pad_len): ns bags x pad_len output rows, flat over groups
-template <int V>
+template <int V, int DT>
 __device__ void warp_pad_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m, int ns, int b0, int glog,
                                unsigned longmask) {
-  constexpr int U = kU / V;
+  constexpr int U = kU / V * kRawScale<DT>;
   const int lane = threadIdx.x & 31;
   const int G = 32 >> glog;
   const int q = lane >> glog, sub = lane & ((1 << glog) - 1);
@@ -432,7 +530,7 @@ __device__ void warp_pad_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m,
   const int total = ns * P;
   const float* E = m.weight;
   for (int base = 0; base < total; base += G * U) {
-    float4 vals[U][V];
+    RowRaw<DT> vals[U][V];
     int o[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -445,7 +543,7 @@ __device__ void warp_pad_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m,
 #pragma unroll
       for (int v = 0; v < V; ++v) {
         const int f4 = sub + v * 32;
-        vals[u][v] = (r >= 0 && f4 < m.dim4) ? ldg4(E + (int64_t)r * m.dim + f4 * 4) : f4zero();
+        vals[u][v] = (r >= 0 && f4 < m.dim4) ? row_raw<DT>(E, m.dim, m.qscale, r, f4) : raw_zero<DT>();
       }
     }
 #pragma unroll
@@ -457,7 +555,7 @@ __device__ void warp_pad_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m,
 #pragma unroll
       for (int v = 0; v < V; ++v) {
         const int f4 = sub + v * 32;
-        if (f4 < m.dim4) *reinterpret_cast<float4*>(dst + f4 * 4) = vals[u][v];
+        if (f4 < m.dim4) *reinterpret_cast<float4*>(dst + f4 * 4) = raw_f4<DT>(vals[u][v]);
       }
     }
   }
@@ -466,10 +564,10 @@ __device__ void warp_pad_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m,
 // ---------------------------------------------------------------------------
 // phase C: one long bag, the whole warp, values transformed on the fly
 // ---------------------------------------------------------------------------
-template <int V, bool WT>
+template <int V, bool WT, int DT>
 __device__ void warp_long_bag(const FwdArgs& a, int st, const ColMeta& m, const float* W, int32_t b, int64_t lo,
                               int64_t hi, int glog) {
-  constexpr int U = kU / V;
+  constexpr int U = kU / V * (WT ? 1 : kRawScale<DT>);
   const int lane = threadIdx.x & 31;
   const int G = 32 >> glog;
   const int grp = lane >> glog, sub = lane & ((1 << glog) - 1);
@@ -487,7 +585,7 @@ __device__ void warp_long_bag(const FwdArgs& a, int st, const ColMeta& m, const 
         record<WT>(a, st, lo + p, row, m, padded_gsrc(a, m, b, p));
       }
       for (int k = 0; k < cnt; k += U * G) {
-        float4 v[U][V];
+        RowRaw<DT> v[U][V];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int j = k + u * G + grp;
@@ -496,7 +594,7 @@ __device__ void warp_long_bag(const FwdArgs& a, int st, const ColMeta& m, const 
 #pragma unroll
           for (int q = 0; q < V; ++q) {
             const int f4 = sub + q * 32;
-            v[u][q] = (ok && f4 < m.dim4) ? ldg4(E + (int64_t)r * m.dim + f4 * 4) : f4zero();
+            v[u][q] = (ok && f4 < m.dim4) ? row_raw<DT>(E, m.dim, m.qscale, r, f4) : raw_zero<DT>();
           }
         }
 #pragma unroll
@@ -505,7 +603,8 @@ __device__ void warp_long_bag(const FwdArgs& a, int st, const ColMeta& m, const 
 #pragma unroll
           for (int q = 0; q < V; ++q) {
             const int f4 = sub + q * 32;
-            if (j < cnt && f4 < m.dim4) *reinterpret_cast<float4*>(dst + (p0 + j) * m.dim + f4 * 4) = v[u][q];
+            if (j < cnt && f4 < m.dim4)
+              *reinterpret_cast<float4*>(dst + (p0 + j) * m.dim + f4 * 4) = raw_f4<DT>(v[u][q]);
           }
         }
       }
@@ -533,7 +632,7 @@ __device__ void warp_long_bag(const FwdArgs& a, int st, const ColMeta& m, const 
     }
     nv += __popc(__ballot_sync(kFull, row >= 0));
     for (int k = 0; k < cnt; k += U * G) {
-      float4 v[U][V];
+      RowRaw<DT> v[U][V];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int j = k + u * G + grp;
@@ -542,21 +641,23 @@ __device__ void warp_long_bag(const FwdArgs& a, int st, const ColMeta& m, const 
 #pragma unroll
         for (int q = 0; q < V; ++q) {
           const int f4 = sub + q * 32;
-          v[u][q] = (ok && f4 < m.dim4) ? ldg4(E + (int64_t)r * m.dim + f4 * 4) : f4zero();
+          v[u][q] = (ok && f4 < m.dim4) ? row_raw<DT>(E, m.dim, m.qscale, r, f4) : raw_zero<DT>();
         }
       }
+      float wj[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) wj[u] = 1.0f;
       if (WT && W) {
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const float wj = __shfl_sync(kFull, wl, (k + u * G + grp) & 31);
-#pragma unroll
-          for (int q = 0; q < V; ++q) v[u][q] = f4scale(wj, v[u][q]);
-        }
+        for (int u = 0; u < U; ++u) wj[u] = __shfl_sync(kFull, wl, (k + u * G + grp) & 31);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u)
 #pragma unroll
-        for (int q = 0; q < V; ++q) kadd4(acc[q], cmp[q], v[u][q]);
+        for (int q = 0; q < V; ++q) {
+          const float4 x = raw_f4<DT>(v[u][q]);
+          kadd4(acc[q], cmp[q], (WT && W) ? f4scale(wj[u], x) : x);
+        }
     }
   }
 #pragma unroll
@@ -593,7 +694,7 @@ __device__ void warp_long_bag(const FwdArgs& a, int st, const ColMeta& m, const 
 // kOneHotBags bags share each round trip.  WT: the launch carries weights
 // (records hold them); W: this column's value weights, or null.
 // ---------------------------------------------------------------------------
-template <int V, bool WT>
+template <int V, bool WT, int DT>
 __device__ void warp_onehot_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m, const float* W, int st,
                                   int64_t t0, int nb, int b0, int glog) {
   constexpr int U = kUPool / V;
@@ -621,7 +722,7 @@ __device__ void warp_onehot_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta&
   const int q = lane >> glog, sub = lane & ((1 << glog) - 1);
   const float* E = m.weight;
   for (int j = q; j < nb; j += G * U) {
-    float4 vals[U][V];
+    RowRaw<DT> vals[U][V];
     int r[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -630,7 +731,7 @@ __device__ void warp_onehot_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta&
 #pragma unroll
       for (int v = 0; v < V; ++v) {
         const int f4 = sub + v * 32;
-        vals[u][v] = (r[u] >= 0 && f4 < m.dim4) ? ldg4(E + (int64_t)r[u] * m.dim + f4 * 4) : f4zero();
+        vals[u][v] = (r[u] >= 0 && f4 < m.dim4) ? row_raw<DT>(E, m.dim, m.qscale, r[u], f4) : raw_zero<DT>();
       }
     }
 #pragma unroll
@@ -645,7 +746,7 @@ __device__ void warp_onehot_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta&
       for (int v = 0; v < V; ++v) {
         const int f4 = sub + v * 32;
         if (f4 < m.dim4) {
-          const float4 e = wt ? f4scale(wk, vals[u][v]) : vals[u][v];
+          const float4 e = wt ? f4scale(wk, raw_f4<DT>(vals[u][v])) : raw_f4<DT>(vals[u][v]);
           *reinterpret_cast<float4*>(y + f4 * 4) = finish(m, e, cnt, f4);
         }
       }
@@ -658,7 +759,7 @@ __device__ void warp_onehot_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta&
 // ---------------------------------------------------------------------------
 // the kernel: one warp per element tile
 // ---------------------------------------------------------------------------
-template <bool WT>
+template <bool WT, bool LP>
 __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int64_t tile);
 
 // Two schedules.  Static: one tile per warp, the grid covers all tiles (warps
@@ -669,9 +770,10 @@ __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int
 // idling beside a sibling that drew long ones; the last warp to finish
 // resets the counter for the next launch (CUDA-graph safe: no host state
 // changes between launches).
-// WT: a launch with value weights gets its own instance, so the unweighted
-// one keeps its registers for loads in flight.
-template <bool WT>
+// WT: a launch with value weights, LP: one with tables stored below fp32;
+// each gets its own instance, so the plain fp32 one keeps its registers for
+// loads in flight.
+template <bool WT, bool LP>
 __global__ void __launch_bounds__(kFwdThreads, 4) k_forward(const FwdArgs a) {
   __shared__ WarpSmem smem[kFwdWarpsPerCta];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -680,7 +782,7 @@ __global__ void __launch_bounds__(kFwdThreads, 4) k_forward(const FwdArgs a) {
   // the first tile of every warp is its warp index; tickets count from there
   int64_t tile = (int64_t)blockIdx.x * kFwdWarpsPerCta + (threadIdx.x >> 5);
   while (tile < n_tiles) {
-    forward_tile<WT>(a, ws, tile);
+    forward_tile<WT, LP>(a, ws, tile);
     if (!a.dynamic) break;   // static: one tile per warp
     unsigned long long tk = 0;
     if (lane == 0) tk = atomicAdd(&a.ticket[0], 1ull);
@@ -696,7 +798,7 @@ __global__ void __launch_bounds__(kFwdThreads, 4) k_forward(const FwdArgs a) {
   }
 }
 
-template <bool WT>
+template <bool WT, bool LP>
 __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int64_t tile) {
   const int lane = threadIdx.x & 31;
   int st = 0;
@@ -754,8 +856,11 @@ __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int
       stop = __reduce_min_sync(kFull, stop);
       const float* W = WT && m.pooling == EMB_POOL_SUM ? a.wts[st] : nullptr;
       const int glog = lanes_log2(m.dim4);
-      if (m.dim4 > 32) warp_onehot_chunk<2, WT>(a, ws, m, W, st, lo0, stop, b0, glog);
-      else warp_onehot_chunk<1, WT>(a, ws, m, W, st, lo0, stop, b0, glog);
+      with_dtype<LP>(m.dtype, [&](auto dt) {
+        constexpr int DT = decltype(dt)::value;
+        if (m.dim4 > 32) warp_onehot_chunk<2, WT, DT>(a, ws, m, W, st, lo0, stop, b0, glog);
+        else warp_onehot_chunk<1, WT, DT>(a, ws, m, W, st, lo0, stop, b0, glog);
+      });
       cur += stop;
       continue;
     }
@@ -834,24 +939,30 @@ __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int
     // ---- phase B: pool / copy ----
     const int glog = lanes_log2(m.dim4);
     const float* W = WT && m.pooling == EMB_POOL_SUM ? a.wts[st] : nullptr;   // value weights
-    if (padded) {
-      if (m.dim4 > 32) warp_pad_chunk<2>(a, ws, m, ns, b0, glog, longmask);
-      else warp_pad_chunk<1>(a, ws, m, ns, b0, glog, longmask);
-    } else if (WT && W) {
-      if (m.dim4 > 32) warp_pool_chunk<2, true>(a, ws, m, W, ns, T, b0, glog, longmask);
-      else warp_pool_chunk<1, true>(a, ws, m, W, ns, T, b0, glog, longmask);
-    } else {
-      if (m.dim4 > 32) warp_pool_chunk<2, false>(a, ws, m, W, ns, T, b0, glog, longmask);
-      else warp_pool_chunk<1, false>(a, ws, m, W, ns, T, b0, glog, longmask);
-    }
+    with_dtype<LP>(m.dtype, [&](auto dt) {
+      constexpr int DT = decltype(dt)::value;
+      if (padded) {
+        if (m.dim4 > 32) warp_pad_chunk<2, DT>(a, ws, m, ns, b0, glog, longmask);
+        else warp_pad_chunk<1, DT>(a, ws, m, ns, b0, glog, longmask);
+      } else if (WT && W) {
+        if (m.dim4 > 32) warp_pool_chunk<2, true, DT>(a, ws, m, W, ns, T, b0, glog, longmask);
+        else warp_pool_chunk<1, true, DT>(a, ws, m, W, ns, T, b0, glog, longmask);
+      } else {
+        if (m.dim4 > 32) warp_pool_chunk<2, false, DT>(a, ws, m, W, ns, T, b0, glog, longmask);
+        else warp_pool_chunk<1, false, DT>(a, ws, m, W, ns, T, b0, glog, longmask);
+      }
+    });
 
     // ---- phase C: long bags of the chunk ----
     for (unsigned lm = longmask; lm; lm &= lm - 1) {
       const int i = __ffs(lm) - 1;
       const int64_t blo = __shfl_sync(kFull, lo, i);
       const int64_t bhi = __shfl_sync(kFull, hi, i);
-      if (m.dim4 > 32) warp_long_bag<2, WT>(a, st, m, W, b0 + i, blo, bhi, glog);
-      else warp_long_bag<1, WT>(a, st, m, W, b0 + i, blo, bhi, glog);
+      with_dtype<LP>(m.dtype, [&](auto dt) {
+        constexpr int DT = decltype(dt)::value;
+        if (m.dim4 > 32) warp_long_bag<2, WT, DT>(a, st, m, W, b0 + i, blo, bhi, glog);
+        else warp_long_bag<1, WT, DT>(a, st, m, W, b0 + i, blo, bhi, glog);
+      });
     }
     __syncwarp();
     cur += ns;
@@ -860,7 +971,7 @@ __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int
 
 int forward_ctas_per_sm() {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_forward<false>, kFwdThreads, 0) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_forward<false, false>, kFwdThreads, 0) != cudaSuccess) {
     cudaGetLastError();
     n = 4;
   }
@@ -924,8 +1035,14 @@ emb_status launch_forward(emb_plan_s* p, int32_t batch, const int64_t* ids, cons
   if (a.dynamic) grid = std::min<int64_t>(grid, resident);
   a.ticket = p->fwd_ticket;
   a.n_warps = grid * kFwdWarpsPerCta;
-  if (a.wts[0] || a.wts[1]) k_forward<true><<<(unsigned)grid, kFwdThreads, 0, stream>>>(a);
-  else k_forward<false><<<(unsigned)grid, kFwdThreads, 0, stream>>>(a);
+  const bool wt = a.wts[0] || a.wts[1];
+  if (p->low_precision) {
+    if (wt) k_forward<true, true><<<(unsigned)grid, kFwdThreads, 0, stream>>>(a);
+    else k_forward<false, true><<<(unsigned)grid, kFwdThreads, 0, stream>>>(a);
+  } else {
+    if (wt) k_forward<true, false><<<(unsigned)grid, kFwdThreads, 0, stream>>>(a);
+    else k_forward<false, false><<<(unsigned)grid, kFwdThreads, 0, stream>>>(a);
+  }
   return cuda_status(cudaGetLastError());
 }
 

@@ -70,6 +70,9 @@ emb_status validate_column(const emb_column_desc& c, bool training) {
   }
   if (training && (!c.adagrad_acc || !aligned16(c.adagrad_acc))) return EMB_ERR_INVALID_ARG;
   if (c.default_vec && !aligned16(c.default_vec)) return EMB_ERR_INVALID_ARG;
+  if (c.table_dtype < EMB_DT_F32 || c.table_dtype > EMB_DT_I8 || c.reserved != 0) return EMB_ERR_INVALID_ARG;
+  if (c.table_dtype == EMB_DT_I8 && (!c.row_scale || ((uintptr_t)c.row_scale & 3u) != 0)) return EMB_ERR_INVALID_ARG;
+  if (training && c.table_dtype != EMB_DT_F32) return EMB_ERR_UNSUPPORTED;   // low-precision tables are read-only
   return EMB_OK;
 }
 
@@ -116,12 +119,15 @@ extern "C" emb_status emb_plan_create(const emb_column_desc* cols, int32_t n_col
       tm.dim = d.dim;
       tm.dim4 = d.dim / 4;
       p->tables_h.push_back(tm);
+      p->table_first_col.push_back(c);
       p->table_base_h.push_back((uint32_t)base);
       base += (uint64_t)d.num_rows;
       p->col_table.push_back(t);
     } else {
       const TableMeta& tm = p->tables_h[it->second];
-      if (tm.num_rows != d.num_rows || tm.dim != d.dim || tm.acc != d.adagrad_acc) {
+      const emb_column_desc& d0 = cols[p->table_first_col[it->second]];
+      if (tm.num_rows != d.num_rows || tm.dim != d.dim || tm.acc != d.adagrad_acc ||
+          d0.table_dtype != d.table_dtype || (d.table_dtype == EMB_DT_I8 && d0.row_scale != d.row_scale)) {
         free_plan(p);
         return EMB_ERR_INVALID_ARG;
       }
@@ -147,6 +153,9 @@ extern "C" emb_status emb_plan_create(const emb_column_desc* cols, int32_t n_col
     ColMeta& m = p->meta_h[c];
     m.weight = d.weight;
     m.acc = d.adagrad_acc;
+    m.qscale = d.table_dtype == EMB_DT_I8 ? d.row_scale : nullptr;
+    m.dtype = d.table_dtype;
+    if (d.table_dtype != EMB_DT_F32) p->low_precision = true;
     m.dflt = d.default_vec;
     m.bnd = d.boundaries;
     m.num_rows = d.num_rows;

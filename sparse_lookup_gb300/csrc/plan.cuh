@@ -67,6 +67,8 @@ struct emb_plan_s {
   std::vector<emb::ColMeta> meta_h;
   std::vector<int32_t> col_table;
   std::vector<emb::TableMeta> tables_h;
+  std::vector<int32_t> table_first_col;   // first column of each table
+  bool low_precision = false;            // some table is stored below fp32
   std::vector<uint32_t> table_base_h;  // [n_tables + 1]
   emb::ColMeta* meta_d = nullptr;
   int32_t* stream_cols_d = nullptr;    // id-stream columns, then f-stream columns

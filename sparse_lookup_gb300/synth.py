@@ -396,6 +396,35 @@ def make_table(spec: TableSpec, device="cpu"):
     return t
 
 
+def lowp_table(t, dtype: str):
+    """A copy of fp32 table t stored as "bf16" / "f16" (round to nearest
+    even), or "i8" with a per-row symmetric scale (max |row| / 127, 1 for an
+    all-zero row; q = round(x / scale) in [-127, 127]).  Returns (table,
+    row scales or None)."""
+    import torch
+    if dtype == "f32":
+        return t, None
+    if dtype == "bf16":
+        return t.to(torch.bfloat16), None
+    if dtype == "f16":
+        return t.to(torch.float16), None
+    if dtype == "i8":
+        amax = t.abs().amax(dim=1)
+        scale = torch.where(amax > 0, amax / 127.0, torch.ones_like(amax)).to(torch.float32).contiguous()
+        q = torch.round(t / scale[:, None]).clamp_(-127, 127).to(torch.int8).contiguous()
+        return q, scale
+    raise ValueError("table dtype %r" % dtype)
+
+
+def table_host(t):
+    """Host copy of a (possibly low-precision) table as the oracle reads it:
+    float32, uint16 bit patterns for bf16 / f16, int8."""
+    import torch
+    if t.dtype in (torch.bfloat16, torch.float16):
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
 def make_grad(shape, seed: int, device="cpu"):
     """Upstream gradient N(0, 1) from a seeded generator."""
     import torch
