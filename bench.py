@@ -457,12 +457,12 @@ def run_reference(args):
 
 
 # DRAM bytes per algorithmic byte of k_forward from the committed ncu captures
-# of the 200-column cases (97.41 MB of DRAM
+# of the 200-column cases (97.91 MB of DRAM
 # traffic for 136.84 MB of algorithmic bytes with bags of 1..20 values,
-# 126.39 MB for 197.08 MB with one value per bag).  A full launch is too large
+# 126.54 MB for 197.08 MB with one value per bag).  A full launch is too large
 # to capture; its traffic is the same ratio times its algorithmic bytes.  Set
 # to {} whenever k_forward changes until it is captured again.
-FORWARD_TRAFFIC_RATIO = {"inference": 97.41 / 136.84, "inference-onehot": 126.39 / 197.08}
+FORWARD_TRAFFIC_RATIO = {"inference": 97.91 / 136.84, "inference-onehot": 126.54 / 197.08}
 
 
 def traffic_estimate(workload, fbytes):
