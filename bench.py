@@ -456,13 +456,12 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-# DRAM bytes per algorithmic byte of k_forward from the committed ncu captures
-# of the 200-column cases (97.91 MB of DRAM
-# traffic for 136.84 MB of algorithmic bytes with bags of 1..20 values,
-# 126.54 MB for 197.08 MB with one value per bag).  A full launch is too large
-# to capture; its traffic is the same ratio times its algorithmic bytes.  Set
-# to {} whenever k_forward changes until it is captured again.
-FORWARD_TRAFFIC_RATIO = {"inference": 97.91 / 136.84, "inference-onehot": 126.54 / 197.08}
+# DRAM bytes per algorithmic byte of k_forward from the committed ncu capture
+# of the 200-column case (97.29 MB of DRAM traffic for 136.84 MB of
+# algorithmic bytes with bags of 1..20 values).  A full launch is too large
+# to capture; its traffic is the same ratio times its algorithmic bytes.
+# Remove an entry whenever k_forward changes until it is captured again.
+FORWARD_TRAFFIC_RATIO = {"inference": 97.29 / 136.84}
 
 
 def traffic_estimate(workload, fbytes):

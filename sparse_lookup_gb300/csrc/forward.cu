@@ -44,8 +44,7 @@ constexpr int kOneHotBags = 256;   // bags of one value each that one warp chunk
 constexpr int kFwdWarpsPerCta = kFwdThreads / kWarp;
 
 struct FwdArgs {
-  const ColMeta* meta;
-  const int32_t* stream_cols;
+  const ColMeta* meta;     // id-stream columns, then f-stream columns
   const int64_t* ids;
   const float* fvals;
   const float* wts[2];     // per-value weights of each stream (SUM columns), or null
@@ -238,6 +237,29 @@ __device__ int2 warp_lower_bound2(const int32_t* offs, int S, int64_t e_lo, int6
   const int64_t e = h ? e_hi : e_lo;
   bool bad = false;
   int lo = 0, hi = S;
+  if (S > 0) {
+    // First round: 16 probes around the segment a uniform spread of the n
+    // values over the S segments puts at e, over a window of about twice the
+    // square root of its distance to the nearer end (the spread of a sum of
+    // that many similar bag lengths).  If the answer lies outside the window
+    // the search goes on from there over the rest of [0, S].
+    const int g = e >= n ? S : (int)(e * (int64_t)S / (n > 1 ? n : 1));
+    const int d = min(g, S - g);
+    const int half_w = min(2048, 32 + 2 * (int)sqrtf((float)d));
+    const int wlo = max(0, g - half_w), whi = min(S, g + half_w);
+    const int wstep = max(1, (whi - wlo) / 15);
+    auto probe_at = [&](int j) { return min(wlo + j * wstep, S - 1); };
+    const bool less = clamp_off(__ldg(offs + probe_at(sl)), n, bad) < e;
+    const int k = __popc(__ballot_sync(kFull, less) & half);
+    if (k == 0) {
+      hi = probe_at(0);
+    } else if (k == 16) {
+      lo = probe_at(15) + 1;
+    } else {
+      lo = probe_at(k - 1) + 1;
+      hi = probe_at(k);
+    }
+  }
   for (;;) {
     const bool more = hi - lo > 16;
     if (!__any_sync(kFull, more)) break;
@@ -760,7 +782,7 @@ __device__ void warp_onehot_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta&
 // the kernel: one warp per element tile
 // ---------------------------------------------------------------------------
 template <bool WT, bool LP>
-__device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int64_t tile);
+__device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int st, int64_t tile);
 
 // Two schedules.  Static: one tile per warp, the grid covers all tiles (warps
 // of one CTA hold neighbouring tiles, whose offset searches share L1).
@@ -780,9 +802,10 @@ __global__ void __launch_bounds__(kFwdThreads, 4) k_forward(const FwdArgs a) {
   WarpSmem& ws = smem[warp];
   const int64_t n_tiles = a.tiles[0] + a.tiles[1];
   // the first tile of every warp is its warp index; tickets count from there
-  int64_t tile = (int64_t)blockIdx.x * kFwdWarpsPerCta + (threadIdx.x >> 5);
+  int64_t tile = (int64_t)blockIdx.x * kFwdWarpsPerCta + warp;
   while (tile < n_tiles) {
-    forward_tile<WT, LP>(a, ws, tile);
+    const int st = tile < a.tiles[0] ? 0 : 1;
+    forward_tile<WT, LP>(a, ws, st, st ? tile - a.tiles[0] : tile);
     if (!a.dynamic) break;   // static: one tile per warp
     unsigned long long tk = 0;
     if (lane == 0) tk = atomicAdd(&a.ticket[0], 1ull);
@@ -799,13 +822,8 @@ __global__ void __launch_bounds__(kFwdThreads, 4) k_forward(const FwdArgs a) {
 }
 
 template <bool WT, bool LP>
-__device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int64_t tile) {
+__device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int st, int64_t tile) {
   const int lane = threadIdx.x & 31;
-  int st = 0;
-  if (tile >= a.tiles[0]) {
-    st = 1;
-    tile -= a.tiles[0];
-  }
   const int S = a.ncols[st] * a.batch;
   const int32_t* offs = a.offs[st];
   const int64_t n = a.n[st];
@@ -820,10 +838,16 @@ __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int
     const int cl0 = (int)div_magic32((uint32_t)cur, a.bdiv);
     const int b0 = cur - cl0 * a.batch;
     const int navail = min(32, min(s_hi, (cl0 + 1) * a.batch) - cur);
+    // the bags' offsets and the column's metadata are loaded side by side
+    int32_t o_lo = 0, o_hi = 0;
+    if (lane < navail) {
+      o_lo = __ldg(offs + cur + lane);
+      o_hi = __ldg(offs + cur + lane + 1);
+    }
     static_assert(sizeof(ColMeta) % 4 == 0 && sizeof(ColMeta) / 4 <= 32, "metadata copy");
     if (lane < (int)(sizeof(ColMeta) / 4))
       reinterpret_cast<int32_t*>(&ws.cm)[lane] =
-          __ldg(reinterpret_cast<const int32_t*>(a.meta + __ldg(a.stream_cols + a.col_base[st] + cl0)) + lane);
+          __ldg(reinterpret_cast<const int32_t*>(a.meta + a.col_base[st] + cl0) + lane);
     __syncwarp();
     const ColMeta& m = ws.cm;
     const bool padded = m.pooling == EMB_POOL_NONE_PADDED;
@@ -832,8 +856,8 @@ __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int
     bool is_long = false, one = false;
     if (lane < navail) {
       bool bad = false;
-      lo = clamp_off(__ldg(offs + cur + lane), n, bad);
-      hi = clamp_off(__ldg(offs + cur + lane + 1), n, bad);
+      lo = clamp_off(o_lo, n, bad);
+      hi = clamp_off(o_hi, n, bad);
       if (hi < lo) { hi = lo; bad = true; }
       if (bad) latch(a.status, EMB_ERR_BAD_INDEX);
       one = !bad && hi - lo == 1;
@@ -985,7 +1009,6 @@ emb_status launch_forward(emb_plan_s* p, int32_t batch, const int64_t* ids, cons
   if (batch == 0) return EMB_OK;
   FwdArgs a{};
   a.meta = p->meta_d;
-  a.stream_cols = p->stream_cols_d;
   a.ids = ids;
   a.fvals = fvals;
   a.wts[0] = id_weights;

@@ -15,7 +15,6 @@ namespace {
 void free_plan(emb_plan_s* p) {
   if (!p) return;
   cudaFree(p->meta_d);
-  cudaFree(p->stream_cols_d);
   cudaFree(p->colg_d);
   cudaFree(p->tables_d);
   cudaFree(p->table_base_d);
@@ -200,16 +199,18 @@ extern "C" emb_status emb_plan_create(const emb_column_desc* cols, int32_t n_col
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess) e = dmalloc(&p->meta_d, n_cols, &total);
-  if (e == cudaSuccess) e = dmalloc(&p->stream_cols_d, sc.size(), &total);
   if (e == cudaSuccess) e = dmalloc(&p->colg_d, n_cols, &total);
   if (e == cudaSuccess) e = dmalloc(&p->tables_d, p->tables_h.size(), &total);
   if (e == cudaSuccess) e = dmalloc(&p->table_base_d, p->table_base_h.size(), &total);
   if (e == cudaSuccess) e = dmalloc(&p->status_d, 1, &total);
   if (e == cudaSuccess) e = dmalloc(&p->fwd_ticket, 2, &total);
   if (e == cudaSuccess) e = cudaMemset(p->fwd_ticket, 0, 2 * sizeof(unsigned long long));
-  if (e == cudaSuccess) e = cudaMemcpy(p->meta_d, p->meta_h.data(), sizeof(ColMeta) * n_cols, cudaMemcpyHostToDevice);
-  if (e == cudaSuccess && !sc.empty())
-    e = cudaMemcpy(p->stream_cols_d, sc.data(), sizeof(int32_t) * sc.size(), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) {
+    // the forward reads a column's metadata by its position in its stream
+    std::vector<ColMeta> ms(sc.size());
+    for (size_t i = 0; i < sc.size(); ++i) ms[i] = p->meta_h[sc[i]];
+    e = cudaMemcpy(p->meta_d, ms.data(), sizeof(ColMeta) * ms.size(), cudaMemcpyHostToDevice);
+  }
   if (e == cudaSuccess)
     e = cudaMemcpy(p->tables_d, p->tables_h.data(), sizeof(TableMeta) * p->tables_h.size(), cudaMemcpyHostToDevice);
   if (e == cudaSuccess)

@@ -70,8 +70,7 @@ struct emb_plan_s {
   std::vector<int32_t> table_first_col;   // first column of each table
   bool low_precision = false;            // some table is stored below fp32
   std::vector<uint32_t> table_base_h;  // [n_tables + 1]
-  emb::ColMeta* meta_d = nullptr;
-  int32_t* stream_cols_d = nullptr;    // id-stream columns, then f-stream columns
+  emb::ColMeta* meta_d = nullptr;      // id-stream columns, then f-stream columns, in plan order
   int4* colg_d = nullptr;              // per column: (out_col, 1 if MEAN, dim/4) for the backward
   emb::TableMeta* tables_d = nullptr;
   uint32_t* table_base_d = nullptr;
