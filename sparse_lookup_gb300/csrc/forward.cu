@@ -4,10 +4,12 @@
 // Work decomposition (element-count tiling, RecIS §3.1 "Thread mapping for
 // skewed inputs"): each of the two jagged value streams is cut into tiles of
 // E consecutive elements and every WARP owns one tile: the (column, bag)
-// segments whose FIRST element lies in the tile.  Each pooled output row
-// therefore has exactly one writer (RecIS §3.2 Algorithm 1, forward: no
-// atomics), and warps never wait on each other -- there is no CTA barrier,
-// so a warp stalled on memory never holds up another.
+// segments whose FIRST element lies in the tile.  A stream of short bags is
+// cut into runs of whole 32-bag chunks of about E values instead, which
+// need no search for their ends.  Each pooled output row therefore has
+// exactly one writer (RecIS §3.2 Algorithm 1, forward: no atomics), and
+// warps never wait on each other -- there is no CTA barrier, so a warp
+// stalled on memory never holds up another.
 //
 // A warp walks its segments in chunks that stay inside one column (one table,
 // one dim, one transform) and hold at most 32 bags and kWarpElems values of
@@ -41,6 +43,8 @@ constexpr int kU = 4;              // row loads in flight per lane (halved for t
 constexpr int kUA = 4;             // raw values in flight per lane in phase A
 constexpr int kUPool = 4;          // row loads in flight per lane when pooling short bags (8 spills)
 constexpr int kOneHotBags = 256;   // bags of one value each that one warp chunk copies
+constexpr int kMaxTileBags = 1024;  // static schedule: at most this many bags per tile
+constexpr int64_t kShortBagMean = 16;   // static schedule: streams with shorter bags tile by bags
 constexpr int kFwdWarpsPerCta = kFwdThreads / kWarp;
 
 struct FwdArgs {
@@ -53,7 +57,8 @@ struct FwdArgs {
   int32_t ncols[2];
   int32_t col_base[2];
   int64_t tiles[2];
-  int32_t tile_elems;
+  int32_t tile_elems;      // value tiles: values per tile
+  int32_t tile_bags[2];    // per stream: bags per tile, or 0 for value tiles
   int32_t batch;
   DivMagic32 bdiv;
   int64_t ldo;
@@ -827,11 +832,19 @@ __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int
   const int S = a.ncols[st] * a.batch;
   const int32_t* offs = a.offs[st];
   const int64_t n = a.n[st];
-  const int64_t e0 = tile * a.tile_elems;
-  const bool last = tile == a.tiles[st] - 1;
-  const int2 ends = warp_lower_bound2(offs, S, e0, last ? INT64_MAX : e0 + a.tile_elems, n);
-  int cur = ends.x;
-  const int s_hi = ends.y;
+  int cur, s_hi;
+  if (a.tile_bags[st] > 0) {
+    // a run of tile_bags consecutive bags
+    cur = (int)(tile * a.tile_bags[st]);
+    s_hi = min(S, cur + a.tile_bags[st]);
+  } else {
+    // a range of tile_elems values: the bags whose first value lies in it
+    const int64_t e0 = tile * a.tile_elems;
+    const bool last = tile == a.tiles[st] - 1;
+    const int2 ends = warp_lower_bound2(offs, S, e0, last ? INT64_MAX : e0 + a.tile_elems, n);
+    cur = ends.x;
+    s_hi = ends.y;
+  }
 
   while (cur < s_hi) {
     // ---- setup: one lane per bag, all inside column cl0 ----
@@ -1051,6 +1064,35 @@ emb_status launch_forward(emb_plan_s* p, int32_t batch, const int64_t* ids, cons
   a.tile_elems = (int32_t)E;
   a.tiles[0] = a.ncols[0] > 0 ? n_ids / E + 1 : 0;
   a.tiles[1] = a.ncols[1] > 0 ? n_fvals / E + 1 : 0;
+  if (!a.dynamic) {
+    // Streams of short bags (mean length <= kShortBagMean): a tile is a run
+    // of bags, about E values' worth rounded to whole 32-bag chunks, so its
+    // ends need no search -- the search is a large share of the chain of
+    // dependent loads such a small tile walks (measured on the inference,
+    // one-value and dynamic workloads: 0.184 -> 0.175 ms, 0.224 -> 0.220 ms,
+    // 0.220 -> 0.189 ms; 64-bag tiles were slower, 0.203 ms).  Longer bags
+    // keep value tiles: there the search is cheap beside the gathers and
+    // equal value counts per tile balance the warps (measured 4 % faster on
+    // the training workload than tiles of bags).  A launch too small to
+    // give every resident warp a tile keeps the smaller value tiles: there
+    // the number of warps in flight decides (200 inference columns: 55.7 us
+    // with value tiles, 65.3 us with 32-bag tiles).
+    const int64_t nv[2] = {n_ids, n_fvals};
+    int64_t k[2] = {0, 0}, t[2] = {a.tiles[0], a.tiles[1]};
+    for (int st = 0; st < 2; ++st) {
+      const int64_t S = (int64_t)batch * a.ncols[st];
+      if (S == 0 || nv[st] > kShortBagMean * S) continue;
+      const int64_t kb = nv[st] > 0 ? E * S / nv[st] : kMaxTileBags;
+      k[st] = std::min<int64_t>(std::max<int64_t>(kWarp, (kb + kWarp / 2) / kWarp * kWarp), kMaxTileBags);
+      t[st] = (S + k[st] - 1) / k[st];
+    }
+    if ((k[0] || k[1]) && t[0] + t[1] >= warps) {
+      for (int st = 0; st < 2; ++st) {
+        a.tile_bags[st] = (int32_t)k[st];
+        a.tiles[st] = t[st];
+      }
+    }
+  }
   const int64_t tiles = a.tiles[0] + a.tiles[1];
   if (tiles == 0) return EMB_OK;
   const int64_t resident = (int64_t)p->sm_count * p->fwd_ctas_per_sm;
