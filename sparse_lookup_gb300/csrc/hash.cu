@@ -203,7 +203,15 @@ __global__ void __launch_bounds__(256) k_hash_probe(const HashArgs h, const int3
   bool first = false;   // this occurrence moved last_seen to this step
   if (old >= 0) {
     out = old;
-    if ((uint32_t)(sw_seen >> 32) != step) first = atomicExch(&s->last_seen, step) != step;
+    if ((uint32_t)(sw_seen >> 32) != step) {
+      // Lanes of this warp that hold the same slot touch it with one
+      // exchange: a hot key's occurrences would otherwise queue thousands of
+      // atomics on one address.  The exchange still decides the call's first
+      // touch across warps; the other lanes of the group are not first.
+      const unsigned act = __activemask();
+      const unsigned grp = __match_any_sync(act, (unsigned long long)found);
+      if ((int)(threadIdx.x & 31) == __ffs(grp) - 1) first = atomicExch(&s->last_seen, step) != step;
+    }
   } else {
     // Count and touch with atomic updates of the whole (state, last_seen)
     // word, so that "first occurrence of this call" and "count reached the
