@@ -526,12 +526,12 @@ def run_reference(args):
 
 
 # DRAM bytes per algorithmic byte of k_forward from the committed ncu capture
-# of the 320-column case (154.82 MB of DRAM traffic for 226.27 MB of
+# of the 320-column case (154.67 MB of DRAM traffic for 226.27 MB of
 # algorithmic bytes with bags of 1..20 values, tiled by bags like the full
 # launch).  A full launch is too large to capture; its traffic is the same
 # ratio times its algorithmic bytes.  Remove an entry whenever k_forward
 # changes until it is captured again.
-FORWARD_TRAFFIC_RATIO = {"inference": 154.82 / 226.27}
+FORWARD_TRAFFIC_RATIO = {"inference": 154.67 / 226.27}
 
 
 def traffic_estimate(workload, fbytes):

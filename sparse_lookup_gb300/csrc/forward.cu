@@ -59,6 +59,9 @@ struct FwdArgs {
   int64_t tiles[2];
   int32_t tile_elems;      // value tiles: values per tile
   int32_t tile_bags[2];    // per stream: bags per tile, or 0 for value tiles
+  const int32_t* lpt;      // bag tiles: per stream, column positions in work order (null: stream order)
+  int32_t tpc[2];          // bag tiles in work order: tiles per column (batch / tile_bags), else 0
+  DivMagic32 tpc_div[2];
   int32_t batch;
   DivMagic32 bdiv;
   int64_t ldo;
@@ -810,7 +813,13 @@ __global__ void __launch_bounds__(kFwdThreads, 4) k_forward(const FwdArgs a) {
   int64_t tile = (int64_t)blockIdx.x * kFwdWarpsPerCta + warp;
   while (tile < n_tiles) {
     const int st = tile < a.tiles[0] ? 0 : 1;
-    forward_tile<WT, LP>(a, ws, st, st ? tile - a.tiles[0] : tile);
+    int64_t lt = st ? tile - a.tiles[0] : tile;
+    if (a.tpc[st] > 0) {
+      // bag tiles whole columns apart: take the columns in work order
+      const int j = (int)div_magic32((uint32_t)lt, a.tpc_div[st]);
+      lt = (int64_t)__ldg(a.lpt + a.col_base[st] + j) * a.tpc[st] + (lt - (int64_t)j * a.tpc[st]);
+    }
+    forward_tile<WT, LP>(a, ws, st, lt);
     if (!a.dynamic) break;   // static: one tile per warp
     unsigned long long tk = 0;
     if (lane == 0) tk = atomicAdd(&a.ticket[0], 1ull);
@@ -1090,6 +1099,16 @@ emb_status launch_forward(emb_plan_s* p, int32_t batch, const int64_t* ids, cons
       for (int st = 0; st < 2; ++st) {
         a.tile_bags[st] = (int32_t)k[st];
         a.tiles[st] = t[st];
+        // Tiles that split the batch evenly cover whole columns: deal them
+        // column by column, widest stored rows first, so the longest tiles
+        // start early and the launch does not end on them (inference
+        // 0.175 -> 0.170 ms; a launch in stream order that ends on wide
+        // columns leaves SMs idle while their last tiles run).
+        if (k[st] > 0 && batch % k[st] == 0 && p->lpt_d) {
+          a.lpt = p->lpt_d;
+          a.tpc[st] = (int32_t)(batch / k[st]);
+          a.tpc_div[st] = make_div_magic32((uint32_t)a.tpc[st]);
+        }
       }
     }
   }
