@@ -1007,12 +1007,83 @@ def bench_dynamic(torch, sl, w, args, dev, stream, flush):
     et, _ = timed_steps(torch, min(args.steps, 5), stream, flush, e2e_body)
     res["e2e_ms"] = statistics.mean(et["e2e"])
     res["e2e"] = {"value": valid / (res["e2e_ms"] / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
-                  "d2h_bytes_per_step": out_p.numel() * 4}
+                  "d2h_bytes_per_step": out_p.numel() * 4,
+                  "mode": "one step at a time: H2D, step, D2H in order on one stream"}
+    # the same steps streamed (the keys of step i+1 copied in and the pooled
+    # output of step i copied out beside the step's kernels)
+    ms = e2e_dynamic_streamed(torch, ht, plan, w, min(args.steps, 5), stream, flush, hb, rows, out, out_p, G,
+                              state)
+    serial = res["e2e"]
+    res["e2e"] = {"value": valid / (ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+                  "d2h_bytes_per_step": out_p.numel() * 4,
+                  "mode": "streamed: step i+1's keys in and step i's pooled output out beside the step's kernels "
+                          "(double buffers, three streams, L2 flushed before each step inside the timed region)",
+                  "one_step_at_a_time": {"value": serial["value"], "ms_per_step": res["e2e_ms"]},
+                  "ms_per_step": ms}
+    res["e2e_ms"] = ms
     res["ceiling"] = gather_ceiling(torch, sl, {dim * 4: valid}, dev) if not args.no_ceiling else None
     if not args.no_cpu_baseline and dist_env()[0] == 0:
         rate, sample = cpu_dynamic_sample(w, budget_s=12.0)
         res["cpu"] = {"value": rate, "unit": "rows/s", "cores": 1, "kind": "oracle", "sample": sample}
     return res
+
+
+def e2e_dynamic_streamed(torch, ht, plan, w, steps, comp, flush, hb, rows, out, out_p, G, state):
+    """Mean ms per dynamic-table step through the public calls, every step's
+    keys, table ids and offsets copied in from pinned host memory and its
+    pooled output copied back, the copies on their own streams beside the
+    kernels (two sets of device buffers; a set is refilled only after the
+    step that used it is done)."""
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    B, ttl = w.B, w.extra["ttl"]
+    bufs = [[d for _, d in hb], [torch.empty_like(d) for _, d in hb]]
+    outb = [out, torch.empty_like(out)]
+    outp = [out_p, torch.empty(out.shape, dtype=out.dtype).pin_memory()]
+    n = hb[1][1].numel()
+
+    def run(k):
+        ev_in = [torch.cuda.Event() for _ in range(k)]
+        ev_fwd = [torch.cuda.Event() for _ in range(k)]
+        ev_done = [torch.cuda.Event() for _ in range(k)]
+        ev_out = [torch.cuda.Event() for _ in range(k)]
+        a, b_ = event_pair(torch)
+        torch.cuda.synchronize()
+        a.record(s_in)
+        for i in range(k):
+            b = i % 2
+            if i >= 2:
+                s_in.wait_event(ev_done[i - 2])
+            with torch.cuda.stream(s_in):
+                for (src, _), dst in zip(hb, bufs[b]):
+                    dst.copy_(src, non_blocking=True)
+            ev_in[i].record(s_in)
+            comp.wait_event(ev_in[i])
+            if i >= 2:
+                comp.wait_event(ev_out[i - 2])
+            flush.fill_(float(i))
+            t = state["t"]
+            tids, keys, off = bufs[b]
+            ht.lookup_or_insert(tids, keys, t, rows_out=rows[:n], stream=comp)
+            plan.forward(B, rows[:n], off, None, None, out=outb[b], stream=comp)
+            ev_fwd[i].record(comp)
+            s_out.wait_event(ev_fwd[i])
+            with torch.cuda.stream(s_out):
+                outp[b].copy_(outb[b], non_blocking=True)
+            ev_out[i].record(s_out)
+            plan.backward_update(G, None, w.lr, w.eps, stream=comp)
+            ht.evict_expired(t, ttl, stream=comp)
+            ev_done[i].record(comp)
+            state["t"] = t + 1
+        s_out.wait_event(ev_done[k - 1])
+        b_.record(s_out)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b_) / k
+
+    run(2)
+    ms = run(steps)
+    if ht.device_status() not in (0, 5) or plan.device_status() != 0:
+        raise SystemExit("device status after the streamed steps")
+    return ms
 
 
 def pipelined_steps(torch, ht, plan, batches, state, w, args, stream, G, out):
