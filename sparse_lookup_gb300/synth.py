@@ -382,6 +382,62 @@ def random_small(seed: int, C: int | None = None, B: int | None = None, train: b
     return Workload("random%d" % seed, B, cols, tabs, offs, vals, lr=0.05, train=train, seed=seed, weights=wts)
 
 
+def random_many_bags(seed: int, B: int = 4096, C: int = 96, train: bool = True) -> Workload:
+    """Mixed plans with many short bags (mean length about 4), large enough
+    that a launch tiles its streams by bags on a 152-SM GPU: every transform
+    and pooling (padded columns with short pad_len), dims 4..128, empty bags,
+    rare long bags of 129..400 values, columns of one-value bags, truncated
+    bags, shared tables, value weights on some plans."""
+    r = np.random.default_rng([seed, 17])
+    cols, tabs, offs, vals = [], [], [], []
+    for c in range(C):
+        kind = str(r.choice(["identity", "hash_mod", "bucketize", "hash_mod"]))
+        dim = int(r.choice((4, 8, 12, 16, 32, 64, 128)))
+        pooling = str(r.choice(["sum", "mean", "sum", "mean", "padded"]))
+        if r.random() < 0.1:
+            lens = np.ones(B, np.int64)
+            lens[r.random(B) < 0.02] = 0
+        else:
+            lens = r.integers(0, 9, B)
+            lens[r.random(B) < 0.1] = 0
+            long = r.random(B) < 0.002
+            lens[long] = r.integers(129, 401, int(long.sum()))
+        n = int(lens.sum())
+        bnd = None
+        if kind == "bucketize":
+            bnd = np.unique(np.sort(r.standard_normal(int(r.integers(1, 60))).astype(np.float32)))
+            rows = int(bnd.size) + 1
+            v = r.standard_normal(n).astype(np.float32)
+            v[r.random(n) < 0.02] = np.nan
+        else:
+            rows = int(r.integers(1, 50000))
+            if kind == "identity":
+                v = r.integers(-3, rows + 3, n, dtype=np.int64)
+            else:
+                v = r.integers(-2 ** 63, 2 ** 63 - 1, n, dtype=np.int64, endpoint=True)
+        table = c
+        if c > 0 and kind != "bucketize" and r.random() < 0.15:
+            prev = [i for i, pc in enumerate(cols) if pc.transform != "bucketize"]
+            if prev:
+                j = int(r.choice(prev))
+                table, rows, dim = cols[j].table, cols[j].num_rows, cols[j].dim
+                if kind == "identity":
+                    v = r.integers(-3, rows + 3, n, dtype=np.int64)
+        default = r.standard_normal(dim).astype(np.float32) if r.random() < 0.2 else None
+        pad = int(r.integers(1, 13)) if pooling == "padded" else 0
+        trunc = int(r.integers(1, 6)) if pooling != "padded" and r.random() < 0.15 else 0
+        cols.append(ColumnSpec(kind, pooling, rows, dim, table, boundaries=bnd, default=default, pad_len=pad,
+                               max_len=trunc))
+        tabs.append(TableSpec(rows, dim, seed * 1000 + 500 + c) if table == c else None)
+        offs.append(bag_offsets(lens))
+        vals.append(v)
+    wts = None
+    if r.random() < 0.5:
+        wts = [r.uniform(-1.0, 2.0, int(o[-1])).astype(np.float32) for o in offs]
+    return Workload("many_bags%d" % seed, B, cols, tabs, offs, vals, lr=0.05, train=train, seed=seed,
+                    weights=wts)
+
+
 # --------------------------------------------------------------------------
 # materialisation helpers (inputs only)
 # --------------------------------------------------------------------------

@@ -29,6 +29,13 @@ def test_random_small_plans(seed):
     check_train_step(TrainStep(synth.random_small(100 + seed)))
 
 
+@pytest.mark.parametrize("seed,B,C", [(4, 4096, 96), (5, 3000, 128)])
+def test_many_short_bags_training_step(seed, B, C):
+    """A training step over a forward whose short-bag streams tile by runs of
+    32-bag chunks (the records it writes feed the backward)."""
+    check_train_step(TrainStep(synth.random_many_bags(seed, B, C)))
+
+
 def test_well_conditioned_accumulator_start():
     """acc0 = 0.1: no first-step sign sensitivity, nothing excluded."""
     assert check_train_step(TrainStep(synth.random_small(7), acc_init=0.1)) == 0

@@ -64,6 +64,19 @@ def test_random_small_plans(seed):
     check_full(w, m, out, seq, rows)
 
 
+@pytest.mark.parametrize("seed,B,C", [(0, 4096, 96), (1, 3000, 128), (2, 4096, 96), (3, 3000, 128)])
+def test_many_short_bags(seed, B, C):
+    """Launches with more tiles than a GB300 holds warps, whose short-bag
+    streams are cut into runs of 32-bag chunks instead of value tiles: dealt
+    column by column, widest rows first, where the tiles split the batch
+    evenly (B 4096); tiles across column ends where they do not (B 3000).
+    Long, empty and one-value bags, padded and truncated columns, weights,
+    shared tables."""
+    w = synth.random_many_bags(seed, B, C)
+    m, plan, out, seq, rows = run_forward(w)
+    check_full(w, m, out, seq, rows)
+
+
 @pytest.mark.parametrize("seed", range(12))
 def test_one_value_bags(seed):
     """Runs of one-value bags (copied without pooling, up to 256 bags per
