@@ -845,7 +845,7 @@ __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int
   if (a.tile_bags[st] > 0) {
     // a run of tile_bags consecutive bags
     cur = (int)(tile * a.tile_bags[st]);
-    s_hi = min(S, cur + a.tile_bags[st]);
+    s_hi = (int)min((int64_t)S, (int64_t)cur + a.tile_bags[st]);
   } else {
     // a range of tile_elems values: the bags whose first value lies in it
     const int64_t e0 = tile * a.tile_elems;
