@@ -525,13 +525,14 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-# DRAM bytes per algorithmic byte of k_forward from the committed ncu capture
-# of the 320-column case (154.67 MB of DRAM traffic for 226.27 MB of
-# algorithmic bytes with bags of 1..20 values, tiled by bags like the full
-# launch).  A full launch is too large to capture; its traffic is the same
-# ratio times its algorithmic bytes.  Remove an entry whenever k_forward
-# changes until it is captured again.
-FORWARD_TRAFFIC_RATIO = {"inference": 154.67 / 226.27}
+# DRAM bytes per algorithmic byte of k_forward from the committed ncu captures
+# of the 320-column cases, tiled by bags like the full launches (154.75 MB of
+# DRAM traffic for 226.27 MB of algorithmic bytes with bags of 1..20 values;
+# 246.92 MB for 326.92 MB with one value per bag at batch 4096).  A full
+# launch is too large to capture; its traffic is the same ratio times its
+# algorithmic bytes.  Remove an entry whenever k_forward changes until it is
+# captured again.
+FORWARD_TRAFFIC_RATIO = {"inference": 154.75 / 226.27, "inference-onehot": 246.92 / 326.92}
 
 
 def traffic_estimate(workload, fbytes):
