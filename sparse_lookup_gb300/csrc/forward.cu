@@ -59,7 +59,7 @@ struct FwdArgs {
   int64_t tiles[2];
   int32_t tile_elems;      // value tiles: values per tile
   int32_t tile_bags[2];    // per stream: bags per tile, or 0 for value tiles
-  const int32_t* lpt;      // bag tiles: per stream, column positions in work order (null: stream order)
+  const int32_t* col_order;  // bag tiles: per stream, column positions in work order (null: stream order)
   int32_t tpc[2];          // bag tiles in work order: tiles per column (batch / tile_bags), else 0
   DivMagic32 tpc_div[2];
   int32_t batch;
@@ -817,7 +817,7 @@ __global__ void __launch_bounds__(kFwdThreads, 4) k_forward(const FwdArgs a) {
     if (a.tpc[st] > 0) {
       // bag tiles whole columns apart: take the columns in work order
       const int j = (int)div_magic32((uint32_t)lt, a.tpc_div[st]);
-      lt = (int64_t)__ldg(a.lpt + a.col_base[st] + j) * a.tpc[st] + (lt - (int64_t)j * a.tpc[st]);
+      lt = (int64_t)__ldg(a.col_order + a.col_base[st] + j) * a.tpc[st] + (lt - (int64_t)j * a.tpc[st]);
     }
     forward_tile<WT, LP>(a, ws, st, lt);
     if (!a.dynamic) break;   // static: one tile per warp
@@ -1104,8 +1104,8 @@ emb_status launch_forward(emb_plan_s* p, int32_t batch, const int64_t* ids, cons
         // start early and the launch does not end on them (inference
         // 0.175 -> 0.170 ms; a launch in stream order that ends on wide
         // columns leaves SMs idle while their last tiles run).
-        if (k[st] > 0 && batch % k[st] == 0 && p->lpt_d) {
-          a.lpt = p->lpt_d;
+        if (k[st] > 0 && batch % k[st] == 0 && p->col_order_d) {
+          a.col_order = p->col_order_d;
           a.tpc[st] = (int32_t)(batch / k[st]);
           a.tpc_div[st] = make_div_magic32((uint32_t)a.tpc[st]);
         }

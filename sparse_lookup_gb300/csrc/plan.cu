@@ -20,7 +20,7 @@ void free_plan(emb_plan_s* p) {
   cudaFree(p->table_base_d);
   cudaFree(p->status_d);
   cudaFree(p->fwd_ticket);
-  cudaFree(p->lpt_d);
+  cudaFree(p->col_order_d);
   Workspace& w = p->ws;
   cudaFree(w.keys[0]);
   cudaFree(w.keys[1]);
@@ -215,7 +215,7 @@ extern "C" emb_status emb_plan_create(const emb_column_desc* cols, int32_t n_col
   if (e == cudaSuccess && !sc.empty()) {
     // work order of the forward's bag tiles: within each stream, the columns
     // with the widest stored rows first (ties in plan order)
-    std::vector<int32_t> lpt;
+    std::vector<int32_t> order;
     for (int st = 0; st < 2; ++st) {
       std::vector<int32_t> pos(stream_cols[st].size());
       for (size_t i = 0; i < pos.size(); ++i) pos[i] = (int32_t)i;
@@ -225,10 +225,10 @@ extern "C" emb_status emb_plan_create(const emb_column_desc* cols, int32_t n_col
         return (int64_t)d.dim * el;
       };
       std::stable_sort(pos.begin(), pos.end(), [&](int32_t x, int32_t y) { return row_bytes(x) > row_bytes(y); });
-      lpt.insert(lpt.end(), pos.begin(), pos.end());
+      order.insert(order.end(), pos.begin(), pos.end());
     }
-    e = dmalloc(&p->lpt_d, lpt.size(), &total);
-    if (e == cudaSuccess) e = cudaMemcpy(p->lpt_d, lpt.data(), sizeof(int32_t) * lpt.size(), cudaMemcpyHostToDevice);
+    e = dmalloc(&p->col_order_d, order.size(), &total);
+    if (e == cudaSuccess) e = cudaMemcpy(p->col_order_d, order.data(), sizeof(int32_t) * order.size(), cudaMemcpyHostToDevice);
   }
   if (e == cudaSuccess)
     e = cudaMemcpy(p->tables_d, p->tables_h.data(), sizeof(TableMeta) * p->tables_h.size(), cudaMemcpyHostToDevice);

@@ -84,7 +84,7 @@ struct emb_plan_s {
   int key_bits = 0;
   uint32_t* status_d = nullptr;
   unsigned long long* fwd_ticket = nullptr;   // forward tile tickets (next tile, warps done)
-  int32_t* lpt_d = nullptr;   // per stream: its columns' stream positions, widest stored rows first
+  int32_t* col_order_d = nullptr;   // per stream: its columns' stream positions, widest stored rows first
   int sm_count = 0;
   int fwd_ctas_per_sm = 0;
   emb::Workspace ws;
