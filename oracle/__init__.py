@@ -89,6 +89,8 @@ def lib():
         L.orc_hash_evict.argtypes = [c_void_p, c_uint32, c_uint32]
         L.orc_hash_export.restype = c_int64
         L.orc_hash_export.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64]
+        L.orc_hash_last_admitted.restype = c_int64
+        L.orc_hash_last_admitted.argtypes = [c_void_p, c_void_p, c_int64]
         for f in ("orc_hash_size", "orc_hash_bump", "orc_hash_free_count"):
             getattr(L, f).restype = c_int64
             getattr(L, f).argtypes = [c_void_p]
@@ -248,7 +250,8 @@ def backward_adagrad(cols, B, offsets, values, G, Gseq, W, acc, lr, eps, weights
 
 def backward_rows(cols, B, offsets, values, G, Gseq, targets, W_rows, acc_rows, lr, eps, weights=None):
     """The backward + Adagrad of backward_adagrad restricted to chosen rows,
-    for tables too large to copy to the host.  targets: (table, row) pairs;
+    for tables too large to copy to the host.  targets: (table, row) pairs,
+    or a tuple of two arrays (tables int32, rows int64);
     W_rows / acc_rows: float32 [n_targets, dim] host copies of those rows
     before the step, updated in place.  Each target's gradient is summed in
     the same order as backward_adagrad sums it.  Returns dict(table, row,
@@ -260,10 +263,14 @@ def backward_rows(cols, B, offsets, values, G, Gseq, targets, W_rows, acc_rows, 
     ids, fv = _values(cols, values)
     G = np.ascontiguousarray(G, np.float32) if G is not None else np.zeros((B, 1), np.float32)
     gs = [None if g is None else np.ascontiguousarray(g, np.float32) for g in (Gseq or [None] * C)]
-    t_table = np.ascontiguousarray([t for t, _ in targets], np.int32)
-    t_row = np.ascontiguousarray([r for _, r in targets], np.int64)
+    if isinstance(targets, tuple) and len(targets) == 2 and isinstance(targets[0], np.ndarray):
+        t_table = np.ascontiguousarray(targets[0], np.int32)
+        t_row = np.ascontiguousarray(targets[1], np.int64)
+    else:
+        t_table = np.ascontiguousarray([t for t, _ in targets], np.int32)
+        t_row = np.ascontiguousarray([r for _, r in targets], np.int64)
     order = np.lexsort((t_row, t_table))
-    assert np.array_equal(order, np.arange(len(targets))), "targets must ascend by (table, row)"
+    assert np.array_equal(order, np.arange(t_row.size)), "targets must ascend by (table, row)"
     assert W_rows.dtype == np.float32 and W_rows.flags.c_contiguous and W_rows.shape == acc_rows.shape
     assert acc_rows.dtype == np.float32 and acc_rows.flags.c_contiguous
     n, ld = W_rows.shape
@@ -345,6 +352,14 @@ class Hash:
 
     def free_count(self):
         return int(lib().orc_hash_free_count(self._h))
+
+    def last_admitted(self):
+        """Rows the last lookup_or_insert handed out (and initialised), in
+        admission order."""
+        n = int(lib().orc_hash_last_admitted(self._h, None, 0))
+        out = np.empty(max(n, 1), np.int64)
+        lib().orc_hash_last_admitted(self._h, _ptr(out), n)
+        return out[:n]
 
     def export(self):
         """All live entries as a dict of arrays sorted by (tid, key)."""

@@ -29,7 +29,7 @@
  *            (collision-free table, admission after an occurrence threshold,
  *            expiry of IDs idle longer than a per-table period).
  *
- * Readings where the pages are silent (each is restated in the design doc):
+ * Readings where the pages are silent (each is restated in the design notes):
  *  - hash transform = one output step of SplitMix64 (Steele, Lea & Flood,
  *    OOPSLA 2014, as in Vigna's splitmix64.c) with the state set to the ID
  *    reinterpreted as u64, then unsigned 64-bit modulo the table rows;
@@ -528,6 +528,8 @@ typedef struct orc_hash {
     int64_t* free_rows; /* rows released by expiry */
     int64_t n_free, cap_free;
     int64_t bump;       /* rows >= bump were never handed out */
+    int64_t* admitted;  /* rows handed out by the last lookup, in admission order */
+    int64_t n_admitted, cap_admitted;
 } orc_hash;
 
 static uint64_t bucket_of(const orc_hash* h, int32_t tid, int64_t key)
@@ -555,8 +557,10 @@ orc_hash* orc_hash_create(int64_t row_capacity, int32_t dim, int32_t threshold,
     h->ent = (orc_entry*)malloc(sizeof(orc_entry) * (size_t)h->cap_ent);
     h->cap_free = 1 << 10;
     h->free_rows = (int64_t*)malloc(sizeof(int64_t) * (size_t)h->cap_free);
-    if (!h->heads || !h->ent || !h->free_rows) {
-        free(h->heads); free(h->ent); free(h->free_rows); free(h);
+    h->cap_admitted = 1 << 10;
+    h->admitted = (int64_t*)malloc(sizeof(int64_t) * (size_t)h->cap_admitted);
+    if (!h->heads || !h->ent || !h->free_rows || !h->admitted) {
+        free(h->heads); free(h->ent); free(h->free_rows); free(h->admitted); free(h);
         return NULL;
     }
     for (int64_t i = 0; i < h->nbuckets; ++i) h->heads[i] = -1;
@@ -570,6 +574,7 @@ void orc_hash_destroy(orc_hash* h)
     free(h->heads);
     free(h->ent);
     free(h->free_rows);
+    free(h->admitted);
     free(h);
 }
 
@@ -672,6 +677,7 @@ int orc_hash_lookup_or_insert(orc_hash* h, const int32_t* tids, const int64_t* k
 {
     if (!h || n < 0) return ORC_ERR_ARG;
     int status = ORC_OK;
+    h->n_admitted = 0;
     /* 1. count every occurrence and touch its entry */
     int64_t n_new = 0;
     for (int64_t i = 0; i < n; ++i) {
@@ -703,6 +709,12 @@ int orc_hash_lookup_or_insert(orc_hash* h, const int32_t* tids, const int64_t* k
             }
         }
         qsort(nk, (size_t)m, sizeof(newkey), cmp_newkey);
+        if (m > h->cap_admitted) {
+            int64_t* na = (int64_t*)realloc(h->admitted, sizeof(int64_t) * (size_t)m);
+            if (!na) { free(nk); return ORC_ERR_OOM; }
+            h->admitted = na;
+            h->cap_admitted = m;
+        }
         qsort(h->free_rows, (size_t)h->n_free, sizeof(int64_t), cmp_i64);
         int64_t used_free = 0;
         for (int64_t k = 0; k < m; ++k) {
@@ -713,6 +725,7 @@ int orc_hash_lookup_or_insert(orc_hash* h, const int32_t* tids, const int64_t* k
             else { x->row = -1; status = ORC_ERR_FULL; continue; }
             x->admitted = 1;
             x->row = row;
+            h->admitted[h->n_admitted++] = row;
             for (int32_t d = 0; d < h->dim; ++d) {
                 h->W[row * h->dim + d] = orc_hash_init_value(h->seed, x->tid, x->key, d, h->init_scale);
                 h->acc[row * h->dim + d] = 0.0f;
@@ -784,6 +797,15 @@ int64_t orc_hash_export(const orc_hash* h, int32_t* tids, int64_t* keys, int64_t
             ++k;
         }
     return k;
+}
+
+/* Rows the last lookup handed out (and initialised), in admission order.
+ * Returns their number (all are written when cap allows). */
+int64_t orc_hash_last_admitted(const orc_hash* h, int64_t* rows, int64_t cap)
+{
+    if (!h) return 0;
+    for (int64_t i = 0; i < h->n_admitted && i < cap; ++i) rows[i] = h->admitted[i];
+    return h->n_admitted;
 }
 
 int64_t orc_hash_size(const orc_hash* h) { return h ? h->live : 0; }

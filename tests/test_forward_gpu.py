@@ -9,7 +9,7 @@ from sparse_lookup_gb300 import build as slbuild
 from sparse_lookup_gb300 import synth
 from sparse_lookup_gb300.synth import ColumnSpec, TableSpec, Workload
 
-from helpers import Materialized, assert_close, oracle_sampled_forward, pooled_slices, seq_slices
+from helpers import Materialized, assert_close, pooled_slices, seq_slices
 
 pytestmark = pytest.mark.gpu
 
@@ -179,22 +179,42 @@ def test_deterministic():
 
 
 @pytest.mark.slow
-def test_inference_workload_full_size_sampled():
-    """1000-column inference workload at full size (the configuration the
-    forward benchmark times): every transformed row is checked bit-exactly
-    against the oracle; pooled outputs on 3000 sampled bags."""
-    import torch
+def test_inference_workload_full_size_every_output():
+    """1000-column inference workload at full size, in the launch
+    configuration the forward benchmark times: every transformed row
+    bit-exact and every pooled output element (512 x 30k) within 1e-5 rel /
+    1e-6 abs of the oracle, which runs on chunks of columns whose tables are
+    copied to the host a chunk at a time."""
+    import dataclasses
     w = synth.inference()
     m, plan, out, seq, rows_dbg = run_forward(w)
     got_rows = m.rows_dbg_split(rows_dbg)
     for c in range(0, len(w.columns)):
         ref = oracle.column_rows(w.columns[c], w.values[c])
         assert np.array_equal(got_rows[c], ref), c
-    rng = np.random.default_rng(0)
-    bags = [(int(c), int(b)) for c, b in zip(rng.integers(0, len(w.columns), 3000), rng.integers(0, w.B, 3000))]
-    ref = oracle_sampled_forward(w, m.tables, bags)
-    sl_, _ = pooled_slices(w.columns)
+    psl, _ = pooled_slices(w.columns)
     o = out.cpu().numpy()
-    for (c, b), v in ref.items():
-        off, d = sl_[c]
-        assert_close(o[b, off:off + d], v, "bag %s" % ((c, b),))
+    checked = 0
+
+    def run_chunk(chunk):
+        specs = [dataclasses.replace(w.columns[c], table=j) for j, c in enumerate(chunk)]
+        tabs = [m.tables[w.columns[c].table].cpu().numpy() for c in chunk]
+        ref, _ = oracle.forward(specs, w.B, [w.offsets[c] for c in chunk], [w.values[c] for c in chunk], tabs)
+        pos = 0
+        for c in chunk:
+            off, d = psl[c]
+            assert_close(o[:, off:off + d], ref[:, pos:pos + d], "column %d" % c)
+            pos += d
+        return sum(w.columns[c].dim for c in chunk) * w.B
+
+    chunk, held = [], 0
+    for c, col in enumerate(w.columns):
+        nbytes = col.num_rows * col.dim * 4
+        if chunk and held + nbytes > (1 << 30):
+            checked += run_chunk(chunk)
+            chunk, held = [], 0
+        chunk.append(c)
+        held += nbytes
+    if chunk:
+        checked += run_chunk(chunk)
+    assert checked == o.size

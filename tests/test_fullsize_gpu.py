@@ -2,20 +2,24 @@
 the 200-column training step, the 20-column sequence workload (mean and
 padded), and 50 steps of the dynamic hash-table stream.
 
-Tables of these workloads are too large to copy to the host, so the checks
-are on samples the oracle can compute one by one: pooled outputs of sampled
-bags (a compact one-bag problem each), unique rows and counts of the whole
-step (bit-exact), and the aggregated gradient and Adagrad update of sampled
-rows -- the hottest rows (their contributions span many CTAs) plus random
-ones -- computed by the oracle's backward restricted to those rows.
+Every output is checked.  The tables are too large to copy to the host at
+once, so the oracle runs one column at a time (each of these workloads gives
+every column a table of its own): the column's table is copied to the host
+for its forward; for its backward the table's initial values are drawn
+again from their seed on the device and the touched rows gathered, so the
+oracle's backward restricted to those rows (orc_backward_rows) starts from
+the same rows the library updated.  Unique rows and counts of the whole step
+are bit-exact; every pooled output, every padded copy (bit-exact), every
+touched row's aggregated gradient, weights and accumulator are compared.
 """
+import dataclasses
 import gc
 
 import numpy as np
 import pytest
 
 import oracle
-from helpers import (Materialized, assert_close, check_row_update, compare_hash_maps, oracle_sampled_forward,
+from helpers import (Materialized, assert_close, assert_close_skip, check_rows, compare_hash_maps, excluded_cap,
                      pooled_slices, seq_slices, DynamicRun)
 from sparse_lookup_gb300 import synth
 
@@ -28,48 +32,33 @@ def _free():
     torch.cuda.empty_cache()
 
 
-def _check_sampled_forward(w, m, out, seq, n_bags, rng):
-    bags = [(int(c), int(b)) for c, b in zip(rng.integers(0, len(w.columns), n_bags), rng.integers(0, w.B, n_bags))]
-    ref = oracle_sampled_forward(w, m.tables, bags)
-    psl, _ = pooled_slices(w.columns)
-    ssl, _ = seq_slices(w.columns, w.B)
-    o = out.cpu().numpy() if out is not None and out.numel() else None
-    for (c, b), v in ref.items():
-        if w.columns[c].pooling == "padded":
-            start, shape = ssl[c]
-            n = int(np.prod(shape[1:]))
-            got = seq[start + b * n:start + (b + 1) * n].cpu().numpy().reshape(shape[1:])
-            assert np.array_equal(got, v), "padded bag %s" % ((c, b),)   # a copy: bit-exact
-        else:
-            off, d = psl[c]
-            assert_close(o[b, off:off + d], v, "bag %s" % ((c, b),))
-
-
-def _full_training_step(w, n_bags=1500, n_hot=16, n_rand=300):
-    """Forward + backward/Adagrad of workload w at full size, checked on
-    samples against the oracle."""
+def _full_training_step(w):
+    """Forward + backward/Adagrad of workload w at full size, every output
+    checked against the oracle column by column."""
     import torch
     import sparse_lookup_gb300 as sl
+    assert len({c.table for c in w.columns}) == len(w.columns), "one table per column"
     m = Materialized(w, "cuda", with_acc=True, acc_init=0.0)
     plan = sl.Plan(w.columns, m.tables, m.accs, max_batch=w.B, max_ids=m.n_ids + m.n_f, training=True)
     out, seq = plan.forward(w.B, m.ids, m.id_off, m.fv, m.f_off)
     torch.cuda.synchronize()
     assert plan.device_status() == 0
-    rng = np.random.default_rng(2024)
-    _check_sampled_forward(w, m, out, seq, n_bags, rng)
+    psl, _ = pooled_slices(w.columns)
+    ssl, _ = seq_slices(w.columns, w.B)
+    o = out.cpu().numpy() if out is not None and out.numel() else None
 
-    # rows to follow through the backward: the hottest and random ones
-    u = oracle.unique_counts(w.columns, w.B, w.offsets, w.values)
-    order = np.argsort(-u["count"], kind="stable")
-    pick = np.unique(np.concatenate([order[:n_hot], rng.choice(len(u["row"]), n_rand, replace=False)]))
-    targets = [(int(u["table"][i]), int(u["row"][i])) for i in pick]
-    dims = {c.table: c.dim for c in w.columns}
-    ld = max(dims.values())
-    W0 = np.zeros((len(targets), ld), np.float32)
-    A0 = np.zeros((len(targets), ld), np.float32)
-    for k, (t, r) in enumerate(targets):
-        W0[k, :dims[t]] = m.tables[t][r].cpu().numpy()
-        A0[k, :dims[t]] = m.accs[t][r].cpu().numpy()
+    # forward: every pooled element and every padded copy, one column at a time
+    for c, col in enumerate(w.columns):
+        spec = dataclasses.replace(col, table=0)
+        ref, rseq = oracle.forward([spec], w.B, [w.offsets[c]], [w.values[c]], [m.tables[col.table].cpu().numpy()])
+        if col.pooling == "padded":
+            start, shape = ssl[c]
+            got = seq[start:start + int(np.prod(shape))].cpu().numpy().reshape(shape)
+            assert np.array_equal(got, rseq[0]), "padded column %d" % c   # a copy: bit-exact
+        else:
+            off, d = psl[c]
+            assert_close(o[:, off:off + d], ref, "column %d" % c)
+    del o
 
     width = plan.out_width
     G = synth.make_grad((w.B, max(width, 1)), 77, "cuda")[:, :width].contiguous() if width else None
@@ -79,36 +68,52 @@ def _full_training_step(w, n_bags=1500, n_hot=16, n_rand=300):
     assert plan.device_status() == 0
 
     # unique rows and counts of the whole step: bit-exact
+    u = oracle.unique_counts(w.columns, w.B, w.offsets, w.values)
     col_table = plan.info["col_table"]
     t2s = {}
     for c, t in zip(w.columns, col_table):
         t2s.setdefault(int(t), c.table)
     gt = np.array([t2s[int(t)] for t in dbg["table"].cpu().numpy()], np.int64)
-    grow = dbg["row"].cpu().numpy()
     assert np.array_equal(gt, u["table"]), "unique tables"
-    assert np.array_equal(grow, u["row"]), "unique rows"
+    assert np.array_equal(dbg["row"].cpu().numpy(), u["row"]), "unique rows"
     assert np.array_equal(dbg["count"].cpu().numpy().astype(np.int64), u["count"]), "counts"
 
-    # sampled rows: the oracle's backward restricted to them
+    # every touched row, one column (= table) at a time
     G_h = G.cpu().numpy() if G is not None else None
-    Gs_h = None
-    if Gseq is not None:
-        flat = Gseq.cpu().numpy()
-        ssl, _ = seq_slices(w.columns, w.B)
-        Gs_h = [None if sp is None else flat[sp[0]:sp[0] + int(np.prod(sp[1]))].reshape(sp[1]) for sp in ssl]
-    Wr, Ar = W0.copy(), A0.copy()
-    ref = oracle.backward_rows(w.columns, w.B, w.offsets, w.values, G_h, Gs_h, targets, Wr, Ar, w.lr, w.eps)
-    assert np.array_equal(ref["count"], u["count"][pick])
-    g_gpu = dbg["grad"][torch.from_numpy(pick).cuda()].cpu().numpy()
+    flat = Gseq.cpu().numpy() if Gseq is not None else None
     excluded, total = 0, 0
-    for k, (t, r) in enumerate(targets):
-        d = dims[t]
-        e, n = check_row_update((t, r), ref["grad"][k, :d], ref["absgrad"][k, :d], ref["count"][k],
-                                g_gpu[k, :d], W0[k, :d], A0[k, :d], m.tables[t][r].cpu().numpy(),
-                                m.accs[t][r].cpu().numpy(), Wr[k, :d], Ar[k, :d], w.lr, w.eps)
+    for c, col in enumerate(w.columns):
+        sel = np.flatnonzero(u["table"] == col.table)
+        if not sel.size:
+            continue
+        rows = u["row"][sel]
+        idx = torch.from_numpy(rows).cuda()
+        W0 = synth.make_table(w.tables[col.table], "cuda")[idx].cpu().numpy()
+        A0 = np.zeros_like(W0)
+        Wg = m.tables[col.table][idx].cpu().numpy()
+        Ag = m.accs[col.table][idx].cpu().numpy()
+        g = dbg["grad"][torch.from_numpy(sel).cuda(), :col.dim].cpu().numpy()
+        spec = dataclasses.replace(col, table=0)
+        if col.pooling == "padded":
+            start, shape = ssl[c]
+            Gc, Gs = None, [flat[start:start + int(np.prod(shape))].reshape(shape)]
+        else:
+            off, d = psl[c]
+            Gc, Gs = np.ascontiguousarray(G_h[:, off:off + d]), None
+        Wr, Ar = W0.copy(), A0.copy()
+        ref = oracle.backward_rows([spec], w.B, [w.offsets[c]], [w.values[c]], Gc, Gs,
+                                   (np.zeros(rows.size, np.int32), rows), Wr, Ar, w.lr, w.eps)
+        assert np.array_equal(ref["count"], u["count"][sel]), "counts of column %d" % c
+        e, n, _, _ = check_rows(ref["grad"], ref["absgrad"], ref["count"], g, W0, A0, Wg, Ag, Wr, Ar, w.lr, w.eps,
+                             what="column %d" % c)
         excluded += e
         total += n
-    assert excluded <= max(16, 1e-5 * total), (excluded, total)
+        del W0, Wg, Ag
+    dims = {col.table: col.dim for col in w.columns}
+    tabs, n_per = np.unique(u["table"], return_counts=True)
+    assert total == int(sum(dims[int(t)] * int(k) for t, k in zip(tabs, n_per))), "every touched element checked"
+    assert excluded <= excluded_cap(total), (excluded, total)
+    print("excluded %d of %d updated elements" % (excluded, total))
     del m, plan, out, seq, G, Gseq, dbg
     _free()
 
@@ -125,30 +130,32 @@ def test_sequence_workload_mean_full_size():
 
 def test_sequence_workload_padded_full_size():
     """20 columns, batch 1024, unpooled [1024, 1000, 128] per column."""
-    _full_training_step(synth.sequences(mode="padded"), n_bags=300)
+    _full_training_step(synth.sequences(mode="padded"))
 
 
 def test_dynamic_stream_full_size():
     """100 columns over one 2^27-slot table, batch 16384, 50 steps of
     lookup-or-insert -> forward -> backward/Adagrad -> expiry: rows bit-exact
-    every step, hash maps bit-exact every tenth step, pooled outputs and the
-    admitted rows' weights within tolerance."""
+    every step, hash maps bit-exact every tenth step, every step's pooled
+    output within 1e-5 rel / 1e-6 abs of the oracle's forward over the rows
+    the library read, and every touched row's gradient, weights and
+    accumulator within 1e-5 rel / 1e-6 abs of the free-running oracle
+    (exclusions: elements the fp32 sum leaves ill-conditioned, counted); the
+    row pool at the end too."""
     w = synth.dynamic()
     ex = w.extra
     run = DynamicRun(C=len(w.columns), B=w.B, steps=ex["steps"], num_slots=ex["num_slots"], cap=ex["row_capacity"],
                      dim=w.columns[0].dim, thr=ex["threshold"], ttl=ex["ttl"], seed=w.seed, alpha=ex["alpha"],
                      key_bits=ex["key_bits"], lr=w.lr, max_probes=ex["max_probes"])
     for t in range(run.steps):
-        check = t % 10 == 9
-        r = run.step(t, check=True, check_out=check)
+        r = run.step(t)
         assert r["status"][0] in (0, 5) and r["status"][1] == 0, r["status"]
         g, o = r["rows"]
         assert np.array_equal(g, o), "rows step %d" % t
-        if check:
-            assert_close(*r["out"], what="pooled step %d" % t)
+        assert_close_skip(*r["out"], what="pooled step %d" % t)
+        if t % 10 == 9:
             compare_hash_maps(run.ht.export(), run.oh.export(), "step %d" % t)
-    adm = run.oh.export()
-    rows = adm["row"][adm["row"] >= 0]
-    assert_close(run.ht.weight.cpu().numpy()[rows], run.oh.W[rows], "row pool weights", rtol=1e-4, atol=1e-5)
+    run.pool.check_pool(run.ht.weight, run.ht.acc)
+    print("excluded %d of %d updated elements" % (run.excluded, run.checked))
     del run
     _free()

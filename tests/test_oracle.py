@@ -366,8 +366,10 @@ def test_hash_hand_traced_scenario():
     A, B_, C, D, E, F_, G_, H = 100, 50, 7, 8, 30, 20, 9, 10
     rows, st = h.lookup_or_insert([0] * 6, [A, A, B_, B_, B_, C], 0)
     assert st == 0 and rows.tolist() == [-1, -1, 0, 0, 0, -1]
+    assert h.last_admitted().tolist() == [0]
     rows, st = h.lookup_or_insert([0] * 3, [A, C, D], 1)
     assert rows.tolist() == [1, -1, -1]
+    assert h.last_admitted().tolist() == [1]
     ex = h.export()
     assert dict(zip(ex["key"].tolist(), ex["count"].tolist())) == {A: 3, B_: 3, C: 2, D: 1}
     assert h.evict(3, 2) == 1            # only B (idle 3 > 2) at now = 3
@@ -375,14 +377,18 @@ def test_hash_hand_traced_scenario():
     assert h.size() == 0 and h.free_count() == 2
     rows, st = h.lookup_or_insert([0] * 6, [E, E, E, F_, F_, F_], 5)
     assert st == 0 and rows.tolist() == [1, 1, 1, 0, 0, 0]   # F < E: F takes row 0
+    assert h.last_admitted().tolist() == [0, 1]               # admission order: F, then E
     rows, st = h.lookup_or_insert([0] * 6, [G_, G_, G_, H, H, H], 6)
     assert st == oracle.ERR_FULL and rows.tolist() == [2, 2, 2, -1, -1, -1]
+    assert h.last_admitted().tolist() == [2]
     # H stays counting and is admitted as soon as a row is free again
     rows, st = h.lookup_or_insert([0], [H], 7)
     assert st == oracle.ERR_FULL and rows.tolist() == [-1]
+    assert h.last_admitted().tolist() == []
     assert h.evict(8, 2) == 2
     rows, st = h.lookup_or_insert([0], [H], 8)
     assert st == 0 and rows.tolist() == [0]
+    assert h.last_admitted().tolist() == [0]
 
 
 def test_hash_init_values_are_exact_and_in_range():

@@ -1,17 +1,18 @@
 """GPU parity of the pipelined dynamic-table step (the lookup of step t+1 and
 the expiry of step t on a low-priority stream beside step t's backward)
 against the oracle run step by step in order: every step's rows bit-exact,
-pooled outputs within tolerance, the final map identical."""
+pooled outputs within 1e-5 rel / 1e-6 abs, the final map identical and the
+row pool's weights and accumulators within 1e-5 rel / 1e-6 abs (exclusions:
+elements the fp32 sum left ill-conditioned at some step, counted)."""
 import numpy as np
 import pytest
 
-import oracle
 import sparse_lookup_gb300 as sl
 from sparse_lookup_gb300 import build as slbuild
 from sparse_lookup_gb300 import synth
 from sparse_lookup_gb300.pipeline import DynamicPipeline
 
-from helpers import assert_close, compare_hash_maps
+from helpers import OraclePool, assert_close_skip, compare_hash_maps
 
 pytestmark = pytest.mark.gpu
 
@@ -60,24 +61,14 @@ def test_pipelined_steps_match_the_oracle_in_order(ttl, thr):
     torch.cuda.synchronize()
     assert ht.device_status() in (0, 5) and plan.device_status() == 0
 
-    oh = oracle.Hash(cap, dim, thr, seed, 0.01)
+    pool = OraclePool(cap, dim, thr, seed, cols, B, lr, 1e-10)
     for t in range(steps):
         d = data[t]
-        rows_o, _ = oh.lookup_or_insert(d["tids"], d["keys"], t)
-        assert np.array_equal(rows[t].cpu().numpy(), rows_o), "rows step %d" % t
-        vals, pos = [], 0
-        for o in d["offs"]:
-            n = int(o[-1])
-            vals.append(rows_o[pos:pos + n])
-            pos += n
-        ref = oracle.forward(cols, B, d["offs"], vals, [oh.W])[0]
-        assert_close(outs[t].cpu().numpy(), ref, what="pooled step %d" % t)
-        oracle.backward_adagrad(cols, B, d["offs"], vals, Gs[t].cpu().numpy(), None, [oh.W], [oh.acc], lr, 1e-10)
-        oh.evict(t, ttl)
-    compare_hash_maps(ht.export(), oh.export(), "final map")
-    adm = oh.export()
-    live = adm["row"][adm["row"] >= 0]
-    assert_close(ht.weight.cpu().numpy()[live], oh.W[live], "row pool weights", rtol=1e-4, atol=1e-5)
+        o = pool.step(d["tids"], d["keys"], t, d["offs"], Gs[t].cpu().numpy(), ttl)
+        assert np.array_equal(rows[t].cpu().numpy(), o["rows"]), "rows step %d" % t
+        assert_close_skip(outs[t].cpu().numpy(), o["out"], o["out_skip"], what="pooled step %d" % t)
+    compare_hash_maps(ht.export(), pool.oh.export(), "final map")
+    pool.check_pool(ht.weight, ht.acc)
 
 
 def test_forward_before_prefetch_is_rejected():
