@@ -325,6 +325,28 @@ emb_status hash_evict_expired(emb_hash h, uint32_t now, uint32_t ttl, void* stre
 emb_status hash_export(emb_hash h, int32_t* tids, int64_t* keys, int64_t* rows, int32_t* counts,
                        uint32_t* last_seen, int64_t cap, int64_t* n_out, void* stream);
 
+/* hash_import -- restores the table from a snapshot that hash_export wrote
+ * (checkpoint and resume: the pages' table is restored from snapshots of the
+ * parameter servers [Monolith §2.3]).  The table is cleared first (every slot
+ * empty, every row free); it then holds exactly the n entries given, with the
+ * same meaning as hash_export's outputs: tids, keys, rows (the admitted
+ * entry's row, -1 while counting), counts (occurrences counted while
+ * counting; NULL = 0), last_seen.  Rows keep their numbers, so the row pool
+ * restored through hash_rows (the caller copies the weights and accumulators
+ * back) matches the entries; the pool itself is not touched.  Later lookups,
+ * admissions and expiries then behave as they would have on the table the
+ * snapshot was taken from.  Checked on the device: key range, distinct
+ * (tid, key) pairs, admitted rows below row_capacity and distinct, counts
+ * >= 0, last_seen != 2^32 - 1; a bad entry is left out and latches
+ * EMB_ERR_INVALID_ARG (the table then holds the other entries, and rows a
+ * rejected entry claimed may stay marked used: import a good snapshot
+ * again); max_probes slots probed without a place latches
+ * EMB_ERR_PROBE_LIMIT.  Expiries sweep every slot until the latest imported
+ * last_seen is more than ttl behind.  All arrays device [n];
+ * n <= num_slots.  Synchronizes `stream`. */
+emb_status hash_import(emb_hash h, const int32_t* tids, const int64_t* keys, const int64_t* rows,
+                       const int32_t* counts, const uint32_t* last_seen, int64_t n, void* stream);
+
 /* Synchronizes `stream`, returns and clears the latched device status. */
 emb_status hash_get_device_status(emb_hash h, void* stream);
 
@@ -347,7 +369,7 @@ emb_status hash_destroy(emb_hash h);
  * and acc ([num_rows, dim] fp32, 16-byte aligned) takes one step
  *   acc += g*g;  w -= lr * g / (sqrt(acc) + eps).
  *
- * Scratch: a fixed area of about 6.4 MB compiled into the library as a
+ * Scratch: a fixed area of about 8.6 MB compiled into the library as a
  * file-scope device array; every GPU that loads the library holds it until
  * the process exits.  Limits: n <= 262144 (2^18), dim <= 256, num_rows <
  * 2^31; larger sizes return EMB_ERR_UNSUPPORTED before any work is queued.
@@ -357,14 +379,54 @@ emb_status hash_destroy(emb_hash h);
  * call's contents (each call clears what must start at zero): calls whose
  * work overlaps on the GPU -- on different streams, or from different host
  * threads -- race and corrupt each other's results; serialize them.
+ * Device-side errors (a wait of the sort that ran out: EMB_ERR_TIMEOUT) are
+ * latched into a status word of the area, read and cleared by
+ * emb_noalloc_get_device_status; a call whose sort gave up a wait leaves
+ * weight and acc untouched.
  * Calls no cudaMalloc, cudaFree or allocating library routine. */
 emb_status emb_sparse_adagrad_noalloc(const int64_t* rows, int64_t n, const float* grads, float* weight,
                                       float* acc, int64_t num_rows, int32_t dim, float lr, float eps,
                                       void* stream);
 
+/* emb_noalloc_get_device_status -- companion of emb_sparse_adagrad_noalloc
+ * (no counterpart on the pages either): synchronizes `stream`, returns the
+ * first device-side error latched by emb_sparse_adagrad_noalloc calls on the
+ * current device since the last query (EMB_OK if none) and clears it.
+ * Allocates nothing (the word lives in the same file-scope area). */
+emb_status emb_noalloc_get_device_status(void* stream);
+
 /* ------------------------------------------------------------------------ */
-/* Host-side self tests of arithmetic shared by host and device code         */
+/* Self tests and fault injection (no counterpart on the pages)              */
 /* ------------------------------------------------------------------------ */
+
+/* emb_selftest_sort_timeout -- makes the bounded wait of the radix sort's
+ * decoupled look-back run out on purpose, without faulting or hanging the
+ * GPU: one pass over two tiles in which only the second tile runs, so its
+ * wait for the first tile's counts can never end; after its bound (about a
+ * second) the tile latches EMB_ERR_TIMEOUT and raises the sort's fail word,
+ * then a run reduction over the incomplete output must see that word and
+ * leave its table untouched.  Allocates and frees its own small buffers and
+ * synchronizes the device.  All pointers are host:
+ *  latched          the status the sort latched (EMB_ERR_TIMEOUT expected)
+ *  fail_word        the sort's fail word afterwards (nonzero expected)
+ *  table_untouched  1 if the reduction left its table as it was
+ *  wait_ms          optional: device time of the waiting pass */
+emb_status emb_selftest_sort_timeout(uint32_t* latched, uint32_t* fail_word, int32_t* table_untouched,
+                                     float* wait_ms);
+
+/* emb_debug_fail_alloc -- host-side fault injection for the create calls:
+ * after `after` more device allocations by emb_plan_create / hash_create /
+ * the self tests succeed, the next one fails as if the device were out of
+ * memory (nothing is asked of the driver), then the hook disarms itself.
+ * after = -1 disarms it.  Every create call must then return EMB_ERR_OOM
+ * with *out NULL and nothing leaked. */
+emb_status emb_debug_fail_alloc(int64_t after);
+
+/* emb_debug_live_allocations -- number and bytes (host, optional) of the
+ * device allocations the library's handles hold right now. */
+emb_status emb_debug_live_allocations(int64_t* count, int64_t* bytes);
+
+/* Host-side self test of arithmetic shared by host and device code: */
 
 /* Row of each value under a HASH_MOD column with `num_rows` rows, computed on
  * the HOST by the same inline code the kernels run (splitmix64 and the

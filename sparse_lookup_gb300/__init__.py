@@ -85,6 +85,7 @@ _SIGS = {
     "hash_rows": (c_int32, [c_void_p, POINTER(c_void_p), POINTER(c_void_p)]),
     "hash_lookup_or_insert": (c_int32, [c_void_p, c_void_p, c_void_p, c_int64, c_uint32, c_void_p, c_void_p]),
     "hash_evict_expired": (c_int32, [c_void_p, c_uint32, c_uint32, c_void_p, c_void_p]),
+    "hash_import": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_void_p]),
     "hash_export": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int64,
                               POINTER(c_int64), c_void_p]),
     "hash_get_device_status": (c_int32, [c_void_p, c_void_p]),
@@ -93,6 +94,10 @@ _SIGS = {
                                              c_float, c_float, c_void_p]),
     "emb_calibrate_gather": (c_int32, [c_void_p, c_int64, c_int32, c_void_p, c_int64, c_void_p, c_void_p]),
     "emb_selftest_hash_mod": (c_int32, [c_void_p, c_int64, c_int64, c_void_p]),
+    "emb_noalloc_get_device_status": (c_int32, [c_void_p]),
+    "emb_selftest_sort_timeout": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p]),
+    "emb_debug_fail_alloc": (c_int32, [c_int64]),
+    "emb_debug_live_allocations": (c_int32, [c_void_p, c_void_p]),
     "emb_version": (c_char_p, []),
 }
 
@@ -214,6 +219,11 @@ def hash_export(h, tids, keys, rows, counts, last_seen, cap, stream=None):
     return n.value
 
 
+def hash_import(h, tids, keys, rows, counts, last_seen, n, stream=None):
+    _check(lib().hash_import(h, ptr(tids), ptr(keys), ptr(rows), ptr(counts), ptr(last_seen), n, _stream(stream)),
+           "hash_import")
+
+
 def hash_get_device_status(h, stream=None):
     return int(lib().hash_get_device_status(h, _stream(stream)))
 
@@ -227,6 +237,33 @@ def emb_sparse_adagrad_noalloc(rows, n, grads, weight, acc, num_rows, dim, lr, e
     inside the library; n <= 2^18, dim <= 256)."""
     _check(lib().emb_sparse_adagrad_noalloc(ptr(rows), n, ptr(grads), ptr(weight), ptr(acc), num_rows, dim, lr,
                                             eps, _stream(stream)), "emb_sparse_adagrad_noalloc")
+
+
+def emb_noalloc_get_device_status(stream=None):
+    """Latched device status of emb_sparse_adagrad_noalloc calls (cleared)."""
+    return int(lib().emb_noalloc_get_device_status(_stream(stream)))
+
+
+def emb_selftest_sort_timeout():
+    """Runs the sort's bounded-wait self test; returns dict(status, latched,
+    fail_word, table_untouched, wait_ms)."""
+    latched, fail = ctypes.c_uint32(0), ctypes.c_uint32(0)
+    untouched, ms = ctypes.c_int32(0), ctypes.c_float(0.0)
+    st = lib().emb_selftest_sort_timeout(ctypes.byref(latched), ctypes.byref(fail), ctypes.byref(untouched),
+                                         ctypes.byref(ms))
+    return dict(status=int(st), latched=latched.value, fail_word=fail.value, table_untouched=bool(untouched.value),
+                wait_ms=ms.value)
+
+
+def emb_debug_fail_alloc(after):
+    _check(lib().emb_debug_fail_alloc(after), "emb_debug_fail_alloc")
+
+
+def emb_debug_live_allocations():
+    """(count, bytes) of the device allocations the library's handles hold."""
+    c, b = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(lib().emb_debug_live_allocations(ctypes.byref(c), ctypes.byref(b)), "emb_debug_live_allocations")
+    return c.value, b.value
 
 
 def emb_calibrate_gather(table, num_rows, dim, row_idx, n, sink, stream=None):
@@ -401,6 +438,22 @@ class HashTable:
         s = s[:m].cpu().numpy().view(np.uint32)
         order = np.lexsort((k, t))
         return dict(tid=t[order], key=k[order], row=r[order], count=c[order], last_seen=s[order])
+
+    def import_entries(self, snap, stream=None):
+        """Restore the entries of a snapshot (a dict as export() returns:
+        host arrays tid, key, row, count, last_seen); the row pool is the
+        caller's to restore through .weight / .acc."""
+        import numpy as np
+        import torch
+        n = int(len(snap["key"]))
+        dev = "cuda"
+        t = torch.from_numpy(np.ascontiguousarray(snap["tid"], np.int32)).to(dev)
+        k = torch.from_numpy(np.ascontiguousarray(snap["key"], np.int64)).to(dev)
+        r = torch.from_numpy(np.ascontiguousarray(snap["row"], np.int64)).to(dev)
+        cnt = np.where(np.asarray(snap["row"]) >= 0, 0, np.asarray(snap["count"]))
+        c = torch.from_numpy(np.ascontiguousarray(cnt, np.int32)).to(dev)
+        s = torch.from_numpy(np.ascontiguousarray(snap["last_seen"], np.uint32).view(np.int32)).to(dev)
+        hash_import(self.handle, t, k, r, c, s, n, stream)
 
     def device_status(self, stream=None):
         return hash_get_device_status(self.handle, stream)

@@ -11,8 +11,8 @@
 //                       8-bit digit with bounded decoupled look-back;
 //   3. k_segreduce   -- lane groups of dim/4 lanes each walk an equal
 //                       contiguous range of sorted contributions in order,
-//                       gathering scale * G rows with 16-byte loads (several
-//                       in flight) and summing each run; a run that begins
+//                       gathering scale * G rows (several in flight) and
+//                       summing each run; a run that begins
 //                       and ends in one range is finished at once (fp32
 //                       Adagrad on its row); runs cut by range boundaries are
 //                       combined in shared memory in range order, runs cut by
@@ -151,6 +151,7 @@ struct SegArgs {
   int32_t maxdim4;
   int32_t glog;
   int32_t span;           // sorted entries per CTA (a multiple of the lane groups per CTA)
+  const uint32_t* sort_fail;   // the sort's fail word: nonzero = its output has holes, do nothing
   // debug outputs
   const uint32_t* rank;
   int32_t* dbg_table;
@@ -160,6 +161,11 @@ struct SegArgs {
   int32_t dbg_ld;
 };
 
+
+// Lanes of a lane group; lane `sub` of a group holds float4 slices sub,
+// sub + lanes, sub + 2 * lanes, ... of a row (consecutive lanes, consecutive
+// 16-byte slices: each slice index v is one coalesced access per group).
+__device__ __forceinline__ int seg_lanes(const SegArgs& a) { return 1 << a.glog; }
 
 __device__ __forceinline__ float4 seg_f4zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 
@@ -182,7 +188,7 @@ __device__ void finish_row(const SegArgs& a, uint32_t key, int64_t end, const fl
   float* A = tm.acc + row * tm.dim;
 #pragma unroll
   for (int v = 0; v < V; ++v) {
-    const int f4 = sub + v * 32;
+    const int f4 = sub + v * seg_lanes(a);
     if (f4 < tm.dim4) {
       float4 w = *reinterpret_cast<float4*>(W + f4 * 4);
       float4 ac = *reinterpret_cast<float4*>(A + f4 * 4);
@@ -198,7 +204,7 @@ __device__ void finish_row(const SegArgs& a, uint32_t key, int64_t end, const fl
     const uint32_t u = a.rank[end - 1] - 1;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-      const int f4 = sub + v * 32;
+      const int f4 = sub + v * seg_lanes(a);
       if (f4 < tm.dim4) *reinterpret_cast<float4*>(a.dbg_grad + (int64_t)u * a.dbg_ld + f4 * 4) = g[v];
     }
   }
@@ -255,7 +261,7 @@ struct PendingRow {
 #pragma unroll
     for (int v = 0; v < V; ++v) {
       g[v] = grad[v];
-      const int f4 = sub + v * 32;
+      const int f4 = sub + v * seg_lanes(a);
       if (f4 < dim4) {
         w[v] = *reinterpret_cast<const float4*>(W + f4 * 4);
         acc[v] = *reinterpret_cast<const float4*>(A + f4 * 4);
@@ -268,7 +274,7 @@ struct PendingRow {
     on = false;
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-      const int f4 = sub + v * 32;
+      const int f4 = sub + v * seg_lanes(a);
       if (f4 < dim4) {
         adagrad1_fast(w[v].x, acc[v].x, g[v].x, a.lr, a.eps);
         adagrad1_fast(w[v].y, acc[v].y, g[v].y, a.lr, a.eps);
@@ -282,7 +288,7 @@ struct PendingRow {
       const uint32_t u = a.rank[end - 1] - 1;
 #pragma unroll
       for (int v = 0; v < V; ++v) {
-        const int f4 = sub + v * 32;
+        const int f4 = sub + v * seg_lanes(a);
         if (f4 < dim4) *reinterpret_cast<float4*>(a.dbg_grad + (int64_t)u * a.dbg_ld + f4 * 4) = g[v];
       }
     }
@@ -292,7 +298,6 @@ struct PendingRow {
 // Sorted entries per CTA: about 64 per lane group (measured best on the
 // training and sequence workloads), between 256 and kSegSpanMax.
 constexpr int kSegSpanMax = 1024;
-constexpr int kSegPerThread = kSegSpanMax / kSegThreads;
 constexpr int kSegPerGroup = 64;
 
 inline int seg_span(int glog) {
@@ -300,19 +305,30 @@ inline int seg_span(int glog) {
   const int s = kSegPerGroup * ng;
   return s < 256 ? 256 : (s > kSegSpanMax ? kSegSpanMax : s);
 }
-// Gradient rows in flight per lane group (4 rows of V float4 per lane) and
-// resident CTAs per SM.  Measured on the training and sequence workloads:
-// 4-deep groups in more warps beat 6- or 8-deep groups in fewer (more warps
-// hide the gather latency better), and six 4-warp CTAs over 1024
-// contributions beat three 8-warp CTAs over 2048 (a CTA's warps wait at its
-// barrier for its slowest lane group; smaller CTAs wait less).  Rows wider
-// than 128 floats take fewer CTAs to stay within the registers.
+
+// The plan's span: seg_span, or less for a step with too few contributions
+// to give every SM two CTAs -- down to four entries per lane group and at
+// least kUnit entries (the plan's partial buffers hold n / kUnit CTAs).  A
+// lane group's chain of dependent row loads is then a few runs long.
+inline int seg_span_plan(int glog, int64_t n, int sms) {
+  const int ng = kSegThreads / 32 * (32 >> glog);
+  const int full = seg_span(glog);
+  const int64_t want = (n + 2 * (int64_t)sms - 1) / (2 * (int64_t)sms);
+  int s = full;
+  while (s > want && s / 2 >= kUnit && s / 2 >= ng * 4 && (s / 2) % ng == 0) s /= 2;
+  return s;
+}
+// Resident CTAs per SM (rows wider than 128 floats take fewer to stay within
+// the registers), and gradient rows in flight per lane group.  The rows are
+// staged in shared memory by per-thread asynchronous copies (cp.async, 16 B
+// per lane and row): each lane copies and later reads only its own slice, so
+// a ring of kSegRing rows per group needs no barrier, and the rows in
+// flight cost shared memory instead of registers.
 template <int V>
 struct SegDepth {
-  static constexpr int value = 4;
   static constexpr int ctas = V == 1 ? 6 : 4;
+  static constexpr int ring = 8;   // rows in flight per lane group
 };
-constexpr int kSegMaxGroups = kSegWarps * 32;     // dim 4: 32 one-lane groups per warp
 constexpr uint32_t kOffPad = 0x80000000u;         // offset refers to grad_seq
 constexpr uint32_t kNoKey = 0xFFFFFFFFu;          // above every key and the sentinel
 
@@ -326,28 +342,62 @@ struct __align__(16) SegRec {
   uint32_t d4;
 };
 
-struct SegSmem {
-  SegRec rec[kSegSpanMax];
-  float4 part[2][kSegWarps * 64];       // head / tail partial of each lane group
-  int32_t head_end[kSegMaxGroups];      // end of the run cut at the group's start, -1 if none
-  uint32_t tail_key[kSegMaxGroups];     // key of the run left open at the group's end
-  uint8_t head_thru[kSegMaxGroups];     // that head run covers the whole range and goes on
-  uint8_t tail_valid[kSegMaxGroups];
+// Dynamic shared memory of one CTA, laid out for its span and row width:
+// the decoded records, the head / tail partial of each lane group, the
+// gradient-row ring of every lane, and the per-group run bookkeeping.
+struct SegLayout {
+  int rec, part, ring, head_end, tail_key, head_thru, tail_valid, bytes;
+  __host__ __device__ static SegLayout of(int span, int ng, int d4, int v, int ring_depth) {
+    SegLayout L;
+    int o = 0;
+    L.rec = o;
+    o += span * (int)sizeof(SegRec);
+    L.part = o;
+    o += 2 * ng * d4 * 16;
+    L.ring = o;
+    o += ring_depth * kSegThreads * v * 16;
+    L.head_end = o;
+    o += ng * 4;
+    L.tail_key = o;
+    o += ng * 4;
+    L.head_thru = o;
+    o += ng;
+    L.tail_valid = o;
+    o += ng;
+    L.bytes = (o + 15) & ~15;
+    return L;
+  }
 };
 
-// Runs of sorted contributions are reduced by LANE GROUPS of dim/4 lanes
-// (one float4 column slice per lane): the CTA's span is cut into equal
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// 16 bytes global -> shared, asynchronous; bytes < 16 zero-fills the rest
+// (0: nothing is read and the slot reads as zeros).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Runs of sorted contributions are reduced by LANE GROUPS (V float4 slices
+// of a row per lane, see seg_lanes): the CTA's span is cut into equal
 // contiguous ranges, one per group, and a group walks its range in order,
-// SegDepth<V> gradient rows in flight, adding each row into the open run's sum and
-// closing the run where the key changes.  A run closed inside the range that
-// also began there is finished at once (Adagrad on its row, deferred by one
-// run so the weight/accumulator loads overlap the next gathers); a run cut at
-// the range start leaves a head partial and one open at the range end a tail
-// partial, combined in group order after a barrier (and across CTAs by
-// k_seg_fixup).
+// kSegRing gradient rows in flight, adding each row into the open run's sum
+// and closing the run where the key changes.  A run closed inside the range
+// that also began there is finished at once (Adagrad on its row, deferred by
+// one run so the weight/accumulator loads overlap the next gathers); a run
+// cut at the range start leaves a head partial and one open at the range end
+// a tail partial, combined in group order after a barrier (and across CTAs
+// by k_seg_fixup).
 template <int V>
 __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(const SegArgs a) {
-  __shared__ SegSmem sm;
+  extern __shared__ __align__(16) unsigned char seg_smem[];
+  if (*(volatile const uint32_t*)a.sort_fail) return;   // the same for every thread of the CTA
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int glog = a.glog;
   const int G = 32 >> glog;
@@ -358,6 +408,15 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
   const int64_t B1 = min(B0 + (int64_t)a.span, a.n);
   const int span = (int)(B1 - B0);
   const int D4 = a.maxdim4;
+  constexpr int kSegRing = SegDepth<V>::ring;
+  const SegLayout L = SegLayout::of(a.span, NG, D4, V, kSegRing);
+  SegRec* rec = reinterpret_cast<SegRec*>(seg_smem + L.rec);
+  float4* part = reinterpret_cast<float4*>(seg_smem + L.part);   // [2][NG * D4]
+  float4* ring = reinterpret_cast<float4*>(seg_smem + L.ring);   // [kSegRing][kSegThreads * V]
+  int32_t* head_end = reinterpret_cast<int32_t*>(seg_smem + L.head_end);
+  uint32_t* tail_key = reinterpret_cast<uint32_t*>(seg_smem + L.tail_key);
+  uint8_t* head_thru = seg_smem + L.head_thru;
+  uint8_t* tail_valid = seg_smem + L.tail_valid;
 
   // ---- decode the CTA's entries, coalesced, into shared memory; the
   //      weight and accumulator rows of every run that starts here are
@@ -365,10 +424,7 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
   uint32_t lkey = a.sentinel;
   int ld4 = 0;
   TableCursor ptc;
-#pragma unroll
-  for (int k = 0; k < kSegPerThread; ++k) {
-    if (k * kSegThreads >= span) break;
-    const int e = k * kSegThreads + tid;
+  for (int e = tid; e < a.span; e += kSegThreads) {
     SegRec r;
     r.key = a.sentinel;
     r.off = 0u;
@@ -376,6 +432,7 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
     r.d4 = 0u;
     if (e < span) {
       const uint32_t key = __ldg(a.keys + B0 + e);
+      uint32_t val = __ldg(a.vals + B0 + e);   // loaded beside the key
       r.key = key;
       if (key != a.sentinel && (B0 + e == 0 || __ldg(a.keys + B0 + e - 1) != key)) {
         ptc.seek(a, key);
@@ -384,7 +441,6 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
         prefetch_l2(ptc.acc + row * ptc.dim, (uint32_t)ptc.dim * 4u);
       }
       if (key != a.sentinel) {
-        uint32_t val = __ldg(a.vals + B0 + e);
         float wr = 1.0f;   // value weight of a SUM contribution
         if (a.rec_src) {
           const uint2 rs = __ldg(a.rec_src + val);
@@ -409,12 +465,12 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
         }
       }
     }
-    sm.rec[e] = r;
+    rec[e] = r;
   }
   for (int g = tid; g < NG; g += kSegThreads) {
-    sm.head_end[g] = -1;
-    sm.head_thru[g] = 0;
-    sm.tail_valid[g] = 0;
+    head_end[g] = -1;
+    head_thru[g] = 0;
+    tail_valid[g] = 0;
   }
   __syncthreads();
 
@@ -424,76 +480,88 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
   uint32_t ckey = kNoKey;   // key of the open run
   bool chead = false;       // the open run began before this range
   if (r0 < r1) {
-    ckey = sm.rec[r0].key;
-    const uint32_t prev = r0 > 0 ? sm.rec[r0 - 1].key : (B0 > 0 ? __ldg(a.keys + B0 - 1) : kNoKey);
+    ckey = rec[r0].key;
+    const uint32_t prev = r0 > 0 ? rec[r0 - 1].key : (B0 > 0 ? __ldg(a.keys + B0 - 1) : kNoKey);
     chead = prev == ckey && ckey != a.sentinel;
   }
+  // this lane's ring slots: slot j holds V float4 at ring[(j * kSegThreads + tid) * V + v]
+  const uint32_t ring0 = smem_u32(ring + (size_t)tid * V);
+  constexpr uint32_t kSlotBytes = (uint32_t)kSegThreads * V * 16u;
+  auto issue = [&](int e, int slot) {
+    if (e < r1) {
+      const SegRec r = rec[e];
+      const float* src = (r.off & kOffPad) ? a.grad_seq + (int64_t)(r.off & ~kOffPad) * 4
+                                           : a.grad_out + (int64_t)r.off * 4;
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int f4 = sub + v * seg_lanes(a);
+        const bool in = f4 < (int)r.d4;
+        // a lane past the row reads nothing (zero fill) from a valid address
+        cp_async16(ring0 + (uint32_t)slot * kSlotBytes + v * 16u, in ? (const void*)(src + f4 * 4) : (const void*)a.keys,
+                   in ? 16u : 0u);
+      }
+    }
+    cp_async_commit();   // one group per entry, empty past the range
+  };
+#pragma unroll
+  for (int k = 0; k < kSegRing; ++k) issue(r0 + k, k);
+
   float4 acc[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) acc[v] = seg_f4zero();
   TableCursor tc;
   PendingRow<V> pend;
-  constexpr int kSegU = SegDepth<V>::value;
-  for (int i0 = r0; i0 < r1; i0 += kSegU) {
-    uint32_t key[kSegU];
-    float sc[kSegU];
-    float4 x[kSegU][V];
+  int slot = 0;
+  for (int e = r0; e < r1; ++e) {
+    cp_async_wait<kSegRing - 1>();   // entry e's row has landed
+    const uint32_t key = rec[e].key;
+    const float sc = rec[e].scale;
+    float4 x[V];
 #pragma unroll
-    for (int u = 0; u < kSegU; ++u) {
-      const int e = i0 + u;
-      const SegRec r = e < r1 ? sm.rec[e] : SegRec{kNoKey, 0u, 0.0f, 0u};
-      key[u] = r.key;
-      sc[u] = r.scale;
-      const float* src = (r.off & kOffPad) ? a.grad_seq + (int64_t)(r.off & ~kOffPad) * 4
-                                           : a.grad_out + (int64_t)r.off * 4;
+    for (int v = 0; v < V; ++v) x[v] = ring[((size_t)slot * kSegThreads + tid) * V + v];
+    if (key != ckey) {   // the open run ends before this entry
+      if (ckey != a.sentinel) {
+        if (chead) {
 #pragma unroll
-      for (int v = 0; v < V; ++v) {
-        const int f4 = sub + v * 32;
-        x[u][v] = f4 < (int)r.d4 ? __ldg(reinterpret_cast<const float4*>(src + f4 * 4)) : seg_f4zero();
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kSegU; ++u) {
-      if (i0 + u < r1 && key[u] != ckey) {   // the open run ends before this entry
-        if (ckey != a.sentinel) {
-          if (chead) {
-#pragma unroll
-            for (int v = 0; v < V; ++v) {
-              const int f4 = sub + v * 32;
-              if (f4 < D4) sm.part[0][grp * D4 + f4] = acc[v];
-            }
-            if (sub == 0) sm.head_end[grp] = i0 + u;
-          } else {
-            pend.retire(a, sub);
-            tc.seek(a, ckey);
-            pend.issue(a, tc, ckey, B0 + i0 + u, acc, sub);
+          for (int v = 0; v < V; ++v) {
+            const int f4 = sub + v * seg_lanes(a);
+            if (f4 < D4) part[grp * D4 + f4] = acc[v];
           }
+          if (sub == 0) head_end[grp] = e;
+        } else {
+          pend.retire(a, sub);
+          tc.seek(a, ckey);
+          pend.issue(a, tc, ckey, B0 + e, acc, sub);
         }
-        ckey = key[u];
-        chead = false;
-#pragma unroll
-        for (int v = 0; v < V; ++v) acc[v] = seg_f4zero();
       }
+      ckey = key;
+      chead = false;
 #pragma unroll
-      for (int v = 0; v < V; ++v) {
-        acc[v].x = fmaf(x[u][v].x, sc[u], acc[v].x);
-        acc[v].y = fmaf(x[u][v].y, sc[u], acc[v].y);
-        acc[v].z = fmaf(x[u][v].z, sc[u], acc[v].z);
-        acc[v].w = fmaf(x[u][v].w, sc[u], acc[v].w);
-      }
+      for (int v = 0; v < V; ++v) acc[v] = seg_f4zero();
     }
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      acc[v].x = fmaf(x[v].x, sc, acc[v].x);
+      acc[v].y = fmaf(x[v].y, sc, acc[v].y);
+      acc[v].z = fmaf(x[v].z, sc, acc[v].z);
+      acc[v].w = fmaf(x[v].w, sc, acc[v].w);
+    }
+    // the slot just read takes the row kSegRing entries ahead
+    issue(e + kSegRing, slot);
+    slot = slot + 1 == kSegRing ? 0 : slot + 1;
   }
+  cp_async_wait<0>();
   // the run open at the range end: finished here, or left as a partial
   if (r0 < r1 && ckey != a.sentinel) {
-    const uint32_t key_after = r1 < span ? sm.rec[r1].key : (B1 < a.n ? __ldg(a.keys + B1) : kNoKey);
+    const uint32_t key_after = r1 < span ? rec[r1].key : (B1 < a.n ? __ldg(a.keys + B1) : kNoKey);
     if (key_after != ckey) {
       if (chead) {
 #pragma unroll
         for (int v = 0; v < V; ++v) {
-          const int f4 = sub + v * 32;
-          if (f4 < D4) sm.part[0][grp * D4 + f4] = acc[v];
+          const int f4 = sub + v * seg_lanes(a);
+          if (f4 < D4) part[grp * D4 + f4] = acc[v];
         }
-        if (sub == 0) sm.head_end[grp] = r1;
+        if (sub == 0) head_end[grp] = r1;
       } else {
         pend.retire(a, sub);
         tc.seek(a, ckey);
@@ -503,16 +571,16 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
       const int side = chead ? 0 : 1;
 #pragma unroll
       for (int v = 0; v < V; ++v) {
-        const int f4 = sub + v * 32;
-        if (f4 < D4) sm.part[side][grp * D4 + f4] = acc[v];
+        const int f4 = sub + v * seg_lanes(a);
+        if (f4 < D4) part[side * NG * D4 + grp * D4 + f4] = acc[v];
       }
       if (sub == 0) {
         if (chead) {
-          sm.head_end[grp] = r1;
-          sm.head_thru[grp] = 1;
+          head_end[grp] = r1;
+          head_thru[grp] = 1;
         } else {
-          sm.tail_valid[grp] = 1;
-          sm.tail_key[grp] = ckey;
+          tail_valid[grp] = 1;
+          tail_key[grp] = ckey;
         }
       }
     }
@@ -524,35 +592,35 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
   //      head partials of the following groups in order ----
   int32_t* P = a.part_pos + (int64_t)blockIdx.x * 2;
   float4* GP = a.partial + (int64_t)blockIdx.x * 2 * D4;
-  if (sm.tail_valid[grp]) {
+  if (tail_valid[grp]) {
     float4 s[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-      const int f4 = sub + v * 32;
-      s[v] = f4 < D4 ? sm.part[1][grp * D4 + f4] : seg_f4zero();
+      const int f4 = sub + v * seg_lanes(a);
+      s[v] = f4 < D4 ? part[NG * D4 + grp * D4 + f4] : seg_f4zero();
     }
     int g2 = grp + 1;
     bool thru = true;
     int end = span;
     while (g2 < NG && thru) {
-      if (sm.head_end[g2] < 0) break;
+      if (head_end[g2] < 0) break;
 #pragma unroll
       for (int v = 0; v < V; ++v) {
-        const int f4 = sub + v * 32;
-        if (f4 < D4) seg_f4add(s[v], sm.part[0][g2 * D4 + f4]);
+        const int f4 = sub + v * seg_lanes(a);
+        if (f4 < D4) seg_f4add(s[v], part[g2 * D4 + f4]);
       }
-      thru = sm.head_thru[g2] != 0;
-      end = sm.head_end[g2];
+      thru = head_thru[g2] != 0;
+      end = head_end[g2];
       ++g2;
     }
     if (g2 == NG && thru) {
 #pragma unroll
       for (int v = 0; v < V; ++v) {
-        const int f4 = sub + v * 32;
+        const int f4 = sub + v * seg_lanes(a);
         if (f4 < D4) GP[D4 + f4] = s[v];
       }
     } else {
-      finish_row<V>(a, sm.tail_key[grp], B0 + end, s, sub);
+      finish_row<V>(a, tail_key[grp], B0 + end, s, sub);
     }
   }
   // ---- the run cut at the CTA start: group 0 sums the head partials ----
@@ -562,28 +630,28 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
     float4 s[V];
 #pragma unroll
     for (int v = 0; v < V; ++v) s[v] = seg_f4zero();
-    if (sm.head_end[0] >= 0) {
+    if (head_end[0] >= 0) {
       int g2 = 0;
       thru = true;
       while (g2 < NG && thru) {
-        if (sm.head_end[g2] < 0) {
+        if (head_end[g2] < 0) {
           thru = false;
           break;
         }
 #pragma unroll
         for (int v = 0; v < V; ++v) {
-          const int f4 = sub + v * 32;
-          if (f4 < D4) seg_f4add(s[v], sm.part[0][g2 * D4 + f4]);
+          const int f4 = sub + v * seg_lanes(a);
+          if (f4 < D4) seg_f4add(s[v], part[g2 * D4 + f4]);
         }
-        thru = sm.head_thru[g2] != 0;
-        end = sm.head_end[g2];
+        thru = head_thru[g2] != 0;
+        end = head_end[g2];
         ++g2;
       }
       if (g2 < NG) thru = false;
     }
 #pragma unroll
     for (int v = 0; v < V; ++v) {
-      const int f4 = sub + v * 32;
+      const int f4 = sub + v * seg_lanes(a);
       if (f4 < D4) GP[f4] = s[v];
     }
     if (sub == 0) {
@@ -595,9 +663,10 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
 
 // Runs cut by CTA boundaries: one lane group per boundary b (between CTA b-1
 // and CTA b) that is the first boundary inside its run.
-constexpr int kFixLook = 8;
 template <int V>
 __global__ void __launch_bounds__(kSegThreads) k_seg_fixup(const SegArgs a, int n_blocks, int64_t span) {
+  constexpr int kFixLook = 8;   // CTA partials loaded per round trip
+  if (*(volatile const uint32_t*)a.sort_fail) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int glog = a.glog;
   const int G = 32 >> glog;
@@ -614,7 +683,7 @@ __global__ void __launch_bounds__(kSegThreads) k_seg_fixup(const SegArgs a, int 
   const float4* T = a.partial + (b - 1) * 2 * D4 + D4;
 #pragma unroll
   for (int v = 0; v < V; ++v) {
-    const int f4 = sub + v * 32;
+    const int f4 = sub + v * seg_lanes(a);
     s[v] = f4 < D4 ? T[f4] : seg_f4zero();
   }
   // CTAs c, c+1, ... contribute their head partials while the one before
@@ -634,7 +703,7 @@ __global__ void __launch_bounds__(kSegThreads) k_seg_fixup(const SegArgs a, int 
       hp[j] = in ? a.part_pos[cj * 2] : 0;
 #pragma unroll
       for (int v = 0; v < V; ++v) {
-        const int f4 = sub + v * 32;
+        const int f4 = sub + v * seg_lanes(a);
         h[j][v] = (in && f4 < D4) ? a.partial[cj * 2 * D4 + f4] : seg_f4zero();
       }
     }
@@ -643,7 +712,7 @@ __global__ void __launch_bounds__(kSegThreads) k_seg_fixup(const SegArgs a, int 
       if (go) {
 #pragma unroll
         for (int v = 0; v < V; ++v)
-          if (sub + v * 32 < D4) seg_f4add(s[v], h[j][v]);
+          if (sub + v * seg_lanes(a) < D4) seg_f4add(s[v], h[j][v]);
         end = (c + j) * span + hp[j];
         go = thru[j] && c + j + 1 < n_blocks;
       }
@@ -651,6 +720,44 @@ __global__ void __launch_bounds__(kSegThreads) k_seg_fixup(const SegArgs a, int 
     c += kFixLook;
   }
   finish_row<V>(a, key, end, s, sub);
+}
+
+// Shared memory bytes of a k_segreduce launch, and the launch itself (the
+// attribute for more than 48 KB is set on first use).
+// Float4 slices per lane of the run reduction: one, with lane groups of
+// dim/4 lanes; two for rows wider than 128 floats (groups of 32 lanes).
+// Measured on the training workload (backward + Adagrad per step): four
+// slices per lane (eight 4-lane groups per warp) 6.13 ms and two 5.92 ms
+// against 4.61 ms with one -- with more groups per warp nearly every step
+// of the walk has some group closing a run, so the whole warp pays the
+// retire path each step.
+inline int seg_v(int maxdim4) { return maxdim4 > 32 ? 2 : 1; }
+
+// log2 of the lanes per group for rows of up to maxdim4 float4.
+inline int seg_glog(int maxdim4) {
+  const int v = seg_v(maxdim4);
+  const int need = (maxdim4 + v - 1) / v;
+  int glog = 0;
+  while ((1 << glog) < need) ++glog;
+  return glog;
+}
+
+template <int V>
+inline emb_status launch_segreduce_v(const SegArgs& a, int64_t n_blocks, cudaStream_t stream) {
+  const int NG = kSegWarps * (32 >> a.glog);
+  const unsigned fix_grid = (unsigned)std::max<int64_t>(1, (n_blocks - 1 + NG - 1) / NG);
+  const int smem = SegLayout::of(a.span, NG, a.maxdim4, V, SegDepth<V>::ring).bytes;
+  EMB_CUDA_TRY(cudaFuncSetAttribute(k_segreduce<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+  k_segreduce<V><<<(unsigned)n_blocks, kSegThreads, smem, stream>>>(a);
+  if (n_blocks > 1) k_seg_fixup<V><<<fix_grid, kSegThreads, 0, stream>>>(a, (int)n_blocks, a.span);
+  return EMB_OK;
+}
+
+// The run reduction and the fixup of its cut runs (the shared-memory size
+// attribute is set on every launch: it depends on the span and row width).
+inline emb_status launch_segreduce(const SegArgs& a, int64_t n_blocks, cudaStream_t stream) {
+  return seg_v(a.maxdim4) == 2 ? launch_segreduce_v<2>(a, n_blocks, stream)
+                               : launch_segreduce_v<1>(a, n_blocks, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -691,17 +798,16 @@ emb_status launch_backward(emb_plan_s* p, const float* grad_out, const float* gr
   a.lr = lr;
   a.eps = eps;
   a.maxdim4 = p->max_dim / 4;
-  int g = a.maxdim4 > 32 ? 32 : a.maxdim4, glog = 0;
-  while ((1 << glog) < g) ++glog;
+  const int glog = seg_glog(a.maxdim4);
   a.glog = glog;
-  const int NG = kSegWarps * (32 >> glog);
-  a.span = seg_span(glog);
+  a.span = seg_span_plan(glog, n, p->sm_count);
   const int64_t span = a.span;
   const int64_t n_blocks = (n + span - 1) / span;
   if (n_blocks > w.n_units_max) return EMB_ERR_UNSUPPORTED;
   a.partial = w.partial;
   a.part_pos = w.part_pos;
   a.part_thru = w.part_thru;
+  a.sort_fail = sort_fail_word(w.hist, p->key_bits);
   if (want_dbg) {
     const int nb = (int)((n + kScanBlock - 1) / kScanBlock);
     k_rank_reduce<<<nb, kScanBlock, 0, stream>>>(skeys, n, p->key_total, w.scan_part);
@@ -715,14 +821,8 @@ emb_status launch_backward(emb_plan_s* p, const float* grad_out, const float* gr
     a.dbg_grad = dbg->agg_grad;
     a.dbg_ld = p->max_dim;
   }
-  const unsigned fix_grid = (unsigned)std::max<int64_t>(1, (n_blocks - 1 + NG - 1) / NG);
-  if (a.maxdim4 > 32) {
-    k_segreduce<2><<<(unsigned)n_blocks, kSegThreads, 0, stream>>>(a);
-    if (n_blocks > 1) k_seg_fixup<2><<<fix_grid, kSegThreads, 0, stream>>>(a, (int)n_blocks, span);
-  } else {
-    k_segreduce<1><<<(unsigned)n_blocks, kSegThreads, 0, stream>>>(a);
-    if (n_blocks > 1) k_seg_fixup<1><<<fix_grid, kSegThreads, 0, stream>>>(a, (int)n_blocks, span);
-  }
+  st = launch_segreduce(a, n_blocks, stream);
+  if (st != EMB_OK) return st;
   if (want_dbg && (dbg->uniq_table || dbg->uniq_row || dbg->counts)) {
     const int64_t* nu = dbg->n_unique ? dbg->n_unique : reinterpret_cast<const int64_t*>(w.n_runs);
     k_dbg_runs<<<p->sm_count * 4, 256, 0, stream>>>(skeys, n, p->key_total, w.head_pos, nu, p->table_base_d,
@@ -744,9 +844,9 @@ namespace {
 constexpr int64_t kNoAllocMaxN = int64_t(1) << 18;   // contributions per call
 constexpr int kNoAllocMaxDim = 256;
 constexpr int64_t kNoAllocTiles = (kNoAllocMaxN + kSortTile - 1) / kSortTile;
-constexpr int64_t kNoAllocBlocks = (kNoAllocMaxN + 255) / 256;   // the smallest span seg_span() returns
+constexpr int64_t kNoAllocBlocks = (kNoAllocMaxN + kUnit - 1) / kUnit;   // the smallest span seg_span_plan() returns
 // sort_scratch_words for up to 32-bit keys: four passes of 8-bit digits
-constexpr size_t kNoAllocSortWords = 4 * 256 + 4 + 4 * kNoAllocTiles * 256;
+constexpr size_t kNoAllocSortWords = 4 * 256 + 4 + 1 + 4 * kNoAllocTiles * 256;
 
 struct NoAllocScratch {
   uint32_t keys[2][kNoAllocMaxN];
@@ -758,6 +858,7 @@ struct NoAllocScratch {
   TableMeta table;
   uint32_t table_base[2];
   int4 colg;
+  uint32_t status;   // first device-side error since the last emb_noalloc_get_device_status
 };
 
 }  // namespace
@@ -812,6 +913,8 @@ emb_status noalloc_scratch(NoAllocScratch** out, int* sms) {
     }
     int count = 0;
     EMB_CUDA_TRY(cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev));
+    // the status word starts clear on this device
+    EMB_CUDA_TRY(cudaMemset(&static_cast<NoAllocScratch*>(ptr)->status, 0, sizeof(uint32_t)));
     g_noalloc_sms[dev] = count > 0 ? count : 1;
     g_noalloc_addr[dev] = ptr;
   }
@@ -847,7 +950,7 @@ extern "C" emb_status emb_sparse_adagrad_noalloc(const int64_t* rows, int64_t n,
   uint32_t* const nv[2] = {s->vals[0], s->vals[1]};
   int res = 0;
   // the sort clears its part of the area (histograms, tickets, look-back words) itself
-  st = radix_sort_pairs<uint32_t>(nk, nv, n, nullptr, n, key_bits, s->sortw, sms, nullptr, stream, &res);
+  st = radix_sort_pairs<uint32_t>(nk, nv, n, nullptr, n, key_bits, s->sortw, sms, &s->status, stream, &res);
   if (st != EMB_OK) return st;
   SegArgs a{};
   a.keys = s->keys[res];
@@ -867,23 +970,191 @@ extern "C" emb_status emb_sparse_adagrad_noalloc(const int64_t* rows, int64_t n,
   a.lr = lr;
   a.eps = eps;
   a.maxdim4 = dim / 4;
-  int g = a.maxdim4 > 32 ? 32 : a.maxdim4, glog = 0;
-  while ((1 << glog) < g) ++glog;
+  const int glog = seg_glog(a.maxdim4);
   a.glog = glog;
-  const int NG = kSegWarps * (32 >> glog);
-  a.span = seg_span(glog);
+  a.span = seg_span_plan(glog, n, sms);   // the plan path's span: the same sums in the same order
   const int64_t span = a.span;
   const int64_t n_blocks = (n + span - 1) / span;
   a.partial = s->partial;
   a.part_pos = s->part_pos;
   a.part_thru = s->part_thru;
-  const unsigned fix_grid = (unsigned)std::max<int64_t>(1, (n_blocks - 1 + NG - 1) / NG);
-  if (a.maxdim4 > 32) {
-    k_segreduce<2><<<(unsigned)n_blocks, kSegThreads, 0, stream>>>(a);
-    if (n_blocks > 1) k_seg_fixup<2><<<fix_grid, kSegThreads, 0, stream>>>(a, (int)n_blocks, span);
-  } else {
-    k_segreduce<1><<<(unsigned)n_blocks, kSegThreads, 0, stream>>>(a);
-    if (n_blocks > 1) k_seg_fixup<1><<<fix_grid, kSegThreads, 0, stream>>>(a, (int)n_blocks, span);
-  }
+  a.sort_fail = sort_fail_word(s->sortw, key_bits);
+  st = launch_segreduce(a, n_blocks, stream);
+  if (st != EMB_OK) return st;
   return cuda_status(cudaGetLastError());
+}
+
+extern "C" emb_status emb_noalloc_get_device_status(void* stream_) {
+  using namespace emb;
+  NoAllocScratch* s = nullptr;
+  int sms = 1;
+  emb_status st = noalloc_scratch(&s, &sms);
+  if (st != EMB_OK) return st;
+  cudaStream_t stream = (cudaStream_t)stream_;
+  uint32_t code = 0;
+  EMB_CUDA_TRY(cudaMemcpyAsync(&code, &s->status, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream));
+  EMB_CUDA_TRY(cudaMemsetAsync(&s->status, 0, sizeof(uint32_t), stream));
+  EMB_CUDA_TRY(cudaStreamSynchronize(stream));
+  return (emb_status)code;
+}
+
+// ===========================================================================
+// emb_selftest_sort_timeout: the bounded wait of the sort's look-back, made
+// to run out on purpose (no counterpart on the pages; see include/emb.h).
+// ===========================================================================
+namespace emb {
+namespace {
+
+__global__ void k_selftest_fill(uint32_t* keys, uint32_t* vals, uint32_t* out_keys, uint32_t* out_vals, int64_t n,
+                                uint32_t n_rows, float* grads, int dim) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    keys[i] = (uint32_t)(i % n_rows);   // valid rows of the test table
+    vals[i] = (uint32_t)i;              // gradient row i exists
+    out_keys[i] = n_rows;               // the sentinel: a hole reads as "no row"
+    out_vals[i] = 0u;
+    for (int d = 0; d < dim; ++d) grads[i * dim + d] = 1.0f;
+  }
+}
+
+}  // namespace
+}  // namespace emb
+
+extern "C" emb_status emb_selftest_sort_timeout(uint32_t* latched, uint32_t* fail_word, int32_t* table_untouched,
+                                                float* wait_ms) {
+  using namespace emb;
+  if (!latched || !fail_word || !table_untouched) return EMB_ERR_INVALID_ARG;
+  constexpr uint32_t kRows = 16;
+  constexpr int kDim = 4;
+  const int64_t n = 2 * (int64_t)kSortTile;   // two tiles of one pass
+  const int key_bits = 8;                      // one pass of 8-bit digits
+  uint32_t *keys[2] = {nullptr, nullptr}, *vals[2] = {nullptr, nullptr}, *scratch = nullptr, *status = nullptr;
+  float *grads = nullptr, *W = nullptr, *A = nullptr;
+  float4* partial = nullptr;
+  int32_t* part_pos = nullptr;
+  uint8_t* part_thru = nullptr;
+  TableMeta* tm_d = nullptr;
+  uint32_t* base_d = nullptr;
+  int4* colg_d = nullptr;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  const size_t words = sort_scratch_words<uint32_t>(key_bits, n);
+  const int64_t n_blocks = (n + 255) / 256;
+  cudaError_t e = cudaSuccess;
+  auto alloc = [&](auto** p, size_t bytes) {
+    if (e == cudaSuccess) e = dev_alloc((void**)p, bytes);
+  };
+  for (int i = 0; i < 2; ++i) {
+    alloc(&keys[i], sizeof(uint32_t) * n);
+    alloc(&vals[i], sizeof(uint32_t) * n);
+  }
+  alloc(&scratch, sizeof(uint32_t) * words);
+  alloc(&status, sizeof(uint32_t));
+  alloc(&grads, sizeof(float) * n * kDim);
+  alloc(&W, sizeof(float) * kRows * kDim);
+  alloc(&A, sizeof(float) * kRows * kDim);
+  alloc(&partial, sizeof(float4) * n_blocks * 2);
+  alloc(&part_pos, sizeof(int32_t) * n_blocks * 2);
+  alloc(&part_thru, n_blocks);
+  alloc(&tm_d, sizeof(TableMeta));
+  alloc(&base_d, sizeof(uint32_t) * 2);
+  alloc(&colg_d, sizeof(int4));
+  if (e == cudaSuccess) e = cudaEventCreate(&e0);
+  if (e == cudaSuccess) e = cudaEventCreate(&e1);
+  float w_init[kRows * kDim];
+  for (uint32_t i = 0; i < kRows * kDim; ++i) w_init[i] = 0.5f + (float)i;
+  if (e == cudaSuccess) e = cudaMemcpy(W, w_init, sizeof(w_init), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemset(A, 0, sizeof(float) * kRows * kDim);
+  if (e == cudaSuccess) e = cudaMemset(scratch, 0, sizeof(uint32_t) * words);
+  if (e == cudaSuccess) e = cudaMemset(status, 0, sizeof(uint32_t));
+  if (e == cudaSuccess) {
+    TableMeta tm{};
+    tm.weight = W;
+    tm.acc = A;
+    tm.num_rows = kRows;
+    tm.dim = kDim;
+    tm.dim4 = kDim / 4;
+    const uint32_t base[2] = {0u, kRows};
+    const int4 cg = make_int4(0, 0, kDim / 4, 0);
+    e = cudaMemcpy(tm_d, &tm, sizeof(tm), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(base_d, base, sizeof(base), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(colg_d, &cg, sizeof(cg), cudaMemcpyHostToDevice);
+  }
+  uint32_t* hist = scratch;
+  uint32_t* tickets = hist + 256;
+  uint32_t* fail = sort_fail_word(scratch, key_bits);
+  uint32_t* lookback = fail + 1;
+  const int smem = (int)sizeof(SortSmemT<uint32_t, 8>);
+  if (e == cudaSuccess) {
+    k_selftest_fill<<<64, 256>>>(keys[0], vals[0], keys[1], vals[1], n, kRows, grads, kDim);
+    k_digit_hist_t<uint32_t, 8><<<8, 512>>>(keys[0], n, nullptr, 1, hist);
+    // the first ticket is already taken: the one CTA below draws tile 1,
+    // whose look-back waits on tile 0, which no CTA will ever publish
+    const uint32_t one = 1u;
+    e = cudaMemcpy(tickets, &one, sizeof(one), cudaMemcpyHostToDevice);
+  }
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_onesweep_t<uint32_t, 8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess) {
+    cudaEventRecord(e0);
+    k_onesweep_t<uint32_t, 8, false><<<1, kSortThreads, smem>>>(keys[0], vals[0], keys[1], vals[1], n, nullptr, 0,
+                                                                hist, lookback, tickets, status, fail);
+    cudaEventRecord(e1);
+    // a run reduction over the incomplete output: must see the fail word
+    SegArgs a{};
+    a.keys = keys[1];
+    a.vals = vals[1];
+    a.n = n;
+    a.sentinel = kRows;
+    a.colg = colg_d;
+    a.grad_out = grads;
+    a.ldg = kDim;
+    a.batch = (int32_t)n;
+    a.bdiv = make_div_magic32((uint32_t)n);
+    a.tables = tm_d;
+    a.table_base = base_d;
+    a.n_tables = 1;
+    a.lr = 0.5f;
+    a.eps = 1e-10f;
+    a.maxdim4 = kDim / 4;
+    a.glog = 0;
+    a.span = 256;   // seg_span for one-lane groups
+    a.partial = partial;
+    a.part_pos = part_pos;
+    a.part_thru = part_thru;
+    a.sort_fail = fail;
+    if (launch_segreduce(a, n_blocks, 0) != EMB_OK) e = cudaErrorInvalidValue;
+    if (e == cudaSuccess) e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) {
+    float w_after[kRows * kDim];
+    e = cudaMemcpy(w_after, W, sizeof(w_after), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemcpy(latched, status, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemcpy(fail_word, fail, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+    *table_untouched = 1;
+    for (uint32_t i = 0; i < kRows * kDim; ++i)
+      if (w_after[i] != w_init[i]) *table_untouched = 0;
+    if (wait_ms && e == cudaSuccess) e = cudaEventElapsedTime(wait_ms, e0, e1);
+  }
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  for (int i = 0; i < 2; ++i) {
+    dev_free(keys[i]);
+    dev_free(vals[i]);
+  }
+  dev_free(scratch);
+  dev_free(status);
+  dev_free(grads);
+  dev_free(W);
+  dev_free(A);
+  dev_free(partial);
+  dev_free(part_pos);
+  dev_free(part_thru);
+  dev_free(tm_d);
+  dev_free(base_d);
+  dev_free(colg_d);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_status(e);
+  }
+  return EMB_OK;
 }

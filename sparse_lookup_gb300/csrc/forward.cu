@@ -1070,6 +1070,12 @@ emb_status launch_forward(emb_plan_s* p, int32_t batch, const int64_t* ids, cons
   const int64_t want = total / std::max<int64_t>(1, (a.dynamic ? 32 : 16) * warps);
   int64_t E = a.dynamic ? 128 : 256;
   while (E < want && E < kMaxTileElems) E <<= 1;
+  // A launch so small that its tiles would occupy under an eighth of the
+  // resident warps (a few thousand values) takes smaller value tiles, down
+  // to 32 values: each warp's chain of dependent loads is then one or two
+  // chunks long instead of several.
+  if (!a.dynamic)
+    while (E > 32 && total / E < warps / 8) E >>= 1;
   a.tile_elems = (int32_t)E;
   a.tiles[0] = a.ncols[0] > 0 ? n_ids / E + 1 : 0;
   a.tiles[1] = a.ncols[1] > 0 ? n_fvals / E + 1 : 0;

@@ -83,7 +83,7 @@ struct emb_hash_s {
   uint32_t* free_rows = nullptr;   // [max_keys] the lowest free rows, ascending
   uint64_t* nkeys[2] = {nullptr, nullptr};
   uint32_t* nvals[2] = {nullptr, nullptr};
-  uint32_t* counters = nullptr;    // [0] listed keys, [1] exported entries
+  uint32_t* counters = nullptr;    // [0] listed keys, [1] exported entries, [2] latest imported step
   uint32_t* sort_scratch = nullptr;
   uint32_t* status = nullptr;
   int sm_count = 0;
@@ -124,18 +124,19 @@ __device__ __forceinline__ uint64_t home_slot(uint64_t fkey, uint64_t mask) {
   return splitmix64(fkey ^ 0x5851F42D4C957F2Dull) & mask;
 }
 
-// K-H1
-__global__ void __launch_bounds__(256) k_hash_probe(const HashArgs h, const int32_t* __restrict__ tids,
-                                                    const int64_t* __restrict__ keys, int64_t n, uint32_t step,
-                                                    int64_t* __restrict__ rows_out) {
-  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
-  if (i >= n) return;
+// K-H1, one occurrence: find or insert its key, touch and count; writes its
+// row (or -2 - slot for a key listed for admission, -1 otherwise) and
+// returns true when this occurrence moved the slot's last_seen to `step`
+// (the call's first touch of the entry), with the slot in *slot_out.
+__device__ __forceinline__ bool probe_one(const HashArgs& h, const int32_t* __restrict__ tids,
+                                          const int64_t* __restrict__ keys, int64_t i, uint32_t step,
+                                          int64_t* __restrict__ rows_out, uint32_t* slot_out) {
   const int32_t tid = tids[i];
   const int64_t key = keys[i];
   if (tid < 0 || tid >= (1 << kTidBits) || key < 0 || key >= (int64_t(1) << kKeyBits)) {
     latch(h.status, EMB_ERR_INVALID_ARG);
     rows_out[i] = -1;
-    return;
+    return false;
   }
   const unsigned long long fkey = ((unsigned long long)tid << kKeyBits) | (unsigned long long)key;
   // Probe from the home slot until the key or an EMPTY slot turns up (the
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(256) k_hash_probe(const HashArgs h, const int3
   if (found < 0) {
     latch(h.status, EMB_ERR_PROBE_LIMIT);
     rows_out[i] = -1;
-    return;
+    return false;
   }
   Slot* s = &h.slots[found];
   unsigned long long* sw = reinterpret_cast<unsigned long long*>(&s->state);
@@ -258,21 +259,36 @@ __global__ void __launch_bounds__(256) k_hash_probe(const HashArgs h, const int3
     }
   }
   rows_out[i] = out;
-  // a slot's first touch of the call goes on the call's list (one per
-  // distinct slot, so at most n entries), one atomic per warp
-  if (h.touch) {
-    const unsigned act = __activemask();
-    const unsigned fm = __ballot_sync(act, first);
-    if (fm) {
-      const int lane = threadIdx.x & 31, leader = __ffs(act) - 1;
-      uint32_t base = 0;
-      if (lane == leader) base = atomicAdd(h.touch_n, (uint32_t)__popc(fm));
-      base = __shfl_sync(act, base, leader);
-      if (first) {
-        const uint32_t idx = base + (uint32_t)__popc(fm & ((1u << lane) - 1u));
-        if ((int64_t)idx < h.max_keys) h.touch[idx] = (uint32_t)found;
-      }
-    }
+  *slot_out = (uint32_t)found;
+  return first;
+}
+
+// K-H1.  A slot's first touch of the call goes on the call's list (one entry
+// per distinct slot, so at most n): the CTA counts its first touches in
+// shared memory and takes their places in the list with ONE global atomic
+// (a per-warp atomic on the one list counter queued about 128 K returning
+// atomics on a single address per call).
+__global__ void __launch_bounds__(256) k_hash_probe(const HashArgs h, const int32_t* __restrict__ tids,
+                                                    const int64_t* __restrict__ keys, int64_t n, uint32_t step,
+                                                    int64_t* __restrict__ rows_out) {
+  __shared__ uint32_t s_cnt, s_base;
+  if (threadIdx.x == 0) s_cnt = 0;
+  __syncthreads();
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  uint32_t slot = 0;
+  const bool first = i < n && probe_one(h, tids, keys, i, step, rows_out, &slot);
+  if (!h.touch) return;   // the same for the whole grid
+  const int lane = threadIdx.x & 31;
+  const unsigned fm = __ballot_sync(kFull, first);
+  uint32_t wbase = 0;
+  if (lane == 0 && fm) wbase = atomicAdd(&s_cnt, (uint32_t)__popc(fm));
+  wbase = __shfl_sync(kFull, wbase, 0);
+  __syncthreads();
+  if (threadIdx.x == 0) s_base = s_cnt ? atomicAdd(h.touch_n, s_cnt) : 0u;
+  __syncthreads();
+  if (first) {
+    const uint32_t idx = s_base + wbase + (uint32_t)__popc(fm & ((1u << lane) - 1u));
+    if ((int64_t)idx < h.max_keys) h.touch[idx] = slot;
   }
 }
 
@@ -357,11 +373,16 @@ __device__ __forceinline__ float init_value(uint64_t fkey, uint64_t seed, int d,
 
 // K-H2: the i-th listed key (ascending) takes the i-th free row, listed by
 // k_free_down; k_hash_mark sets the bits of the rows handed out afterwards.
+// Both do nothing when the sort of the listed keys gave up a wait (sort_fail
+// set, EMB_ERR_TIMEOUT latched): its output then has holes, and the listed
+// keys stay counting.
 __global__ void __launch_bounds__(256) k_hash_admit(Slot* slots, const uint64_t* __restrict__ skeys,
                                                     const uint32_t* __restrict__ svals, const uint32_t* n_new,
                                                     int64_t max_keys, const uint32_t* free_scan,
                                                     const uint32_t* __restrict__ free_rows, int64_t nw, float* W,
-                                                    float* A, int dim, uint64_t seed, float scale, uint32_t* status) {
+                                                    float* A, int dim, uint64_t seed, float scale, uint32_t* status,
+                                                    const uint32_t* sort_fail) {
+  if (*(volatile const uint32_t*)sort_fail) return;
   const int lane = threadIdx.x & 31;
   const int64_t warp = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -383,7 +404,9 @@ __global__ void __launch_bounds__(256) k_hash_admit(Slot* slots, const uint64_t*
 }
 
 __global__ void __launch_bounds__(256) k_hash_mark(const Slot* slots, const uint32_t* __restrict__ svals,
-                                                   const uint32_t* n_new, int64_t max_keys, uint32_t* used) {
+                                                   const uint32_t* n_new, int64_t max_keys, uint32_t* used,
+                                                   const uint32_t* sort_fail) {
+  if (*(volatile const uint32_t*)sort_fail) return;
   const int64_t nn = ((int64_t)*n_new < max_keys) ? (int64_t)*n_new : max_keys;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nn; i += (int64_t)gridDim.x * blockDim.x) {
     const int32_t st = slots[svals[i]].state;
@@ -497,6 +520,61 @@ __global__ void k_hash_init(Slot* slots, int64_t ns, uint32_t* used, int64_t nw,
   }
 }
 
+// hash_import: entry i of a snapshot into a cleared table (every slot EMPTY,
+// no tombstone): probe from its home slot to the first EMPTY slot and claim
+// it; meeting its own key on the way means the snapshot lists it twice.  An
+// admitted entry marks its row used; a row marked already is listed twice.
+// Bad entries latch EMB_ERR_INVALID_ARG and are left out.
+__global__ void __launch_bounds__(256) k_hash_import(Slot* slots, uint64_t mask, int32_t max_probes, int64_t cap,
+                                                     uint32_t* used, const int32_t* __restrict__ tids,
+                                                     const int64_t* __restrict__ keys,
+                                                     const int64_t* __restrict__ rows,
+                                                     const int32_t* __restrict__ counts,
+                                                     const uint32_t* __restrict__ last_seen, int64_t n,
+                                                     uint32_t* status, uint32_t* max_seen) {
+  const int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int32_t tid = tids[i];
+  const int64_t key = keys[i];
+  const int64_t row = rows[i];
+  const int32_t cnt = counts ? counts[i] : 0;
+  const uint32_t ls = last_seen[i];
+  if (tid < 0 || tid >= (1 << kTidBits) || key < 0 || key >= (int64_t(1) << kKeyBits) || row >= cap ||
+      (row < 0 && (row != -1 || cnt < 0 || cnt == 0x7FFFFFFF)) || ls == kNeverSeen) {
+    latch(status, EMB_ERR_INVALID_ARG);
+    return;
+  }
+  if (row >= 0) {
+    const uint32_t bit = 1u << (row & 31);
+    if (atomicOr(&used[row >> 5], bit) & bit) {   // a second entry with this row
+      latch(status, EMB_ERR_INVALID_ARG);
+      return;
+    }
+  }
+  const unsigned long long fkey = ((unsigned long long)tid << kKeyBits) | (unsigned long long)key;
+  uint64_t pos = home_slot(fkey, mask);
+  for (int budget = max_probes; budget > 0; --budget, pos = (pos + 1) & mask) {
+    const unsigned long long k = *(volatile unsigned long long*)&slots[pos].key;
+    if (k == fkey) {   // listed twice
+      latch(status, EMB_ERR_INVALID_ARG);
+      return;
+    }
+    if (k != kEmptyKey) continue;
+    const unsigned long long old = atomicCAS(&slots[pos].key, kEmptyKey, fkey);
+    if (old == fkey) {
+      latch(status, EMB_ERR_INVALID_ARG);
+      return;
+    }
+    if (old != kEmptyKey) continue;   // another key took it: go on past it
+    const int32_t state = row >= 0 ? (int32_t)row : -1 - cnt;
+    *reinterpret_cast<unsigned long long*>(&slots[pos].state) =
+        ((unsigned long long)ls << 32) | (unsigned long long)(uint32_t)state;
+    atomicMax(max_seen, ls);
+    return;
+  }
+  latch(status, EMB_ERR_PROBE_LIMIT);
+}
+
 __global__ void k_hash_export(const Slot* slots, int64_t ns, int32_t* tids, int64_t* keys, int64_t* rows,
                               int32_t* counts, uint32_t* last_seen, int64_t cap, uint32_t* ctr) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < ns; i += (int64_t)gridDim.x * blockDim.x) {
@@ -521,22 +599,22 @@ namespace {
 
 void free_hash(emb_hash_s* h) {
   if (!h) return;
-  cudaFree(h->slots);
-  cudaFree(h->W);
-  cudaFree(h->acc);
-  cudaFree(h->used);
-  cudaFree(h->free_scan);
-  cudaFree(h->scan_part);
-  cudaFree(h->free_rows);
-  cudaFree(h->nkeys[0]);
-  cudaFree(h->nkeys[1]);
-  cudaFree(h->nvals[0]);
-  cudaFree(h->nvals[1]);
-  cudaFree(h->counters);
-  cudaFree(h->sort_scratch);
-  cudaFree(h->status);
-  cudaFree(h->touch);
-  cudaFree(h->touch_n);
+  dev_free(h->slots);
+  dev_free(h->W);
+  dev_free(h->acc);
+  dev_free(h->used);
+  dev_free(h->free_scan);
+  dev_free(h->scan_part);
+  dev_free(h->free_rows);
+  dev_free(h->nkeys[0]);
+  dev_free(h->nkeys[1]);
+  dev_free(h->nvals[0]);
+  dev_free(h->nvals[1]);
+  dev_free(h->counters);
+  dev_free(h->sort_scratch);
+  dev_free(h->status);
+  dev_free(h->touch);
+  dev_free(h->touch_n);
   delete h;
 }
 
@@ -570,7 +648,7 @@ extern "C" emb_status hash_create(int64_t num_slots, int64_t row_capacity, int32
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, dev);
   auto alloc = [&](auto** p, size_t bytes) {
-    if (e == cudaSuccess) e = cudaMalloc((void**)p, bytes > 0 ? bytes : 1);
+    if (e == cudaSuccess) e = dev_alloc((void**)p, bytes > 0 ? bytes : 1);
   };
   alloc(&h->slots, sizeof(Slot) * (size_t)num_slots);
   alloc(&h->W, sizeof(float) * (size_t)row_capacity * dim);
@@ -665,8 +743,10 @@ extern "C" emb_status hash_lookup_or_insert(emb_hash h, const int32_t* table_ids
                                            h->max_keys, h->free_rows);
   k_hash_admit<<<h->sm_count * 4, 256, 0, stream>>>(h->slots, h->nkeys[res], h->nvals[res], h->counters,
                                                      h->max_keys, h->free_scan, h->free_rows, h->n_words, h->W,
-                                                     h->acc, h->dim, h->seed, h->init_scale, h->status);
-  k_hash_mark<<<h->sm_count * 2, 256, 0, stream>>>(h->slots, h->nvals[res], h->counters, h->max_keys, h->used);
+                                                     h->acc, h->dim, h->seed, h->init_scale, h->status,
+                                                     sort_fail_word(h->sort_scratch, kHashKeyBits));
+  k_hash_mark<<<h->sm_count * 2, 256, 0, stream>>>(h->slots, h->nvals[res], h->counters, h->max_keys, h->used,
+                                                   sort_fail_word(h->sort_scratch, kHashKeyBits));
   k_hash_fix<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(h->slots, n, rows_out);
   return cuda_status(cudaGetLastError());
 }
@@ -715,6 +795,32 @@ extern "C" emb_status hash_export(emb_hash h, int32_t* tids, int64_t* keys, int6
   EMB_CUDA_TRY(cudaMemcpyAsync(&cnt, h->counters + 1, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream));
   EMB_CUDA_TRY(cudaStreamSynchronize(stream));
   *n_out = cnt;
+  return EMB_OK;
+}
+
+extern "C" emb_status hash_import(emb_hash h, const int32_t* tids, const int64_t* keys, const int64_t* rows,
+                                  const int32_t* counts, const uint32_t* last_seen, int64_t n, void* stream_) {
+  if (!h || n < 0) return EMB_ERR_INVALID_ARG;
+  if (n > h->num_slots) return EMB_ERR_UNSUPPORTED;
+  if (n > 0 && (!tids || !keys || !rows || !last_seen)) return EMB_ERR_INVALID_ARG;
+  cudaStream_t stream = (cudaStream_t)stream_;
+  // clear: every slot EMPTY, every row of the pool free
+  k_hash_init<<<h->sm_count * 8, 256, 0, stream>>>(h->slots, h->num_slots, h->used, h->n_words, h->cap);
+  EMB_CUDA_TRY(cudaMemsetAsync(h->counters + 2, 0, sizeof(uint32_t), stream));
+  if (n > 0)
+    k_hash_import<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(
+        h->slots, (uint64_t)h->num_slots - 1, h->max_probes, h->cap, h->used, tids, keys, rows, counts, last_seen, n,
+        h->status, h->counters + 2);
+  EMB_CUDA_TRY(cudaGetLastError());
+  uint32_t latest = 0;
+  EMB_CUDA_TRY(cudaMemcpyAsync(&latest, h->counters + 2, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream));
+  EMB_CUDA_TRY(cudaStreamSynchronize(stream));
+  // no touch list holds the imported entries: expiries sweep every slot
+  // until the latest imported step is more than ttl behind
+  for (int l = 0; l < kTouchLists; ++l) h->list_live[l] = false;
+  h->cur_list = -1;
+  h->lists_valid = n == 0;
+  h->unrecorded_step = n == 0 ? -1 : (int64_t)latest;
   return EMB_OK;
 }
 

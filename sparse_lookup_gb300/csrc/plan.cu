@@ -1,9 +1,12 @@
 // plan.cu -- emb_plan_create / destroy / info / device status and the C-ABI
 // wrappers of the forward and backward launches.
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <map>
+#include <mutex>
 #include <new>
+#include <unordered_map>
 
 #include "plan.cuh"
 #include "radix.cuh"
@@ -12,37 +15,96 @@ using namespace emb;
 
 namespace {
 
+std::mutex g_alloc_mu;
+std::unordered_map<void*, size_t> g_live;     // live handle allocations -> bytes
+int64_t g_live_bytes = 0;
+std::atomic<int64_t> g_fail_after{-1};        // allocations to grant before one fails; -1 = off
+
+}  // namespace
+
+namespace emb {
+
+cudaError_t dev_alloc(void** p, size_t bytes) {
+  *p = nullptr;
+  int64_t k = g_fail_after.load();
+  while (k >= 0) {
+    if (g_fail_after.compare_exchange_weak(k, k - 1)) {
+      if (k == 0) return cudaErrorMemoryAllocation;   // injected: nothing was asked of the driver
+      break;
+    }
+  }
+  const cudaError_t e = cudaMalloc(p, bytes);
+  if (e != cudaSuccess) {
+    *p = nullptr;
+    return e;
+  }
+  std::lock_guard<std::mutex> lk(g_alloc_mu);
+  g_live[*p] = bytes;
+  g_live_bytes += (int64_t)bytes;
+  return cudaSuccess;
+}
+
+void dev_free(void* p) {
+  if (!p) return;
+  {
+    std::lock_guard<std::mutex> lk(g_alloc_mu);
+    auto it = g_live.find(p);
+    if (it != g_live.end()) {
+      g_live_bytes -= (int64_t)it->second;
+      g_live.erase(it);
+    }
+  }
+  cudaFree(p);
+}
+
+}  // namespace emb
+
+extern "C" emb_status emb_debug_fail_alloc(int64_t after) {
+  if (after < -1) return EMB_ERR_INVALID_ARG;
+  g_fail_after.store(after);
+  return EMB_OK;
+}
+
+extern "C" emb_status emb_debug_live_allocations(int64_t* count, int64_t* bytes) {
+  std::lock_guard<std::mutex> lk(g_alloc_mu);
+  if (count) *count = (int64_t)g_live.size();
+  if (bytes) *bytes = g_live_bytes;
+  return EMB_OK;
+}
+
+namespace {
+
 void free_plan(emb_plan_s* p) {
   if (!p) return;
-  cudaFree(p->meta_d);
-  cudaFree(p->colg_d);
-  cudaFree(p->tables_d);
-  cudaFree(p->table_base_d);
-  cudaFree(p->status_d);
-  cudaFree(p->fwd_ticket);
-  cudaFree(p->col_order_d);
+  dev_free(p->meta_d);
+  dev_free(p->colg_d);
+  dev_free(p->tables_d);
+  dev_free(p->table_base_d);
+  dev_free(p->status_d);
+  dev_free(p->fwd_ticket);
+  dev_free(p->col_order_d);
   Workspace& w = p->ws;
-  cudaFree(w.keys[0]);
-  cudaFree(w.keys[1]);
-  cudaFree(w.vals[0]);
-  cudaFree(w.vals[1]);
-  cudaFree(w.inv_n);
-  cudaFree(w.rec_src);
-  cudaFree(w.touched);
-  cudaFree(w.bit_part);
-  cudaFree(w.n_uniq);
-  cudaFree(w.uniq);
-  cudaFree(w.slot_of);
-  cudaFree(w.cgrad);
-  cudaFree(w.ucount);
-  cudaFree(w.hist);
-  cudaFree(w.run_head);
-  cudaFree(w.head_pos);
-  cudaFree(w.n_runs);
-  cudaFree(w.scan_part);
-  cudaFree(w.partial);
-  cudaFree(w.part_pos);
-  cudaFree(w.part_thru);
+  dev_free(w.keys[0]);
+  dev_free(w.keys[1]);
+  dev_free(w.vals[0]);
+  dev_free(w.vals[1]);
+  dev_free(w.inv_n);
+  dev_free(w.rec_src);
+  dev_free(w.touched);
+  dev_free(w.bit_part);
+  dev_free(w.n_uniq);
+  dev_free(w.uniq);
+  dev_free(w.slot_of);
+  dev_free(w.cgrad);
+  dev_free(w.ucount);
+  dev_free(w.hist);
+  dev_free(w.run_head);
+  dev_free(w.head_pos);
+  dev_free(w.n_runs);
+  dev_free(w.scan_part);
+  dev_free(w.partial);
+  dev_free(w.part_pos);
+  dev_free(w.part_thru);
   delete p;
 }
 
@@ -50,7 +112,7 @@ template <class T>
 cudaError_t dmalloc(T** ptr, size_t count, size_t* total) {
   size_t bytes = sizeof(T) * (count > 0 ? count : 1);
   *total += bytes;
-  return cudaMalloc((void**)ptr, bytes);
+  return dev_alloc((void**)ptr, bytes);
 }
 
 emb_status validate_column(const emb_column_desc& c, bool training) {

@@ -110,6 +110,14 @@ inline emb_status cuda_status(cudaError_t e) {
     if (_e != cudaSuccess) return ::emb::cuda_status(_e); \
   } while (0)
 
+// Device memory of the plan and hash handles: every allocation goes through
+// dev_alloc and every release through dev_free (plan.cu), which keep a count
+// of live allocations and can be armed to fail one allocation on the host
+// (emb_debug_fail_alloc), so that tests reach each error path of a create
+// call without exhausting the GPU.  dev_free(nullptr) does nothing.
+cudaError_t dev_alloc(void** p, size_t bytes);
+void dev_free(void* p);
+
 // Launch-side entry points implemented in forward.cu / backward.cu / atomic.cu.
 emb_status launch_forward(emb_plan_s* p, int32_t batch, const int64_t* ids, const int32_t* id_offsets,
                           const float* id_weights, int64_t n_ids, const float* fvals, const int32_t* f_offsets,

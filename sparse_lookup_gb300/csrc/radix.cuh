@@ -7,7 +7,11 @@
 // Merrill, "Onesweep: a faster least significant digit radix sort for GPUs",
 // 2022).  Tiles are taken in launch order from a ticket counter, so a CTA
 // only ever waits on CTAs that are already running; every wait is bounded and
-// latches EMB_ERR_TIMEOUT instead of hanging.
+// latches EMB_ERR_TIMEOUT instead of hanging.  A tile whose wait gave up has
+// no valid output offsets: it also raises the sort's fail word (in its
+// scratch, cleared by each sort), and kernels that consume the sorted pairs
+// check that word and do nothing when it is set, since the output then has
+// holes holding an earlier call's pairs.
 //
 // The element count may live in device memory (n_dev != nullptr): grids are
 // then sized for the capacity, the count is clamped to it and tiles past the
@@ -157,7 +161,7 @@ template <class K, int BITS>
 __device__ __forceinline__ void onesweep_tile(SortSmemT<K, BITS>& sm, const K* __restrict__ kin,
                                               const uint32_t* __restrict__ vin, K* __restrict__ kout,
                                               uint32_t* __restrict__ vout, uint32_t n, uint32_t t, int tile_n,
-                                              int shift, uint32_t* lookback, uint32_t* status) {
+                                              int shift, uint32_t* lookback, uint32_t* status, uint32_t* fail) {
   using Count = typename SortSmemT<K, BITS>::Count;
   constexpr int R = 1 << BITS;
   constexpr int PER = (R + kSortThreads - 1) / kSortThreads;   // digits per thread
@@ -276,6 +280,7 @@ __device__ __forceinline__ void onesweep_tile(SortSmemT<K, BITS>& sm, const K* _
         if (z < kLookWin) {   // word j is not published yet
           if (++spins > kSpinLimit) {
             latch(status, EMB_ERR_TIMEOUT);
+            *(volatile uint32_t*)fail = 1u;
             break;
           }
           __nanosleep(32);
@@ -307,7 +312,8 @@ template <class K, int BITS, bool PERSIST>
 __global__ void __launch_bounds__(kSortThreads, 2)
     k_onesweep_t(const K* __restrict__ kin, const uint32_t* __restrict__ vin, K* __restrict__ kout,
                  uint32_t* __restrict__ vout, int64_t n0, const uint32_t* n_dev, int shift,
-                 const uint32_t* __restrict__ hist, uint32_t* lookback, uint32_t* tile_ctr, uint32_t* status) {
+                 const uint32_t* __restrict__ hist, uint32_t* lookback, uint32_t* tile_ctr, uint32_t* status,
+                 uint32_t* fail) {
   constexpr int R = 1 << BITS;
   constexpr int PER = (R + kSortThreads - 1) / kSortThreads;
   constexpr int TILE = sort_tile<K>();
@@ -333,20 +339,29 @@ __global__ void __launch_bounds__(kSortThreads, 2)
     if ((int64_t)t >= tiles) return;   // past the data: nobody waits on this ticket
     const int64_t left = n - (int64_t)t * TILE;
     onesweep_tile<K, BITS>(sm, kin, vin, kout, vout, (uint32_t)n, t, left >= TILE ? TILE : (int)left, shift,
-                           lookback, status);
+                           lookback, status, fail);
     if (PERSIST) __syncthreads();   // the tile's shared memory is free again
   } while (PERSIST);
 }
 
 // Words of scratch the sort of keys with key_bits bits needs for cap pairs:
-// hist [passes][R], tickets [passes], look-back words [passes][tiles][R].
+// hist [passes][R], tickets [passes], the fail word, look-back words
+// [passes][tiles][R].
 template <class K>
 inline size_t sort_scratch_words(int key_bits, int64_t cap) {
   int bits = 8, passes = 1;
   sort_plan(key_bits, &bits, &passes);
   const size_t R = (size_t)1 << bits;
   const int64_t tiles = (cap + sort_tile<K>() - 1) / sort_tile<K>();
-  return (size_t)passes * R + passes + (size_t)passes * tiles * R;
+  return (size_t)passes * R + passes + 1 + (size_t)passes * tiles * R;
+}
+
+// The fail word inside a sort's scratch: nonzero after a sort in which a
+// look-back wait gave up (its output is then incomplete).
+inline uint32_t* sort_fail_word(uint32_t* scratch, int key_bits) {
+  int bits = 8, passes = 1;
+  sort_plan(key_bits, &bits, &passes);
+  return scratch + (size_t)passes * ((size_t)1 << bits) + passes;
 }
 
 template <class K, int BITS>
@@ -357,7 +372,8 @@ inline emb_status radix_sort_passes(K* const keys[2], uint32_t* const vals[2], i
   const int64_t tiles = (cap + sort_tile<K>() - 1) / sort_tile<K>();
   uint32_t* hist = scratch;
   uint32_t* tickets = hist + (size_t)passes * R;
-  uint32_t* lookback = tickets + passes;
+  uint32_t* fail = tickets + passes;
+  uint32_t* lookback = fail + 1;
   const int hgrid = (int)std::min<int64_t>((cap + 511) / 512, (int64_t)sm_count * 4);
   k_digit_hist_t<K, BITS><<<hgrid, 512, 0, stream>>>(keys[0], n, n_dev, passes, hist);
   const bool persist = n_dev != nullptr;
@@ -372,11 +388,11 @@ inline emb_status radix_sort_passes(K* const keys[2], uint32_t* const vals[2], i
     if (persist)
       k_onesweep_t<K, BITS, true><<<(unsigned)grid, kSortThreads, smem, stream>>>(
           keys[in], vals[in], keys[out], vals[out], n, n_dev, ps * BITS, hist + ps * R,
-          lookback + (size_t)ps * tiles * R, tickets + ps, status);
+          lookback + (size_t)ps * tiles * R, tickets + ps, status, fail);
     else
       k_onesweep_t<K, BITS, false><<<(unsigned)grid, kSortThreads, smem, stream>>>(
           keys[in], vals[in], keys[out], vals[out], n, n_dev, ps * BITS, hist + ps * R,
-          lookback + (size_t)ps * tiles * R, tickets + ps, status);
+          lookback + (size_t)ps * tiles * R, tickets + ps, status, fail);
   }
   return EMB_OK;
 }
@@ -384,7 +400,8 @@ inline emb_status radix_sort_passes(K* const keys[2], uint32_t* const vals[2], i
 // Sorts keys[0]/vals[0] (n pairs, or *n_dev of at most cap) by their low
 // key_bits bits into keys[p&1], vals[p&1] with p = the number of passes.
 // `scratch` holds sort_scratch_words<K>(key_bits, cap) words and is cleared
-// here.  Returns the index of the buffer holding the result.
+// here (fail word included: sort_fail_word reads as 0 unless a wait of this
+// sort gave up).  Returns the index of the buffer holding the result.
 template <class K>
 inline emb_status radix_sort_pairs(K* const keys[2], uint32_t* const vals[2], int64_t n, const uint32_t* n_dev,
                                    int64_t cap, int key_bits, uint32_t* scratch, int sm_count, uint32_t* status,

@@ -9,7 +9,7 @@ import sparse_lookup_gb300 as sl
 from sparse_lookup_gb300 import build as slbuild
 from sparse_lookup_gb300 import synth
 
-from helpers import DynamicRun, assert_close, compare_hash_maps
+from helpers import DynamicRun, assert_close, assert_close_skip, compare_hash_maps
 
 pytestmark = pytest.mark.gpu
 
@@ -119,15 +119,104 @@ def test_keys_outside_the_range_are_rejected_on_the_device():
 
 def test_dynamic_training_loop_small():
     """lookup -> forward -> backward/Adagrad -> evict for 20 steps of a scaled
-    dynamic workload; rows bit-exact, pooled output and the row pool within
-    1e-5 rel / 1e-6 abs of the oracle."""
+    dynamic workload: rows bit-exact; every step's pooled output within 1e-5
+    rel / 1e-6 abs of the oracle's forward over the rows the library read;
+    every touched row's gradient, weights and accumulator, and the row pool
+    at the end, within 1e-5 rel / 1e-6 abs of the oracle running the same
+    steps on its own row pool, the only exclusions being elements the fp32
+    sum leaves ill-conditioned (in that step or an earlier one), counted."""
     run = DynamicRun(C=8, B=512, steps=20, num_slots=1 << 16, cap=1 << 13, ttl=4, key_bits=20)
+    skipped = 0
     for t in range(run.steps):
-        r = run.step(t, check=True)
+        r = run.step(t)
         assert r["status"][0] in (0, 5) and r["status"][1] == 0, r["status"]
         g, o = r["rows"]
         assert np.array_equal(g, o), "rows step %d" % t
-        assert_close(*r["out"], what="pooled step %d" % t)
-    adm = run.oh.export()
-    rows = adm["row"][adm["row"] >= 0]
-    assert_close(run.ht.weight.cpu().numpy()[rows], run.oh.W[rows], "row pool weights", rtol=1e-4, atol=1e-5)
+        skipped += assert_close_skip(*r["out"], what="pooled step %d" % t)
+    run.pool.check_pool(run.ht.weight, run.ht.acc)
+    assert run.checked > 0
+    print("excluded %d of %d updated elements; %d pooled elements skipped" % (run.excluded, run.checked, skipped))
+
+
+def _stream_step(ht, oh, t, C, B, ttl, seed=1011):
+    offs, keys = synth.dynamic_keys(seed, t, C, B, 1.2, 16, 5)
+    tids = np.concatenate([np.full(k.size, c, np.int32) for c, k in enumerate(keys)])
+    allk = np.concatenate(keys)
+    got, st = lookup(ht, tids, allk, t)
+    ref, st_o = oh.lookup_or_insert(tids, allk, t)
+    assert st == st_o, (st, st_o)
+    assert np.array_equal(np.asarray(got, np.int64), ref), "rows step %d" % t
+    ht.evict_expired(t, ttl)
+    oh.evict(t, ttl)
+
+
+@pytest.mark.parametrize("cap,thr,ttl", [(1 << 12, 2, 3), (300, 3, 5)])
+def test_export_import_resumes_the_stream(cap, thr, ttl):
+    """A table restored from its own snapshot (hash_export, then hash_import
+    into a fresh table with the row pool copied back) continues the stream as
+    the oracle, which never stopped, does: rows bit-exact every step, maps
+    equal after every step, admitted rows initialised identically.  The small
+    pool runs full, so entries still counting above the threshold are in the
+    snapshot too."""
+    import torch
+    C, B, slots, dim = 6, 256, 1 << 14, 8
+    ht = sl.HashTable(slots, cap, dim, thr, 256, 7, 0.01, C * B * 5)
+    oh = oracle.Hash(cap, dim, thr, 7, 0.01)
+    for t in range(8):
+        _stream_step(ht, oh, t, C, B, ttl)
+    snap = ht.export()
+    compare_hash_maps(snap, oh.export(), "snapshot")
+    ht2 = sl.HashTable(slots, cap, dim, thr, 256, 7, 0.01, C * B * 5)
+    ht2.import_entries(snap)
+    ht2.weight.copy_(ht.weight)
+    ht2.acc.copy_(ht.acc)
+    assert ht2.device_status() == 0
+    compare_hash_maps(ht2.export(), oh.export(), "imported")
+    del ht
+    for t in range(8, 24):
+        _stream_step(ht2, oh, t, C, B, ttl)
+        compare_hash_maps(ht2.export(), oh.export(), "step %d" % t)
+    live = oh.export()["row"]
+    live = live[live >= 0]
+    assert np.array_equal(ht2.weight.cpu().numpy()[live], oh.W[live])
+
+
+def test_import_into_a_used_table_replaces_its_entries():
+    """hash_import clears the table first: importing a snapshot into the very
+    table it came from, after further steps, brings back the older map."""
+    C, B, cap, slots, dim, thr, ttl = 4, 128, 2048, 1 << 13, 4, 2, 4
+    ht = sl.HashTable(slots, cap, dim, thr, 256, 3, 0.01, C * B * 5)
+    oh = oracle.Hash(cap, dim, thr, 3, 0.01)
+    for t in range(5):
+        _stream_step(ht, oh, t, C, B, ttl, seed=1012)
+    snap = ht.export()
+    for t in range(5, 9):
+        _stream_step(ht, oh, t, C, B, ttl, seed=1012)
+    ht.import_entries(snap)
+    assert ht.device_status() == 0
+    got = ht.export()
+    for k in ("tid", "key", "row", "last_seen"):
+        assert np.array_equal(got[k], snap[k]), k
+    counting = snap["row"] < 0
+    assert np.array_equal(got["count"][counting], snap["count"][counting])
+
+
+@pytest.mark.parametrize("bad", ["dup_key", "dup_row", "row_range", "key_range", "never_seen"])
+def test_import_rejects_a_bad_snapshot_on_the_device(bad):
+    ht = sl.HashTable(1024, 16, 4, 2, 64, 1, 0.1, 64)
+    snap = dict(tid=np.array([0, 0, 1], np.int32), key=np.array([5, 6, 5], np.int64),
+                row=np.array([0, 1, -1], np.int64), count=np.array([-1, -1, 1], np.int32),
+                last_seen=np.array([3, 4, 4], np.uint32))
+    if bad == "dup_key":
+        snap["key"][1] = 5
+    elif bad == "dup_row":
+        snap["row"][1] = 0
+    elif bad == "row_range":
+        snap["row"][1] = 16
+    elif bad == "key_range":
+        snap["key"][2] = 1 << 48
+    else:
+        snap["last_seen"][0] = 0xFFFFFFFF
+    ht.import_entries(snap)
+    assert ht.device_status() == 1
+    assert len(ht.export()["key"]) == 2   # the bad entry is left out
