@@ -202,6 +202,34 @@ def backward_bytes(w, n_contrib, valid_per_col, n_unique, dim):
     return n_contrib * 8 + n_contrib * 16 + grad + n_unique * 16 * dim
 
 
+def forward_bytes_compulsory(w, stats, table_dtype="f32"):
+    """forward_bytes with each table's distinct rows read once instead of
+    once per occurrence: the least a forward must move however skewed its
+    ids are (the rest can come from caches)."""
+    total = 0
+    dims = {}
+    for c, o in zip(w.columns, w.offsets):
+        n = int(o[-1])
+        e = 4 if c.transform == "bucketize" else 8
+        nb = 0 if c.boundaries is None else c.boundaries.size
+        total += (w.B + 1) * 4 + n * e + 4 * nb
+        total += w.B * 4 * c.dim * (c.pad_len if c.pooling == "padded" else 1)
+        dims[c.table] = c
+    for t, u in stats["unique_per_table"].items():
+        total += u * row_bytes(dims[t], table_dtype)
+    return total
+
+
+def backward_bytes_compulsory(w, n_contrib, stats, n_unique, dim):
+    """backward_bytes with the upstream gradient read once (each bag's
+    gradient row of a pooled column once, every padded position once)
+    instead of once per contribution."""
+    grad = 0
+    for c, nv, ne in zip(w.columns, stats["valid"], stats["nonempty_bags"]):
+        grad += (nv if c.pooling == "padded" else ne) * 4 * c.dim
+    return n_contrib * 8 + n_contrib * 16 + grad + n_unique * 16 * dim
+
+
 # ---------------------------------------------------------------------------
 # timing harness
 # ---------------------------------------------------------------------------
@@ -525,19 +553,34 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-# DRAM bytes per algorithmic byte of k_forward from the committed ncu captures
-# of the 320-column cases, tiled by bags like the full launches (154.75 MB of
-# DRAM traffic for 226.27 MB of algorithmic bytes with bags of 1..20 values;
-# 246.92 MB for 326.92 MB with one value per bag at batch 4096).  A full
-# launch is too large to capture; its traffic is the same ratio times its
-# algorithmic bytes.  Remove an entry whenever k_forward changes until it is
-# captured again.
-FORWARD_TRAFFIC_RATIO = {"inference": 154.75 / 226.27, "inference-onehot": 246.92 / 326.92}
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
+# ncu captures of the full-size launches, one pass each (profiles/ keeps the
+# summaries and commands).  An entry holds while the sources its kernels are
+# built from still hash as they did at the capture (KERNEL_SOURCES); once
+# they change, the bench reports the traffic as null until it is captured
+# again.
+KERNEL_SOURCES = {
+    "k_forward": ("forward.cu", "common.cuh", "plan.cuh"),
+    "backward": ("backward.cu", "radix.cuh", "update.cuh", "common.cuh", "plan.cuh"),
+}
+TRAFFIC = {}
 
 
-def traffic_estimate(workload, fbytes):
-    r = FORWARD_TRAFFIC_RATIO.get(workload)
-    return None if r is None else r * fbytes
+def kernel_src_hash(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "sparse_lookup_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(workload, kernel):
+    """{"bytes": DRAM bytes per launch, "source": capture} or None."""
+    e = TRAFFIC.get((workload, kernel))
+    if e is None or kernel not in KERNEL_SOURCES or e["src"] != kernel_src_hash(kernel):
+        return None
+    return {"bytes": e["bytes"], "source": e["source"]}
 
 
 def is_training(args):
@@ -556,7 +599,61 @@ def metric_name(workload, forward_only=False):
 # our arm
 # ---------------------------------------------------------------------------
 
+def roofline_obj(nbytes, nbytes_comp, ms, peak, peak_kind, traffic, **extra):
+    """HBM roofline of one launch (or call): occurrence-counted bytes (every
+    gathered occurrence's row) and compulsory bytes (each distinct row once)
+    over its mean event time, against the measured copy bandwidth."""
+    ach = nbytes / (ms / 1e3) / 1e9
+    achc = nbytes_comp / (ms / 1e3) / 1e9
+    out = {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+           "traffic": traffic.get("bytes") if traffic else None,
+           "bytes_per_launch": nbytes, "launch_ms": ms,
+           "bytes_compulsory": nbytes_comp, "achieved_compulsory": achc, "frac_compulsory": achc / peak,
+           "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy burst)"}
+    if traffic:
+        out["traffic_dram_gbs"] = traffic["bytes"] / (ms / 1e3) / 1e9
+        out["traffic_source"] = traffic["source"]
+    out.update(extra)
+    return out
+
+
+def training_leg(torch, sl, args, dev, stream, flush, peak, peak_kind):
+    """The fwd + bwd + Adagrad half of the metric, in the same run as the
+    forward line: the 200-column training workload (batch 8192, dim 64,
+    Zipf(1.1) ids, 3% out of range), device-timed steps with L2 flushed
+    between them."""
+    import argparse as _ap
+    import gc
+    w = synth.training()
+    a2 = _ap.Namespace(**vars(args))
+    a2.steps, a2.warmup, a2.backward, a2.table_dtype = args.training_steps, 3, "sort", "f32"
+    res = bench_plan(torch, sl, w, a2, dev, stream, flush, train=True, leg_only=True)
+    fw = statistics.mean(res["times"]["fwd"])
+    bw = statistics.mean(res["times"]["bwd"])
+    out = {"workload": w.name, "columns": len(w.columns), "batch": w.B, "dtype": "f32",
+           "ids_per_step": res["config"]["ids_per_step"],
+           "rows_gathered_per_step": res["rows_per_step"],
+           "distinct_rows_per_step": res["config"]["distinct_rows_per_step"],
+           "unique_rows_per_step": res["config"]["unique_rows_per_step"],
+           "steps": a2.steps, "warmup": a2.warmup,
+           "fwd_ms": fw, "bwd_ms": bw, "step_ms": res["ms_step"],
+           "rows_per_s": res["rows_per_step"] / (res["ms_step"] / 1e3),
+           "roofline": roofline_obj(res["fbytes"], res["fbytes_compulsory"], fw, peak, peak_kind,
+                                    traffic_for("training", "k_forward"), kernel="k_forward"),
+           "roofline_backward": roofline_obj(res["bbytes"], res["bbytes_compulsory"], bw, peak, peak_kind,
+                                             traffic_for("training", "backward"),
+                                             kernels="digit histogram, radix passes, run reduction + Adagrad, "
+                                                     "fixup"),
+           "gpu_launches": res["launches"], "clocks": res["clocks"],
+           "l2": "flushed between steps (2x L2 write, outside events)"}
+    del res, w
+    gc.collect()
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
+    import gc
     import torch
     import sparse_lookup_gb300 as sl
 
@@ -580,7 +677,7 @@ def run_ours(args):
     _, res["e2e"]["value"] = aggregate_ranks(torch, res["e2e_ms"], res["rows_per_step"], dev)
     peak, peak_kind = peaks()
     fw_ms = statistics.mean(res["times"]["fwd"])
-    achieved = res["fbytes"] / (fw_ms / 1e3) / 1e9
+    wl = w.name if args.table_dtype == "f32" else "%s-%s" % (w.name, args.table_dtype)
     line = {
         "metric": metric_name(args.workload, args.forward_only),
         "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -591,12 +688,8 @@ def run_ours(args):
                            if getattr(args, "pipeline", False) else
                            "flushed between steps (2x L2 write, outside events)"),
                        parallelism="replicas" if world > 1 else "1 GPU"),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak,
-                     "traffic": traffic_estimate(w.name if args.table_dtype == "f32" else
-                                                 "%s-%s" % (w.name, args.table_dtype), res["fbytes"]),
-                     "kernel": "k_forward", "bytes_per_launch": res["fbytes"], "launch_ms": fw_ms,
-                     "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy burst)"},
+        "roofline": roofline_obj(res["fbytes"], res.get("fbytes_compulsory", res["fbytes"]), fw_ms, peak, peak_kind,
+                                 traffic_for(wl, "k_forward"), kernel="k_forward"),
         "step_ms": {k: statistics.mean(v) for k, v in res["times"].items()},
         "e2e": res["e2e"],
         "gpu_launches": res["launches"],
@@ -606,40 +699,61 @@ def run_ours(args):
     }
     if "bbytes" in res:
         b_ms = statistics.mean(res["times"]["bwd"])
-        ab = res["bbytes"] / (b_ms / 1e3) / 1e9
-        line["roofline_backward"] = {"bound": "hbm", "achieved": ab, "peak": peak, "unit": "GB/s", "frac": ab / peak,
-                                     "bytes_per_call": res["bbytes"], "call_ms": b_ms,
-                                     "kernels": ("row bitmap, slot compaction, warp-merged atomics, Adagrad pass"
-                                                 if args.backward == "atomic" else
-                                                 "digit histogram, radix passes, run reduction + Adagrad, fixup")}
+        line["roofline_backward"] = roofline_obj(
+            res["bbytes"], res["bbytes_compulsory"], b_ms, peak, peak_kind, traffic_for(wl, "backward"),
+            kernels=("row bitmap, slot compaction, warp-merged atomics, Adagrad pass" if args.backward == "atomic"
+                     else "digit histogram, radix passes, run reduction + Adagrad, fixup"))
     if res.get("ceiling"):
         line["gather_ceiling"] = res["ceiling"]
-        line["gather_ceiling"]["frac_forward"] = achieved / res["ceiling"]["mix_gbs"]
+        if "row_bytes" in res:
+            # row bytes alone against the rate of row gathers alone
+            line["gather_ceiling"]["frac_rows"] = res["row_bytes"] / (fw_ms / 1e3) / 1e9 / res["ceiling"]["mix_gbs"]
+    del res
+    gc.collect()
+    torch.cuda.empty_cache()
+    if args.workload == "inference" and args.table_dtype == "f32" and not args.no_training_leg and args.columns is None:
+        line["training"] = training_leg(torch, sl, args, dev, stream, flush, peak, peak_kind)
+        line["gpu_launches"] += line["training"]["gpu_launches"]
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
 
 
-def valid_counts(w, rows_dbg, n_ids):
+def row_stats(w, rows_dbg, n_ids):
+    """From the library's transformed rows: valid (read) values per column,
+    distinct rows read per table, and bags with at least one valid value per
+    column.  Values past a padded column's pad_len (or a pooled column's
+    max_len) are not read."""
     r = rows_dbg.cpu().numpy()
-    out, pos = [], {0: 0, 1: n_ids}
+    valid, nonempty, per_table = [], [], {}
+    pos = {0: 0, 1: n_ids}
     for c, o in zip(w.columns, w.offsets):
         s = 1 if c.transform == "bucketize" else 0
         n = int(o[-1])
         rr = r[pos[s]:pos[s] + n]
-        if c.pooling == "padded":
-            # values past pad_len are not read
-            lens = np.diff(o)
-            keep = np.concatenate([np.arange(l) < c.pad_len for l in lens]) if n else np.zeros(0, bool)
-            out.append(int(((rr >= 0) & keep).sum()))
-        else:
-            out.append(int((rr >= 0).sum()))
         pos[s] += n
-    return out
+        o64 = np.asarray(o, np.int64)
+        bag = np.repeat(np.arange(w.B), np.diff(o64))
+        keep = rr >= 0
+        cut = c.pad_len if c.pooling == "padded" else int(getattr(c, "max_len", 0) or 0)
+        if cut > 0 and n:
+            keep &= (np.arange(n) - o64[bag]) < cut
+        valid.append(int(keep.sum()))
+        nonempty.append(int(np.count_nonzero(np.bincount(bag[keep], minlength=w.B))) if n else 0)
+        per_table.setdefault(c.table, []).append(rr[keep])
+    uniq = {t: int(np.unique(np.concatenate(v)).size) for t, v in per_table.items()}
+    return {"valid": valid, "nonempty_bags": nonempty, "unique_per_table": uniq}
 
 
-def bench_plan(torch, sl, w, args, dev, stream, flush, train):
+def valid_counts(w, rows_dbg, n_ids):
+    return row_stats(w, rows_dbg, n_ids)["valid"]
+
+
+def bench_plan(torch, sl, w, args, dev, stream, flush, train, leg_only=False):
+    """Time the workload's steps (forward, and for training plans backward +
+    Adagrad).  leg_only: only the device-timed steps (no end-to-end leg, graph,
+    gather ceiling or CPU baseline)."""
     tables = [None if t is None else synth.make_table(t, dev) for t in w.tables]
     accs = [None if t is None else torch.zeros_like(t) for t in tables] if train else None
     ids_h, id_off_h, fv_h, f_off_h = synth.jagged(w)
@@ -667,12 +781,16 @@ def bench_plan(torch, sl, w, args, dev, stream, flush, train):
     torch.cuda.synchronize()
     if plan.device_status() != 0:
         raise SystemExit("device status after the forward")
-    valid = valid_counts(w, rows_dbg, n_ids)
+    stats = row_stats(w, rows_dbg, n_ids)
+    valid = stats["valid"]
     del rows_dbg
     rows_per_step = sum(valid)
     fbytes = forward_bytes(w, valid, dt)
     res = {"rows_per_step": rows_per_step, "fbytes": fbytes,
-           "config": {"ids_per_step": n_all, "rows_gathered_per_step": rows_per_step, "table_dtype": dt}}
+           "fbytes_compulsory": forward_bytes_compulsory(w, stats, dt),
+           "row_bytes": sum(nv * row_bytes(c, dt) for c, nv in zip(w.columns, valid)),
+           "config": {"ids_per_step": n_all, "rows_gathered_per_step": rows_per_step, "table_dtype": dt,
+                      "distinct_rows_per_step": int(sum(stats["unique_per_table"].values()))}}
     G = Gseq = None
     if train:
         width = plan.out_width
@@ -683,6 +801,8 @@ def bench_plan(torch, sl, w, args, dev, stream, flush, train):
         n_unique = int(dbg["row"].numel())
         del dbg
         res["bbytes"] = backward_bytes(w, n_all, valid, n_unique, max(c.dim for c in w.columns))
+        res["bbytes_compulsory"] = backward_bytes_compulsory(w, n_all, stats, n_unique,
+                                                             max(c.dim for c in w.columns))
         res["config"]["unique_rows_per_step"] = n_unique
         res["config"]["backward"] = args.backward
 
@@ -719,6 +839,8 @@ def bench_plan(torch, sl, w, args, dev, stream, flush, train):
     res["launches"] = args.steps * (1 + bwd_launches)
     if plan.device_status() != 0:
         raise SystemExit("device status after the timed steps")
+    if leg_only:
+        return res
 
     # end to end through the C ABI with pinned host buffers
     host = [(torch.from_numpy(x).pin_memory(), d) for x, d in ((ids_h, ids), (id_off_h, id_off), (fv_h, fv),
@@ -1159,6 +1281,10 @@ def main():
                     help="dynamic workload: pipelined steps (next lookup beside this backward)")
     ap.add_argument("--backward", default="sort", choices=["sort", "atomic"],
                     help="training workloads: the sort-based backward or the atomic one")
+    ap.add_argument("--no-training-leg", action="store_true",
+                    help="inference workload: skip the training (fwd + bwd + Adagrad) leg of the line")
+    ap.add_argument("--training-steps", type=int, default=10,
+                    help="timed steps of the training leg")
     ap.add_argument("--graph", type=int, default=0,
                     help="also time this many back-to-back replays of one step captured in a CUDA graph")
     args = ap.parse_args()
