@@ -563,7 +563,12 @@ KERNEL_SOURCES = {
     "k_forward": ("forward.cu", "common.cuh", "plan.cuh"),
     "backward": ("backward.cu", "radix.cuh", "update.cuh", "common.cuh", "plan.cuh"),
 }
-TRAFFIC = {}
+TRAFFIC = {
+    ("inference", "k_forward"): {"bytes": 494.00e6 + 49.74e6, "src": "77136f5ee8806b8b",
+                                 "source": "profiles/traffic_full_size.md (ncu, 1 pass, full-size launch)"},
+    ("training", "k_forward"): {"bytes": 2.90e9 + 783.85e6, "src": "77136f5ee8806b8b",
+                                "source": "profiles/traffic_full_size.md (ncu, 1 pass, full-size launch)"},
+}
 
 
 def kernel_src_hash(kernel):

@@ -299,6 +299,7 @@ struct PendingRow {
 // training and sequence workloads), between 256 and kSegSpanMax.
 constexpr int kSegSpanMax = 1024;
 constexpr int kSegPerGroup = 64;
+constexpr int kSegDec = 4;   // entries a thread decodes per batch of loads
 
 inline int seg_span(int glog) {
   const int ng = kSegThreads / 32 * (32 >> glog);
@@ -421,32 +422,65 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
   // ---- decode the CTA's entries, coalesced, into shared memory; the
   //      weight and accumulator rows of every run that starts here are
   //      prefetched into L2 so that the updates below find them there ----
+  //      Entries are taken kSegDec per thread at a time and each stage's
+  //      loads (key, previous key and source; weight; column; 1/n) are all
+  //      issued before any is used, so a thread waits for each stage once
+  //      instead of once per entry.
   uint32_t lkey = a.sentinel;
   int ld4 = 0;
   TableCursor ptc;
-  for (int e = tid; e < a.span; e += kSegThreads) {
-    SegRec r;
-    r.key = a.sentinel;
-    r.off = 0u;
-    r.scale = 0.0f;
-    r.d4 = 0u;
-    if (e < span) {
-      const uint32_t key = __ldg(a.keys + B0 + e);
-      uint32_t val = __ldg(a.vals + B0 + e);   // loaded beside the key
-      r.key = key;
-      if (key != a.sentinel && (B0 + e == 0 || __ldg(a.keys + B0 + e - 1) != key)) {
-        ptc.seek(a, key);
-        const int64_t row = key - ptc.base;
-        prefetch_l2(ptc.weight + row * ptc.dim, (uint32_t)ptc.dim * 4u);
-        prefetch_l2(ptc.acc + row * ptc.dim, (uint32_t)ptc.dim * 4u);
+  for (int e0 = tid; e0 < a.span; e0 += kSegDec * kSegThreads) {
+    uint32_t kk[kSegDec], kp[kSegDec], vv[kSegDec];
+#pragma unroll
+    for (int j = 0; j < kSegDec; ++j) {
+      const int e = e0 + j * kSegThreads;
+      kk[j] = a.sentinel;
+      kp[j] = kNoKey;
+      vv[j] = 0u;
+      if (e < span) {
+        kk[j] = __ldg(a.keys + B0 + e);
+        vv[j] = __ldg(a.vals + B0 + e);
+        if (B0 + e > 0) kp[j] = __ldg(a.keys + B0 + e - 1);
       }
-      if (key != a.sentinel) {
-        float wr = 1.0f;   // value weight of a SUM contribution
-        if (a.rec_src) {
-          const uint2 rs = __ldg(a.rec_src + val);
-          val = rs.x;
-          wr = __uint_as_float(rs.y);
+    }
+    float wr[kSegDec];   // value weight of a SUM contribution
+#pragma unroll
+    for (int j = 0; j < kSegDec; ++j) {
+      wr[j] = 1.0f;
+      if (a.rec_src && kk[j] != a.sentinel) {
+        const uint2 rs = __ldg(a.rec_src + vv[j]);
+        vv[j] = rs.x;
+        wr[j] = __uint_as_float(rs.y);
+      }
+    }
+    int4 cg[kSegDec];
+#pragma unroll
+    for (int j = 0; j < kSegDec; ++j) {
+      cg[j] = make_int4(0, 0, 0, 0);
+      if (kk[j] != a.sentinel && !(vv[j] & kPadBit)) cg[j] = __ldg(a.colg + div_magic32(vv[j], a.bdiv));
+    }
+    float sc[kSegDec];
+#pragma unroll
+    for (int j = 0; j < kSegDec; ++j) sc[j] = cg[j].y ? __ldg(a.inv_n + vv[j]) : wr[j];
+#pragma unroll
+    for (int j = 0; j < kSegDec; ++j) {
+      const int e = e0 + j * kSegThreads;
+      if (e >= a.span) break;
+      SegRec r;
+      r.key = a.sentinel;
+      r.off = 0u;
+      r.scale = 0.0f;
+      r.d4 = 0u;
+      const uint32_t key = kk[j];
+      if (e < span && key != a.sentinel) {
+        r.key = key;
+        if (kp[j] != key) {   // a run starts here
+          ptc.seek(a, key);
+          const int64_t row = key - ptc.base;
+          prefetch_l2(ptc.weight + row * ptc.dim, (uint32_t)ptc.dim * 4u);
+          prefetch_l2(ptc.acc + row * ptc.dim, (uint32_t)ptc.dim * 4u);
         }
+        const uint32_t val = vv[j];
         if (val & kPadBit) {
           if (key != lkey) {
             lkey = key;
@@ -458,14 +492,13 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
         } else {
           const uint32_t c = div_magic32(val, a.bdiv);
           const uint32_t b = val - c * (uint32_t)a.batch;
-          const int4 cg = __ldg(a.colg + c);
-          r.scale = cg.y ? __ldg(a.inv_n + val) : wr;
-          r.d4 = (uint32_t)cg.z;
-          r.off = (uint32_t)(((int64_t)b * a.ldg + cg.x) >> 2);
+          r.scale = sc[j];
+          r.d4 = (uint32_t)cg[j].z;
+          r.off = (uint32_t)(((int64_t)b * a.ldg + cg[j].x) >> 2);
         }
       }
+      rec[e] = r;
     }
-    rec[e] = r;
   }
   for (int g = tid; g < NG; g += kSegThreads) {
     head_end[g] = -1;

@@ -344,6 +344,46 @@ __global__ void __launch_bounds__(kSortThreads, 2)
   } while (PERSIST);
 }
 
+// A sort whose pairs fit one tile, all passes in one CTA (small steps, where
+// the separate histogram and pass launches cost more than the work): each
+// pass counts its digits in shared memory, scans them and ranks and
+// scatters the tile as tile 0, which publishes its counts and never waits.
+// At most two passes: each buffer is then read at most once after it was
+// written in this kernel (the ranking reads its input through the
+// read-only path, which must not see a line cached before the write).
+template <class K, int BITS>
+__global__ void __launch_bounds__(kSortThreads, 1)
+    k_sort_one_tile(K* k0, uint32_t* v0, K* k1, uint32_t* v1, int n, int passes, uint32_t* lookback,
+                    uint32_t* status, uint32_t* fail) {
+  constexpr int R = 1 << BITS;
+  constexpr int PER = (R + kSortThreads - 1) / kSortThreads;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  SortSmemT<K, BITS>& sm = *reinterpret_cast<SortSmemT<K, BITS>*>(smem_raw);
+  const int tid = threadIdx.x;
+  if (tid == 0) *(volatile uint32_t*)fail = 0u;   // no wait here can run out
+  for (int p = 0; p < passes; ++p) {
+    const K* kin = (p & 1) ? k1 : k0;
+    const uint32_t* vin = (p & 1) ? v1 : v0;
+    K* kout = (p & 1) ? k0 : k1;
+    uint32_t* vout = (p & 1) ? v0 : v1;
+    for (int i = tid; i < R; i += kSortThreads) sm.hscan[i] = 0u;
+    for (int i = tid; i < kSortWarps * R; i += kSortThreads) (&sm.whist[0][0])[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < n; i += kSortThreads) atomicAdd(&sm.hscan[sort_digit<K, BITS>(kin[i], p * BITS)], 1u);
+    __syncthreads();
+    uint32_t hv[PER];
+#pragma unroll
+    for (int q = 0; q < PER; ++q) hv[q] = tid * PER + q < R ? sm.hscan[tid * PER + q] : 0u;
+    sort_scan_digits<R>(hv, sm.wsum);
+#pragma unroll
+    for (int q = 0; q < PER; ++q)
+      if (tid * PER + q < R) sm.hscan[tid * PER + q] = hv[q];
+    __syncthreads();
+    onesweep_tile<K, BITS>(sm, kin, vin, kout, vout, (uint32_t)n, 0u, n, p * BITS, lookback, status, fail);
+    __syncthreads();   // this pass's output is complete (and visible to the block) before the next reads it
+  }
+}
+
 // Words of scratch the sort of keys with key_bits bits needs for cap pairs:
 // hist [passes][R], tickets [passes], the fail word, look-back words
 // [passes][tiles][R].
@@ -413,6 +453,17 @@ inline emb_status radix_sort_pairs(K* const keys[2], uint32_t* const vals[2], in
   int bits = 8, passes = 1;
   sort_plan(key_bits, &bits, &passes);
   if (passes > kMaxSortPasses) return EMB_ERR_UNSUPPORTED;
+  if (!n_dev && n <= (int64_t)sort_tile<K>() && passes <= 2) {
+    // one tile: every pass in one CTA, no scratch to clear (tile 0 only
+    // writes its look-back words and never reads them)
+    const int smem = (int)sizeof(SortSmemT<K, 8>);
+    EMB_CUDA_TRY(cudaFuncSetAttribute(k_sort_one_tile<K, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+    uint32_t* fail = sort_fail_word(scratch, key_bits);
+    k_sort_one_tile<K, 8><<<1, kSortThreads, smem, stream>>>(keys[0], vals[0], keys[1], vals[1], (int)n, passes,
+                                                             fail + 1, status, fail);
+    *result = passes & 1;
+    return cuda_status(cudaGetLastError());
+  }
   EMB_CUDA_TRY(cudaMemsetAsync(scratch, 0, sort_scratch_words<K>(key_bits, cap) * sizeof(uint32_t), stream));
   const emb_status st =
       radix_sort_passes<K, 8>(keys, vals, n, n_dev, cap, passes, scratch, sm_count, status, stream);
