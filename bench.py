@@ -568,6 +568,10 @@ TRAFFIC = {
                                  "source": "profiles/traffic_full_size.md (ncu, 1 pass, full-size launch)"},
     ("training", "k_forward"): {"bytes": 2.90e9 + 783.85e6, "src": "77136f5ee8806b8b",
                                 "source": "profiles/traffic_full_size.md (ncu, 1 pass, full-size launch)"},
+    # the whole backward call: digit histogram, four radix passes, run
+    # reduction with Adagrad, fixup
+    ("training", "backward"): {"bytes": 12425220690, "src": "50128a77288f069a",
+                               "source": "profiles/traffic_full_size.md (ncu, 1 pass, each launch of one call)"},
 }
 
 
