@@ -709,7 +709,8 @@ def run_ours(args):
     if "bbytes" in res:
         b_ms = statistics.mean(res["times"]["bwd"])
         line["roofline_backward"] = roofline_obj(
-            res["bbytes"], res["bbytes_compulsory"], b_ms, peak, peak_kind, traffic_for(wl, "backward"),
+            res["bbytes"], res["bbytes_compulsory"], b_ms, peak, peak_kind,
+            traffic_for(wl, "backward") if args.backward == "sort" else None,
             kernels=("row bitmap, slot compaction, warp-merged atomics, Adagrad pass" if args.backward == "atomic"
                      else "digit histogram, radix passes, run reduction + Adagrad, fixup"))
     if res.get("ceiling"):
