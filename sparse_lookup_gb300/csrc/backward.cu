@@ -840,7 +840,7 @@ emb_status launch_backward(emb_plan_s* p, const float* grad_out, const float* gr
   a.partial = w.partial;
   a.part_pos = w.part_pos;
   a.part_thru = w.part_thru;
-  a.sort_fail = sort_fail_word(w.hist, p->key_bits);
+  a.sort_fail = sort_fail_word<uint32_t>(w.hist, p->key_bits);
   if (want_dbg) {
     const int nb = (int)((n + kScanBlock - 1) / kScanBlock);
     k_rank_reduce<<<nb, kScanBlock, 0, stream>>>(skeys, n, p->key_total, w.scan_part);
@@ -878,8 +878,10 @@ constexpr int64_t kNoAllocMaxN = int64_t(1) << 18;   // contributions per call
 constexpr int kNoAllocMaxDim = 256;
 constexpr int64_t kNoAllocTiles = (kNoAllocMaxN + kSortTile - 1) / kSortTile;
 constexpr int64_t kNoAllocBlocks = (kNoAllocMaxN + kUnit - 1) / kUnit;   // the smallest span seg_span_plan() returns
-// sort_scratch_words for up to 32-bit keys: four passes of 8-bit digits
-constexpr size_t kNoAllocSortWords = 4 * 256 + 4 + 1 + 4 * kNoAllocTiles * 256;
+// sort_scratch_words for up to 32-bit keys: the larger of four passes of
+// 8-bit digits and three of 9-bit digits
+constexpr size_t kNoAllocSortWords = 3 * 512 + 3 + 1 + 3 * kNoAllocTiles * 512;
+static_assert(kNoAllocSortWords >= 4 * 256 + 4 + 1 + 4 * kNoAllocTiles * 256, "no-alloc sort scratch");
 
 struct NoAllocScratch {
   uint32_t keys[2][kNoAllocMaxN];
@@ -1011,7 +1013,7 @@ extern "C" emb_status emb_sparse_adagrad_noalloc(const int64_t* rows, int64_t n,
   a.partial = s->partial;
   a.part_pos = s->part_pos;
   a.part_thru = s->part_thru;
-  a.sort_fail = sort_fail_word(s->sortw, key_bits);
+  a.sort_fail = sort_fail_word<uint32_t>(s->sortw, key_bits);
   st = launch_segreduce(a, n_blocks, stream);
   if (st != EMB_OK) return st;
   return cuda_status(cudaGetLastError());
@@ -1113,7 +1115,7 @@ extern "C" emb_status emb_selftest_sort_timeout(uint32_t* latched, uint32_t* fai
   }
   uint32_t* hist = scratch;
   uint32_t* tickets = hist + 256;
-  uint32_t* fail = sort_fail_word(scratch, key_bits);
+  uint32_t* fail = sort_fail_word<uint32_t>(scratch, key_bits);
   uint32_t* lookback = fail + 1;
   const int smem = (int)sizeof(SortSmemT<uint32_t, 8>);
   if (e == cudaSuccess) {

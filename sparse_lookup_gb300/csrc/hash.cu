@@ -744,9 +744,9 @@ extern "C" emb_status hash_lookup_or_insert(emb_hash h, const int32_t* table_ids
   k_hash_admit<<<h->sm_count * 4, 256, 0, stream>>>(h->slots, h->nkeys[res], h->nvals[res], h->counters,
                                                      h->max_keys, h->free_scan, h->free_rows, h->n_words, h->W,
                                                      h->acc, h->dim, h->seed, h->init_scale, h->status,
-                                                     sort_fail_word(h->sort_scratch, kHashKeyBits));
+                                                     sort_fail_word<uint64_t>(h->sort_scratch, kHashKeyBits));
   k_hash_mark<<<h->sm_count * 2, 256, 0, stream>>>(h->slots, h->nvals[res], h->counters, h->max_keys, h->used,
-                                                   sort_fail_word(h->sort_scratch, kHashKeyBits));
+                                                   sort_fail_word<uint64_t>(h->sort_scratch, kHashKeyBits));
   k_hash_fix<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(h->slots, n, rows_out);
   return cuda_status(cudaGetLastError());
 }

@@ -68,9 +68,17 @@ struct SortSmemT {
 // measured on 41.75 M training pairs of 30-bit keys, three passes of 10-bit
 // digits (1024 bins, 7.5 pairs per bin and tile) took 1.44 ms against 1.21 ms
 // for four passes of 8-bit digits -- the per-tile digit work and the shorter
-// output runs cost more than the pass saved.
+// output runs cost more than the pass saved.  32-bit keys of 25 to 27 bits
+// take three passes of 9-bit digits instead of four passes of which the
+// last would sort three bits or fewer.
+template <class K>
 inline void sort_plan(int key_bits, int* bits, int* passes) {
   const int kb = key_bits < 1 ? 1 : key_bits;
+  if (sizeof(K) == 4 && kb > 24 && kb <= 27) {
+    *bits = 9;
+    *passes = 3;
+    return;
+  }
   *bits = 8;
   *passes = (kb + 7) / 8;
 }
@@ -390,7 +398,7 @@ __global__ void __launch_bounds__(kSortThreads, 1)
 template <class K>
 inline size_t sort_scratch_words(int key_bits, int64_t cap) {
   int bits = 8, passes = 1;
-  sort_plan(key_bits, &bits, &passes);
+  sort_plan<K>(key_bits, &bits, &passes);
   const size_t R = (size_t)1 << bits;
   const int64_t tiles = (cap + sort_tile<K>() - 1) / sort_tile<K>();
   return (size_t)passes * R + passes + 1 + (size_t)passes * tiles * R;
@@ -398,9 +406,10 @@ inline size_t sort_scratch_words(int key_bits, int64_t cap) {
 
 // The fail word inside a sort's scratch: nonzero after a sort in which a
 // look-back wait gave up (its output is then incomplete).
+template <class K>
 inline uint32_t* sort_fail_word(uint32_t* scratch, int key_bits) {
   int bits = 8, passes = 1;
-  sort_plan(key_bits, &bits, &passes);
+  sort_plan<K>(key_bits, &bits, &passes);
   return scratch + (size_t)passes * ((size_t)1 << bits) + passes;
 }
 
@@ -451,22 +460,27 @@ inline emb_status radix_sort_pairs(K* const keys[2], uint32_t* const vals[2], in
   if (cap > (int64_t)kCountMask) return EMB_ERR_UNSUPPORTED;   // look-back words count in 30 bits
   if (n_dev) n = cap;
   int bits = 8, passes = 1;
-  sort_plan(key_bits, &bits, &passes);
+  sort_plan<K>(key_bits, &bits, &passes);
   if (passes > kMaxSortPasses) return EMB_ERR_UNSUPPORTED;
   if (!n_dev && n <= (int64_t)sort_tile<K>() && passes <= 2) {
     // one tile: every pass in one CTA, no scratch to clear (tile 0 only
     // writes its look-back words and never reads them)
     const int smem = (int)sizeof(SortSmemT<K, 8>);
     EMB_CUDA_TRY(cudaFuncSetAttribute(k_sort_one_tile<K, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-    uint32_t* fail = sort_fail_word(scratch, key_bits);
+    uint32_t* fail = sort_fail_word<K>(scratch, key_bits);
     k_sort_one_tile<K, 8><<<1, kSortThreads, smem, stream>>>(keys[0], vals[0], keys[1], vals[1], (int)n, passes,
                                                              fail + 1, status, fail);
     *result = passes & 1;
     return cuda_status(cudaGetLastError());
   }
   EMB_CUDA_TRY(cudaMemsetAsync(scratch, 0, sort_scratch_words<K>(key_bits, cap) * sizeof(uint32_t), stream));
-  const emb_status st =
-      radix_sort_passes<K, 8>(keys, vals, n, n_dev, cap, passes, scratch, sm_count, status, stream);
+  emb_status st;
+  if constexpr (sizeof(K) == 4) {
+    st = bits == 9 ? radix_sort_passes<K, 9>(keys, vals, n, n_dev, cap, passes, scratch, sm_count, status, stream)
+                   : radix_sort_passes<K, 8>(keys, vals, n, n_dev, cap, passes, scratch, sm_count, status, stream);
+  } else {
+    st = radix_sort_passes<K, 8>(keys, vals, n, n_dev, cap, passes, scratch, sm_count, status, stream);
+  }
   if (st != EMB_OK) return st;
   *result = passes & 1;
   return cuda_status(cudaGetLastError());

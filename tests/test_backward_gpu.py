@@ -57,6 +57,26 @@ def test_hot_row_spans_many_ctas():
         check_train_step(TrainStep(w))
 
 
+@pytest.mark.parametrize("rows", [(1 << 24) + 3, 40_000_000, (1 << 27) - 2000])
+def test_keys_of_25_to_27_bits_sort_in_three_passes(rows):
+    """Row keys of 25, 26 and 27 bits (three passes of 9-bit digits, the
+    last digit's top bits unused at 25 and 26), two tables, hot rows that
+    span many CTAs beside rows near the top of the key range; enough
+    contributions for several sort tiles."""
+    rng = np.random.default_rng(rows % 1000)
+    B = 2048
+    lens = rng.integers(1, 30, B)
+    n = int(lens.sum())
+    small = 1000
+    ids = rng.integers(rows - 5000, rows, n).astype(np.int64)
+    ids[rng.random(n) < 0.3] = rows - 7
+    ids2 = rng.integers(0, small, n).astype(np.int64)
+    cols = [ColumnSpec("identity", "sum", rows, 4, 0), ColumnSpec("identity", "mean", small, 4, 1)]
+    w = Workload("wide-keys", B, cols, [TableSpec(rows, 4, 11), TableSpec(small, 4, 12)],
+                 [synth.bag_offsets(lens)] * 2, [ids, ids2], lr=0.01)
+    check_train_step(TrainStep(w))
+
+
 def test_padded_and_mean_sequences_small():
     w = synth.sequences(seed=5, mode="padded", C=3, B=40, rows=3000, dim=128, len_lo=50, len_hi=300,
                         pad_len=200)
