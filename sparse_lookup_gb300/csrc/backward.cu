@@ -348,7 +348,7 @@ struct __align__(16) SegRec {
 // gradient-row ring of every lane, and the per-group run bookkeeping.
 struct SegLayout {
   int rec, part, ring, head_end, tail_key, head_thru, tail_valid, bytes;
-  __host__ __device__ static SegLayout of(int span, int ng, int d4, int v, int ring_depth) {
+  __host__ __device__ static SegLayout of(int span, int ng, int d4, int v, int ring_depth, int threads = kSegThreads) {
     SegLayout L;
     int o = 0;
     L.rec = o;
@@ -356,7 +356,7 @@ struct SegLayout {
     L.part = o;
     o += 2 * ng * d4 * 16;
     L.ring = o;
-    o += ring_depth * kSegThreads * v * 16;
+    o += ring_depth * threads * v * 16;
     L.head_end = o;
     o += ng * 4;
     L.tail_key = o;
@@ -395,25 +395,25 @@ __device__ __forceinline__ void cp_async_wait() {
 // cut at the range start leaves a head partial and one open at the range end
 // a tail partial, combined in group order after a barrier (and across CTAs
 // by k_seg_fixup).
-template <int V>
-__global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(const SegArgs a) {
-  extern __shared__ __align__(16) unsigned char seg_smem[];
-  if (*(volatile const uint32_t*)a.sort_fail) return;   // the same for every thread of the CTA
+// The work of one CTA of TH threads over the `span` sorted entries starting
+// at cta * span; seg_smem: its dynamic shared memory (SegLayout).
+template <int V, int TH>
+__device__ __forceinline__ void segreduce_body(const SegArgs& a, int64_t cta, unsigned char* seg_smem) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int glog = a.glog;
   const int G = 32 >> glog;
   const int q = lane >> glog, sub = lane & ((1 << glog) - 1);
-  const int NG = kSegWarps * G;
+  const int NG = (TH / 32) * G;
   const int grp = warp * G + q;
-  const int64_t B0 = (int64_t)blockIdx.x * a.span;
+  const int64_t B0 = (int64_t)cta * a.span;
   const int64_t B1 = min(B0 + (int64_t)a.span, a.n);
   const int span = (int)(B1 - B0);
   const int D4 = a.maxdim4;
   constexpr int kSegRing = SegDepth<V>::ring;
-  const SegLayout L = SegLayout::of(a.span, NG, D4, V, kSegRing);
+  const SegLayout L = SegLayout::of(a.span, NG, D4, V, kSegRing, TH);
   SegRec* rec = reinterpret_cast<SegRec*>(seg_smem + L.rec);
   float4* part = reinterpret_cast<float4*>(seg_smem + L.part);   // [2][NG * D4]
-  float4* ring = reinterpret_cast<float4*>(seg_smem + L.ring);   // [kSegRing][kSegThreads * V]
+  float4* ring = reinterpret_cast<float4*>(seg_smem + L.ring);   // [kSegRing][TH * V]
   int32_t* head_end = reinterpret_cast<int32_t*>(seg_smem + L.head_end);
   uint32_t* tail_key = reinterpret_cast<uint32_t*>(seg_smem + L.tail_key);
   uint8_t* head_thru = seg_smem + L.head_thru;
@@ -429,11 +429,11 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
   uint32_t lkey = a.sentinel;
   int ld4 = 0;
   TableCursor ptc;
-  for (int e0 = tid; e0 < a.span; e0 += kSegDec * kSegThreads) {
+  for (int e0 = tid; e0 < a.span; e0 += kSegDec * TH) {
     uint32_t kk[kSegDec], kp[kSegDec], vv[kSegDec];
 #pragma unroll
     for (int j = 0; j < kSegDec; ++j) {
-      const int e = e0 + j * kSegThreads;
+      const int e = e0 + j * TH;
       kk[j] = a.sentinel;
       kp[j] = kNoKey;
       vv[j] = 0u;
@@ -464,7 +464,7 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
     for (int j = 0; j < kSegDec; ++j) sc[j] = cg[j].y ? __ldg(a.inv_n + vv[j]) : wr[j];
 #pragma unroll
     for (int j = 0; j < kSegDec; ++j) {
-      const int e = e0 + j * kSegThreads;
+      const int e = e0 + j * TH;
       if (e >= a.span) break;
       SegRec r;
       r.key = a.sentinel;
@@ -500,7 +500,7 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
       rec[e] = r;
     }
   }
-  for (int g = tid; g < NG; g += kSegThreads) {
+  for (int g = tid; g < NG; g += TH) {
     head_end[g] = -1;
     head_thru[g] = 0;
     tail_valid[g] = 0;
@@ -517,9 +517,9 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
     const uint32_t prev = r0 > 0 ? rec[r0 - 1].key : (B0 > 0 ? __ldg(a.keys + B0 - 1) : kNoKey);
     chead = prev == ckey && ckey != a.sentinel;
   }
-  // this lane's ring slots: slot j holds V float4 at ring[(j * kSegThreads + tid) * V + v]
+  // this lane's ring slots: slot j holds V float4 at ring[(j * TH + tid) * V + v]
   const uint32_t ring0 = smem_u32(ring + (size_t)tid * V);
-  constexpr uint32_t kSlotBytes = (uint32_t)kSegThreads * V * 16u;
+  constexpr uint32_t kSlotBytes = (uint32_t)TH * V * 16u;
   auto issue = [&](int e, int slot) {
     if (e < r1) {
       const SegRec r = rec[e];
@@ -551,7 +551,7 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
     const float sc = rec[e].scale;
     float4 x[V];
 #pragma unroll
-    for (int v = 0; v < V; ++v) x[v] = ring[((size_t)slot * kSegThreads + tid) * V + v];
+    for (int v = 0; v < V; ++v) x[v] = ring[((size_t)slot * TH + tid) * V + v];
     if (key != ckey) {   // the open run ends before this entry
       if (ckey != a.sentinel) {
         if (chead) {
@@ -623,8 +623,8 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
 
   // ---- runs cut between groups: the group holding a run's start adds the
   //      head partials of the following groups in order ----
-  int32_t* P = a.part_pos + (int64_t)blockIdx.x * 2;
-  float4* GP = a.partial + (int64_t)blockIdx.x * 2 * D4;
+  int32_t* P = a.part_pos + (int64_t)cta * 2;
+  float4* GP = a.partial + (int64_t)cta * 2 * D4;
   if (tail_valid[grp]) {
     float4 s[V];
 #pragma unroll
@@ -689,9 +689,16 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
     }
     if (sub == 0) {
       P[0] = end;
-      a.part_thru[blockIdx.x] = thru ? 1 : 0;
+      a.part_thru[cta] = thru ? 1 : 0;
     }
   }
+}
+
+template <int V>
+__global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(const SegArgs a) {
+  extern __shared__ __align__(16) unsigned char seg_smem[];
+  if (*(volatile const uint32_t*)a.sort_fail) return;   // the same for every thread of the CTA
+  segreduce_body<V, kSegThreads>(a, blockIdx.x, seg_smem);
 }
 
 // Runs cut by CTA boundaries: one lane group per boundary b (between CTA b-1
@@ -805,16 +812,7 @@ emb_status launch_backward(emb_plan_s* p, const float* grad_out, const float* gr
     if (want_dbg && dbg->n_unique) EMB_CUDA_TRY(cudaMemsetAsync(dbg->n_unique, 0, sizeof(int64_t), stream));
     return EMB_OK;
   }
-  int res = 0;
-  emb_status st = radix_sort_pairs<uint32_t>(w.keys, w.vals, n, nullptr, n, p->key_bits, w.hist, p->sm_count,
-                                             p->status_d, stream, &res);
-  if (st != EMB_OK) return st;
-  const uint32_t* skeys = w.keys[res];
-  const uint32_t* svals = w.vals[res];
-
   SegArgs a{};
-  a.keys = skeys;
-  a.vals = svals;
   a.n = n;
   a.sentinel = p->key_total;
   a.colg = p->colg_d;
@@ -831,33 +829,43 @@ emb_status launch_backward(emb_plan_s* p, const float* grad_out, const float* gr
   a.lr = lr;
   a.eps = eps;
   a.maxdim4 = p->max_dim / 4;
-  const int glog = seg_glog(a.maxdim4);
-  a.glog = glog;
-  a.span = seg_span_plan(glog, n, p->sm_count);
-  const int64_t span = a.span;
-  const int64_t n_blocks = (n + span - 1) / span;
-  if (n_blocks > w.n_units_max) return EMB_ERR_UNSUPPORTED;
   a.partial = w.partial;
   a.part_pos = w.part_pos;
   a.part_thru = w.part_thru;
-  a.sort_fail = sort_fail_word<uint32_t>(w.hist, p->key_bits);
+  int64_t* const n_uniq = want_dbg ? (dbg->n_unique ? dbg->n_unique : reinterpret_cast<int64_t*>(w.n_runs)) : nullptr;
   if (want_dbg) {
-    const int nb = (int)((n + kScanBlock - 1) / kScanBlock);
-    k_rank_reduce<<<nb, kScanBlock, 0, stream>>>(skeys, n, p->key_total, w.scan_part);
-    k_rank_top<<<1, kScanBlock, 0, stream>>>(w.scan_part, nb,
-                                             dbg->n_unique ? dbg->n_unique : reinterpret_cast<int64_t*>(w.n_runs));
-    k_rank_down<<<nb, kScanBlock, 0, stream>>>(skeys, n, p->key_total, w.scan_part, w.run_head, w.head_pos);
-    a.rank = w.run_head;
     a.dbg_table = dbg->uniq_table;
     a.dbg_row = dbg->uniq_row;
     a.dbg_count = dbg->counts;
     a.dbg_grad = dbg->agg_grad;
     a.dbg_ld = p->max_dim;
   }
+  int res = 0;
+  emb_status st = radix_sort_pairs<uint32_t>(w.keys, w.vals, n, nullptr, n, p->key_bits, w.hist, p->sm_count,
+                                             p->status_d, stream, &res);
+  if (st != EMB_OK) return st;
+  const uint32_t* skeys = w.keys[res];
+  const uint32_t* svals = w.vals[res];
+  a.keys = skeys;
+  a.vals = svals;
+  const int glog = seg_glog(a.maxdim4);
+  a.glog = glog;
+  a.span = seg_span_plan(glog, n, p->sm_count);
+  const int64_t span = a.span;
+  const int64_t n_blocks = (n + span - 1) / span;
+  if (n_blocks > w.n_units_max) return EMB_ERR_UNSUPPORTED;
+  a.sort_fail = sort_fail_word<uint32_t>(w.hist, p->key_bits);
+  if (want_dbg) {
+    const int nb = (int)((n + kScanBlock - 1) / kScanBlock);
+    k_rank_reduce<<<nb, kScanBlock, 0, stream>>>(skeys, n, p->key_total, w.scan_part);
+    k_rank_top<<<1, kScanBlock, 0, stream>>>(w.scan_part, nb, n_uniq);
+    k_rank_down<<<nb, kScanBlock, 0, stream>>>(skeys, n, p->key_total, w.scan_part, w.run_head, w.head_pos);
+    a.rank = w.run_head;
+  }
   st = launch_segreduce(a, n_blocks, stream);
   if (st != EMB_OK) return st;
   if (want_dbg && (dbg->uniq_table || dbg->uniq_row || dbg->counts)) {
-    const int64_t* nu = dbg->n_unique ? dbg->n_unique : reinterpret_cast<const int64_t*>(w.n_runs);
+    const int64_t* nu = n_uniq;
     k_dbg_runs<<<p->sm_count * 4, 256, 0, stream>>>(skeys, n, p->key_total, w.head_pos, nu, p->table_base_d,
                                                     p->n_tables, dbg->uniq_table, dbg->uniq_row, dbg->counts);
   }
@@ -983,13 +991,7 @@ extern "C" emb_status emb_sparse_adagrad_noalloc(const int64_t* rows, int64_t n,
   k_noalloc_pairs<<<(unsigned)((n + 255) / 256), 256, 0, stream>>>(rows, n, num_rows, s->keys[0], s->vals[0]);
   uint32_t* const nk[2] = {s->keys[0], s->keys[1]};
   uint32_t* const nv[2] = {s->vals[0], s->vals[1]};
-  int res = 0;
-  // the sort clears its part of the area (histograms, tickets, look-back words) itself
-  st = radix_sort_pairs<uint32_t>(nk, nv, n, nullptr, n, key_bits, s->sortw, sms, &s->status, stream, &res);
-  if (st != EMB_OK) return st;
   SegArgs a{};
-  a.keys = s->keys[res];
-  a.vals = s->vals[res];
   a.n = n;
   a.sentinel = (uint32_t)num_rows;
   a.colg = &s->colg;
@@ -1005,14 +1007,21 @@ extern "C" emb_status emb_sparse_adagrad_noalloc(const int64_t* rows, int64_t n,
   a.lr = lr;
   a.eps = eps;
   a.maxdim4 = dim / 4;
-  const int glog = seg_glog(a.maxdim4);
-  a.glog = glog;
-  a.span = seg_span_plan(glog, n, sms);   // the plan path's span: the same sums in the same order
-  const int64_t span = a.span;
-  const int64_t n_blocks = (n + span - 1) / span;
   a.partial = s->partial;
   a.part_pos = s->part_pos;
   a.part_thru = s->part_thru;
+  // the plan path's spans: the same sums in the same order
+  int res = 0;
+  // the sort clears its part of the area (histograms, tickets, look-back words) itself
+  st = radix_sort_pairs<uint32_t>(nk, nv, n, nullptr, n, key_bits, s->sortw, sms, &s->status, stream, &res);
+  if (st != EMB_OK) return st;
+  a.keys = s->keys[res];
+  a.vals = s->vals[res];
+  const int glog = seg_glog(a.maxdim4);
+  a.glog = glog;
+  a.span = seg_span_plan(glog, n, sms);
+  const int64_t span = a.span;
+  const int64_t n_blocks = (n + span - 1) / span;
   a.sort_fail = sort_fail_word<uint32_t>(s->sortw, key_bits);
   st = launch_segreduce(a, n_blocks, stream);
   if (st != EMB_OK) return st;
