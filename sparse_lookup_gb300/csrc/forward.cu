@@ -25,8 +25,10 @@
 //          four deep and sum them per bag; a bag that spans ranges leaves
 //          head/tail partials which the group holding its first value adds up
 //          in range order (deterministic);
-//   C.     bags longer than kLongBag (padded: pad_len > kLongBag) are pooled /
-//          copied by the whole warp, 32 values per step.
+//   C.     pooled bags longer than kLongBag are pooled by the whole warp, 32
+//          values per step.
+// Padded columns with pad_len > kLongBag are copied in pieces of about
+// kPadPiece positions, tiles of their own after the value tiles.
 // Empty bags and bags whose values were all dropped get the default vector.
 #include <algorithm>
 
@@ -45,6 +47,7 @@ constexpr int kUPool = 4;          // row loads in flight per lane when pooling 
 constexpr int kOneHotBags = 256;   // bags of one value each that one warp chunk copies
 constexpr int kMaxTileBags = 1024;  // static schedule: at most this many bags per tile
 constexpr int64_t kShortBagMean = 16;   // static schedule: streams with shorter bags tile by bags
+constexpr int kPadPiece = 64;      // positions per piece of a long padded bag (about)
 constexpr int kFwdWarpsPerCta = kFwdThreads / kWarp;
 
 struct FwdArgs {
@@ -78,6 +81,14 @@ struct FwdArgs {
   unsigned long long* ticket;   // [0] next tile, [1] warps done; both 0 between launches
   int64_t n_warps;              // warps launched
   int32_t dynamic;              // schedule: 0 static, 1 persistent warps with tickets
+  // pieces of long padded bags, the tiles after the value tiles: tile t is
+  // piece t mod npc of bag (t / npc) mod batch of long padded column
+  // t / (batch * npc)
+  int64_t pad_tiles;
+  const int32_t* pad_cols;      // meta position of each long padded column
+  int32_t pad_npc;              // pieces per bag
+  DivMagic32 pad_ndiv;          // division by pad_npc
+  DivMagic32 pad_bdiv;          // division by batch * pad_npc
 };
 
 struct __align__(16) WarpSmem {
@@ -585,14 +596,77 @@ __device__ void warp_pad_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta& m,
 #pragma unroll
       for (int v = 0; v < V; ++v) {
         const int f4 = sub + v * 32;
-        if (f4 < m.dim4) *reinterpret_cast<float4*>(dst + f4 * 4) = raw_f4<DT>(vals[u][v]);
+        if (f4 < m.dim4) __stcs(reinterpret_cast<float4*>(dst + f4 * 4), raw_f4<DT>(vals[u][v]));
       }
     }
   }
 }
 
 // ---------------------------------------------------------------------------
-// phase C: one long bag, the whole warp, values transformed on the fly
+// padded pieces: positions [p_lo, p_hi) of one padded bag, the whole warp
+// ---------------------------------------------------------------------------
+// A long padded bag (pad_len > kLongBag) is copied in pieces of positions,
+// each a tile of its own, so that no warp copies a whole bag while the rest
+// of the launch has finished.  Positions past the bag's values are zeros.
+// The output is written once and never read back by the launch: its stores
+// are marked evict-first, so they do not push table rows out of L2.
+template <int V, bool WT, int DT>
+__device__ void warp_pad_piece(const FwdArgs& a, int st, const ColMeta& m, int32_t b, int64_t lo, int64_t hi,
+                               int p_lo, int p_hi, int glog) {
+  constexpr int U = kU / V * (WT ? 1 : kRawScale<DT>);
+  const int lane = threadIdx.x & 31;
+  const int G = 32 >> glog;
+  const int grp = lane >> glog, sub = lane & ((1 << glog) - 1);
+  const float* E = m.weight;
+  const int P = m.pad_len;
+  const int64_t len = hi - lo;
+  float* dst = a.seq_out + m.seq_unit * a.batch + (int64_t)b * P * m.dim;
+  for (int p0 = p_lo; p0 < p_hi; p0 += 32) {
+    const int cnt = min(32, p_hi - p0);
+    if (p0 >= len) {
+      // zeros only: the positions' rows are contiguous in the output
+      float4* z = reinterpret_cast<float4*>(dst + (int64_t)p0 * m.dim);
+      for (int k = lane; k < cnt * m.dim4; k += 32) __stcs(z + k, f4zero());
+      continue;
+    }
+    int32_t row = -1;
+    const int p = p0 + lane;
+    if (lane < cnt && p < len) {
+      row = col_row(m, a.ids, a.fvals, lo + p);
+      record<WT>(a, st, lo + p, row, m, padded_gsrc(a, m, b, p));
+    }
+    for (int k = 0; k < cnt; k += U * G) {
+      RowRaw<DT> v[U][V];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = k + u * G + grp;
+        const int r = __shfl_sync(kFull, row, j & 31);
+        const bool ok = (j < cnt) && (r >= 0);
+#pragma unroll
+        for (int q = 0; q < V; ++q) {
+          const int f4 = sub + q * 32;
+          v[u][q] = (ok && f4 < m.dim4) ? row_raw<DT>(E, m.dim, m.qscale, r, f4) : raw_zero<DT>();
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = k + u * G + grp;
+#pragma unroll
+        for (int q = 0; q < V; ++q) {
+          const int f4 = sub + q * 32;
+          if (j < cnt && f4 < m.dim4)
+            __stcs(reinterpret_cast<float4*>(dst + (int64_t)(p0 + j) * m.dim + f4 * 4), raw_f4<DT>(v[u][q]));
+        }
+      }
+    }
+  }
+  // values past pad_len: no output, no gradient (recorded by the last piece)
+  if (p_hi == P && (a.rows_dbg || a.keys))
+    for (int64_t t = lo + P + lane; t < hi; t += 32) record_cut(a, st, t, m);
+}
+
+// ---------------------------------------------------------------------------
+// phase C: one long pooled bag, the whole warp, values transformed on the fly
 // ---------------------------------------------------------------------------
 template <int V, bool WT, int DT>
 __device__ void warp_long_bag(const FwdArgs& a, int st, const ColMeta& m, const float* W, int32_t b, int64_t lo,
@@ -602,47 +676,6 @@ __device__ void warp_long_bag(const FwdArgs& a, int st, const ColMeta& m, const 
   const int G = 32 >> glog;
   const int grp = lane >> glog, sub = lane & ((1 << glog) - 1);
   const float* E = m.weight;
-  if (m.pooling == EMB_POOL_NONE_PADDED) {
-    const int P = m.pad_len;
-    const int64_t len = hi - lo;
-    float* dst = a.seq_out + m.seq_unit * a.batch + (int64_t)b * P * m.dim;
-    for (int64_t p0 = 0; p0 < P; p0 += 32) {
-      const int cnt = (int)(P - p0 < 32 ? P - p0 : 32);
-      int32_t row = -1;
-      const int64_t p = p0 + lane;
-      if (lane < cnt && p < len) {
-        row = col_row(m, a.ids, a.fvals, lo + p);
-        record<WT>(a, st, lo + p, row, m, padded_gsrc(a, m, b, p));
-      }
-      for (int k = 0; k < cnt; k += U * G) {
-        RowRaw<DT> v[U][V];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int j = k + u * G + grp;
-          const int r = __shfl_sync(kFull, row, j & 31);
-          const bool ok = (j < cnt) && (r >= 0);
-#pragma unroll
-          for (int q = 0; q < V; ++q) {
-            const int f4 = sub + q * 32;
-            v[u][q] = (ok && f4 < m.dim4) ? row_raw<DT>(E, m.dim, m.qscale, r, f4) : raw_zero<DT>();
-          }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int j = k + u * G + grp;
-#pragma unroll
-          for (int q = 0; q < V; ++q) {
-            const int f4 = sub + q * 32;
-            if (j < cnt && f4 < m.dim4)
-              *reinterpret_cast<float4*>(dst + (p0 + j) * m.dim + f4 * 4) = raw_f4<DT>(v[u][q]);
-          }
-        }
-      }
-    }
-    if (a.rows_dbg || a.keys)
-      for (int64_t t = lo + P + lane; t < hi; t += 32) record_cut(a, st, t, m);
-    return;
-  }
   const uint32_t gsrc = pooled_gsrc(a, m, b);
   float4 acc[V], cmp[V];
 #pragma unroll
@@ -791,6 +824,8 @@ __device__ void warp_onehot_chunk(const FwdArgs& a, WarpSmem& ws, const ColMeta&
 // ---------------------------------------------------------------------------
 template <bool WT, bool LP>
 __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int st, int64_t tile);
+template <bool WT, bool LP>
+__device__ __forceinline__ void forward_piece(const FwdArgs& a, WarpSmem& ws, int64_t t);
 
 // Two schedules.  Static: one tile per warp, the grid covers all tiles (warps
 // of one CTA hold neighbouring tiles, whose offset searches share L1).
@@ -808,18 +843,23 @@ __global__ void __launch_bounds__(kFwdThreads, 4) k_forward(const FwdArgs a) {
   __shared__ WarpSmem smem[kFwdWarpsPerCta];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   WarpSmem& ws = smem[warp];
-  const int64_t n_tiles = a.tiles[0] + a.tiles[1];
+  const int64_t n_vt = a.tiles[0] + a.tiles[1];
+  const int64_t n_tiles = n_vt + a.pad_tiles;
   // the first tile of every warp is its warp index; tickets count from there
   int64_t tile = (int64_t)blockIdx.x * kFwdWarpsPerCta + warp;
   while (tile < n_tiles) {
-    const int st = tile < a.tiles[0] ? 0 : 1;
-    int64_t lt = st ? tile - a.tiles[0] : tile;
-    if (a.tpc[st] > 0) {
-      // bag tiles whole columns apart: take the columns in work order
-      const int j = (int)div_magic32((uint32_t)lt, a.tpc_div[st]);
-      lt = (int64_t)__ldg(a.col_order + a.col_base[st] + j) * a.tpc[st] + (lt - (int64_t)j * a.tpc[st]);
+    if (tile >= n_vt) {
+      forward_piece<WT, LP>(a, ws, tile - n_vt);
+    } else {
+      const int st = tile < a.tiles[0] ? 0 : 1;
+      int64_t lt = st ? tile - a.tiles[0] : tile;
+      if (a.tpc[st] > 0) {
+        // bag tiles whole columns apart: take the columns in work order
+        const int j = (int)div_magic32((uint32_t)lt, a.tpc_div[st]);
+        lt = (int64_t)__ldg(a.col_order + a.col_base[st] + j) * a.tpc[st] + (lt - (int64_t)j * a.tpc[st]);
+      }
+      forward_tile<WT, LP>(a, ws, st, lt);
     }
-    forward_tile<WT, LP>(a, ws, st, lt);
     if (!a.dynamic) break;   // static: one tile per warp
     unsigned long long tk = 0;
     if (lane == 0) tk = atomicAdd(&a.ticket[0], 1ull);
@@ -833,6 +873,47 @@ __global__ void __launch_bounds__(kFwdThreads, 4) k_forward(const FwdArgs a) {
       atomicExch(&a.ticket[1], 0ull);
     }
   }
+}
+
+// One piece of a long padded bag: its column, bag and positions follow from
+// the piece index alone.
+template <bool WT, bool LP>
+__device__ __forceinline__ void forward_piece(const FwdArgs& a, WarpSmem& ws, int64_t t) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t tt = (uint32_t)t;
+  const uint32_t j = div_magic32(tt, a.pad_bdiv);
+  const uint32_t r = tt - j * a.pad_bdiv.d;
+  const uint32_t b = div_magic32(r, a.pad_ndiv);
+  const int q = (int)(r - b * a.pad_ndiv.d);
+  const int mi = __ldg(a.pad_cols + j);
+  const int st = mi >= a.ncols[0] ? 1 : 0;
+  const int64_t seg = (int64_t)(mi - a.col_base[st]) * a.batch + b;
+  const int32_t o_lo = __ldg(a.offs[st] + seg), o_hi = __ldg(a.offs[st] + seg + 1);
+  __syncwarp();   // the previous tile's reads of ws.cm are done
+  if (lane < (int)(sizeof(ColMeta) / 4))
+    reinterpret_cast<int32_t*>(&ws.cm)[lane] = __ldg(reinterpret_cast<const int32_t*>(a.meta + mi) + lane);
+  __syncwarp();
+  const ColMeta& m = ws.cm;
+  bool bad = false;
+  const int64_t lo = clamp_off(o_lo, a.n[st], bad);
+  int64_t hi = clamp_off(o_hi, a.n[st], bad);
+  if (hi < lo) {
+    hi = lo;
+    bad = true;
+  }
+  if (bad && lane == 0) latch(a.status, EMB_ERR_BAD_INDEX);
+  const int P = m.pad_len;
+  const int PL = ((P + a.pad_npc - 1) / a.pad_npc + 31) & ~31;   // positions per piece
+  const int p_lo = q * PL, p_hi = min(P, p_lo + PL);
+  if (p_lo < p_hi) {
+    const int glog = lanes_log2(m.dim4);
+    with_dtype<LP>(m.dtype, [&](auto dt) {
+      constexpr int DT = decltype(dt)::value;
+      if (m.dim4 > 32) warp_pad_piece<2, WT, DT>(a, st, m, (int32_t)b, lo, hi, p_lo, p_hi, glog);
+      else warp_pad_piece<1, WT, DT>(a, st, m, (int32_t)b, lo, hi, p_lo, p_hi, glog);
+    });
+  }
+  __syncwarp();
 }
 
 template <bool WT, bool LP>
@@ -999,8 +1080,9 @@ __device__ __forceinline__ void forward_tile(const FwdArgs& a, WarpSmem& ws, int
       }
     });
 
-    // ---- phase C: long bags of the chunk ----
-    for (unsigned lm = longmask; lm; lm &= lm - 1) {
+    // ---- phase C: long pooled bags of the chunk (long padded bags are
+    //      copied by their pieces' tiles) ----
+    for (unsigned lm = padded ? 0u : longmask; lm; lm &= lm - 1) {
       const int i = __ffs(lm) - 1;
       const int64_t blo = __shfl_sync(kFull, lo, i);
       const int64_t bhi = __shfl_sync(kFull, hi, i);
@@ -1077,8 +1159,22 @@ emb_status launch_forward(emb_plan_s* p, int32_t batch, const int64_t* ids, cons
   if (!a.dynamic)
     while (E > 32 && total / E < warps / 8) E >>= 1;
   a.tile_elems = (int32_t)E;
-  a.tiles[0] = a.ncols[0] > 0 ? n_ids / E + 1 : 0;
-  a.tiles[1] = a.ncols[1] > 0 ? n_fvals / E + 1 : 0;
+  // a stream whose columns are all long padded has no value tiles: its
+  // pieces do all its work
+  a.tiles[0] = a.ncols[0] > 0 && !p->long_padded_only[0] ? n_ids / E + 1 : 0;
+  a.tiles[1] = a.ncols[1] > 0 && !p->long_padded_only[1] ? n_fvals / E + 1 : 0;
+  if (p->n_long_padded > 0) {
+    // pieces of about kPadPiece positions, as many per bag for every column
+    // (at most 2^31 pieces in all)
+    const int64_t bags = (int64_t)batch * p->n_long_padded;
+    int64_t npc = (p->max_long_pad + kPadPiece - 1) / kPadPiece;
+    npc = std::max<int64_t>(1, std::min<int64_t>(npc, INT32_MAX / bags));
+    a.pad_tiles = bags * npc;
+    a.pad_cols = p->pad_cols_d;
+    a.pad_npc = (int32_t)npc;
+    a.pad_ndiv = make_div_magic32((uint32_t)npc);
+    a.pad_bdiv = make_div_magic32((uint32_t)(batch * npc));
+  }
   if (!a.dynamic) {
     // Streams of short bags (mean length <= kShortBagMean): a tile is a run
     // of bags, about E values' worth rounded to whole 32-bag chunks, so its
@@ -1096,7 +1192,7 @@ emb_status launch_forward(emb_plan_s* p, int32_t batch, const int64_t* ids, cons
     int64_t k[2] = {0, 0}, t[2] = {a.tiles[0], a.tiles[1]};
     for (int st = 0; st < 2; ++st) {
       const int64_t S = (int64_t)batch * a.ncols[st];
-      if (S == 0 || nv[st] > kShortBagMean * S) continue;
+      if (S == 0 || a.tiles[st] == 0 || nv[st] > kShortBagMean * S) continue;
       const int64_t kb = nv[st] > 0 ? E * S / nv[st] : kMaxTileBags;
       k[st] = std::min<int64_t>(std::max<int64_t>(kWarp, (kb + kWarp / 2) / kWarp * kWarp), kMaxTileBags);
       t[st] = (S + k[st] - 1) / k[st];
@@ -1118,7 +1214,7 @@ emb_status launch_forward(emb_plan_s* p, int32_t batch, const int64_t* ids, cons
       }
     }
   }
-  const int64_t tiles = a.tiles[0] + a.tiles[1];
+  const int64_t tiles = a.tiles[0] + a.tiles[1] + a.pad_tiles;
   if (tiles == 0) return EMB_OK;
   const int64_t resident = (int64_t)p->sm_count * p->fwd_ctas_per_sm;
   int64_t grid = (tiles + kFwdWarpsPerCta - 1) / kFwdWarpsPerCta;

@@ -83,6 +83,7 @@ void free_plan(emb_plan_s* p) {
   dev_free(p->status_d);
   dev_free(p->fwd_ticket);
   dev_free(p->col_order_d);
+  dev_free(p->pad_cols_d);
   Workspace& w = p->ws;
   dev_free(w.keys[0]);
   dev_free(w.keys[1]);
@@ -291,6 +292,31 @@ extern "C" emb_status emb_plan_create(const emb_column_desc* cols, int32_t n_col
     }
     e = dmalloc(&p->col_order_d, order.size(), &total);
     if (e == cudaSuccess) e = cudaMemcpy(p->col_order_d, order.data(), sizeof(int32_t) * order.size(), cudaMemcpyHostToDevice);
+  }
+  if (e == cudaSuccess) {
+    // long padded columns, by their position in meta_d
+    std::vector<int32_t> pads;
+    for (size_t i = 0; i < sc.size(); ++i) {
+      const ColMeta& m = p->meta_h[sc[i]];
+      if (m.pooling == EMB_POOL_NONE_PADDED && m.pad_len > kLongBag) {
+        pads.push_back((int32_t)i);
+        p->max_long_pad = std::max(p->max_long_pad, m.pad_len);
+      }
+    }
+    p->n_long_padded = (int32_t)pads.size();
+    for (int st = 0; st < 2; ++st) {
+      bool all = !stream_cols[st].empty();
+      for (int32_t c : stream_cols[st]) {
+        const ColMeta& m = p->meta_h[c];
+        all = all && m.pooling == EMB_POOL_NONE_PADDED && m.pad_len > kLongBag;
+      }
+      p->long_padded_only[st] = all;
+    }
+    if (!pads.empty()) {
+      e = dmalloc(&p->pad_cols_d, pads.size(), &total);
+      if (e == cudaSuccess)
+        e = cudaMemcpy(p->pad_cols_d, pads.data(), sizeof(int32_t) * pads.size(), cudaMemcpyHostToDevice);
+    }
   }
   if (e == cudaSuccess)
     e = cudaMemcpy(p->tables_d, p->tables_h.data(), sizeof(TableMeta) * p->tables_h.size(), cudaMemcpyHostToDevice);

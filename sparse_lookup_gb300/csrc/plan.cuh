@@ -85,6 +85,12 @@ struct emb_plan_s {
   uint32_t* status_d = nullptr;
   unsigned long long* fwd_ticket = nullptr;   // forward tile tickets (next tile, warps done)
   int32_t* col_order_d = nullptr;   // per stream: its columns' stream positions, widest stored rows first
+  // Padded columns with pad_len > kLongBag: the forward copies their bags in
+  // pieces of positions, dealt as tiles of their own.
+  int32_t n_long_padded = 0;
+  int32_t max_long_pad = 0;
+  bool long_padded_only[2] = {false, false};   // per stream: it has columns, all long padded
+  int32_t* pad_cols_d = nullptr;               // their positions in meta_d
   int sm_count = 0;
   int fwd_ctas_per_sm = 0;
   emb::Workspace ws;

@@ -5,6 +5,7 @@ import numpy as np
 
 import oracle
 from sparse_lookup_gb300 import synth
+from sparse_lookup_gb300.synth import ColumnSpec, TableSpec, Workload
 
 RTOL = 1e-5
 ATOL = 1e-6
@@ -543,3 +544,62 @@ def assert_close_skip(got, ref, skip, what=""):
     keep = ~np.asarray(skip, bool)
     assert_close(np.asarray(got)[keep], np.asarray(ref)[keep], what)
     return int((~keep).sum())
+
+
+def padded_pieces_case(case):
+    """Plans with padded columns longer than the whole-warp threshold (their
+    bags are copied in pieces of positions): "ids-only" (a stream of only
+    such columns, pad lengths 130 / 777 / 300 / 1000, dims 8 / 128 / 36 /
+    200), "fvals-only" (a bucketized one alone in its stream), "mixed" (beside
+    pooled columns in both streams) and "static" (bags of a few values)."""
+    rng = np.random.default_rng({"ids-only": 11, "fvals-only": 12, "mixed": 13, "static": 14}[case])
+    B = 50
+    bnd = np.sort(rng.normal(size=60)).astype(np.float32)
+
+    def lens(hi):
+        x = rng.integers(0, hi, B)
+        x[::9] = 0
+        return x
+
+    def ids(n, rows):
+        return rng.integers(-5, rows + 5, n).astype(np.int64)
+
+    cols, tabs, offs, vals = [], [], [], []
+
+    def add(col, tab, ln, v):
+        cols.append(col)
+        tabs.append(tab)
+        offs.append(synth.bag_offsets(ln))
+        vals.append(v)
+
+    if case == "ids-only":
+        # the id stream holds only long padded columns: pieces do all of it
+        for k, (pad, dim) in enumerate(((130, 8), (777, 128), (300, 36), (1000, 200))):
+            ln = lens(pad + 200)
+            add(ColumnSpec("identity" if k != 2 else "hash_mod", "padded", 900, dim, k, pad_len=pad),
+                TableSpec(900, dim, 30 + k), ln,
+                ids(int(ln.sum()), 900) if k != 2 else rng.integers(-2 ** 63, 2 ** 63 - 1, int(ln.sum()),
+                                                                    dtype=np.int64))
+    elif case == "fvals-only":
+        # the value stream holds one long padded column, the id stream pools
+        ln = lens(1300)
+        add(ColumnSpec("bucketize", "padded", 61, 200, 0, boundaries=bnd, pad_len=1000), TableSpec(61, 200, 40),
+            ln, rng.normal(size=int(ln.sum())).astype(np.float32))
+        ln = lens(40)
+        add(ColumnSpec("identity", "sum", 500, 64, 1), TableSpec(500, 64, 41), ln, ids(int(ln.sum()), 500))
+    elif case == "mixed":
+        # long padded columns beside pooled ones in both streams
+        for k, (pool, pad) in enumerate((("padded", 300), ("sum", 0), ("mean", 0), ("padded", 1000))):
+            ln = lens(1200)
+            add(ColumnSpec("identity", pool, 700, 64, k, pad_len=pad), TableSpec(700, 64, 50 + k), ln,
+                ids(int(ln.sum()), 700))
+        ln = lens(400)
+        add(ColumnSpec("bucketize", "padded", 61, 32, 4, boundaries=bnd, pad_len=130), TableSpec(61, 32, 54), ln,
+            rng.normal(size=int(ln.sum())).astype(np.float32))
+    else:
+        # bags of a few values under a long pad: a launch of one tile per warp
+        for k, pad in enumerate((300, 1000)):
+            ln = lens(6)
+            add(ColumnSpec("identity", "padded", 400, 16, k, pad_len=pad), TableSpec(400, 16, 60 + k), ln,
+                ids(int(ln.sum()), 400))
+    return Workload("padded-" + case, B, cols, tabs, offs, vals, lr=0.01)

@@ -9,7 +9,7 @@ from sparse_lookup_gb300 import synth
 from sparse_lookup_gb300.synth import ColumnSpec, TableSpec, Workload
 
 import oracle
-from helpers import TrainStep, assert_close, check_train_step
+from helpers import TrainStep, assert_close, check_train_step, padded_pieces_case
 
 pytestmark = pytest.mark.gpu
 
@@ -83,6 +83,14 @@ def test_padded_and_mean_sequences_small():
     check_train_step(TrainStep(w))
     w = synth.sequences(seed=6, mode="mean", C=3, B=40, rows=3000, dim=128, len_lo=50, len_hi=300)
     check_train_step(TrainStep(w))
+
+
+@pytest.mark.parametrize("case", ["ids-only", "fvals-only", "mixed", "static"])
+def test_long_padded_pieces_training_step(case):
+    """Forward + backward + Adagrad of plans whose long padded bags are
+    copied in pieces: every position's gradient reaches its row once, cut
+    values and zero positions none."""
+    check_train_step(TrainStep(padded_pieces_case(case)))
 
 
 def test_truncated_sequences():

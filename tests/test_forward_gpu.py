@@ -9,7 +9,7 @@ from sparse_lookup_gb300 import build as slbuild
 from sparse_lookup_gb300 import synth
 from sparse_lookup_gb300.synth import ColumnSpec, TableSpec, Workload
 
-from helpers import Materialized, assert_close, pooled_slices, seq_slices
+from helpers import Materialized, assert_close, padded_pieces_case, pooled_slices, seq_slices
 
 pytestmark = pytest.mark.gpu
 
@@ -114,6 +114,20 @@ def test_long_bags_take_the_cta_path():
     vals = [rng.integers(-2 ** 63, 2 ** 63 - 1, n, dtype=np.int64), rng.integers(-5, 5005, n).astype(np.int64)]
     off = synth.bag_offsets(lens)
     w = Workload("long", B, cols, [TableSpec(5000, 64, 1), TableSpec(5000, 128, 2)], [off, off], vals)
+    m, plan, out, seq, rows = run_forward(w)
+    check_full(w, m, out, seq, rows)
+
+
+@pytest.mark.parametrize("case", ["ids-only", "fvals-only", "mixed", "static"])
+def test_long_padded_bags_copied_in_pieces(case):
+    """Padded columns longer than the whole-warp threshold are copied in
+    pieces of positions, dealt as tiles of their own: pad lengths 130 (a
+    piece past the end), 300, 777 and 1000 (pieces with ragged ends), bags
+    from empty to past pad_len (their cut values recorded by the last
+    piece), a stream of only such columns (no value tiles at all), one that
+    mixes them with pooled columns, and bags so short that the launch takes
+    one tile per warp."""
+    w = padded_pieces_case(case)
     m, plan, out, seq, rows = run_forward(w)
     check_full(w, m, out, seq, rows)
 
