@@ -603,3 +603,44 @@ def padded_pieces_case(case):
             add(ColumnSpec("identity", "padded", 400, 16, k, pad_len=pad), TableSpec(400, 16, 60 + k), ln,
                 ids(int(ln.sum()), 400))
     return Workload("padded-" + case, B, cols, tabs, offs, vals, lr=0.01)
+
+
+def long_pooled_case(case):
+    """Plans with long pooled bags (129 to 5000 values) beside short and empty
+    ones, whose launches take the dynamic schedule: "sum-mean" (both poolings,
+    dims 8 / 64 / 128), "weighted" (value weights on SUM columns), "fvals"
+    (bucketized values), "truncated" (max_len 150 and 1000) and "wide" (rows
+    of 200 floats)."""
+    rng = np.random.default_rng({"sum-mean": 21, "weighted": 22, "fvals": 23, "truncated": 24, "wide": 25}[case])
+    B = 48
+    bnd = np.sort(rng.normal(size=40)).astype(np.float32)
+
+    def lens():
+        x = np.where(rng.random(B) < 0.6, rng.integers(129, 5000, B), rng.integers(0, 20, B))
+        x[::11] = 0
+        return x
+
+    cols, tabs, offs, vals = [], [], [], []
+    dims = {"sum-mean": (8, 64, 128), "weighted": (32, 64), "fvals": (16, 64), "truncated": (64, 128),
+            "wide": (200, 36)}[case]
+    for k, dim in enumerate(dims):
+        ln = lens()
+        n = int(ln.sum())
+        pool = "mean" if k % 2 else "sum"
+        if case == "weighted":
+            pool = "sum"
+        if case == "fvals" and k == 0:
+            cols.append(ColumnSpec("bucketize", pool, bnd.size + 1, dim, k, boundaries=bnd))
+            tabs.append(TableSpec(bnd.size + 1, dim, 70 + k))
+            vals.append(rng.normal(size=n).astype(np.float32))
+        else:
+            rows = 3000
+            cols.append(ColumnSpec("identity", pool, rows, dim, k,
+                                   max_len=(150, 1000)[k] if case == "truncated" else 0))
+            tabs.append(TableSpec(rows, dim, 70 + k))
+            vals.append(rng.integers(-5, rows + 5, n).astype(np.int64))
+        offs.append(synth.bag_offsets(ln))
+    w = Workload("long-" + case, B, cols, tabs, offs, vals, lr=0.01)
+    if case == "weighted":
+        w.weights = [rng.uniform(-1.0, 2.0, int(o[-1])).astype(np.float32) for o in offs]
+    return w

@@ -9,7 +9,7 @@ from sparse_lookup_gb300 import build as slbuild
 from sparse_lookup_gb300 import synth
 from sparse_lookup_gb300.synth import ColumnSpec, TableSpec, Workload
 
-from helpers import Materialized, assert_close, padded_pieces_case, pooled_slices, seq_slices
+from helpers import Materialized, assert_close, long_pooled_case, padded_pieces_case, pooled_slices, seq_slices
 
 pytestmark = pytest.mark.gpu
 
@@ -130,6 +130,24 @@ def test_long_padded_bags_copied_in_pieces(case):
     w = padded_pieces_case(case)
     m, plan, out, seq, rows = run_forward(w)
     check_full(w, m, out, seq, rows)
+
+
+@pytest.mark.parametrize("case", ["sum-mean", "weighted", "fvals", "truncated", "wide"])
+def test_long_pooled_bags_in_training_plans(case):
+    """Training plans (which record every value for the backward) with long
+    pooled bags under the dynamic schedule: bags of 129 to 5000 values beside
+    short and empty ones, sum and mean, value weights, bucketized values,
+    truncation and rows of 200 floats.  A second launch into a fresh output
+    gives the same bits."""
+    import torch
+    w = long_pooled_case(case)
+    m, plan, out, seq, rows = run_forward(w, training=True)
+    check_full(w, m, out, seq, rows)
+    fresh = torch.full_like(out, float("nan"))
+    plan.forward(w.B, m.ids, m.id_off, m.fv, m.f_off, out=fresh, id_weights=m.idw, f_weights=m.fw)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    assert torch.equal(fresh, out)
 
 
 def test_all_bags_empty_and_defaults():
