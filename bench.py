@@ -564,13 +564,15 @@ KERNEL_SOURCES = {
     "backward": ("backward.cu", "radix.cuh", "update.cuh", "common.cuh", "plan.cuh"),
 }
 TRAFFIC = {
-    ("inference", "k_forward"): {"bytes": 494.00e6 + 49.74e6, "src": "77136f5ee8806b8b",
+    ("inference", "k_forward"): {"bytes": 493.89e6 + 48.25e6, "src": "a6316c726612c0d0",
                                  "source": "profiles/traffic_full_size.md (ncu, 1 pass, full-size launch)"},
-    ("training", "k_forward"): {"bytes": 2.90e9 + 783.85e6, "src": "77136f5ee8806b8b",
+    ("training", "k_forward"): {"bytes": 2896.36e6 + 776.44e6, "src": "a6316c726612c0d0",
                                 "source": "profiles/traffic_full_size.md (ncu, 1 pass, full-size launch)"},
+    ("sequences-padded", "k_forward"): {"bytes": 2118.57e6 + 10536.77e6, "src": "a6316c726612c0d0",
+                                        "source": "profiles/traffic_full_size.md (ncu, 1 pass, full-size launch)"},
     # the whole backward call: digit histogram, four radix passes, run
     # reduction with Adagrad, fixup
-    ("training", "backward"): {"bytes": 12425220690, "src": "50128a77288f069a",
+    ("training", "backward"): {"bytes": 12856284160, "src": "dd09374e99d8e0df",
                                "source": "profiles/traffic_full_size.md (ncu, 1 pass, each launch of one call)"},
 }
 
@@ -908,25 +910,30 @@ def bench_plan(torch, sl, w, args, dev, stream, flush, train, leg_only=False):
                       "ms_per_step": ms}
         res["e2e_ms"] = ms
     if args.graph:
-        # one whole step captured in a CUDA graph and replayed back to back:
-        # the step without per-launch host cost (L2 not flushed between replays)
+        # whole steps captured in a CUDA graph (up to 100 steps per graph, so
+        # that one graph launch from the host covers many steps) and replayed
+        # back to back: the steps without per-launch host cost (L2 not flushed
+        # between steps)
+        per = min(args.graph, 100)
+        reps = max(1, args.graph // per)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, capture_error_mode="relaxed"):
-            plan.forward(w.B, ids, id_off, fv, f_off, out=out, seq_out=seq)
-            if train:
-                plan.backward_update(G, Gseq, w.lr, w.eps)
+            for _ in range(per):
+                plan.forward(w.B, ids, id_off, fv, f_off, out=out, seq_out=seq)
+                if train:
+                    plan.backward_update(G, Gseq, w.lr, w.eps)
         g.replay()
         torch.cuda.synchronize()
         a, b = event_pair(torch)
         a.record(stream)
-        for _ in range(args.graph):
+        for _ in range(reps):
             g.replay()
         b.record(stream)
         torch.cuda.synchronize()
-        us = a.elapsed_time(b) * 1e3 / args.graph
-        res["config"]["graph"] = {"replays": args.graph, "us_per_step": us,
+        us = a.elapsed_time(b) * 1e3 / (reps * per)
+        res["config"]["graph"] = {"steps": reps * per, "steps_per_graph": per, "us_per_step": us,
                                   "rows_per_s": rows_per_step / (us * 1e-6),
-                                  "l2": "not flushed between replays"}
+                                  "l2": "not flushed between steps"}
         if plan.device_status() != 0:
             raise SystemExit("device status after the graph replays")
     res["ceiling"] = gather_ceiling(torch, sl, row_sizes_mix(w, valid, dt), dev) if not args.no_ceiling else None
@@ -1296,7 +1303,7 @@ def main():
     ap.add_argument("--training-steps", type=int, default=10,
                     help="timed steps of the training leg")
     ap.add_argument("--graph", type=int, default=0,
-                    help="also time this many back-to-back replays of one step captured in a CUDA graph")
+                    help="also time this many steps captured in CUDA graphs of up to 100 steps, replayed back to back")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -697,6 +697,8 @@ __device__ __forceinline__ void segreduce_body(const SegArgs& a, int64_t cta, un
 template <int V>
 __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(const SegArgs a) {
   extern __shared__ __align__(16) unsigned char seg_smem[];
+  pdl_wait();   // the sort has finished
+  pdl_trigger();   // the fixup launched after this kernel may be scheduled
   if (*(volatile const uint32_t*)a.sort_fail) return;   // the same for every thread of the CTA
   segreduce_body<V, kSegThreads>(a, blockIdx.x, seg_smem);
 }
@@ -706,6 +708,7 @@ __global__ void __launch_bounds__(kSegThreads, SegDepth<V>::ctas) k_segreduce(co
 template <int V>
 __global__ void __launch_bounds__(kSegThreads) k_seg_fixup(const SegArgs a, int n_blocks, int64_t span) {
   constexpr int kFixLook = 8;   // CTA partials loaded per round trip
+  pdl_wait();   // every CTA of the run reduction has finished
   if (*(volatile const uint32_t*)a.sort_fail) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int glog = a.glog;
@@ -788,8 +791,9 @@ inline emb_status launch_segreduce_v(const SegArgs& a, int64_t n_blocks, cudaStr
   const unsigned fix_grid = (unsigned)std::max<int64_t>(1, (n_blocks - 1 + NG - 1) / NG);
   const int smem = SegLayout::of(a.span, NG, a.maxdim4, V, SegDepth<V>::ring).bytes;
   EMB_CUDA_TRY(cudaFuncSetAttribute(k_segreduce<V>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
-  k_segreduce<V><<<(unsigned)n_blocks, kSegThreads, smem, stream>>>(a);
-  if (n_blocks > 1) k_seg_fixup<V><<<fix_grid, kSegThreads, 0, stream>>>(a, (int)n_blocks, a.span);
+  EMB_CUDA_TRY(launch_dependent(k_segreduce<V>, (unsigned)n_blocks, kSegThreads, smem, stream, a));
+  if (n_blocks > 1)
+    EMB_CUDA_TRY(launch_dependent(k_seg_fixup<V>, fix_grid, kSegThreads, 0, stream, a, (int)n_blocks, a.span));
   return EMB_OK;
 }
 

@@ -101,7 +101,35 @@ EMB_HD uint32_t div_magic32(uint32_t z, const DivMagic32& g) {
 __device__ __forceinline__ void latch(uint32_t* st, uint32_t code) {
   if (st && *((volatile uint32_t*)st) == 0u) atomicCAS(st, 0u, code);
 }
+
+// Programmatic dependent launch.  A kernel launched by launch_dependent()
+// may be scheduled before the kernel ahead of it in the stream has finished:
+// it calls pdl_wait() before its first memory access, which returns once
+// that kernel has completed and its writes are visible (and at once for a
+// kernel launched the ordinary way).  The kernel ahead calls pdl_trigger()
+// to let its dependant's CTAs be scheduled once all of its own CTAs have
+// started, so the dependant's launch overlaps its last wave.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 #endif
+
+// Launch `kernel` so that it may start while the previous kernel in the
+// stream finishes (it must begin with pdl_wait()).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                                    cudaStream_t stream, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 // ---------------------------------------------------------------------------
 // Metadata the kernels read.

@@ -368,6 +368,7 @@ __global__ void __launch_bounds__(kSortThreads, 1)
   extern __shared__ __align__(16) unsigned char smem_raw[];
   SortSmemT<K, BITS>& sm = *reinterpret_cast<SortSmemT<K, BITS>*>(smem_raw);
   const int tid = threadIdx.x;
+  pdl_trigger();   // the run reduction launched after this sort may be scheduled
   if (tid == 0) *(volatile uint32_t*)fail = 0u;   // no wait here can run out
   for (int p = 0; p < passes; ++p) {
     const K* kin = (p & 1) ? k1 : k0;

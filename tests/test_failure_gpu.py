@@ -29,6 +29,14 @@ def disarm():
     sl.emb_debug_fail_alloc(-1)
 
 
+def _settled_live_allocations():
+    # plans and tables of earlier tests that are no longer referenced are
+    # freed now, not by a garbage collection in the middle of the count
+    import gc
+    gc.collect()
+    return sl.emb_debug_live_allocations()
+
+
 def test_sort_wait_that_runs_out_is_reported_and_its_output_unused():
     r = sl.emb_selftest_sort_timeout()
     assert r["status"] == 0, r
@@ -55,7 +63,7 @@ def _plan_args(training):
 @pytest.mark.parametrize("training,backward", [(False, "sort"), (True, "sort"), (True, "atomic")])
 def test_every_plan_allocation_failure_returns_oom_and_leaks_nothing(training, backward):
     cols, tabs, accs = _plan_args(training)
-    base = sl.emb_debug_live_allocations()
+    base = _settled_live_allocations()
     failures = 0
     for k in range(200):
         sl.emb_debug_fail_alloc(k)
@@ -80,7 +88,7 @@ def test_every_plan_allocation_failure_returns_oom_and_leaks_nothing(training, b
 
 
 def test_every_hash_allocation_failure_returns_oom_and_leaks_nothing():
-    base = sl.emb_debug_live_allocations()
+    base = _settled_live_allocations()
     failures = 0
     for k in range(100):
         sl.emb_debug_fail_alloc(k)
