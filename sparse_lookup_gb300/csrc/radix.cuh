@@ -116,8 +116,7 @@ __global__ void __launch_bounds__(512) k_digit_hist_t(const K* __restrict__ keys
 
 // Lanes of the warp holding the same digit d, found with one ballot per digit
 // bit: the mask starts full and each ballot keeps the lanes that agree with
-// this lane on that bit.  NB = digit bits + 1 when some lanes hold the "no
-// item" marker 1 << digit bits.  All lanes must call.
+// this lane on that bit.  All lanes must call.
 template <int NB>
 __device__ __forceinline__ unsigned warp_match_digit(uint32_t d) {
   unsigned peers = kFull;
@@ -163,8 +162,14 @@ __device__ __forceinline__ void sort_scan_digits(uint32_t (&v)[(R + kSortThreads
 // One tile of a pass: rank the items by digit within the tile (stable: warp
 // order, then item order, then lane order), publish the tile's digit counts,
 // place the items in shared memory in digit order, find the tile's global
-// digit offsets by look-back, write out.  FULL: the tile holds TILE items
-// (no per-item bounds, one ballot less).
+// digit offsets by look-back, write out.  The lanes holding the same digit
+// are found by one ballot per digit bit on a full tile's first pass and by
+// one match.any otherwise: match.any takes longer the more distinct values a
+// warp holds, and the lowest digit of keys in their input order is close to
+// uniform, while the later passes see runs of repeated (Zipf-hot) keys and a
+// partial tile's missing items all hold the marker digit R (measured on the
+// training, sequence and tiny workloads).  FULL: the tile holds TILE items
+// (no per-item bounds).
 template <class K, int BITS>
 __device__ __forceinline__ void onesweep_tile(SortSmemT<K, BITS>& sm, const K* __restrict__ kin,
                                               const uint32_t* __restrict__ vin, K* __restrict__ kout,
@@ -196,7 +201,7 @@ __device__ __forceinline__ void onesweep_tile(SortSmemT<K, BITS>& sm, const K* _
   for (int i = 0; i < ITEMS; ++i) {
     const bool ok = FULL || w0 + i * 32 + lane < tile_n;
     const uint32_t d = ok ? sort_digit<K, BITS>(k[i], shift) : (uint32_t)R;
-    const unsigned peers = FULL ? warp_match_digit<BITS>(d) : warp_match_digit<BITS + 1>(d);
+    const unsigned peers = (FULL && shift == 0) ? warp_match_digit<BITS>(d) : __match_any_sync(kFull, d);
     const int leader = 31 - __clz(peers);
     uint32_t old = 0;
     if (lane == leader && ok) {
