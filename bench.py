@@ -554,8 +554,8 @@ def run_reference(args):
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
-# ncu captures of the full-size launches, one pass each (profiles/ keeps the
-# summaries and commands).  An entry holds while the sources its kernels are
+# ncu captures of the full-size launches, one pass each (the capture
+# commands are kept with their summaries).  An entry holds while the sources its kernels are
 # built from still hash as they did at the capture (KERNEL_SOURCES); once
 # they change, the bench reports the traffic as null until it is captured
 # again.
@@ -565,25 +565,25 @@ KERNEL_SOURCES = {
 }
 TRAFFIC = {
     ("inference", "k_forward"): {"bytes": 493.89e6 + 48.25e6, "src": "a6316c726612c0d0",
-                                 "source": "profiles/traffic_full_size.md (ncu, 1 pass, full-size launch)"},
+                                 "source": "ncu, 1 pass, the full-size launch"},
     ("inference-onehot", "k_forward"): {"bytes": 446.35e6 + 461.28e6, "src": "a6316c726612c0d0",
-                                        "source": "profiles/traffic_full_size.md (ncu, 1 pass, full-size launch)"},
+                                        "source": "ncu, 1 pass, the full-size launch"},
     ("training", "k_forward"): {"bytes": 2888.51e6 + 775.99e6, "src": "a6316c726612c0d0",
-                                "source": "profiles/traffic_full_size.md (ncu, 1 pass, full-size launch)"},
+                                "source": "ncu, 1 pass, the full-size launch"},
     ("sequences-mean", "k_forward"): {"bytes": 2345.59e6 + 118.51e6, "src": "a6316c726612c0d0",
-                                      "source": "profiles/traffic_full_size.md (ncu, 1 pass, full-size launch)"},
+                                      "source": "ncu, 1 pass, the full-size launch"},
     ("sequences-padded", "k_forward"): {"bytes": 2118.57e6 + 10536.77e6, "src": "a6316c726612c0d0",
-                                        "source": "profiles/traffic_full_size.md (ncu, 1 pass, full-size launch)"},
+                                        "source": "ncu, 1 pass, the full-size launch"},
     ("dynamic", "k_forward"): {"bytes": 73.23e6 + 188.18e6, "src": "a6316c726612c0d0",
-                               "source": "profiles/traffic_full_size.md (ncu, 1 pass, full-size launch)"},
+                               "source": "ncu, 1 pass, the full-size launch"},
     # the whole backward call: digit histogram, four radix passes, run
     # reduction with Adagrad, fixup
     ("training", "backward"): {"bytes": 12855822848, "src": "1f6e971f78c704da",
-                               "source": "profiles/traffic_full_size.md (ncu, 1 pass, each launch of one call)"},
+                               "source": "ncu, 1 pass, each launch of one full-size call"},
     ("sequences-mean", "backward"): {"bytes": 8857675264, "src": "1f6e971f78c704da",
-                                     "source": "profiles/traffic_full_size.md (ncu, 1 pass, each launch of one call)"},
+                                     "source": "ncu, 1 pass, each launch of one full-size call"},
     ("sequences-padded", "backward"): {"bytes": 14028081920, "src": "1f6e971f78c704da",
-                                       "source": "profiles/traffic_full_size.md (ncu, 1 pass, each launch of one call)"},
+                                       "source": "ncu, 1 pass, each launch of one full-size call"},
 }
 
 
