@@ -76,3 +76,88 @@ def test_reference_arm_line():
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def _rows_dbg(w):
+    """The transformed row of every value as the library reports it (rows of
+    values past a cut included), from the oracle, laid out id stream first."""
+    import numpy as np
+    import torch
+
+    import oracle
+    tabs = [None if t is None else np.zeros((t.num_rows, t.dim), np.float32) for t in w.tables]
+    _, _, rows = oracle.forward(w.columns, w.B, w.offsets, w.values, tabs, want_rows=True)
+    ids = [r for c, r in zip(w.columns, rows) if c.transform != "bucketize"]
+    fvs = [r for c, r in zip(w.columns, rows) if c.transform == "bucketize"]
+    n_ids = int(sum(r.size for r in ids))
+    flat = np.concatenate([np.asarray(r, np.int64) for r in ids + fvs]) if ids or fvs else np.zeros(0, np.int64)
+    return torch.from_numpy(flat), n_ids, rows
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3, 4])
+def test_row_statistics_and_compulsory_bytes_by_brute_force(bench, seed):
+    """The valid values, non-empty bags and distinct rows per table that the
+    compulsory byte counts rest on, and the counts themselves, against a
+    value-by-value count (padded cuts, truncation, dropped ids, shared
+    tables)."""
+    from sparse_lookup_gb300 import synth
+    w = synth.random_small(seed, C=8, B=30, train=True, allow_weights=False)
+    rows_dbg, n_ids, rows = _rows_dbg(w)
+    st = bench.row_stats(w, rows_dbg, n_ids)
+    valid, nonempty, seen = [], [], {}
+    for c, o, r in zip(w.columns, w.offsets, rows):
+        cut = c.pad_len if c.pooling == "padded" else int(c.max_len or 0)
+        nv, bags = 0, set()
+        for b in range(w.B):
+            for p in range(int(o[b]), int(o[b + 1])):
+                if r[p] >= 0 and (cut == 0 or p - int(o[b]) < cut):
+                    nv += 1
+                    bags.add(b)
+                    seen.setdefault(c.table, set()).add(int(r[p]))
+        valid.append(nv)
+        nonempty.append(len(bags))
+    assert st["valid"] == valid
+    assert st["nonempty_bags"] == nonempty
+    assert st["unique_per_table"] == {t: len(s) for t, s in seen.items()}
+
+    fixed = 0
+    for c, o in zip(w.columns, w.offsets):
+        n = int(o[-1])
+        per_value = 4 if c.transform == "bucketize" else 8
+        nb = 0 if c.boundaries is None else c.boundaries.size
+        out_rows = w.B * (c.pad_len if c.pooling == "padded" else 1)
+        fixed += (w.B + 1) * 4 + n * per_value + 4 * nb + out_rows * c.dim * 4
+    dim_of = {c.table: c.dim for c in w.columns}
+    rows_once = sum(len(s) * dim_of[t] * 4 for t, s in seen.items())
+    assert bench.forward_bytes_compulsory(w, st) == fixed + rows_once
+    rows_each = sum(nv * c.dim * 4 for c, nv in zip(w.columns, valid))
+    assert bench.forward_bytes(w, valid) == fixed + rows_each
+
+    n_contrib = int(rows_dbg.numel())
+    n_unique = sum(len(s) for s in seen.values())
+    dmax = max(c.dim for c in w.columns)
+    grad_once = sum((nv if c.pooling == "padded" else ne) * c.dim * 4
+                    for c, nv, ne in zip(w.columns, valid, nonempty))
+    assert bench.backward_bytes_compulsory(w, n_contrib, st, n_unique, dmax) == \
+        n_contrib * 24 + grad_once + n_unique * 16 * dmax
+
+
+def test_traffic_entry_holds_only_for_the_sources_it_was_captured_from(bench, monkeypatch):
+    """A DRAM traffic figure is reported only while the kernel sources hash as
+    they did at its capture; any other hash turns it into null."""
+    key = next(iter(bench.TRAFFIC))
+    entry = bench.TRAFFIC[key]
+    monkeypatch.setattr(bench, "kernel_src_hash", lambda kernel: entry["src"])
+    assert bench.traffic_for(*key)["bytes"] == entry["bytes"]
+    monkeypatch.setattr(bench, "kernel_src_hash", lambda kernel: "0" * 16)
+    assert bench.traffic_for(*key) is None
+    assert bench.traffic_for("no-such-workload", "k_forward") is None
+
+
+def test_roofline_fractions(bench):
+    """Achieved bandwidth and fractions of one launch from bytes and time."""
+    r = bench.roofline_obj(6.0e9, 3.0e9, 2.0, 6000.0, "measured", {"bytes": 4.5e9, "source": "a capture"})
+    assert r["achieved"] == pytest.approx(3000.0) and r["frac"] == pytest.approx(0.5)
+    assert r["achieved_compulsory"] == pytest.approx(1500.0) and r["frac_compulsory"] == pytest.approx(0.25)
+    assert r["traffic"] == 4.5e9 and r["traffic_dram_gbs"] == pytest.approx(2250.0)
+    assert bench.roofline_obj(1.0, 1.0, 1.0, 1.0, "measured", None)["traffic"] is None
